@@ -1,0 +1,151 @@
+/*
+ * fmpq.h -- C ABI of the GB300 (sm_103a) FMPQ W4Ax library.
+ *
+ * The method (COMET: Towards Practical W4A4KV4 LLMs Serving; FMPQ, "fine-grained
+ * mixed-precision quantization"):
+ *   - the K input channels of a linear layer are permuted so that outlier channels
+ *     collect in a few blocks, and split into blocks of 128 channels
+ *     (COMET news article, section 1 "outlier distribution");
+ *   - activations are quantized per token and per block: INT8 for the outlier blocks,
+ *     INT4 for the rest (same section, the "dynamic precision" sentence);
+ *   - weights are INT4, per output channel and per block, prepared offline
+ *     (QServe explainer, section "W4A8 GEMM core design": static weights are reordered
+ *     offline at no runtime cost);
+ *   - the W4Ax GEMM forms exact integer partial sums per block and applies the
+ *     dequantization scales in an FP32 epilogue (COMET abstract: mixed W4A4/W4A8 matrix
+ *     multiplication with a mixed-precision data layout; QUIK explainer, section "kernel
+ *     fusion": dequantization fused into the GEMM epilogue).
+ *
+ * Conventions for every call:
+ *   - Pointers are DEVICE pointers unless the parameter name ends in "_host".
+ *   - The caller owns every device buffer and stream. The library owns only the layout
+ *     handle (a host struct plus small device tables allocated once by
+ *     fmpq_layout_create on the device current at that time).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream),
+ *     never synchronize (except fmpq_layout_create/destroy and fmpq_device_status), and
+ *     allocate no memory.
+ *   - Argument errors are reported synchronously by the return value and launch nothing.
+ *     A CUDA launch failure returns FMPQ_ERR_CUDA. A device-side wait that gives up (a
+ *     bounded wait, never a hang) records FMPQ_ERR_TIMEOUT in the layout's device status
+ *     word, read by fmpq_device_status. The library never aborts, traps or prints.
+ *   - All data buffers must be 16-byte aligned (FMPQ_ERR_MISALIGNED otherwise).
+ *   - Inputs must be finite (no NaN/Inf); results for non-finite inputs are unspecified.
+ */
+#ifndef FMPQ_H
+#define FMPQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fmpq_status {
+    FMPQ_OK = 0,
+    FMPQ_ERR_INVALID_ARG = 1,       /* null pointer, bad permutation, bad mask value, ... */
+    FMPQ_ERR_UNSUPPORTED_SHAPE = 2, /* K % 128 != 0, N % 16 != 0, sizes out of range */
+    FMPQ_ERR_MISALIGNED = 3,        /* pointer or leading dimension misaligned */
+    FMPQ_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed */
+    FMPQ_ERR_TIMEOUT = 5,           /* (device status) a bounded device wait gave up */
+    FMPQ_ERR_DEVICE = 6,            /* no usable sm_103 device / layout used on another device */
+    FMPQ_ERR_WORKSPACE = 7          /* workspace missing or too small */
+} fmpq_status;
+
+#define FMPQ_BLOCK 128              /* channels per quantization block */
+#define FMPQ_MAX_K 65536            /* largest supported K */
+
+/* Opaque, library-owned description of one layer's channel permutation and block mask. */
+typedef struct fmpq_layout fmpq_layout;
+
+/* Create a layout.
+ *   K                  number of input channels; K % 128 == 0, 128 <= K <= FMPQ_MAX_K.
+ *   perm_host[K]       gather permutation: permuted channel j is input channel perm[j]
+ *                      (COMET news article, section 1: channel reordering gathers the
+ *                      outliers into the same blocks). Must be a permutation of [0, K).
+ *   outlier_block_mask_host[K/128]  1 = INT8 block (outlier block), 0 = INT4 block.
+ *   out                receives the handle.
+ * Uploads small device tables on the current device (synchronous). */
+fmpq_status fmpq_layout_create(int32_t K, const int32_t* perm_host,
+                               const uint8_t* outlier_block_mask_host, fmpq_layout** out);
+void fmpq_layout_destroy(fmpq_layout* layout);
+int32_t fmpq_layout_k(const fmpq_layout* layout);
+int32_t fmpq_layout_num_blocks(const fmpq_layout* layout);
+int32_t fmpq_layout_num_int8_blocks(const fmpq_layout* layout);
+
+/* Bytes of the packed activation buffer for M tokens: M * (64 * n4 + 128 * n8).
+ * Layout (block-major; the method's "mixed-precision data layout", made concrete here so
+ * that the GEMM converts 8 INT4 codes to 8 tensor-core operands with three integer ops):
+ *   block b occupies bytes [M*off_b, M*(off_b + w_b)), w_b = 64 (INT4) or 128 (INT8),
+ *   off_b = sum of w over the blocks before b; inside a block, row m takes w_b bytes.
+ *   INT8 block row: byte c = sign(q_c) << 7 | |q_c|           (sign-magnitude, |q| <= 127)
+ *   INT4 block row: 16 little-endian 32-bit words; word g holds channels 8g..8g+7;
+ *     byte j (0..3): bits 0-2 = |q_{8g+j}|, bit 7 = sign(q_{8g+j}),
+ *                    bits 4-6 = |q_{8g+4+j}|, bit 3 = sign(q_{8g+4+((j+3)%4)}).
+ *   sign(q) = 1 iff q < 0. */
+size_t fmpq_packed_a_bytes(const fmpq_layout* layout, int64_t M);
+
+/* Bytes of the packed weight buffer for N output channels: ceil(N/256)*256 * K/2.
+ * The packed weight format is implementation-defined (tile-major, padded to 256 rows);
+ * w4_unpack_weights decodes it. */
+size_t fmpq_packed_w_bytes(const fmpq_layout* layout, int64_t N);
+
+/* Fused activation quantizer (one pass: gather-permute, per-(token, block) absmax,
+ * fp16 scale, round-half-even quantization, INT4/INT8 packing).
+ *   X         fp16 [M][ldx], ldx >= K, ldx % 8 == 0.
+ *   M         1 <= M <= 2^31-1.
+ *   A_packed  fmpq_packed_a_bytes(layout, M) bytes (layout above).
+ *   a_scales  fp16 [K/128][M]: a_scales[b*M + m] = fp16_rne(fp32(absmax)/qmax),
+ *             qmax = 127 (INT8 block) or 7 (INT4 block).
+ * Codes: q = clamp(rne(fp32(x) / fp32(scale)), -qmax, qmax); a zero scale gives q = 0. */
+fmpq_status fmpq_quantize(const fmpq_layout* layout, const void* X, int64_t ldx, int64_t M,
+                          void* A_packed, void* a_scales, void* stream);
+
+/* Offline weight preparation: W fp16 [N][ldw] (ldw >= K, ldw % 8 == 0, N % 16 == 0)
+ * -> W_packed (fmpq_packed_w_bytes) and w_scales fp16 [K/128][N], INT4 range [-7, 7]
+ * per output channel and block, same scale and rounding rule as the activations, on the
+ * permuted channel order. */
+fmpq_status w4_pack_weights(const fmpq_layout* layout, const void* W, int64_t ldw, int64_t N,
+                            void* W_packed, void* w_scales, void* stream);
+
+/* Debug/test: decode W_packed to codes Wq int8 [N][K] (permuted channel order). */
+fmpq_status w4_unpack_weights(const fmpq_layout* layout, const void* W_packed, int64_t N,
+                              int8_t* Wq, void* stream);
+
+/* Workspace bytes w4ax_gemm needs for this shape (0 when it needs none). */
+size_t w4ax_gemm_workspace_bytes(const fmpq_layout* layout, int64_t M, int64_t N);
+
+/* The W4Ax GEMM:
+ *   Y[m][n] = fp16_rn( sum_b a_scales[b][m] * w_scales[b][n] * P[m][n][b] ),
+ *   P[m][n][b] = sum over channels j of block b of qa[m][j] * qw[n][j]   (exact integers),
+ * accumulated in FP32.
+ *   Y          fp16 [M][ldy], ldy >= N, ldy % 8 == 0; N % 16 == 0.
+ *   workspace  w4ax_gemm_workspace_bytes(layout, M, N) bytes (may be NULL when that is 0);
+ *              contents need no initialization and are left in a reusable state. */
+fmpq_status w4ax_gemm(const fmpq_layout* layout, const void* A_packed, const void* a_scales,
+                      const void* W_packed, const void* w_scales, int64_t M, int64_t N,
+                      void* Y, int64_t ldy, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Debug/test: the exact per-block integer partial sums P computed by the GEMM's own
+ * tensor-core path, for the window [m0, m0+mcount) x [n0, n0+ncount):
+ *   P int32 [mcount][ncount][K/128]. */
+fmpq_status w4ax_gemm_partials(const fmpq_layout* layout, const void* A_packed,
+                               const void* W_packed, int64_t M, int64_t N, int64_t m0,
+                               int64_t mcount, int64_t n0, int64_t ncount, int32_t* P,
+                               void* stream);
+
+/* Read (and, if clear != 0, reset) the layout's device status word. Synchronizes the
+ * device. *code = FMPQ_OK or the first error a kernel recorded (e.g. FMPQ_ERR_TIMEOUT). */
+fmpq_status fmpq_device_status(const fmpq_layout* layout, int32_t* code, int32_t clear);
+
+/* Static description of a status code. */
+const char* fmpq_status_string(fmpq_status status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t fmpq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FMPQ_H */

@@ -1,0 +1,206 @@
+"""CPU oracle for the FMPQ W4Ax path -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline legs of ``bench.py``
+may import this package. The product library never does, and shares no code with it.
+
+The arithmetic lives in ``fmpq_oracle.c`` (plain C, compiled with gcc, no fast-math,
+no FMA contraction); this module only builds it and marshals numpy arrays. See the C
+file's header for the steps it follows and the readings it takes where the pages are
+silent.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fmpq_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "liboracle.so")
+BLOCK = 128
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc into oracle/_build/liboracle.so (idempotent)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(_SRC):
+        return _SO
+    tmp = _SO + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=gnu11", "-O2", "-fPIC", "-shared", "-fno-fast-math", "-ffp-contract=off",
+           "-fopenmp", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_SO)
+            P = ctypes.c_void_p
+            i64, i32 = ctypes.c_int64, ctypes.c_int
+            lib.oracle_f32_to_f16.argtypes = [ctypes.c_float]
+            lib.oracle_f32_to_f16.restype = ctypes.c_uint16
+            lib.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
+            lib.oracle_f16_to_f32.restype = ctypes.c_float
+            lib.oracle_f32_to_f16_array.argtypes = [P, i64, P]
+            lib.oracle_f16_to_f32_array.argtypes = [P, i64, P]
+            lib.oracle_quantize_activations.argtypes = [P, i64, i32, i32, P, P, P, P, P]
+            lib.oracle_quantize_activations.restype = i32
+            lib.oracle_unpack_activations.argtypes = [P, P, i32, i32, P]
+            lib.oracle_unpack_activations.restype = i32
+            lib.oracle_quantize_weights.argtypes = [P, i64, i32, i32, P, P, P]
+            lib.oracle_quantize_weights.restype = i32
+            lib.oracle_partials.argtypes = [P, P, i32, i32, i32, P]
+            lib.oracle_partials_zero_ext.argtypes = [P, P, i32, i32, i32, P]
+            lib.oracle_epilogue_f64.argtypes = [P, P, P, i32, i32, i32, P]
+            lib.oracle_epilogue_exact.argtypes = [P, P, P, i32, i32, i32, P]
+            lib.oracle_gemm_sample.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P, P, P]
+            lib.oracle_block_offset.argtypes = [P, i32]
+            lib.oracle_block_offset.restype = i64
+            lib.oracle_packed_a_bytes.argtypes = [P, i32, i32]
+            lib.oracle_packed_a_bytes.restype = i64
+            lib.oracle_num_threads.restype = i32
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+# ---- fp16 ----------------------------------------------------------------------------
+
+def f32_to_f16_bits(x) -> np.ndarray:
+    x = _c(x, np.float32).ravel()
+    out = np.empty(x.size, dtype=np.uint16)
+    _load().oracle_f32_to_f16_array(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def f16_bits_to_f32(h) -> np.ndarray:
+    h = _c(h, np.uint16).ravel()
+    out = np.empty(h.size, dtype=np.float32)
+    _load().oracle_f16_to_f32_array(_ptr(h), h.size, _ptr(out))
+    return out
+
+
+# ---- quantizer -----------------------------------------------------------------------
+
+def packed_a_bytes(mask, K: int, M: int) -> int:
+    mask = _c(mask, np.uint8)
+    return int(_load().oracle_packed_a_bytes(_ptr(mask), K, M))
+
+
+def block_offsets(mask) -> np.ndarray:
+    """Per-block byte offset (units of M) of the packed activation layout."""
+    mask = _c(mask, np.uint8)
+    return np.array([_load().oracle_block_offset(_ptr(mask), b) for b in range(mask.size)], dtype=np.int64)
+
+
+def quantize_activations(X, perm, mask, want_codes: bool = True):
+    """X fp16 [M, K] -> (A_packed uint8, a_scales fp16-bits uint16 [nb, M], Aq int8 [M, K] or None)."""
+    Xb = _c(np.asarray(X, dtype=np.float16).view(np.uint16), np.uint16)
+    M, K = Xb.shape
+    perm = _c(perm, np.int32)
+    mask = _c(mask, np.uint8)
+    nb = K // BLOCK
+    A = np.zeros(packed_a_bytes(mask, K, M), dtype=np.uint8)
+    s = np.zeros((nb, M), dtype=np.uint16)
+    Aq = np.zeros((M, K), dtype=np.int8) if want_codes else None
+    rc = _load().oracle_quantize_activations(_ptr(Xb), K, M, K, _ptr(perm), _ptr(mask), _ptr(A), _ptr(s),
+                                             _ptr(Aq) if want_codes else None)
+    if rc != 0:
+        raise ValueError(f"oracle_quantize_activations failed ({rc})")
+    return A, s, Aq
+
+
+def unpack_activations(A_packed, mask, M: int, K: int) -> np.ndarray:
+    A_packed = _c(A_packed, np.uint8)
+    mask = _c(mask, np.uint8)
+    Aq = np.zeros((M, K), dtype=np.int8)
+    rc = _load().oracle_unpack_activations(_ptr(A_packed), _ptr(mask), M, K, _ptr(Aq))
+    if rc != 0:
+        raise ValueError("oracle_unpack_activations failed")
+    return Aq
+
+
+def quantize_weights(W, perm):
+    """W fp16 [N, K] -> (Wq int8 [N, K] permuted order, w_scales fp16-bits uint16 [nb, N])."""
+    Wb = _c(np.asarray(W, dtype=np.float16).view(np.uint16), np.uint16)
+    N, K = Wb.shape
+    perm = _c(perm, np.int32)
+    Wq = np.zeros((N, K), dtype=np.int8)
+    s = np.zeros((K // BLOCK, N), dtype=np.uint16)
+    rc = _load().oracle_quantize_weights(_ptr(Wb), K, N, K, _ptr(perm), _ptr(Wq), _ptr(s))
+    if rc != 0:
+        raise ValueError("oracle_quantize_weights failed")
+    return Wq, s
+
+
+# ---- partials and epilogue -------------------------------------------------------------
+
+def partials(Aq, Wq, zero_ext: bool = False) -> np.ndarray:
+    """P int32 [M, N, nb], exact per-block integer partial sums."""
+    Aq = _c(Aq, np.int8)
+    Wq = _c(Wq, np.int8)
+    M, K = Aq.shape
+    N = Wq.shape[0]
+    P = np.zeros((M, N, K // BLOCK), dtype=np.int32)
+    fn = _load().oracle_partials_zero_ext if zero_ext else _load().oracle_partials
+    fn(_ptr(Aq), _ptr(Wq), M, N, K, _ptr(P))
+    return P
+
+
+def epilogue(P, a_scales, w_scales, exact: bool = False) -> np.ndarray:
+    """Y fp64 [M, N] = sum_b sx[b, m] * sw[b, n] * P[m, n, b] (fp64 block order, or exact)."""
+    P = _c(P, np.int32)
+    M, N, nb = P.shape
+    sx = _c(a_scales, np.uint16)
+    sw = _c(w_scales, np.uint16)
+    Y = np.zeros((M, N), dtype=np.float64)
+    fn = _load().oracle_epilogue_exact if exact else _load().oracle_epilogue_f64
+    fn(_ptr(P), _ptr(sx), _ptr(sw), M, N, nb, _ptr(Y))
+    return Y
+
+
+def gemm_sample(Aq, Wq, a_scales, w_scales, ms, ns):
+    """Per-block partials P [S, nb] and Y [S] at output positions (ms[s], ns[s])."""
+    Aq = _c(Aq, np.int8)
+    Wq = _c(Wq, np.int8)
+    M, K = Aq.shape
+    N = Wq.shape[0]
+    ms = _c(ms, np.int32)
+    ns = _c(ns, np.int32)
+    S = ms.size
+    P = np.zeros((S, K // BLOCK), dtype=np.int32)
+    Y = np.zeros(S, dtype=np.float64)
+    _load().oracle_gemm_sample(_ptr(Aq), _ptr(Wq), _ptr(_c(a_scales, np.uint16)), _ptr(_c(w_scales, np.uint16)),
+                               M, N, K, S, _ptr(ms), _ptr(ns), _ptr(P), _ptr(Y))
+    return P, Y
+
+
+def reference(X, W, perm, mask):
+    """Whole path on the CPU for small shapes: returns a dict of every intermediate."""
+    A, sx, Aq = quantize_activations(X, perm, mask)
+    Wq, sw = quantize_weights(W, perm)
+    P = partials(Aq, Wq)
+    Y = epilogue(P, sx, sw)
+    return dict(A_packed=A, a_scales=sx, Aq=Aq, Wq=Wq, w_scales=sw, P=P, Y=Y)

@@ -1,0 +1,381 @@
+/*
+ * CPU oracle for the FMPQ W4Ax path -- TEST INFRASTRUCTURE ONLY.
+ *
+ * Only the test suite, the smoke check and the benchmark's CPU-baseline leg load this
+ * library. The product (the CUDA library under bit_quantized_gemm_fmpq_gb300/csrc) shares
+ * no code, header, table or constant with it, and never calls it.
+ *
+ * What it computes, step by step, in the order the method states it:
+ *   1. gather-permute the channels, Xp[m, j] = X[m, perm[j]]        (COMET news article,
+ *      section 1 "outlier distribution": channel reordering gathers the outliers)
+ *   2. split the K channels into blocks of 128                        (same section)
+ *   3. per token and block: absmax, fp16 scale, round-half-even quantization to INT8 for
+ *      outlier blocks and INT4 for the rest                          (same section; the
+ *      "dynamic precision" sentence), symmetric ranges [-127,127] / [-7,7]
+ *   4. INT4 weights, per output channel and block, quantized the same way offline
+ *   5. exact integer partial sums per block P[m,n,b]                 (COMET abstract:
+ *      W4A4/W4A8 mixed-precision matrix multiplication)
+ *   6. scale-and-sum epilogue Y[m,n] = sum_b sx[m,b] * sw[n,b] * P[m,n,b]  (QUIK explainer,
+ *      section "kernel fusion": dequantization applied in the GEMM epilogue)
+ *
+ * Readings where the pages are silent (each listed with its reason in the design notes):
+ *   - symmetric absmax quantization; INT4 range [-7,7], INT8 range [-127,127]
+ *   - scale s = fp16_rne( fp32(absmax) / fp32(qmax) ); a zero scale quantizes the block to 0
+ *   - q = clamp( rne_f32( fp32(x) / fp32(s) ), -qmax, qmax ) with IEEE fp32 division
+ *   - packed activation layout: block-major (block b at byte M*off_b, 64 or 128 bytes per
+ *     row); INT8 codes as sign-magnitude bytes; INT4 codes as sign-magnitude 3+1-bit fields,
+ *     8 channels per 32-bit word: byte j holds |q_j| in bits 0-2 and sign(q_j) in bit 7,
+ *     |q_{4+j}| in bits 4-6 and sign(q_{4+(j+3)%4}) in bit 3 (the layout is chosen so the
+ *     tensor-core operand bytes fall out with a mask and a rotate; the oracle only writes it)
+ *
+ * Floating point here is IEEE fp32 where the method decides an integer (the kernel's
+ * precision), and fp64 or exact int128 fixed point for the epilogue reference.
+ * Build with -O2 -fno-fast-math -ffp-contract=off.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_BLOCK 128
+
+/* ------------------------------------------------------------------------------------
+ * IEEE 754 binary16 <-> binary32, written from the format's definition (value based).
+ * ------------------------------------------------------------------------------------ */
+
+/* binary16 bits -> value.  normal: (1024 + f) * 2^(e - 25); subnormal: f * 2^-24. */
+float oracle_f16_to_f32(uint16_t h) {
+    unsigned sign = (h >> 15) & 1u, e = (h >> 10) & 31u, f = h & 1023u;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024u + f), (int)e - 25);
+    return (float)(sign ? -v : v);
+}
+
+/* round a non-negative double that is an exact multiple of 1/2 ... to an integer, ties to even
+ * (used on values r = |x| / quantum, which are exact in double) */
+static double round_half_even_d(double r) {
+    double fl = floor(r);
+    double d = r - fl;
+    if (d > 0.5) return fl + 1.0;
+    if (d < 0.5) return fl;
+    return (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+}
+
+/* value -> binary16 bits, round to nearest, ties to even (finite inputs; NaN -> 0x7e00). */
+uint16_t oracle_f32_to_f16(float x) {
+    if (isnan(x)) return 0x7e00;
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs((double)x);
+    if (a >= 65520.0) return sign | 0x7c00;           /* 65504 + half an ulp (16): overflow */
+    if (a == 0.0) return sign;
+    /* quantum of the binade that contains a (subnormal binades share 2^-24) */
+    int e2;
+    frexp(a, &e2);                                      /* a = m * 2^e2, m in [0.5, 1) */
+    int ex = e2 - 1;                                    /* floor(log2 a) */
+    double quantum = (ex < -14) ? ldexp(1.0, -24) : ldexp(1.0, ex - 10);
+    double n = round_half_even_d(a / quantum);          /* exact division by a power of 2 */
+    double v = n * quantum;                             /* the rounded value */
+    if (v >= 65520.0) return sign | 0x7c00;
+    if (v < ldexp(1.0, -14)) {                          /* subnormal (or zero) */
+        return sign | (uint16_t)(v / ldexp(1.0, -24));
+    }
+    frexp(v, &e2);
+    ex = e2 - 1;
+    unsigned frac = (unsigned)(v / ldexp(1.0, ex - 10)) - 1024u;
+    unsigned expf = (unsigned)(ex + 15);
+    if (expf >= 31) return sign | 0x7c00;
+    return sign | (uint16_t)((expf << 10) | frac);
+}
+
+void oracle_f32_to_f16_array(const float* x, int64_t n, uint16_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_f32_to_f16(x[i]);
+}
+
+void oracle_f16_to_f32_array(const uint16_t* h, int64_t n, float* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_f16_to_f32(h[i]);
+}
+
+/* ------------------------------------------------------------------------------------
+ * Quantization of one block of 128 values (steps 3-4 above).
+ * ------------------------------------------------------------------------------------ */
+
+/* round-half-even of an fp32 value to an integer (|v| well below 2^23 here) */
+static int32_t rne_f32_to_int(float v) {
+    float fl = floorf(v);
+    float d = v - fl;                                   /* exact: fl and v share the binade */
+    int32_t i = (int32_t)fl;
+    if (d > 0.5f) return i + 1;
+    if (d < 0.5f) return i;
+    return (i % 2 == 0) ? i : i + 1;
+}
+
+/* Quantize 128 fp16 values xs (already permuted) with range [-qmax, qmax].
+ * Writes q[128] and returns the fp16 scale bits. */
+static uint16_t quantize_block(const uint16_t* xs, int qmax, int8_t* q) {
+    float absmax = 0.0f;
+    for (int j = 0; j < ORACLE_BLOCK; ++j) {
+        float v = fabsf(oracle_f16_to_f32(xs[j]));
+        if (v > absmax) absmax = v;
+    }
+    float s32 = absmax / (float)qmax;                   /* IEEE fp32 division */
+    uint16_t s16 = oracle_f32_to_f16(s32);
+    float s = oracle_f16_to_f32(s16);
+    for (int j = 0; j < ORACLE_BLOCK; ++j) {
+        if (s == 0.0f) { q[j] = 0; continue; }
+        float r = oracle_f16_to_f32(xs[j]) / s;          /* IEEE fp32 division */
+        int32_t v = rne_f32_to_int(r);
+        if (v > qmax) v = qmax;
+        if (v < -qmax) v = -qmax;
+        q[j] = (int8_t)v;
+    }
+    return s16;
+}
+
+/* ------------------------------------------------------------------------------------
+ * Packed code formats (sign-magnitude).
+ * ------------------------------------------------------------------------------------ */
+
+static unsigned sgn(int8_t q) { return q < 0 ? 1u : 0u; }
+static unsigned mag(int8_t q) { return (unsigned)(q < 0 ? -q : q); }
+
+/* INT8 row: byte c = sign(q_c) << 7 | |q_c| */
+static void pack_int8_row(const int8_t* q, uint8_t* dst) {
+    for (int c = 0; c < ORACLE_BLOCK; ++c) dst[c] = (uint8_t)((sgn(q[c]) << 7) | mag(q[c]));
+}
+
+static void unpack_int8_row(const uint8_t* src, int8_t* q) {
+    for (int c = 0; c < ORACLE_BLOCK; ++c) {
+        int v = src[c] & 0x7F;
+        q[c] = (int8_t)((src[c] & 0x80) ? -v : v);
+    }
+}
+
+/* INT4 row: 16 groups of 8 channels, 4 bytes per group (byte 4g+j of the row):
+ *   bits 0-2 |q[8g+j]|, bit 7 sign(q[8g+j]), bits 4-6 |q[8g+4+j]|, bit 3 sign(q[8g+4+(j+3)%4]) */
+static void pack_int4_row(const int8_t* q, uint8_t* dst) {
+    for (int g = 0; g < 16; ++g) {
+        const int8_t* e = q + 8 * g;
+        for (int j = 0; j < 4; ++j) {
+            unsigned byte = mag(e[j]) | (sgn(e[j]) << 7) | (mag(e[4 + j]) << 4) | (sgn(e[4 + (j + 3) % 4]) << 3);
+            dst[4 * g + j] = (uint8_t)byte;
+        }
+    }
+}
+
+static void unpack_int4_row(const uint8_t* src, int8_t* q) {
+    for (int g = 0; g < 16; ++g) {
+        const uint8_t* w = src + 4 * g;
+        for (int j = 0; j < 4; ++j) {
+            int lo = w[j] & 7, hi = (w[j] >> 4) & 7;
+            q[8 * g + j] = (int8_t)((w[j] & 0x80) ? -lo : lo);
+            /* the sign of element 4+j sits in bit 3 of byte (j+1)%4 */
+            q[8 * g + 4 + j] = (int8_t)((w[(j + 1) % 4] & 0x08) ? -hi : hi);
+        }
+    }
+}
+
+/* Byte offset of block b inside the packed activation buffer, in units of M:
+ * off_b = sum_{b' < b} width(b'), width = 64 bytes (INT4) or 128 bytes (INT8) per row. */
+int64_t oracle_block_offset(const uint8_t* mask, int b) {
+    int64_t off = 0;
+    for (int i = 0; i < b; ++i) off += mask[i] ? 128 : 64;
+    return off;
+}
+
+int64_t oracle_packed_a_bytes(const uint8_t* mask, int K, int M) {
+    return oracle_block_offset(mask, K / ORACLE_BLOCK) * (int64_t)M;
+}
+
+/* Activations: X fp16 bits [M][ldx] -> packed A, a_scales [nb][M] (fp16 bits) and, if
+ * Aq != NULL, the integer codes Aq [M][K] in permuted channel order. Returns 0 on success. */
+int oracle_quantize_activations(const uint16_t* X, int64_t ldx, int M, int K,
+                                const int32_t* perm, const uint8_t* mask,
+                                uint8_t* A_packed, uint16_t* a_scales, int8_t* Aq) {
+    if (K % ORACLE_BLOCK) return -1;
+    const int nb = K / ORACLE_BLOCK;
+    int64_t* off = (int64_t*)malloc(sizeof(int64_t) * (size_t)nb);
+    if (!off) return -2;
+    for (int b = 0; b < nb; ++b) off[b] = oracle_block_offset(mask, b);
+#pragma omp parallel for schedule(static)
+    for (int m = 0; m < M; ++m) {
+        uint16_t xs[ORACLE_BLOCK];
+        int8_t q[ORACLE_BLOCK];
+        for (int b = 0; b < nb; ++b) {
+            /* step 1: gather-permute this block's channels */
+            for (int j = 0; j < ORACLE_BLOCK; ++j)
+                xs[j] = X[(int64_t)m * ldx + perm[b * ORACLE_BLOCK + j]];
+            /* steps 2-3: per-block scale and codes */
+            const int qmax = mask[b] ? 127 : 7;
+            a_scales[(int64_t)b * M + m] = quantize_block(xs, qmax, q);
+            if (Aq)
+                for (int j = 0; j < ORACLE_BLOCK; ++j) Aq[(int64_t)m * K + b * ORACLE_BLOCK + j] = q[j];
+            /* pack */
+            uint8_t* dst = A_packed + off[b] * M;
+            if (mask[b]) pack_int8_row(q, dst + (int64_t)m * 128);
+            else pack_int4_row(q, dst + (int64_t)m * 64);
+        }
+    }
+    free(off);
+    return 0;
+}
+
+/* Decode the canonical packed activation buffer back to codes Aq [M][K]. */
+int oracle_unpack_activations(const uint8_t* A_packed, const uint8_t* mask, int M, int K, int8_t* Aq) {
+    if (K % ORACLE_BLOCK) return -1;
+    const int nb = K / ORACLE_BLOCK;
+    for (int b = 0; b < nb; ++b) {
+        const uint8_t* src = A_packed + oracle_block_offset(mask, b) * M;
+        for (int m = 0; m < M; ++m) {
+            int8_t* row = Aq + (int64_t)m * K + b * ORACLE_BLOCK;
+            if (mask[b]) unpack_int8_row(src + (int64_t)m * 128, row);
+            else unpack_int4_row(src + (int64_t)m * 64, row);
+        }
+    }
+    return 0;
+}
+
+/* Weights (offline): W fp16 bits [N][ldw] -> codes Wq [N][K] in permuted channel order
+ * (INT4 range [-7,7] everywhere) and w_scales [nb][N] (fp16 bits). The same channel
+ * permutation is applied to W so the products pair up (QUIK explainer, step 1: the
+ * weight matrix is reordered together with the outlier columns). */
+int oracle_quantize_weights(const uint16_t* W, int64_t ldw, int N, int K, const int32_t* perm,
+                            int8_t* Wq, uint16_t* w_scales) {
+    if (K % ORACLE_BLOCK) return -1;
+    const int nb = K / ORACLE_BLOCK;
+#pragma omp parallel for schedule(static)
+    for (int n = 0; n < N; ++n) {
+        uint16_t xs[ORACLE_BLOCK];
+        for (int b = 0; b < nb; ++b) {
+            for (int j = 0; j < ORACLE_BLOCK; ++j) xs[j] = W[(int64_t)n * ldw + perm[b * ORACLE_BLOCK + j]];
+            w_scales[(int64_t)b * N + n] = quantize_block(xs, 7, Wq + (int64_t)n * K + b * ORACLE_BLOCK);
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------------------
+ * Integer partial sums and the epilogue (steps 5-6).
+ * ------------------------------------------------------------------------------------ */
+
+/* P[m][n][b] = sum_{j in block b} Aq[m][j] * Wq[n][j], exact (int64 accumulate). */
+void oracle_partials(const int8_t* Aq, const int8_t* Wq, int M, int N, int K, int32_t* P) {
+    const int nb = K / ORACLE_BLOCK;
+#pragma omp parallel for schedule(static)
+    for (int m = 0; m < M; ++m)
+        for (int n = 0; n < N; ++n)
+            for (int b = 0; b < nb; ++b) {
+                int64_t acc = 0;
+                for (int j = b * ORACLE_BLOCK; j < (b + 1) * ORACLE_BLOCK; ++j)
+                    acc += (int64_t)Aq[(int64_t)m * K + j] * (int64_t)Wq[(int64_t)n * K + j];
+                P[((int64_t)m * N + n) * nb + b] = (int32_t)acc;
+            }
+}
+
+/* The zero-extension form (COMET news article, section 3: unsigned extension of the 4-bit
+ * weight, compensated through the scale path): with u = q_w + 8 in [1, 15],
+ *   P = sum_j q_x * u  -  8 * sum_j q_x,
+ * the correction depending only on (m, b). */
+void oracle_partials_zero_ext(const int8_t* Aq, const int8_t* Wq, int M, int N, int K, int32_t* P) {
+    const int nb = K / ORACLE_BLOCK;
+#pragma omp parallel for schedule(static)
+    for (int m = 0; m < M; ++m)
+        for (int b = 0; b < nb; ++b) {
+            int64_t sx = 0;
+            for (int j = b * ORACLE_BLOCK; j < (b + 1) * ORACLE_BLOCK; ++j) sx += Aq[(int64_t)m * K + j];
+            for (int n = 0; n < N; ++n) {
+                int64_t acc = 0;
+                for (int j = b * ORACLE_BLOCK; j < (b + 1) * ORACLE_BLOCK; ++j) {
+                    int64_t u = (int64_t)Wq[(int64_t)n * K + j] + 8;   /* zero-extended code */
+                    acc += (int64_t)Aq[(int64_t)m * K + j] * u;
+                }
+                P[((int64_t)m * N + n) * nb + b] = (int32_t)(acc - 8 * sx);
+            }
+        }
+}
+
+/* Y[m][n] = sum_b sx[b][m] * sw[b][n] * P[m][n][b], accumulated in fp64 in block order.
+ * Each term is exact in fp64 (11 + 11 + 17 significant bits); only the sum rounds. */
+void oracle_epilogue_f64(const int32_t* P, const uint16_t* a_scales, const uint16_t* w_scales,
+                         int M, int N, int nb, double* Y) {
+#pragma omp parallel for schedule(static)
+    for (int m = 0; m < M; ++m)
+        for (int n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int b = 0; b < nb; ++b) {
+                double sx = oracle_f16_to_f32(a_scales[(int64_t)b * M + m]);
+                double sw = oracle_f16_to_f32(w_scales[(int64_t)b * N + n]);
+                acc += sx * sw * (double)P[((int64_t)m * N + n) * nb + b];
+            }
+            Y[(int64_t)m * N + n] = acc;
+        }
+}
+
+/* fp16 value as integer * 2^(e + 24), e + 24 >= 0 (so the unit is 2^-24) */
+static void f16_fixed(uint16_t h, int64_t* mant, int* shift) {
+    unsigned sign = (h >> 15) & 1u, e = (h >> 10) & 31u, f = h & 1023u;
+    int64_t m;
+    int sh;
+    if (e == 0) { m = f; sh = 0; }                      /* f * 2^-24 */
+    else { m = 1024 + f; sh = (int)e - 1; }             /* (1024+f) * 2^(e-25) = m * 2^-24 * 2^(e-1) */
+    *mant = sign ? -m : m;
+    *shift = sh;
+}
+
+/* The same sum evaluated exactly: every term is an integer multiple of 2^-48, summed in a
+ * signed 128-bit accumulator, then rounded once to the nearest double. */
+void oracle_epilogue_exact(const int32_t* P, const uint16_t* a_scales, const uint16_t* w_scales,
+                           int M, int N, int nb, double* Y) {
+#pragma omp parallel for schedule(static)
+    for (int m = 0; m < M; ++m)
+        for (int n = 0; n < N; ++n) {
+            __int128 acc = 0;
+            for (int b = 0; b < nb; ++b) {
+                int64_t mx, mw;
+                int shx, shw;
+                f16_fixed(a_scales[(int64_t)b * M + m], &mx, &shx);
+                f16_fixed(w_scales[(int64_t)b * N + n], &mw, &shw);
+                __int128 t = (__int128)mx * (__int128)mw * (__int128)P[((int64_t)m * N + n) * nb + b];
+                acc += t << (shx + shw);
+            }
+            Y[(int64_t)m * N + n] = ldexp((double)acc, -48);
+        }
+}
+
+/* Sampled reference for large shapes: for S output positions (ms[s], ns[s]) compute the
+ * per-block partials P[s][b] (exact) and Y[s] (fp64, block order) from the codes and scales. */
+void oracle_gemm_sample(const int8_t* Aq, const int8_t* Wq, const uint16_t* a_scales,
+                        const uint16_t* w_scales, int M, int N, int K, int S,
+                        const int32_t* ms, const int32_t* ns, int32_t* P, double* Y) {
+    const int nb = K / ORACLE_BLOCK;
+#pragma omp parallel for schedule(static)
+    for (int s = 0; s < S; ++s) {
+        const int m = ms[s], n = ns[s];
+        double acc = 0.0;
+        for (int b = 0; b < nb; ++b) {
+            int64_t p = 0;
+            for (int j = b * ORACLE_BLOCK; j < (b + 1) * ORACLE_BLOCK; ++j)
+                p += (int64_t)Aq[(int64_t)m * K + j] * (int64_t)Wq[(int64_t)n * K + j];
+            if (P) P[(int64_t)s * nb + b] = (int32_t)p;
+            double sx = oracle_f16_to_f32(a_scales[(int64_t)b * M + m]);
+            double sw = oracle_f16_to_f32(w_scales[(int64_t)b * N + n]);
+            acc += sx * sw * (double)p;
+        }
+        Y[s] = acc;
+    }
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
