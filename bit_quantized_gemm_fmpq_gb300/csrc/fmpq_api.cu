@@ -1,0 +1,224 @@
+// C ABI of the FMPQ W4Ax library (declared in include/fmpq.h): argument validation,
+// layout handles, and kernel launches on the caller's stream.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/fmpq.h"
+#include "fmpq_internal.h"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fmpq_status check_device(const fmpq_layout* L) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FMPQ_ERR_CUDA;
+    return dev == L->device ? FMPQ_OK : FMPQ_ERR_DEVICE;
+}
+
+fmpq_status launched(cudaError_t e) { return e == cudaSuccess ? FMPQ_OK : FMPQ_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+fmpq_status fmpq_layout_create(int32_t K, const int32_t* perm_host, const uint8_t* outlier_block_mask_host,
+                               fmpq_layout** out) {
+    if (out == nullptr || perm_host == nullptr || outlier_block_mask_host == nullptr) return FMPQ_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (K < FMPQ_BLOCK || K > FMPQ_MAX_K || K % FMPQ_BLOCK != 0) return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    const int nb = K / FMPQ_BLOCK;
+    std::vector<uint8_t> seen(static_cast<size_t>(K), 0);
+    std::vector<uint16_t> perm16(static_cast<size_t>(K));
+    for (int j = 0; j < K; ++j) {
+        const int32_t c = perm_host[j];
+        if (c < 0 || c >= K || seen[c]) return FMPQ_ERR_INVALID_ARG;
+        seen[c] = 1;
+        perm16[j] = static_cast<uint16_t>(c);
+    }
+    std::vector<int32_t> boff(static_cast<size_t>(nb));
+    int n8 = 0;
+    int32_t off = 0;
+    for (int b = 0; b < nb; ++b) {
+        const uint8_t m = outlier_block_mask_host[b];
+        if (m > 1) return FMPQ_ERR_INVALID_ARG;
+        boff[b] = off;
+        off += m ? 128 : 64;
+        n8 += m;
+    }
+    int dev = -1, major = 0, minor = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FMPQ_ERR_DEVICE;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return FMPQ_ERR_DEVICE;
+    if (major != 10 || minor != 3) return FMPQ_ERR_DEVICE;  // built for sm_103a only
+
+    fmpq_layout* L = new (std::nothrow) fmpq_layout();
+    if (L == nullptr) return FMPQ_ERR_INVALID_ARG;
+    L->K = K;
+    L->nb = nb;
+    L->n8 = n8;
+    L->device = dev;
+    L->num_sms = sms;
+    L->row_bytes = off;
+    bool ok = cudaMalloc(&L->d_perm16, sizeof(uint16_t) * K) == cudaSuccess &&
+              cudaMalloc(&L->d_mask, static_cast<size_t>(nb)) == cudaSuccess &&
+              cudaMalloc(&L->d_boff, sizeof(int32_t) * nb) == cudaSuccess &&
+              cudaMalloc(&L->d_status, sizeof(int32_t)) == cudaSuccess;
+    ok = ok && cudaMemcpy(L->d_perm16, perm16.data(), sizeof(uint16_t) * K, cudaMemcpyHostToDevice) == cudaSuccess &&
+         cudaMemcpy(L->d_mask, outlier_block_mask_host, static_cast<size_t>(nb), cudaMemcpyHostToDevice) == cudaSuccess &&
+         cudaMemcpy(L->d_boff, boff.data(), sizeof(int32_t) * nb, cudaMemcpyHostToDevice) == cudaSuccess &&
+         cudaMemset(L->d_status, 0, sizeof(int32_t)) == cudaSuccess;
+    if (!ok) {
+        fmpq_layout_destroy(L);
+        return FMPQ_ERR_CUDA;
+    }
+    *out = L;
+    return FMPQ_OK;
+}
+
+void fmpq_layout_destroy(fmpq_layout* L) {
+    if (L == nullptr) return;
+    int prev = -1;
+    const bool switched = cudaGetDevice(&prev) == cudaSuccess && prev != L->device && L->device >= 0 &&
+                          cudaSetDevice(L->device) == cudaSuccess;
+    cudaDeviceSynchronize();
+    cudaFree(L->d_perm16);
+    cudaFree(L->d_mask);
+    cudaFree(L->d_boff);
+    cudaFree(L->d_status);
+    if (switched) cudaSetDevice(prev);
+    delete L;
+}
+
+int32_t fmpq_layout_k(const fmpq_layout* L) { return L ? L->K : 0; }
+int32_t fmpq_layout_num_blocks(const fmpq_layout* L) { return L ? L->nb : 0; }
+int32_t fmpq_layout_num_int8_blocks(const fmpq_layout* L) { return L ? L->n8 : 0; }
+
+size_t fmpq_packed_a_bytes(const fmpq_layout* L, int64_t M) {
+    if (L == nullptr || M < 0) return 0;
+    return static_cast<size_t>(M) * static_cast<size_t>(L->row_bytes);
+}
+
+size_t fmpq_packed_w_bytes(const fmpq_layout* L, int64_t N) {
+    if (L == nullptr || N < 0) return 0;
+    const int64_t npad = (N + fmpq::kTileN - 1) / fmpq::kTileN * fmpq::kTileN;
+    return static_cast<size_t>(npad) * static_cast<size_t>(L->K / 2);
+}
+
+fmpq_status fmpq_quantize(const fmpq_layout* L, const void* X, int64_t ldx, int64_t M, void* A_packed,
+                          void* a_scales, void* stream) {
+    if (L == nullptr || X == nullptr || A_packed == nullptr || a_scales == nullptr) return FMPQ_ERR_INVALID_ARG;
+    if (M < 1 || M > INT32_MAX || ldx < L->K) return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (ldx % 8 != 0 || !aligned16(X) || !aligned16(A_packed) || !aligned16(a_scales)) return FMPQ_ERR_MISALIGNED;
+    if (fmpq_status st = check_device(L)) return st;
+    return launched(fmpq::launch_quantize(*L, X, ldx, M, A_packed, a_scales, static_cast<cudaStream_t>(stream)));
+}
+
+fmpq_status w4_pack_weights(const fmpq_layout* L, const void* W, int64_t ldw, int64_t N, void* W_packed,
+                            void* w_scales, void* stream) {
+    if (L == nullptr || W == nullptr || W_packed == nullptr || w_scales == nullptr) return FMPQ_ERR_INVALID_ARG;
+    if (N < 16 || N % 16 != 0 || N > INT32_MAX || ldw < L->K) return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (ldw % 8 != 0 || !aligned16(W) || !aligned16(W_packed) || !aligned16(w_scales)) return FMPQ_ERR_MISALIGNED;
+    if (fmpq_status st = check_device(L)) return st;
+    return launched(fmpq::launch_pack_weights(*L, W, ldw, N, W_packed, w_scales, static_cast<cudaStream_t>(stream)));
+}
+
+fmpq_status w4_unpack_weights(const fmpq_layout* L, const void* W_packed, int64_t N, int8_t* Wq, void* stream) {
+    if (L == nullptr || W_packed == nullptr || Wq == nullptr) return FMPQ_ERR_INVALID_ARG;
+    if (N < 16 || N % 16 != 0 || N > INT32_MAX) return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(W_packed) || !aligned16(Wq)) return FMPQ_ERR_MISALIGNED;
+    if (fmpq_status st = check_device(L)) return st;
+    return launched(fmpq::launch_unpack_weights(*L, W_packed, N, Wq, static_cast<cudaStream_t>(stream)));
+}
+
+size_t w4ax_gemm_workspace_bytes(const fmpq_layout* L, int64_t M, int64_t N) {
+    if (L == nullptr || M < 1 || N < 1) return 0;
+    return fmpq::gemm_workspace_bytes(*L, M, N);
+}
+
+fmpq_status w4ax_gemm(const fmpq_layout* L, const void* A_packed, const void* a_scales, const void* W_packed,
+                      const void* w_scales, int64_t M, int64_t N, void* Y, int64_t ldy, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+    if (L == nullptr || A_packed == nullptr || a_scales == nullptr || W_packed == nullptr || w_scales == nullptr ||
+        Y == nullptr)
+        return FMPQ_ERR_INVALID_ARG;
+    if (M < 1 || M > INT32_MAX || N < 16 || N % 16 != 0 || N > INT32_MAX || ldy < N)
+        return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (ldy % 8 != 0 || !aligned16(A_packed) || !aligned16(a_scales) || !aligned16(W_packed) ||
+        !aligned16(w_scales) || !aligned16(Y))
+        return FMPQ_ERR_MISALIGNED;
+    const size_t need = fmpq::gemm_workspace_bytes(*L, M, N);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return FMPQ_ERR_WORKSPACE;
+    if (need > 0 && !aligned16(workspace)) return FMPQ_ERR_MISALIGNED;
+    if (fmpq_status st = check_device(L)) return st;
+    fmpq::GemmArgs a{};
+    a.A = A_packed;
+    a.a_scales = a_scales;
+    a.W = W_packed;
+    a.w_scales = w_scales;
+    a.M = M;
+    a.N = N;
+    a.Y = Y;
+    a.ldy = ldy;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    return launched(fmpq::launch_gemm(*L, a, static_cast<cudaStream_t>(stream)));
+}
+
+fmpq_status w4ax_gemm_partials(const fmpq_layout* L, const void* A_packed, const void* W_packed, int64_t M,
+                               int64_t N, int64_t m0, int64_t mcount, int64_t n0, int64_t ncount, int32_t* P,
+                               void* stream) {
+    if (L == nullptr || A_packed == nullptr || W_packed == nullptr || P == nullptr) return FMPQ_ERR_INVALID_ARG;
+    if (M < 1 || M > INT32_MAX || N < 16 || N % 16 != 0 || N > INT32_MAX) return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (m0 < 0 || mcount < 1 || m0 + mcount > M || n0 < 0 || ncount < 1 || n0 + ncount > N)
+        return FMPQ_ERR_INVALID_ARG;
+    if (!aligned16(A_packed) || !aligned16(W_packed)) return FMPQ_ERR_MISALIGNED;
+    if (fmpq_status st = check_device(L)) return st;
+    fmpq::GemmArgs a{};
+    a.A = A_packed;
+    a.W = W_packed;
+    a.M = M;
+    a.N = N;
+    a.P = P;
+    a.pm0 = m0;
+    a.pmcount = mcount;
+    a.pn0 = n0;
+    a.pncount = ncount;
+    // scales are not used by the partial-sum export; point them at valid memory
+    a.a_scales = A_packed;
+    a.w_scales = W_packed;
+    return launched(fmpq::launch_gemm(*L, a, static_cast<cudaStream_t>(stream)));
+}
+
+fmpq_status fmpq_device_status(const fmpq_layout* L, int32_t* code, int32_t clear) {
+    if (L == nullptr || code == nullptr) return FMPQ_ERR_INVALID_ARG;
+    if (fmpq_status st = check_device(L)) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) return FMPQ_ERR_CUDA;
+    if (cudaMemcpy(code, L->d_status, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess) return FMPQ_ERR_CUDA;
+    if (clear && cudaMemset(L->d_status, 0, sizeof(int32_t)) != cudaSuccess) return FMPQ_ERR_CUDA;
+    return FMPQ_OK;
+}
+
+const char* fmpq_status_string(fmpq_status s) {
+    switch (s) {
+        case FMPQ_OK: return "ok";
+        case FMPQ_ERR_INVALID_ARG: return "invalid argument";
+        case FMPQ_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case FMPQ_ERR_MISALIGNED: return "misaligned pointer or leading dimension";
+        case FMPQ_ERR_CUDA: return "CUDA error";
+        case FMPQ_ERR_TIMEOUT: return "device wait timed out";
+        case FMPQ_ERR_DEVICE: return "unsupported or wrong device";
+        case FMPQ_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+int32_t fmpq_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,52 @@
+// Host-side internals shared by the C-ABI implementation and the kernel launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+struct fmpq_layout {
+    int32_t K = 0;
+    int32_t nb = 0;          // K / 128
+    int32_t n8 = 0;          // number of INT8 blocks
+    int device = -1;
+    int num_sms = 0;
+    uint16_t* d_perm16 = nullptr;  // [K] gather permutation (K <= 65536)
+    uint8_t* d_mask = nullptr;     // [nb] 1 = INT8 block
+    int32_t* d_boff = nullptr;     // [nb] packed-A block offset in bytes per row
+    int32_t* d_status = nullptr;   // device status word
+    int64_t row_bytes = 0;         // packed-A bytes per token: 64*n4 + 128*n8
+};
+
+namespace fmpq {
+
+constexpr int kBlock = 128;
+constexpr int kTileN = 256;          // packed-weight row grouping and GEMM tile width
+constexpr int kTileM = 128;
+
+// Launchers (return cudaGetLastError() after the launch).
+cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, int64_t M, void* A, void* scales,
+                            cudaStream_t stream);
+cudaError_t launch_pack_weights(const fmpq_layout& L, const void* W, int64_t ldw, int64_t N, void* Wp,
+                                void* scales, cudaStream_t stream);
+cudaError_t launch_unpack_weights(const fmpq_layout& L, const void* Wp, int64_t N, int8_t* Wq, cudaStream_t stream);
+
+struct GemmArgs {
+    const void* A;
+    const void* a_scales;
+    const void* W;
+    const void* w_scales;
+    int64_t M, N;
+    void* Y;
+    int64_t ldy;
+    void* workspace;
+    size_t workspace_bytes;
+    // partial-sum export (debug): when P != nullptr the kernel writes P instead of Y
+    int32_t* P;
+    int64_t pm0, pmcount, pn0, pncount;
+};
+
+size_t gemm_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N);
+cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& args, cudaStream_t stream);
+
+}  // namespace fmpq

@@ -1,0 +1,322 @@
+// FMPQ activation quantizer and offline weight packing (sm_103a).
+//
+// Activation quantizer: one fused pass per token row -- gather-permute (QUIK explainer,
+// "kernel fusion": one kernel reads the input, computes the statistics, quantizes and
+// splits in a single pass), per-(token, 128-channel block) absmax, fp16 scale, exact
+// round-half-even quantization to INT8 (outlier blocks) or INT4 (the rest; COMET news
+// article, section 1), and packing into the sign-magnitude layout documented in fmpq.h.
+//
+// HBM-bound design: persistent CTAs (one per SM) stream whole rows into shared memory with
+// TMA bulk copies (a dedicated producer warp, double/triple-buffered), keep the permutation
+// resident in shared memory as 16-bit indices, gather from shared memory, and write the
+// packed codes with coalesced stores.
+#include <cuda_fp16.h>
+
+#include "fmpq_device.cuh"
+#include "fmpq_internal.h"
+
+namespace fmpq {
+namespace {
+
+constexpr int kQuantWarps = 8;                       // compute warps; +1 producer warp
+constexpr int kQuantThreads = (kQuantWarps + 1) * 32;
+constexpr int kQuantSmemBudget = 200 * 1024;
+
+// ---------------------------------------------------------------------------------
+// Per-lane quantization of 4 values of one block (the warp covers the block's 128
+// channels, 4 per lane). Returns the 4 sign-magnitude bytes (byte i = element i) and,
+// through *scale_bits, the block's fp16 scale.
+//
+// Scale: s = fp16_rne(fp32(absmax) / qmax) with IEEE division.
+// Codes: q = clamp(rne(x / s), -qmax, qmax), where rne(x/s) is the round-half-even of the
+// exact quotient. For fp16 x and s the exact quotient is never within 3e-5 of a
+// half-integer unless it is one, so this equals rounding the fp32 IEEE quotient; it is
+// computed as a reciprocal multiply (error < 2e-5) whose few near-half cases (|frac| >
+// 0.4999) are resolved with the exact remainder x - q*s (one FMA, exact here).
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t quantize4(const uint16_t (&h)[4], int qmax, uint16_t* scale_bits) {
+    uint32_t a = max(max(h[0] & 0x7FFFu, h[1] & 0x7FFFu), max(h[2] & 0x7FFFu, h[3] & 0x7FFFu));
+    a = __reduce_max_sync(0xFFFFFFFFu, a);
+    const float amax = __half2float(__ushort_as_half(static_cast<unsigned short>(a)));
+    const __half s16 = __float2half_rn(__fdiv_rn(amax, static_cast<float>(qmax)));
+    *scale_bits = __half_as_ushort(s16);
+    const float s = __half2float(s16);
+    if (s == 0.0f) return 0u;  // warp-uniform
+
+    const float inv = __frcp_rn(s);
+    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: adding it rounds to an integer (RNE)
+    float ax[4], r[4];
+    uint32_t mag[4];
+    bool near_half = false;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float x = __half2float(__ushort_as_half(h[i]));
+        ax[i] = fabsf(x);
+        const float t = __fmul_rn(ax[i], inv) + kMagic;
+        r[i] = t - kMagic;                                   // rint(|x| * inv), exact
+        mag[i] = __float_as_uint(t) & 0x3FFu;
+        const float f = __fmul_rn(ax[i], inv) - r[i];
+        near_half |= (fabsf(f) > 0.4999f);
+    }
+    if (__any_sync(0xFFFFFFFFu, near_half)) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float e = fmaf(-r[i], s, ax[i]);           // exact remainder |x| - r*s
+            const float e2 = e + e;
+            if (e2 > s) {
+                mag[i] += 1;
+            } else if (e2 < -s) {
+                mag[i] -= 1;
+            } else if ((e2 == s || e2 == -s) && (mag[i] & 1u)) {
+                mag[i] = (e2 > 0.0f) ? mag[i] + 1 : mag[i] - 1;  // tie: to even
+            }
+        }
+    }
+    if (s < 6.103515625e-05f) {  // subnormal scale: rounding can overshoot qmax (warp-uniform)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mag[i] = min(mag[i], static_cast<uint32_t>(qmax));
+    }
+    uint32_t v = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t sign = ((h[i] & 0x8000u) && mag[i]) ? 0x80u : 0u;
+        v |= (mag[i] | sign) << (8 * i);
+    }
+    return v;
+}
+
+// INT4 packing of a warp's 4-code groups: lanes 2g and 2g+1 hold channels 8g..8g+3 and
+// 8g+4..8g+7 as sign-magnitude bytes v; the packed word is v_even | rotl(v_odd, 4)
+// (magnitudes 4..7 move to bits 4-6 and their signs to bit 3 of the next byte).
+// Valid in even lanes.
+__device__ __forceinline__ uint32_t pack_int4_pair(uint32_t v, int lane) {
+    const uint32_t mine = (lane & 1) ? __funnelshift_l(v, v, 4) : v;
+    return mine | __shfl_xor_sync(0xFFFFFFFFu, mine, 1);
+}
+
+struct QuantParams {
+    const uint16_t* X;
+    int64_t ldx;
+    int64_t M;
+    int K, nb, stages;
+    const uint16_t* perm;
+    const uint8_t* mask;
+    const int32_t* boff;
+    uint8_t* A;
+    uint16_t* scales;
+    int32_t* status;
+};
+
+__global__ void __launch_bounds__(kQuantThreads, 1) quantize_kernel(QuantParams p) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    const int K = p.K, nb = p.nb, S = p.stages;
+    uint16_t* perm_s = reinterpret_cast<uint16_t*>(smem_raw);                       // [K]
+    uint16_t* rows_s = perm_s + K;                                                 // [S][K]
+    uint8_t* mask_s = reinterpret_cast<uint8_t*>(rows_s + static_cast<size_t>(S) * K);  // [nb]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + ((2ull * K * (S + 1) + nb + 15) & ~15ull));
+    uint64_t* full = bars;        // [S]
+    uint64_t* empty = bars + S;   // [S]
+    uint64_t* perm_bar = bars + 2 * S;
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            dev::mbar_init(&full[s], 1);
+            dev::mbar_init(&empty[s], kQuantWarps);
+        }
+        dev::mbar_init(perm_bar, 1);
+        abort_flag = 0;
+        dev::fence_barrier_init();
+    }
+    for (int b = threadIdx.x; b < nb; b += blockDim.x) mask_s[b] = p.mask[b];
+    __syncthreads();
+
+    const uint32_t row_bytes = static_cast<uint32_t>(K) * 2u;
+    if (warp == kQuantWarps) {
+        // ---------------- producer: permutation once, then rows into the stage ring
+        if (lane == 0) {
+            dev::mbar_arrive_expect_tx(perm_bar, row_bytes);
+            dev::bulk_g2s(perm_s, p.perm, row_bytes, perm_bar);
+            int64_t i = 0;
+            for (int64_t m = blockIdx.x; m < p.M; m += gridDim.x, ++i) {
+                const int s = static_cast<int>(i % S);
+                const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
+                if (!dev::mbar_wait(&empty[s], ph ^ 1u, &abort_flag)) {
+                    abort_flag = 1;
+                    break;
+                }
+                dev::mbar_arrive_expect_tx(&full[s], row_bytes);
+                dev::bulk_g2s(rows_s + static_cast<size_t>(s) * K, p.X + m * p.ldx, row_bytes, &full[s]);
+            }
+            // drain: every stage's latest copy must have landed before the CTA exits
+            const int64_t issued = i;
+            for (int s = 0; s < S; ++s) {
+                if (issued <= s) break;
+                const int64_t last = s + ((issued - 1 - s) / S) * S;
+                dev::mbar_wait(&full[s], static_cast<uint32_t>((last / S) & 1), nullptr);
+            }
+            dev::mbar_wait(perm_bar, 0, nullptr);
+        }
+    } else {
+        // ---------------- compute warps
+        bool ok = true;
+        if (lane == 0) ok = dev::mbar_wait(perm_bar, 0, &abort_flag);
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        int64_t i = 0;
+        for (int64_t m = blockIdx.x; ok && m < p.M; m += gridDim.x, ++i) {
+            const int s = static_cast<int>(i % S);
+            const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
+            if (lane == 0) ok = dev::mbar_wait(&full[s], ph, &abort_flag);
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok) break;
+            const uint16_t* xrow = rows_s + static_cast<size_t>(s) * K;
+            for (int b = warp; b < nb; b += kQuantWarps) {
+                const int j0 = b * kBlock + lane * 4;
+                const uint2 pp = *reinterpret_cast<const uint2*>(perm_s + j0);
+                uint16_t h[4];
+                h[0] = xrow[pp.x & 0xFFFFu];
+                h[1] = xrow[pp.x >> 16];
+                h[2] = xrow[pp.y & 0xFFFFu];
+                h[3] = xrow[pp.y >> 16];
+                const bool is8 = mask_s[b] != 0;
+                uint16_t sbits;
+                const uint32_t v = quantize4(h, is8 ? 127 : 7, &sbits);
+                uint8_t* blk = p.A + static_cast<int64_t>(p.boff[b]) * p.M;
+                if (is8) {
+                    reinterpret_cast<uint32_t*>(blk + m * 128)[lane] = v;
+                } else {
+                    const uint32_t word = pack_int4_pair(v, lane);
+                    if ((lane & 1) == 0) reinterpret_cast<uint32_t*>(blk + m * 64)[lane >> 1] = word;
+                }
+                if (lane == 0) p.scales[static_cast<int64_t>(b) * p.M + m] = sbits;
+            }
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(&empty[s]);
+        }
+        if (!ok && lane == 0) abort_flag = 1;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && abort_flag) dev::report(p.status, dev::kStatusTimeout);
+}
+
+// ---------------------------------------------------------------------------------
+// Offline weight packing: one warp per (output channel n, block b). Same scale and
+// rounding rule as the activations with qmax = 7. Output layout (implementation-defined):
+// rows grouped by 256; group g, block b occupies 16 KB at ((g*nb + b) * 16384), row r of
+// the group at + r*64, in the INT4 word format of the packed activations. Rows past N
+// (padding up to a multiple of 256) are written as zero codes.
+// ---------------------------------------------------------------------------------
+struct PackParams {
+    const uint16_t* W;
+    int64_t ldw;
+    int64_t N, Npad;
+    int K, nb;
+    const uint16_t* perm;
+    uint8_t* Wp;
+    uint16_t* scales;
+};
+
+__global__ void __launch_bounds__(256) pack_weights_kernel(PackParams p) {
+    const int lane = threadIdx.x & 31;
+    const int64_t task = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (task >= p.Npad * p.nb) return;  // warp-uniform
+    const int64_t n = task / p.nb;
+    const int b = static_cast<int>(task % p.nb);
+    uint32_t v = 0;
+    uint16_t sbits = 0;
+    if (n < p.N) {
+        uint16_t h[4];
+        const int j0 = b * kBlock + lane * 4;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = p.W[n * p.ldw + p.perm[j0 + i]];
+        v = quantize4(h, 7, &sbits);
+    }
+    const uint32_t word = pack_int4_pair(v, lane);
+    uint8_t* dst = p.Wp + ((n / kTileN) * p.nb + b) * 16384 + (n % kTileN) * 64;
+    if ((lane & 1) == 0) reinterpret_cast<uint32_t*>(dst)[lane >> 1] = word;
+    if (lane == 0 && n < p.N) p.scales[static_cast<int64_t>(b) * p.N + n] = sbits;
+}
+
+// Debug decode of the packed weights to int8 codes [N][K] (permuted channel order).
+__global__ void unpack_weights_kernel(const uint8_t* Wp, int64_t N, int K, int nb, int8_t* Wq) {
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;  // one word
+    const int64_t words_per_row = K / 8;
+    if (t >= N * words_per_row) return;
+    const int64_t n = t / words_per_row;
+    const int wi = static_cast<int>(t % words_per_row);
+    const int b = wi / 16, g = wi % 16;
+    const uint32_t w =
+        *reinterpret_cast<const uint32_t*>(Wp + ((n / kTileN) * nb + b) * 16384 + (n % kTileN) * 64 + g * 4);
+    int8_t* out = Wq + n * K + b * kBlock + g * 8;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t byte = (w >> (8 * j)) & 0xFFu;
+        const uint32_t next = (w >> (8 * ((j + 1) & 3))) & 0xFFu;
+        const int lo = byte & 7, hi = (byte >> 4) & 7;
+        out[j] = static_cast<int8_t>((byte & 0x80u) ? -lo : lo);
+        out[4 + j] = static_cast<int8_t>((next & 0x08u) ? -hi : hi);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, int64_t M, void* A, void* scales,
+                            cudaStream_t stream) {
+    const int K = L.K;
+    const size_t fixed = 2ull * K + L.nb + 16 + 1024;
+    int stages = static_cast<int>((kQuantSmemBudget - fixed) / (2ull * K));
+    stages = stages < 1 ? 1 : (stages > 4 ? 4 : stages);
+    const size_t smem = ((2ull * K * (stages + 1) + L.nb + 15) & ~15ull) + 8ull * (2 * stages + 1);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kQuantSmemBudget + 16 * 1024);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    QuantParams p;
+    p.X = static_cast<const uint16_t*>(X);
+    p.ldx = ldx;
+    p.M = M;
+    p.K = K;
+    p.nb = L.nb;
+    p.stages = stages;
+    p.perm = L.d_perm16;
+    p.mask = L.d_mask;
+    p.boff = L.d_boff;
+    p.A = static_cast<uint8_t*>(A);
+    p.scales = static_cast<uint16_t*>(scales);
+    p.status = L.d_status;
+    const int64_t grid = M < L.num_sms ? M : L.num_sms;
+    quantize_kernel<<<static_cast<unsigned>(grid), kQuantThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_weights(const fmpq_layout& L, const void* W, int64_t ldw, int64_t N, void* Wp,
+                                void* scales, cudaStream_t stream) {
+    PackParams p;
+    p.W = static_cast<const uint16_t*>(W);
+    p.ldw = ldw;
+    p.N = N;
+    p.Npad = (N + kTileN - 1) / kTileN * kTileN;
+    p.K = L.K;
+    p.nb = L.nb;
+    p.perm = L.d_perm16;
+    p.Wp = static_cast<uint8_t*>(Wp);
+    p.scales = static_cast<uint16_t*>(scales);
+    const int64_t warps = p.Npad * p.nb;
+    const int64_t blocks = (warps * 32 + 255) / 256;
+    pack_weights_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_unpack_weights(const fmpq_layout& L, const void* Wp, int64_t N, int8_t* Wq, cudaStream_t stream) {
+    const int64_t words = N * (L.K / 8);
+    const int64_t blocks = (words + 255) / 256;
+    unpack_weights_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(static_cast<const uint8_t*>(Wp), N,
+                                                                             L.K, L.nb, Wq);
+    return cudaGetLastError();
+}
+
+}  // namespace fmpq

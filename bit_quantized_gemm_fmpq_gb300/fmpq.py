@@ -1,0 +1,230 @@
+"""Thin Python binding of the C ABI in include/fmpq.h (argument marshalling only).
+
+Every function here forwards to the CUDA library built in-tree
+(bit_quantized_gemm_fmpq_gb300/_build/libfmpq_gb300.so); all the arithmetic runs in its
+kernels. Torch is used only to own device memory and to supply the current CUDA stream.
+If the library is missing, the first call raises ``FmpqLibraryMissing``: there is no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libfmpq_gb300.so")
+BLOCK = 128
+TILE_N = 256
+
+_lib = None
+_lock = threading.Lock()
+
+STATUS = {
+    0: "FMPQ_OK", 1: "FMPQ_ERR_INVALID_ARG", 2: "FMPQ_ERR_UNSUPPORTED_SHAPE", 3: "FMPQ_ERR_MISALIGNED",
+    4: "FMPQ_ERR_CUDA", 5: "FMPQ_ERR_TIMEOUT", 6: "FMPQ_ERR_DEVICE", 7: "FMPQ_ERR_WORKSPACE",
+}
+
+# C-ABI symbols and their ctypes signatures (restype, argtypes)
+_P, _I32, _I64, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+SIGNATURES = {
+    "fmpq_layout_create": (_I32, [_I32, _P, _P, ctypes.POINTER(_P)]),
+    "fmpq_layout_destroy": (None, [_P]),
+    "fmpq_layout_k": (_I32, [_P]),
+    "fmpq_layout_num_blocks": (_I32, [_P]),
+    "fmpq_layout_num_int8_blocks": (_I32, [_P]),
+    "fmpq_packed_a_bytes": (_SZ, [_P, _I64]),
+    "fmpq_packed_w_bytes": (_SZ, [_P, _I64]),
+    "fmpq_quantize": (_I32, [_P, _P, _I64, _I64, _P, _P, _P]),
+    "w4_pack_weights": (_I32, [_P, _P, _I64, _I64, _P, _P, _P]),
+    "w4_unpack_weights": (_I32, [_P, _P, _I64, _P, _P]),
+    "w4ax_gemm_workspace_bytes": (_SZ, [_P, _I64, _I64]),
+    "w4ax_gemm": (_I32, [_P, _P, _P, _P, _P, _I64, _I64, _P, _I64, _P, _SZ, _P]),
+    "w4ax_gemm_partials": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P]),
+    "fmpq_device_status": (_I32, [_P, ctypes.POINTER(_I32), _I32]),
+    "fmpq_status_string": (ctypes.c_char_p, [_I32]),
+    "fmpq_version": (_I32, []),
+}
+
+
+class FmpqLibraryMissing(RuntimeError):
+    pass
+
+
+class FmpqError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {STATUS.get(code, code)}")
+        self.code = code
+
+
+def load_library():
+    """Load the in-tree CUDA library (raises FmpqLibraryMissing when it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise FmpqLibraryMissing(
+                    f"{LIB_PATH} is missing: build it with `python -m bit_quantized_gemm_fmpq_gb300.build`")
+            lib = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(lib, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise FmpqError(fn, code)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+class Layout:
+    """Owns an fmpq_layout* (channel permutation + outlier-block mask) on the current device."""
+
+    def __init__(self, K: int, perm, mask):
+        lib = load_library()
+        perm = np.ascontiguousarray(perm, dtype=np.int32)
+        mask = np.ascontiguousarray(mask, dtype=np.uint8)
+        if perm.shape != (K,) or mask.shape != (K // BLOCK,):
+            raise ValueError("perm must have K entries and mask K/128 entries")
+        h = ctypes.c_void_p()
+        _check("fmpq_layout_create", lib.fmpq_layout_create(K, perm.ctypes.data, mask.ctypes.data, ctypes.byref(h)))
+        self._h = h
+        self._lib = lib
+        self.K = K
+        self.nb = K // BLOCK
+        self.mask = mask.copy()
+        self.perm = perm.copy()
+        self._workspaces = {}
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            self._lib.fmpq_layout_destroy(self._h)
+            self._h = ctypes.c_void_p()
+        self._workspaces = {}
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def n8(self) -> int:
+        return int(self._lib.fmpq_layout_num_int8_blocks(self._h))
+
+    def packed_a_bytes(self, M: int) -> int:
+        return int(self._lib.fmpq_packed_a_bytes(self._h, M))
+
+    def packed_w_bytes(self, N: int) -> int:
+        return int(self._lib.fmpq_packed_w_bytes(self._h, N))
+
+    def workspace_bytes(self, M: int, N: int) -> int:
+        return int(self._lib.w4ax_gemm_workspace_bytes(self._h, M, N))
+
+    def workspace(self, M: int, N: int):
+        """A zero-initialised, reusable workspace tensor for (M, N) (cached per size)."""
+        import torch
+        nbytes = self.workspace_bytes(M, N)
+        if nbytes == 0:
+            return None
+        ws = self._workspaces.get(nbytes)
+        if ws is None:
+            ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+            self._workspaces[nbytes] = ws
+        return ws
+
+
+# ---- the C-ABI entry points, same names ---------------------------------------------------
+
+def fmpq_layout_create(K: int, perm, mask) -> Layout:
+    return Layout(K, perm, mask)
+
+
+def fmpq_quantize(layout: Layout, X, A_packed=None, a_scales=None, stream=None):
+    """X: fp16 CUDA tensor [M, >=K] (row stride multiple of 8). Returns (A_packed u8, a_scales fp16 [nb, M])."""
+    import torch
+    M = X.shape[0]
+    if A_packed is None:
+        A_packed = torch.empty(layout.packed_a_bytes(M), dtype=torch.uint8, device=X.device)
+    if a_scales is None:
+        a_scales = torch.empty((layout.nb, M), dtype=torch.float16, device=X.device)
+    _check("fmpq_quantize", layout._lib.fmpq_quantize(layout.handle, _ptr(X), X.stride(0), M, _ptr(A_packed),
+                                                        _ptr(a_scales), _stream(stream)))
+    return A_packed, a_scales
+
+
+def w4_pack_weights(layout: Layout, W, W_packed=None, w_scales=None, stream=None):
+    """W: fp16 CUDA tensor [N, >=K]. Returns (W_packed u8, w_scales fp16 [nb, N])."""
+    import torch
+    N = W.shape[0]
+    if W_packed is None:
+        W_packed = torch.empty(layout.packed_w_bytes(N), dtype=torch.uint8, device=W.device)
+    if w_scales is None:
+        w_scales = torch.empty((layout.nb, N), dtype=torch.float16, device=W.device)
+    _check("w4_pack_weights", layout._lib.w4_pack_weights(layout.handle, _ptr(W), W.stride(0), N, _ptr(W_packed),
+                                                            _ptr(w_scales), _stream(stream)))
+    return W_packed, w_scales
+
+
+def w4_unpack_weights(layout: Layout, W_packed, N: int, stream=None):
+    import torch
+    Wq = torch.empty((N, layout.K), dtype=torch.int8, device=W_packed.device)
+    _check("w4_unpack_weights", layout._lib.w4_unpack_weights(layout.handle, _ptr(W_packed), N, _ptr(Wq),
+                                                                _stream(stream)))
+    return Wq
+
+
+def w4ax_gemm(layout: Layout, A_packed, a_scales, W_packed, w_scales, M: int, N: int, Y=None, workspace=None,
+              stream=None):
+    """Returns Y fp16 [M, N] (or writes into the given Y [M, >=N])."""
+    import torch
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float16, device=A_packed.device)
+    if workspace is None:
+        workspace = layout.workspace(M, N)
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    _check("w4ax_gemm", layout._lib.w4ax_gemm(layout.handle, _ptr(A_packed), _ptr(a_scales), _ptr(W_packed),
+                                                _ptr(w_scales), M, N, _ptr(Y), Y.stride(0), _ptr(workspace),
+                                                ws_bytes, _stream(stream)))
+    return Y
+
+
+def w4ax_gemm_partials(layout: Layout, A_packed, W_packed, M: int, N: int, m0: int, mcount: int, n0: int,
+                       ncount: int, stream=None):
+    """Exact per-block integer partial sums P int32 [mcount, ncount, nb] from the GEMM's tensor-core path."""
+    import torch
+    P = torch.zeros((mcount, ncount, layout.nb), dtype=torch.int32, device=A_packed.device)
+    _check("w4ax_gemm_partials", layout._lib.w4ax_gemm_partials(layout.handle, _ptr(A_packed), _ptr(W_packed), M, N,
+                                                                  m0, mcount, n0, ncount, _ptr(P), _stream(stream)))
+    return P
+
+
+def fmpq_device_status(layout: Layout, clear: bool = True) -> int:
+    code = ctypes.c_int32(0)
+    _check("fmpq_device_status", layout._lib.fmpq_device_status(layout.handle, ctypes.byref(code), int(clear)))
+    return int(code.value)
+
+
+def fmpq_version() -> int:
+    return int(load_library().fmpq_version())

@@ -37,6 +37,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define FMPQ_API __attribute__((visibility("default")))
+#else
+#define FMPQ_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -53,7 +59,7 @@ typedef enum fmpq_status {
 } fmpq_status;
 
 #define FMPQ_BLOCK 128              /* channels per quantization block */
-#define FMPQ_MAX_K 65536            /* largest supported K */
+#define FMPQ_MAX_K 32768            /* largest supported K */
 
 /* Opaque, library-owned description of one layer's channel permutation and block mask. */
 typedef struct fmpq_layout fmpq_layout;
@@ -66,12 +72,12 @@ typedef struct fmpq_layout fmpq_layout;
  *   outlier_block_mask_host[K/128]  1 = INT8 block (outlier block), 0 = INT4 block.
  *   out                receives the handle.
  * Uploads small device tables on the current device (synchronous). */
-fmpq_status fmpq_layout_create(int32_t K, const int32_t* perm_host,
+FMPQ_API fmpq_status fmpq_layout_create(int32_t K, const int32_t* perm_host,
                                const uint8_t* outlier_block_mask_host, fmpq_layout** out);
-void fmpq_layout_destroy(fmpq_layout* layout);
-int32_t fmpq_layout_k(const fmpq_layout* layout);
-int32_t fmpq_layout_num_blocks(const fmpq_layout* layout);
-int32_t fmpq_layout_num_int8_blocks(const fmpq_layout* layout);
+FMPQ_API void fmpq_layout_destroy(fmpq_layout* layout);
+FMPQ_API int32_t fmpq_layout_k(const fmpq_layout* layout);
+FMPQ_API int32_t fmpq_layout_num_blocks(const fmpq_layout* layout);
+FMPQ_API int32_t fmpq_layout_num_int8_blocks(const fmpq_layout* layout);
 
 /* Bytes of the packed activation buffer for M tokens: M * (64 * n4 + 128 * n8).
  * Layout (block-major; the method's "mixed-precision data layout", made concrete here so
@@ -83,12 +89,12 @@ int32_t fmpq_layout_num_int8_blocks(const fmpq_layout* layout);
  *     byte j (0..3): bits 0-2 = |q_{8g+j}|, bit 7 = sign(q_{8g+j}),
  *                    bits 4-6 = |q_{8g+4+j}|, bit 3 = sign(q_{8g+4+((j+3)%4)}).
  *   sign(q) = 1 iff q < 0. */
-size_t fmpq_packed_a_bytes(const fmpq_layout* layout, int64_t M);
+FMPQ_API size_t fmpq_packed_a_bytes(const fmpq_layout* layout, int64_t M);
 
 /* Bytes of the packed weight buffer for N output channels: ceil(N/256)*256 * K/2.
  * The packed weight format is implementation-defined (tile-major, padded to 256 rows);
  * w4_unpack_weights decodes it. */
-size_t fmpq_packed_w_bytes(const fmpq_layout* layout, int64_t N);
+FMPQ_API size_t fmpq_packed_w_bytes(const fmpq_layout* layout, int64_t N);
 
 /* Fused activation quantizer (one pass: gather-permute, per-(token, block) absmax,
  * fp16 scale, round-half-even quantization, INT4/INT8 packing).
@@ -98,22 +104,24 @@ size_t fmpq_packed_w_bytes(const fmpq_layout* layout, int64_t N);
  *   a_scales  fp16 [K/128][M]: a_scales[b*M + m] = fp16_rne(fp32(absmax)/qmax),
  *             qmax = 127 (INT8 block) or 7 (INT4 block).
  * Codes: q = clamp(rne(fp32(x) / fp32(scale)), -qmax, qmax); a zero scale gives q = 0. */
-fmpq_status fmpq_quantize(const fmpq_layout* layout, const void* X, int64_t ldx, int64_t M,
+FMPQ_API fmpq_status fmpq_quantize(const fmpq_layout* layout, const void* X, int64_t ldx, int64_t M,
                           void* A_packed, void* a_scales, void* stream);
 
 /* Offline weight preparation: W fp16 [N][ldw] (ldw >= K, ldw % 8 == 0, N % 16 == 0)
  * -> W_packed (fmpq_packed_w_bytes) and w_scales fp16 [K/128][N], INT4 range [-7, 7]
  * per output channel and block, same scale and rounding rule as the activations, on the
  * permuted channel order. */
-fmpq_status w4_pack_weights(const fmpq_layout* layout, const void* W, int64_t ldw, int64_t N,
+FMPQ_API fmpq_status w4_pack_weights(const fmpq_layout* layout, const void* W, int64_t ldw, int64_t N,
                             void* W_packed, void* w_scales, void* stream);
 
 /* Debug/test: decode W_packed to codes Wq int8 [N][K] (permuted channel order). */
-fmpq_status w4_unpack_weights(const fmpq_layout* layout, const void* W_packed, int64_t N,
+FMPQ_API fmpq_status w4_unpack_weights(const fmpq_layout* layout, const void* W_packed, int64_t N,
                               int8_t* Wq, void* stream);
 
-/* Workspace bytes w4ax_gemm needs for this shape (0 when it needs none). */
-size_t w4ax_gemm_workspace_bytes(const fmpq_layout* layout, int64_t M, int64_t N);
+/* Workspace bytes w4ax_gemm needs for this shape (0 when it needs none). Shapes with few
+ * output tiles split K across CTAs; the workspace then holds the FP32 partial tiles and one
+ * arrival counter per output tile. */
+FMPQ_API size_t w4ax_gemm_workspace_bytes(const fmpq_layout* layout, int64_t M, int64_t N);
 
 /* The W4Ax GEMM:
  *   Y[m][n] = fp16_rn( sum_b a_scales[b][m] * w_scales[b][n] * P[m][n][b] ),
@@ -121,28 +129,31 @@ size_t w4ax_gemm_workspace_bytes(const fmpq_layout* layout, int64_t M, int64_t N
  * accumulated in FP32.
  *   Y          fp16 [M][ldy], ldy >= N, ldy % 8 == 0; N % 16 == 0.
  *   workspace  w4ax_gemm_workspace_bytes(layout, M, N) bytes (may be NULL when that is 0);
- *              contents need no initialization and are left in a reusable state. */
-fmpq_status w4ax_gemm(const fmpq_layout* layout, const void* A_packed, const void* a_scales,
+ *              zero-filled once before its first use; each call returns the arrival
+ *              counters it uses to zero, so the buffer is reused without re-initialization.
+ *              Calls that share a workspace must not run concurrently.
+ * The split-K reduction sums the K-splits in a fixed order, so results are deterministic. */
+FMPQ_API fmpq_status w4ax_gemm(const fmpq_layout* layout, const void* A_packed, const void* a_scales,
                       const void* W_packed, const void* w_scales, int64_t M, int64_t N,
                       void* Y, int64_t ldy, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Debug/test: the exact per-block integer partial sums P computed by the GEMM's own
  * tensor-core path, for the window [m0, m0+mcount) x [n0, n0+ncount):
  *   P int32 [mcount][ncount][K/128]. */
-fmpq_status w4ax_gemm_partials(const fmpq_layout* layout, const void* A_packed,
+FMPQ_API fmpq_status w4ax_gemm_partials(const fmpq_layout* layout, const void* A_packed,
                                const void* W_packed, int64_t M, int64_t N, int64_t m0,
                                int64_t mcount, int64_t n0, int64_t ncount, int32_t* P,
                                void* stream);
 
 /* Read (and, if clear != 0, reset) the layout's device status word. Synchronizes the
  * device. *code = FMPQ_OK or the first error a kernel recorded (e.g. FMPQ_ERR_TIMEOUT). */
-fmpq_status fmpq_device_status(const fmpq_layout* layout, int32_t* code, int32_t clear);
+FMPQ_API fmpq_status fmpq_device_status(const fmpq_layout* layout, int32_t* code, int32_t clear);
 
 /* Static description of a status code. */
-const char* fmpq_status_string(fmpq_status status);
+FMPQ_API const char* fmpq_status_string(fmpq_status status);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
-int32_t fmpq_version(void);
+FMPQ_API int32_t fmpq_version(void);
 
 #ifdef __cplusplus
 }
