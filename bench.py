@@ -1,0 +1,368 @@
+#!/usr/bin/env python
+"""Benchmark of the FMPQ W4Ax hot path on GB300.
+
+A step is one pass of the hot path over one batch: the fused activation quantizer
+(gather-permute, per-block scales, INT4/INT8 codes) followed by the W4Ax GEMM with its FP32
+epilogue, on the LLaMA-70B down-projection shape (M=4096 tokens, K=28672, N=8192; synthetic
+Laplace activations with 10% outlier channels, 27 of 224 blocks INT8). The INT4 weights are
+packed once beforehand (offline preparation; timed separately and reported, not in the step).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line. `value` is effective TOPS (2*M*N*K per step, INT4 and INT8 blocks
+counted alike) summed over ranks with the max per-rank step time; `e2e` is the same metric
+with the host->device copy of X and the device->host copy of Y inside every step.
+`--impl reference` times the CPU oracle (test infrastructure, never tuned) on bounded
+samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "llama70b_down"
+METRIC = "W4Ax GEMM effective TOPS (% INT8 TC peak) at M=4096; quantizer HBM GB/s"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-steps", type=int, default=0,
+                    help="run this many untimed steps and exit (for profilers)")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------------- helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"fmpq_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.25)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sms, maxs, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, mx = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            sms.append(sm)
+            maxs.append(mx)
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        os.unlink(self.path)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxs), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_quantized_gemm_fmpq_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on this source."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    with open(PROFILE_TRAFFIC) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample_rate(w, target_s: float, rows: int = 8, cols: int = 4096, max_rounds: int = 2000):
+    """Time the oracle (quantizer on `rows` tokens + per-block partials and fp64 epilogue for
+    rows x cols outputs, weights pre-quantized) repeatedly until `target_s` seconds of CPU
+    work; return effective TOPS and a description."""
+    import oracle
+    Wq, sw = oracle.quantize_weights(w.W[:cols], w.perm)
+    done_ops, elapsed, rounds, r0 = 0.0, 0.0, 0, 0
+    while elapsed < target_s and rounds < max_rounds:
+        Xs = w.X[r0:r0 + rows]
+        t0 = time.perf_counter()
+        _, sx, Aq = oracle.quantize_activations(Xs, w.perm, w.mask)
+        ms, ns = np.meshgrid(np.arange(rows, dtype=np.int32), np.arange(cols, dtype=np.int32), indexing="ij")
+        oracle.gemm_sample(Aq, Wq, sx, sw, ms.ravel(), ns.ravel())
+        elapsed += time.perf_counter() - t0
+        done_ops += 2.0 * rows * cols * w.K
+        rounds += 1
+        r0 = (r0 + rows) % (w.M - rows)
+    sample = (f"{rounds} rounds x ({rows} tokens quantized + {rows}x{cols} outputs over K={w.K}) "
+              f"of the {w.M}x{w.K}x{w.N} workload, weights pre-quantized")
+    return done_ops / elapsed / 1e12, elapsed, sample, oracle.num_threads()
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from bit_quantized_gemm_fmpq_gb300 import workloads as wl
+    import oracle
+    oracle.build()
+    w = wl.llama70b_down()
+    per_step = min(2.0, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample_rate(w, per_step / 4, max_rounds=1)
+    vals, total = [], 0.0
+    sample = ""
+    cores = oracle.num_threads()
+    for _ in range(args.steps):
+        v, el, sample, cores = oracle_sample_rate(w, per_step, max_rounds=64)
+        vals.append(v)
+        total += el
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8/int64 (fp64 epilogue)",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "M": w.M, "K": w.K, "N": w.N, "n8_blocks": int(w.mask.sum()),
+                                        "sample": "bounded sample per step"},
+        "cpu_baseline": {"value": value, "unit": "TOPS", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------- our arm
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    world, rank, local = dist_env()
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    from bit_quantized_gemm_fmpq_gb300 import build as fbuild
+    if rank == 0:
+        fbuild.build()
+    if world > 1:
+        torch.distributed.barrier()
+    from bit_quantized_gemm_fmpq_gb300 import fmpq
+    from bit_quantized_gemm_fmpq_gb300 import workloads as wl
+    fmpq.load_library()
+
+    w = wl.llama70b_down()
+    M, K, N = w.M, w.K, w.N
+    layout = fmpq.Layout(K, w.perm, w.mask)
+    stream = torch.cuda.current_stream()
+    X = torch.from_numpy(w.X).cuda()
+    Wd = torch.from_numpy(w.W).cuda()
+    # offline weight preparation (timed once, not part of the step)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    fmpq.w4_pack_weights(layout, Wd)  # warm
+    Wp = torch.empty(layout.packed_w_bytes(N), dtype=torch.uint8, device="cuda")
+    sw = torch.empty((layout.nb, N), dtype=torch.float16, device="cuda")
+    e0.record()
+    fmpq.w4_pack_weights(layout, Wd, Wp, sw)
+    e1.record()
+    torch.cuda.synchronize()
+    pack_ms = e0.elapsed_time(e1)
+    del Wd
+    A = torch.empty(layout.packed_a_bytes(M), dtype=torch.uint8, device="cuda")
+    sx = torch.empty((layout.nb, M), dtype=torch.float16, device="cuda")
+    Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    ws = layout.workspace(M, N)
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device="cuda")
+
+    def step():
+        fmpq.fmpq_quantize(layout, X, A, sx, stream=stream)
+        fmpq.w4ax_gemm(layout, A, sx, Wp, sw, M, N, Y, workspace=ws, stream=stream)
+
+    if args.profile_steps:
+        for _ in range(args.profile_steps):
+            step()
+        torch.cuda.synchronize()
+        return
+
+    for _ in range(max(3, args.warmup)):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        fmpq.fmpq_quantize(layout, X, A, sx, stream=stream)
+        ev[i][1].record(stream)
+        fmpq.w4ax_gemm(layout, A, sx, Wp, sw, M, N, Y, workspace=ws, stream=stream)
+        ev[i][2].record(stream)
+        flush.zero_()  # L2 flush between steps (outside the timed events)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    q_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    g_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    step_ms = sum(q + g for q, g in zip(q_ms, g_ms)) / args.steps
+    if world > 1:
+        t = torch.tensor([step_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(t.item())
+    status = fmpq.fmpq_device_status(layout)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+
+    flops = 2.0 * M * N * K
+    value = world * flops / (step_ms * 1e-3) / 1e12
+    gemm_ms = statistics.mean(g_ms)
+    quant_ms = statistics.mean(q_ms)
+    peaks = measured_peaks()
+    fp8_peak = peaks["bf16_tflops"] * 2.0   # nominal dense fp8/bf16 ratio (4.5 / 2.25)
+    gemm_tflops = flops / (gemm_ms * 1e-3) / 1e12
+    a_bytes = layout.packed_a_bytes(M)
+    quant_bytes = 2 * M * K + 2 * K + a_bytes + 2 * layout.nb * M
+    quant_gbs = quant_bytes / (quant_ms * 1e-3) / 1e9
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        Xh = torch.from_numpy(w.X).pin_memory()
+        Yh = torch.empty((M, N), dtype=torch.float16).pin_memory()
+        n_e2e = max(3, min(args.steps, 50))
+        for _ in range(2):
+            X.copy_(Xh, non_blocking=True)
+            step()
+            Yh.copy_(Y, non_blocking=True)
+        torch.cuda.synchronize()
+        t_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_e2e)]
+        for i in range(n_e2e):
+            t_ev[i][0].record(stream)
+            X.copy_(Xh, non_blocking=True)
+            step()
+            Yh.copy_(Y, non_blocking=True)
+            t_ev[i][1].record(stream)
+            flush.zero_()
+        torch.cuda.synchronize()
+        e2e_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in t_ev)
+        if world > 1:
+            t = torch.tensor([e2e_ms], device="cuda")
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TOPS",
+               "h2d_bytes_per_step": int(Xh.numel() * 2), "d2h_bytes_per_step": int(Yh.numel() * 2),
+               "ms_per_step": e2e_ms}
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.barrier()
+            torch.distributed.destroy_process_group()
+        return
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        v, el, sample, cores = oracle_sample_rate(w, target_s=10.0)
+        cpu = {"value": v, "unit": "TOPS", "cores": cores, "kind": "oracle", "sample": sample, "seconds": el}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int4/int8 codes on e4m3 tensor cores, fp32 epilogue",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N, "n8_blocks": int(w.mask.sum()), "nb": layout.nb,
+                   "step": "fmpq_quantize + w4ax_gemm", "l2": "flushed between steps (2x L2 write, untimed)",
+                   "parallelism": f"replicated weights, one {M}-token batch per GPU"},
+        "gemm": {"ms": gemm_ms, "tflops_effective": gemm_tflops, "frac_fp8_peak": gemm_tflops / fp8_peak},
+        "quantizer": {"ms": quant_ms, "gbs": quant_gbs, "frac_hbm": quant_gbs / peaks["hbm_gbs"],
+                      "bytes": quant_bytes},
+        "offline_pack_ms": pack_ms,
+        "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak, "unit": "TFLOP/s",
+                     "frac": gemm_tflops / fp8_peak, "traffic": recorded_traffic("w4ax_gemm"),
+                     "kernel": "w4ax_gemm_kernel",
+                     "peak_source": f"{peaks['source']} bf16 burst x 2 (nominal fp8/bf16 dense ratio)"},
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
