@@ -42,6 +42,7 @@ SIGNATURES = {
     "w4_unpack_weights": (_I32, [_P, _P, _I64, _P, _P]),
     "w4ax_gemm_workspace_bytes": (_SZ, [_P, _I64, _I64]),
     "w4ax_gemm": (_I32, [_P, _P, _P, _P, _P, _I64, _I64, _P, _I64, _P, _SZ, _P]),
+    "w4ax_gemm_noalloc": (_I32, [_P, _P, _P, _P, _P, _I64, _I64, _P, _I64, _P]),
     "w4ax_gemm_partials": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P]),
     "fmpq_device_status": (_I32, [_P, ctypes.POINTER(_I32), _I32]),
     "fmpq_status_string": (ctypes.c_char_p, [_I32]),
@@ -207,6 +208,19 @@ def w4ax_gemm(layout: Layout, A_packed, a_scales, W_packed, w_scales, M: int, N:
     _check("w4ax_gemm", layout._lib.w4ax_gemm(layout.handle, _ptr(A_packed), _ptr(a_scales), _ptr(W_packed),
                                                 _ptr(w_scales), M, N, _ptr(Y), Y.stride(0), _ptr(workspace),
                                                 ws_bytes, _stream(stream)))
+    return Y
+
+
+def w4ax_gemm_noalloc(layout: Layout, A_packed, a_scales, W_packed, w_scales, M: int, N: int, Y=None,
+                      stream=None):
+    """w4ax_gemm without a workspace argument: for callers that cannot allocate device memory,
+    the library's own fixed device array serves as the split-K workspace."""
+    import torch
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float16, device=A_packed.device)
+    _check("w4ax_gemm_noalloc", layout._lib.w4ax_gemm_noalloc(layout.handle, _ptr(A_packed), _ptr(a_scales),
+                                                                _ptr(W_packed), _ptr(w_scales), M, N, _ptr(Y),
+                                                                Y.stride(0), _stream(stream)))
     return Y
 
 

@@ -137,6 +137,24 @@ FMPQ_API fmpq_status w4ax_gemm(const fmpq_layout* layout, const void* A_packed, 
                       const void* W_packed, const void* w_scales, int64_t M, int64_t N,
                       void* Y, int64_t ldy, void* workspace, size_t workspace_bytes, void* stream);
 
+/* The same GEMM for callers that cannot allocate device memory (a pool that owns the whole
+ * device, a serving path that must not allocate mid-flight, a host without access to the
+ * allocator). It takes no workspace: when the shape needs one (w4ax_gemm_workspace_bytes > 0),
+ * the library uses its own fixed device array of 20 MiB of partial tiles + 64 KiB of
+ * counters, which every GPU that loads the library holds until exit. The paper has no
+ * counterpart; this is an interface convenience.
+ *   - Arguments and results are those of w4ax_gemm (no workspace arguments).
+ *   - The first call on a device looks up the array's device address and zeroes its counters
+ *     (synchronously); make that first call before any stream capture.
+ *   - Shapes whose workspace would exceed the array return FMPQ_ERR_WORKSPACE.
+ *   - All calls share the array: calls that overlap on the GPU (e.g. on two streams) race
+ *     and must be serialized by the caller.
+ *   - Allocates nothing. */
+FMPQ_API fmpq_status w4ax_gemm_noalloc(const fmpq_layout* layout, const void* A_packed,
+                                       const void* a_scales, const void* W_packed,
+                                       const void* w_scales, int64_t M, int64_t N, void* Y,
+                                       int64_t ldy, void* stream);
+
 /* Debug/test: the exact per-block integer partial sums P computed by the GEMM's own
  * tensor-core path, for the window [m0, m0+mcount) x [n0, n0+ncount):
  *   P int32 [mcount][ncount][K/128]. */

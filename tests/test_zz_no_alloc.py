@@ -1,0 +1,41 @@
+"""GPU test of w4ax_gemm_noalloc, the GEMM entry point for callers that cannot allocate
+device memory (the library supplies the split-K workspace from its own fixed device array).
+Its output must match w4ax_gemm's within the tolerance the parity tests use, on two calls in
+a row (the second call reuses the array the first one left behind). This file is collected
+last so a run that stops at the first failure has already run every other test."""
+import numpy as np
+import pytest
+
+from bit_quantized_gemm_fmpq_gb300 import workloads as wl
+from tests.gpu_helpers import Y_TOL, to_dev, y_error
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fmpq_mod():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_quantized_gemm_fmpq_gb300 import build, fmpq
+    build.build()
+    fmpq.load_library()
+    return fmpq
+
+
+@pytest.mark.parametrize("M,N,K,n8", [
+    (16, 512, 2048, 2),    # few output tiles: split-K, the workspace comes from the fixed array
+    (1, 1024, 4096, 3),    # one token, split-K
+    (300, 784, 1024, 2),   # enough tiles: no workspace needed
+])
+def test_noalloc_matches_gemm(fmpq_mod, M, N, K, n8):
+    w = wl.synthetic(M, N, K, n8=n8, seed=M * 7 + N + K)
+    layout = fmpq_mod.Layout(w.K, w.perm, w.mask)
+    A, sx = fmpq_mod.fmpq_quantize(layout, to_dev(w.X))
+    Wp, sw = fmpq_mod.w4_pack_weights(layout, to_dev(w.W))
+    ref = fmpq_mod.w4ax_gemm(layout, A, sx, Wp, sw, M, N).cpu().numpy().astype(np.float64)
+    for _ in range(2):
+        Y = fmpq_mod.w4ax_gemm_noalloc(layout, A, sx, Wp, sw, M, N).cpu().numpy()
+        assert y_error(Y, ref) <= Y_TOL
+    assert fmpq_mod.fmpq_device_status(layout) == 0
+    layout.close()
