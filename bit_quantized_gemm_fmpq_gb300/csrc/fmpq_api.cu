@@ -40,14 +40,15 @@ fmpq_status fmpq_layout_create(int32_t K, const int32_t* perm_host, const uint8_
         seen[c] = 1;
         perm16[j] = static_cast<uint16_t>(c);
     }
-    std::vector<int32_t> boff(static_cast<size_t>(nb));
+    // plane offsets: an INT4 block has one code plane, an INT8 block two
+    std::vector<int32_t> poff(static_cast<size_t>(nb));
     int n8 = 0;
-    int32_t off = 0;
+    int32_t planes = 0;
     for (int b = 0; b < nb; ++b) {
         const uint8_t m = outlier_block_mask_host[b];
         if (m > 1) return FMPQ_ERR_INVALID_ARG;
-        boff[b] = off;
-        off += m ? 128 : 64;
+        poff[b] = planes;
+        planes += m ? 2 : 1;
         n8 += m;
     }
     int dev = -1, major = 0, minor = 0, sms = 0;
@@ -65,14 +66,15 @@ fmpq_status fmpq_layout_create(int32_t K, const int32_t* perm_host, const uint8_
     L->n8 = n8;
     L->device = dev;
     L->num_sms = sms;
-    L->row_bytes = off;
+    L->planes = planes;
+    L->row_bytes = static_cast<int64_t>(planes) * FMPQ_BLOCK;
     bool ok = cudaMalloc(&L->d_perm16, sizeof(uint16_t) * K) == cudaSuccess &&
               cudaMalloc(&L->d_mask, static_cast<size_t>(nb)) == cudaSuccess &&
-              cudaMalloc(&L->d_boff, sizeof(int32_t) * nb) == cudaSuccess &&
+              cudaMalloc(&L->d_poff, sizeof(int32_t) * nb) == cudaSuccess &&
               cudaMalloc(&L->d_status, sizeof(int32_t)) == cudaSuccess;
     ok = ok && cudaMemcpy(L->d_perm16, perm16.data(), sizeof(uint16_t) * K, cudaMemcpyHostToDevice) == cudaSuccess &&
          cudaMemcpy(L->d_mask, outlier_block_mask_host, static_cast<size_t>(nb), cudaMemcpyHostToDevice) == cudaSuccess &&
-         cudaMemcpy(L->d_boff, boff.data(), sizeof(int32_t) * nb, cudaMemcpyHostToDevice) == cudaSuccess &&
+         cudaMemcpy(L->d_poff, poff.data(), sizeof(int32_t) * nb, cudaMemcpyHostToDevice) == cudaSuccess &&
          cudaMemset(L->d_status, 0, sizeof(int32_t)) == cudaSuccess;
     if (!ok) {
         fmpq_layout_destroy(L);
@@ -90,7 +92,7 @@ void fmpq_layout_destroy(fmpq_layout* L) {
     cudaDeviceSynchronize();
     cudaFree(L->d_perm16);
     cudaFree(L->d_mask);
-    cudaFree(L->d_boff);
+    cudaFree(L->d_poff);
     cudaFree(L->d_status);
     if (switched) cudaSetDevice(prev);
     delete L;

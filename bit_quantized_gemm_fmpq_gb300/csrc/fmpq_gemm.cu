@@ -6,24 +6,24 @@
 // conversion; QUIK explainer, "kernel fusion": dequantization in the GEMM epilogue).
 //
 // GB300 mapping (sm_103a has no integer tcgen05 MMA):
-//   * Codes become E4M3 tensor-core operands exactly: the byte s0000mmm is the E4M3 value
-//     (-1)^s * m * 2^-9 for m <= 15 (subnormal/normal boundary is linear there). The packed
-//     sign-magnitude layouts give these bytes with a mask (and a rotate for the upper four
-//     codes of each INT4 word) -- the restructured storage format that makes 4-bit ->
+//   * Codes are exact E4M3 tensor-core operands. The activation quantizer already writes
+//     them that way (one byte per code, value part * 2^-9, rows pre-swizzled), so a
+//     128-row activation tile is one bulk copy straight into the operand ring. An INT8
+//     block has two planes (|q| mod 16 and the rest) that accumulate into the same TMEM
+//     tile, so every block ends in one FP32 tile P * 2^-18 (exact: |P| < 2^17).
+//   * INT4 weights stay 4-bit in HBM: converter warps turn each packed word into 8
+//     operand bytes with a mask and a rotate (the sign-magnitude byte s0000mmm is the E4M3
+//     value (-1)^s * m * 2^-9) -- the restructured storage format that makes 4-bit ->
 //     8-bit conversion a couple of instructions (COMET news article, section 3).
-//   * An INT8 code |a| = 16h + l (h <= 7, l <= 15) is split into two "virtual blocks"
-//     (l and h, both exact in this encoding); the h part's row scale carries the factor 16.
-//   * tcgen05.mma kind::f8f6f4 (M=128, N=256, K=32) accumulates each virtual block into a
-//     fresh FP32 TMEM tile; products are multiples of 2^-18 with |P| < 2^17, so the FP32
-//     accumulator holds P * 2^-18 exactly.
-//   * Per virtual block the epilogue warps read the tile (tcgen05.ld) and accumulate
-//     acc += (w_scale[n] * a_scale[m] * 2^18) * D in FP32 registers (packed f32x2 math);
-//     TMEM is double-buffered so the MMA of the next block overlaps this epilogue.
+//   * tcgen05.mma kind::f8f6f4 (M=128, N=256, K=32) with the accumulator in TMEM,
+//     double-buffered so the MMA of the next block overlaps the epilogue of this one.
+//   * Per block the epilogue warps read the tile (tcgen05.ld) and accumulate
+//     acc += (w_scale[n] * a_scale[m] * 2^18) * D in FP32 registers (packed f32x2 math).
 //
 // Warp roles (512 threads, one CTA per SM, persistent over tiles):
-//   warp 0       TMA producer: packed A tile and packed W tile per block (bulk copies)
+//   warp 0       TMA producer: activation code planes and the packed weight tile per block
 //   warp 1       tcgen05 MMA issuer (one thread) + TMEM owner
-//   warps 2-7    converters: packed codes -> 128B-swizzled K-major E4M3 operand tiles
+//   warps 2-7    converters: packed weight codes -> 128B-swizzled K-major E4M3 tile
 //   warps 8-15   epilogue: per-block FP32 scale-and-sum, fp16 output (or split-K partials)
 #include <cuda_fp16.h>
 
@@ -34,21 +34,21 @@ namespace fmpq {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kPkStages = 3;  // packed-code ring (per block)
-constexpr int kCvStages = 2;  // operand ring (per virtual block)
+constexpr int kStages = 3;    // per-block stage: activation planes + packed weights
+constexpr int kCvStages = 2;  // converted weight tiles
 constexpr int kConvWarps = 6;
+constexpr int kConvThreads = kConvWarps * 32;
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr uint32_t kTmemCols = 512;  // two 128 x 256 FP32 accumulators
 constexpr uint32_t kIdesc = dev::idesc_e4m3_f32(128, 256);
 
 struct __align__(1024) Smem {
-    uint8_t cvA[kCvStages][128 * 128];  // E4M3 operand A (tokens x 128 K), swizzled
-    uint8_t cvB[kCvStages][256 * 128];  // E4M3 operand B (weights x 128 K), swizzled
-    uint8_t pkA[kPkStages][128 * 128];  // packed activation codes (64 or 128 B per row)
-    uint8_t pkW[kPkStages][256 * 64];   // packed weight codes
-    float sw[2][256];                   // per-block weight scales (fp32) for the epilogue
-    uint64_t pk_full[kPkStages], pk_empty[kPkStages];
+    uint8_t opA[kStages][2][128 * 128];  // activation code planes (operand-ready, swizzled)
+    uint8_t cvB[kCvStages][256 * 128];   // E4M3 weight operand (256 rows x 128 K), swizzled
+    uint8_t pkW[kStages][256 * 64];      // packed weight codes
+    float sw[2][256];                    // per-block weight scales (fp32) for the epilogue
+    uint64_t st_full[kStages], st_empty[kStages];
     uint64_t cv_full[kCvStages], cv_empty[kCvStages];
     uint64_t acc_full[2], acc_empty[2];
     uint64_t mma_done;
@@ -66,7 +66,7 @@ struct Params {
     int64_t ldy;
     int M, N, nb;
     const uint8_t* mask;
-    const int32_t* boff;
+    const int32_t* poff;   // first code plane of each block
     int32_t* status;
     // tiles: the kernel covers m-tiles [mt0, mt0 + mtiles) x n-tiles [nt0, nt0 + ntiles)
     int mt0, mtiles, nt0, ntiles;
@@ -100,27 +100,27 @@ __device__ __forceinline__ Unit unit_of(const Params& p, int u) {
 // ---------------------------------------------------------------- TMA producer (warp 0)
 __device__ __forceinline__ void producer_role(const Params& p, Smem& s, int lane, volatile int* abort_flag) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
-    // ======================= TMA producer
     if (lane == 0) {
         uint32_t it = 0;
         bool ok = true;
+        const int64_t plane_bytes = static_cast<int64_t>(p.M) * kBlock;
         for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
             const Unit t = unit_of(p, u);
             const int m0 = t.mt * kTileM;
-            const int rows = min(kTileM, p.M - m0);
+            const uint32_t abytes = static_cast<uint32_t>(min(kTileM, p.M - m0)) * kBlock;
             for (int b = t.b0; b < t.b1; ++b, ++it) {
-                const int st = it % kPkStages;
-                if (!dev::mbar_wait(&s.pk_empty[st], ((it / kPkStages) & 1) ^ 1, abort_flag)) {
+                const int st = it % kStages;
+                if (!dev::mbar_wait(&s.st_empty[st], ((it / kStages) & 1) ^ 1, abort_flag)) {
                     ok = false;
                     break;
                 }
-                const int wb = p.mask[b] ? 128 : 64;
-                const uint32_t abytes = static_cast<uint32_t>(rows * wb);
-                dev::mbar_arrive_expect_tx(&s.pk_full[st], abytes + 256 * 64);
-                dev::bulk_g2s(s.pkA[st], p.A + static_cast<int64_t>(p.boff[b]) * p.M + static_cast<int64_t>(m0) * wb,
-                              abytes, &s.pk_full[st]);
+                const int planes = p.mask[b] ? 2 : 1;
+                dev::mbar_arrive_expect_tx(&s.st_full[st], abytes * planes + 256 * 64);
+                const uint8_t* a0 = p.A + static_cast<int64_t>(p.poff[b]) * plane_bytes + static_cast<int64_t>(m0) * kBlock;
+                dev::bulk_g2s(s.opA[st][0], a0, abytes, &s.st_full[st]);
+                if (planes == 2) dev::bulk_g2s(s.opA[st][1], a0 + plane_bytes, abytes, &s.st_full[st]);
                 dev::bulk_g2s(s.pkW[st], p.W + (static_cast<int64_t>(t.nt) * p.nb + b) * (256 * 64), 256 * 64,
-                              &s.pk_full[st]);
+                              &s.st_full[st]);
             }
         }
         if (!ok) {
@@ -128,10 +128,10 @@ __device__ __forceinline__ void producer_role(const Params& p, Smem& s, int lane
             dev::report(p.status, dev::kStatusTimeout);
         }
         // drain copies in flight
-        for (int st = 0; st < kPkStages; ++st) {
+        for (int st = 0; st < kStages; ++st) {
             if (it <= static_cast<uint32_t>(st)) break;
-            const uint32_t last = st + ((it - 1 - st) / kPkStages) * kPkStages;
-            dev::mbar_wait(&s.pk_full[st], (last / kPkStages) & 1, nullptr);
+            const uint32_t last = st + ((it - 1 - st) / kStages) * kStages;
+            dev::mbar_wait(&s.st_full[st], (last / kStages) & 1, nullptr);
         }
     }
 }
@@ -139,31 +139,34 @@ __device__ __forceinline__ void producer_role(const Params& p, Smem& s, int lane
 // ---------------------------------------------------------------- MMA issuer (warp 1)
 __device__ __forceinline__ void mma_role(const Params& p, Smem& s, int lane, uint32_t tmem, volatile int* abort_flag) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
-    // ======================= MMA issuer
     if (lane == 0) {
-        uint32_t v = 0;
+        uint32_t it = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
             const Unit t = unit_of(p, u);
-            for (int b = t.b0; ok && b < t.b1; ++b) {
-                const int nvb = p.mask[b] ? 2 : 1;
-                for (int vb = 0; vb < nvb; ++vb, ++v) {
-                    const int cs = v % kCvStages;
-                    const int ab = v & 1;
-                    if (!dev::mbar_wait(&s.cv_full[cs], (v / kCvStages) & 1, abort_flag) ||
-                        !dev::mbar_wait(&s.acc_empty[ab], ((v >> 1) & 1) ^ 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    dev::tc_fence_after();
-                    const uint64_t ad = dev::sdesc_k_sw128(dev::smem_u32(s.cvA[cs]));
-                    const uint64_t bd = dev::sdesc_k_sw128(dev::smem_u32(s.cvB[cs]));
-                    const uint32_t d = tmem + static_cast<uint32_t>(ab) * 256u;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) dev::mma_e4m3(d, ad + 2 * k, bd + 2 * k, kIdesc, k > 0 ? 1u : 0u);
-                    dev::mma_commit(&s.cv_empty[cs]);
-                    dev::mma_commit(&s.acc_full[ab]);
+            for (int b = t.b0; b < t.b1; ++b, ++it) {
+                const int st = it % kStages;
+                const int cs = it % kCvStages;
+                const int ab = it & 1;
+                if (!dev::mbar_wait(&s.st_full[st], (it / kStages) & 1, abort_flag) ||
+                    !dev::mbar_wait(&s.cv_full[cs], (it / kCvStages) & 1, abort_flag) ||
+                    !dev::mbar_wait(&s.acc_empty[ab], ((it >> 1) & 1) ^ 1, abort_flag)) {
+                    ok = false;
+                    break;
                 }
+                dev::tc_fence_after();
+                const uint64_t bd = dev::sdesc_k_sw128(dev::smem_u32(s.cvB[cs]));
+                const uint32_t d = tmem + static_cast<uint32_t>(ab) * 256u;
+                const int planes = p.mask[b] ? 2 : 1;
+                for (int pl = 0; pl < planes; ++pl) {
+                    const uint64_t ad = dev::sdesc_k_sw128(dev::smem_u32(s.opA[st][pl]));
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        dev::mma_e4m3(d, ad + 2 * k, bd + 2 * k, kIdesc, (pl > 0 || k > 0) ? 1u : 0u);
+                }
+                dev::mma_commit(&s.st_empty[st]);
+                dev::mma_commit(&s.cv_empty[cs]);
+                dev::mma_commit(&s.acc_full[ab]);
             }
         }
         if (!ok) {
@@ -177,65 +180,49 @@ __device__ __forceinline__ void mma_role(const Params& p, Smem& s, int lane, uin
 }
 
 // ---------------------------------------------------------------- converters (warps 2-7)
+// The weight tile is 256 rows x 8 chunks (8 packed bytes in, 16 operand bytes out). Thread
+// ct converts items ct + 192k: item i is row i/8, chunk i%8. Since 192 = 24 rows, the
+// chunk and the row's swizzle phase (row mod 8) are the same for every k, so each item's
+// source and destination are the thread's base offsets plus constants.
 __device__ __forceinline__ void converter_role(const Params& p, Smem& s, int warp, int lane, volatile int* abort_flag) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
-    // ======================= converters: packed codes -> swizzled E4M3 operand tiles
     const int ct = (warp - 2) * 32 + lane;
-    constexpr int kCt = kConvWarps * 32;
-    uint32_t it = 0, v = 0;
+    const int r0 = ct >> 3, c = ct & 7;
+    const uint32_t src0 = static_cast<uint32_t>(r0 * 64 + c * 8);
+    const uint32_t dst0 = static_cast<uint32_t>(r0 * 128 + ((c ^ (r0 & 7)) << 4));
+    constexpr int kFull = (256 * 8) / kConvThreads;                      // 10 items for every thread
+    const bool extra = ct + kFull * kConvThreads < 256 * 8;              // an 11th for the first 128
+    uint32_t it = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
         const Unit t = unit_of(p, u);
-        for (int b = t.b0; ok && b < t.b1; ++b, ++it) {
-            const int st = it % kPkStages;
-            if (lane == 0) ok = dev::mbar_wait(&s.pk_full[st], (it / kPkStages) & 1, abort_flag);
+        for (int b = t.b0; b < t.b1; ++b, ++it) {
+            const int st = it % kStages;
+            const int cs = it % kCvStages;
+            if (lane == 0)
+                ok = dev::mbar_wait(&s.st_full[st], (it / kStages) & 1, abort_flag) &&
+                     dev::mbar_wait(&s.cv_empty[cs], ((it / kCvStages) & 1) ^ 1, abort_flag);
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             if (!ok) break;
-            const bool is8 = p.mask[b] != 0;
-            const int nvb = is8 ? 2 : 1;
-            for (int vb = 0; vb < nvb; ++vb, ++v) {
-                const int cs = v % kCvStages;
-                if (lane == 0) ok = dev::mbar_wait(&s.cv_empty[cs], ((v / kCvStages) & 1) ^ 1, abort_flag);
-                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-                if (!ok) break;
-                // A tile: 128 rows x 8 chunks of 16 operand bytes
-                if (!is8) {
-                    for (int i = ct; i < 128 * 8; i += kCt) {
-                        const int r = i >> 3, c = i & 7;
-                        const uint2 w = *reinterpret_cast<const uint2*>(s.pkA[st] + r * 64 + c * 8);
-                        *reinterpret_cast<uint4*>(s.cvA[cs] + r * 128 + ((c ^ (r & 7)) << 4)) =
-                            make_uint4(lo4(w.x), hi4(w.x), lo4(w.y), hi4(w.y));
-                    }
-                } else {
-                    for (int i = ct; i < 128 * 8; i += kCt) {
-                        const int r = i >> 3, c = i & 7;
-                        const uint4 w = *reinterpret_cast<const uint4*>(s.pkA[st] + r * 128 + c * 16);
-                        uint4 o;
-                        if (vb == 0) {  // l = |a| & 15 with the sign
-                            o = make_uint4(w.x & 0x8F8F8F8Fu, w.y & 0x8F8F8F8Fu, w.z & 0x8F8F8F8Fu,
-                                           w.w & 0x8F8F8F8Fu);
-                        } else {        // h = |a| >> 4 with the sign
-                            o = make_uint4(((w.x >> 4) & 0x07070707u) | (w.x & 0x80808080u),
-                                           ((w.y >> 4) & 0x07070707u) | (w.y & 0x80808080u),
-                                           ((w.z >> 4) & 0x07070707u) | (w.z & 0x80808080u),
-                                           ((w.w >> 4) & 0x07070707u) | (w.w & 0x80808080u));
-                        }
-                        *reinterpret_cast<uint4*>(s.cvA[cs] + r * 128 + ((c ^ (r & 7)) << 4)) = o;
-                    }
-                }
-                // B tile: 256 weight rows
-                for (int i = ct; i < 256 * 8; i += kCt) {
-                    const int r = i >> 3, c = i & 7;
-                    const uint2 w = *reinterpret_cast<const uint2*>(s.pkW[st] + r * 64 + c * 8);
-                    *reinterpret_cast<uint4*>(s.cvB[cs] + r * 128 + ((c ^ (r & 7)) << 4)) =
-                        make_uint4(lo4(w.x), hi4(w.x), lo4(w.y), hi4(w.y));
-                }
-                dev::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) dev::mbar_arrive(&s.cv_full[cs]);
+            const uint8_t* src = s.pkW[st] + src0;
+            uint8_t* dst = s.cvB[cs] + dst0;
+#pragma unroll
+            for (int k0 = 0; k0 < kFull; k0 += 5) {
+                uint2 w[5];
+#pragma unroll
+                for (int k = 0; k < 5; ++k) w[k] = *reinterpret_cast<const uint2*>(src + (k0 + k) * 24 * 64);
+#pragma unroll
+                for (int k = 0; k < 5; ++k)
+                    *reinterpret_cast<uint4*>(dst + (k0 + k) * 24 * 128) =
+                        make_uint4(lo4(w[k].x), hi4(w[k].x), lo4(w[k].y), hi4(w[k].y));
             }
+            if (extra) {
+                const uint2 w = *reinterpret_cast<const uint2*>(src + kFull * 24 * 64);
+                *reinterpret_cast<uint4*>(dst + kFull * 24 * 128) = make_uint4(lo4(w.x), hi4(w.x), lo4(w.y), hi4(w.y));
+            }
+            dev::fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) dev::mbar_arrive(&s.pk_empty[st]);
+            if (lane == 0) dev::mbar_arrive(&s.cv_full[cs]);
         }
     }
     if (!ok && lane == 0) {
@@ -268,7 +255,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, int warp
         const int ncol = n0 + et;
         float sw_next = (t.b0 < t.b1 && ncol < p.N) ? __half2float(__ushort_as_half(p.w_scales[static_cast<int64_t>(t.b0) * p.N + ncol])) : 0.f;
         float sx_next = (t.b0 < t.b1 && row_ok) ? __half2float(__ushort_as_half(p.a_scales[static_cast<int64_t>(t.b0) * p.M + row])) : 0.f;
-        for (int b = t.b0; b < t.b1; ++b, ++bstep) {
+        for (int b = t.b0; b < t.b1; ++b, ++bstep, ++v) {
             const float sw_cur = sw_next, sx_cur = sx_next;
             if (b + 1 < t.b1) {
                 sw_next = (ncol < p.N) ? __half2float(__ushort_as_half(p.w_scales[static_cast<int64_t>(b + 1) * p.N + ncol])) : 0.f;
@@ -277,62 +264,56 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, int warp
             float* swb = s.sw[bstep & 1];
             swb[et] = sw_cur;
             dev::named_bar_sync(1, kEpiThreads);
-            const bool is8 = p.mask[b] != 0;
-            const int nvb = is8 ? 2 : 1;
-            for (int vb = 0; vb < nvb; ++vb, ++v) {
-                const int ab = v & 1;
-                if (ok) {
-                    if (lane == 0) ok = dev::mbar_wait(&s.acc_full[ab], (v >> 1) & 1, abort_flag);
-                    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-                }
-                if (ok) {
-                    dev::tc_fence_after();
-                    const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + ab * 256u + h * 128u;
-                    if constexpr (!kPartials) {
-                        // 2^18 undoes the operand encoding; the h part of an INT8 code is x16
-                        const float sxp = sx_cur * ((is8 && vb == 1) ? 4194304.0f : 262144.0f);
-                        const float2 sx2 = make_float2(sxp, sxp);
+            const int ab = v & 1;
+            if (ok) {
+                if (lane == 0) ok = dev::mbar_wait(&s.acc_full[ab], (v >> 1) & 1, abort_flag);
+                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            }
+            if (ok) {
+                dev::tc_fence_after();
+                const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + ab * 256u + h * 128u;
+                if constexpr (!kPartials) {
+                    // 2^18 undoes the operand encoding (both operands carry 2^-9)
+                    const float sxp = sx_cur * 262144.0f;
+                    const float2 sx2 = make_float2(sxp, sxp);
 #pragma unroll
-                        for (int chunk = 0; chunk < 4; ++chunk) {
-                            uint32_t d[32];
-                            dev::tmem_ld32(taddr + chunk * 32, d);
-                            dev::tmem_ld_wait();
-                            const float4* sw4 = reinterpret_cast<const float4*>(swb + h * 128 + chunk * 32);
+                    for (int chunk = 0; chunk < 4; ++chunk) {
+                        uint32_t d[32];
+                        dev::tmem_ld32(taddr + chunk * 32, d);
+                        dev::tmem_ld_wait();
+                        const float4* sw4 = reinterpret_cast<const float4*>(swb + h * 128 + chunk * 32);
 #pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                const float4 w4 = sw4[j];
-                                const float2 c01 = dev::fmul2(make_float2(w4.x, w4.y), sx2);
-                                const float2 c23 = dev::fmul2(make_float2(w4.z, w4.w), sx2);
-                                float2& a01 = acc[chunk * 16 + 2 * j];
-                                float2& a23 = acc[chunk * 16 + 2 * j + 1];
-                                a01 = dev::ffma2(make_float2(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1])), c01, a01);
-                                a23 = dev::ffma2(make_float2(__uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3])), c23, a23);
-                            }
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 w4 = sw4[j];
+                            const float2 c01 = dev::fmul2(make_float2(w4.x, w4.y), sx2);
+                            const float2 c23 = dev::fmul2(make_float2(w4.z, w4.w), sx2);
+                            float2& a01 = acc[chunk * 16 + 2 * j];
+                            float2& a23 = acc[chunk * 16 + 2 * j + 1];
+                            a01 = dev::ffma2(make_float2(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1])), c01, a01);
+                            a23 = dev::ffma2(make_float2(__uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3])), c23, a23);
                         }
-                    } else {
-                        // export exact partial sums of the requested window
+                    }
+                } else {
+                    // export exact partial sums of the requested window
 #pragma unroll 1
-                        for (int chunk = 0; chunk < 4; ++chunk) {
-                            uint32_t d[32];
-                            dev::tmem_ld32(taddr + chunk * 32, d);
-                            dev::tmem_ld_wait();
-                            if (row_ok && row >= p.pm0 && row < p.pm0 + p.pmcount) {
-                                for (int j = 0; j < 32; ++j) {
-                                    const int n = n0 + h * 128 + chunk * 32 + j;
-                                    if (n < p.pn0 || n >= p.pn0 + p.pncount || n >= p.N) continue;
-                                    const int pv = __float2int_rn(__uint_as_float(d[j]) * 262144.0f);
-                                    int32_t* dst = p.P + (static_cast<int64_t>(row - p.pm0) * p.pncount + (n - p.pn0)) * p.nb + b;
-                                    if (is8 && vb == 1) *dst += 16 * pv;
-                                    else *dst = pv;
-                                }
+                    for (int chunk = 0; chunk < 4; ++chunk) {
+                        uint32_t d[32];
+                        dev::tmem_ld32(taddr + chunk * 32, d);
+                        dev::tmem_ld_wait();
+                        if (row_ok && row >= p.pm0 && row < p.pm0 + p.pmcount) {
+                            for (int j = 0; j < 32; ++j) {
+                                const int n = n0 + h * 128 + chunk * 32 + j;
+                                if (n < p.pn0 || n >= p.pn0 + p.pncount || n >= p.N) continue;
+                                p.P[(static_cast<int64_t>(row - p.pm0) * p.pncount + (n - p.pn0)) * p.nb + b] =
+                                    __float2int_rn(__uint_as_float(d[j]) * 262144.0f);
                             }
                         }
                     }
-                    dev::tc_fence_before();
                 }
-                __syncwarp();
-                if (lane == 0 && ok) dev::mbar_arrive(&s.acc_empty[ab]);
+                dev::tc_fence_before();
             }
+            __syncwarp();
+            if (lane == 0 && ok) dev::mbar_arrive(&s.acc_empty[ab]);
         }
         if constexpr (!kPartials) {
             const int cbase = n0 + h * 128;
@@ -430,9 +411,9 @@ __global__ void __launch_bounds__(kThreads, 1) w4ax_gemm_kernel(const Params p) 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kPkStages; ++i) {
-            dev::mbar_init(&s.pk_full[i], 1);
-            dev::mbar_init(&s.pk_empty[i], kConvWarps);
+        for (int i = 0; i < kStages; ++i) {
+            dev::mbar_init(&s.st_full[i], 1);
+            dev::mbar_init(&s.st_empty[i], 1);
         }
         for (int i = 0; i < kCvStages; ++i) {
             dev::mbar_init(&s.cv_full[i], kConvWarps);
@@ -516,7 +497,7 @@ cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& a, cudaStream_t st
     p.N = static_cast<int>(a.N);
     p.nb = L.nb;
     p.mask = L.d_mask;
-    p.boff = L.d_boff;
+    p.poff = L.d_poff;
     p.status = L.d_status;
     const bool partials = a.P != nullptr;
     if (partials) {

@@ -13,9 +13,10 @@ struct fmpq_layout {
     int num_sms = 0;
     uint16_t* d_perm16 = nullptr;  // [K] gather permutation (K <= 65536)
     uint8_t* d_mask = nullptr;     // [nb] 1 = INT8 block
-    int32_t* d_boff = nullptr;     // [nb] packed-A block offset in bytes per row
+    int32_t* d_poff = nullptr;     // [nb] first code plane of each block (planes before it)
     int32_t* d_status = nullptr;   // device status word
-    int64_t row_bytes = 0;         // packed-A bytes per token: 64*n4 + 128*n8
+    int32_t planes = 0;            // code planes: n4 + 2*n8
+    int64_t row_bytes = 0;         // packed-A bytes per token: 128 * planes
 };
 
 namespace fmpq {

@@ -4,12 +4,12 @@
 // "kernel fusion": one kernel reads the input, computes the statistics, quantizes and
 // splits in a single pass), per-(token, 128-channel block) absmax, fp16 scale, exact
 // round-half-even quantization to INT8 (outlier blocks) or INT4 (the rest; COMET news
-// article, section 1), and packing into the sign-magnitude layout documented in fmpq.h.
+// article, section 1), and encoding into the operand-ready code planes documented in fmpq.h.
 //
 // HBM-bound design: persistent CTAs (one per SM) stream whole rows into shared memory with
-// TMA bulk copies (a dedicated producer warp, double/triple-buffered), keep the permutation
-// resident in shared memory as 16-bit indices, gather from shared memory, and write the
-// packed codes with coalesced stores.
+// TMA bulk copies (a dedicated producer warp, several stages), keep each lane's gather
+// offsets in registers, gather from shared memory, and write the code planes with
+// coalesced stores (each half-warp writes one 128-byte plane row).
 #include <cuda_fp16.h>
 
 #include "fmpq_device.cuh"
@@ -18,13 +18,9 @@
 namespace fmpq {
 namespace {
 
-constexpr int kQuantWarps = 8;                       // compute warps; +1 producer warp
-constexpr int kQuantThreads = (kQuantWarps + 1) * 32;
-constexpr int kQuantSmemBudget = 200 * 1024;
-
 // ---------------------------------------------------------------------------------
-// Per-lane quantization of 4 values of one block (the warp covers the block's 128
-// channels, 4 per lane). Returns the 4 sign-magnitude bytes (byte i = element i) and,
+// Weight quantization (offline packing): per-lane quantization of 4 values of one block
+// (the warp covers the block's 128 channels, 4 per lane). Returns the 4 sign-magnitude bytes (byte i = element i) and,
 // through *scale_bits, the block's fp16 scale.
 //
 // Scale: s = fp16_rne(fp32(absmax) / qmax) with IEEE division.
@@ -94,6 +90,25 @@ __device__ __forceinline__ uint32_t pack_int4_pair(uint32_t v, int lane) {
     return mine | __shfl_xor_sync(0xFFFFFFFFu, mine, 1);
 }
 
+// ---------------------------------------------------------------------------------
+// Activation quantizer.
+//
+// A warp quantizes two blocks of one token at a time: lanes 0-15 one block, lanes 16-31
+// another, 8 channels per lane. Warp w of the 16 compute warps owns blocks w, w+16,
+// w+32, ... for every token, so each lane keeps the gather offsets of its channels in
+// registers for the whole kernel. Rows of X are streamed into a shared-memory ring by a
+// producer warp (bulk copies); the gather reads them from there.
+//
+// Output: operand-ready code planes (layout in fmpq.h). A code's byte is sign<<7 | the
+// E4M3 encoding of part * 2^-9: INT4 part = |q|; INT8 low part = |q| & 15 (the same bits),
+// INT8 high part = |q| & 0x70, whose E4M3 encoding is looked up in an 8-entry table.
+// The sign bit is the sign bit of the fp16 input.
+// ---------------------------------------------------------------------------------
+constexpr int kQWarps = 16;                        // compute warps; +1 producer warp
+constexpr int kQThreads = (kQWarps + 1) * 32;
+constexpr int kQMaxIters = 8;                      // block pairs per warp (nb <= 256)
+constexpr int kQSmemBudget = 200 * 1024;
+
 struct QuantParams {
     const uint16_t* X;
     int64_t ldx;
@@ -101,43 +116,60 @@ struct QuantParams {
     int K, nb, stages;
     const uint16_t* perm;
     const uint8_t* mask;
-    const int32_t* boff;
+    const int32_t* poff;
     uint8_t* A;
     uint16_t* scales;
     int32_t* status;
 };
 
-__global__ void __launch_bounds__(kQuantThreads, 1) quantize_kernel(QuantParams p) {
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// Byte 0 of four floats -> one word (the magnitudes sit in the low mantissa byte of
+// x + 1.5 * 2^23).
+__device__ __forceinline__ uint32_t low_bytes4(float a, float b, float c, float d) {
+    const uint32_t ab = __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x0040);
+    const uint32_t cd = __byte_perm(__float_as_uint(c), __float_as_uint(d), 0x0040);
+    return __byte_perm(ab, cd, 0x5410);
+}
+
+// INT8 high plane from the sign-magnitude code bytes w: byte = sign | E4M3(16h * 2^-9),
+// h = bits 4-6 of the magnitude. E4M3 of h * 2^-5 for h = 0..7:
+// 0x00 0x10 0x18 0x1C 0x20 0x22 0x24 0x26.
+__device__ __forceinline__ uint32_t high_plane(uint32_t w) {
+    const uint32_t hw = (w >> 4) & 0x07070707u;           // h per byte
+    const uint32_t nib = hw | (hw >> 4);                   // nibbles h0 h1 . h2 ...
+    const uint32_t sel = __byte_perm(nib, 0u, 0x0020);     // selector nibbles h0 h1 h2 h3
+    return __byte_perm(0x1C181000u, 0x26242220u, sel) | (w & 0x80808080u);
+}
+
+__global__ void __launch_bounds__(kQThreads, 1) quantize_kernel(QuantParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int K = p.K, nb = p.nb, S = p.stages;
-    uint16_t* perm_s = reinterpret_cast<uint16_t*>(smem_raw);                       // [K]
-    uint16_t* rows_s = perm_s + K;                                                 // [S][K]
-    uint8_t* mask_s = reinterpret_cast<uint8_t*>(rows_s + static_cast<size_t>(S) * K);  // [nb]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + ((2ull * K * (S + 1) + nb + 15) & ~15ull));
+    uint16_t* rows_s = reinterpret_cast<uint16_t*>(smem_raw);                            // [S][K]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + ((2ull * K * S + 15) & ~15ull));
     uint64_t* full = bars;        // [S]
     uint64_t* empty = bars + S;   // [S]
-    uint64_t* perm_bar = bars + 2 * S;
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             dev::mbar_init(&full[s], 1);
-            dev::mbar_init(&empty[s], kQuantWarps);
+            dev::mbar_init(&empty[s], kQWarps);
         }
-        dev::mbar_init(perm_bar, 1);
         abort_flag = 0;
         dev::fence_barrier_init();
     }
-    for (int b = threadIdx.x; b < nb; b += blockDim.x) mask_s[b] = p.mask[b];
     __syncthreads();
 
     const uint32_t row_bytes = static_cast<uint32_t>(K) * 2u;
-    if (warp == kQuantWarps) {
-        // ---------------- producer: permutation once, then rows into the stage ring
+    if (warp == kQWarps) {
+        // ---------------- producer: rows of X into the stage ring
         if (lane == 0) {
-            dev::mbar_arrive_expect_tx(perm_bar, row_bytes);
-            dev::bulk_g2s(perm_s, p.perm, row_bytes, perm_bar);
             int64_t i = 0;
             for (int64_t m = blockIdx.x; m < p.M; m += gridDim.x, ++i) {
                 const int s = static_cast<int>(i % S);
@@ -156,40 +188,133 @@ __global__ void __launch_bounds__(kQuantThreads, 1) quantize_kernel(QuantParams 
                 const int64_t last = s + ((issued - 1 - s) / S) * S;
                 dev::mbar_wait(&full[s], static_cast<uint32_t>((last / S) & 1), nullptr);
             }
-            dev::mbar_wait(perm_bar, 0, nullptr);
         }
+        __syncwarp();
     } else {
         // ---------------- compute warps
-        bool ok = true;
-        if (lane == 0) ok = dev::mbar_wait(perm_bar, 0, &abort_flag);
-        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        const bool upper = lane >= 16;
+        const int sub = lane & 15;                          // 8-channel group inside the block
+        const uint32_t hmask = upper ? 0xFFFF0000u : 0x0000FFFFu;
+        // per iteration j: this lane's block, its gather byte offsets, plane offset, precision
+        uint4 goff[kQMaxIters];
+        uint32_t is8_bits = 0, valid_bits = 0;
+#pragma unroll
+        for (int j = 0; j < kQMaxIters; ++j) {
+            const int b = warp + 32 * j + (upper ? 16 : 0);
+            const bool valid = b < nb;
+            uint4 g = make_uint4(0, 0, 0, 0);
+            if (valid) {
+                const uint4 pr = *reinterpret_cast<const uint4*>(p.perm + b * kBlock + sub * 8);
+                // channel index -> byte offset inside the row (indices < 32768)
+                g = make_uint4(pr.x << 1, pr.y << 1, pr.z << 1, pr.w << 1);
+                if (p.mask[b]) is8_bits |= 1u << j;
+                valid_bits |= 1u << j;
+            }
+            goff[j] = g;
+        }
+        const int iters = (nb - warp + 31) / 32;            // iterations with a valid lower block
+        const int64_t plane_stride = p.M * kBlock;
+
         int64_t i = 0;
-        for (int64_t m = blockIdx.x; ok && m < p.M; m += gridDim.x, ++i) {
+        bool ok = true;
+        for (int64_t m = blockIdx.x; m < p.M; m += gridDim.x, ++i) {
             const int s = static_cast<int>(i % S);
             const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
             if (lane == 0) ok = dev::mbar_wait(&full[s], ph, &abort_flag);
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             if (!ok) break;
-            const uint16_t* xrow = rows_s + static_cast<size_t>(s) * K;
-            for (int b = warp; b < nb; b += kQuantWarps) {
-                const int j0 = b * kBlock + lane * 4;
-                const uint2 pp = *reinterpret_cast<const uint2*>(perm_s + j0);
-                uint16_t h[4];
-                h[0] = xrow[pp.x & 0xFFFFu];
-                h[1] = xrow[pp.x >> 16];
-                h[2] = xrow[pp.y & 0xFFFFu];
-                h[3] = xrow[pp.y >> 16];
-                const bool is8 = mask_s[b] != 0;
-                uint16_t sbits;
-                const uint32_t v = quantize4(h, is8 ? 127 : 7, &sbits);
-                uint8_t* blk = p.A + static_cast<int64_t>(p.boff[b]) * p.M;
-                if (is8) {
-                    reinterpret_cast<uint32_t*>(blk + m * 128)[lane] = v;
-                } else {
-                    const uint32_t word = pack_int4_pair(v, lane);
-                    if ((lane & 1) == 0) reinterpret_cast<uint32_t*>(blk + m * 64)[lane >> 1] = word;
+            const uint8_t* row = reinterpret_cast<const uint8_t*>(rows_s + static_cast<size_t>(s) * K);
+            const uint32_t chunk_off = ((static_cast<uint32_t>(sub >> 1) ^ static_cast<uint32_t>(m & 7)) << 4) +
+                                       static_cast<uint32_t>(sub & 1) * 8u;
+#pragma unroll
+            for (int j = 0; j < kQMaxIters; ++j) {
+                if (j >= iters) break;                       // warp-uniform
+                const bool valid = (valid_bits >> j) & 1u;
+                const bool is8 = (is8_bits >> j) & 1u;
+                // gather 8 fp16 values, paired into half2 words
+                const uint4 g = goff[j];
+                uint32_t h2[4];
+                {
+                    const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t lo = *reinterpret_cast<const uint16_t*>(row + (gw[k] & 0xFFFFu));
+                        const uint32_t hi = *reinterpret_cast<const uint16_t*>(row + (gw[k] >> 16));
+                        h2[k] = __byte_perm(lo, hi, 0x5410);
+                    }
                 }
-                if (lane == 0) p.scales[static_cast<int64_t>(b) * p.M + m] = sbits;
+                // absmax of the half-warp's 128 values
+                uint32_t ab[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) ab[k] = h2[k] & 0x7FFF7FFFu;
+                const __half2 m01 = __hmax2(*reinterpret_cast<const __half2*>(&ab[0]),
+                                            *reinterpret_cast<const __half2*>(&ab[1]));
+                const __half2 m23 = __hmax2(*reinterpret_cast<const __half2*>(&ab[2]),
+                                            *reinterpret_cast<const __half2*>(&ab[3]));
+                const __half2 mx = __hmax2(m01, m23);
+                const __half lm = __hmax(__low2half(mx), __high2half(mx));
+                const uint32_t amax_bits = __reduce_max_sync(hmask, static_cast<uint32_t>(__half_as_ushort(lm)));
+                // scale: fp16(fp32(absmax) * fp32(1/qmax)) equals fp16(fp32(absmax) / qmax)
+                // for every finite fp16 absmax and qmax in {7, 127}
+                const float amax = __half2float(__ushort_as_half(static_cast<unsigned short>(amax_bits)));
+                const float qm = is8 ? 127.0f : 7.0f;
+                const __half s16 = __float2half_rn(__fmul_rn(amax, is8 ? (1.0f / 127.0f) : (1.0f / 7.0f)));
+                const float sc = __half2float(s16);
+                const float inv = sc > 0.0f ? rcp_approx(sc) : 0.0f;
+
+                // codes: rne(|x| / s) via |x| * inv (relative error < 2^-22) and the
+                // 1.5 * 2^23 rounding constant; near-half quotients are settled exactly
+                constexpr float kMagic = 12582912.0f;
+                float ax[8], r[8];
+                bool near_half = false;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ab[k]));
+                    ax[2 * k] = f.x;
+                    ax[2 * k + 1] = f.y;
+                }
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float t = __fmul_rn(ax[k], inv);
+                    r[k] = __fsub_rn(__fadd_rn(t, kMagic), kMagic);
+                    near_half |= fabsf(__fsub_rn(t, r[k])) > 0.4999f;
+                }
+                if (__any_sync(0xFFFFFFFFu, near_half) && sc > 0.0f) {
+                    // (a zero scale keeps every code 0: its lanes skip the correction)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const float e = fmaf(-r[k], sc, ax[k]);   // exact remainder |x| - r*s
+                        const float e2 = e + e;
+                        if (e2 > sc) r[k] += 1.0f;
+                        else if (e2 < -sc) r[k] -= 1.0f;
+                        else if (e2 == sc || e2 == -sc) {
+                            const bool odd = (static_cast<int>(r[k]) & 1) != 0;
+                            if (odd) r[k] += (e2 > 0.0f) ? 1.0f : -1.0f;   // tie: to even
+                        }
+                    }
+                }
+                if (__any_sync(0xFFFFFFFFu, sc > 0.0f && sc < 6.103515625e-05f)) {
+                    // subnormal scale: the quotient can round past qmax
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) r[k] = fminf(r[k], qm);
+                }
+                uint32_t w0 = low_bytes4(r[0] + kMagic, r[1] + kMagic, r[2] + kMagic, r[3] + kMagic);
+                uint32_t w1 = low_bytes4(r[4] + kMagic, r[5] + kMagic, r[6] + kMagic, r[7] + kMagic);
+                // sign bits of the inputs (bit 15 of each half) into bit 7 of each byte
+                w0 |= __byte_perm(h2[0], h2[1], 0x7531) & 0x80808080u;
+                w1 |= __byte_perm(h2[2], h2[3], 0x7531) & 0x80808080u;
+
+                if (valid) {
+                    const int b = warp + 32 * j + (upper ? 16 : 0);
+                    uint8_t* dst = p.A + (static_cast<int64_t>(__ldg(p.poff + b)) * p.M + m) * kBlock + chunk_off;
+                    if (!is8) {
+                        *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
+                    } else {
+                        *reinterpret_cast<uint2*>(dst) = make_uint2(w0 & 0x8F8F8F8Fu, w1 & 0x8F8F8F8Fu);
+                        *reinterpret_cast<uint2*>(dst + plane_stride) = make_uint2(high_plane(w0), high_plane(w1));
+                    }
+                    if (sub == 0) p.scales[static_cast<int64_t>(b) * p.M + m] = __half_as_ushort(s16);
+                }
             }
             __syncwarp();
             if (lane == 0) dev::mbar_arrive(&empty[s]);
@@ -264,14 +389,14 @@ __global__ void unpack_weights_kernel(const uint8_t* Wp, int64_t N, int K, int n
 cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, int64_t M, void* A, void* scales,
                             cudaStream_t stream) {
     const int K = L.K;
-    const size_t fixed = 2ull * K + L.nb + 16 + 1024;
-    int stages = static_cast<int>((kQuantSmemBudget - fixed) / (2ull * K));
-    stages = stages < 1 ? 1 : (stages > 4 ? 4 : stages);
-    const size_t smem = ((2ull * K * (stages + 1) + L.nb + 15) & ~15ull) + 8ull * (2 * stages + 1);
+    const size_t fixed = 16 + 1024;
+    int stages = static_cast<int>((kQSmemBudget - fixed) / (2ull * K));
+    stages = stages < 1 ? 1 : (stages > 8 ? 8 : stages);
+    const size_t smem = ((2ull * K * stages + 15) & ~15ull) + 8ull * (2 * stages);
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kQuantSmemBudget + 16 * 1024);
+                                             kQSmemBudget + 16 * 1024);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -284,12 +409,12 @@ cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, in
     p.stages = stages;
     p.perm = L.d_perm16;
     p.mask = L.d_mask;
-    p.boff = L.d_boff;
+    p.poff = L.d_poff;
     p.A = static_cast<uint8_t*>(A);
     p.scales = static_cast<uint16_t*>(scales);
     p.status = L.d_status;
     const int64_t grid = M < L.num_sms ? M : L.num_sms;
-    quantize_kernel<<<static_cast<unsigned>(grid), kQuantThreads, smem, stream>>>(p);
+    quantize_kernel<<<static_cast<unsigned>(grid), kQThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }
 

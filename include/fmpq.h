@@ -79,16 +79,18 @@ FMPQ_API int32_t fmpq_layout_k(const fmpq_layout* layout);
 FMPQ_API int32_t fmpq_layout_num_blocks(const fmpq_layout* layout);
 FMPQ_API int32_t fmpq_layout_num_int8_blocks(const fmpq_layout* layout);
 
-/* Bytes of the packed activation buffer for M tokens: M * (64 * n4 + 128 * n8).
- * Layout (block-major; the method's "mixed-precision data layout", made concrete here so
- * that the GEMM converts 8 INT4 codes to 8 tensor-core operands with three integer ops):
- *   block b occupies bytes [M*off_b, M*(off_b + w_b)), w_b = 64 (INT4) or 128 (INT8),
- *   off_b = sum of w over the blocks before b; inside a block, row m takes w_b bytes.
- *   INT8 block row: byte c = sign(q_c) << 7 | |q_c|           (sign-magnitude, |q| <= 127)
- *   INT4 block row: 16 little-endian 32-bit words; word g holds channels 8g..8g+7;
- *     byte j (0..3): bits 0-2 = |q_{8g+j}|, bit 7 = sign(q_{8g+j}),
- *                    bits 4-6 = |q_{8g+4+j}|, bit 3 = sign(q_{8g+4+((j+3)%4)}).
- *   sign(q) = 1 iff q < 0. */
+/* Bytes of the packed activation buffer for M tokens: M * 128 * (n4 + 2 * n8).
+ * Layout: operand-ready code planes (the method's "mixed-precision data layout", made
+ * concrete for a tensor core whose narrowest exact integer path is 8-bit E4M3):
+ *   - One byte per code: bit 7 = sign bit of the fp16 input, bits 0-6 = the E4M3 encoding
+ *     of part * 2^-9, where part is |q| for an INT4 block. An INT8 block has two planes,
+ *     part = |q| mod 16 (low plane) and part = |q| - |q| mod 16 (high plane); the parts of
+ *     a code sum to |q|. (For part <= 15 the encoding is the integer part itself.)
+ *   - Planes follow block order: block b's first plane is plane poff_b = n4 + 2*n8 counted
+ *     over the blocks before b; plane p occupies bytes [p*M*128, (p+1)*M*128).
+ *   - Row m of a plane is 128 bytes; the 16 channels 16c..16c+15 of the block are stored
+ *     in order in the 16-byte chunk at position c XOR (m mod 8), so that a copy of 128
+ *     rows starting at a multiple of 128 is a 128-byte-swizzled K-major operand tile. */
 FMPQ_API size_t fmpq_packed_a_bytes(const fmpq_layout* layout, int64_t M);
 
 /* Bytes of the packed weight buffer for N output channels: ceil(N/256)*256 * K/2.

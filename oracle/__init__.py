@@ -65,8 +65,10 @@ def _load():
             lib.oracle_epilogue_f64.argtypes = [P, P, P, i32, i32, i32, P]
             lib.oracle_epilogue_exact.argtypes = [P, P, P, i32, i32, i32, P]
             lib.oracle_gemm_sample.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P, P, P]
-            lib.oracle_block_offset.argtypes = [P, i32]
-            lib.oracle_block_offset.restype = i64
+            lib.oracle_plane_offset.argtypes = [P, i32]
+            lib.oracle_plane_offset.restype = i64
+            lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_value.restype = ctypes.c_double
             lib.oracle_packed_a_bytes.argtypes = [P, i32, i32]
             lib.oracle_packed_a_bytes.restype = i64
             lib.oracle_num_threads.restype = i32
@@ -109,10 +111,15 @@ def packed_a_bytes(mask, K: int, M: int) -> int:
     return int(_load().oracle_packed_a_bytes(_ptr(mask), K, M))
 
 
-def block_offsets(mask) -> np.ndarray:
-    """Per-block byte offset (units of M) of the packed activation layout."""
+def plane_offsets(mask) -> np.ndarray:
+    """Per-block plane offset of the packed activation layout (a plane is M x 128 bytes)."""
     mask = _c(mask, np.uint8)
-    return np.array([_load().oracle_block_offset(_ptr(mask), b) for b in range(mask.size)], dtype=np.int64)
+    return np.array([_load().oracle_plane_offset(_ptr(mask), b) for b in range(mask.size)], dtype=np.int64)
+
+
+def e4m3_value(byte: int) -> float:
+    """Value of an E4M3 byte, decoded from the format's definition."""
+    return float(_load().oracle_e4m3_value(int(byte) & 0xFF))
 
 
 def quantize_activations(X, perm, mask, want_codes: bool = True):

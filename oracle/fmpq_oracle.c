@@ -22,11 +22,10 @@
  *   - symmetric absmax quantization; INT4 range [-7,7], INT8 range [-127,127]
  *   - scale s = fp16_rne( fp32(absmax) / fp32(qmax) ); a zero scale quantizes the block to 0
  *   - q = clamp( rne_f32( fp32(x) / fp32(s) ), -qmax, qmax ) with IEEE fp32 division
- *   - packed activation layout: block-major (block b at byte M*off_b, 64 or 128 bytes per
- *     row); INT8 codes as sign-magnitude bytes; INT4 codes as sign-magnitude 3+1-bit fields,
- *     8 channels per 32-bit word: byte j holds |q_j| in bits 0-2 and sign(q_j) in bit 7,
- *     |q_{4+j}| in bits 4-6 and sign(q_{4+(j+3)%4}) in bit 3 (the layout is chosen so the
- *     tensor-core operand bytes fall out with a mask and a rotate; the oracle only writes it)
+ *   - packed activation layout (an encoding, not arithmetic of the method): one byte per
+ *     code holding an E4M3 number equal to part of |q| times 2^-9 (INT8 codes use two
+ *     planes, |q| mod 16 and the rest), planes block after block, 16-byte chunks of each
+ *     128-byte row rotated by XOR with the row index mod 8 (see "Packed activation format")
  *
  * Floating point here is IEEE fp32 where the method decides an integer (the kernel's
  * precision), and fp64 or exact int128 fixed point for the epilogue reference.
@@ -140,58 +139,98 @@ static uint16_t quantize_block(const uint16_t* xs, int qmax, int8_t* q) {
 }
 
 /* ------------------------------------------------------------------------------------
- * Packed code formats (sign-magnitude).
+ * Packed activation format: operand-ready code planes.
+ *
+ * Every code is stored as one byte holding the E4M3 number (FP8: 1 sign bit, 4 exponent
+ * bits with bias 7, 3 mantissa bits; exponent field 0 is subnormal) equal to a part of
+ * the code's magnitude times 2^-9, with bit 7 = the sign bit of the fp16 input (so a
+ * negative input whose code is 0 gives -0, numerically 0).
+ *   INT4 block: one plane, part = |q|                       (0..7)
+ *   INT8 block: two planes, part = |q| mod 16               (0..15)  [the "low" plane]
+ *                           part = |q| - (|q| mod 16)       (0..112) [the "high" plane]
+ * The parts of a code sum to |q|. Planes are stored block after block (plane offset of
+ * block b = number of planes of the blocks before it); a plane is [M][128] bytes; in row m
+ * the 16-byte chunk holding channels 16c..16c+15 sits at chunk position c XOR (m mod 8).
  * ------------------------------------------------------------------------------------ */
 
-static unsigned sgn(int8_t q) { return q < 0 ? 1u : 0u; }
+/* Value of an E4M3 byte, from the format's definition (0x7F/0xFF are NaN). */
+double oracle_e4m3_value(uint8_t b) {
+    int sign = (b >> 7) & 1, e = (b >> 3) & 15, f = b & 7;
+    double v;
+    if (e == 15 && f == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)f / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)f / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* The non-negative E4M3 byte whose value is exactly n * 2^-9 (found by search over the
+ * encodings), or -1 if no encoding has that value. */
+static int e4m3_of_multiple(int n) {
+    const double target = ldexp((double)n, -9);
+    for (int b = 0; b < 128; ++b) {
+        const double v = oracle_e4m3_value((uint8_t)b);
+        if (!isnan(v) && v == target) return b;
+    }
+    return -1;
+}
+
 static unsigned mag(int8_t q) { return (unsigned)(q < 0 ? -q : q); }
 
-/* INT8 row: byte c = sign(q_c) << 7 | |q_c| */
-static void pack_int8_row(const int8_t* q, uint8_t* dst) {
-    for (int c = 0; c < ORACLE_BLOCK; ++c) dst[c] = (uint8_t)((sgn(q[c]) << 7) | mag(q[c]));
+/* part of |q| stored in plane `plane` of a block */
+static unsigned code_part(int8_t q, int is_int8, int plane) {
+    const unsigned a = mag(q);
+    if (!is_int8) return a;
+    return plane == 0 ? a % 16u : a - a % 16u;
 }
 
-static void unpack_int8_row(const uint8_t* src, int8_t* q) {
-    for (int c = 0; c < ORACLE_BLOCK; ++c) {
-        int v = src[c] & 0x7F;
-        q[c] = (int8_t)((src[c] & 0x80) ? -v : v);
-    }
+/* byte position of channel c in row m of a plane */
+static int64_t plane_pos(int m, int c) {
+    return (int64_t)((((c / 16) ^ (m % 8)) * 16) + c % 16);
 }
 
-/* INT4 row: 16 groups of 8 channels, 4 bytes per group (byte 4g+j of the row):
- *   bits 0-2 |q[8g+j]|, bit 7 sign(q[8g+j]), bits 4-6 |q[8g+4+j]|, bit 3 sign(q[8g+4+(j+3)%4]) */
-static void pack_int4_row(const int8_t* q, uint8_t* dst) {
-    for (int g = 0; g < 16; ++g) {
-        const int8_t* e = q + 8 * g;
-        for (int j = 0; j < 4; ++j) {
-            unsigned byte = mag(e[j]) | (sgn(e[j]) << 7) | (mag(e[4 + j]) << 4) | (sgn(e[4 + (j + 3) % 4]) << 3);
-            dst[4 * g + j] = (uint8_t)byte;
-        }
-    }
-}
+static int num_planes(const uint8_t* mask, int b) { return mask[b] ? 2 : 1; }
 
-static void unpack_int4_row(const uint8_t* src, int8_t* q) {
-    for (int g = 0; g < 16; ++g) {
-        const uint8_t* w = src + 4 * g;
-        for (int j = 0; j < 4; ++j) {
-            int lo = w[j] & 7, hi = (w[j] >> 4) & 7;
-            q[8 * g + j] = (int8_t)((w[j] & 0x80) ? -lo : lo);
-            /* the sign of element 4+j sits in bit 3 of byte (j+1)%4 */
-            q[8 * g + 4 + j] = (int8_t)((w[(j + 1) % 4] & 0x08) ? -hi : hi);
-        }
-    }
-}
-
-/* Byte offset of block b inside the packed activation buffer, in units of M:
- * off_b = sum_{b' < b} width(b'), width = 64 bytes (INT4) or 128 bytes (INT8) per row. */
-int64_t oracle_block_offset(const uint8_t* mask, int b) {
+/* Plane offset of block b: planes of the blocks before it. */
+int64_t oracle_plane_offset(const uint8_t* mask, int b) {
     int64_t off = 0;
-    for (int i = 0; i < b; ++i) off += mask[i] ? 128 : 64;
+    for (int i = 0; i < b; ++i) off += num_planes(mask, i);
     return off;
 }
 
 int64_t oracle_packed_a_bytes(const uint8_t* mask, int K, int M) {
-    return oracle_block_offset(mask, K / ORACLE_BLOCK) * (int64_t)M;
+    return oracle_plane_offset(mask, K / ORACLE_BLOCK) * (int64_t)M * ORACLE_BLOCK;
+}
+
+/* Write the codes q[128] of token m, block b into its plane(s); xs[128] are the block's
+ * fp16 inputs (for the sign bit). */
+static void pack_block_row(const int8_t* q, const uint16_t* xs, int is_int8, uint8_t* A_packed, int64_t plane0,
+                           int M, int m) {
+    for (int p = 0; p < (is_int8 ? 2 : 1); ++p) {
+        uint8_t* row = A_packed + (plane0 + p) * (int64_t)M * ORACLE_BLOCK + (int64_t)m * ORACLE_BLOCK;
+        for (int c = 0; c < ORACLE_BLOCK; ++c) {
+            const int e = e4m3_of_multiple((int)code_part(q[c], is_int8, p));
+            row[plane_pos(m, c)] = (uint8_t)(((xs[c] >> 15) << 7) | (unsigned)e);
+        }
+    }
+}
+
+/* Read the codes of token m, block b back from its plane(s): the parts' values sum to
+ * |q| * 2^-9; the sign is bit 7 of the first plane. */
+static void unpack_block_row(const uint8_t* A_packed, int is_int8, int64_t plane0, int M, int m, int8_t* q) {
+    for (int c = 0; c < ORACLE_BLOCK; ++c) {
+        double v = 0.0;
+        unsigned sign = 0;
+        for (int p = 0; p < (is_int8 ? 2 : 1); ++p) {
+            const uint8_t byte =
+                A_packed[(plane0 + p) * (int64_t)M * ORACLE_BLOCK + (int64_t)m * ORACLE_BLOCK + plane_pos(m, c)];
+            v += fabs(oracle_e4m3_value(byte));
+            if (p == 0) sign = byte >> 7;
+        }
+        const int a = (int)ldexp(v, 9);
+        q[c] = (int8_t)(sign ? -a : a);
+    }
 }
 
 /* Activations: X fp16 bits [M][ldx] -> packed A, a_scales [nb][M] (fp16 bits) and, if
@@ -203,7 +242,7 @@ int oracle_quantize_activations(const uint16_t* X, int64_t ldx, int M, int K,
     const int nb = K / ORACLE_BLOCK;
     int64_t* off = (int64_t*)malloc(sizeof(int64_t) * (size_t)nb);
     if (!off) return -2;
-    for (int b = 0; b < nb; ++b) off[b] = oracle_block_offset(mask, b);
+    for (int b = 0; b < nb; ++b) off[b] = oracle_plane_offset(mask, b);
 #pragma omp parallel for schedule(static)
     for (int m = 0; m < M; ++m) {
         uint16_t xs[ORACLE_BLOCK];
@@ -218,26 +257,21 @@ int oracle_quantize_activations(const uint16_t* X, int64_t ldx, int M, int K,
             if (Aq)
                 for (int j = 0; j < ORACLE_BLOCK; ++j) Aq[(int64_t)m * K + b * ORACLE_BLOCK + j] = q[j];
             /* pack */
-            uint8_t* dst = A_packed + off[b] * M;
-            if (mask[b]) pack_int8_row(q, dst + (int64_t)m * 128);
-            else pack_int4_row(q, dst + (int64_t)m * 64);
+            pack_block_row(q, xs, mask[b] != 0, A_packed, off[b], M, m);
         }
     }
     free(off);
     return 0;
 }
 
-/* Decode the canonical packed activation buffer back to codes Aq [M][K]. */
+/* Decode the packed activation buffer back to codes Aq [M][K]. */
 int oracle_unpack_activations(const uint8_t* A_packed, const uint8_t* mask, int M, int K, int8_t* Aq) {
     if (K % ORACLE_BLOCK) return -1;
     const int nb = K / ORACLE_BLOCK;
     for (int b = 0; b < nb; ++b) {
-        const uint8_t* src = A_packed + oracle_block_offset(mask, b) * M;
-        for (int m = 0; m < M; ++m) {
-            int8_t* row = Aq + (int64_t)m * K + b * ORACLE_BLOCK;
-            if (mask[b]) unpack_int8_row(src + (int64_t)m * 128, row);
-            else unpack_int4_row(src + (int64_t)m * 64, row);
-        }
+        const int64_t plane0 = oracle_plane_offset(mask, b);
+        for (int m = 0; m < M; ++m)
+            unpack_block_row(A_packed, mask[b] != 0, plane0, M, m, Aq + (int64_t)m * K + b * ORACLE_BLOCK);
     }
     return 0;
 }

@@ -189,3 +189,25 @@ def test_config_decode(fmpq_mod, oracle_mod, M):
 @pytest.mark.parametrize("frac", wl.LOAD_BALANCE_FRACS)
 def test_config_load_balance(fmpq_mod, oracle_mod, frac):
     _sampled_check(fmpq_mod, oracle_mod, wl.load_balance(frac), window=(1000, 40, 28672 - 80, 80))
+
+
+def test_scale_every_fp16_absmax(fmpq_mod, oracle_mod):
+    """Every finite non-negative fp16 value as the absmax of an INT4 and of an INT8 block
+    (one token each), the other channels random fractions of it: scales and code planes
+    bit-exact against the oracle."""
+    rng = np.random.default_rng(5)
+    amax = np.arange(0, 0x7C00, dtype=np.uint16).view(np.float16).astype(np.float32)
+    M, K = amax.size, 256
+    frac = rng.uniform(-1.0, 1.0, size=(M, K)).astype(np.float32)
+    X = (frac * amax[:, None]).astype(np.float16)
+    X[:, 0] = amax.astype(np.float16)
+    X[:, 128] = (-amax).astype(np.float16)
+    perm = np.arange(K, dtype=np.int32)
+    mask = np.array([0, 1], np.uint8)
+    layout = fmpq_mod.Layout(K, perm, mask)
+    A, sx = fmpq_mod.fmpq_quantize(layout, to_dev(X))
+    A_ref, sx_ref, _ = oracle_mod.quantize_activations(X, perm, mask, want_codes=False)
+    assert np.array_equal(sx.cpu().numpy().view(np.uint16), sx_ref)
+    assert np.array_equal(A.cpu().numpy(), A_ref)
+    assert fmpq_mod.fmpq_device_status(layout) == 0
+    layout.close()

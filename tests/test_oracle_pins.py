@@ -168,24 +168,68 @@ def test_gather_direction(oracle_mod):
 
 def test_packed_layout_example(oracle_mod):
     ex = json.load(open(GOLDEN))["packed_layout_example"]
-    X = np.zeros((1, 256), dtype=np.float16)
-    X[0, : len(ex["block0_x"])] = ex["block0_x"]
-    X[0, 128: 128 + len(ex["block1_x"])] = ex["block1_x"]
+    M = ex["M"]
+    X = np.zeros((M, 256), dtype=np.float16)
+    X[0, : len(ex["row0_block0_x"])] = ex["row0_block0_x"]
+    X[0, 128: 128 + len(ex["row0_block1_x"])] = ex["row0_block1_x"]
+    for c, v in ex["row3_x_at"].items():
+        X[3, int(c)] = v
     mask = np.array(ex["mask"], dtype=np.uint8)
     A, s, Aq = oracle_mod.quantize_activations(X, np.arange(256, dtype=np.int32), mask)
     assert A.size == ex["total_bytes"]
-    b0 = [int(v, 16) for v in ex["expected_bytes_prefix_block0"]]
-    b1 = [int(v, 16) for v in ex["expected_bytes_prefix_block1"]]
-    assert list(A[: len(b0)]) == b0
-    assert list(A[64: 64 + len(b1)]) == b1
-    assert np.all(A[len(b0):64] == 0) and np.all(A[64 + len(b1):] == 0)
+    want = np.zeros(ex["total_bytes"], dtype=np.uint8)
+    for pos, v in ex["expected_nonzero"]:
+        want[pos] = int(v, 16)
+    assert np.array_equal(A, want), np.nonzero(A != want)
+    assert [int(v, 16) for v in ex["expected_scales_bits"]["row0"]] == list(s[:, 0])
+    assert [int(v, 16) for v in ex["expected_scales_bits"]["row3"]] == list(s[:, 3])
+
+
+def test_e4m3_decoder_against_torch(oracle_mod):
+    """The oracle's E4M3 decoder (written from the format's definition) against torch's
+    float8_e4m3fn conversion, on all 256 encodings."""
+    torch = pytest.importorskip("torch")
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle_mod.e4m3_value(b) for b in range(256)])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def test_plane_bytes_decode_to_code_parts(oracle_mod):
+    """Every code in [-127, 127] of an INT8 block and [-7, 7] of an INT4 block: its plane
+    bytes decode (E4M3 definition) to parts that sum to |q| * 2^-9, with the code's sign."""
+    K, M = 256, 255
+    X = np.zeros((M, K), dtype=np.float16)
+    q = np.arange(-127, 128)
+    # one token per code: channel 128 holds the code, channel 129 pins absmax at 127
+    X[:, 128] = q.astype(np.float16)
+    X[:, 129] = np.float16(127)
+    X[:, 0] = np.clip(q, -7, 7).astype(np.float16)
+    X[:, 1] = np.float16(7)
+    mask = np.array([0, 1], np.uint8)
+    A, s, Aq = oracle_mod.quantize_activations(X, np.arange(K, dtype=np.int32), mask)
+    assert np.array_equal(Aq[:, 128], q) and np.array_equal(Aq[:, 0], np.clip(q, -7, 7))
+    planes = A.reshape(3, M, 128)
+    for m in range(M):
+        pos = 16 * ((128 // 16 - 8) ^ (m % 8))          # channel 128 = chunk 0 of block 1
+        lo, hi = planes[1, m, pos], planes[2, m, pos]
+        v = abs(oracle_mod.e4m3_value(lo)) + abs(oracle_mod.e4m3_value(hi))
+        assert v * 512 == abs(q[m])
+        assert (lo >> 7) == (q[m] < 0) and (hi >> 7) == (q[m] < 0)
+        assert abs(oracle_mod.e4m3_value(lo)) * 512 == abs(q[m]) % 16
+        b4 = planes[0, m, 16 * (0 ^ (m % 8))]             # channel 0 = chunk 0 of block 0
+        assert abs(oracle_mod.e4m3_value(b4)) * 512 == min(abs(q[m]), 7)
+        assert (b4 >> 7) == (q[m] < 0)
 
 
 @pytest.mark.parametrize("seed", [0, 3])
 def test_pack_unpack_roundtrip(oracle_mod, seed):
     X, perm, mask = _rand_case(seed, M=7)
     A, _, Aq = oracle_mod.quantize_activations(X, perm, mask)
-    assert A.size == 7 * sum(128 if m else 64 for m in mask)
+    assert A.size == 7 * 128 * sum(2 if m else 1 for m in mask)
     assert np.array_equal(oracle_mod.unpack_activations(A, mask, 7, X.shape[1]), Aq)
 
 
