@@ -11,19 +11,21 @@
 //     128-row activation tile is one bulk copy straight into the operand ring. An INT8
 //     block has two planes (|q| mod 16 and the rest) that accumulate into the same TMEM
 //     tile, so every block ends in one FP32 tile P * 2^-18 (exact: |P| < 2^17).
-//   * INT4 weights stay 4-bit in HBM: converter warps turn each packed word into 8
-//     operand bytes with a mask and a rotate (the sign-magnitude byte s0000mmm is the E4M3
-//     value (-1)^s * m * 2^-9) -- the restructured storage format that makes 4-bit ->
-//     8-bit conversion a couple of instructions (COMET news article, section 3).
+//   * INT4 weights stay 4-bit in HBM: converter warps read the packed words straight
+//     from global memory and turn each into 8 operand bytes with a mask and a rotate (the
+//     sign-magnitude byte s0000mmm is the E4M3 value (-1)^s * m * 2^-9) -- the
+//     restructured storage format that makes 4-bit -> 8-bit conversion a couple of
+//     instructions (COMET news article, section 3).
 //   * tcgen05.mma kind::f8f6f4 (M=128, N=256, K=32) with the accumulator in TMEM,
 //     double-buffered so the MMA of the next block overlaps the epilogue of this one.
-//   * Per block the epilogue warps read the tile (tcgen05.ld) and accumulate
-//     acc += (w_scale[n] * a_scale[m] * 2^18) * D in FP32 registers (packed f32x2 math).
+//   * Per block the epilogue warps read the tile (tcgen05.ld 16x256b: two rows and
+//     column pairs per thread, so each weight scale read serves two rows) and accumulate
+//     acc += D * (w_scale[n] * a_scale[m] * 2^18) in FP32 registers (packed f32x2 math).
 //
 // Warp roles (512 threads, one CTA per SM, persistent over tiles):
-//   warp 0       TMA producer: activation code planes and the packed weight tile per block
+//   warp 0       TMA producer: activation code planes per block (bulk copies)
 //   warp 1       tcgen05 MMA issuer (one thread) + TMEM owner
-//   warps 2-7    converters: packed weight codes -> 128B-swizzled K-major E4M3 tile
+//   warps 2-7    converters: packed weight codes (global) -> 128B-swizzled E4M3 tile (smem)
 //   warps 8-15   epilogue: per-block FP32 scale-and-sum, fp16 output (or split-K partials)
 #include <cuda_fp16.h>
 
@@ -34,20 +36,23 @@ namespace fmpq {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kStages = 3;    // per-block stage: activation planes + packed weights
-constexpr int kCvStages = 2;  // converted weight tiles
+constexpr int kStages = 3;    // activation stages (two plane slots each)
+constexpr int kCvStages = 3;  // converted weight tiles
 constexpr int kConvWarps = 6;
 constexpr int kConvThreads = kConvWarps * 32;
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr uint32_t kTmemCols = 512;  // two 128 x 256 FP32 accumulators
 constexpr uint32_t kIdesc = dev::idesc_e4m3_f32(128, 256);
+// Weight scales of a block, staged for the epilogue: column n = 8g + 2c + j goes to
+// [c][2g + j]. Each epilogue thread reads the 64 values of its column pairs contiguously;
+// rows of 68 floats put the four c groups' 16-byte reads in distinct banks.
+constexpr int kSwStride = 68;
 
 struct __align__(1024) Smem {
     uint8_t opA[kStages][2][128 * 128];  // activation code planes (operand-ready, swizzled)
     uint8_t cvB[kCvStages][256 * 128];   // E4M3 weight operand (256 rows x 128 K), swizzled
-    uint8_t pkW[kStages][256 * 64];      // packed weight codes
-    float sw[2][256];                    // per-block weight scales (fp32) for the epilogue
+    float sw[2][4 * kSwStride];          // per-block weight scales (fp32), permuted
     uint64_t st_full[kStages], st_empty[kStages];
     uint64_t cv_full[kCvStages], cv_empty[kCvStages];
     uint64_t acc_full[2], acc_empty[2];
@@ -115,12 +120,10 @@ __device__ __forceinline__ void producer_role(const Params& p, Smem& s, int lane
                     break;
                 }
                 const int planes = p.mask[b] ? 2 : 1;
-                dev::mbar_arrive_expect_tx(&s.st_full[st], abytes * planes + 256 * 64);
+                dev::mbar_arrive_expect_tx(&s.st_full[st], abytes * planes);
                 const uint8_t* a0 = p.A + static_cast<int64_t>(p.poff[b]) * plane_bytes + static_cast<int64_t>(m0) * kBlock;
                 dev::bulk_g2s(s.opA[st][0], a0, abytes, &s.st_full[st]);
                 if (planes == 2) dev::bulk_g2s(s.opA[st][1], a0 + plane_bytes, abytes, &s.st_full[st]);
-                dev::bulk_g2s(s.pkW[st], p.W + (static_cast<int64_t>(t.nt) * p.nb + b) * (256 * 64), 256 * 64,
-                              &s.st_full[st]);
             }
         }
         if (!ok) {
@@ -180,50 +183,62 @@ __device__ __forceinline__ void mma_role(const Params& p, Smem& s, int lane, uin
 }
 
 // ---------------------------------------------------------------- converters (warps 2-7)
-// The weight tile is 256 rows x 8 chunks (8 packed bytes in, 16 operand bytes out). Thread
-// ct converts items ct + 192k: item i is row i/8, chunk i%8. Since 192 = 24 rows, the
-// chunk and the row's swizzle phase (row mod 8) are the same for every k, so each item's
-// source and destination are the thread's base offsets plus constants.
+// A weight tile (256 rows x 64 packed bytes) is 1024 pieces of 16 bytes; piece i is row
+// i/4, bytes 16*(i%4).. of the row, i.e. 32 codes = two 16-byte operand chunks. Thread ct
+// converts pieces ct + 192k: 192 pieces = 48 rows, so the piece's column and the row's
+// swizzle phase (row mod 8) are the same for every k and all addresses are the thread's
+// base offsets plus constants. The next block's pieces are loaded from global memory while
+// the converter waits for a free operand slot.
 __device__ __forceinline__ void converter_role(const Params& p, Smem& s, int warp, int lane, volatile int* abort_flag) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
     const int ct = (warp - 2) * 32 + lane;
-    const int r0 = ct >> 3, c = ct & 7;
-    const uint32_t src0 = static_cast<uint32_t>(r0 * 64 + c * 8);
-    const uint32_t dst0 = static_cast<uint32_t>(r0 * 128 + ((c ^ (r0 & 7)) << 4));
-    constexpr int kFull = (256 * 8) / kConvThreads;                      // 10 items for every thread
-    const bool extra = ct + kFull * kConvThreads < 256 * 8;              // an 11th for the first 128
-    uint32_t it = 0;
+    const int r0 = ct >> 2, c4 = ct & 3;
+    const uint32_t phase = static_cast<uint32_t>(r0 & 7);
+    const uint32_t src0 = static_cast<uint32_t>(r0 * 64 + c4 * 16);
+    const uint32_t dstA = static_cast<uint32_t>(r0 * 128) + (((2u * c4) ^ phase) << 4);
+    const uint32_t dstB = static_cast<uint32_t>(r0 * 128) + (((2u * c4 + 1u) ^ phase) << 4);
+    constexpr int kFull = 1024 / kConvThreads;                // 5 pieces for every thread
+    const bool extra = ct + kFull * kConvThreads < 1024;      // a 6th for the first 64
+    constexpr int kRowStep = kConvThreads / 4;                // 48 rows between a thread's pieces
+
+    int u = blockIdx.x;
+    if (u >= num_units) return;
+    Unit t = unit_of(p, u);
+    int b = t.b0;
+    uint4 w[kFull + 1];
+    auto load = [&](const Unit& tt, int bb) {
+        const uint8_t* g = p.W + (static_cast<int64_t>(tt.nt) * p.nb + bb) * (256 * 64) + src0;
+#pragma unroll
+        for (int k = 0; k < kFull; ++k) w[k] = __ldg(reinterpret_cast<const uint4*>(g + k * kRowStep * 64));
+        if (extra) w[kFull] = __ldg(reinterpret_cast<const uint4*>(g + kFull * kRowStep * 64));
+    };
+    load(t, b);
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
-        const Unit t = unit_of(p, u);
-        for (int b = t.b0; b < t.b1; ++b, ++it) {
-            const int st = it % kStages;
-            const int cs = it % kCvStages;
-            if (lane == 0)
-                ok = dev::mbar_wait(&s.st_full[st], (it / kStages) & 1, abort_flag) &&
-                     dev::mbar_wait(&s.cv_empty[cs], ((it / kCvStages) & 1) ^ 1, abort_flag);
-            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-            if (!ok) break;
-            const uint8_t* src = s.pkW[st] + src0;
-            uint8_t* dst = s.cvB[cs] + dst0;
+    for (uint32_t it = 0;; ++it) {
+        const int cs = it % kCvStages;
+        if (lane == 0) ok = dev::mbar_wait(&s.cv_empty[cs], ((it / kCvStages) & 1) ^ 1, abort_flag);
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (!ok) break;
+        uint8_t* dst = s.cvB[cs];
 #pragma unroll
-            for (int k0 = 0; k0 < kFull; k0 += 5) {
-                uint2 w[5];
-#pragma unroll
-                for (int k = 0; k < 5; ++k) w[k] = *reinterpret_cast<const uint2*>(src + (k0 + k) * 24 * 64);
-#pragma unroll
-                for (int k = 0; k < 5; ++k)
-                    *reinterpret_cast<uint4*>(dst + (k0 + k) * 24 * 128) =
-                        make_uint4(lo4(w[k].x), hi4(w[k].x), lo4(w[k].y), hi4(w[k].y));
+        for (int k = 0; k <= kFull; ++k) {
+            if (k < kFull || extra) {
+                const uint4 v = w[k];
+                *reinterpret_cast<uint4*>(dst + dstA + k * kRowStep * 128) = make_uint4(lo4(v.x), hi4(v.x), lo4(v.y), hi4(v.y));
+                *reinterpret_cast<uint4*>(dst + dstB + k * kRowStep * 128) = make_uint4(lo4(v.z), hi4(v.z), lo4(v.w), hi4(v.w));
             }
-            if (extra) {
-                const uint2 w = *reinterpret_cast<const uint2*>(src + kFull * 24 * 64);
-                *reinterpret_cast<uint4*>(dst + kFull * 24 * 128) = make_uint4(lo4(w.x), hi4(w.x), lo4(w.y), hi4(w.y));
-            }
-            dev::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) dev::mbar_arrive(&s.cv_full[cs]);
         }
+        dev::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) dev::mbar_arrive(&s.cv_full[cs]);
+        // next block
+        if (++b == t.b1) {
+            u += gridDim.x;
+            if (u >= num_units) break;
+            t = unit_of(p, u);
+            b = t.b0;
+        }
+        load(t, b);
     }
     if (!ok && lane == 0) {
         *abort_flag = 1;
@@ -232,37 +247,56 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, int war
 }
 
 // ---------------------------------------------------------------- epilogue (warps 8-15)
+// Warp e (0..7) covers TMEM lanes 32*(warp%4) + 16*(e/4) + [0, 16) -- tile rows -- and all
+// 256 columns, read with tcgen05.ld 16x256b: thread t holds rows t/4 and t/4 + 8 of that
+// slab and columns 8g + 2(t%4) + {0, 1}, g = 0..31 (four registers per 8 columns:
+// row0 col0, row0 col1, row1 col0, row1 col1).
 template <bool kPartials>
 __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, int warp, int lane, uint32_t tmem,
                                               volatile int* abort_flag) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
-    // ======================= epilogue
-    const int ew = warp - 8;           // 0..7
-    const int q = warp & 3;            // TMEM lane quarter of this warp
-    const int h = ew >> 2;             // column half: 0 -> cols 0..127, 1 -> 128..255
-    const int et = ew * 32 + lane;     // 0..255
-    uint32_t v = 0, bstep = 0;
+    const int ew = warp - 8;                         // 0..7
+    const int q = warp & 3;                          // TMEM lane quarter of this warp
+    const int slab = q * 32 + (ew >> 2) * 16;        // first tile row of this warp
+    const int tq = lane & 3, tr = lane >> 2;
+    const int lr0 = slab + tr, lr1 = slab + tr + 8;  // this thread's tile rows
+    const int et = ew * 32 + lane;                   // staging column 0..255
+    const int st_idx = ((et & 7) >> 1) * kSwStride + (et >> 3) * 2 + (et & 1);
+    const uint32_t lane_addr = static_cast<uint32_t>(slab) << 16;
+    uint32_t v = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
         const Unit t = unit_of(p, u);
         const int m0 = t.mt * kTileM, n0 = t.nt * kTileN;
-        const int row = m0 + q * 32 + lane;
-        const bool row_ok = row < p.M;
-        float2 acc[64];
+        const int row0 = m0 + lr0, row1 = m0 + lr1;
+        const bool ok0 = row0 < p.M, ok1 = row1 < p.M;
+        float2 accA[32], accB[32];   // rows lr0 / lr1, column pair g
 #pragma unroll
-        for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.f, 0.f);
-        // prefetch scales of the first block
+        for (int g = 0; g < 32; ++g) {
+            accA[g] = make_float2(0.f, 0.f);
+            accB[g] = make_float2(0.f, 0.f);
+        }
+        // scales are fetched two blocks ahead (global loads outlast a block's epilogue)
         const int ncol = n0 + et;
-        float sw_next = (t.b0 < t.b1 && ncol < p.N) ? __half2float(__ushort_as_half(p.w_scales[static_cast<int64_t>(t.b0) * p.N + ncol])) : 0.f;
-        float sx_next = (t.b0 < t.b1 && row_ok) ? __half2float(__ushort_as_half(p.a_scales[static_cast<int64_t>(t.b0) * p.M + row])) : 0.f;
-        for (int b = t.b0; b < t.b1; ++b, ++bstep, ++v) {
-            const float sw_cur = sw_next, sx_cur = sx_next;
-            if (b + 1 < t.b1) {
-                sw_next = (ncol < p.N) ? __half2float(__ushort_as_half(p.w_scales[static_cast<int64_t>(b + 1) * p.N + ncol])) : 0.f;
-                sx_next = row_ok ? __half2float(__ushort_as_half(p.a_scales[static_cast<int64_t>(b + 1) * p.M + row])) : 0.f;
-            }
-            float* swb = s.sw[bstep & 1];
-            swb[et] = sw_cur;
+        auto load_sw = [&](int b) -> float {
+            return (b < t.b1 && ncol < p.N) ? __half2float(__ushort_as_half(__ldg(p.w_scales + static_cast<int64_t>(b) * p.N + ncol))) : 0.f;
+        };
+        auto load_sx = [&](int b, int row, bool rok) -> float {
+            return (b < t.b1 && rok) ? __half2float(__ushort_as_half(__ldg(p.a_scales + static_cast<int64_t>(b) * p.M + row))) : 0.f;
+        };
+        float sw1 = load_sw(t.b0), sw2 = load_sw(t.b0 + 1);
+        float xa1 = load_sx(t.b0, row0, ok0), xa2 = load_sx(t.b0 + 1, row0, ok0);
+        float xb1 = load_sx(t.b0, row1, ok1), xb2 = load_sx(t.b0 + 1, row1, ok1);
+        for (int b = t.b0; b < t.b1; ++b, ++v) {
+            const float sw_cur = sw1, xa = xa1, xb = xb1;
+            sw1 = sw2;
+            xa1 = xa2;
+            xb1 = xb2;
+            sw2 = load_sw(b + 2);
+            xa2 = load_sx(b + 2, row0, ok0);
+            xb2 = load_sx(b + 2, row1, ok1);
+            float* swb = s.sw[v & 1];
+            swb[st_idx] = sw_cur;
             dev::named_bar_sync(1, kEpiThreads);
             const int ab = v & 1;
             if (ok) {
@@ -271,41 +305,48 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, int warp
             }
             if (ok) {
                 dev::tc_fence_after();
-                const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + ab * 256u + h * 128u;
+                const uint32_t taddr = tmem + lane_addr + ab * 256u;
                 if constexpr (!kPartials) {
                     // 2^18 undoes the operand encoding (both operands carry 2^-9)
-                    const float sxp = sx_cur * 262144.0f;
-                    const float2 sx2 = make_float2(sxp, sxp);
+                    const float2 sxa = make_float2(xa * 262144.0f, xa * 262144.0f);
+                    const float2 sxb = make_float2(xb * 262144.0f, xb * 262144.0f);
+                    const float4* swv = reinterpret_cast<const float4*>(swb + tq * kSwStride);
+                    // 8 chunks of 32 columns; the TMEM load of chunk c+1 overlaps the math of c
+                    uint32_t d0[16], d1[16];
+                    dev::tmem_ld16x256b_x4(taddr, d0);
 #pragma unroll
-                    for (int chunk = 0; chunk < 4; ++chunk) {
-                        uint32_t d[32];
-                        dev::tmem_ld32(taddr + chunk * 32, d);
-                        dev::tmem_ld_wait();
-                        const float4* sw4 = reinterpret_cast<const float4*>(swb + h * 128 + chunk * 32);
+                    for (int c = 0; c < 8; ++c) {
+                        const float4 f0 = swv[2 * c], f1 = swv[2 * c + 1];   // column pairs g = 4c..4c+3
+                        uint32_t (&dc)[16] = (c & 1) ? d1 : d0;
+                        uint32_t (&dn)[16] = (c & 1) ? d0 : d1;
+                        dev::tmem_ld_wait16(dc);
+                        if (c < 7) dev::tmem_ld16x256b_x4(taddr + (c + 1) * 32, dn);
+                        const float2 swp[4] = {make_float2(f0.x, f0.y), make_float2(f0.z, f0.w),
+                                               make_float2(f1.x, f1.y), make_float2(f1.z, f1.w)};
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const float4 w4 = sw4[j];
-                            const float2 c01 = dev::fmul2(make_float2(w4.x, w4.y), sx2);
-                            const float2 c23 = dev::fmul2(make_float2(w4.z, w4.w), sx2);
-                            float2& a01 = acc[chunk * 16 + 2 * j];
-                            float2& a23 = acc[chunk * 16 + 2 * j + 1];
-                            a01 = dev::ffma2(make_float2(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1])), c01, a01);
-                            a23 = dev::ffma2(make_float2(__uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3])), c23, a23);
+                        for (int i = 0; i < 4; ++i) {
+                            const int g = 4 * c + i;
+                            const float2 ca = dev::fmul2(swp[i], sxa);
+                            const float2 cb = dev::fmul2(swp[i], sxb);
+                            accA[g] = dev::ffma2(make_float2(__uint_as_float(dc[4 * i]), __uint_as_float(dc[4 * i + 1])), ca, accA[g]);
+                            accB[g] = dev::ffma2(make_float2(__uint_as_float(dc[4 * i + 2]), __uint_as_float(dc[4 * i + 3])), cb, accB[g]);
                         }
                     }
                 } else {
                     // export exact partial sums of the requested window
 #pragma unroll 1
-                    for (int chunk = 0; chunk < 4; ++chunk) {
-                        uint32_t d[32];
-                        dev::tmem_ld32(taddr + chunk * 32, d);
-                        dev::tmem_ld_wait();
-                        if (row_ok && row >= p.pm0 && row < p.pm0 + p.pmcount) {
-                            for (int j = 0; j < 32; ++j) {
-                                const int n = n0 + h * 128 + chunk * 32 + j;
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t d[16];
+                        dev::tmem_ld16x256b_x4(taddr + c * 32, d);
+                        dev::tmem_ld_wait16(d);
+                        for (int i = 0; i < 4; ++i) {
+                            for (int e = 0; e < 4; ++e) {
+                                const int row = (e < 2) ? row0 : row1;
+                                const int n = n0 + 8 * (4 * c + i) + 2 * tq + (e & 1);
+                                if (row >= p.M || row < p.pm0 || row >= p.pm0 + p.pmcount) continue;
                                 if (n < p.pn0 || n >= p.pn0 + p.pncount || n >= p.N) continue;
                                 p.P[(static_cast<int64_t>(row - p.pm0) * p.pncount + (n - p.pn0)) * p.nb + b] =
-                                    __float2int_rn(__uint_as_float(d[j]) * 262144.0f);
+                                    __float2int_rn(__uint_as_float(d[4 * i + e]) * 262144.0f);
                             }
                         }
                     }
@@ -316,36 +357,27 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, int warp
             if (lane == 0 && ok) dev::mbar_arrive(&s.acc_empty[ab]);
         }
         if constexpr (!kPartials) {
-            const int cbase = n0 + h * 128;
-            if (p.splits == 1) {
-                if (row_ok) {
-                    uint16_t* yrow = p.Y + static_cast<int64_t>(row) * p.ldy;
+            auto store_rows = [&]() {
 #pragma unroll
-                    for (int c8 = 0; c8 < 16; ++c8) {
-                        const int col = cbase + c8 * 8;
-                        if (col < p.N) {
-                            uint4 o;
-                            __half2 h0 = __floats2half2_rn(acc[c8 * 4 + 0].x, acc[c8 * 4 + 0].y);
-                            __half2 h1 = __floats2half2_rn(acc[c8 * 4 + 1].x, acc[c8 * 4 + 1].y);
-                            __half2 h2 = __floats2half2_rn(acc[c8 * 4 + 2].x, acc[c8 * 4 + 2].y);
-                            __half2 h3 = __floats2half2_rn(acc[c8 * 4 + 3].x, acc[c8 * 4 + 3].y);
-                            o.x = *reinterpret_cast<uint32_t*>(&h0);
-                            o.y = *reinterpret_cast<uint32_t*>(&h1);
-                            o.z = *reinterpret_cast<uint32_t*>(&h2);
-                            o.w = *reinterpret_cast<uint32_t*>(&h3);
-                            *reinterpret_cast<uint4*>(yrow + col) = o;
-                        }
+                for (int g = 0; g < 32; ++g) {
+                    const int col = n0 + 8 * g + 2 * tq;
+                    if (col < p.N) {
+                        if (ok0) *reinterpret_cast<__half2*>(p.Y + static_cast<int64_t>(row0) * p.ldy + col) = __floats2half2_rn(accA[g].x, accA[g].y);
+                        if (ok1) *reinterpret_cast<__half2*>(p.Y + static_cast<int64_t>(row1) * p.ldy + col) = __floats2half2_rn(accB[g].x, accB[g].y);
                     }
                 }
+            };
+            if (p.splits == 1) {
+                store_rows();
             } else {
                 // split-K: publish this split's FP32 partial; the last split to arrive sums
                 // all of them in split order (deterministic) and writes Y.
-                float* part = p.ws_partial +
-                              ((static_cast<int64_t>(t.tile) * p.splits + t.split) * kTileM + q * 32 + lane) * kTileN + h * 128;
-                if (row_ok) {
+                float* base = p.ws_partial + (static_cast<int64_t>(t.tile) * p.splits + t.split) * kTileM * kTileN;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        __stcg(reinterpret_cast<float4*>(part) + i, make_float4(acc[2 * i].x, acc[2 * i].y, acc[2 * i + 1].x, acc[2 * i + 1].y));
+                for (int g = 0; g < 32; ++g) {
+                    const int cc = 8 * g + 2 * tq;
+                    __stcg(reinterpret_cast<float2*>(base + lr0 * kTileN + cc), accA[g]);
+                    __stcg(reinterpret_cast<float2*>(base + lr1 * kTileN + cc), accB[g]);
                 }
                 __threadfence();
                 dev::named_bar_sync(1, kEpiThreads);
@@ -360,40 +392,24 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, int warp
                     // every split (this one included) is in the workspace: sum in split order
                     __threadfence();
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) acc[i] = make_float2(0.f, 0.f);
-                    if (row_ok) {
-                        for (int sp = 0; sp < p.splits; ++sp) {
-                            const float* o = p.ws_partial +
-                                             ((static_cast<int64_t>(t.tile) * p.splits + sp) * kTileM + q * 32 + lane) * kTileN + h * 128;
+                    for (int g = 0; g < 32; ++g) {
+                        accA[g] = make_float2(0.f, 0.f);
+                        accB[g] = make_float2(0.f, 0.f);
+                    }
+                    for (int sp = 0; sp < p.splits; ++sp) {
+                        const float* o = p.ws_partial + (static_cast<int64_t>(t.tile) * p.splits + sp) * kTileM * kTileN;
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) {
-                                const float4 f = __ldcg(reinterpret_cast<const float4*>(o) + i);
-                                acc[2 * i].x += f.x;
-                                acc[2 * i].y += f.y;
-                                acc[2 * i + 1].x += f.z;
-                                acc[2 * i + 1].y += f.w;
-                            }
+                        for (int g = 0; g < 32; ++g) {
+                            const int cc = 8 * g + 2 * tq;
+                            const float2 fa = __ldcg(reinterpret_cast<const float2*>(o + lr0 * kTileN + cc));
+                            const float2 fb = __ldcg(reinterpret_cast<const float2*>(o + lr1 * kTileN + cc));
+                            accA[g].x += fa.x;
+                            accA[g].y += fa.y;
+                            accB[g].x += fb.x;
+                            accB[g].y += fb.y;
                         }
                     }
-                    if (row_ok) {
-                        uint16_t* yrow = p.Y + static_cast<int64_t>(row) * p.ldy;
-#pragma unroll
-                        for (int c8 = 0; c8 < 16; ++c8) {
-                            const int col = cbase + c8 * 8;
-                            if (col < p.N) {
-                                uint4 o;
-                                __half2 h0 = __floats2half2_rn(acc[c8 * 4 + 0].x, acc[c8 * 4 + 0].y);
-                                __half2 h1 = __floats2half2_rn(acc[c8 * 4 + 1].x, acc[c8 * 4 + 1].y);
-                                __half2 h2 = __floats2half2_rn(acc[c8 * 4 + 2].x, acc[c8 * 4 + 2].y);
-                                __half2 h3 = __floats2half2_rn(acc[c8 * 4 + 3].x, acc[c8 * 4 + 3].y);
-                                o.x = *reinterpret_cast<uint32_t*>(&h0);
-                                o.y = *reinterpret_cast<uint32_t*>(&h1);
-                                o.z = *reinterpret_cast<uint32_t*>(&h2);
-                                o.w = *reinterpret_cast<uint32_t*>(&h3);
-                                *reinterpret_cast<uint4*>(yrow + col) = o;
-                            }
-                        }
-                    }
+                    store_rows();
                 }
             }
         }
