@@ -25,7 +25,8 @@
 // Warp roles (512 threads, one CTA per SM, persistent over tiles):
 //   warp 0       TMA producer: activation code planes per block (bulk copies)
 //   warp 1       tcgen05 MMA issuer (one thread) + TMEM owner
-//   warps 2-7    converters: packed weight codes (global) -> 128B-swizzled E4M3 tile (smem)
+//   warps 2-7    converters: packed weight codes (global) -> 128B-swizzled E4M3 tile (smem),
+//                and the block's scales -> fp32 scale slot for the epilogue
 //   warps 8-15   epilogue: per-block FP32 scale-and-sum, fp16 output (or split-K partials)
 #include <cuda_fp16.h>
 
@@ -38,6 +39,7 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kStages = 3;    // activation stages (two plane slots each)
 constexpr int kCvStages = 3;  // converted weight tiles
+constexpr int kScStages = 4;  // per-block scales staged for the epilogue
 constexpr int kConvWarps = 6;
 constexpr int kConvThreads = kConvWarps * 32;
 constexpr int kEpiWarps = 8;
@@ -49,12 +51,18 @@ constexpr uint32_t kIdesc = dev::idesc_e4m3_f32(128, 256);
 // rows of 68 floats put the four c groups' 16-byte reads in distinct banks.
 constexpr int kSwStride = 68;
 
+struct ScaleSlot {
+    float sw[4 * kSwStride];  // weight scales of the tile's 256 columns (permuted, see above)
+    float sx[128];            // activation scales of the tile's 128 rows, times 2^18
+};
+
 struct __align__(1024) Smem {
     uint8_t opA[kStages][2][128 * 128];  // activation code planes (operand-ready, swizzled)
     uint8_t cvB[kCvStages][256 * 128];   // E4M3 weight operand (256 rows x 128 K), swizzled
-    float sw[2][4 * kSwStride];          // per-block weight scales (fp32), permuted
+    ScaleSlot sc[kScStages];             // per-block scales (fp32) for the epilogue
     uint64_t st_full[kStages], st_empty[kStages];
     uint64_t cv_full[kCvStages], cv_empty[kCvStages];
+    uint64_t sc_full[kScStages], sc_empty[kScStages];
     uint64_t acc_full[2], acc_empty[2];
     uint64_t mma_done;
     uint32_t tmem_base;
@@ -201,22 +209,38 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, int war
     const bool extra = ct + kFull * kConvThreads < 1024;      // a 6th for the first 64
     constexpr int kRowStep = kConvThreads / 4;                // 48 rows between a thread's pieces
 
+    // scales of the block: thread ct stages entries ct and ct + 192 of [256 weight scales |
+    // 128 activation scales]
+    const int i0 = ct, i1 = ct + kConvThreads;
+    const int sw_dst0 = ((i0 & 7) >> 1) * kSwStride + (i0 >> 3) * 2 + (i0 & 1);
+    const int sw_dst1 = i1 < 256 ? ((i1 & 7) >> 1) * kSwStride + (i1 >> 3) * 2 + (i1 & 1) : 0;
+
     int u = blockIdx.x;
     if (u >= num_units) return;
     Unit t = unit_of(p, u);
     int b = t.b0;
     uint4 w[kFull + 1];
+    uint16_t sc0 = 0, sc1 = 0;
     auto load = [&](const Unit& tt, int bb) {
         const uint8_t* g = p.W + (static_cast<int64_t>(tt.nt) * p.nb + bb) * (256 * 64) + src0;
 #pragma unroll
         for (int k = 0; k < kFull; ++k) w[k] = __ldg(reinterpret_cast<const uint4*>(g + k * kRowStep * 64));
         if (extra) w[kFull] = __ldg(reinterpret_cast<const uint4*>(g + kFull * kRowStep * 64));
+        const int n0 = tt.nt * kTileN, m0 = tt.mt * kTileM;
+        sc0 = (n0 + i0 < p.N) ? __ldg(p.w_scales + static_cast<int64_t>(bb) * p.N + n0 + i0) : uint16_t(0);
+        if (i1 < 256)
+            sc1 = (n0 + i1 < p.N) ? __ldg(p.w_scales + static_cast<int64_t>(bb) * p.N + n0 + i1) : uint16_t(0);
+        else
+            sc1 = (m0 + i1 - 256 < p.M) ? __ldg(p.a_scales + static_cast<int64_t>(bb) * p.M + m0 + i1 - 256) : uint16_t(0);
     };
     load(t, b);
     bool ok = true;
     for (uint32_t it = 0;; ++it) {
         const int cs = it % kCvStages;
-        if (lane == 0) ok = dev::mbar_wait(&s.cv_empty[cs], ((it / kCvStages) & 1) ^ 1, abort_flag);
+        const int ss = it % kScStages;
+        if (lane == 0)
+            ok = dev::mbar_wait(&s.cv_empty[cs], ((it / kCvStages) & 1) ^ 1, abort_flag) &&
+                 dev::mbar_wait(&s.sc_empty[ss], ((it / kScStages) & 1) ^ 1, abort_flag);
         ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
         if (!ok) break;
         uint8_t* dst = s.cvB[cs];
@@ -228,9 +252,18 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, int war
                 *reinterpret_cast<uint4*>(dst + dstB + k * kRowStep * 128) = make_uint4(lo4(v.z), hi4(v.z), lo4(v.w), hi4(v.w));
             }
         }
+        ScaleSlot& sl = s.sc[ss];
+        sl.sw[sw_dst0] = __half2float(__ushort_as_half(sc0));
+        if (i1 < 256)
+            sl.sw[sw_dst1] = __half2float(__ushort_as_half(sc1));
+        else
+            sl.sx[i1 - 256] = __half2float(__ushort_as_half(sc1)) * 262144.0f;   // 2^18 undoes the operand encoding
         dev::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) dev::mbar_arrive(&s.cv_full[cs]);
+        if (lane == 0) {
+            dev::mbar_arrive(&s.cv_full[cs]);
+            dev::mbar_arrive(&s.sc_full[ss]);
+        }
         // next block
         if (++b == t.b1) {
             u += gridDim.x;
@@ -260,8 +293,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, int warp
     const int slab = q * 32 + (ew >> 2) * 16;        // first tile row of this warp
     const int tq = lane & 3, tr = lane >> 2;
     const int lr0 = slab + tr, lr1 = slab + tr + 8;  // this thread's tile rows
-    const int et = ew * 32 + lane;                   // staging column 0..255
-    const int st_idx = ((et & 7) >> 1) * kSwStride + (et >> 3) * 2 + (et & 1);
+    const int et = ew * 32 + lane;                   // 0..255
     const uint32_t lane_addr = static_cast<uint32_t>(slab) << 16;
     uint32_t v = 0;
     bool ok = true;
@@ -276,41 +308,25 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, int warp
             accA[g] = make_float2(0.f, 0.f);
             accB[g] = make_float2(0.f, 0.f);
         }
-        // scales are fetched two blocks ahead (global loads outlast a block's epilogue)
-        const int ncol = n0 + et;
-        auto load_sw = [&](int b) -> float {
-            return (b < t.b1 && ncol < p.N) ? __half2float(__ushort_as_half(__ldg(p.w_scales + static_cast<int64_t>(b) * p.N + ncol))) : 0.f;
-        };
-        auto load_sx = [&](int b, int row, bool rok) -> float {
-            return (b < t.b1 && rok) ? __half2float(__ushort_as_half(__ldg(p.a_scales + static_cast<int64_t>(b) * p.M + row))) : 0.f;
-        };
-        float sw1 = load_sw(t.b0), sw2 = load_sw(t.b0 + 1);
-        float xa1 = load_sx(t.b0, row0, ok0), xa2 = load_sx(t.b0 + 1, row0, ok0);
-        float xb1 = load_sx(t.b0, row1, ok1), xb2 = load_sx(t.b0 + 1, row1, ok1);
         for (int b = t.b0; b < t.b1; ++b, ++v) {
-            const float sw_cur = sw1, xa = xa1, xb = xb1;
-            sw1 = sw2;
-            xa1 = xa2;
-            xb1 = xb2;
-            sw2 = load_sw(b + 2);
-            xa2 = load_sx(b + 2, row0, ok0);
-            xb2 = load_sx(b + 2, row1, ok1);
-            float* swb = s.sw[v & 1];
-            swb[st_idx] = sw_cur;
-            dev::named_bar_sync(1, kEpiThreads);
             const int ab = v & 1;
+            const int ss = v % kScStages;
             if (ok) {
-                if (lane == 0) ok = dev::mbar_wait(&s.acc_full[ab], (v >> 1) & 1, abort_flag);
+                if (lane == 0)
+                    ok = dev::mbar_wait(&s.sc_full[ss], (v / kScStages) & 1, abort_flag) &&
+                         dev::mbar_wait(&s.acc_full[ab], (v >> 1) & 1, abort_flag);
                 ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                __syncwarp();   // orders lane 0's acquire before the other lanes' scale reads
             }
+            const ScaleSlot& sl = s.sc[ss];
             if (ok) {
                 dev::tc_fence_after();
                 const uint32_t taddr = tmem + lane_addr + ab * 256u;
                 if constexpr (!kPartials) {
-                    // 2^18 undoes the operand encoding (both operands carry 2^-9)
-                    const float2 sxa = make_float2(xa * 262144.0f, xa * 262144.0f);
-                    const float2 sxb = make_float2(xb * 262144.0f, xb * 262144.0f);
-                    const float4* swv = reinterpret_cast<const float4*>(swb + tq * kSwStride);
+                    const float xa = sl.sx[lr0], xb = sl.sx[lr1];   // include 2^18 (operand encoding)
+                    const float2 sxa = make_float2(xa, xa);
+                    const float2 sxb = make_float2(xb, xb);
+                    const float4* swv = reinterpret_cast<const float4*>(sl.sw + tq * kSwStride);
                     // 8 chunks of 32 columns; the TMEM load of chunk c+1 overlaps the math of c
                     uint32_t d0[16], d1[16];
                     dev::tmem_ld16x256b_x4(taddr, d0);
@@ -354,7 +370,10 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, int warp
                 dev::tc_fence_before();
             }
             __syncwarp();
-            if (lane == 0 && ok) dev::mbar_arrive(&s.acc_empty[ab]);
+            if (lane == 0 && ok) {
+                dev::mbar_arrive(&s.acc_empty[ab]);
+                dev::mbar_arrive(&s.sc_empty[ss]);
+            }
         }
         if constexpr (!kPartials) {
             auto store_rows = [&]() {
@@ -434,6 +453,10 @@ __global__ void __launch_bounds__(kThreads, 1) w4ax_gemm_kernel(const Params p) 
         for (int i = 0; i < kCvStages; ++i) {
             dev::mbar_init(&s.cv_full[i], kConvWarps);
             dev::mbar_init(&s.cv_empty[i], 1);
+        }
+        for (int i = 0; i < kScStages; ++i) {
+            dev::mbar_init(&s.sc_full[i], kConvWarps);
+            dev::mbar_init(&s.sc_empty[i], kEpiWarps);
         }
         for (int i = 0; i < 2; ++i) {
             dev::mbar_init(&s.acc_full[i], 1);
