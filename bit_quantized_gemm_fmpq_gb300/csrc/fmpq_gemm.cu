@@ -11,8 +11,8 @@
 //     128-row activation tile is one bulk copy straight into the operand ring. An INT8
 //     block has two planes (|q| mod 16 and the rest) that accumulate into the same TMEM
 //     tile, so every block ends in one FP32 tile P * 2^-18 (exact: |P| < 2^17).
-//   * INT4 weights stay 4-bit in HBM: converter warps read the packed words straight
-//     from global memory and turn each into 8 operand bytes with a mask and a rotate (the
+//   * INT4 weights stay 4-bit in HBM: converter warps take the packed words from a
+//     bulk-copy ring and turn each into 8 operand bytes with a mask and a rotate (the
 //     sign-magnitude byte s0000mmm is the E4M3 value (-1)^s * m * 2^-9) -- the
 //     restructured storage format that makes 4-bit -> 8-bit conversion a couple of
 //     instructions (COMET news article, section 3).
@@ -23,9 +23,9 @@
 //     acc += D * (w_scale[n] * a_scale[m] * 2^18) in FP32 registers (packed f32x2 math).
 //
 // Warp roles (512 threads, one CTA per SM, persistent over tiles):
-//   warp 0       TMA producer: activation code planes per block (bulk copies)
+//   warp 0       TMA producer: activation code planes and packed weight tiles (bulk copies)
 //   warp 1       tcgen05 MMA issuer (one thread) + TMEM owner
-//   warps 2-7    converters: packed weight codes (global) -> 128B-swizzled E4M3 tile (smem),
+//   warps 2-7    converters: packed weight codes -> 128B-swizzled E4M3 tile,
 //                and the block's scales -> fp32 scale slot for the epilogue
 //   warps 8-15   epilogue: per-block FP32 scale-and-sum, fp16 output (or split-K partials)
 #include <cuda_fp16.h>
@@ -37,8 +37,10 @@ namespace fmpq {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kStages = 3;    // activation stages (two plane slots each)
-constexpr int kCvStages = 3;  // converted weight tiles
+constexpr int kASlots = 6;    // activation plane slots (an INT4 block takes one, INT8 two)
+constexpr int kWStages = 3;   // packed weight tiles (bulk copies)
+constexpr int kCvStages = 2;  // converted weight tiles
+constexpr int kGroupM = 8;    // tile order: bands of 8 m-tiles, n-tiles inside a band
 constexpr int kScStages = 4;  // per-block scales staged for the epilogue
 constexpr int kConvWarps = 6;
 constexpr int kConvThreads = kConvWarps * 32;
@@ -57,10 +59,12 @@ struct ScaleSlot {
 };
 
 struct __align__(1024) Smem {
-    uint8_t opA[kStages][2][128 * 128];  // activation code planes (operand-ready, swizzled)
+    uint8_t opA[kASlots][128 * 128];     // activation code planes (operand-ready, swizzled)
     uint8_t cvB[kCvStages][256 * 128];   // E4M3 weight operand (256 rows x 128 K), swizzled
+    uint8_t pkW[kWStages][256 * 64];     // packed weight codes
     ScaleSlot sc[kScStages];             // per-block scales (fp32) for the epilogue
-    uint64_t st_full[kStages], st_empty[kStages];
+    uint64_t a_full[kASlots], a_empty[kASlots];
+    uint64_t w_full[kWStages], w_empty[kWStages];
     uint64_t cv_full[kCvStages], cv_empty[kCvStages];
     uint64_t sc_full[kScStages], sc_empty[kScStages];
     uint64_t acc_full[2], acc_empty[2];
@@ -94,8 +98,9 @@ struct Params {
 __device__ __forceinline__ uint32_t lo4(uint32_t w) { return w & 0x87878787u; }
 __device__ __forceinline__ uint32_t hi4(uint32_t w) { return __funnelshift_r(w, w, 4) & 0x87878787u; }
 
-// Work unit u -> (tile, split). Tiles are ordered m-fastest so the CTAs running together
-// share weight panels in L2.
+// Work unit u -> (tile, split). Tiles run in bands of kGroupM m-tiles; inside a band the
+// m-tile varies fastest, so the CTAs running together (a band of 8 m-tiles x ~19 n-tiles
+// on 152 SMs) share activation and weight blocks in L2.
 struct Unit {
     int mt, nt, tile, split, b0, b1;
 };
@@ -103,8 +108,11 @@ __device__ __forceinline__ Unit unit_of(const Params& p, int u) {
     Unit r;
     r.tile = u / p.splits;
     r.split = u % p.splits;
-    r.mt = p.mt0 + r.tile % p.mtiles;
-    r.nt = p.nt0 + r.tile / p.mtiles;
+    const int band = r.tile / (kGroupM * p.ntiles);
+    const int in_band = r.tile - band * kGroupM * p.ntiles;
+    const int gm = min(kGroupM, p.mtiles - band * kGroupM);   // m-tiles in this band
+    r.mt = p.mt0 + band * kGroupM + in_band % gm;
+    r.nt = p.nt0 + in_band / gm;
     r.b0 = static_cast<int>((static_cast<int64_t>(r.split) * p.nb) / p.splits);
     r.b1 = static_cast<int>((static_cast<int64_t>(r.split + 1) * p.nb) / p.splits);
     return r;
@@ -114,24 +122,32 @@ __device__ __forceinline__ Unit unit_of(const Params& p, int u) {
 __device__ __forceinline__ void producer_role(const Params& p, Smem& s, int lane, volatile int* abort_flag) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
     if (lane == 0) {
-        uint32_t it = 0;
+        uint32_t pc = 0, wc = 0;   // planes and weight tiles issued
         bool ok = true;
         const int64_t plane_bytes = static_cast<int64_t>(p.M) * kBlock;
         for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
             const Unit t = unit_of(p, u);
             const int m0 = t.mt * kTileM;
             const uint32_t abytes = static_cast<uint32_t>(min(kTileM, p.M - m0)) * kBlock;
-            for (int b = t.b0; b < t.b1; ++b, ++it) {
-                const int st = it % kStages;
-                if (!dev::mbar_wait(&s.st_empty[st], ((it / kStages) & 1) ^ 1, abort_flag)) {
+            for (int b = t.b0; ok && b < t.b1; ++b, ++wc) {
+                const int ws = wc % kWStages;
+                if (!dev::mbar_wait(&s.w_empty[ws], ((wc / kWStages) & 1) ^ 1, abort_flag)) {
                     ok = false;
                     break;
                 }
+                dev::mbar_arrive_expect_tx(&s.w_full[ws], 256 * 64);
+                dev::bulk_g2s(s.pkW[ws], p.W + (static_cast<int64_t>(t.nt) * p.nb + b) * (256 * 64), 256 * 64, &s.w_full[ws]);
                 const int planes = p.mask[b] ? 2 : 1;
-                dev::mbar_arrive_expect_tx(&s.st_full[st], abytes * planes);
                 const uint8_t* a0 = p.A + static_cast<int64_t>(p.poff[b]) * plane_bytes + static_cast<int64_t>(m0) * kBlock;
-                dev::bulk_g2s(s.opA[st][0], a0, abytes, &s.st_full[st]);
-                if (planes == 2) dev::bulk_g2s(s.opA[st][1], a0 + plane_bytes, abytes, &s.st_full[st]);
+                for (int pl = 0; pl < planes; ++pl, ++pc) {
+                    const int sl = pc % kASlots;
+                    if (!dev::mbar_wait(&s.a_empty[sl], ((pc / kASlots) & 1) ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    dev::mbar_arrive_expect_tx(&s.a_full[sl], abytes);
+                    dev::bulk_g2s(s.opA[sl], a0 + pl * plane_bytes, abytes, &s.a_full[sl]);
+                }
             }
         }
         if (!ok) {
@@ -139,10 +155,15 @@ __device__ __forceinline__ void producer_role(const Params& p, Smem& s, int lane
             dev::report(p.status, dev::kStatusTimeout);
         }
         // drain copies in flight
-        for (int st = 0; st < kStages; ++st) {
-            if (it <= static_cast<uint32_t>(st)) break;
-            const uint32_t last = st + ((it - 1 - st) / kStages) * kStages;
-            dev::mbar_wait(&s.st_full[st], (last / kStages) & 1, nullptr);
+        for (int sl = 0; sl < kASlots; ++sl) {
+            if (pc <= static_cast<uint32_t>(sl)) break;
+            const uint32_t last = sl + ((pc - 1 - sl) / kASlots) * kASlots;
+            dev::mbar_wait(&s.a_full[sl], (last / kASlots) & 1, nullptr);
+        }
+        for (int ws = 0; ws < kWStages; ++ws) {
+            if (wc <= static_cast<uint32_t>(ws)) break;
+            const uint32_t last = ws + ((wc - 1 - ws) / kWStages) * kWStages;
+            dev::mbar_wait(&s.w_full[ws], (last / kWStages) & 1, nullptr);
         }
     }
 }
@@ -151,31 +172,35 @@ __device__ __forceinline__ void producer_role(const Params& p, Smem& s, int lane
 __device__ __forceinline__ void mma_role(const Params& p, Smem& s, int lane, uint32_t tmem, volatile int* abort_flag) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
     if (lane == 0) {
-        uint32_t it = 0;
+        uint32_t it = 0, pc = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
             const Unit t = unit_of(p, u);
-            for (int b = t.b0; b < t.b1; ++b, ++it) {
-                const int st = it % kStages;
+            for (int b = t.b0; ok && b < t.b1; ++b, ++it) {
                 const int cs = it % kCvStages;
                 const int ab = it & 1;
-                if (!dev::mbar_wait(&s.st_full[st], (it / kStages) & 1, abort_flag) ||
-                    !dev::mbar_wait(&s.cv_full[cs], (it / kCvStages) & 1, abort_flag) ||
+                const int planes = p.mask[b] ? 2 : 1;
+                if (!dev::mbar_wait(&s.cv_full[cs], (it / kCvStages) & 1, abort_flag) ||
                     !dev::mbar_wait(&s.acc_empty[ab], ((it >> 1) & 1) ^ 1, abort_flag)) {
                     ok = false;
                     break;
                 }
-                dev::tc_fence_after();
                 const uint64_t bd = dev::sdesc_k_sw128(dev::smem_u32(s.cvB[cs]));
                 const uint32_t d = tmem + static_cast<uint32_t>(ab) * 256u;
-                const int planes = p.mask[b] ? 2 : 1;
-                for (int pl = 0; pl < planes; ++pl) {
-                    const uint64_t ad = dev::sdesc_k_sw128(dev::smem_u32(s.opA[st][pl]));
+                for (int pl = 0; pl < planes; ++pl, ++pc) {
+                    const int sl = pc % kASlots;
+                    if (!dev::mbar_wait(&s.a_full[sl], (pc / kASlots) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    dev::tc_fence_after();
+                    const uint64_t ad = dev::sdesc_k_sw128(dev::smem_u32(s.opA[sl]));
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         dev::mma_e4m3(d, ad + 2 * k, bd + 2 * k, kIdesc, (pl > 0 || k > 0) ? 1u : 0u);
+                    dev::mma_commit(&s.a_empty[sl]);
                 }
-                dev::mma_commit(&s.st_empty[st]);
+                if (!ok) break;
                 dev::mma_commit(&s.cv_empty[cs]);
                 dev::mma_commit(&s.acc_full[ab]);
             }
@@ -195,8 +220,8 @@ __device__ __forceinline__ void mma_role(const Params& p, Smem& s, int lane, uin
 // i/4, bytes 16*(i%4).. of the row, i.e. 32 codes = two 16-byte operand chunks. Thread ct
 // converts pieces ct + 192k: 192 pieces = 48 rows, so the piece's column and the row's
 // swizzle phase (row mod 8) are the same for every k and all addresses are the thread's
-// base offsets plus constants. The next block's pieces are loaded from global memory while
-// the converter waits for a free operand slot.
+// base offsets plus constants. The converters also stage the block's scales (256 weight
+// scales, 128 activation scales) for the epilogue, fetched one block ahead.
 __device__ __forceinline__ void converter_role(const Params& p, Smem& s, int warp, int lane, volatile int* abort_flag) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
     const int ct = (warp - 2) * 32 + lane;
@@ -208,7 +233,6 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, int war
     constexpr int kFull = 1024 / kConvThreads;                // 5 pieces for every thread
     const bool extra = ct + kFull * kConvThreads < 1024;      // a 6th for the first 64
     constexpr int kRowStep = kConvThreads / 4;                // 48 rows between a thread's pieces
-
     // scales of the block: thread ct stages entries ct and ct + 192 of [256 weight scales |
     // 128 activation scales]
     const int i0 = ct, i1 = ct + kConvThreads;
@@ -219,13 +243,8 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, int war
     if (u >= num_units) return;
     Unit t = unit_of(p, u);
     int b = t.b0;
-    uint4 w[kFull + 1];
     uint16_t sc0 = 0, sc1 = 0;
-    auto load = [&](const Unit& tt, int bb) {
-        const uint8_t* g = p.W + (static_cast<int64_t>(tt.nt) * p.nb + bb) * (256 * 64) + src0;
-#pragma unroll
-        for (int k = 0; k < kFull; ++k) w[k] = __ldg(reinterpret_cast<const uint4*>(g + k * kRowStep * 64));
-        if (extra) w[kFull] = __ldg(reinterpret_cast<const uint4*>(g + kFull * kRowStep * 64));
+    auto load_scales = [&](const Unit& tt, int bb) {
         const int n0 = tt.nt * kTileN, m0 = tt.mt * kTileM;
         sc0 = (n0 + i0 < p.N) ? __ldg(p.w_scales + static_cast<int64_t>(bb) * p.N + n0 + i0) : uint16_t(0);
         if (i1 < 256)
@@ -233,17 +252,25 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, int war
         else
             sc1 = (m0 + i1 - 256 < p.M) ? __ldg(p.a_scales + static_cast<int64_t>(bb) * p.M + m0 + i1 - 256) : uint16_t(0);
     };
-    load(t, b);
+    load_scales(t, b);
     bool ok = true;
     for (uint32_t it = 0;; ++it) {
+        const int ws = it % kWStages;
         const int cs = it % kCvStages;
         const int ss = it % kScStages;
         if (lane == 0)
-            ok = dev::mbar_wait(&s.cv_empty[cs], ((it / kCvStages) & 1) ^ 1, abort_flag) &&
+            ok = dev::mbar_wait(&s.w_full[ws], (it / kWStages) & 1, abort_flag) &&
+                 dev::mbar_wait(&s.cv_empty[cs], ((it / kCvStages) & 1) ^ 1, abort_flag) &&
                  dev::mbar_wait(&s.sc_empty[ss], ((it / kScStages) & 1) ^ 1, abort_flag);
         ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
         if (!ok) break;
+        __syncwarp();   // orders lane 0's acquire of the weight tile before the other lanes' reads
+        const uint8_t* src = s.pkW[ws] + src0;
         uint8_t* dst = s.cvB[cs];
+        uint4 w[kFull + 1];
+#pragma unroll
+        for (int k = 0; k <= kFull; ++k)
+            if (k < kFull || extra) w[k] = *reinterpret_cast<const uint4*>(src + k * kRowStep * 64);
 #pragma unroll
         for (int k = 0; k <= kFull; ++k) {
             if (k < kFull || extra) {
@@ -261,6 +288,7 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, int war
         dev::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
+            dev::mbar_arrive(&s.w_empty[ws]);
             dev::mbar_arrive(&s.cv_full[cs]);
             dev::mbar_arrive(&s.sc_full[ss]);
         }
@@ -271,7 +299,7 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, int war
             t = unit_of(p, u);
             b = t.b0;
         }
-        load(t, b);
+        load_scales(t, b);
     }
     if (!ok && lane == 0) {
         *abort_flag = 1;
@@ -446,9 +474,13 @@ __global__ void __launch_bounds__(kThreads, 1) w4ax_gemm_kernel(const Params p) 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            dev::mbar_init(&s.st_full[i], 1);
-            dev::mbar_init(&s.st_empty[i], 1);
+        for (int i = 0; i < kASlots; ++i) {
+            dev::mbar_init(&s.a_full[i], 1);
+            dev::mbar_init(&s.a_empty[i], 1);
+        }
+        for (int i = 0; i < kWStages; ++i) {
+            dev::mbar_init(&s.w_full[i], 1);
+            dev::mbar_init(&s.w_empty[i], kConvWarps);
         }
         for (int i = 0; i < kCvStages; ++i) {
             dev::mbar_init(&s.cv_full[i], kConvWarps);
