@@ -22,11 +22,12 @@
 //     column pairs per thread, so each weight scale read serves two rows) and accumulate
 //     acc += D * (w_scale[n] * a_scale[m] * 2^18) in FP32 registers (packed f32x2 math).
 //
-// Warp roles (512 threads, one CTA per SM, persistent over tiles):
-//   warp 0       TMA producer: activation code planes and packed weight tiles (bulk copies)
-//   warp 1       tcgen05 MMA issuer (one thread) + TMEM owner
-//   warps 2-7    converters: packed weight codes -> 128B-swizzled E4M3 tile,
-//                and the block's scales -> fp32 scale slot for the epilogue
+// Warp roles (512 threads, one CTA per SM, persistent over pair tiles):
+//   warp 0       weight producer: this CTA's half of each packed weight tile (bulk copies)
+//   warp 1       even CTA: tcgen05 pair-MMA issuer; odd CTA: forwards operand readiness
+//   warps 2-5    converters: packed weight codes -> 128B-swizzled E4M3 half-tile, and the
+//                block's scales -> fp32 scale slot for the epilogue
+//   warp 6       activation producer: this CTA's 128 rows of each block's plane(s)
 //   warps 8-15   epilogue: per-block FP32 scale-and-sum, fp16 output (or split-K partials)
 #include <cuda_fp16.h>
 
@@ -37,17 +38,19 @@ namespace fmpq {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kASlots = 6;    // activation plane slots (an INT4 block takes one, INT8 two)
-constexpr int kWStages = 3;   // packed weight tiles (bulk copies)
-constexpr int kCvStages = 2;  // converted weight tiles
-constexpr int kGroupM = 8;    // tile order: bands of 8 m-tiles, n-tiles inside a band
+constexpr int kPairM = 256;   // rows of a pair tile (128 per CTA)
+constexpr int kASlots = 8;    // activation plane slots (an INT4 block takes one, INT8 two)
+constexpr int kWStages = 6;   // packed weight half-tiles (bulk copies)
+constexpr int kCvStages = 2;  // converted weight half-tiles
 constexpr int kScStages = 4;  // per-block scales staged for the epilogue
-constexpr int kConvWarps = 6;
+constexpr int kPeer = 4;      // odd-CTA readiness signals in flight to the even CTA
+constexpr int kGroupM = 4;    // tile order: bands of 4 pair m-tiles, n-tiles inside a band
+constexpr int kConvWarps = 4;
+constexpr int kConvWarp0 = 2;   // converters are warps 2..5; warp 6 issues the activation copies
 constexpr int kConvThreads = kConvWarps * 32;
 constexpr int kEpiWarps = 8;
-constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr uint32_t kTmemCols = 512;  // two 128 x 256 FP32 accumulators
-constexpr uint32_t kIdesc = dev::idesc_e4m3_f32(128, 256);
+constexpr uint32_t kTmemCols = 512;  // two 128 x 256 FP32 accumulators per CTA
+constexpr uint32_t kIdesc = dev::idesc_e4m3_f32(256, 256);
 // Weight scales of a block, staged for the epilogue: column n = 8g + 2c + j goes to
 // [c][2g + j]. Each epilogue thread reads the 64 values of its column pairs contiguously;
 // rows of 68 floats put the four c groups' 16-byte reads in distinct banks.
@@ -55,19 +58,20 @@ constexpr int kSwStride = 68;
 
 struct ScaleSlot {
     float sw[4 * kSwStride];  // weight scales of the tile's 256 columns (permuted, see above)
-    float sx[128];            // activation scales of the tile's 128 rows, times 2^18
+    float sx[128];            // activation scales of this CTA's 128 rows, times 2^18
 };
 
 struct __align__(1024) Smem {
     uint8_t opA[kASlots][128 * 128];     // activation code planes (operand-ready, swizzled)
-    uint8_t cvB[kCvStages][256 * 128];   // E4M3 weight operand (256 rows x 128 K), swizzled
-    uint8_t pkW[kWStages][256 * 64];     // packed weight codes
+    uint8_t cvB[kCvStages][128 * 128];   // E4M3 weight operand: this CTA's 128 rows x 128 K
+    uint8_t pkW[kWStages][128 * 64];     // packed weight codes of this CTA's 128 rows
     ScaleSlot sc[kScStages];             // per-block scales (fp32) for the epilogue
     uint64_t a_full[kASlots], a_empty[kASlots];
     uint64_t w_full[kWStages], w_empty[kWStages];
     uint64_t cv_full[kCvStages], cv_empty[kCvStages];
     uint64_t sc_full[kScStages], sc_empty[kScStages];
     uint64_t acc_full[2], acc_empty[2];
+    uint64_t peer_full[kPeer];
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -85,11 +89,11 @@ struct Params {
     const uint8_t* mask;
     const int32_t* poff;   // first code plane of each block
     int32_t* status;
-    // tiles: the kernel covers m-tiles [mt0, mt0 + mtiles) x n-tiles [nt0, nt0 + ntiles)
+    // pair tiles (256 x 256): m-tiles [mt0, mt0 + mtiles) x n-tiles [nt0, nt0 + ntiles)
     int mt0, mtiles, nt0, ntiles;
     int splits;            // K splits per tile (1 = none)
-    float* ws_partial;     // [tiles][splits][128][256] FP32 partial sums (splits > 1)
-    int32_t* ws_count;     // [tiles] arrival counters (zero between calls)
+    float* ws_partial;     // [tiles][splits][256][256] FP32 partial sums (splits > 1)
+    int32_t* ws_count;     // [tiles][2] arrival counters per CTA half (zero between calls)
     // partial-sum export
     int32_t* P;
     int pm0, pmcount, pn0, pncount;
@@ -98,9 +102,9 @@ struct Params {
 __device__ __forceinline__ uint32_t lo4(uint32_t w) { return w & 0x87878787u; }
 __device__ __forceinline__ uint32_t hi4(uint32_t w) { return __funnelshift_r(w, w, 4) & 0x87878787u; }
 
-// Work unit u -> (tile, split). Tiles run in bands of kGroupM m-tiles; inside a band the
-// m-tile varies fastest, so the CTAs running together (a band of 8 m-tiles x ~19 n-tiles
-// on 152 SMs) share activation and weight blocks in L2.
+// Work unit u -> (pair tile, split). Tiles run in bands of kGroupM m-tiles; inside a band
+// the m-tile varies fastest, so the pairs running together share activation and weight
+// blocks in L2.
 struct Unit {
     int mt, nt, tile, split, b0, b1;
 };
@@ -118,139 +122,163 @@ __device__ __forceinline__ Unit unit_of(const Params& p, int u) {
     return r;
 }
 
-// ---------------------------------------------------------------- TMA producer (warp 0)
-__device__ __forceinline__ void producer_role(const Params& p, Smem& s, int lane, volatile int* abort_flag) {
+__device__ __forceinline__ void fail(const Params& p, volatile int* abort_flag) {
+    *abort_flag = 1;
+    dev::report(p.status, dev::kStatusTimeout);
+}
+
+// ---------------------------------------------------------------- producers (warps 0 and 6)
+// Warp 0 streams this CTA's 128 rows (8 KB) of each block's packed weight tile; warp 6
+// streams this CTA's 128 activation rows of each block's plane(s). Separate threads, so the
+// activation prefetch depth is set by its own ring, not by the weight conversion.
+__device__ __forceinline__ void weight_producer(const Params& p, Smem& s, uint32_t rank, volatile int* abort_flag) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
-    if (lane == 0) {
-        uint32_t pc = 0, wc = 0;   // planes and weight tiles issued
-        bool ok = true;
-        const int64_t plane_bytes = static_cast<int64_t>(p.M) * kBlock;
-        for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
-            const Unit t = unit_of(p, u);
-            const int m0 = t.mt * kTileM;
-            const uint32_t abytes = static_cast<uint32_t>(min(kTileM, p.M - m0)) * kBlock;
-            for (int b = t.b0; ok && b < t.b1; ++b, ++wc) {
-                const int ws = wc % kWStages;
-                if (!dev::mbar_wait(&s.w_empty[ws], ((wc / kWStages) & 1) ^ 1, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                dev::mbar_arrive_expect_tx(&s.w_full[ws], 256 * 64);
-                dev::bulk_g2s(s.pkW[ws], p.W + (static_cast<int64_t>(t.nt) * p.nb + b) * (256 * 64), 256 * 64, &s.w_full[ws]);
-                const int planes = p.mask[b] ? 2 : 1;
-                const uint8_t* a0 = p.A + static_cast<int64_t>(p.poff[b]) * plane_bytes + static_cast<int64_t>(m0) * kBlock;
-                for (int pl = 0; pl < planes; ++pl, ++pc) {
-                    const int sl = pc % kASlots;
-                    if (!dev::mbar_wait(&s.a_empty[sl], ((pc / kASlots) & 1) ^ 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    dev::mbar_arrive_expect_tx(&s.a_full[sl], abytes);
-                    dev::bulk_g2s(s.opA[sl], a0 + pl * plane_bytes, abytes, &s.a_full[sl]);
-                }
+    uint32_t wc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x >> 1; ok && u < num_units; u += gridDim.x >> 1) {
+        const Unit t = unit_of(p, u);
+        for (int b = t.b0; b < t.b1; ++b, ++wc) {
+            const int ws = wc % kWStages;
+            if (!dev::mbar_wait(&s.w_empty[ws], ((wc / kWStages) & 1) ^ 1, abort_flag)) {
+                ok = false;
+                break;
             }
+            dev::mbar_arrive_expect_tx(&s.w_full[ws], 128 * 64);
+            dev::bulk_g2s(s.pkW[ws], p.W + (static_cast<int64_t>(t.nt) * p.nb + b) * (256 * 64) + rank * (128 * 64),
+                          128 * 64, &s.w_full[ws]);
         }
-        if (!ok) {
-            *abort_flag = 1;
-            dev::report(p.status, dev::kStatusTimeout);
-        }
-        // drain copies in flight
-        for (int sl = 0; sl < kASlots; ++sl) {
-            if (pc <= static_cast<uint32_t>(sl)) break;
-            const uint32_t last = sl + ((pc - 1 - sl) / kASlots) * kASlots;
-            dev::mbar_wait(&s.a_full[sl], (last / kASlots) & 1, nullptr);
-        }
-        for (int ws = 0; ws < kWStages; ++ws) {
-            if (wc <= static_cast<uint32_t>(ws)) break;
-            const uint32_t last = ws + ((wc - 1 - ws) / kWStages) * kWStages;
-            dev::mbar_wait(&s.w_full[ws], (last / kWStages) & 1, nullptr);
-        }
+    }
+    if (!ok) fail(p, abort_flag);
+    for (int ws = 0; ws < kWStages; ++ws) {   // drain copies in flight
+        if (wc <= static_cast<uint32_t>(ws)) break;
+        const uint32_t last = ws + ((wc - 1 - ws) / kWStages) * kWStages;
+        dev::mbar_wait(&s.w_full[ws], (last / kWStages) & 1, nullptr);
     }
 }
 
-// ---------------------------------------------------------------- MMA issuer (warp 1)
-__device__ __forceinline__ void mma_role(const Params& p, Smem& s, int lane, uint32_t tmem, volatile int* abort_flag) {
+__device__ __forceinline__ void activation_producer(const Params& p, Smem& s, uint32_t rank,
+                                                    volatile int* abort_flag) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
-    if (lane == 0) {
-        uint32_t it = 0, pc = 0;
-        bool ok = true;
-        for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
-            const Unit t = unit_of(p, u);
-            for (int b = t.b0; ok && b < t.b1; ++b, ++it) {
-                const int cs = it % kCvStages;
-                const int ab = it & 1;
-                const int planes = p.mask[b] ? 2 : 1;
-                if (!dev::mbar_wait(&s.cv_full[cs], (it / kCvStages) & 1, abort_flag) ||
-                    !dev::mbar_wait(&s.acc_empty[ab], ((it >> 1) & 1) ^ 1, abort_flag)) {
+    uint32_t pc = 0;
+    bool ok = true;
+    const int64_t plane_bytes = static_cast<int64_t>(p.M) * kBlock;
+    for (int u = blockIdx.x >> 1; ok && u < num_units; u += gridDim.x >> 1) {
+        const Unit t = unit_of(p, u);
+        const int r0 = t.mt * kPairM + static_cast<int>(rank) * 128;
+        const uint32_t abytes = static_cast<uint32_t>(max(0, min(128, p.M - r0))) * kBlock;
+        for (int b = t.b0; ok && b < t.b1; ++b) {
+            const int planes = p.mask[b] ? 2 : 1;
+            const uint8_t* a0 = p.A + static_cast<int64_t>(p.poff[b]) * plane_bytes + static_cast<int64_t>(r0) * kBlock;
+            for (int pl = 0; pl < planes; ++pl, ++pc) {
+                const int sl = pc % kASlots;
+                if (!dev::mbar_wait(&s.a_empty[sl], ((pc / kASlots) & 1) ^ 1, abort_flag)) {
                     ok = false;
                     break;
                 }
-                const uint64_t bd = dev::sdesc_k_sw128(dev::smem_u32(s.cvB[cs]));
-                const uint32_t d = tmem + static_cast<uint32_t>(ab) * 256u;
-                for (int pl = 0; pl < planes; ++pl, ++pc) {
-                    const int sl = pc % kASlots;
-                    if (!dev::mbar_wait(&s.a_full[sl], (pc / kASlots) & 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    dev::tc_fence_after();
-                    const uint64_t ad = dev::sdesc_k_sw128(dev::smem_u32(s.opA[sl]));
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        dev::mma_e4m3(d, ad + 2 * k, bd + 2 * k, kIdesc, (pl > 0 || k > 0) ? 1u : 0u);
-                    dev::mma_commit(&s.a_empty[sl]);
-                }
-                if (!ok) break;
-                dev::mma_commit(&s.cv_empty[cs]);
-                dev::mma_commit(&s.acc_full[ab]);
+                dev::mbar_arrive_expect_tx(&s.a_full[sl], abytes);   // rows past M: nothing to copy
+                if (abytes > 0) dev::bulk_g2s(s.opA[sl], a0 + pl * plane_bytes, abytes, &s.a_full[sl]);
             }
         }
-        if (!ok) {
-            *abort_flag = 1;
-            dev::report(p.status, dev::kStatusTimeout);
+    }
+    if (!ok) fail(p, abort_flag);
+    for (int sl = 0; sl < kASlots; ++sl) {   // drain copies in flight
+        if (pc <= static_cast<uint32_t>(sl)) break;
+        const uint32_t last = sl + ((pc - 1 - sl) / kASlots) * kASlots;
+        dev::mbar_wait(&s.a_full[sl], (last / kASlots) & 1, nullptr);
+    }
+}
+
+// ---------------------------------------------------------------- MMA issuer / forwarder (warp 1)
+// Even CTA: issues the pair MMAs once its own operands, the odd CTA's operands (signalled
+// on peer_full) and a free accumulator (released by both CTAs' epilogues) are ready, and
+// commits to the barriers of both CTAs. Odd CTA: forwards the readiness of its operands.
+__device__ __forceinline__ void mma_role(const Params& p, Smem& s, uint32_t rank, int lane, uint32_t tmem,
+                                         volatile int* abort_flag) {
+    const int num_units = p.mtiles * p.ntiles * p.splits;
+    if (lane != 0) return;
+    uint32_t it = 0, pc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x >> 1; ok && u < num_units; u += gridDim.x >> 1) {
+        const Unit t = unit_of(p, u);
+        for (int b = t.b0; ok && b < t.b1; ++b, ++it) {
+            const int cs = it % kCvStages;
+            const int planes = p.mask[b] ? 2 : 1;
+            if (rank != 0) {
+                ok = dev::mbar_wait(&s.cv_full[cs], (it / kCvStages) & 1, abort_flag);
+                for (int pl = 0; ok && pl < planes; ++pl, ++pc)
+                    ok = dev::mbar_wait(&s.a_full[pc % kASlots], (pc / kASlots) & 1, abort_flag);
+                if (!ok) break;
+                dev::mbar_arrive_remote(dev::mapa(&s.peer_full[it % kPeer], 0));
+                continue;
+            }
+            const int ab = it & 1;
+            if (!dev::mbar_wait(&s.cv_full[cs], (it / kCvStages) & 1, abort_flag) ||
+                !dev::mbar_wait(&s.peer_full[it % kPeer], (it / kPeer) & 1, abort_flag) ||
+                !dev::mbar_wait(&s.acc_empty[ab], ((it >> 1) & 1) ^ 1, abort_flag)) {
+                ok = false;
+                break;
+            }
+            const uint64_t bd = dev::sdesc_k_sw128(dev::smem_u32(s.cvB[cs]));
+            const uint32_t d = tmem + static_cast<uint32_t>(ab) * 256u;
+            for (int pl = 0; pl < planes; ++pl, ++pc) {
+                const int sl = pc % kASlots;
+                if (!dev::mbar_wait(&s.a_full[sl], (pc / kASlots) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                dev::tc_fence_after();
+                const uint64_t ad = dev::sdesc_k_sw128(dev::smem_u32(s.opA[sl]));
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    dev::mma_e4m3_pair(d, ad + 2 * k, bd + 2 * k, kIdesc, (pl > 0 || k > 0) ? 1u : 0u);
+                dev::mma_commit_pair(&s.a_empty[sl]);
+            }
+            if (!ok) break;
+            dev::mma_commit_pair(&s.cv_empty[cs]);
+            dev::mma_commit_pair(&s.acc_full[ab]);
         }
+    }
+    if (!ok) fail(p, abort_flag);
+    if (rank == 0) {
         // every MMA issued must finish before TMEM is released
-        dev::mma_commit(&s.mma_done);
+        dev::mma_commit_pair(&s.mma_done);
         dev::mbar_wait(&s.mma_done, 0, nullptr);
     }
 }
 
-// ---------------------------------------------------------------- converters (warps 2-7)
-// A weight tile (256 rows x 64 packed bytes) is 1024 pieces of 16 bytes; piece i is row
-// i/4, bytes 16*(i%4).. of the row, i.e. 32 codes = two 16-byte operand chunks. Thread ct
-// converts pieces ct + 192k: 192 pieces = 48 rows, so the piece's column and the row's
-// swizzle phase (row mod 8) are the same for every k and all addresses are the thread's
-// base offsets plus constants. The converters also stage the block's scales (256 weight
-// scales, 128 activation scales) for the epilogue, fetched one block ahead.
-__device__ __forceinline__ void converter_role(const Params& p, Smem& s, int warp, int lane, volatile int* abort_flag) {
+// ---------------------------------------------------------------- converters (warps 2-5)
+// The CTA's half of a weight tile (128 rows x 64 packed bytes) is 512 pieces of 16 bytes;
+// piece i is row i/4, bytes 16*(i%4).. of the row, i.e. 32 codes = two 16-byte operand
+// chunks. Thread ct (0..127) converts pieces ct + 128k, k = 0..3: 128 pieces = 32 rows, so
+// the piece's column and the row's swizzle phase (row mod 8) are the same for every k and
+// all addresses are the thread's base offsets plus constants. The converters also stage the
+// block's scales -- entries ct, ct + 128, ct + 256 of [256 weight scales | this CTA's 128
+// activation scales] -- for the epilogue, fetched one block ahead.
+__device__ __forceinline__ void converter_role(const Params& p, Smem& s, uint32_t rank, int warp, int lane,
+                                               volatile int* abort_flag) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
-    const int ct = (warp - 2) * 32 + lane;
+    const int ct = (warp - kConvWarp0) * 32 + lane;
     const int r0 = ct >> 2, c4 = ct & 3;
     const uint32_t phase = static_cast<uint32_t>(r0 & 7);
     const uint32_t src0 = static_cast<uint32_t>(r0 * 64 + c4 * 16);
     const uint32_t dstA = static_cast<uint32_t>(r0 * 128) + (((2u * c4) ^ phase) << 4);
     const uint32_t dstB = static_cast<uint32_t>(r0 * 128) + (((2u * c4 + 1u) ^ phase) << 4);
-    constexpr int kFull = 1024 / kConvThreads;                // 5 pieces for every thread
-    const bool extra = ct + kFull * kConvThreads < 1024;      // a 6th for the first 64
-    constexpr int kRowStep = kConvThreads / 4;                // 48 rows between a thread's pieces
-    // scales of the block: thread ct stages entries ct and ct + 192 of [256 weight scales |
-    // 128 activation scales]
-    const int i0 = ct, i1 = ct + kConvThreads;
-    const int sw_dst0 = ((i0 & 7) >> 1) * kSwStride + (i0 >> 3) * 2 + (i0 & 1);
-    const int sw_dst1 = i1 < 256 ? ((i1 & 7) >> 1) * kSwStride + (i1 >> 3) * 2 + (i1 & 1) : 0;
+    constexpr int kPieces = 512 / kConvThreads;               // 4 pieces per thread
+    constexpr int kRowStep = kConvThreads / 4;                // 32 rows between a thread's pieces
+    auto sw_pos = [](int i) { return ((i & 7) >> 1) * kSwStride + (i >> 3) * 2 + (i & 1); };
+    const int swd0 = sw_pos(ct), swd1 = sw_pos(ct + 128);
 
-    int u = blockIdx.x;
+    int u = blockIdx.x >> 1;
     if (u >= num_units) return;
     Unit t = unit_of(p, u);
     int b = t.b0;
-    uint16_t sc0 = 0, sc1 = 0;
+    uint16_t sc0 = 0, sc1 = 0, sc2 = 0;
     auto load_scales = [&](const Unit& tt, int bb) {
-        const int n0 = tt.nt * kTileN, m0 = tt.mt * kTileM;
-        sc0 = (n0 + i0 < p.N) ? __ldg(p.w_scales + static_cast<int64_t>(bb) * p.N + n0 + i0) : uint16_t(0);
-        if (i1 < 256)
-            sc1 = (n0 + i1 < p.N) ? __ldg(p.w_scales + static_cast<int64_t>(bb) * p.N + n0 + i1) : uint16_t(0);
-        else
-            sc1 = (m0 + i1 - 256 < p.M) ? __ldg(p.a_scales + static_cast<int64_t>(bb) * p.M + m0 + i1 - 256) : uint16_t(0);
+        const int n0 = tt.nt * kTileN, m0 = tt.mt * kPairM + static_cast<int>(rank) * 128;
+        const uint16_t* ws = p.w_scales + static_cast<int64_t>(bb) * p.N + n0;
+        sc0 = (n0 + ct < p.N) ? __ldg(ws + ct) : uint16_t(0);
+        sc1 = (n0 + ct + 128 < p.N) ? __ldg(ws + ct + 128) : uint16_t(0);
+        sc2 = (m0 + ct < p.M) ? __ldg(p.a_scales + static_cast<int64_t>(bb) * p.M + m0 + ct) : uint16_t(0);
     };
     load_scales(t, b);
     bool ok = true;
@@ -267,24 +295,19 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, int war
         __syncwarp();   // orders lane 0's acquire of the weight tile before the other lanes' reads
         const uint8_t* src = s.pkW[ws] + src0;
         uint8_t* dst = s.cvB[cs];
-        uint4 w[kFull + 1];
+        uint4 w[kPieces];
 #pragma unroll
-        for (int k = 0; k <= kFull; ++k)
-            if (k < kFull || extra) w[k] = *reinterpret_cast<const uint4*>(src + k * kRowStep * 64);
+        for (int k = 0; k < kPieces; ++k) w[k] = *reinterpret_cast<const uint4*>(src + k * kRowStep * 64);
 #pragma unroll
-        for (int k = 0; k <= kFull; ++k) {
-            if (k < kFull || extra) {
-                const uint4 v = w[k];
-                *reinterpret_cast<uint4*>(dst + dstA + k * kRowStep * 128) = make_uint4(lo4(v.x), hi4(v.x), lo4(v.y), hi4(v.y));
-                *reinterpret_cast<uint4*>(dst + dstB + k * kRowStep * 128) = make_uint4(lo4(v.z), hi4(v.z), lo4(v.w), hi4(v.w));
-            }
+        for (int k = 0; k < kPieces; ++k) {
+            const uint4 v = w[k];
+            *reinterpret_cast<uint4*>(dst + dstA + k * kRowStep * 128) = make_uint4(lo4(v.x), hi4(v.x), lo4(v.y), hi4(v.y));
+            *reinterpret_cast<uint4*>(dst + dstB + k * kRowStep * 128) = make_uint4(lo4(v.z), hi4(v.z), lo4(v.w), hi4(v.w));
         }
         ScaleSlot& sl = s.sc[ss];
-        sl.sw[sw_dst0] = __half2float(__ushort_as_half(sc0));
-        if (i1 < 256)
-            sl.sw[sw_dst1] = __half2float(__ushort_as_half(sc1));
-        else
-            sl.sx[i1 - 256] = __half2float(__ushort_as_half(sc1)) * 262144.0f;   // 2^18 undoes the operand encoding
+        sl.sw[swd0] = __half2float(__ushort_as_half(sc0));
+        sl.sw[swd1] = __half2float(__ushort_as_half(sc1));
+        sl.sx[ct] = __half2float(__ushort_as_half(sc2)) * 262144.0f;   // 2^18 undoes the operand encoding
         dev::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -294,40 +317,38 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, int war
         }
         // next block
         if (++b == t.b1) {
-            u += gridDim.x;
+            u += gridDim.x >> 1;
             if (u >= num_units) break;
             t = unit_of(p, u);
             b = t.b0;
         }
         load_scales(t, b);
     }
-    if (!ok && lane == 0) {
-        *abort_flag = 1;
-        dev::report(p.status, dev::kStatusTimeout);
-    }
+    if (!ok && lane == 0) fail(p, abort_flag);
 }
 
 // ---------------------------------------------------------------- epilogue (warps 8-15)
-// Warp e (0..7) covers TMEM lanes 32*(warp%4) + 16*(e/4) + [0, 16) -- tile rows -- and all
-// 256 columns, read with tcgen05.ld 16x256b: thread t holds rows t/4 and t/4 + 8 of that
-// slab and columns 8g + 2(t%4) + {0, 1}, g = 0..31 (four registers per 8 columns:
+// Warp e (0..7) covers TMEM lanes 32*(warp%4) + 16*(e/4) + [0, 16) -- this CTA's tile rows --
+// and all 256 columns, read with tcgen05.ld 16x256b: thread t holds rows t/4 and t/4 + 8 of
+// that slab and columns 8g + 2(t%4) + {0, 1}, g = 0..31 (four registers per 8 columns:
 // row0 col0, row0 col1, row1 col0, row1 col1).
 template <bool kPartials>
-__device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, int warp, int lane, uint32_t tmem,
-                                              volatile int* abort_flag) {
+__device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, uint32_t rank, int warp, int lane,
+                                              uint32_t tmem, volatile int* abort_flag) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
     const int ew = warp - 8;                         // 0..7
     const int q = warp & 3;                          // TMEM lane quarter of this warp
-    const int slab = q * 32 + (ew >> 2) * 16;        // first tile row of this warp
+    const int slab = q * 32 + (ew >> 2) * 16;        // first local row of this warp
     const int tq = lane & 3, tr = lane >> 2;
-    const int lr0 = slab + tr, lr1 = slab + tr + 8;  // this thread's tile rows
+    const int lr0 = slab + tr, lr1 = slab + tr + 8;  // this thread's local rows
     const int et = ew * 32 + lane;                   // 0..255
     const uint32_t lane_addr = static_cast<uint32_t>(slab) << 16;
+    const uint32_t acc_empty0 = dev::mapa(&s.acc_empty[0], 0), acc_empty1 = dev::mapa(&s.acc_empty[1], 0);
     uint32_t v = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+    for (int u = blockIdx.x >> 1; u < num_units; u += gridDim.x >> 1) {
         const Unit t = unit_of(p, u);
-        const int m0 = t.mt * kTileM, n0 = t.nt * kTileN;
+        const int m0 = t.mt * kPairM + static_cast<int>(rank) * 128, n0 = t.nt * kTileN;
         const int row0 = m0 + lr0, row1 = m0 + lr1;
         const bool ok0 = row0 < p.M, ok1 = row1 < p.M;
         float2 accA[32], accB[32];   // rows lr0 / lr1, column pair g
@@ -399,7 +420,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, int warp
             }
             __syncwarp();
             if (lane == 0 && ok) {
-                dev::mbar_arrive(&s.acc_empty[ab]);
+                dev::mbar_arrive_remote(ab ? acc_empty1 : acc_empty0);   // the even CTA issues the MMAs
                 dev::mbar_arrive(&s.sc_empty[ss]);
             }
         }
@@ -417,24 +438,26 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, int warp
             if (p.splits == 1) {
                 store_rows();
             } else {
-                // split-K: publish this split's FP32 partial; the last split to arrive sums
-                // all of them in split order (deterministic) and writes Y.
-                float* base = p.ws_partial + (static_cast<int64_t>(t.tile) * p.splits + t.split) * kTileM * kTileN;
+                // split-K: publish this split's FP32 partial (this CTA's half of the tile); the
+                // last split to arrive sums all of them in split order (deterministic).
+                const int hrow = static_cast<int>(rank) * 128;
+                float* base = p.ws_partial + (static_cast<int64_t>(t.tile) * p.splits + t.split) * kPairM * kTileN;
 #pragma unroll
                 for (int g = 0; g < 32; ++g) {
                     const int cc = 8 * g + 2 * tq;
-                    __stcg(reinterpret_cast<float2*>(base + lr0 * kTileN + cc), accA[g]);
-                    __stcg(reinterpret_cast<float2*>(base + lr1 * kTileN + cc), accB[g]);
+                    __stcg(reinterpret_cast<float2*>(base + (hrow + lr0) * kTileN + cc), accA[g]);
+                    __stcg(reinterpret_cast<float2*>(base + (hrow + lr1) * kTileN + cc), accB[g]);
                 }
                 __threadfence();
-                dev::named_bar_sync(1, kEpiThreads);
+                dev::named_bar_sync(1, kEpiWarps * 32);
                 if (et == 0) {
-                    const int prev = atomicAdd(p.ws_count + t.tile, 1);
+                    int32_t* cnt = p.ws_count + t.tile * 2 + rank;
+                    const int prev = atomicAdd(cnt, 1);
                     const int last = (prev == p.splits - 1);
-                    if (last) p.ws_count[t.tile] = 0;  // reusable for the next call
+                    if (last) *cnt = 0;  // reusable for the next call
                     s.fixup_last = last;
                 }
-                dev::named_bar_sync(1, kEpiThreads);
+                dev::named_bar_sync(1, kEpiWarps * 32);
                 if (s.fixup_last) {
                     // every split (this one included) is in the workspace: sum in split order
                     __threadfence();
@@ -444,12 +467,12 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, int warp
                         accB[g] = make_float2(0.f, 0.f);
                     }
                     for (int sp = 0; sp < p.splits; ++sp) {
-                        const float* o = p.ws_partial + (static_cast<int64_t>(t.tile) * p.splits + sp) * kTileM * kTileN;
+                        const float* o = p.ws_partial + (static_cast<int64_t>(t.tile) * p.splits + sp) * kPairM * kTileN;
 #pragma unroll
                         for (int g = 0; g < 32; ++g) {
                             const int cc = 8 * g + 2 * tq;
-                            const float2 fa = __ldcg(reinterpret_cast<const float2*>(o + lr0 * kTileN + cc));
-                            const float2 fb = __ldcg(reinterpret_cast<const float2*>(o + lr1 * kTileN + cc));
+                            const float2 fa = __ldcg(reinterpret_cast<const float2*>(o + (hrow + lr0) * kTileN + cc));
+                            const float2 fb = __ldcg(reinterpret_cast<const float2*>(o + (hrow + lr1) * kTileN + cc));
                             accA[g].x += fa.x;
                             accA[g].y += fa.y;
                             accB[g].x += fb.x;
@@ -461,17 +484,15 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, int warp
             }
         }
     }
-    if (!ok && lane == 0) {
-        *abort_flag = 1;
-        dev::report(p.status, dev::kStatusTimeout);
-    }
+    if (!ok && lane == 0) fail(p, abort_flag);
 }
 
 template <bool kPartials>
-__global__ void __launch_bounds__(kThreads, 1) w4ax_gemm_kernel(const Params p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) w4ax_gemm_kernel(const Params p) {
     extern __shared__ uint8_t smem_raw[];
     Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = dev::cluster_ctarank();
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kASlots; ++i) {
@@ -492,58 +513,95 @@ __global__ void __launch_bounds__(kThreads, 1) w4ax_gemm_kernel(const Params p) 
         }
         for (int i = 0; i < 2; ++i) {
             dev::mbar_init(&s.acc_full[i], 1);
-            dev::mbar_init(&s.acc_empty[i], kEpiWarps);
+            dev::mbar_init(&s.acc_empty[i], 2 * kEpiWarps);   // epilogue warps of both CTAs
         }
+        for (int i = 0; i < kPeer; ++i) dev::mbar_init(&s.peer_full[i], 1);
         dev::mbar_init(&s.mma_done, 1);
         s.abort_flag = 0;
         dev::fence_barrier_init();
     }
-    if (warp == 1) dev::tmem_alloc(&s.tmem_base, kTmemCols);
+    if (warp == 1) dev::tmem_alloc_pair(&s.tmem_base, kTmemCols);
     dev::tc_fence_before();
     __syncthreads();
+    dev::cluster_sync();   // both CTAs' barriers and TMEM exist before any cross-CTA traffic
     dev::tc_fence_after();
     const uint32_t tmem = s.tmem_base;
     volatile int* abort_flag = &s.abort_flag;
 
     if (warp < 8) {
         dev::setmaxnreg_dec<64>();
-        if (warp == 0)
-            producer_role(p, s, lane, abort_flag);
-        else if (warp == 1)
-            mma_role(p, s, lane, tmem, abort_flag);
-        else
-            converter_role(p, s, warp, lane, abort_flag);
+        if (warp == 0) {
+            if (lane == 0) weight_producer(p, s, rank, abort_flag);
+        } else if (warp == 1) {
+            mma_role(p, s, rank, lane, tmem, abort_flag);
+        } else if (warp < kConvWarp0 + kConvWarps) {
+            converter_role(p, s, rank, warp, lane, abort_flag);
+        } else if (warp == 6) {
+            if (lane == 0) activation_producer(p, s, rank, abort_flag);
+        }
     } else {
         dev::setmaxnreg_inc<192>();
-        epilogue_role<kPartials>(p, s, warp, lane, tmem, abort_flag);
+        epilogue_role<kPartials>(p, s, rank, warp, lane, tmem, abort_flag);
     }
 
     dev::tc_fence_before();
     __syncthreads();
+    dev::cluster_sync();   // the peer's MMAs, commits and arrivals on this CTA are done
     if (warp == 1) {
         dev::tc_fence_after();
-        dev::tmem_dealloc(tmem, kTmemCols);
+        dev::tmem_dealloc_pair(tmem, kTmemCols);
     }
 }
 
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
 
+// Pairs (2-CTA clusters) that can be resident at once: the persistent grid never launches
+// more, so no cluster waits for another to finish. Asked once per device.
+int max_pairs(const fmpq_layout& L) {
+    static int cached[64] = {};
+    const int dev = L.device;
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    int pairs = L.num_sms / 2 > 0 ? L.num_sms / 2 : 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = sizeof(Smem) + 1024;
+    int clusters = 0;
+    if (cudaFuncSetAttribute(w4ax_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(Smem) + 1024)) == cudaSuccess &&
+        cudaOccupancyMaxActiveClusters(&clusters, w4ax_gemm_kernel<false>, &cfg) == cudaSuccess && clusters > 0 &&
+        clusters < pairs)
+        pairs = clusters;
+    cudaGetLastError();   // a failed query leaves no sticky error behind
+    if (dev >= 0 && dev < 64) cached[dev] = pairs;
+    return pairs;
+}
+
 int choose_splits(const fmpq_layout& L, int64_t tiles) {
-    if (tiles * 2 > L.num_sms) return 1;
-    int s = static_cast<int>(L.num_sms / tiles);
+    const int pairs = max_pairs(L);
+    if (tiles * 2 > pairs) return 1;
+    int s = static_cast<int>(pairs / tiles);
     if (s > L.nb) s = L.nb;
     if (s > 16) s = 16;
     return s < 1 ? 1 : s;
 }
 
+int64_t pair_tiles(int64_t M, int64_t N) { return ((M + kPairM - 1) / kPairM) * ((N + kTileN - 1) / kTileN); }
+
 }  // namespace
 
+size_t gemm_counter_bytes(const fmpq_layout& L, int64_t M, int64_t N) {
+    const int64_t tiles = pair_tiles(M, N);
+    if (choose_splits(L, tiles) == 1) return 0;
+    return static_cast<size_t>(tiles) * 2 * sizeof(int32_t) + 16;
+}
+
 size_t gemm_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N) {
-    const int64_t tiles = ((M + kTileM - 1) / kTileM) * ((N + kTileN - 1) / kTileN);
+    const int64_t tiles = pair_tiles(M, N);
     const int splits = choose_splits(L, tiles);
     if (splits == 1) return 0;
-    return static_cast<size_t>(tiles) * splits * kTileM * kTileN * sizeof(float) + static_cast<size_t>(tiles) * 4 + 16;
+    return static_cast<size_t>(tiles) * splits * kPairM * kTileN * sizeof(float) + gemm_counter_bytes(L, M, N);
 }
 
 cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& a, cudaStream_t stream) {
@@ -572,8 +630,8 @@ cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& a, cudaStream_t st
     p.status = L.d_status;
     const bool partials = a.P != nullptr;
     if (partials) {
-        p.mt0 = static_cast<int>(a.pm0 / kTileM);
-        p.mtiles = static_cast<int>((a.pm0 + a.pmcount - 1) / kTileM) - p.mt0 + 1;
+        p.mt0 = static_cast<int>(a.pm0 / kPairM);
+        p.mtiles = static_cast<int>((a.pm0 + a.pmcount - 1) / kPairM) - p.mt0 + 1;
         p.nt0 = static_cast<int>(a.pn0 / kTileN);
         p.ntiles = static_cast<int>((a.pn0 + a.pncount - 1) / kTileN) - p.nt0 + 1;
         p.splits = 1;
@@ -584,7 +642,7 @@ cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& a, cudaStream_t st
         p.pncount = static_cast<int>(a.pncount);
     } else {
         p.mt0 = 0;
-        p.mtiles = static_cast<int>((a.M + kTileM - 1) / kTileM);
+        p.mtiles = static_cast<int>((a.M + kPairM - 1) / kPairM);
         p.nt0 = 0;
         p.ntiles = static_cast<int>((a.N + kTileN - 1) / kTileN);
         p.splits = choose_splits(L, static_cast<int64_t>(p.mtiles) * p.ntiles);
@@ -592,11 +650,12 @@ cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& a, cudaStream_t st
             const int64_t tiles = static_cast<int64_t>(p.mtiles) * p.ntiles;
             p.ws_partial = static_cast<float*>(a.workspace);
             p.ws_count = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(a.workspace) +
-                                                    static_cast<size_t>(tiles) * p.splits * kTileM * kTileN * sizeof(float));
+                                                    static_cast<size_t>(tiles) * p.splits * kPairM * kTileN * sizeof(float));
         }
     }
     const int64_t units = static_cast<int64_t>(p.mtiles) * p.ntiles * p.splits;
-    const int grid = static_cast<int>(units < L.num_sms ? units : L.num_sms);
+    const int pairs = static_cast<int>(units < max_pairs(L) ? units : max_pairs(L));
+    const int grid = 2 * pairs;   // clusters of two CTAs (one pair per two SMs)
     if (partials)
         w4ax_gemm_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(p);
     else

@@ -23,7 +23,6 @@ namespace fmpq {
 
 constexpr int kBlock = 128;
 constexpr int kTileN = 256;          // packed-weight row grouping and GEMM tile width
-constexpr int kTileM = 128;
 
 // Launchers (return cudaGetLastError() after the launch).
 cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, int64_t M, void* A, void* scales,
@@ -47,7 +46,10 @@ struct GemmArgs {
     int64_t pm0, pmcount, pn0, pncount;
 };
 
+// Workspace of a split-K launch: FP32 partial tiles followed by the arrival counters
+// (gemm_counter_bytes of it, at the end). Both are 0 when the shape needs no split.
 size_t gemm_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N);
+size_t gemm_counter_bytes(const fmpq_layout& L, int64_t M, int64_t N);
 cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& args, cudaStream_t stream);
 
 }  // namespace fmpq

@@ -80,8 +80,7 @@ fmpq_status w4ax_gemm_noalloc(const fmpq_layout* L, const void* A_packed, const 
     a.ldy = ldy;
     const size_t need = fmpq::gemm_workspace_bytes(*L, M, N);
     if (need > 0) {
-        const int64_t tiles = ((M + fmpq::kTileM - 1) / fmpq::kTileM) * ((N + fmpq::kTileN - 1) / fmpq::kTileN);
-        const size_t counters = static_cast<size_t>(tiles) * 4 + 16;
+        const size_t counters = fmpq::gemm_counter_bytes(*L, M, N);
         if (need < counters) return FMPQ_ERR_WORKSPACE;
         const size_t partials = need - counters;
         if (partials > kScratchBytes || counters > kCounterBytes) return FMPQ_ERR_WORKSPACE;  // shape too large
