@@ -43,7 +43,7 @@ constexpr int kASlots = 8;    // activation plane slots (an INT4 block takes one
 constexpr int kWStages = 6;   // packed weight half-tiles (bulk copies)
 constexpr int kCvStages = 2;  // converted weight half-tiles
 constexpr int kScStages = 4;  // per-block scales staged for the epilogue
-constexpr int kPeer = 4;      // odd-CTA readiness signals in flight to the even CTA
+constexpr int kBlk = 16;      // per-block readiness / release barriers (ring over blocks)
 constexpr int kGroupM = 4;    // tile order: bands of 4 pair m-tiles, n-tiles inside a band
 constexpr int kConvWarps = 4;
 constexpr int kConvWarp0 = 2;   // converters are warps 2..5; warp 6 issues the activation copies
@@ -66,12 +66,15 @@ struct __align__(1024) Smem {
     uint8_t cvB[kCvStages][128 * 128];   // E4M3 weight operand: this CTA's 128 rows x 128 K
     uint8_t pkW[kWStages][128 * 64];     // packed weight codes of this CTA's 128 rows
     ScaleSlot sc[kScStages];             // per-block scales (fp32) for the epilogue
-    uint64_t a_full[kASlots], a_empty[kASlots];
+    // blk_full[b % kBlk]: block b's operands are in place in this CTA -- the activation
+    //   planes (bulk-copy bytes), the converted weight tile (converter warps) and, in the
+    //   even CTA, the odd CTA's operands (one forwarded arrival).
+    // blk_empty[b % kBlk]: block b's MMAs have finished (its activation slots and converted
+    //   weight slot may be reused); committed by the even CTA to both CTAs.
+    uint64_t blk_full[kBlk], blk_empty[kBlk];
     uint64_t w_full[kWStages], w_empty[kWStages];
-    uint64_t cv_full[kCvStages], cv_empty[kCvStages];
     uint64_t sc_full[kScStages], sc_empty[kScStages];
     uint64_t acc_full[2], acc_empty[2];
-    uint64_t peer_full[kPeer];
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -159,82 +162,93 @@ __device__ __forceinline__ void weight_producer(const Params& p, Smem& s, uint32
 __device__ __forceinline__ void activation_producer(const Params& p, Smem& s, uint32_t rank,
                                                     volatile int* abort_flag) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
-    uint32_t pc = 0;
+    uint32_t pc = 0, it = 0;        // planes and blocks issued
+    int32_t slot_block[kASlots];    // block that last used each plane slot (-1: none)
+#pragma unroll
+    for (int i = 0; i < kASlots; ++i) slot_block[i] = -1;
     bool ok = true;
     const int64_t plane_bytes = static_cast<int64_t>(p.M) * kBlock;
     for (int u = blockIdx.x >> 1; ok && u < num_units; u += gridDim.x >> 1) {
         const Unit t = unit_of(p, u);
         const int r0 = t.mt * kPairM + static_cast<int>(rank) * 128;
         const uint32_t abytes = static_cast<uint32_t>(max(0, min(128, p.M - r0))) * kBlock;
-        for (int b = t.b0; ok && b < t.b1; ++b) {
+        for (int b = t.b0; ok && b < t.b1; ++b, ++it) {
             const int planes = p.mask[b] ? 2 : 1;
-            const uint8_t* a0 = p.A + static_cast<int64_t>(p.poff[b]) * plane_bytes + static_cast<int64_t>(r0) * kBlock;
-            for (int pl = 0; pl < planes; ++pl, ++pc) {
-                const int sl = pc % kASlots;
-                if (!dev::mbar_wait(&s.a_empty[sl], ((pc / kASlots) & 1) ^ 1, abort_flag)) {
+            // the slots of this block's planes must have been released by the MMAs of the
+            // blocks that used them last
+            for (int pl = 0; pl < planes; ++pl) {
+                const int sl = (pc + pl) % kASlots;
+                int32_t last = -1;
+#pragma unroll
+                for (int i = 0; i < kASlots; ++i)
+                    if (i == sl) last = slot_block[i];
+                if (last >= 0 &&
+                    !dev::mbar_wait(&s.blk_empty[last % kBlk], (static_cast<uint32_t>(last) / kBlk) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
-                dev::mbar_arrive_expect_tx(&s.a_full[sl], abytes);   // rows past M: nothing to copy
-                if (abytes > 0) dev::bulk_g2s(s.opA[sl], a0 + pl * plane_bytes, abytes, &s.a_full[sl]);
+            }
+            if (!ok) break;
+            uint64_t* bar = &s.blk_full[it % kBlk];
+            dev::mbar_arrive_expect_tx(bar, abytes * planes);   // rows past M: nothing to copy
+            const uint8_t* a0 = p.A + static_cast<int64_t>(p.poff[b]) * plane_bytes + static_cast<int64_t>(r0) * kBlock;
+            for (int pl = 0; pl < planes; ++pl, ++pc) {
+                const int sl = pc % kASlots;
+#pragma unroll
+                for (int i = 0; i < kASlots; ++i)
+                    if (i == sl) slot_block[i] = static_cast<int32_t>(it);
+                if (abytes > 0) dev::bulk_g2s(s.opA[sl], a0 + pl * plane_bytes, abytes, bar);
             }
         }
     }
     if (!ok) fail(p, abort_flag);
-    for (int sl = 0; sl < kASlots; ++sl) {   // drain copies in flight
-        if (pc <= static_cast<uint32_t>(sl)) break;
-        const uint32_t last = sl + ((pc - 1 - sl) / kASlots) * kASlots;
-        dev::mbar_wait(&s.a_full[sl], (last / kASlots) & 1, nullptr);
+    // drain copies in flight: the last blocks' blk_full phases (they complete with the copies)
+    for (uint32_t k = 0; k < kBlk && k < it; ++k) {
+        const uint32_t b = it - 1 - k;
+        dev::mbar_wait(&s.blk_full[b % kBlk], (b / kBlk) & 1, nullptr);
     }
 }
 
 // ---------------------------------------------------------------- MMA issuer / forwarder (warp 1)
-// Even CTA: issues the pair MMAs once its own operands, the odd CTA's operands (signalled
-// on peer_full) and a free accumulator (released by both CTAs' epilogues) are ready, and
-// commits to the barriers of both CTAs. Odd CTA: forwards the readiness of its operands.
+// Even CTA: per block, waits for blk_full (its own operands and the odd CTA's forwarded
+// readiness) and a free accumulator (released by both CTAs' epilogues), issues the pair
+// MMAs and commits blk_empty and acc_full to both CTAs. Odd CTA: forwards blk_full.
 __device__ __forceinline__ void mma_role(const Params& p, Smem& s, uint32_t rank, int lane, uint32_t tmem,
                                          volatile int* abort_flag) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
     if (lane != 0) return;
     uint32_t it = 0, pc = 0;
     bool ok = true;
+    const uint32_t leader_blk_full = dev::mapa(&s.blk_full[0], 0);
     for (int u = blockIdx.x >> 1; ok && u < num_units; u += gridDim.x >> 1) {
         const Unit t = unit_of(p, u);
         for (int b = t.b0; ok && b < t.b1; ++b, ++it) {
-            const int cs = it % kCvStages;
             const int planes = p.mask[b] ? 2 : 1;
-            if (rank != 0) {
-                ok = dev::mbar_wait(&s.cv_full[cs], (it / kCvStages) & 1, abort_flag);
-                for (int pl = 0; ok && pl < planes; ++pl, ++pc)
-                    ok = dev::mbar_wait(&s.a_full[pc % kASlots], (pc / kASlots) & 1, abort_flag);
-                if (!ok) break;
-                dev::mbar_arrive_remote(dev::mapa(&s.peer_full[it % kPeer], 0));
-                continue;
-            }
-            const int ab = it & 1;
-            if (!dev::mbar_wait(&s.cv_full[cs], (it / kCvStages) & 1, abort_flag) ||
-                !dev::mbar_wait(&s.peer_full[it % kPeer], (it / kPeer) & 1, abort_flag) ||
-                !dev::mbar_wait(&s.acc_empty[ab], ((it >> 1) & 1) ^ 1, abort_flag)) {
+            if (!dev::mbar_wait(&s.blk_full[it % kBlk], (it / kBlk) & 1, abort_flag)) {
                 ok = false;
                 break;
             }
-            const uint64_t bd = dev::sdesc_k_sw128(dev::smem_u32(s.cvB[cs]));
+            if (rank != 0) {
+                // odd CTA: this block's operands are in place here; tell the even CTA
+                dev::mbar_arrive_remote(leader_blk_full + static_cast<uint32_t>(it % kBlk) * 8u);
+                pc += planes;
+                continue;
+            }
+            const int ab = it & 1;
+            if (!dev::mbar_wait(&s.acc_empty[ab], ((it >> 1) & 1) ^ 1, abort_flag)) {
+                ok = false;
+                break;
+            }
+            dev::tc_fence_after();
+            const uint64_t bd = dev::sdesc_k_sw128(dev::smem_u32(s.cvB[it % kCvStages]));
             const uint32_t d = tmem + static_cast<uint32_t>(ab) * 256u;
             for (int pl = 0; pl < planes; ++pl, ++pc) {
-                const int sl = pc % kASlots;
-                if (!dev::mbar_wait(&s.a_full[sl], (pc / kASlots) & 1, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                dev::tc_fence_after();
-                const uint64_t ad = dev::sdesc_k_sw128(dev::smem_u32(s.opA[sl]));
+                const uint64_t ad = dev::sdesc_k_sw128(dev::smem_u32(s.opA[pc % kASlots]));
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     dev::mma_e4m3_pair(d, ad + 2 * k, bd + 2 * k, kIdesc, (pl > 0 || k > 0) ? 1u : 0u);
-                dev::mma_commit_pair(&s.a_empty[sl]);
             }
-            if (!ok) break;
-            dev::mma_commit_pair(&s.cv_empty[cs]);
+            dev::mma_commit_pair(&s.blk_empty[it % kBlk]);
             dev::mma_commit_pair(&s.acc_full[ab]);
         }
     }
@@ -286,10 +300,14 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, uint32_
         const int ws = it % kWStages;
         const int cs = it % kCvStages;
         const int ss = it % kScStages;
-        if (lane == 0)
+        if (lane == 0) {
             ok = dev::mbar_wait(&s.w_full[ws], (it / kWStages) & 1, abort_flag) &&
-                 dev::mbar_wait(&s.cv_empty[cs], ((it / kCvStages) & 1) ^ 1, abort_flag) &&
                  dev::mbar_wait(&s.sc_empty[ss], ((it / kScStages) & 1) ^ 1, abort_flag);
+            if (ok && it >= static_cast<uint32_t>(kCvStages)) {   // converted slot: MMAs of block it - kCvStages done
+                const uint32_t prev = it - kCvStages;
+                ok = dev::mbar_wait(&s.blk_empty[prev % kBlk], (prev / kBlk) & 1, abort_flag);
+            }
+        }
         ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
         if (!ok) break;
         __syncwarp();   // orders lane 0's acquire of the weight tile before the other lanes' reads
@@ -312,7 +330,7 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, uint32_
         __syncwarp();
         if (lane == 0) {
             dev::mbar_arrive(&s.w_empty[ws]);
-            dev::mbar_arrive(&s.cv_full[cs]);
+            dev::mbar_arrive(&s.blk_full[it % kBlk]);
             dev::mbar_arrive(&s.sc_full[ss]);
         }
         // next block
@@ -495,17 +513,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) w4ax_ge
     const uint32_t rank = dev::cluster_ctarank();
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kASlots; ++i) {
-            dev::mbar_init(&s.a_full[i], 1);
-            dev::mbar_init(&s.a_empty[i], 1);
+        for (int i = 0; i < kBlk; ++i) {
+            // producer (expect-tx arrival) + converter warps (+ the odd CTA's forward)
+            dev::mbar_init(&s.blk_full[i], 1 + kConvWarps + (rank == 0 ? 1 : 0));
+            dev::mbar_init(&s.blk_empty[i], 1);
         }
         for (int i = 0; i < kWStages; ++i) {
             dev::mbar_init(&s.w_full[i], 1);
             dev::mbar_init(&s.w_empty[i], kConvWarps);
-        }
-        for (int i = 0; i < kCvStages; ++i) {
-            dev::mbar_init(&s.cv_full[i], kConvWarps);
-            dev::mbar_init(&s.cv_empty[i], 1);
         }
         for (int i = 0; i < kScStages; ++i) {
             dev::mbar_init(&s.sc_full[i], kConvWarps);
@@ -515,7 +530,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) w4ax_ge
             dev::mbar_init(&s.acc_full[i], 1);
             dev::mbar_init(&s.acc_empty[i], 2 * kEpiWarps);   // epilogue warps of both CTAs
         }
-        for (int i = 0; i < kPeer; ++i) dev::mbar_init(&s.peer_full[i], 1);
         dev::mbar_init(&s.mma_done, 1);
         s.abort_flag = 0;
         dev::fence_barrier_init();

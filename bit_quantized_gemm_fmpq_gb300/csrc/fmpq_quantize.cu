@@ -128,8 +128,8 @@ __device__ __forceinline__ float rcp_approx(float x) {
     return r;
 }
 
-// Byte 0 of four floats -> one word (the magnitudes sit in the low mantissa byte of
-// x + 1.5 * 2^23).
+// Byte 0 of four floats -> one word (a magnitude r sits in the low mantissa byte of
+// r + 1.5 * 2^23).
 __device__ __forceinline__ uint32_t low_bytes4(float a, float b, float c, float d) {
     const uint32_t ab = __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x0040);
     const uint32_t cd = __byte_perm(__float_as_uint(c), __float_as_uint(d), 0x0040);
@@ -262,10 +262,13 @@ __global__ void __launch_bounds__(kQThreads, 1) quantize_kernel(QuantParams p) {
                 const float sc = __half2float(s16);
                 const float inv = sc > 0.0f ? rcp_approx(sc) : 0.0f;
 
-                // codes: rne(|x| / s) via |x| * inv (relative error < 2^-22) and the
-                // 1.5 * 2^23 rounding constant; near-half quotients are settled exactly
+                // codes: rne(|x| / s). tm = fma(|x|, inv, 1.5 * 2^23) rounds |x| * inv
+                // (relative error < 2^-22) to an integer held in tm's low mantissa bits;
+                // quotients within 1e-4 of a half-integer are settled with the exact
+                // remainder |x| - r*s (the exact quotient of two fp16 values is never
+                // within 3e-5 of a half-integer unless it is one)
                 constexpr float kMagic = 12582912.0f;
-                float ax[8], r[8];
+                float ax[8], tm[8];
                 bool near_half = false;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
@@ -275,31 +278,29 @@ __global__ void __launch_bounds__(kQThreads, 1) quantize_kernel(QuantParams p) {
                 }
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
-                    const float t = __fmul_rn(ax[k], inv);
-                    r[k] = __fsub_rn(__fadd_rn(t, kMagic), kMagic);
-                    near_half |= fabsf(__fsub_rn(t, r[k])) > 0.4999f;
+                    tm[k] = __fmaf_rn(ax[k], inv, kMagic);
+                    near_half |= fabsf(__fmaf_rn(ax[k], inv, kMagic - tm[k])) > 0.4999f;
                 }
                 if (__any_sync(0xFFFFFFFFu, near_half) && sc > 0.0f) {
                     // (a zero scale keeps every code 0: its lanes skip the correction)
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const float e = fmaf(-r[k], sc, ax[k]);   // exact remainder |x| - r*s
+                        float r = tm[k] - kMagic;
+                        const float e = fmaf(-r, sc, ax[k]);   // exact remainder |x| - r*s
                         const float e2 = e + e;
-                        if (e2 > sc) r[k] += 1.0f;
-                        else if (e2 < -sc) r[k] -= 1.0f;
-                        else if (e2 == sc || e2 == -sc) {
-                            const bool odd = (static_cast<int>(r[k]) & 1) != 0;
-                            if (odd) r[k] += (e2 > 0.0f) ? 1.0f : -1.0f;   // tie: to even
-                        }
+                        if (e2 > sc) r += 1.0f;
+                        else if (e2 < -sc) r -= 1.0f;
+                        else if ((e2 == sc || e2 == -sc) && (static_cast<int>(r) & 1)) r += (e2 > 0.0f) ? 1.0f : -1.0f;  // tie: to even
+                        tm[k] = r + kMagic;
                     }
                 }
                 if (__any_sync(0xFFFFFFFFu, sc > 0.0f && sc < 6.103515625e-05f)) {
                     // subnormal scale: the quotient can round past qmax
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) r[k] = fminf(r[k], qm);
+                    for (int k = 0; k < 8; ++k) tm[k] = fminf(tm[k], qm + kMagic);
                 }
-                uint32_t w0 = low_bytes4(r[0] + kMagic, r[1] + kMagic, r[2] + kMagic, r[3] + kMagic);
-                uint32_t w1 = low_bytes4(r[4] + kMagic, r[5] + kMagic, r[6] + kMagic, r[7] + kMagic);
+                uint32_t w0 = low_bytes4(tm[0], tm[1], tm[2], tm[3]);
+                uint32_t w1 = low_bytes4(tm[4], tm[5], tm[6], tm[7]);
                 // sign bits of the inputs (bit 15 of each half) into bit 7 of each byte
                 w0 |= __byte_perm(h2[0], h2[1], 0x7531) & 0x80808080u;
                 w1 |= __byte_perm(h2[2], h2[3], 0x7531) & 0x80808080u;
