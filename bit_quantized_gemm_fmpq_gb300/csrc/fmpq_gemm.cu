@@ -300,17 +300,16 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, uint32_
         const int ws = it % kWStages;
         const int cs = it % kCvStages;
         const int ss = it % kScStages;
-        if (lane == 0) {
-            ok = dev::mbar_wait(&s.w_full[ws], (it / kWStages) & 1, abort_flag) &&
-                 dev::mbar_wait(&s.sc_empty[ss], ((it / kScStages) & 1) ^ 1, abort_flag);
-            if (ok && it >= static_cast<uint32_t>(kCvStages)) {   // converted slot: MMAs of block it - kCvStages done
-                const uint32_t prev = it - kCvStages;
-                ok = dev::mbar_wait(&s.blk_empty[prev % kBlk], (prev / kBlk) & 1, abort_flag);
-            }
+        // every lane waits (a converged warp polls faster than one lane with 31 parked);
+        // the vote keeps the decision uniform
+        ok = dev::mbar_wait(&s.w_full[ws], (it / kWStages) & 1, abort_flag) &&
+             dev::mbar_wait(&s.sc_empty[ss], ((it / kScStages) & 1) ^ 1, abort_flag);
+        if (ok && it >= static_cast<uint32_t>(kCvStages)) {   // converted slot: MMAs of block it - kCvStages done
+            const uint32_t prev = it - kCvStages;
+            ok = dev::mbar_wait(&s.blk_empty[prev % kBlk], (prev / kBlk) & 1, abort_flag);
         }
-        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok) break;
-        __syncwarp();   // orders lane 0's acquire of the weight tile before the other lanes' reads
         const uint8_t* src = s.pkW[ws] + src0;
         uint8_t* dst = s.cvB[cs];
         uint4 w[kPieces];
@@ -379,11 +378,11 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, uint32_t
             const int ab = v & 1;
             const int ss = v % kScStages;
             if (ok) {
-                if (lane == 0)
-                    ok = dev::mbar_wait(&s.sc_full[ss], (v / kScStages) & 1, abort_flag) &&
-                         dev::mbar_wait(&s.acc_full[ab], (v >> 1) & 1, abort_flag);
-                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-                __syncwarp();   // orders lane 0's acquire before the other lanes' scale reads
+                // every lane waits (each acquires the scales it reads); the vote keeps the
+                // decision uniform
+                ok = dev::mbar_wait(&s.sc_full[ss], (v / kScStages) & 1, abort_flag) &&
+                     dev::mbar_wait(&s.acc_full[ab], (v >> 1) & 1, abort_flag);
+                ok = __all_sync(0xFFFFFFFFu, ok);
             }
             const ScaleSlot& sl = s.sc[ss];
             if (ok) {

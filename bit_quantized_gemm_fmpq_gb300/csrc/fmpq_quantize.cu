@@ -220,8 +220,7 @@ __global__ void __launch_bounds__(kQThreads, 1) quantize_kernel(QuantParams p) {
         for (int64_t m = blockIdx.x; m < p.M; m += gridDim.x, ++i) {
             const int s = static_cast<int>(i % S);
             const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
-            if (lane == 0) ok = dev::mbar_wait(&full[s], ph, &abort_flag);
-            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&full[s], ph, &abort_flag));   // every lane waits
             if (!ok) break;
             const uint8_t* row = reinterpret_cast<const uint8_t*>(rows_s + static_cast<size_t>(s) * K);
             const uint32_t chunk_off = ((static_cast<uint32_t>(sub >> 1) ^ static_cast<uint32_t>(m & 7)) << 4) +
