@@ -134,7 +134,8 @@ __device__ __forceinline__ void fail(const Params& p, volatile int* abort_flag) 
 // Warp 0 streams this CTA's 128 rows (8 KB) of each block's packed weight tile; warp 6
 // streams this CTA's 128 activation rows of each block's plane(s). Separate threads, so the
 // activation prefetch depth is set by its own ring, not by the weight conversion.
-__device__ __forceinline__ void weight_producer(const Params& p, Smem& s, uint32_t rank, volatile int* abort_flag) {
+__device__ __forceinline__ void weight_producer(const Params& p, Smem& s, uint32_t rank, int lane,
+                                                volatile int* abort_flag) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
     uint32_t wc = 0;
     bool ok = true;
@@ -142,24 +143,29 @@ __device__ __forceinline__ void weight_producer(const Params& p, Smem& s, uint32
         const Unit t = unit_of(p, u);
         for (int b = t.b0; b < t.b1; ++b, ++wc) {
             const int ws = wc % kWStages;
-            if (!dev::mbar_wait(&s.w_empty[ws], ((wc / kWStages) & 1) ^ 1, abort_flag)) {
-                ok = false;
-                break;
+            // the whole warp waits (converged); lane 0 issues
+            ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&s.w_empty[ws], ((wc / kWStages) & 1) ^ 1, abort_flag));
+            if (!ok) break;
+            if (lane == 0) {
+                dev::mbar_arrive_expect_tx(&s.w_full[ws], 128 * 64);
+                dev::bulk_g2s(s.pkW[ws], p.W + (static_cast<int64_t>(t.nt) * p.nb + b) * (256 * 64) + rank * (128 * 64),
+                              128 * 64, &s.w_full[ws]);
             }
-            dev::mbar_arrive_expect_tx(&s.w_full[ws], 128 * 64);
-            dev::bulk_g2s(s.pkW[ws], p.W + (static_cast<int64_t>(t.nt) * p.nb + b) * (256 * 64) + rank * (128 * 64),
-                          128 * 64, &s.w_full[ws]);
+            __syncwarp();
         }
     }
-    if (!ok) fail(p, abort_flag);
-    for (int ws = 0; ws < kWStages; ++ws) {   // drain copies in flight
-        if (wc <= static_cast<uint32_t>(ws)) break;
-        const uint32_t last = ws + ((wc - 1 - ws) / kWStages) * kWStages;
-        dev::mbar_wait(&s.w_full[ws], (last / kWStages) & 1, nullptr);
+    if (!ok && lane == 0) fail(p, abort_flag);
+    if (lane == 0) {
+        for (int ws = 0; ws < kWStages; ++ws) {   // drain copies in flight
+            if (wc <= static_cast<uint32_t>(ws)) break;
+            const uint32_t last = ws + ((wc - 1 - ws) / kWStages) * kWStages;
+            dev::mbar_wait(&s.w_full[ws], (last / kWStages) & 1, nullptr);
+        }
     }
+    __syncwarp();
 }
 
-__device__ __forceinline__ void activation_producer(const Params& p, Smem& s, uint32_t rank,
+__device__ __forceinline__ void activation_producer(const Params& p, Smem& s, uint32_t rank, int lane,
                                                     volatile int* abort_flag) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
     uint32_t pc = 0, it = 0;        // planes and blocks issued
@@ -175,38 +181,40 @@ __device__ __forceinline__ void activation_producer(const Params& p, Smem& s, ui
         for (int b = t.b0; ok && b < t.b1; ++b, ++it) {
             const int planes = p.mask[b] ? 2 : 1;
             // the slots of this block's planes must have been released by the MMAs of the
-            // blocks that used them last
-            for (int pl = 0; pl < planes; ++pl) {
+            // blocks that used them last (the whole warp waits, converged; lane 0 issues)
+            for (int pl = 0; ok && pl < planes; ++pl) {
                 const int sl = (pc + pl) % kASlots;
                 int32_t last = -1;
 #pragma unroll
                 for (int i = 0; i < kASlots; ++i)
                     if (i == sl) last = slot_block[i];
-                if (last >= 0 &&
-                    !dev::mbar_wait(&s.blk_empty[last % kBlk], (static_cast<uint32_t>(last) / kBlk) & 1, abort_flag)) {
-                    ok = false;
-                    break;
-                }
+                if (last >= 0)
+                    ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&s.blk_empty[last % kBlk],
+                                                                (static_cast<uint32_t>(last) / kBlk) & 1, abort_flag));
             }
             if (!ok) break;
             uint64_t* bar = &s.blk_full[it % kBlk];
-            dev::mbar_arrive_expect_tx(bar, abytes * planes);   // rows past M: nothing to copy
+            if (lane == 0) dev::mbar_arrive_expect_tx(bar, abytes * planes);   // rows past M: nothing to copy
             const uint8_t* a0 = p.A + static_cast<int64_t>(p.poff[b]) * plane_bytes + static_cast<int64_t>(r0) * kBlock;
             for (int pl = 0; pl < planes; ++pl, ++pc) {
                 const int sl = pc % kASlots;
 #pragma unroll
                 for (int i = 0; i < kASlots; ++i)
                     if (i == sl) slot_block[i] = static_cast<int32_t>(it);
-                if (abytes > 0) dev::bulk_g2s(s.opA[sl], a0 + pl * plane_bytes, abytes, bar);
+                if (lane == 0 && abytes > 0) dev::bulk_g2s(s.opA[sl], a0 + pl * plane_bytes, abytes, bar);
             }
+            __syncwarp();
         }
     }
-    if (!ok) fail(p, abort_flag);
+    if (!ok && lane == 0) fail(p, abort_flag);
     // drain copies in flight: the last blocks' blk_full phases (they complete with the copies)
-    for (uint32_t k = 0; k < kBlk && k < it; ++k) {
-        const uint32_t b = it - 1 - k;
-        dev::mbar_wait(&s.blk_full[b % kBlk], (b / kBlk) & 1, nullptr);
+    if (lane == 0) {
+        for (uint32_t k = 0; k < kBlk && k < it; ++k) {
+            const uint32_t b = it - 1 - k;
+            dev::mbar_wait(&s.blk_full[b % kBlk], (b / kBlk) & 1, nullptr);
+        }
     }
+    __syncwarp();
 }
 
 // ---------------------------------------------------------------- MMA issuer / forwarder (warp 1)
@@ -216,7 +224,6 @@ __device__ __forceinline__ void activation_producer(const Params& p, Smem& s, ui
 __device__ __forceinline__ void mma_role(const Params& p, Smem& s, uint32_t rank, int lane, uint32_t tmem,
                                          volatile int* abort_flag) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
-    if (lane != 0) return;
     uint32_t it = 0, pc = 0;
     bool ok = true;
     const uint32_t leader_blk_full = dev::mapa(&s.blk_full[0], 0);
@@ -224,40 +231,43 @@ __device__ __forceinline__ void mma_role(const Params& p, Smem& s, uint32_t rank
         const Unit t = unit_of(p, u);
         for (int b = t.b0; ok && b < t.b1; ++b, ++it) {
             const int planes = p.mask[b] ? 2 : 1;
-            if (!dev::mbar_wait(&s.blk_full[it % kBlk], (it / kBlk) & 1, abort_flag)) {
-                ok = false;
-                break;
-            }
+            // the whole warp waits (converged); lane 0 issues
+            ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&s.blk_full[it % kBlk], (it / kBlk) & 1, abort_flag));
+            if (!ok) break;
             if (rank != 0) {
                 // odd CTA: this block's operands are in place here; tell the even CTA
-                dev::mbar_arrive_remote(leader_blk_full + static_cast<uint32_t>(it % kBlk) * 8u);
+                if (lane == 0) dev::mbar_arrive_remote(leader_blk_full + static_cast<uint32_t>(it % kBlk) * 8u);
+                __syncwarp();
                 pc += planes;
                 continue;
             }
             const int ab = it & 1;
-            if (!dev::mbar_wait(&s.acc_empty[ab], ((it >> 1) & 1) ^ 1, abort_flag)) {
-                ok = false;
-                break;
-            }
-            dev::tc_fence_after();
-            const uint64_t bd = dev::sdesc_k_sw128(dev::smem_u32(s.cvB[it % kCvStages]));
-            const uint32_t d = tmem + static_cast<uint32_t>(ab) * 256u;
-            for (int pl = 0; pl < planes; ++pl, ++pc) {
-                const uint64_t ad = dev::sdesc_k_sw128(dev::smem_u32(s.opA[pc % kASlots]));
+            ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&s.acc_empty[ab], ((it >> 1) & 1) ^ 1, abort_flag));
+            if (!ok) break;
+            if (lane == 0) {
+                dev::tc_fence_after();
+                const uint64_t bd = dev::sdesc_k_sw128(dev::smem_u32(s.cvB[it % kCvStages]));
+                const uint32_t d = tmem + static_cast<uint32_t>(ab) * 256u;
+                for (int pl = 0; pl < planes; ++pl) {
+                    const uint64_t ad = dev::sdesc_k_sw128(dev::smem_u32(s.opA[(pc + pl) % kASlots]));
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    dev::mma_e4m3_pair(d, ad + 2 * k, bd + 2 * k, kIdesc, (pl > 0 || k > 0) ? 1u : 0u);
+                    for (int k = 0; k < 4; ++k)
+                        dev::mma_e4m3_pair(d, ad + 2 * k, bd + 2 * k, kIdesc, (pl > 0 || k > 0) ? 1u : 0u);
+                }
+                dev::mma_commit_pair(&s.blk_empty[it % kBlk]);
+                dev::mma_commit_pair(&s.acc_full[ab]);
             }
-            dev::mma_commit_pair(&s.blk_empty[it % kBlk]);
-            dev::mma_commit_pair(&s.acc_full[ab]);
+            __syncwarp();
+            pc += planes;
         }
     }
-    if (!ok) fail(p, abort_flag);
-    if (rank == 0) {
+    if (!ok && lane == 0) fail(p, abort_flag);
+    if (rank == 0 && lane == 0) {
         // every MMA issued must finish before TMEM is released
         dev::mma_commit_pair(&s.mma_done);
         dev::mbar_wait(&s.mma_done, 0, nullptr);
     }
+    __syncwarp();
 }
 
 // ---------------------------------------------------------------- converters (warps 2-5)
@@ -544,13 +554,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) w4ax_ge
     if (warp < 8) {
         dev::setmaxnreg_dec<64>();
         if (warp == 0) {
-            if (lane == 0) weight_producer(p, s, rank, abort_flag);
+            weight_producer(p, s, rank, lane, abort_flag);
         } else if (warp == 1) {
             mma_role(p, s, rank, lane, tmem, abort_flag);
         } else if (warp < kConvWarp0 + kConvWarps) {
             converter_role(p, s, rank, warp, lane, abort_flag);
         } else if (warp == 6) {
-            if (lane == 0) activation_producer(p, s, rank, abort_flag);
+            activation_producer(p, s, rank, lane, abort_flag);
         }
     } else {
         dev::setmaxnreg_inc<192>();
