@@ -10,6 +10,8 @@
 #include "../../include/fmpq.h"
 #include "fmpq_internal.h"
 
+static_assert(FMPQ_MAX_K / FMPQ_BLOCK <= fmpq::kMaxBlocks, "kernel block tables hold every block");
+
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

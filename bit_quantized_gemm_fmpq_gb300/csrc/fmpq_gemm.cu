@@ -66,15 +66,22 @@ struct __align__(1024) Smem {
     uint8_t cvB[kCvStages][128 * 128];   // E4M3 weight operand: this CTA's 128 rows x 128 K
     uint8_t pkW[kWStages][128 * 64];     // packed weight codes of this CTA's 128 rows
     ScaleSlot sc[kScStages];             // per-block scales (fp32) for the epilogue
+    // The layout's block tables, staged once: the MMA issuer and the activation producer
+    // look them up every block.
+    int32_t poff[kMaxBlocks];            // first code plane of each block
+    uint8_t mask[kMaxBlocks];            // 1 = INT8 block (two planes)
+    uint32_t maskw[kMaxBlocks / 32];     // the same, one bit per block
     // blk_full[b % kBlk]: block b's operands are in place in this CTA -- the activation
-    //   planes (bulk-copy bytes), the converted weight tile (converter warps) and, in the
-    //   even CTA, the odd CTA's operands (one forwarded arrival).
+    //   planes (bulk-copy bytes), the converted weight tile (converter warps). In the even
+    //   CTA it also gathers everything else the MMAs of block b wait for: the odd CTA's
+    //   operands (one forwarded arrival) and the accumulator they overwrite (the epilogue
+    //   warps of both CTAs, done with block b - 2). One wait per block for the issuer.
     // blk_empty[b % kBlk]: block b's MMAs have finished (its activation slots and converted
     //   weight slot may be reused); committed by the even CTA to both CTAs.
     uint64_t blk_full[kBlk], blk_empty[kBlk];
     uint64_t w_full[kWStages], w_empty[kWStages];
     uint64_t sc_full[kScStages], sc_empty[kScStages];
-    uint64_t acc_full[2], acc_empty[2];
+    uint64_t acc_full[2];
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -179,7 +186,7 @@ __device__ __forceinline__ void activation_producer(const Params& p, Smem& s, ui
         const int r0 = t.mt * kPairM + static_cast<int>(rank) * 128;
         const uint32_t abytes = static_cast<uint32_t>(max(0, min(128, p.M - r0))) * kBlock;
         for (int b = t.b0; ok && b < t.b1; ++b, ++it) {
-            const int planes = p.mask[b] ? 2 : 1;
+            const int planes = s.mask[b] ? 2 : 1;
             // the slots of this block's planes must have been released by the MMAs of the
             // blocks that used them last (the whole warp waits, converged; lane 0 issues)
             for (int pl = 0; ok && pl < planes; ++pl) {
@@ -195,7 +202,7 @@ __device__ __forceinline__ void activation_producer(const Params& p, Smem& s, ui
             if (!ok) break;
             uint64_t* bar = &s.blk_full[it % kBlk];
             if (lane == 0) dev::mbar_arrive_expect_tx(bar, abytes * planes);   // rows past M: nothing to copy
-            const uint8_t* a0 = p.A + static_cast<int64_t>(p.poff[b]) * plane_bytes + static_cast<int64_t>(r0) * kBlock;
+            const uint8_t* a0 = p.A + static_cast<int64_t>(s.poff[b]) * plane_bytes + static_cast<int64_t>(r0) * kBlock;
             for (int pl = 0; pl < planes; ++pl, ++pc) {
                 const int sl = pc % kASlots;
 #pragma unroll
@@ -218,19 +225,22 @@ __device__ __forceinline__ void activation_producer(const Params& p, Smem& s, ui
 }
 
 // ---------------------------------------------------------------- MMA issuer / forwarder (warp 1)
-// Even CTA: per block, waits for blk_full (its own operands and the odd CTA's forwarded
-// readiness) and a free accumulator (released by both CTAs' epilogues), issues the pair
-// MMAs and commits blk_empty and acc_full to both CTAs. Odd CTA: forwards blk_full.
+// Even CTA: per block, waits for blk_full (both CTAs' operands and the free accumulator),
+// issues the pair MMAs and commits blk_empty and acc_full to both CTAs. Odd CTA: forwards
+// blk_full. This warp's time per block lies on the loop through the two accumulators
+// (MMAs -> epilogue -> release -> next MMAs), so it does one mbarrier wait per block and
+// reads the INT8 mask one 32-bit word per 32 blocks.
 __device__ __forceinline__ void mma_role(const Params& p, Smem& s, uint32_t rank, int lane, uint32_t tmem,
                                          volatile int* abort_flag) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
-    uint32_t it = 0, pc = 0;
+    uint32_t it = 0, pc = 0, mw = 0;
     bool ok = true;
     const uint32_t leader_blk_full = dev::mapa(&s.blk_full[0], 0);
     for (int u = blockIdx.x >> 1; ok && u < num_units; u += gridDim.x >> 1) {
         const Unit t = unit_of(p, u);
         for (int b = t.b0; ok && b < t.b1; ++b, ++it) {
-            const int planes = p.mask[b] ? 2 : 1;
+            if (b == t.b0 || (b & 31) == 0) mw = s.maskw[b >> 5];
+            const int planes = 1 + static_cast<int>((mw >> (b & 31)) & 1u);
             // the whole warp waits (converged); lane 0 issues
             ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&s.blk_full[it % kBlk], (it / kBlk) & 1, abort_flag));
             if (!ok) break;
@@ -242,8 +252,6 @@ __device__ __forceinline__ void mma_role(const Params& p, Smem& s, uint32_t rank
                 continue;
             }
             const int ab = it & 1;
-            ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&s.acc_empty[ab], ((it >> 1) & 1) ^ 1, abort_flag));
-            if (!ok) break;
             if (lane == 0) {
                 dev::tc_fence_after();
                 const uint64_t bd = dev::sdesc_k_sw128(dev::smem_u32(s.cvB[it % kCvStages]));
@@ -370,7 +378,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, uint32_t
     const int lr0 = slab + tr, lr1 = slab + tr + 8;  // this thread's local rows
     const int et = ew * 32 + lane;                   // 0..255
     const uint32_t lane_addr = static_cast<uint32_t>(slab) << 16;
-    const uint32_t acc_empty0 = dev::mapa(&s.acc_empty[0], 0), acc_empty1 = dev::mapa(&s.acc_empty[1], 0);
+    const uint32_t leader_blk_full = dev::mapa(&s.blk_full[0], 0);
     uint32_t v = 0;
     bool ok = true;
     for (int u = blockIdx.x >> 1; u < num_units; u += gridDim.x >> 1) {
@@ -395,6 +403,8 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, uint32_t
                 ok = __all_sync(0xFFFFFFFFu, ok);
             }
             const ScaleSlot& sl = s.sc[ss];
+            // accumulator ab is free for block v + 2, whose MMAs the even CTA issues
+            const uint32_t release = leader_blk_full + static_cast<uint32_t>((v + 2) % kBlk) * 8u;
             if (ok) {
                 dev::tc_fence_after();
                 const uint32_t taddr = tmem + lane_addr + ab * 256u;
@@ -447,7 +457,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, uint32_t
             }
             __syncwarp();
             if (lane == 0 && ok) {
-                dev::mbar_arrive_remote(ab ? acc_empty1 : acc_empty0);   // the even CTA issues the MMAs
+                dev::mbar_arrive_remote(release);
                 dev::mbar_arrive(&s.sc_empty[ss]);
             }
         }
@@ -523,8 +533,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) w4ax_ge
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kBlk; ++i) {
-            // producer (expect-tx arrival) + converter warps (+ the odd CTA's forward)
-            dev::mbar_init(&s.blk_full[i], 1 + kConvWarps + (rank == 0 ? 1 : 0));
+            // producer (expect-tx arrival) + converter warps; in the even CTA also the odd
+            // CTA's forward and both CTAs' epilogue warps (accumulator released)
+            dev::mbar_init(&s.blk_full[i], 1 + kConvWarps + (rank == 0 ? 1 + 2 * kEpiWarps : 0));
             dev::mbar_init(&s.blk_empty[i], 1);
         }
         for (int i = 0; i < kWStages; ++i) {
@@ -535,13 +546,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) w4ax_ge
             dev::mbar_init(&s.sc_full[i], kConvWarps);
             dev::mbar_init(&s.sc_empty[i], kEpiWarps);
         }
-        for (int i = 0; i < 2; ++i) {
-            dev::mbar_init(&s.acc_full[i], 1);
-            dev::mbar_init(&s.acc_empty[i], 2 * kEpiWarps);   // epilogue warps of both CTAs
-        }
+        for (int i = 0; i < 2; ++i) dev::mbar_init(&s.acc_full[i], 1);
         dev::mbar_init(&s.mma_done, 1);
         s.abort_flag = 0;
+        if (rank == 0) {
+            // blocks 0 and 1 find both accumulators free
+            for (int i = 0; i < 2; ++i)
+                for (int k = 0; k < 2 * kEpiWarps; ++k) dev::mbar_arrive(&s.blk_full[i]);
+        }
         dev::fence_barrier_init();
+    }
+    for (int b = threadIdx.x; b < p.nb; b += kThreads) {
+        s.mask[b] = p.mask[b];
+        s.poff[b] = p.poff[b];
+    }
+    if (warp < kMaxBlocks / 32) {
+        const int b = warp * 32 + lane;
+        const uint32_t bits = __ballot_sync(0xFFFFFFFFu, b < p.nb && p.mask[b] != 0);
+        if (lane == 0) s.maskw[warp] = bits;
     }
     if (warp == 1) dev::tmem_alloc_pair(&s.tmem_base, kTmemCols);
     dev::tc_fence_before();

@@ -22,6 +22,7 @@ struct fmpq_layout {
 namespace fmpq {
 
 constexpr int kBlock = 128;
+constexpr int kMaxBlocks = 256;     // K <= 32768
 constexpr int kTileN = 256;          // packed-weight row grouping and GEMM tile width
 
 // Launchers (return cudaGetLastError() after the launch).
