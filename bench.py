@@ -8,6 +8,7 @@ Laplace activations with 10% outlier channels, 27 of 224 blocks INT8). The INT4 
 packed once beforehand (offline preparation; timed separately and reported, not in the step).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --sweep      # the other workloads: one JSON line each (not the step metric)
 
 Prints one JSON line. `value` is effective TOPS (2*M*N*K per step, INT4 and INT8 blocks
 counted alike) summed over ranks with the max per-rank step time; `e2e` is the same metric
@@ -47,6 +48,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="run this many untimed steps and exit (for profilers)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the quantizer and GEMM on the LLaMA-7B QKV, decode (M=1..128) and "
+                         "load-balance (INT8 fraction 0-50%%) workloads, one JSON line each")
     return ap.parse_args()
 
 
@@ -197,12 +201,119 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+
+# ------------------------------------------------------------------------------- sweep
+
+def run_sweep(args):
+    """Quantizer and GEMM alone on the other workloads of the method's evaluation shapes, each
+    against its own roofline: the GEMM is tensor-bound at large M (2MNK over the fp8 peak) and
+    HBM-bound in decode (packed A + scales + packed W + Y over the measured copy bandwidth).
+    Inputs larger than L2 are not guaranteed here, so L2 is flushed before every timed launch;
+    decode is also timed as a CUDA graph of back-to-back launches over weight copies that
+    together exceed L2 (the serving case: no flush, no launch gaps)."""
+    import torch
+    from bit_quantized_gemm_fmpq_gb300 import build as fbuild
+    fbuild.build()
+    from bit_quantized_gemm_fmpq_gb300 import fmpq
+    from bit_quantized_gemm_fmpq_gb300 import workloads as wl
+    fmpq.load_library()
+    torch.cuda.set_device(0)
+    peaks = measured_peaks()
+    fp8_peak = peaks["bf16_tflops"] * 2.0
+    hbm = peaks["hbm_gbs"]
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device="cuda")
+    iters = max(10, min(args.steps, 100))
+
+    def timed(fn):
+        for _ in range(5):
+            fn()
+            flush.zero_()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(iters):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            ts.append((e0, e1))
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ts)
+
+    configs = [("llama7b_qkv", lambda: wl.llama7b_qkv())]
+    configs += [(f"decode_m{m}", (lambda m=m: wl.decode(m))) for m in (1, 8, 16, 32, 64, 128)]
+    configs += [(f"load_balance_{int(f * 100)}pct", (lambda f=f: wl.load_balance(f))) for f in (0.0, 0.10, 0.25, 0.50)]
+    sampler = ClockSampler(0)
+    for name, make in configs:
+        w = make()
+        M, K, N = w.M, w.K, w.N
+        layout = fmpq.Layout(K, w.perm, w.mask)
+        X = torch.from_numpy(w.X).cuda()
+        Wd = torch.from_numpy(w.W).cuda()
+        Wp, sw = fmpq.w4_pack_weights(layout, Wd)
+        del Wd
+        A = torch.empty(layout.packed_a_bytes(M), dtype=torch.uint8, device="cuda")
+        sx = torch.empty((layout.nb, M), dtype=torch.float16, device="cuda")
+        Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        ws = layout.workspace(M, N)
+        sampler.start()
+        q_ms = timed(lambda: fmpq.fmpq_quantize(layout, X, A, sx))
+        g_ms = timed(lambda: fmpq.w4ax_gemm(layout, A, sx, Wp, sw, M, N, Y, workspace=ws))
+        graph_ms = None
+        if M <= 128:
+            copies = [Wp] + [Wp.clone() for _ in range(4)]   # 5 x packed W > L2
+            reps = 20
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for r in range(reps):
+                    fmpq.w4ax_gemm(layout, A, sx, copies[r % len(copies)], sw, M, N, Y, workspace=ws)
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(5):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            graph_ms = e0.elapsed_time(e1) / (5 * reps)
+            del copies, g
+        clocks = sampler.stop()
+        if fmpq.fmpq_device_status(layout) != 0:
+            raise RuntimeError(f"device status after {name}")
+        flops = 2.0 * M * N * K
+        gbytes = layout.packed_a_bytes(M) + 2 * layout.nb * M + layout.packed_w_bytes(N) + 2 * layout.nb * N + 2 * M * N
+        qbytes = 2 * M * K + 2 * K + layout.packed_a_bytes(M) + 2 * layout.nb * M
+        t_tensor = flops / (fp8_peak * 1e12) * 1e3
+        t_hbm = gbytes / (hbm * 1e9) * 1e3
+        bound = "tensor" if t_tensor >= t_hbm else "hbm"
+        line = {
+            "sweep": name, "M": M, "K": K, "N": N, "n8_blocks": int(w.mask.sum()), "bound": bound,
+            "gemm_ms": g_ms, "gemm_tflops_effective": flops / (g_ms * 1e-3) / 1e12,
+            "gemm_gbs": gbytes / (g_ms * 1e-3) / 1e9,
+            "gemm_frac": max(t_tensor, t_hbm) / g_ms,
+            "gemm_frac_of": "fp8 peak (measured bf16 burst x 2)" if bound == "tensor" else "measured HBM copy bandwidth",
+            "gemm_graph_ms": graph_ms,
+            "gemm_graph_frac": (max(t_tensor, t_hbm) / graph_ms) if graph_ms else None,
+            "quant_ms": q_ms, "quant_gbs": qbytes / (q_ms * 1e-3) / 1e9,
+            "quant_frac_hbm": qbytes / (q_ms * 1e-3) / 1e9 / hbm,
+            "l2": "flushed before every timed launch (graph: 5 rotating weight copies, no flush)",
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+        del X, A, sx, Y, Wp, sw, ws, layout
+        torch.cuda.empty_cache()
+
 # ------------------------------------------------------------------------------- our arm
 
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.sweep:
+        run_sweep(args)
         return
     world, rank, local = dist_env()
     import torch
