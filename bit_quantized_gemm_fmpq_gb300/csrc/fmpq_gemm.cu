@@ -637,12 +637,14 @@ int64_t pair_tiles(int64_t M, int64_t N) { return ((M + kPairM - 1) / kPairM) * 
 }  // namespace
 
 size_t gemm_counter_bytes(const fmpq_layout& L, int64_t M, int64_t N) {
+    if (gemm_small_path(M)) return gemm_small_counter_bytes(L, M, N);
     const int64_t tiles = pair_tiles(M, N);
     if (choose_splits(L, tiles) == 1) return 0;
     return static_cast<size_t>(tiles) * 2 * sizeof(int32_t) + 16;
 }
 
 size_t gemm_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N) {
+    if (gemm_small_path(M)) return gemm_small_workspace_bytes(L, M, N);
     const int64_t tiles = pair_tiles(M, N);
     const int splits = choose_splits(L, tiles);
     if (splits == 1) return 0;
@@ -650,6 +652,7 @@ size_t gemm_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N) {
 }
 
 cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& a, cudaStream_t stream) {
+    if (a.P == nullptr && gemm_small_path(a.M)) return launch_gemm_small(L, a, stream);
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(w4ax_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,

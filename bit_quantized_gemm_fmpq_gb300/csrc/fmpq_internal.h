@@ -53,4 +53,11 @@ size_t gemm_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N);
 size_t gemm_counter_bytes(const fmpq_layout& L, int64_t M, int64_t N);
 cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& args, cudaStream_t stream);
 
+// Few tokens (M <= 128): the operand-swapped GEMM (output channels on the tensor core's M side,
+// tokens on its N side). launch_gemm and the workspace queries dispatch to it.
+bool gemm_small_path(int64_t M);
+size_t gemm_small_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N);
+size_t gemm_small_counter_bytes(const fmpq_layout& L, int64_t M, int64_t N);
+cudaError_t launch_gemm_small(const fmpq_layout& L, const GemmArgs& args, cudaStream_t stream);
+
 }  // namespace fmpq

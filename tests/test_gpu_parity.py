@@ -55,6 +55,12 @@ def test_tiny_config(fmpq_mod, oracle_mod):
     (200, 512, 1024, 8),     # all INT8
     (200, 512, 1024, 0),     # all INT4
     (40, 256, 128, 0),       # single block
+    # few tokens (the operand-swapped GEMM): token tiles of 16/32/64/128, ragged N
+    (5, 272, 384, 1),        # 16-token tile, last channel tile 16 wide
+    (17, 528, 1024, 2),      # 32-token tile with 17 tokens
+    (100, 784, 2048, 3),     # 128-token tile with 100 tokens, ragged N
+    (128, 400, 640, 5),      # all INT8, full 128-token tile
+    (33, 256, 256, 0),       # all INT4, 64-token tile
 ])
 def test_shapes(fmpq_mod, oracle_mod, M, N, K, n8):
     w = wl.synthetic(M, N, K, n8=n8, seed=M + N + K)
