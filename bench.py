@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="run this many untimed steps and exit (for profilers)")
+    ap.add_argument("--sweep-only", default="",
+                    help="with --sweep: run only the named workload (e.g. decode_m16)")
     ap.add_argument("--sweep", action="store_true",
                     help="time the quantizer and GEMM on the LLaMA-7B QKV, decode (M=1..128) and "
                          "load-balance (INT8 fraction 0-50%%) workloads, one JSON line each")
@@ -244,6 +246,10 @@ def run_sweep(args):
     configs = [("llama7b_qkv", lambda: wl.llama7b_qkv())]
     configs += [(f"decode_m{m}", (lambda m=m: wl.decode(m))) for m in (1, 8, 16, 32, 64, 128)]
     configs += [(f"load_balance_{int(f * 100)}pct", (lambda f=f: wl.load_balance(f))) for f in (0.0, 0.10, 0.25, 0.50)]
+    if args.sweep_only:
+        configs = [c for c in configs if c[0] == args.sweep_only]
+        if not configs:
+            raise SystemExit(f"unknown workload {args.sweep_only}")
     sampler = ClockSampler(0)
     for name, make in configs:
         w = make()
