@@ -106,7 +106,6 @@ __device__ __forceinline__ uint32_t pack_int4_pair(uint32_t v, int lane) {
 // ---------------------------------------------------------------------------------
 constexpr int kQWarps = 16;                        // compute warps; +1 producer warp
 constexpr int kQThreads = (kQWarps + 1) * 32;
-constexpr int kQMaxIters = 8;                      // block pairs per warp (nb <= 256)
 constexpr int kQSmemBudget = 200 * 1024;
 
 struct QuantParams {
@@ -114,6 +113,7 @@ struct QuantParams {
     int64_t ldx;
     int64_t M;
     int K, nb, stages;
+    int iters;              // block pairs per compute warp: ceil(nb / 32)
     const uint16_t* perm;
     const uint8_t* mask;
     const int32_t* poff;
@@ -146,11 +146,23 @@ __device__ __forceinline__ uint32_t high_plane(uint32_t w) {
     return __byte_perm(0x1C181000u, 0x26242220u, sel) | (w & 0x80808080u);
 }
 
+// Shared memory: [S] rows of X | gather offsets [iters][16 warps][32 lanes] (8 byte offsets of
+// 16 bits per lane and block pair) | plane offset per block | full / empty barriers per stage.
+__host__ __device__ inline size_t quant_gtab_offset(int K, int S) { return (2ull * K * S + 15) & ~15ull; }
+__host__ __device__ inline size_t quant_poff_offset(int K, int S, int iters) {
+    return quant_gtab_offset(K, S) + static_cast<size_t>(iters) * kQWarps * 32 * 16;
+}
+__host__ __device__ inline size_t quant_bars_offset(int K, int S, int iters, int nb) {
+    return quant_poff_offset(K, S, iters) + ((4ull * nb + 15) & ~15ull);
+}
+
 __global__ void __launch_bounds__(kQThreads, 1) quantize_kernel(QuantParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int K = p.K, nb = p.nb, S = p.stages;
-    uint16_t* rows_s = reinterpret_cast<uint16_t*>(smem_raw);                            // [S][K]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + ((2ull * K * S + 15) & ~15ull));
+    uint16_t* rows_s = reinterpret_cast<uint16_t*>(smem_raw);                                // [S][K]
+    uint4* gtab = reinterpret_cast<uint4*>(smem_raw + quant_gtab_offset(K, S));               // [iters][16][32]
+    int32_t* s_poff = reinterpret_cast<int32_t*>(smem_raw + quant_poff_offset(K, S, p.iters)); // [nb]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + quant_bars_offset(K, S, p.iters, nb));
     uint64_t* full = bars;        // [S]
     uint64_t* empty = bars + S;   // [S]
     __shared__ int abort_flag;
@@ -164,6 +176,7 @@ __global__ void __launch_bounds__(kQThreads, 1) quantize_kernel(QuantParams p) {
         abort_flag = 0;
         dev::fence_barrier_init();
     }
+    for (int b = threadIdx.x; b < nb; b += kQThreads) s_poff[b] = p.poff[b];
     __syncthreads();
 
     const uint32_t row_bytes = static_cast<uint32_t>(K) * 2u;
@@ -195,11 +208,11 @@ __global__ void __launch_bounds__(kQThreads, 1) quantize_kernel(QuantParams p) {
         const bool upper = lane >= 16;
         const int sub = lane & 15;                          // 8-channel group inside the block
         const uint32_t hmask = upper ? 0xFFFF0000u : 0x0000FFFFu;
-        // per iteration j: this lane's block, its gather byte offsets, plane offset, precision
-        uint4 goff[kQMaxIters];
+        // per iteration j: this lane's block, its gather byte offsets (in shared memory, so the
+        // loop over j stays compact), precision and validity bits
+        uint4* my_goff = gtab + warp * 32 + lane;          // entry j at my_goff[j * kQWarps * 32]
         uint32_t is8_bits = 0, valid_bits = 0;
-#pragma unroll
-        for (int j = 0; j < kQMaxIters; ++j) {
+        for (int j = 0; j < p.iters; ++j) {
             const int b = warp + 32 * j + (upper ? 16 : 0);
             const bool valid = b < nb;
             uint4 g = make_uint4(0, 0, 0, 0);
@@ -210,8 +223,9 @@ __global__ void __launch_bounds__(kQThreads, 1) quantize_kernel(QuantParams p) {
                 if (p.mask[b]) is8_bits |= 1u << j;
                 valid_bits |= 1u << j;
             }
-            goff[j] = g;
+            my_goff[j * kQWarps * 32] = g;
         }
+        __syncwarp();
         const int iters = (nb - warp + 31) / 32;            // iterations with a valid lower block
         const int64_t plane_stride = p.M * kBlock;
 
@@ -225,13 +239,12 @@ __global__ void __launch_bounds__(kQThreads, 1) quantize_kernel(QuantParams p) {
             const uint8_t* row = reinterpret_cast<const uint8_t*>(rows_s + static_cast<size_t>(s) * K);
             const uint32_t chunk_off = ((static_cast<uint32_t>(sub >> 1) ^ static_cast<uint32_t>(m & 7)) << 4) +
                                        static_cast<uint32_t>(sub & 1) * 8u;
-#pragma unroll
-            for (int j = 0; j < kQMaxIters; ++j) {
-                if (j >= iters) break;                       // warp-uniform
+#pragma unroll 1
+            for (int j = 0; j < iters; ++j) {                // warp-uniform bound
                 const bool valid = (valid_bits >> j) & 1u;
                 const bool is8 = (is8_bits >> j) & 1u;
                 // gather 8 fp16 values, paired into half2 words
-                const uint4 g = goff[j];
+                const uint4 g = my_goff[j * kQWarps * 32];
                 uint32_t h2[4];
                 {
                     const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
@@ -306,7 +319,7 @@ __global__ void __launch_bounds__(kQThreads, 1) quantize_kernel(QuantParams p) {
 
                 if (valid) {
                     const int b = warp + 32 * j + (upper ? 16 : 0);
-                    uint8_t* dst = p.A + (static_cast<int64_t>(__ldg(p.poff + b)) * p.M + m) * kBlock + chunk_off;
+                    uint8_t* dst = p.A + (static_cast<int64_t>(s_poff[b]) * p.M + m) * kBlock + chunk_off;
                     if (!is8) {
                         *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
                     } else {
@@ -389,10 +402,11 @@ __global__ void unpack_weights_kernel(const uint8_t* Wp, int64_t N, int K, int n
 cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, int64_t M, void* A, void* scales,
                             cudaStream_t stream) {
     const int K = L.K;
-    const size_t fixed = 16 + 1024;
+    const int iters = (L.nb + 31) / 32;
+    const size_t fixed = static_cast<size_t>(iters) * kQWarps * 32 * 16 + ((4ull * L.nb + 15) & ~15ull) + 16 * 16 + 1024;
     int stages = static_cast<int>((kQSmemBudget - fixed) / (2ull * K));
     stages = stages < 1 ? 1 : (stages > 8 ? 8 : stages);
-    const size_t smem = ((2ull * K * stages + 15) & ~15ull) + 8ull * (2 * stages);
+    const size_t smem = quant_bars_offset(K, stages, iters, L.nb) + 8ull * (2 * stages);
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -407,6 +421,7 @@ cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, in
     p.K = K;
     p.nb = L.nb;
     p.stages = stages;
+    p.iters = iters;
     p.perm = L.d_perm16;
     p.mask = L.d_mask;
     p.poff = L.d_poff;
