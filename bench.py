@@ -52,7 +52,8 @@ def parse_args():
                     help="with --sweep: run only the named workload (e.g. decode_m16)")
     ap.add_argument("--sweep", action="store_true",
                     help="time the quantizer and GEMM on the LLaMA-7B QKV, decode (M=1..128) and "
-                         "load-balance (INT8 fraction 0-50%%) workloads, one JSON line each")
+                         "load-balance (INT8 fraction 0-50%%) workloads, and the calibration "
+                         "statistics kernel, one JSON line each")
     return ap.parse_args()
 
 
@@ -247,9 +248,10 @@ def run_sweep(args):
     configs += [(f"decode_m{m}", (lambda m=m: wl.decode(m))) for m in (1, 8, 16, 32, 64, 128)]
     configs += [(f"load_balance_{int(f * 100)}pct", (lambda f=f: wl.load_balance(f))) for f in (0.0, 0.10, 0.25, 0.50)]
     if args.sweep_only:
+        names = [c[0] for c in configs] + ["calibrate_llama70b_down"]
+        if args.sweep_only not in names:
+            raise SystemExit(f"unknown workload {args.sweep_only}; one of {names}")
         configs = [c for c in configs if c[0] == args.sweep_only]
-        if not configs:
-            raise SystemExit(f"unknown workload {args.sweep_only}")
     sampler = ClockSampler(0)
     for name, make in configs:
         w = make()
@@ -310,6 +312,19 @@ def run_sweep(args):
         print(json.dumps(line), flush=True)
         del X, A, sx, Y, Wp, sw, ws, layout
         torch.cuda.empty_cache()
+    if not args.sweep_only or args.sweep_only == "calibrate_llama70b_down":
+        # offline calibration: per-channel absmax over the 4096 x 28672 activations (HBM-bound)
+        w = wl.llama70b_down()
+        X = torch.from_numpy(w.X).cuda()
+        out = torch.empty(w.K, dtype=torch.int32, device="cuda")
+        sampler.start()
+        ms = timed(lambda: fmpq.fmpq_channel_absmax(X, out))
+        clocks = sampler.stop()
+        nbytes = 2 * w.M * w.K + 4 * w.K
+        print(json.dumps({"sweep": "calibrate_llama70b_down", "M": w.M, "K": w.K, "bound": "hbm",
+                          "kernel": "channel_absmax_kernel", "ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9,
+                          "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm,
+                          "l2": "flushed before every timed launch", "clocks": clocks}), flush=True)
 
 # ------------------------------------------------------------------------------- our arm
 

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cmath>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -198,6 +199,40 @@ fmpq_status w4ax_gemm_partials(const fmpq_layout* L, const void* A_packed, const
     a.a_scales = A_packed;
     a.w_scales = W_packed;
     return launched(fmpq::launch_gemm(*L, a, static_cast<cudaStream_t>(stream)));
+}
+
+fmpq_status fmpq_channel_absmax(const void* X, int64_t ldx, int64_t T, int32_t K, uint32_t* absmax, void* stream) {
+    if (X == nullptr || absmax == nullptr) return FMPQ_ERR_INVALID_ARG;
+    if (K < FMPQ_BLOCK || K > FMPQ_MAX_K || K % FMPQ_BLOCK != 0 || T < 1 || ldx < K) return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (ldx % 8 != 0 || !aligned16(X) || !aligned16(absmax)) return FMPQ_ERR_MISALIGNED;
+    int dev = -1, major = 0, minor = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FMPQ_ERR_DEVICE;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return FMPQ_ERR_DEVICE;
+    if (major != 10 || minor != 3) return FMPQ_ERR_DEVICE;
+    return launched(fmpq::launch_channel_absmax(X, ldx, T, K, absmax, sms, static_cast<cudaStream_t>(stream)));
+}
+
+fmpq_status fmpq_plan_layout(int32_t K, const uint32_t* absmax_host, int32_t n8, int32_t* perm_host,
+                             uint8_t* mask_host) {
+    if (absmax_host == nullptr || perm_host == nullptr || mask_host == nullptr) return FMPQ_ERR_INVALID_ARG;
+    if (K < FMPQ_BLOCK || K > FMPQ_MAX_K || K % FMPQ_BLOCK != 0) return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (n8 < 0 || n8 > K / FMPQ_BLOCK) return FMPQ_ERR_INVALID_ARG;
+    try {
+        fmpq::plan_layout(K, absmax_host, n8, perm_host, mask_host);
+    } catch (const std::bad_alloc&) {
+        return FMPQ_ERR_INVALID_ARG;
+    }
+    return FMPQ_OK;
+}
+
+int32_t fmpq_outlier_blocks(int32_t K, double fraction) {
+    if (K < FMPQ_BLOCK || K > FMPQ_MAX_K || K % FMPQ_BLOCK != 0 || !(fraction >= 0.0 && fraction <= 1.0)) return -1;
+    const long long n_out = std::llround(fraction * K);
+    const long long n8 = (n_out + FMPQ_BLOCK - 1) / FMPQ_BLOCK;
+    return static_cast<int32_t>(n8 < K / FMPQ_BLOCK ? n8 : K / FMPQ_BLOCK);
 }
 
 fmpq_status fmpq_device_status(const fmpq_layout* L, int32_t* code, int32_t clear) {

@@ -53,6 +53,11 @@ size_t gemm_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N);
 size_t gemm_counter_bytes(const fmpq_layout& L, int64_t M, int64_t N);
 cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& args, cudaStream_t stream);
 
+// Calibration: per-channel absmax (zeroes `out`, then reduces) and the host layout planner.
+cudaError_t launch_channel_absmax(const void* X, int64_t ldx, int64_t T, int K, uint32_t* out, int num_sms,
+                                  cudaStream_t stream);
+void plan_layout(int K, const uint32_t* absmax, int n8, int32_t* perm, uint8_t* mask);
+
 // Few tokens (M <= 128): the operand-swapped GEMM (output channels on the tensor core's M side,
 // tokens on its N side). launch_gemm and the workspace queries dispatch to it.
 bool gemm_small_path(int64_t M);

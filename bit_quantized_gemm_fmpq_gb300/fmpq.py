@@ -45,6 +45,9 @@ SIGNATURES = {
     "w4ax_gemm_noalloc": (_I32, [_P, _P, _P, _P, _P, _I64, _I64, _P, _I64, _P]),
     "w4ax_gemm_partials": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P]),
     "fmpq_device_status": (_I32, [_P, ctypes.POINTER(_I32), _I32]),
+    "fmpq_channel_absmax": (_I32, [_P, _I64, _I64, _I32, _P, _P]),
+    "fmpq_plan_layout": (_I32, [_I32, _P, _I32, _P, _P]),
+    "fmpq_outlier_blocks": (_I32, [_I32, ctypes.c_double]),
     "fmpq_status_string": (ctypes.c_char_p, [_I32]),
     "fmpq_version": (_I32, []),
 }
@@ -242,3 +245,35 @@ def fmpq_device_status(layout: Layout, clear: bool = True) -> int:
 
 def fmpq_version() -> int:
     return int(load_library().fmpq_version())
+
+
+# ---------------------------------------------------------------------- calibration (offline)
+
+def fmpq_channel_absmax(X, out=None, stream=None):
+    """Per-channel absolute maximum of fp16 X [T][K] (rows may be strided): uint32 [K] of fp16
+    bit patterns, computed on the GPU."""
+    import torch
+    T, K = X.shape
+    if out is None:
+        out = torch.empty(K, dtype=torch.int32, device=X.device)
+    _check("fmpq_channel_absmax", load_library().fmpq_channel_absmax(_ptr(X), X.stride(0), T, K, _ptr(out),
+                                                                         _stream(stream)))
+    return out
+
+
+def fmpq_plan_layout(absmax, n8: int):
+    """Host planner: (perm int32 [K], mask uint8 [K/128]) from per-channel statistics."""
+    a = np.ascontiguousarray(np.asarray(absmax).astype(np.uint32))
+    K = a.size
+    perm = np.empty(K, dtype=np.int32)
+    mask = np.empty(K // BLOCK, dtype=np.uint8)
+    _check("fmpq_plan_layout", load_library().fmpq_plan_layout(K, a.ctypes.data, n8, perm.ctypes.data,
+                                                                   mask.ctypes.data))
+    return perm, mask
+
+
+def fmpq_outlier_blocks(K: int, fraction: float) -> int:
+    n8 = int(load_library().fmpq_outlier_blocks(K, fraction))
+    if n8 < 0:
+        raise ValueError("K must be a multiple of 128 in [128, 32768] and fraction in [0, 1]")
+    return n8

@@ -165,6 +165,38 @@ FMPQ_API fmpq_status w4ax_gemm_partials(const fmpq_layout* layout, const void* A
                                int64_t mcount, int64_t n0, int64_t ncount, int32_t* P,
                                void* stream);
 
+/* ---- Offline layout derivation from calibration activations ----
+ * The activation outliers sit in a small set of channels (about 10%: COMET news article,
+ * section 1), and a permutation gathers them into the same 128-channel blocks, which take
+ * INT8 codes. The outlier channels are found offline on calibration data and moved to the
+ * end (QUIK explainer, "第一步: 识别与重排"). The statistic is each channel's absolute maximum.
+ *
+ * Per-channel absolute maximum over T calibration tokens (asynchronous on `stream`):
+ *   X        fp16 [T][ldx] (device), 1 <= T, ldx >= K, ldx % 8 == 0, 16-byte aligned.
+ *   K        K % 128 == 0, 128 <= K <= FMPQ_MAX_K.
+ *   absmax   uint32 [K] (device, caller-owned): absmax[c] receives the fp16 bit pattern of
+ *            max_t |X[t][c]| (sign bit clear; for finite inputs the bit patterns order like
+ *            the magnitudes). The call zeroes it first, on the same stream. */
+FMPQ_API fmpq_status fmpq_channel_absmax(const void* X, int64_t ldx, int64_t T, int32_t K, uint32_t* absmax,
+                                         void* stream);
+
+/* Layout from channel statistics (host only: no device work, callable without a GPU).
+ *   absmax_host[K]   per-channel statistic, larger = more outlying (e.g. fmpq_channel_absmax).
+ *   n8               INT8 blocks, 0 <= n8 <= K/128.
+ *   perm_host[K]     out: the channels ranked by absmax (larger first, equal values by lower
+ *                    index); the first 128*n8 of the ranking fill the last n8 blocks
+ *                    (positions K-128*n8 .. K-1, in rank order), the other channels fill
+ *                    positions 0 .. K-128*n8-1 in ascending channel order.
+ *   mask_host[K/128] out: 1 for the last n8 blocks, 0 for the others.
+ * The outputs feed fmpq_layout_create. */
+FMPQ_API fmpq_status fmpq_plan_layout(int32_t K, const uint32_t* absmax_host, int32_t n8, int32_t* perm_host,
+                                      uint8_t* mask_host);
+
+/* INT8 blocks for an outlier fraction of the channels: ceil(round(fraction * K) / 128), with
+ * round taking halves away from zero, at most K/128; -1 for an invalid K or a fraction
+ * outside [0, 1]. */
+FMPQ_API int32_t fmpq_outlier_blocks(int32_t K, double fraction);
+
 /* Read (and, if clear != 0, reset) the layout's device status word. Synchronizes the
  * device. *code = FMPQ_OK or the first error a kernel recorded (e.g. FMPQ_ERR_TIMEOUT). */
 FMPQ_API fmpq_status fmpq_device_status(const fmpq_layout* layout, int32_t* code, int32_t clear);

@@ -54,6 +54,9 @@ def _load():
             lib.oracle_f16_to_f32.restype = ctypes.c_float
             lib.oracle_f32_to_f16_array.argtypes = [P, i64, P]
             lib.oracle_f16_to_f32_array.argtypes = [P, i64, P]
+            lib.oracle_channel_absmax.argtypes = [P, i64, i32, P]
+            lib.oracle_plan_layout.argtypes = [i32, P, i32, P, P]
+            lib.oracle_plan_layout.restype = i32
             lib.oracle_quantize_activations.argtypes = [P, i64, i32, i32, P, P, P, P, P]
             lib.oracle_quantize_activations.restype = i32
             lib.oracle_unpack_activations.argtypes = [P, P, i32, i32, P]
@@ -211,3 +214,31 @@ def reference(X, W, perm, mask):
     P = partials(Aq, Wq)
     Y = epilogue(P, sx, sw)
     return dict(A_packed=A, a_scales=sx, Aq=Aq, Wq=Wq, w_scales=sw, P=P, Y=Y)
+
+
+# ---------------------------------------------------------------------- calibration (offline)
+
+def channel_absmax(X) -> np.ndarray:
+    """fp16 bits of each channel's absolute maximum over the rows of X [T][K] (float16)."""
+    X = np.ascontiguousarray(np.asarray(X, dtype=np.float16)).view(np.uint16)
+    T, K = X.shape
+    out = np.empty(K, dtype=np.uint16)
+    _load().oracle_channel_absmax(_ptr(X), T, K, _ptr(out))
+    return out
+
+
+def plan_layout(stat, n8: int):
+    """(perm int32 [K], mask uint8 [K/128]) from per-channel statistics; see fmpq_oracle.c."""
+    stat = np.ascontiguousarray(np.asarray(stat).astype(np.uint32))
+    K = stat.size
+    perm = np.empty(K, dtype=np.int32)
+    mask = np.empty(K // BLOCK, dtype=np.uint8)
+    if _load().oracle_plan_layout(K, _ptr(stat), int(n8), _ptr(perm), _ptr(mask)) != 0:
+        raise ValueError("bad calibration arguments")
+    return perm, mask
+
+
+def outlier_blocks(K: int, fraction: float) -> int:
+    """ceil(round(fraction*K) / 128), halves rounded away from zero, at most K/128."""
+    n_out = int(np.floor(fraction * K + 0.5))
+    return min((n_out + BLOCK - 1) // BLOCK, K // BLOCK)

@@ -413,3 +413,70 @@ int oracle_num_threads(void) {
     return 1;
 #endif
 }
+
+/* ------------------------------------------------------------------------------------
+ * Offline layout derivation from calibration activations.
+ *
+ * COMET news article, section 1: the activation outliers concentrate in about 10% of the
+ * channels, and a channel permutation gathers them into the same 128-channel blocks, which
+ * take 8-bit codes. QUIK explainer, "第一步: 识别与重排": the outlier columns are identified
+ * offline on a calibration set and moved to the end of the matrix. Readings (the pages give
+ * no formula): the statistic is the channel's absolute maximum over the calibration tokens;
+ * channels rank by it, larger first, equal values by lower channel index; the first 128*n8
+ * ranked channels fill the last n8 blocks in rank order, the others fill the first blocks in
+ * ascending channel order; n8 for an outlier fraction f is ceil(round(f*K) / 128), round
+ * taking halves away from zero.
+ * ------------------------------------------------------------------------------------ */
+
+/* out[c] = max over the T rows of X [T][K] of |X[t][c]|, as fp16 bits (sign cleared). */
+void oracle_channel_absmax(const uint16_t* X, int64_t T, int K, uint16_t* out) {
+    for (int c = 0; c < K; ++c) {
+        uint16_t m = 0;
+        for (int64_t t = 0; t < T; ++t) {
+            const uint16_t v = (uint16_t)(X[t * K + c] & 0x7FFFu);
+            if (v > m) m = v;
+        }
+        out[c] = m;
+    }
+}
+
+typedef struct {
+    uint32_t stat;
+    int32_t channel;
+} ranked_channel;
+
+static int ranked_before(const void* pa, const void* pb) {
+    const ranked_channel* a = (const ranked_channel*)pa;
+    const ranked_channel* b = (const ranked_channel*)pb;
+    if (a->stat != b->stat) return a->stat > b->stat ? -1 : 1;   /* larger statistic first */
+    return a->channel < b->channel ? -1 : (a->channel > b->channel ? 1 : 0);
+}
+
+/* perm [K], mask [K/128] from the per-channel statistics stat [K]; returns 0, or -1 for bad
+ * arguments. */
+int oracle_plan_layout(int K, const uint32_t* stat, int n8, int32_t* perm, uint8_t* mask) {
+    const int nb = K / 128;
+    if (K <= 0 || K % 128 != 0 || n8 < 0 || n8 > nb) return -1;
+    ranked_channel* r = (ranked_channel*)malloc(sizeof(ranked_channel) * (size_t)K);
+    uint8_t* in_int8 = (uint8_t*)calloc((size_t)K, 1);
+    if (r == NULL || in_int8 == NULL) {
+        free(r);
+        free(in_int8);
+        return -1;
+    }
+    for (int c = 0; c < K; ++c) {
+        r[c].stat = stat[c];
+        r[c].channel = c;
+    }
+    qsort(r, (size_t)K, sizeof(ranked_channel), ranked_before);
+    const int n_top = 128 * n8;
+    for (int i = 0; i < n_top; ++i) in_int8[r[i].channel] = 1;
+    int j = 0;
+    for (int c = 0; c < K; ++c)
+        if (!in_int8[c]) perm[j++] = c;
+    for (int i = 0; i < n_top; ++i) perm[j++] = r[i].channel;
+    for (int b = 0; b < nb; ++b) mask[b] = (uint8_t)(b >= nb - n8);
+    free(r);
+    free(in_int8);
+    return 0;
+}
