@@ -66,6 +66,23 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time: the whole job takes as long as its slowest rank. One all-reduce
+    of a scalar (NCCL on the GPU in the benchmark, gloo on the CPU in the tests); the data path
+    itself has no collective (each rank runs its own batch against replicated weights)."""
+    if world == 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tops(world: int, ops_per_rank: float, ms: float) -> float:
+    """Whole-job throughput (weak scaling): every rank does ops_per_rank in ms."""
+    return world * ops_per_rank / (ms * 1e-3) / 1e12
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -409,17 +426,13 @@ def main():
         torch.distributed.barrier()
     q_ms = [e[0].elapsed_time(e[1]) for e in ev]
     g_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    step_ms = sum(q + g for q, g in zip(q_ms, g_ms)) / args.steps
-    if world > 1:
-        t = torch.tensor([step_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(sum(q + g for q, g in zip(q_ms, g_ms)) / args.steps, world, "cuda")
     status = fmpq.fmpq_device_status(layout)
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
 
     flops = 2.0 * M * N * K
-    value = world * flops / (step_ms * 1e-3) / 1e12
+    value = aggregate_tops(world, flops, step_ms)
     gemm_ms = statistics.mean(g_ms)
     quant_ms = statistics.mean(q_ms)
     peaks = measured_peaks()
@@ -449,12 +462,8 @@ def main():
             t_ev[i][1].record(stream)
             flush.zero_()
         torch.cuda.synchronize()
-        e2e_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in t_ev)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device="cuda")
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TOPS",
+        e2e_ms = max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in t_ev), world, "cuda")
+        e2e = {"value": aggregate_tops(world, flops, e2e_ms), "unit": "TOPS",
                "h2d_bytes_per_step": int(Xh.numel() * 2), "d2h_bytes_per_step": int(Yh.numel() * 2),
                "ms_per_step": e2e_ms}
 
