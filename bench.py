@@ -265,7 +265,7 @@ def run_sweep(args):
     configs += [(f"decode_m{m}", (lambda m=m: wl.decode(m))) for m in (1, 8, 16, 32, 64, 128)]
     configs += [(f"load_balance_{int(f * 100)}pct", (lambda f=f: wl.load_balance(f))) for f in (0.0, 0.10, 0.25, 0.50)]
     if args.sweep_only:
-        names = [c[0] for c in configs] + ["calibrate_llama70b_down"]
+        names = [c[0] for c in configs] + ["rmsnorm_quantize_llama70b_down", "calibrate_llama70b_down"]
         if args.sweep_only not in names:
             raise SystemExit(f"unknown workload {args.sweep_only}; one of {names}")
         configs = [c for c in configs if c[0] == args.sweep_only]
@@ -329,6 +329,25 @@ def run_sweep(args):
         print(json.dumps(line), flush=True)
         del X, A, sx, Y, Wp, sw, ws, layout
         torch.cuda.empty_cache()
+    if not args.sweep_only or args.sweep_only == "rmsnorm_quantize_llama70b_down":
+        # the quantizer fused with the preceding RMSNorm, on the 4096 x 28672 activations
+        w = wl.llama70b_down()
+        layout = fmpq.Layout(w.K, w.perm, w.mask)
+        X = torch.from_numpy(w.X).cuda()
+        gperm = torch.from_numpy(np.ascontiguousarray(
+            np.random.default_rng(5).uniform(0.5, 1.5, w.K).astype(np.float16)[w.perm])).cuda()
+        A = torch.empty(layout.packed_a_bytes(w.M), dtype=torch.uint8, device="cuda")
+        sx = torch.empty((layout.nb, w.M), dtype=torch.float16, device="cuda")
+        sampler.start()
+        ms_plain = timed(lambda: fmpq.fmpq_quantize(layout, X, A, sx))
+        ms = timed(lambda: fmpq.fmpq_rmsnorm_quantize(layout, X, gperm, 1e-5, A, sx))
+        clocks = sampler.stop()
+        nbytes = 2 * w.M * w.K + 2 * w.K + layout.packed_a_bytes(w.M) + 2 * layout.nb * w.M
+        print(json.dumps({"sweep": "rmsnorm_quantize_llama70b_down", "M": w.M, "K": w.K, "bound": "hbm",
+                          "kernel": "quantize_kernel<true>", "ms": ms, "quantize_only_ms": ms_plain,
+                          "gbs": nbytes / (ms * 1e-3) / 1e9, "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm,
+                          "l2": "flushed before every timed launch", "clocks": clocks}), flush=True)
+        del layout
     if not args.sweep_only or args.sweep_only == "calibrate_llama70b_down":
         # offline calibration: per-channel absmax over the 4096 x 28672 activations (HBM-bound)
         w = wl.llama70b_down()

@@ -125,6 +125,19 @@ fmpq_status fmpq_quantize(const fmpq_layout* L, const void* X, int64_t ldx, int6
     return launched(fmpq::launch_quantize(*L, X, ldx, M, A_packed, a_scales, static_cast<cudaStream_t>(stream)));
 }
 
+fmpq_status fmpq_rmsnorm_quantize(const fmpq_layout* L, const void* X, int64_t ldx, int64_t M, const void* gamma_perm,
+                                  float eps, void* A_packed, void* a_scales, void* stream) {
+    if (L == nullptr || X == nullptr || gamma_perm == nullptr || A_packed == nullptr || a_scales == nullptr)
+        return FMPQ_ERR_INVALID_ARG;
+    if (!(eps > 0.0f) || !(eps < 1e30f)) return FMPQ_ERR_INVALID_ARG;   // positive and finite
+    if (M < 1 || M > INT32_MAX || ldx < L->K) return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (ldx % 8 != 0 || !aligned16(X) || !aligned16(gamma_perm) || !aligned16(A_packed) || !aligned16(a_scales))
+        return FMPQ_ERR_MISALIGNED;
+    if (fmpq_status st = check_device(L)) return st;
+    return launched(fmpq::launch_quantize(*L, X, ldx, M, A_packed, a_scales, static_cast<cudaStream_t>(stream),
+                                          gamma_perm, eps));
+}
+
 fmpq_status w4_pack_weights(const fmpq_layout* L, const void* W, int64_t ldw, int64_t N, void* W_packed,
                             void* w_scales, void* stream) {
     if (L == nullptr || W == nullptr || W_packed == nullptr || w_scales == nullptr) return FMPQ_ERR_INVALID_ARG;

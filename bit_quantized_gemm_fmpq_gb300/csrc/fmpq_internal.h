@@ -26,8 +26,10 @@ constexpr int kMaxBlocks = 256;     // K <= 32768
 constexpr int kTileN = 256;          // packed-weight row grouping and GEMM tile width
 
 // Launchers (return cudaGetLastError() after the launch).
+// gamma_perm != nullptr: the quantized values are the row's RMSNorm with that gamma (permuted
+// channel order) and eps.
 cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, int64_t M, void* A, void* scales,
-                            cudaStream_t stream);
+                            cudaStream_t stream, const void* gamma_perm = nullptr, float eps = 0.0f);
 cudaError_t launch_pack_weights(const fmpq_layout& L, const void* W, int64_t ldw, int64_t N, void* Wp,
                                 void* scales, cudaStream_t stream);
 cudaError_t launch_unpack_weights(const fmpq_layout& L, const void* Wp, int64_t N, int8_t* Wq, cudaStream_t stream);

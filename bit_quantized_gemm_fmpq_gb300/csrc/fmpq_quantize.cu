@@ -105,7 +105,8 @@ __device__ __forceinline__ uint32_t pack_int4_pair(uint32_t v, int lane) {
 // The sign bit is the sign bit of the fp16 input.
 // ---------------------------------------------------------------------------------
 constexpr int kQWarps = 16;                        // compute warps; +1 producer warp
-constexpr int kQThreads = (kQWarps + 1) * 32;
+constexpr int kQNormWarps = 8;                     // fused RMSNorm: warps computing the rows' norms
+constexpr int kQThreads = (kQWarps + 1 + kQNormWarps) * 32;
 constexpr int kQSmemBudget = 200 * 1024;
 
 struct QuantParams {
@@ -120,6 +121,8 @@ struct QuantParams {
     uint8_t* A;
     uint16_t* scales;
     int32_t* status;
+    const uint16_t* gamma_perm;   // fused RMSNorm: gamma in the permuted channel order
+    float eps;
 };
 
 __device__ __forceinline__ float rcp_approx(float x) {
@@ -152,26 +155,42 @@ __host__ __device__ inline size_t quant_gtab_offset(int K, int S) { return (2ull
 __host__ __device__ inline size_t quant_poff_offset(int K, int S, int iters) {
     return quant_gtab_offset(K, S) + static_cast<size_t>(iters) * kQWarps * 32 * 16;
 }
-__host__ __device__ inline size_t quant_bars_offset(int K, int S, int iters, int nb) {
+__host__ __device__ inline size_t quant_chunk_offset(int K, int S, int iters, int nb) {
     return quant_poff_offset(K, S, iters) + ((4ull * nb + 15) & ~15ull);
 }
+__host__ __device__ inline size_t quant_bars_offset(int K, int S, int iters, int nb) {
+    return quant_chunk_offset(K, S, iters, nb) + ((4ull * S * nb + 4ull * S + 15) & ~15ull);
+}
 
+// kNorm: the quantized values are RMSNorm(x) = fp16_rn((fp32(x) * r) * fp32(gamma)) with
+// r = 1 / sqrt(T / K + eps) (IEEE divisions and square root), where T is the row's sum of
+// squares in a fixed order: every 128-channel chunk of the row (input channel order) is summed
+// by 16 lanes of 8 consecutive channels each (sequential fp32 adds of the exact squares), the
+// 16 lane sums are combined by an xor tree (8, 4, 2, 1), and the chunk sums by 32 lanes taking
+// chunks l, l+32, ... sequentially and an xor tree (16, ..., 1).
+template <bool kNorm>
 __global__ void __launch_bounds__(kQThreads, 1) quantize_kernel(QuantParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int K = p.K, nb = p.nb, S = p.stages;
     uint16_t* rows_s = reinterpret_cast<uint16_t*>(smem_raw);                                // [S][K]
     uint4* gtab = reinterpret_cast<uint4*>(smem_raw + quant_gtab_offset(K, S));               // [iters][16][32]
     int32_t* s_poff = reinterpret_cast<int32_t*>(smem_raw + quant_poff_offset(K, S, p.iters)); // [nb]
+    float* chunk_s = reinterpret_cast<float*>(smem_raw + quant_chunk_offset(K, S, p.iters, nb));  // [S][nb]
+    float* r_s = chunk_s + static_cast<size_t>(S) * nb;                                            // [S]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + quant_bars_offset(K, S, p.iters, nb));
-    uint64_t* full = bars;        // [S]
-    uint64_t* empty = bars + S;   // [S]
+    uint64_t* full = bars;            // [S] the row has landed
+    uint64_t* empty = bars + S;       // [S] every reader is done with the row
+    uint64_t* nsync = bars + 2 * S;   // [S] fused RMSNorm: both norm warps' chunk sums are in place
+    uint64_t* rready = bars + 3 * S;  // [S] fused RMSNorm: the row's factor r is in r_s
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             dev::mbar_init(&full[s], 1);
-            dev::mbar_init(&empty[s], kQWarps);
+            dev::mbar_init(&empty[s], kQWarps + (kNorm ? kQNormWarps : 0));
+            dev::mbar_init(&nsync[s], kQNormWarps);
+            dev::mbar_init(&rready[s], 1);
         }
         abort_flag = 0;
         dev::fence_barrier_init();
@@ -203,6 +222,60 @@ __global__ void __launch_bounds__(kQThreads, 1) quantize_kernel(QuantParams p) {
             }
         }
         __syncwarp();
+    } else if (warp > kQWarps) {
+        // ---------------- norm warps (fused RMSNorm): per row, the chunk sums of squares (norm
+        // warp w takes the chunk pairs w, w + 2, ...; each half-warp one chunk) and then, in
+        // norm warp 0, the row total and r; they run ahead of the quantizing warps
+        if constexpr (kNorm) {
+            const int nw = warp - kQWarps - 1;
+            const int half = lane >> 4, sub16 = lane & 15;
+            const uint32_t hm = half ? 0xFFFF0000u : 0x0000FFFFu;
+            int64_t i = 0;
+            bool ok = true;
+            for (int64_t m = blockIdx.x; m < p.M; m += gridDim.x, ++i) {
+                const int s = static_cast<int>(i % S);
+                const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
+                ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&full[s], ph, &abort_flag));
+                if (!ok) break;
+                const uint8_t* row = reinterpret_cast<const uint8_t*>(rows_s + static_cast<size_t>(s) * K);
+                float* cs = chunk_s + static_cast<size_t>(s) * nb;
+                for (int q = nw; 2 * q < nb; q += kQNormWarps) {
+                    const int b = 2 * q + half;
+                    float acc = 0.0f;
+                    if (b < nb) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(row + (b * kBlock + sub16 * 8) * 2);
+                        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[k]));
+                            acc = __fadd_rn(acc, __fmul_rn(f.x, f.x));   // squares of fp16 values are exact
+                            acc = __fadd_rn(acc, __fmul_rn(f.y, f.y));
+                        }
+                    }
+#pragma unroll
+                    for (int st = 8; st >= 1; st >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(hm, acc, st));
+                    if (b < nb && sub16 == 0) cs[b] = acc;
+                }
+                __syncwarp();
+                if (lane == 0) dev::mbar_arrive(&nsync[s]);
+                if (nw == 0) {
+                    ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&nsync[s], ph, &abort_flag));
+                    if (!ok) break;
+                    float t = 0.0f;
+                    for (int b = lane; b < nb; b += 32) t = __fadd_rn(t, cs[b]);
+#pragma unroll
+                    for (int st = 16; st >= 1; st >>= 1) t = __fadd_rn(t, __shfl_xor_sync(0xFFFFFFFFu, t, st));
+                    const float ms = __fdiv_rn(t, static_cast<float>(K));
+                    if (lane == 0) {
+                        r_s[s] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, p.eps)));
+                        dev::mbar_arrive(&rready[s]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) dev::mbar_arrive(&empty[s]);
+            }
+            if (!ok && lane == 0) abort_flag = 1;
+        }
     } else {
         // ---------------- compute warps
         const bool upper = lane >= 16;
@@ -239,6 +312,12 @@ __global__ void __launch_bounds__(kQThreads, 1) quantize_kernel(QuantParams p) {
             const uint8_t* row = reinterpret_cast<const uint8_t*>(rows_s + static_cast<size_t>(s) * K);
             const uint32_t chunk_off = ((static_cast<uint32_t>(sub >> 1) ^ static_cast<uint32_t>(m & 7)) << 4) +
                                        static_cast<uint32_t>(sub & 1) * 8u;
+            float r_norm = 1.0f;
+            if constexpr (kNorm) {
+                ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&rready[s], ph, &abort_flag));   // the row's factor
+                if (!ok) break;
+                r_norm = r_s[s];
+            }
 #pragma unroll 1
             for (int j = 0; j < iters; ++j) {                // warp-uniform bound
                 const bool valid = (valid_bits >> j) & 1u;
@@ -253,6 +332,21 @@ __global__ void __launch_bounds__(kQThreads, 1) quantize_kernel(QuantParams p) {
                         const uint32_t lo = *reinterpret_cast<const uint16_t*>(row + (gw[k] & 0xFFFFu));
                         const uint32_t hi = *reinterpret_cast<const uint16_t*>(row + (gw[k] >> 16));
                         h2[k] = __byte_perm(lo, hi, 0x5410);
+                    }
+                }
+                if constexpr (kNorm) {
+                    // normalize: y = fp16_rn((x * r) * gamma), gamma of the lane's 8 permuted channels
+                    const int bn = warp + 32 * j + (upper ? 16 : 0);
+                    const uint4 gv = valid ? __ldg(reinterpret_cast<const uint4*>(p.gamma_perm + bn * kBlock + sub * 8))
+                                           : make_uint4(0u, 0u, 0u, 0u);
+                    const uint32_t gw4[4] = {gv.x, gv.y, gv.z, gv.w};
+                    const float2 r2 = make_float2(r_norm, r_norm);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&h2[k]));
+                        const float2 g = __half22float2(*reinterpret_cast<const __half2*>(&gw4[k]));
+                        const __half2 y = __float22half2_rn(dev::fmul2(dev::fmul2(x, r2), g));   // (x * r) * g, each rounded
+                        h2[k] = *reinterpret_cast<const uint32_t*>(&y);
                     }
                 }
                 // absmax of the half-warp's 128 values
@@ -400,17 +494,21 @@ __global__ void unpack_weights_kernel(const uint8_t* Wp, int64_t N, int K, int n
 }  // namespace
 
 cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, int64_t M, void* A, void* scales,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, const void* gamma_perm, float eps) {
     const int K = L.K;
     const int iters = (L.nb + 31) / 32;
-    const size_t fixed = static_cast<size_t>(iters) * kQWarps * 32 * 16 + ((4ull * L.nb + 15) & ~15ull) + 16 * 16 + 1024;
+    const size_t fixed = static_cast<size_t>(iters) * kQWarps * 32 * 16 + ((4ull * L.nb + 15) & ~15ull) +
+                         ((4ull * 8 * L.nb + 4ull * 8 + 15) & ~15ull) + 32 * 16 + 1024;
     int stages = static_cast<int>((kQSmemBudget - fixed) / (2ull * K));
     stages = stages < 1 ? 1 : (stages > 8 ? 8 : stages);
-    const size_t smem = quant_bars_offset(K, stages, iters, L.nb) + 8ull * (2 * stages);
+    const size_t smem = quant_bars_offset(K, stages, iters, L.nb) + 8ull * (4 * stages);
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(quantize_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kQSmemBudget + 16 * 1024);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(quantize_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kQSmemBudget + 16 * 1024);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -428,8 +526,13 @@ cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, in
     p.A = static_cast<uint8_t*>(A);
     p.scales = static_cast<uint16_t*>(scales);
     p.status = L.d_status;
+    p.gamma_perm = static_cast<const uint16_t*>(gamma_perm);
+    p.eps = eps;
     const int64_t grid = M < L.num_sms ? M : L.num_sms;
-    quantize_kernel<<<static_cast<unsigned>(grid), kQThreads, smem, stream>>>(p);
+    if (gamma_perm != nullptr)
+        quantize_kernel<true><<<static_cast<unsigned>(grid), kQThreads, smem, stream>>>(p);
+    else
+        quantize_kernel<false><<<static_cast<unsigned>(grid), kQThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }
 

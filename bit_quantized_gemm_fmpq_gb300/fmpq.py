@@ -45,6 +45,7 @@ SIGNATURES = {
     "w4ax_gemm_noalloc": (_I32, [_P, _P, _P, _P, _P, _I64, _I64, _P, _I64, _P]),
     "w4ax_gemm_partials": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P]),
     "fmpq_device_status": (_I32, [_P, ctypes.POINTER(_I32), _I32]),
+    "fmpq_rmsnorm_quantize": (_I32, [_P, _P, _I64, _I64, _P, ctypes.c_float, _P, _P, _P]),
     "fmpq_channel_absmax": (_I32, [_P, _I64, _I64, _I32, _P, _P]),
     "fmpq_plan_layout": (_I32, [_I32, _P, _I32, _P, _P]),
     "fmpq_outlier_blocks": (_I32, [_I32, ctypes.c_double]),
@@ -175,6 +176,20 @@ def fmpq_quantize(layout: Layout, X, A_packed=None, a_scales=None, stream=None):
         a_scales = torch.empty((layout.nb, M), dtype=torch.float16, device=X.device)
     _check("fmpq_quantize", layout._lib.fmpq_quantize(layout.handle, _ptr(X), X.stride(0), M, _ptr(A_packed),
                                                         _ptr(a_scales), _stream(stream)))
+    return A_packed, a_scales
+
+
+def fmpq_rmsnorm_quantize(layout: Layout, X, gamma_perm, eps: float, A_packed=None, a_scales=None, stream=None):
+    """RMSNorm of X fused with the activation quantizer (gamma in the permuted channel order)."""
+    import torch
+    M = X.shape[0]
+    if A_packed is None:
+        A_packed = torch.empty(layout.packed_a_bytes(M), dtype=torch.uint8, device=X.device)
+    if a_scales is None:
+        a_scales = torch.empty((layout.nb, M), dtype=torch.float16, device=X.device)
+    _check("fmpq_rmsnorm_quantize", load_library().fmpq_rmsnorm_quantize(
+        layout.handle, _ptr(X), X.stride(0), M, _ptr(gamma_perm), ctypes.c_float(eps), _ptr(A_packed),
+        _ptr(a_scales), _stream(stream)))
     return A_packed, a_scales
 
 

@@ -109,6 +109,24 @@ FMPQ_API size_t fmpq_packed_w_bytes(const fmpq_layout* layout, int64_t N);
 FMPQ_API fmpq_status fmpq_quantize(const fmpq_layout* layout, const void* X, int64_t ldx, int64_t M,
                           void* A_packed, void* a_scales, void* stream);
 
+/* The quantizer fused with the preceding RMSNorm: the activation quantization of the QKV
+ * projection and the first FFN layer fused into the layer norm before them (QServe explainer,
+ * "运行时设计"). Codes, scales and layout are those of fmpq_quantize applied to
+ *   y[m][c] = fp16_rn( (fp32(x[m][c]) * r_m) * fp32(gamma[c]) ),
+ *   r_m = 1 / sqrt(T_m / K + eps)   (IEEE fp32 division, square root and addition),
+ * where T_m, the sum of x[m][c]^2, is formed in a fixed order so that results are reproducible:
+ * each 128-channel chunk of the row (input channel order) is summed by 16 partial sums of 8
+ * consecutive channels (sequential fp32 additions of the exact squares) combined by an xor
+ * tree of strides 8, 4, 2, 1; the chunk sums are summed by 32 partial sums taking chunks
+ * l, l + 32, l + 64, ... combined by an xor tree of strides 16, 8, 4, 2, 1.
+ *   gamma_perm  fp16 [K]: gamma in the permuted order, gamma_perm[j] = gamma[perm[j]]
+ *               (prepared once, like the weights). 16-byte aligned.
+ *   eps         positive and finite (FMPQ_ERR_INVALID_ARG otherwise).
+ * Other arguments as fmpq_quantize. */
+FMPQ_API fmpq_status fmpq_rmsnorm_quantize(const fmpq_layout* layout, const void* X, int64_t ldx, int64_t M,
+                                           const void* gamma_perm, float eps, void* A_packed, void* a_scales,
+                                           void* stream);
+
 /* Offline weight preparation: W fp16 [N][ldw] (ldw >= K, ldw % 8 == 0, N % 16 == 0)
  * -> W_packed (fmpq_packed_w_bytes) and w_scales fp16 [K/128][N], INT4 range [-7, 7]
  * per output channel and block, same scale and rounding rule as the activations, on the

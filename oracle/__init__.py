@@ -54,6 +54,7 @@ def _load():
             lib.oracle_f16_to_f32.restype = ctypes.c_float
             lib.oracle_f32_to_f16_array.argtypes = [P, i64, P]
             lib.oracle_f16_to_f32_array.argtypes = [P, i64, P]
+            lib.oracle_rmsnorm.argtypes = [P, i64, i32, i32, P, ctypes.c_float, P]
             lib.oracle_channel_absmax.argtypes = [P, i64, i32, P]
             lib.oracle_plan_layout.argtypes = [i32, P, i32, P, P]
             lib.oracle_plan_layout.restype = i32
@@ -242,3 +243,14 @@ def outlier_blocks(K: int, fraction: float) -> int:
     """ceil(round(fraction*K) / 128), halves rounded away from zero, at most K/128."""
     n_out = int(np.floor(fraction * K + 0.5))
     return min((n_out + BLOCK - 1) // BLOCK, K // BLOCK)
+
+
+def rmsnorm(X, gamma, eps: float) -> np.ndarray:
+    """RMSNorm of fp16 X [M][K] with fp16 gamma [K] (input channel order), in the reduction
+    order the library specifies; returns float16 [M][K]."""
+    X = np.ascontiguousarray(np.asarray(X, dtype=np.float16)).view(np.uint16)
+    g = np.ascontiguousarray(np.asarray(gamma, dtype=np.float16)).view(np.uint16)
+    M, K = X.shape
+    Y = np.empty((M, K), dtype=np.uint16)
+    _load().oracle_rmsnorm(_ptr(X), K, M, K, _ptr(g), ctypes.c_float(eps), _ptr(Y))
+    return Y.view(np.float16)

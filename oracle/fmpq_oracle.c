@@ -480,3 +480,57 @@ int oracle_plan_layout(int K, const uint32_t* stat, int n8, int32_t* perm, uint8
     free(in_int8);
     return 0;
 }
+
+/* ------------------------------------------------------------------------------------
+ * RMSNorm fused into the quantizer (QServe explainer, "运行时设计": the activation
+ * quantization of the QKV projection and the first FFN layer is fused into the layer norm
+ * before them; the LLaMA family's layer norm is RMSNorm, y = x / sqrt(mean(x^2) + eps) * gamma).
+ * The sum of squares is formed in the order the library specifies (16 partial sums of 8
+ * channels per 128-channel chunk with an xor tree, then 32 partial sums over the chunks with
+ * an xor tree), every step an IEEE fp32 operation, so the normalized fp16 values are exact
+ * functions of the input. The quantizer above then takes y as its input.
+ * ------------------------------------------------------------------------------------ */
+
+/* v[j] <- v[j] + v[j ^ s] for s = n/2, ..., 1 (all j at once); every entry ends equal. */
+static void xor_tree_f32(float* v, int n) {
+    float tmp[32];
+    for (int s = n / 2; s >= 1; s /= 2) {
+        for (int j = 0; j < n; ++j) tmp[j] = v[j] + v[j ^ s];
+        for (int j = 0; j < n; ++j) v[j] = tmp[j];
+    }
+}
+
+/* Y [M][K] (input channel order) = RMSNorm of X [M][ldx] with gamma [K] (input order). */
+void oracle_rmsnorm(const uint16_t* X, int64_t ldx, int M, int K, const uint16_t* gamma, float eps, uint16_t* Y) {
+    const int nb = K / 128;
+    float* chunk = (float*)malloc(sizeof(float) * (size_t)nb);
+    if (chunk == NULL) return;
+    for (int m = 0; m < M; ++m) {
+        const uint16_t* x = X + (int64_t)m * ldx;
+        for (int b = 0; b < nb; ++b) {
+            float lanes[16];
+            for (int j = 0; j < 16; ++j) {
+                float a = 0.0f;
+                for (int i = 0; i < 8; ++i) {
+                    const float v = oracle_f16_to_f32(x[128 * b + 8 * j + i]);
+                    a = a + v * v;                        /* v*v is exact: one rounding per add */
+                }
+                lanes[j] = a;
+            }
+            xor_tree_f32(lanes, 16);
+            chunk[b] = lanes[0];
+        }
+        float t[32];
+        for (int l = 0; l < 32; ++l) {
+            float a = 0.0f;
+            for (int b = l; b < nb; b += 32) a = a + chunk[b];
+            t[l] = a;
+        }
+        xor_tree_f32(t, 32);
+        const float ms = t[0] / (float)K;
+        const float r = 1.0f / sqrtf(ms + eps);
+        for (int c = 0; c < K; ++c)
+            Y[(int64_t)m * K + c] = oracle_f32_to_f16((oracle_f16_to_f32(x[c]) * r) * oracle_f16_to_f32(gamma[c]));
+    }
+    free(chunk);
+}
