@@ -104,9 +104,12 @@ __device__ __forceinline__ uint32_t pack_int4_pair(uint32_t v, int lane) {
 // INT8 high part = |q| & 0x70, whose E4M3 encoding is looked up in an 8-entry table.
 // The sign bit is the sign bit of the fp16 input.
 // ---------------------------------------------------------------------------------
-constexpr int kQWarps = 16;                        // compute warps; +1 producer warp
+// Compute warps W: per round the half-warps of warp w take blocks w + 2Wj and w + W + 2Wj. The
+// launch picks the largest W in [16, 28] with nb a multiple of 2W (every warp the same number of
+// rounds), else 16; the fused-norm kernel uses 16 compute warps and 8 norm warps.
+constexpr int kQWarpsMin = 16, kQWarpsMax = 28;
 constexpr int kQNormWarps = 8;                     // fused RMSNorm: warps computing the rows' norms
-constexpr int kQThreads = (kQWarps + 1 + kQNormWarps) * 32;
+constexpr int kQMaxThreads = (kQWarpsMax + 1) * 32;   // >= (16 + 1 + 8) * 32
 constexpr int kQSmemBudget = 200 * 1024;
 
 struct QuantParams {
@@ -114,7 +117,8 @@ struct QuantParams {
     int64_t ldx;
     int64_t M;
     int K, nb, stages;
-    int iters;              // block pairs per compute warp: ceil(nb / 32)
+    int iters;              // rounds per compute warp: ceil(nb / (2 * cwarps))
+    int cwarps;             // compute warps (the producer is warp cwarps, norm warps follow)
     const uint16_t* perm;
     const uint8_t* mask;
     const int32_t* poff;
@@ -152,8 +156,8 @@ __device__ __forceinline__ uint32_t high_plane(uint32_t w) {
 // Shared memory: [S] rows of X | gather offsets [iters][16 warps][32 lanes] (8 byte offsets of
 // 16 bits per lane and block pair) | plane offset per block | full / empty barriers per stage.
 __host__ __device__ inline size_t quant_gtab_offset(int K, int S) { return (2ull * K * S + 15) & ~15ull; }
-__host__ __device__ inline size_t quant_poff_offset(int K, int S, int iters) {
-    return quant_gtab_offset(K, S) + static_cast<size_t>(iters) * kQWarps * 32 * 16;
+__host__ __device__ inline size_t quant_poff_offset(int K, int S, int tab_entries) {
+    return quant_gtab_offset(K, S) + static_cast<size_t>(tab_entries) * 32 * 16;   // entries: iters * cwarps
 }
 __host__ __device__ inline size_t quant_chunk_offset(int K, int S, int iters, int nb) {
     return quant_poff_offset(K, S, iters) + ((4ull * nb + 15) & ~15ull);
@@ -169,15 +173,15 @@ __host__ __device__ inline size_t quant_bars_offset(int K, int S, int iters, int
 // 16 lane sums are combined by an xor tree (8, 4, 2, 1), and the chunk sums by 32 lanes taking
 // chunks l, l+32, ... sequentially and an xor tree (16, ..., 1).
 template <bool kNorm>
-__global__ void __launch_bounds__(kQThreads, 1) quantize_kernel(QuantParams p) {
+__global__ void __launch_bounds__(kQMaxThreads, 1) quantize_kernel(QuantParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int K = p.K, nb = p.nb, S = p.stages;
     uint16_t* rows_s = reinterpret_cast<uint16_t*>(smem_raw);                                // [S][K]
     uint4* gtab = reinterpret_cast<uint4*>(smem_raw + quant_gtab_offset(K, S));               // [iters][16][32]
-    int32_t* s_poff = reinterpret_cast<int32_t*>(smem_raw + quant_poff_offset(K, S, p.iters)); // [nb]
-    float* chunk_s = reinterpret_cast<float*>(smem_raw + quant_chunk_offset(K, S, p.iters, nb));  // [S][nb]
+    int32_t* s_poff = reinterpret_cast<int32_t*>(smem_raw + quant_poff_offset(K, S, p.iters * p.cwarps)); // [nb]
+    float* chunk_s = reinterpret_cast<float*>(smem_raw + quant_chunk_offset(K, S, p.iters * p.cwarps, nb));  // [S][nb]
     float* r_s = chunk_s + static_cast<size_t>(S) * nb;                                            // [S]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + quant_bars_offset(K, S, p.iters, nb));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + quant_bars_offset(K, S, p.iters * p.cwarps, nb));
     uint64_t* full = bars;            // [S] the row has landed
     uint64_t* empty = bars + S;       // [S] every reader is done with the row
     uint64_t* nsync = bars + 2 * S;   // [S] fused RMSNorm: both norm warps' chunk sums are in place
@@ -188,18 +192,19 @@ __global__ void __launch_bounds__(kQThreads, 1) quantize_kernel(QuantParams p) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             dev::mbar_init(&full[s], 1);
-            dev::mbar_init(&empty[s], kQWarps + (kNorm ? kQNormWarps : 0));
+            dev::mbar_init(&empty[s], p.cwarps + (kNorm ? kQNormWarps : 0));
             dev::mbar_init(&nsync[s], kQNormWarps);
             dev::mbar_init(&rready[s], 1);
         }
         abort_flag = 0;
         dev::fence_barrier_init();
     }
-    for (int b = threadIdx.x; b < nb; b += kQThreads) s_poff[b] = p.poff[b];
+    for (int b = threadIdx.x; b < nb; b += blockDim.x) s_poff[b] = p.poff[b];
     __syncthreads();
 
     const uint32_t row_bytes = static_cast<uint32_t>(K) * 2u;
-    if (warp == kQWarps) {
+    const int W = p.cwarps;
+    if (warp == W) {
         // ---------------- producer: rows of X into the stage ring
         if (lane == 0) {
             int64_t i = 0;
@@ -222,12 +227,12 @@ __global__ void __launch_bounds__(kQThreads, 1) quantize_kernel(QuantParams p) {
             }
         }
         __syncwarp();
-    } else if (warp > kQWarps) {
+    } else if (warp > W) {
         // ---------------- norm warps (fused RMSNorm): per row, the chunk sums of squares (norm
         // warp w takes the chunk pairs w, w + 2, ...; each half-warp one chunk) and then, in
         // norm warp 0, the row total and r; they run ahead of the quantizing warps
         if constexpr (kNorm) {
-            const int nw = warp - kQWarps - 1;
+            const int nw = warp - W - 1;
             const int half = lane >> 4, sub16 = lane & 15;
             const uint32_t hm = half ? 0xFFFF0000u : 0x0000FFFFu;
             int64_t i = 0;
@@ -283,10 +288,10 @@ __global__ void __launch_bounds__(kQThreads, 1) quantize_kernel(QuantParams p) {
         const uint32_t hmask = upper ? 0xFFFF0000u : 0x0000FFFFu;
         // per iteration j: this lane's block, its gather byte offsets (in shared memory, so the
         // loop over j stays compact), precision and validity bits
-        uint4* my_goff = gtab + warp * 32 + lane;          // entry j at my_goff[j * kQWarps * 32]
+        uint4* my_goff = gtab + warp * 32 + lane;          // entry j at my_goff[j * W * 32]
         uint32_t is8_bits = 0, valid_bits = 0;
         for (int j = 0; j < p.iters; ++j) {
-            const int b = warp + 32 * j + (upper ? 16 : 0);
+            const int b = warp + 2 * W * j + (upper ? W : 0);
             const bool valid = b < nb;
             uint4 g = make_uint4(0, 0, 0, 0);
             if (valid) {
@@ -296,10 +301,10 @@ __global__ void __launch_bounds__(kQThreads, 1) quantize_kernel(QuantParams p) {
                 if (p.mask[b]) is8_bits |= 1u << j;
                 valid_bits |= 1u << j;
             }
-            my_goff[j * kQWarps * 32] = g;
+            my_goff[j * W * 32] = g;
         }
         __syncwarp();
-        const int iters = (nb - warp + 31) / 32;            // iterations with a valid lower block
+        const int iters = (nb - warp + 2 * W - 1) / (2 * W);   // rounds with a valid lower block
         const int64_t plane_stride = p.M * kBlock;
 
         int64_t i = 0;
@@ -323,7 +328,7 @@ __global__ void __launch_bounds__(kQThreads, 1) quantize_kernel(QuantParams p) {
                 const bool valid = (valid_bits >> j) & 1u;
                 const bool is8 = (is8_bits >> j) & 1u;
                 // gather 8 fp16 values, paired into half2 words
-                const uint4 g = my_goff[j * kQWarps * 32];
+                const uint4 g = my_goff[j * W * 32];
                 uint32_t h2[4];
                 {
                     const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
@@ -336,7 +341,7 @@ __global__ void __launch_bounds__(kQThreads, 1) quantize_kernel(QuantParams p) {
                 }
                 if constexpr (kNorm) {
                     // normalize: y = fp16_rn((x * r) * gamma), gamma of the lane's 8 permuted channels
-                    const int bn = warp + 32 * j + (upper ? 16 : 0);
+                    const int bn = warp + 2 * W * j + (upper ? W : 0);
                     const uint4 gv = valid ? __ldg(reinterpret_cast<const uint4*>(p.gamma_perm + bn * kBlock + sub * 8))
                                            : make_uint4(0u, 0u, 0u, 0u);
                     const uint32_t gw4[4] = {gv.x, gv.y, gv.z, gv.w};
@@ -412,7 +417,7 @@ __global__ void __launch_bounds__(kQThreads, 1) quantize_kernel(QuantParams p) {
                 w1 |= __byte_perm(h2[2], h2[3], 0x7531) & 0x80808080u;
 
                 if (valid) {
-                    const int b = warp + 32 * j + (upper ? 16 : 0);
+                    const int b = warp + 2 * W * j + (upper ? W : 0);
                     uint8_t* dst = p.A + (static_cast<int64_t>(s_poff[b]) * p.M + m) * kBlock + chunk_off;
                     if (!is8) {
                         *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
@@ -496,12 +501,19 @@ __global__ void unpack_weights_kernel(const uint8_t* Wp, int64_t N, int K, int n
 cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, int64_t M, void* A, void* scales,
                             cudaStream_t stream, const void* gamma_perm, float eps) {
     const int K = L.K;
-    const int iters = (L.nb + 31) / 32;
-    const size_t fixed = static_cast<size_t>(iters) * kQWarps * 32 * 16 + ((4ull * L.nb + 15) & ~15ull) +
+    int cw = kQWarpsMin;
+    if (gamma_perm == nullptr)
+        for (int w = kQWarpsMax; w > kQWarpsMin; --w)
+            if (L.nb % (2 * w) == 0) {
+                cw = w;
+                break;
+            }
+    const int iters = (L.nb + 2 * cw - 1) / (2 * cw);
+    const size_t fixed = static_cast<size_t>(iters) * cw * 32 * 16 + ((4ull * L.nb + 15) & ~15ull) +
                          ((4ull * 8 * L.nb + 4ull * 8 + 15) & ~15ull) + 32 * 16 + 1024;
     int stages = static_cast<int>((kQSmemBudget - fixed) / (2ull * K));
     stages = stages < 1 ? 1 : (stages > 8 ? 8 : stages);
-    const size_t smem = quant_bars_offset(K, stages, iters, L.nb) + 8ull * (4 * stages);
+    const size_t smem = quant_bars_offset(K, stages, iters * cw, L.nb) + 8ull * (4 * stages);
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(quantize_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -520,6 +532,7 @@ cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, in
     p.nb = L.nb;
     p.stages = stages;
     p.iters = iters;
+    p.cwarps = cw;
     p.perm = L.d_perm16;
     p.mask = L.d_mask;
     p.poff = L.d_poff;
@@ -530,9 +543,9 @@ cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, in
     p.eps = eps;
     const int64_t grid = M < L.num_sms ? M : L.num_sms;
     if (gamma_perm != nullptr)
-        quantize_kernel<true><<<static_cast<unsigned>(grid), kQThreads, smem, stream>>>(p);
+        quantize_kernel<true><<<static_cast<unsigned>(grid), (cw + 1 + kQNormWarps) * 32, smem, stream>>>(p);
     else
-        quantize_kernel<false><<<static_cast<unsigned>(grid), kQThreads, smem, stream>>>(p);
+        quantize_kernel<false><<<static_cast<unsigned>(grid), (cw + 1) * 32, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
