@@ -172,8 +172,9 @@ __host__ __device__ inline size_t quant_bars_offset(int K, int S, int iters, int
 // by 16 lanes of 8 consecutive channels each (sequential fp32 adds of the exact squares), the
 // 16 lane sums are combined by an xor tree (8, 4, 2, 1), and the chunk sums by 32 lanes taking
 // chunks l, l+32, ... sequentially and an xor tree (16, ..., 1).
-template <bool kNorm>
-__global__ void __launch_bounds__(kQMaxThreads, 1) quantize_kernel(QuantParams p) {
+// kTwo: the 16-warp instantiation that two CTAs share an SM with (registers bounded for it).
+template <bool kNorm, bool kTwo = false>
+__global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, kTwo ? 2 : 1) quantize_kernel(QuantParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int K = p.K, nb = p.nb, S = p.stages;
     uint16_t* rows_s = reinterpret_cast<uint16_t*>(smem_raw);                                // [S][K]
@@ -511,8 +512,29 @@ cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, in
     const int iters = (L.nb + 2 * cw - 1) / (2 * cw);
     const size_t fixed = static_cast<size_t>(iters) * cw * 32 * 16 + ((4ull * L.nb + 15) & ~15ull) +
                          ((4ull * 8 * L.nb + 4ull * 8 + 15) & ~15ull) + 32 * 16 + 1024;
-    int stages = static_cast<int>((kQSmemBudget - fixed) / (2ull * K));
-    stages = stages < 1 ? 1 : (stages > 8 ? 8 : stages);
+    auto stages_for = [&](size_t budget) {
+        const int st = budget > fixed ? static_cast<int>((budget - fixed) / (2ull * K)) : 0;
+        return st > 8 ? 8 : st;
+    };
+    // Short rows: two CTAs per SM (16 compute warps each) when each still gets 3+ row stages in
+    // half the budget and both fit; the warps of the second CTA hide the first one's latencies.
+    int per_sm = 1;
+    int stages = stages_for(kQSmemBudget);
+    if (gamma_perm == nullptr && cw == kQWarpsMin && stages_for(kQSmemBudget / 2) >= 3) {
+        const int st2 = stages_for(kQSmemBudget / 2);
+        const size_t smem2 = quant_bars_offset(K, st2, iters * cw, L.nb) + 8ull * (4 * st2);
+        int blocks = 0;
+        if (cudaFuncSetAttribute(quantize_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kQSmemBudget + 16 * 1024) == cudaSuccess &&
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, quantize_kernel<false, true>, (cw + 1) * 32, smem2) ==
+                cudaSuccess &&
+            blocks >= 2) {
+            per_sm = 2;
+            stages = st2;
+        }
+        cudaGetLastError();   // a failed query leaves no sticky error behind
+    }
+    stages = stages < 1 ? 1 : stages;
     const size_t smem = quant_bars_offset(K, stages, iters * cw, L.nb) + 8ull * (4 * stages);
     static bool attr_set = false;
     if (!attr_set) {
@@ -541,9 +563,12 @@ cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, in
     p.status = L.d_status;
     p.gamma_perm = static_cast<const uint16_t*>(gamma_perm);
     p.eps = eps;
-    const int64_t grid = M < L.num_sms ? M : L.num_sms;
+    const int64_t ctas = static_cast<int64_t>(L.num_sms) * per_sm;
+    const int64_t grid = M < ctas ? M : ctas;
     if (gamma_perm != nullptr)
         quantize_kernel<true><<<static_cast<unsigned>(grid), (cw + 1 + kQNormWarps) * 32, smem, stream>>>(p);
+    else if (per_sm == 2)
+        quantize_kernel<false, true><<<static_cast<unsigned>(grid), (cw + 1) * 32, smem, stream>>>(p);
     else
         quantize_kernel<false><<<static_cast<unsigned>(grid), (cw + 1) * 32, smem, stream>>>(p);
     return cudaGetLastError();
