@@ -265,7 +265,8 @@ def run_sweep(args):
     configs += [(f"decode_m{m}", (lambda m=m: wl.decode(m))) for m in (1, 8, 16, 32, 64, 128)]
     configs += [(f"load_balance_{int(f * 100)}pct", (lambda f=f: wl.load_balance(f))) for f in (0.0, 0.10, 0.25, 0.50)]
     if args.sweep_only:
-        names = [c[0] for c in configs] + ["rmsnorm_quantize_llama70b_down", "calibrate_llama70b_down"]
+        names = [c[0] for c in configs] + ["rmsnorm_quantize_llama70b_down", "outlier_split_llama70b_down",
+                                           "calibrate_llama70b_down"]
         if args.sweep_only not in names:
             raise SystemExit(f"unknown workload {args.sweep_only}; one of {names}")
         configs = [c for c in configs if c[0] == args.sweep_only]
@@ -348,6 +349,38 @@ def run_sweep(args):
                           "gbs": nbytes / (ms * 1e-3) / 1e9, "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm,
                           "l2": "flushed before every timed launch", "clocks": clocks}), flush=True)
         del layout
+    if not args.sweep_only or args.sweep_only == "outlier_split_llama70b_down":
+        # outlier split: 256 outlier channels in FP16 (cuBLAS), the other 28416 through the INT4 path
+        w = wl.llama70b_down()
+        n_out = 256
+        rng = np.random.default_rng(6)
+        out_cols = np.sort(rng.choice(w.K, size=n_out, replace=False)).astype(np.int32)
+        base = np.setdiff1d(np.arange(w.K), out_cols).astype(np.int32)
+        Kb = base.size
+        layout = fmpq.select_layout(Kb, w.K, base, np.zeros(Kb // 128, dtype=np.uint8))
+        X = torch.from_numpy(w.X).cuda()
+        Wd = torch.from_numpy(w.W).cuda()
+        Wp, sw = fmpq.w4_pack_weights(layout, Wd)
+        W_out = Wd[:, torch.from_numpy(out_cols).long().cuda()].contiguous()
+        del Wd
+        cols = torch.from_numpy(out_cols).cuda()
+        A = torch.empty(layout.packed_a_bytes(w.M), dtype=torch.uint8, device="cuda")
+        sx = torch.empty((layout.nb, w.M), dtype=torch.float16, device="cuda")
+        Y = torch.empty((w.M, w.N), dtype=torch.float16, device="cuda")
+        X_out = torch.empty((w.M, n_out), dtype=torch.float16, device="cuda")
+        ws = layout.workspace(w.M, w.N)
+        fmpq.fmpq_quantize(layout, X, A, sx)
+        sampler.start()
+        ms_base = timed(lambda: fmpq.w4ax_gemm(layout, A, sx, Wp, sw, w.M, w.N, Y, workspace=ws))
+        ms_out = timed(lambda: fmpq.fmpq_outlier_gemm_fp16(X, cols, W_out, Y, X_out))
+        clocks = sampler.stop()
+        print(json.dumps({"sweep": "outlier_split_llama70b_down", "M": w.M, "K_base": Kb, "n_out": n_out, "N": w.N,
+                          "int4_path_ms": ms_base, "fp16_outlier_path_ms": ms_out,
+                          "int4_path_tflops_effective": 2.0 * w.M * w.N * Kb / (ms_base * 1e-3) / 1e12,
+                          "fp16_outlier_path_tflops": 2.0 * w.M * w.N * n_out / (ms_out * 1e-3) / 1e12,
+                          "l2": "flushed before every timed launch", "clocks": clocks}), flush=True)
+        del layout, Wp, sw, W_out, X, A, sx, Y, X_out, ws
+        torch.cuda.empty_cache()
     if not args.sweep_only or args.sweep_only == "calibrate_llama70b_down":
         # offline calibration: per-channel absmax over the 4096 x 28672 activations (HBM-bound)
         w = wl.llama70b_down()

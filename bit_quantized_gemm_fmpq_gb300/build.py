@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libfmpq_gb300.so")
-SOURCES = ["fmpq_api.cu", "fmpq_quantize.cu", "fmpq_gemm.cu", "fmpq_gemm_small.cu", "fmpq_noalloc.cu", "fmpq_calib.cu"]
+SOURCES = ["fmpq_api.cu", "fmpq_quantize.cu", "fmpq_gemm.cu", "fmpq_gemm_small.cu", "fmpq_noalloc.cu", "fmpq_calib.cu", "fmpq_outlier.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]
 

@@ -25,21 +25,19 @@ fmpq_status check_device(const fmpq_layout* L) {
 
 fmpq_status launched(cudaError_t e) { return e == cudaSuccess ? FMPQ_OK : FMPQ_ERR_CUDA; }
 
-}  // namespace
-
-extern "C" {
-
-fmpq_status fmpq_layout_create(int32_t K, const int32_t* perm_host, const uint8_t* outlier_block_mask_host,
-                               fmpq_layout** out) {
+// Layout over K gathered channels taken from input rows of K_in >= K channels.
+fmpq_status create_layout(int32_t K, int32_t K_in, const int32_t* perm_host, const uint8_t* outlier_block_mask_host,
+                          fmpq_layout** out) {
     if (out == nullptr || perm_host == nullptr || outlier_block_mask_host == nullptr) return FMPQ_ERR_INVALID_ARG;
     *out = nullptr;
     if (K < FMPQ_BLOCK || K > FMPQ_MAX_K || K % FMPQ_BLOCK != 0) return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (K_in < K || K_in > FMPQ_MAX_K || K_in % 8 != 0) return FMPQ_ERR_UNSUPPORTED_SHAPE;
     const int nb = K / FMPQ_BLOCK;
-    std::vector<uint8_t> seen(static_cast<size_t>(K), 0);
+    std::vector<uint8_t> seen(static_cast<size_t>(K_in), 0);
     std::vector<uint16_t> perm16(static_cast<size_t>(K));
     for (int j = 0; j < K; ++j) {
         const int32_t c = perm_host[j];
-        if (c < 0 || c >= K || seen[c]) return FMPQ_ERR_INVALID_ARG;
+        if (c < 0 || c >= K_in || seen[c]) return FMPQ_ERR_INVALID_ARG;
         seen[c] = 1;
         perm16[j] = static_cast<uint16_t>(c);
     }
@@ -65,6 +63,7 @@ fmpq_status fmpq_layout_create(int32_t K, const int32_t* perm_host, const uint8_
     fmpq_layout* L = new (std::nothrow) fmpq_layout();
     if (L == nullptr) return FMPQ_ERR_INVALID_ARG;
     L->K = K;
+    L->K_in = K_in;
     L->nb = nb;
     L->n8 = n8;
     L->device = dev;
@@ -85,6 +84,20 @@ fmpq_status fmpq_layout_create(int32_t K, const int32_t* perm_host, const uint8_
     }
     *out = L;
     return FMPQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fmpq_status fmpq_layout_create(int32_t K, const int32_t* perm_host, const uint8_t* outlier_block_mask_host,
+                               fmpq_layout** out) {
+    return create_layout(K, K, perm_host, outlier_block_mask_host, out);
+}
+
+fmpq_status fmpq_layout_create_select(int32_t K, int32_t K_in, const int32_t* select_host,
+                                      const uint8_t* outlier_block_mask_host, fmpq_layout** out) {
+    return create_layout(K, K_in, select_host, outlier_block_mask_host, out);
 }
 
 void fmpq_layout_destroy(fmpq_layout* L) {
@@ -119,7 +132,7 @@ size_t fmpq_packed_w_bytes(const fmpq_layout* L, int64_t N) {
 fmpq_status fmpq_quantize(const fmpq_layout* L, const void* X, int64_t ldx, int64_t M, void* A_packed,
                           void* a_scales, void* stream) {
     if (L == nullptr || X == nullptr || A_packed == nullptr || a_scales == nullptr) return FMPQ_ERR_INVALID_ARG;
-    if (M < 1 || M > INT32_MAX || ldx < L->K) return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (M < 1 || M > INT32_MAX || ldx < L->K_in) return FMPQ_ERR_UNSUPPORTED_SHAPE;
     if (ldx % 8 != 0 || !aligned16(X) || !aligned16(A_packed) || !aligned16(a_scales)) return FMPQ_ERR_MISALIGNED;
     if (fmpq_status st = check_device(L)) return st;
     return launched(fmpq::launch_quantize(*L, X, ldx, M, A_packed, a_scales, static_cast<cudaStream_t>(stream)));
@@ -130,7 +143,7 @@ fmpq_status fmpq_rmsnorm_quantize(const fmpq_layout* L, const void* X, int64_t l
     if (L == nullptr || X == nullptr || gamma_perm == nullptr || A_packed == nullptr || a_scales == nullptr)
         return FMPQ_ERR_INVALID_ARG;
     if (!(eps > 0.0f) || !(eps < 1e30f)) return FMPQ_ERR_INVALID_ARG;   // positive and finite
-    if (M < 1 || M > INT32_MAX || ldx < L->K) return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (M < 1 || M > INT32_MAX || ldx < L->K || L->K_in != L->K) return FMPQ_ERR_UNSUPPORTED_SHAPE;
     if (ldx % 8 != 0 || !aligned16(X) || !aligned16(gamma_perm) || !aligned16(A_packed) || !aligned16(a_scales))
         return FMPQ_ERR_MISALIGNED;
     if (fmpq_status st = check_device(L)) return st;
@@ -141,7 +154,7 @@ fmpq_status fmpq_rmsnorm_quantize(const fmpq_layout* L, const void* X, int64_t l
 fmpq_status w4_pack_weights(const fmpq_layout* L, const void* W, int64_t ldw, int64_t N, void* W_packed,
                             void* w_scales, void* stream) {
     if (L == nullptr || W == nullptr || W_packed == nullptr || w_scales == nullptr) return FMPQ_ERR_INVALID_ARG;
-    if (N < 16 || N % 16 != 0 || N > INT32_MAX || ldw < L->K) return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (N < 16 || N % 16 != 0 || N > INT32_MAX || ldw < L->K_in) return FMPQ_ERR_UNSUPPORTED_SHAPE;
     if (ldw % 8 != 0 || !aligned16(W) || !aligned16(W_packed) || !aligned16(w_scales)) return FMPQ_ERR_MISALIGNED;
     if (fmpq_status st = check_device(L)) return st;
     return launched(fmpq::launch_pack_weights(*L, W, ldw, N, W_packed, w_scales, static_cast<cudaStream_t>(stream)));
@@ -226,6 +239,23 @@ fmpq_status fmpq_channel_absmax(const void* X, int64_t ldx, int64_t T, int32_t K
         return FMPQ_ERR_DEVICE;
     if (major != 10 || minor != 3) return FMPQ_ERR_DEVICE;
     return launched(fmpq::launch_channel_absmax(X, ldx, T, K, absmax, sms, static_cast<cudaStream_t>(stream)));
+}
+
+fmpq_status fmpq_outlier_gemm_fp16(const void* X, int64_t ldx, int64_t M, const int32_t* cols, int32_t n_out,
+                                   const void* W_out, int64_t ldw_out, int64_t N, void* X_out, void* Y, int64_t ldy,
+                                   void* stream) {
+    if (X == nullptr || cols == nullptr || W_out == nullptr || X_out == nullptr || Y == nullptr)
+        return FMPQ_ERR_INVALID_ARG;
+    if (M < 1 || M > INT32_MAX || n_out < 8 || n_out % 8 != 0 || n_out > FMPQ_MAX_K || N < 1 || N > INT32_MAX ||
+        ldx < 1 || ldw_out < n_out || ldy < N || ldw_out > INT32_MAX || ldy > INT32_MAX)
+        return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (ldx % 8 != 0 || ldw_out % 8 != 0 || ldy % 8 != 0 || !aligned16(X) || !aligned16(cols) || !aligned16(W_out) ||
+        !aligned16(X_out) || !aligned16(Y))
+        return FMPQ_ERR_MISALIGNED;
+    bool cublas_ok = true;
+    const cudaError_t e = fmpq::launch_outlier_gemm(X, ldx, M, cols, n_out, W_out, ldw_out, N, X_out, Y, ldy,
+                                                    static_cast<cudaStream_t>(stream), &cublas_ok);
+    return (e == cudaSuccess && cublas_ok) ? FMPQ_OK : FMPQ_ERR_CUDA;
 }
 
 fmpq_status fmpq_plan_layout(int32_t K, const uint32_t* absmax_host, int32_t n8, int32_t* perm_host,

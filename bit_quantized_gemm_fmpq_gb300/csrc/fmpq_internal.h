@@ -7,6 +7,7 @@
 
 struct fmpq_layout {
     int32_t K = 0;
+    int32_t K_in = 0;        // input row width the permutation selects from (K for a full permutation)
     int32_t nb = 0;          // K / 128
     int32_t n8 = 0;          // number of INT8 blocks
     int device = -1;
@@ -54,6 +55,12 @@ struct GemmArgs {
 size_t gemm_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N);
 size_t gemm_counter_bytes(const fmpq_layout& L, int64_t M, int64_t N);
 cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& args, cudaStream_t stream);
+
+// Outlier split, FP16 path: gather X[:, cols] into X_out, Y += X_out * W_out^T (cuBLAS, loaded on
+// first use). *cublas_ok is false when cuBLAS cannot be loaded or a cuBLAS call fails.
+cudaError_t launch_outlier_gemm(const void* X, int64_t ldx, int64_t M, const int32_t* cols, int n_out,
+                                const void* W_out, int64_t ldw_out, int64_t N, void* X_out, void* Y, int64_t ldy,
+                                cudaStream_t stream, bool* cublas_ok);
 
 // Calibration: per-channel absmax (zeroes `out`, then reduces) and the host layout planner.
 cudaError_t launch_channel_absmax(const void* X, int64_t ldx, int64_t T, int K, uint32_t* out, int num_sms,

@@ -117,6 +117,7 @@ struct QuantParams {
     int64_t ldx;
     int64_t M;
     int K, nb, stages;
+    int Kin;                // staged row width: the channels a layout may select from (>= K)
     int iters;              // rounds per compute warp: ceil(nb / (2 * cwarps))
     int cwarps;             // compute warps (the producer is warp cwarps, norm warps follow)
     const uint16_t* perm;
@@ -176,13 +177,13 @@ __host__ __device__ inline size_t quant_bars_offset(int K, int S, int iters, int
 template <bool kNorm, bool kTwo = false>
 __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, kTwo ? 2 : 1) quantize_kernel(QuantParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    const int K = p.K, nb = p.nb, S = p.stages;
-    uint16_t* rows_s = reinterpret_cast<uint16_t*>(smem_raw);                                // [S][K]
-    uint4* gtab = reinterpret_cast<uint4*>(smem_raw + quant_gtab_offset(K, S));               // [iters][16][32]
-    int32_t* s_poff = reinterpret_cast<int32_t*>(smem_raw + quant_poff_offset(K, S, p.iters * p.cwarps)); // [nb]
-    float* chunk_s = reinterpret_cast<float*>(smem_raw + quant_chunk_offset(K, S, p.iters * p.cwarps, nb));  // [S][nb]
+    const int K = p.K, Kr = p.Kin, nb = p.nb, S = p.stages;
+    uint16_t* rows_s = reinterpret_cast<uint16_t*>(smem_raw);                                // [S][Kin]
+    uint4* gtab = reinterpret_cast<uint4*>(smem_raw + quant_gtab_offset(Kr, S));              // [iters][W][32]
+    int32_t* s_poff = reinterpret_cast<int32_t*>(smem_raw + quant_poff_offset(Kr, S, p.iters * p.cwarps)); // [nb]
+    float* chunk_s = reinterpret_cast<float*>(smem_raw + quant_chunk_offset(Kr, S, p.iters * p.cwarps, nb));  // [S][nb]
     float* r_s = chunk_s + static_cast<size_t>(S) * nb;                                            // [S]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + quant_bars_offset(K, S, p.iters * p.cwarps, nb));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + quant_bars_offset(Kr, S, p.iters * p.cwarps, nb));
     uint64_t* full = bars;            // [S] the row has landed
     uint64_t* empty = bars + S;       // [S] every reader is done with the row
     uint64_t* nsync = bars + 2 * S;   // [S] fused RMSNorm: both norm warps' chunk sums are in place
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
     for (int b = threadIdx.x; b < nb; b += blockDim.x) s_poff[b] = p.poff[b];
     __syncthreads();
 
-    const uint32_t row_bytes = static_cast<uint32_t>(K) * 2u;
+    const uint32_t row_bytes = static_cast<uint32_t>(Kr) * 2u;
     const int W = p.cwarps;
     if (warp == W) {
         // ---------------- producer: rows of X into the stage ring
@@ -217,7 +218,7 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
                     break;
                 }
                 dev::mbar_arrive_expect_tx(&full[s], row_bytes);
-                dev::bulk_g2s(rows_s + static_cast<size_t>(s) * K, p.X + m * p.ldx, row_bytes, &full[s]);
+                dev::bulk_g2s(rows_s + static_cast<size_t>(s) * Kr, p.X + m * p.ldx, row_bytes, &full[s]);
             }
             // drain: every stage's latest copy must have landed before the CTA exits
             const int64_t issued = i;
@@ -243,7 +244,7 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
                 const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
                 ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&full[s], ph, &abort_flag));
                 if (!ok) break;
-                const uint8_t* row = reinterpret_cast<const uint8_t*>(rows_s + static_cast<size_t>(s) * K);
+                const uint8_t* row = reinterpret_cast<const uint8_t*>(rows_s + static_cast<size_t>(s) * Kr);
                 float* cs = chunk_s + static_cast<size_t>(s) * nb;
                 for (int q = nw; 2 * q < nb; q += kQNormWarps) {
                     const int b = 2 * q + half;
@@ -315,7 +316,7 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
             const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
             ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&full[s], ph, &abort_flag));   // every lane waits
             if (!ok) break;
-            const uint8_t* row = reinterpret_cast<const uint8_t*>(rows_s + static_cast<size_t>(s) * K);
+            const uint8_t* row = reinterpret_cast<const uint8_t*>(rows_s + static_cast<size_t>(s) * Kr);
             const uint32_t chunk_off = ((static_cast<uint32_t>(sub >> 1) ^ static_cast<uint32_t>(m & 7)) << 4) +
                                        static_cast<uint32_t>(sub & 1) * 8u;
             float r_norm = 1.0f;
@@ -501,7 +502,7 @@ __global__ void unpack_weights_kernel(const uint8_t* Wp, int64_t N, int K, int n
 
 cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, int64_t M, void* A, void* scales,
                             cudaStream_t stream, const void* gamma_perm, float eps) {
-    const int K = L.K;
+    const int K = L.K, Kin = L.K_in;
     int cw = kQWarpsMin;
     if (gamma_perm == nullptr)
         for (int w = kQWarpsMax; w > kQWarpsMin; --w)
@@ -513,7 +514,7 @@ cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, in
     const size_t fixed = static_cast<size_t>(iters) * cw * 32 * 16 + ((4ull * L.nb + 15) & ~15ull) +
                          ((4ull * 8 * L.nb + 4ull * 8 + 15) & ~15ull) + 32 * 16 + 1024;
     auto stages_for = [&](size_t budget) {
-        const int st = budget > fixed ? static_cast<int>((budget - fixed) / (2ull * K)) : 0;
+        const int st = budget > fixed ? static_cast<int>((budget - fixed) / (2ull * Kin)) : 0;
         return st > 8 ? 8 : st;
     };
     // Short rows: two CTAs per SM (16 compute warps each) when each still gets 3+ row stages in
@@ -522,7 +523,7 @@ cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, in
     int stages = stages_for(kQSmemBudget);
     if (gamma_perm == nullptr && cw == kQWarpsMin && stages_for(kQSmemBudget / 2) >= 3) {
         const int st2 = stages_for(kQSmemBudget / 2);
-        const size_t smem2 = quant_bars_offset(K, st2, iters * cw, L.nb) + 8ull * (4 * st2);
+        const size_t smem2 = quant_bars_offset(Kin, st2, iters * cw, L.nb) + 8ull * (4 * st2);
         int blocks = 0;
         if (cudaFuncSetAttribute(quantize_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kQSmemBudget + 16 * 1024) == cudaSuccess &&
@@ -535,7 +536,7 @@ cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, in
         cudaGetLastError();   // a failed query leaves no sticky error behind
     }
     stages = stages < 1 ? 1 : stages;
-    const size_t smem = quant_bars_offset(K, stages, iters * cw, L.nb) + 8ull * (4 * stages);
+    const size_t smem = quant_bars_offset(Kin, stages, iters * cw, L.nb) + 8ull * (4 * stages);
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(quantize_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -551,6 +552,7 @@ cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, in
     p.ldx = ldx;
     p.M = M;
     p.K = K;
+    p.Kin = Kin;
     p.nb = L.nb;
     p.stages = stages;
     p.iters = iters;

@@ -46,6 +46,8 @@ SIGNATURES = {
     "w4ax_gemm_partials": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P]),
     "fmpq_device_status": (_I32, [_P, ctypes.POINTER(_I32), _I32]),
     "fmpq_rmsnorm_quantize": (_I32, [_P, _P, _I64, _I64, _P, ctypes.c_float, _P, _P, _P]),
+    "fmpq_layout_create_select": (_I32, [_I32, _I32, _P, _P, ctypes.POINTER(_P)]),
+    "fmpq_outlier_gemm_fp16": (_I32, [_P, _I64, _I64, _P, _I32, _P, _I64, _I64, _P, _P, _I64, _P]),
     "fmpq_channel_absmax": (_I32, [_P, _I64, _I64, _I32, _P, _P]),
     "fmpq_plan_layout": (_I32, [_I32, _P, _I32, _P, _P]),
     "fmpq_outlier_blocks": (_I32, [_I32, ctypes.c_double]),
@@ -292,3 +294,40 @@ def fmpq_outlier_blocks(K: int, fraction: float) -> int:
     if n8 < 0:
         raise ValueError("K must be a multiple of 128 in [128, 32768] and fraction in [0, 1]")
     return n8
+
+
+# ---------------------------------------------------------------------- outlier split (QUIK)
+
+def select_layout(K: int, K_in: int, select, mask) -> "Layout":
+    """A Layout over K channels selected (distinct indices < K_in) from rows of K_in channels."""
+    lib = load_library()
+    sel = np.ascontiguousarray(select, dtype=np.int32)
+    mask = np.ascontiguousarray(mask, dtype=np.uint8)
+    if sel.shape != (K,) or mask.shape != (K // BLOCK,):
+        raise ValueError("select must have K entries and mask K/128 entries")
+    h = ctypes.c_void_p()
+    _check("fmpq_layout_create_select",
+           lib.fmpq_layout_create_select(K, K_in, sel.ctypes.data, mask.ctypes.data, ctypes.byref(h)))
+    lay = Layout.__new__(Layout)
+    lay._h = h
+    lay._lib = lib
+    lay.K = K
+    lay.nb = K // BLOCK
+    lay.mask = mask.copy()
+    lay.perm = sel.copy()
+    lay._workspaces = {}
+    return lay
+
+
+def fmpq_outlier_gemm_fp16(X, cols, W_out, Y, X_out=None, stream=None):
+    """Y += X[:, cols] @ W_out^T in FP16 (the outlier path of an outlier split)."""
+    import torch
+    M = X.shape[0]
+    n_out = cols.numel()
+    N = W_out.shape[0]
+    if X_out is None:
+        X_out = torch.empty((M, n_out), dtype=torch.float16, device=X.device)
+    _check("fmpq_outlier_gemm_fp16", load_library().fmpq_outlier_gemm_fp16(
+        _ptr(X), X.stride(0), M, _ptr(cols), n_out, _ptr(W_out), W_out.stride(0), N, _ptr(X_out), _ptr(Y),
+        Y.stride(0), _stream(stream)))
+    return Y

@@ -74,6 +74,14 @@ typedef struct fmpq_layout fmpq_layout;
  * Uploads small device tables on the current device (synchronous). */
 FMPQ_API fmpq_status fmpq_layout_create(int32_t K, const int32_t* perm_host,
                                const uint8_t* outlier_block_mask_host, fmpq_layout** out);
+/* A layout that selects its K channels from wider input rows of K_in channels (K <= K_in <=
+ * FMPQ_MAX_K, K_in % 8 == 0): select_host[K] holds distinct channel indices in [0, K_in). The
+ * quantizer and the weight packing then take rows of at least K_in channels (ldx, ldw >= K_in).
+ * This is the base part of an outlier split (QUIK explainer, "第二步: 前向传播"): the base
+ * channels go through the INT4/INT8 GEMM, the outlier channels through fmpq_outlier_gemm_fp16.
+ * fmpq_rmsnorm_quantize needs K_in == K. */
+FMPQ_API fmpq_status fmpq_layout_create_select(int32_t K, int32_t K_in, const int32_t* select_host,
+                                               const uint8_t* outlier_block_mask_host, fmpq_layout** out);
 FMPQ_API void fmpq_layout_destroy(fmpq_layout* layout);
 FMPQ_API int32_t fmpq_layout_k(const fmpq_layout* layout);
 FMPQ_API int32_t fmpq_layout_num_blocks(const fmpq_layout* layout);
@@ -182,6 +190,22 @@ FMPQ_API fmpq_status w4ax_gemm_partials(const fmpq_layout* layout, const void* A
                                const void* W_packed, int64_t M, int64_t N, int64_t m0,
                                int64_t mcount, int64_t n0, int64_t ncount, int32_t* P,
                                void* stream);
+
+/* The FP16 path of an outlier split (QUIK explainer, "第二步: 前向传播": the outlier columns are
+ * multiplied in FP16 by the unquantized outlier weights and added to the INT4 path's result):
+ *   X_out[m][j] = X[m][cols[j]]   (0 for an index outside [0, ldx))
+ *   Y[m][n]    += sum_j X_out[m][j] * W_out[n][j]   (FP32 accumulation, fp16 result)
+ *   X          fp16 [M][ldx] (device); cols int32 [n_out] (device); n_out % 8 == 0.
+ *   W_out      fp16 [N][ldw_out], ldw_out >= n_out, the outlier columns of the weights (offline).
+ *   X_out      fp16 [M][n_out] device workspace (caller-owned), overwritten.
+ *   Y          fp16 [M][ldy], ldy >= N: read and updated in place (run the INT4 path first).
+ * The product is a plain FP16 GEMM from cuBLAS, loaded at run time on the first call (which
+ * also creates the device's cuBLAS handle: make it before any stream capture). Calls on one
+ * device share that handle and are serialized by a host lock. FMPQ_ERR_CUDA if cuBLAS cannot
+ * be loaded or fails. */
+FMPQ_API fmpq_status fmpq_outlier_gemm_fp16(const void* X, int64_t ldx, int64_t M, const int32_t* cols,
+                                            int32_t n_out, const void* W_out, int64_t ldw_out, int64_t N,
+                                            void* X_out, void* Y, int64_t ldy, void* stream);
 
 /* ---- Offline layout derivation from calibration activations ----
  * The activation outliers sit in a small set of channels (about 10%: COMET news article,

@@ -254,3 +254,24 @@ def rmsnorm(X, gamma, eps: float) -> np.ndarray:
     Y = np.empty((M, K), dtype=np.uint16)
     _load().oracle_rmsnorm(_ptr(X), K, M, K, _ptr(g), ctypes.c_float(eps), _ptr(Y))
     return Y.view(np.float16)
+
+
+# ---------------------------------------------------------------------- outlier split (QUIK)
+
+def quik_reference(X, W, base_cols, out_cols):
+    """QUIK explainer, "第二步: 前向传播": the base columns go through the INT4 path (all blocks
+    INT4, channels in the given order), the outlier columns stay FP16; Y is the sum. Returns
+    (Y_base, Y_outlier) in float64."""
+    base_cols = np.asarray(base_cols, dtype=np.int64)
+    out_cols = np.asarray(out_cols, dtype=np.int64)
+    Xb = np.ascontiguousarray(np.asarray(X, dtype=np.float16)[:, base_cols])
+    Wb = np.ascontiguousarray(np.asarray(W, dtype=np.float16)[:, base_cols])
+    K = base_cols.size
+    ident = np.arange(K, dtype=np.int32)
+    mask = np.zeros(K // BLOCK, dtype=np.uint8)
+    _, sx, Aq = quantize_activations(Xb, ident, mask)
+    Wq, sw = quantize_weights(Wb, ident)
+    Y_base = epilogue(partials(Aq, Wq), sx, sw)
+    Xo = np.asarray(X, dtype=np.float16)[:, out_cols].astype(np.float64)
+    Wo = np.asarray(W, dtype=np.float16)[:, out_cols].astype(np.float64)
+    return Y_base, Xo @ Wo.T

@@ -1,0 +1,95 @@
+"""Outlier split (QUIK explainer, "第二步: 前向传播"): the base columns through the INT4 path
+(a layout selecting them from the full rows), the outlier columns in FP16 (gathered, then a
+plain FP16 GEMM added to the output).
+
+CPU: the reference pinned against the full-layout reference. GPU: the selected-layout quantizer
+bit-exact against the oracle on the gathered base columns; the INT4 path's output against its
+exact value within the output tolerance, and the merged output (the INT4 output in fp16 plus the
+FP16 outlier product, as the pages merge them) against that fp16 output plus the exact outlier
+product within the fp16 roundings of the merge."""
+import numpy as np
+import pytest
+
+from bit_quantized_gemm_fmpq_gb300 import workloads as wl
+
+BLOCK = 128
+
+
+def _problem(M, K_base, n_out, N, seed):
+    rng = np.random.default_rng(seed)
+    K_in = K_base + n_out
+    out_cols = np.sort(rng.choice(K_in, size=n_out, replace=False)).astype(np.int32)
+    base_cols = np.setdiff1d(np.arange(K_in), out_cols).astype(np.int32)
+    X32 = rng.standard_normal((M, K_in)).astype(np.float32)
+    X32[:, out_cols] *= rng.uniform(20.0, 80.0, size=n_out).astype(np.float32)
+    W = (rng.standard_normal((N, K_in)) * 0.02).astype(np.float16)
+    return X32.astype(np.float16), W, base_cols, out_cols
+
+
+def test_reference_base_part_is_the_int4_gemm_of_the_base_columns(oracle_mod):
+    """With the outlier columns of X zeroed the outlier part is 0, and the base part is the
+    full reference of the gathered base problem with every block INT4."""
+    X, W, base, out = _problem(24, 256, 16, 64, 3)
+    X[:, out] = 0
+    yb, yo = oracle_mod.quik_reference(X, W, base, out)
+    assert np.all(yo == 0)
+    Xb, Wb = np.ascontiguousarray(X[:, base]), np.ascontiguousarray(W[:, base])
+    ref = oracle_mod.reference(Xb, Wb, np.arange(base.size, dtype=np.int32), np.zeros(base.size // BLOCK, np.uint8))
+    assert np.array_equal(yb, ref["Y"])
+
+
+@pytest.fixture(scope="module")
+def fmpq_gpu():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_quantized_gemm_fmpq_gb300 import build, fmpq
+    build.build()
+    fmpq.load_library()
+    return fmpq
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("M,K_base,n_out,N", [(256, 1024, 128, 512), (37, 512, 256, 272), (1, 384, 64, 1024)])
+def test_outlier_split_end_to_end(fmpq_gpu, oracle_mod, M, K_base, n_out, N):
+    import torch
+    from tests.gpu_helpers import Y_TOL, y_error
+    X, W, base, out = _problem(M, K_base, n_out, N, M + N)
+    layout = fmpq_gpu.select_layout(K_base, K_base + n_out, base, np.zeros(K_base // BLOCK, np.uint8))
+    Xd = torch.from_numpy(X).cuda()
+    A, sx = fmpq_gpu.fmpq_quantize(layout, Xd)
+    A_ref, sx_ref, _ = oracle_mod.quantize_activations(np.ascontiguousarray(X[:, base]),
+                                                      np.arange(K_base, dtype=np.int32), np.zeros(K_base // BLOCK, np.uint8))
+    assert np.array_equal(A.cpu().numpy(), A_ref) and np.array_equal(sx.cpu().numpy().view(np.uint16), sx_ref)
+    Wp, sw = fmpq_gpu.w4_pack_weights(layout, torch.from_numpy(W).cuda())
+    Y = fmpq_gpu.w4ax_gemm(layout, A, sx, Wp, sw, M, N)
+    yb, yo = oracle_mod.quik_reference(X, W, base, out)
+    # the pages' merge: the INT4 result is brought back to FP16, then the FP16 outlier result is
+    # added. Each part is checked against its exact value (cancellation between the parts makes
+    # the fp16 rounding of the base part large relative to the merged output).
+    Y_base = Y.cpu().numpy()
+    err = y_error(Y_base, yb)
+    assert err <= Y_TOL, f"INT4 path relative error {err:.3e}"
+    cols = torch.from_numpy(out).cuda()
+    W_out = torch.from_numpy(np.ascontiguousarray(W[:, out])).cuda()
+    fmpq_gpu.fmpq_outlier_gemm_fp16(Xd, cols, W_out, Y)
+    # merge: the FP16 outlier product and the sum are each rounded to fp16, so the merged output
+    # is within one fp16 ulp of the product plus one of the result of base output + exact product
+    Ym = Y.cpu().numpy()
+    ulp = lambda v: np.spacing(np.abs(v).astype(np.float16)).astype(np.float64)
+    err = np.abs(Ym.astype(np.float64) - (Y_base.astype(np.float64) + yo))
+    assert np.all(err <= ulp(yo) + ulp(Ym)), f"merge error {err.max():.3e}"
+    assert fmpq_gpu.fmpq_device_status(layout) == 0
+    layout.close()
+
+
+@pytest.mark.gpu
+def test_outlier_split_argument_errors(fmpq_gpu):
+    import torch
+    X = torch.zeros((4, 256), dtype=torch.float16, device="cuda")
+    Y = torch.zeros((4, 64), dtype=torch.float16, device="cuda")
+    W_out = torch.zeros((64, 16), dtype=torch.float16, device="cuda")
+    with pytest.raises(fmpq_gpu.FmpqError):       # 12 outlier columns: not a multiple of 8
+        fmpq_gpu.fmpq_outlier_gemm_fp16(X, torch.zeros(12, dtype=torch.int32, device="cuda"), W_out, Y)
+    with pytest.raises(fmpq_gpu.FmpqError):       # a selection with a repeated channel
+        fmpq_gpu.select_layout(128, 256, np.zeros(128, np.int32), np.zeros(1, np.uint8))
