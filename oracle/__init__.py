@@ -76,6 +76,16 @@ def _load():
             lib.oracle_packed_a_bytes.argtypes = [P, i32, i32]
             lib.oracle_packed_a_bytes.restype = i64
             lib.oracle_num_threads.restype = i32
+            lib.oracle_quantize_activations_asym.argtypes = [P, i64, i32, i32, P, P, P, P, P]
+            lib.oracle_quantize_activations_asym.restype = i32
+            lib.oracle_weight_sums.argtypes = [P, P, i32, i32, P]
+            lib.oracle_epilogue_asym_f64.argtypes = [P, P, P, P, P, i32, i32, i32, P]
+            lib.oracle_qoq_group_batch.argtypes = [P, i32, P, P, P]
+            lib.oracle_qoq_quantize_weights.argtypes = [P, i64, i32, i32, P, P, P, P, P, P]
+            lib.oracle_qoq_quantize_weights.restype = i32
+            lib.oracle_qoq_quantize_activations.argtypes = [P, i64, i32, i32, P, P, P, P, P]
+            lib.oracle_qoq_quantize_activations.restype = i32
+            lib.oracle_epilogue_qoq_f64.argtypes = [P, P, P, P, P, P, i32, i32, i32, P]
             _lib = lib
     return _lib
 
@@ -275,3 +285,123 @@ def quik_reference(X, W, base_cols, out_cols):
     Xo = np.asarray(X, dtype=np.float16)[:, out_cols].astype(np.float64)
     Wo = np.asarray(W, dtype=np.float16)[:, out_cols].astype(np.float64)
     return Y_base, Xo @ Wo.T
+
+
+# ---------------------------------------------------------------------- QUIK asymmetric activations
+
+def quantize_activations_asym(X, perm):
+    """QUIK explainer, "反量化背后的数学": X fp16 [M, K] -> (A_packed uint8 (one plane per block),
+    a_scales, a_zeros (fp16 bits uint16 [nb, M]), Aq int8 [M, K] codes 0..15, permuted order)."""
+    Xb = _c(np.asarray(X, dtype=np.float16).view(np.uint16), np.uint16)
+    M, K = Xb.shape
+    perm = _c(perm, np.int32)
+    nb = K // BLOCK
+    A = np.zeros(nb * M * BLOCK, dtype=np.uint8)
+    s = np.zeros((nb, M), dtype=np.uint16)
+    z = np.zeros((nb, M), dtype=np.uint16)
+    Aq = np.zeros((M, K), dtype=np.int8)
+    if _load().oracle_quantize_activations_asym(_ptr(Xb), K, M, K, _ptr(perm), _ptr(A), _ptr(s), _ptr(z), _ptr(Aq)):
+        raise ValueError("oracle_quantize_activations_asym failed")
+    return A, s, z, Aq
+
+
+def weight_sums(Wq, w_scales) -> np.ndarray:
+    """wsum float32 [nb, N] = sw[b, n] * sum of the block's weight codes."""
+    Wq = _c(Wq, np.int8)
+    N, K = Wq.shape
+    out = np.zeros((K // BLOCK, N), dtype=np.float32)
+    _load().oracle_weight_sums(_ptr(Wq), _ptr(_c(w_scales, np.uint16)), N, K, _ptr(out))
+    return out
+
+
+def epilogue_asym(P, a_scales, a_zeros, w_scales, wsum) -> np.ndarray:
+    """Y fp64 [M, N] = sum_b (sx sw P + z wsum), block order."""
+    P = _c(P, np.int32)
+    M, N, nb = P.shape
+    Y = np.zeros((M, N), dtype=np.float64)
+    _load().oracle_epilogue_asym_f64(_ptr(P), _ptr(_c(a_scales, np.uint16)), _ptr(_c(a_zeros, np.uint16)),
+                                     _ptr(_c(w_scales, np.uint16)), _ptr(_c(wsum, np.float32)), M, N, nb, _ptr(Y))
+    return Y
+
+
+def asym_reference(X, W, perm):
+    """Whole QUIK-asymmetric path on the CPU (every block 4-bit): dict of every intermediate."""
+    A, sx, z, Aq = quantize_activations_asym(X, perm)
+    Wq, sw = quantize_weights(W, perm)
+    wsum = weight_sums(Wq, sw)
+    P = partials(Aq, Wq)
+    Y = epilogue_asym(P, sx, z, sw, wsum)
+    return dict(A_packed=A, a_scales=sx, a_zeros=z, Aq=Aq, Wq=Wq, w_scales=sw, wsum=wsum, P=P, Y=Y)
+
+
+# ---------------------------------------------------------------------- QoQ progressive group quantization
+
+def qoq_group(q8):
+    """One or more groups of 128 INT8 values [G, 128] -> (s2 [G], z2 [G], q4 uint8 [G, 128])."""
+    q8 = _c(np.atleast_2d(q8), np.int8)
+    G = q8.shape[0]
+    s2 = np.zeros(G, dtype=np.int32)
+    z2 = np.zeros(G, dtype=np.int32)
+    q4 = np.zeros((G, BLOCK), dtype=np.uint8)
+    _load().oracle_qoq_group_batch(_ptr(q8), G, _ptr(s2), _ptr(z2), _ptr(q4))
+    return s2, z2, q4
+
+
+def qoq_quantize_weights(W, perm):
+    """W fp16 [N, K] -> dict(q8 int8 [N, K], q4 uint8 [N, K] (permuted order), s1 fp16 bits [N],
+    s2 uint8 [nb, N], z2 uint8 [nb, N])."""
+    Wb = _c(np.asarray(W, dtype=np.float16).view(np.uint16), np.uint16)
+    N, K = Wb.shape
+    nb = K // BLOCK
+    out = dict(q8=np.zeros((N, K), np.int8), q4=np.zeros((N, K), np.uint8), s1=np.zeros(N, np.uint16),
+               s2=np.zeros((nb, N), np.uint8), z2=np.zeros((nb, N), np.uint8))
+    if _load().oracle_qoq_quantize_weights(_ptr(Wb), K, N, K, _ptr(_c(perm, np.int32)), _ptr(out["q8"]),
+                                           _ptr(out["q4"]), _ptr(out["s1"]), _ptr(out["s2"]), _ptr(out["z2"])):
+        raise ValueError("oracle_qoq_quantize_weights failed")
+    return out
+
+
+def qoq_quantize_activations(X, perm):
+    """X fp16 [M, K] -> (A_packed uint8 (two planes per block), a_scales fp16 bits [M],
+    a_sums int32 [nb, M], Aq int8 [M, K])."""
+    Xb = _c(np.asarray(X, dtype=np.float16).view(np.uint16), np.uint16)
+    M, K = Xb.shape
+    nb = K // BLOCK
+    A = np.zeros(2 * nb * M * BLOCK, dtype=np.uint8)
+    s = np.zeros(M, dtype=np.uint16)
+    sums = np.zeros((nb, M), dtype=np.int32)
+    Aq = np.zeros((M, K), dtype=np.int8)
+    if _load().oracle_qoq_quantize_activations(_ptr(Xb), K, M, K, _ptr(_c(perm, np.int32)), _ptr(A), _ptr(s),
+                                               _ptr(sums), _ptr(Aq)):
+        raise ValueError("oracle_qoq_quantize_activations failed")
+    return A, s, sums, Aq
+
+
+def partials_u4(Aq, q4) -> np.ndarray:
+    """P int32 [M, N, nb] with unsigned 4-bit weight codes."""
+    Aq = _c(Aq, np.int8)
+    M, K = Aq.shape
+    N = q4.shape[0]
+    Wq = _c(np.asarray(q4).astype(np.int8), np.int8)    # 0..15 fits int8
+    P = np.zeros((M, N, K // BLOCK), dtype=np.int32)
+    _load().oracle_partials(_ptr(Aq), _ptr(Wq), M, N, K, _ptr(P))
+    return P
+
+
+def epilogue_qoq(P, a_scales, a_sums, s1, s2, z2) -> np.ndarray:
+    P = _c(P, np.int32)
+    M, N, nb = P.shape
+    Y = np.zeros((M, N), dtype=np.float64)
+    _load().oracle_epilogue_qoq_f64(_ptr(P), _ptr(_c(a_scales, np.uint16)), _ptr(_c(a_sums, np.int32)),
+                                    _ptr(_c(s1, np.uint16)), _ptr(_c(s2, np.uint8)), _ptr(_c(z2, np.uint8)),
+                                    M, N, nb, _ptr(Y))
+    return Y
+
+
+def qoq_reference(X, W, perm):
+    """Whole QoQ W4A8 path on the CPU: dict of every intermediate."""
+    A, sx, sums, Aq = qoq_quantize_activations(X, perm)
+    w = qoq_quantize_weights(W, perm)
+    P = partials_u4(Aq, w["q4"])
+    Y = epilogue_qoq(P, sx, sums, w["s1"], w["s2"], w["z2"])
+    return dict(A_packed=A, a_scales=sx, a_sums=sums, Aq=Aq, P=P, Y=Y, **w)

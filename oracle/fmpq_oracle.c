@@ -534,3 +534,247 @@ void oracle_rmsnorm(const uint16_t* X, int64_t ldx, int M, int K, const uint16_t
     }
     free(chunk);
 }
+
+/* ====================================================================================
+ * Quantization variants the pages describe beside FMPQ.
+ * ==================================================================================== */
+
+/* Order key of fp16 bits that follows the value order (-0 sorts below +0; no NaN inputs). */
+static unsigned f16_order_key(uint16_t h) { return (h & 0x8000u) ? (unsigned)(uint16_t)~h : (unsigned)(h | 0x8000u); }
+
+/* round-half-even of the exact rational a / b, b > 0 (integers) */
+static int rne_div(int a, int b) {
+    int q = a / b, r = a % b;                 /* C truncates toward zero */
+    if (r < 0) { q -= 1; r += b; }            /* floor division: 0 <= r < b */
+    if (2 * r > b) return q + 1;
+    if (2 * r == b) return (q % 2 == 0) ? q : q + 1;
+    return q;
+}
+
+/* ---- QUIK asymmetric activations (QUIK explainer, "反量化背后的数学": activations take a
+ * scale and a zero point, weights a scale only; the zero point's contribution z * sum(w)
+ * needs only the weights' sum, computed offline).
+ *
+ * Reading, per token and 128-channel block (every block 4-bit; QUIK's outliers stay fp16):
+ *   z = the block's smallest input (value order, -0 below +0), stored as fp16
+ *   s = fp16_rne( fp32( fp32(max) - fp32(z) ) / 15 )             IEEE fp32 operations
+ *   q = clamp( rne( fp32( fp32(x) - fp32(z) ) / fp32(s) ), 0, 15 ),  q = 0 when s == 0
+ * so x ~ s * q + z. Codes are packed like INT4 codes (one plane, byte = E4M3 of q * 2^-9)
+ * with the sign bit clear. */
+static void quantize_block_asym(const uint16_t* xs, int8_t* q, uint16_t* s_bits, uint16_t* z_bits) {
+    uint16_t lo = xs[0], hi = xs[0];
+    for (int j = 1; j < ORACLE_BLOCK; ++j) {
+        if (f16_order_key(xs[j]) < f16_order_key(lo)) lo = xs[j];
+        if (f16_order_key(xs[j]) > f16_order_key(hi)) hi = xs[j];
+    }
+    const float z = oracle_f16_to_f32(lo);
+    const float d = oracle_f16_to_f32(hi) - z;             /* IEEE fp32 subtraction */
+    const float s32 = d / 15.0f;                            /* IEEE fp32 division */
+    const uint16_t s16 = oracle_f32_to_f16(s32);
+    const float s = oracle_f16_to_f32(s16);
+    for (int j = 0; j < ORACLE_BLOCK; ++j) {
+        if (s == 0.0f) { q[j] = 0; continue; }
+        const float t = (oracle_f16_to_f32(xs[j]) - z) / s;
+        int32_t v = rne_f32_to_int(t);
+        if (v > 15) v = 15;
+        if (v < 0) v = 0;
+        q[j] = (int8_t)v;
+    }
+    *s_bits = s16;
+    *z_bits = lo;
+}
+
+/* X fp16 [M][ldx] -> packed codes (every block one plane), a_scales and a_zeros [nb][M]
+ * (fp16 bits) and, if Aq != NULL, the codes Aq [M][K] (0..15, permuted channel order). */
+int oracle_quantize_activations_asym(const uint16_t* X, int64_t ldx, int M, int K, const int32_t* perm,
+                                     uint8_t* A_packed, uint16_t* a_scales, uint16_t* a_zeros, int8_t* Aq) {
+    if (K % ORACLE_BLOCK) return -1;
+    const int nb = K / ORACLE_BLOCK;
+#pragma omp parallel for schedule(static)
+    for (int m = 0; m < M; ++m) {
+        uint16_t xs[ORACLE_BLOCK];
+        int8_t q[ORACLE_BLOCK];
+        for (int b = 0; b < nb; ++b) {
+            for (int j = 0; j < ORACLE_BLOCK; ++j) xs[j] = X[(int64_t)m * ldx + perm[b * ORACLE_BLOCK + j]];
+            quantize_block_asym(xs, q, &a_scales[(int64_t)b * M + m], &a_zeros[(int64_t)b * M + m]);
+            uint8_t* row = A_packed + (int64_t)b * M * ORACLE_BLOCK + (int64_t)m * ORACLE_BLOCK;
+            for (int c = 0; c < ORACLE_BLOCK; ++c) row[plane_pos(m, c)] = (uint8_t)e4m3_of_multiple(q[c]);
+            if (Aq)
+                for (int j = 0; j < ORACLE_BLOCK; ++j) Aq[(int64_t)m * K + b * ORACLE_BLOCK + j] = q[j];
+        }
+    }
+    return 0;
+}
+
+/* Offline weight sums for the zero-point term: wsum[b][n] = sw[b][n] * sum_{j in b} Wq[n][j]
+ * (the block's dequantized weights summed; exact in fp32: 11-bit scale times |sum| <= 896). */
+void oracle_weight_sums(const int8_t* Wq, const uint16_t* w_scales, int N, int K, float* wsum) {
+    const int nb = K / ORACLE_BLOCK;
+    for (int n = 0; n < N; ++n)
+        for (int b = 0; b < nb; ++b) {
+            int64_t t = 0;
+            for (int j = b * ORACLE_BLOCK; j < (b + 1) * ORACLE_BLOCK; ++j) t += Wq[(int64_t)n * K + j];
+            wsum[(int64_t)b * N + n] = (float)((double)oracle_f16_to_f32(w_scales[(int64_t)b * N + n]) * (double)t);
+        }
+}
+
+/* Y[m][n] = sum_b ( sx[b][m] * sw[b][n] * P[m][n][b] + z[b][m] * wsum[b][n] ), fp64 in block
+ * order; P are the integer sums of the unsigned activation codes times the weight codes. */
+void oracle_epilogue_asym_f64(const int32_t* P, const uint16_t* a_scales, const uint16_t* a_zeros,
+                              const uint16_t* w_scales, const float* wsum, int M, int N, int nb, double* Y) {
+#pragma omp parallel for schedule(static)
+    for (int m = 0; m < M; ++m)
+        for (int n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int b = 0; b < nb; ++b) {
+                const double sx = oracle_f16_to_f32(a_scales[(int64_t)b * M + m]);
+                const double z = oracle_f16_to_f32(a_zeros[(int64_t)b * M + m]);
+                const double sw = oracle_f16_to_f32(w_scales[(int64_t)b * N + n]);
+                acc += sx * sw * (double)P[((int64_t)m * N + n) * nb + b] + z * (double)wsum[(int64_t)b * N + n];
+            }
+            Y[(int64_t)m * N + n] = acc;
+        }
+}
+
+/* ---- QoQ progressive group quantization (QServe explainer, "渐进式分组量化"): the weights are
+ * first quantized per output channel to symmetric INT8, then each group of those INT8 values
+ * to asymmetric UINT4. The INT8 range is narrowed to [-119, 119] (the protective range) so
+ * that the dequantized (q4 - z2) * s2 never leaves the INT8 range.
+ *
+ * Reading (the page gives no formulas):
+ *   s1[n] = fp16_rne( fp32(absmax of row n) / 119 )               IEEE fp32 division
+ *   q8    = clamp( rne_f32( fp32(w) / fp32(s1) ), -119, 119 )      q8 = 0 when s1 == 0
+ *   per group g of 128 channels (the permuted order's blocks), the range [mn, mx] of its q8
+ *   extended to include 0 (mn = min(min q8, 0), mx = max(max q8, 0)), so that the zero point
+ *   is a code:
+ *   s2 = max(1, ceil((mx - mn) / 15))  the smallest integer scale spanning the range in 15 steps
+ *   z2 = clamp( rne(-mn / s2), 0, 15 ) integer zero point
+ *   q4 = clamp( rne(q8 / s2) + z2, 0, 15 )                        (rne of exact rationals)
+ * Dequantized weight: s1 * s2 * (q4 - z2). Every quotient here is an exact rational, rounded
+ * half to even. With |q8| <= 119 the scale is at most ceil(238 / 15) = 16, and a code's
+ * dequantized value is within s2 / 2 <= 8 of q8 or clipped toward 0, so it stays in
+ * [-127, 127]. */
+void oracle_qoq_group(const int8_t* q8, int* s2_out, int* z2_out, uint8_t* q4) {
+    int mn = 0, mx = 0;                       /* the range always includes 0 */
+    for (int j = 0; j < ORACLE_BLOCK; ++j) {
+        if (q8[j] < mn) mn = q8[j];
+        if (q8[j] > mx) mx = q8[j];
+    }
+    int s2 = (mx - mn + 14) / 15;             /* ceil, mx - mn >= 0 */
+    if (s2 < 1) s2 = 1;
+    int z2 = rne_div(-mn, s2);
+    if (z2 < 0) z2 = 0;
+    if (z2 > 15) z2 = 15;
+    for (int j = 0; j < ORACLE_BLOCK; ++j) {
+        int v = rne_div(q8[j], s2) + z2;
+        if (v < 0) v = 0;
+        if (v > 15) v = 15;
+        q4[j] = (uint8_t)v;
+    }
+    *s2_out = s2;
+    *z2_out = z2;
+}
+
+/* Batch form for tests: G groups of 128 INT8 values. */
+void oracle_qoq_group_batch(const int8_t* q8, int G, int32_t* s2, int32_t* z2, uint8_t* q4) {
+    for (int g = 0; g < G; ++g) {
+        int a, c;
+        oracle_qoq_group(q8 + (int64_t)g * ORACLE_BLOCK, &a, &c, q4 + (int64_t)g * ORACLE_BLOCK);
+        s2[g] = a;
+        z2[g] = c;
+    }
+}
+
+/* W fp16 [N][ldw] -> q8 [N][K] and q4 [N][K] (permuted channel order), s1 [N] (fp16 bits),
+ * s2 and z2 [nb][N]. */
+int oracle_qoq_quantize_weights(const uint16_t* W, int64_t ldw, int N, int K, const int32_t* perm, int8_t* q8,
+                                uint8_t* q4, uint16_t* s1, uint8_t* s2, uint8_t* z2) {
+    if (K % ORACLE_BLOCK) return -1;
+    const int nb = K / ORACLE_BLOCK;
+#pragma omp parallel for schedule(static)
+    for (int n = 0; n < N; ++n) {
+        float absmax = 0.0f;
+        for (int c = 0; c < K; ++c) {
+            const float v = fabsf(oracle_f16_to_f32(W[(int64_t)n * ldw + c]));
+            if (v > absmax) absmax = v;
+        }
+        const uint16_t sb = oracle_f32_to_f16(absmax / 119.0f);
+        const float s = oracle_f16_to_f32(sb);
+        s1[n] = sb;
+        int8_t* r8 = q8 + (int64_t)n * K;
+        for (int j = 0; j < K; ++j) {
+            if (s == 0.0f) { r8[j] = 0; continue; }
+            int32_t v = rne_f32_to_int(oracle_f16_to_f32(W[(int64_t)n * ldw + perm[j]]) / s);
+            if (v > 119) v = 119;
+            if (v < -119) v = -119;
+            r8[j] = (int8_t)v;
+        }
+        for (int b = 0; b < nb; ++b) {
+            int a, c;
+            oracle_qoq_group(r8 + b * ORACLE_BLOCK, &a, &c, q4 + (int64_t)n * K + b * ORACLE_BLOCK);
+            s2[(int64_t)b * N + n] = (uint8_t)a;
+            z2[(int64_t)b * N + n] = (uint8_t)c;
+        }
+    }
+    return 0;
+}
+
+/* QoQ activations (QServe explainer, "运行时设计": every GEMM takes W4A8 inputs): per-token
+ * symmetric INT8, s = fp16_rne(fp32(absmax of the row) / 127), q = clamp(rne_f32(x / s), ±127),
+ * every block packed as an INT8 block (two planes); a_sums[b][m] = sum of the block's codes
+ * (the term the group zero point multiplies). */
+int oracle_qoq_quantize_activations(const uint16_t* X, int64_t ldx, int M, int K, const int32_t* perm,
+                                    uint8_t* A_packed, uint16_t* a_scales, int32_t* a_sums, int8_t* Aq) {
+    if (K % ORACLE_BLOCK) return -1;
+    const int nb = K / ORACLE_BLOCK;
+#pragma omp parallel for schedule(static)
+    for (int m = 0; m < M; ++m) {
+        float absmax = 0.0f;
+        for (int c = 0; c < K; ++c) {
+            const float v = fabsf(oracle_f16_to_f32(X[(int64_t)m * ldx + c]));
+            if (v > absmax) absmax = v;
+        }
+        const uint16_t sb = oracle_f32_to_f16(absmax / 127.0f);
+        const float s = oracle_f16_to_f32(sb);
+        a_scales[m] = sb;
+        uint16_t xs[ORACLE_BLOCK];
+        int8_t q[ORACLE_BLOCK];
+        for (int b = 0; b < nb; ++b) {
+            int32_t sum = 0;
+            for (int j = 0; j < ORACLE_BLOCK; ++j) {
+                xs[j] = X[(int64_t)m * ldx + perm[b * ORACLE_BLOCK + j]];
+                int32_t v = 0;
+                if (s != 0.0f) {
+                    v = rne_f32_to_int(oracle_f16_to_f32(xs[j]) / s);
+                    if (v > 127) v = 127;
+                    if (v < -127) v = -127;
+                }
+                q[j] = (int8_t)v;
+                sum += v;
+            }
+            a_sums[(int64_t)b * M + m] = sum;
+            pack_block_row(q, xs, 1, A_packed, 2 * (int64_t)b, M, m);
+            if (Aq)
+                for (int j = 0; j < ORACLE_BLOCK; ++j) Aq[(int64_t)m * K + b * ORACLE_BLOCK + j] = q[j];
+        }
+    }
+    return 0;
+}
+
+/* Y[m][n] = sum_b sx[m] * s1[n] * s2[b][n] * ( P[m][n][b] - z2[b][n] * a_sums[b][m] ), fp64 in
+ * block order, P = exact sums of the INT8 activation codes times the UINT4 codes q4 (the zero
+ * point subtracted after the multiplication, as the QServe explainer's "W4A8逐组快速反量化" does). */
+void oracle_epilogue_qoq_f64(const int32_t* P, const uint16_t* a_scales, const int32_t* a_sums, const uint16_t* s1,
+                             const uint8_t* s2, const uint8_t* z2, int M, int N, int nb, double* Y) {
+#pragma omp parallel for schedule(static)
+    for (int m = 0; m < M; ++m)
+        for (int n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int b = 0; b < nb; ++b) {
+                const int64_t g = (int64_t)b * N + n;
+                const int64_t pz = (int64_t)P[((int64_t)m * N + n) * nb + b] - (int64_t)z2[g] * a_sums[(int64_t)b * M + m];
+                acc += (double)s2[g] * (double)pz;
+            }
+            Y[(int64_t)m * N + n] = (double)oracle_f16_to_f32(a_scales[m]) * (double)oracle_f16_to_f32(s1[n]) * acc;
+        }
+}

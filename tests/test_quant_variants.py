@@ -1,0 +1,205 @@
+"""Quantization variants beside FMPQ's symmetric blocks.
+
+- QUIK asymmetric activations (QUIK explainer, "反量化背后的数学"): activations take a scale and
+  a zero point, weights a scale only, and the zero point's term needs only the weights' sums,
+  precomputed offline.
+- QoQ progressive group quantization (QServe explainer, "渐进式分组量化"): per-channel INT8
+  weights in the protective range [-119, 119], then per-group asymmetric UINT4; W4A8 with
+  per-token INT8 activations ("运行时设计"), the group zero point subtracted after the
+  multiplication ("W4A8逐组快速反量化").
+
+CPU: the oracle pinned to worked examples, closed forms, invariants and an exhaustive check of
+the protective range. GPU: the library's kernels bit-exact against the oracle (codes, scales,
+zero points, sums, partial sums) and Y within the output tolerance.
+"""
+import numpy as np
+import pytest
+
+BLOCK = 128
+
+
+def f16(v):
+    return np.asarray(v, dtype=np.float16)
+
+
+# ---------------------------------------------------------------------- QUIK asymmetric: oracle pins
+
+def test_asym_worked_example(oracle_mod):
+    """min -1, max 14: s = fp16(15 / 15) = 1, z = -1; (x - z) / s = x + 1 rounded half to even."""
+    x = np.zeros((1, BLOCK), dtype=np.float16)
+    vals = {0: -1.0, 1: 14.0, 2: 0.5, 3: 1.5, 4: 2.5, 5: -0.5, 6: 3.25}
+    for j, v in vals.items():
+        x[0, j] = v
+    A, s, z, Aq = oracle_mod.quantize_activations_asym(x, np.arange(BLOCK, dtype=np.int32))
+    assert s[0, 0] == f16(1.0).view(np.uint16)
+    assert z[0, 0] == f16(-1.0).view(np.uint16)
+    want = {0: 0, 1: 15, 2: 2, 3: 2, 4: 4, 5: 0, 6: 4}     # 1.5 -> 2, 2.5 -> 2, 3.5 -> 4, 0.5 -> 0, 4.25 -> 4
+    for j, q in want.items():
+        assert Aq[0, j] == q, (j, Aq[0, j], q)
+    assert np.all(Aq[0, 7:] == 1)                           # x = 0 -> 1
+    # packed: one plane, byte = E4M3 of q * 2^-9 with the sign bit clear; row 0 is unrotated
+    for j in range(BLOCK):
+        assert oracle_mod.e4m3_value(int(A[j])) == Aq[0, j] * 2.0 ** -9
+
+
+def test_asym_constant_and_signed_zero_blocks(oracle_mod):
+    x = np.full((2, 2 * BLOCK), 3.0, dtype=np.float16)
+    x[1, :BLOCK] = 0.0
+    x[1, 5] = -0.0                                          # -0 orders below +0: it is the zero point
+    A, s, z, Aq = oracle_mod.quantize_activations_asym(x, np.arange(2 * BLOCK, dtype=np.int32))
+    assert np.all(s == 0) and np.all(Aq == 0)
+    assert z[0, 0] == f16(3.0).view(np.uint16) and z[1, 0] == f16(3.0).view(np.uint16)
+    assert z[0, 1] == np.uint16(0x8000)
+
+
+@pytest.mark.parametrize("dist", ["normal", "positive", "outliers"])
+def test_asym_invariants(oracle_mod, dist):
+    """Per block: codes in [0, 15]; the minimum maps to 0 and the maximum to 15 (normal scale);
+    |x - (z + q s)| <= s / 2 up to the fp32 roundings of the difference and the quotient."""
+    rng = np.random.default_rng(5)
+    M, K = 16, 1024
+    if dist == "normal":
+        x = rng.standard_normal((M, K))
+    elif dist == "positive":
+        x = rng.uniform(2.0, 3.0, (M, K))                   # far from zero: the zero point matters
+    else:
+        x = rng.standard_normal((M, K))
+        x[:, rng.integers(0, K, 20)] *= 60.0
+    X = x.astype(np.float16)
+    perm = rng.permutation(K).astype(np.int32)
+    _, s, z, Aq = oracle_mod.quantize_activations_asym(X, perm)
+    Xp = X[:, perm].astype(np.float64)
+    sv = oracle_mod.f16_bits_to_f32(s).reshape(s.shape).astype(np.float64)
+    zv = oracle_mod.f16_bits_to_f32(z).reshape(z.shape).astype(np.float64)
+    for b in range(K // BLOCK):
+        blk = Xp[:, b * BLOCK:(b + 1) * BLOCK]
+        q = Aq[:, b * BLOCK:(b + 1) * BLOCK].astype(np.float64)
+        assert q.min() >= 0 and q.max() <= 15
+        assert np.array_equal(zv[b], blk.min(axis=1))
+        rows = np.arange(M)
+        assert np.all(q[rows, blk.argmin(axis=1)] == 0)
+        assert np.all(q[rows, blk.argmax(axis=1)] == 15)
+        err = np.abs(blk - (zv[b][:, None] + q * sv[b][:, None]))
+        assert np.all(err <= 0.5 * sv[b][:, None] * (1 + 1e-5) + 1e-6 * np.abs(blk - zv[b][:, None]))
+
+
+def test_asym_scale_invariance(oracle_mod):
+    """X * 2^k: scale and zero point scale by 2^k exactly, the codes are unchanged."""
+    rng = np.random.default_rng(8)
+    X = (rng.standard_normal((8, 512)) * 0.5).astype(np.float16)
+    perm = rng.permutation(512).astype(np.int32)
+    _, s1, z1, q1 = oracle_mod.quantize_activations_asym(X, perm)
+    X8 = (X.astype(np.float32) * 8).astype(np.float16)
+    _, s8, z8, q8 = oracle_mod.quantize_activations_asym(X8, perm)
+    assert np.array_equal(q1, q8)
+    f = lambda h: oracle_mod.f16_bits_to_f32(h).reshape(h.shape)
+    assert np.array_equal(f(s1) * 8, f(s8)) and np.array_equal(f(z1) * 8, f(z8))
+
+
+def test_asym_epilogue_closed_form(oracle_mod):
+    """The epilogue with the offline weight sums equals dequantize-then-multiply:
+    sum_k (s_x q_x + z) (s_w q_w), evaluated in fp64."""
+    rng = np.random.default_rng(9)
+    M, N, K = 6, 10, 512
+    X = (rng.standard_normal((M, K)) + 1.5).astype(np.float16)
+    W = (rng.standard_normal((N, K)) * 0.03).astype(np.float16)
+    perm = rng.permutation(K).astype(np.int32)
+    r = oracle_mod.asym_reference(X, W, perm)
+    f = lambda h: oracle_mod.f16_bits_to_f32(h).reshape(h.shape).astype(np.float64)
+    sx, z, sw = f(r["a_scales"]), f(r["a_zeros"]), f(r["w_scales"])
+    blk = np.arange(K) // BLOCK
+    Xd = r["Aq"].astype(np.float64) * sx[blk, :].T + z[blk, :].T
+    Wd = r["Wq"].astype(np.float64) * sw[blk, :].T
+    Y = Xd @ Wd.T
+    assert np.allclose(r["Y"], Y, rtol=1e-12, atol=1e-12 * np.abs(Y).max())
+    # the weight sums are the block sums of the dequantized weights
+    assert np.array_equal(r["wsum"].astype(np.float64), Wd.reshape(N, K // BLOCK, BLOCK).sum(axis=2).T)
+
+
+# ---------------------------------------------------------------------- QoQ: oracle pins
+
+def test_qoq_group_worked_examples(oracle_mod):
+    """Range [-119, 119]: s2 = ceil(238 / 15) = 16, z2 = rne(119 / 16 = 7.4375) = 7."""
+    g = np.zeros(BLOCK, dtype=np.int8)
+    g[:7] = [-119, 119, 8, 24, -8, -24, 40]
+    s2, z2, q4 = oracle_mod.qoq_group(g)
+    assert s2[0] == 16 and z2[0] == 7
+    # q8 / 16 rounded half to even, plus 7: 119 -> 7 + 7, 8 -> 0.5 -> 0, 24 -> 1.5 -> 2,
+    # -8 -> -0.5 -> 0, -24 -> -1.5 -> -2, 40 -> 2.5 -> 2
+    assert q4[0, :7].tolist() == [0, 14, 7, 9, 7, 5, 9]
+    assert np.all(q4[0, 7:] == 7)
+    # a positive group: the range is extended to 0, so z2 = 0 and 0 stays exact
+    g = np.full(BLOCK, 3, dtype=np.int8)
+    g[0] = 40
+    s2, z2, q4 = oracle_mod.qoq_group(g)
+    assert s2[0] == 3 and z2[0] == 0 and q4[0, 0] == 13 and q4[0, 1] == 1
+    # all zero: s2 = 1, z2 = 0
+    s2, z2, q4 = oracle_mod.qoq_group(np.zeros(BLOCK, dtype=np.int8))
+    assert s2[0] == 1 and z2[0] == 0 and np.all(q4 == 0)
+
+
+def test_qoq_protective_range_exhaustive(oracle_mod):
+    """For every group range [mn, mx] inside [-119, 119] and every INT8 value in it, the code is
+    in [0, 15] and the dequantized (q4 - z2) * s2 is in [-127, 127] (the protective range's
+    purpose), within s2 of the INT8 value."""
+    lo, hi = np.meshgrid(np.arange(-119, 120), np.arange(-119, 120), indexing="ij")
+    sel = lo <= hi
+    lo, hi = lo[sel], hi[sel]
+    G = lo.size
+    # fill each group with mn, mx and values spread over [mn, mx]; two offsets of the fill
+    # cover every value of ranges wider than the group
+    for phase in range(2):
+        t = (np.arange(BLOCK - 2)[None, :] * 2 + phase) / (2 * (BLOCK - 2) - 1)
+        fill = np.rint(lo[:, None] + t * (hi - lo)[:, None]).astype(np.int64)
+        q8 = np.concatenate([lo[:, None], hi[:, None], fill], axis=1).astype(np.int8)
+        s2, z2, q4 = oracle_mod.qoq_group(q8)
+        deq = (q4.astype(np.int64) - z2[:, None]) * s2[:, None]
+        assert q4.max() <= 15
+        assert np.abs(deq).max() <= 127
+        assert np.all(np.abs(deq - q8) <= s2[:, None])
+        assert s2.max() == 16
+    # every value of [-119, 119] occurs in some group of the sweep
+    assert G == 239 * 240 // 2
+
+
+def test_qoq_weight_rule_worked_example(oracle_mod):
+    """Row absmax 119 -> s1 = 1, q8 = rne(w) (ties to even), then the group rule."""
+    W = np.zeros((1, BLOCK), dtype=np.float16)
+    W[0, :5] = [119.0, -2.5, 3.5, 0.5, -60.0]
+    r = oracle_mod.qoq_quantize_weights(W, np.arange(BLOCK, dtype=np.int32))
+    assert r["s1"][0] == f16(1.0).view(np.uint16)
+    assert r["q8"][0, :5].tolist() == [119, -2, 4, 0, -60]
+    s2, z2, q4 = oracle_mod.qoq_group(r["q8"][0])
+    assert r["s2"][0, 0] == s2[0] and r["z2"][0, 0] == z2[0] and np.array_equal(r["q4"][0], q4[0])
+
+
+def test_qoq_activation_worked_example(oracle_mod):
+    """Per-token scale from the row's absmax (127 -> s = 1), codes rne(x), block sums."""
+    X = np.zeros((1, 2 * BLOCK), dtype=np.float16)
+    X[0, 0], X[0, 1], X[0, 130], X[0, 131] = 127.0, 2.5, -3.5, 1.5
+    A, s, sums, Aq = oracle_mod.qoq_quantize_activations(X, np.arange(2 * BLOCK, dtype=np.int32))
+    assert s[0] == f16(1.0).view(np.uint16)
+    assert Aq[0, 0] == 127 and Aq[0, 1] == 2 and Aq[0, 130] == -4 and Aq[0, 131] == 2
+    assert sums[:, 0].tolist() == [129, -2]
+    # every block is packed as an INT8 block (two planes)
+    assert np.array_equal(oracle_mod.unpack_activations(A, np.ones(2, np.uint8), 1, 2 * BLOCK), Aq)
+
+
+def test_qoq_epilogue_closed_form(oracle_mod):
+    """Zero point subtracted after the multiplication == dequantize-then-multiply in fp64:
+    sum_k (s_x q_x) (s1 s2 (q4 - z2))."""
+    rng = np.random.default_rng(12)
+    M, N, K = 5, 9, 512
+    X = rng.standard_normal((M, K)).astype(np.float16)
+    W = (rng.standard_normal((N, K)) * 0.03 + 0.01).astype(np.float16)
+    perm = rng.permutation(K).astype(np.int32)
+    r = oracle_mod.qoq_reference(X, W, perm)
+    f = lambda h: oracle_mod.f16_bits_to_f32(h).reshape(h.shape).astype(np.float64)
+    blk = np.arange(K) // BLOCK
+    Xd = r["Aq"].astype(np.float64) * f(r["a_scales"])[:, None]
+    Wd = ((r["q4"].astype(np.float64) - r["z2"][blk, :].T) * r["s2"][blk, :].T) * f(r["s1"])[:, None]
+    Y = Xd @ Wd.T
+    assert np.allclose(r["Y"], Y, rtol=1e-12, atol=1e-12 * np.abs(Y).max())
+    # the INT8 intermediate is reproduced by the group codes within s2 / 2 except where clipped
+    deq8 = (r["q4"].astype(np.int64) - r["z2"][blk, :].T) * r["s2"][blk, :].T
+    assert np.all(np.abs(deq8 - r["q8"]) <= r["s2"][blk, :].T)
