@@ -266,6 +266,7 @@ def run_sweep(args):
     configs += [(f"load_balance_{int(f * 100)}pct", (lambda f=f: wl.load_balance(f))) for f in (0.0, 0.10, 0.25, 0.50)]
     if args.sweep_only:
         names = [c[0] for c in configs] + ["rmsnorm_quantize_llama70b_down", "outlier_split_llama70b_down",
+                                           "quik_asym_llama70b_down", "qoq_w4a8_llama70b_down",
                                            "calibrate_llama70b_down"]
         if args.sweep_only not in names:
             raise SystemExit(f"unknown workload {args.sweep_only}; one of {names}")
@@ -380,6 +381,61 @@ def run_sweep(args):
                           "fp16_outlier_path_tflops": 2.0 * w.M * w.N * n_out / (ms_out * 1e-3) / 1e12,
                           "l2": "flushed before every timed launch", "clocks": clocks}), flush=True)
         del layout, Wp, sw, W_out, X, A, sx, Y, X_out, ws
+        torch.cuda.empty_cache()
+    if not args.sweep_only or args.sweep_only == "quik_asym_llama70b_down":
+        # QUIK asymmetric activations (every block 4-bit, zero point per token and block)
+        w = wl.llama70b_down()
+        layout = fmpq.Layout(w.K, w.perm, np.zeros(w.K // 128, dtype=np.uint8))
+        X = torch.from_numpy(w.X).cuda()
+        Wd = torch.from_numpy(w.W).cuda()
+        Wp, sw = fmpq.w4_pack_weights(layout, Wd)
+        del Wd
+        wsum = fmpq.w4_weight_sums(layout, Wp, sw, w.N)
+        A = torch.empty(layout.packed_a_bytes(w.M), dtype=torch.uint8, device="cuda")
+        sx = torch.empty((layout.nb, w.M), dtype=torch.float16, device="cuda")
+        z = torch.empty((layout.nb, w.M), dtype=torch.float16, device="cuda")
+        Y = torch.empty((w.M, w.N), dtype=torch.float16, device="cuda")
+        ws = layout.workspace(w.M, w.N, variant=True)
+        sampler.start()
+        q_ms = timed(lambda: fmpq.fmpq_quantize_asym(layout, X, A, sx, z))
+        g_ms = timed(lambda: fmpq.w4ax_gemm_asym(layout, A, sx, z, Wp, sw, wsum, w.M, w.N, Y, workspace=ws))
+        clocks = sampler.stop()
+        flops = 2.0 * w.M * w.N * w.K
+        qbytes = 2 * w.M * w.K + layout.packed_a_bytes(w.M) + 4 * layout.nb * w.M
+        print(json.dumps({"sweep": "quik_asym_llama70b_down", "M": w.M, "K": w.K, "N": w.N, "n8_blocks": 0,
+                          "gemm_ms": g_ms, "gemm_tflops_effective": flops / (g_ms * 1e-3) / 1e12,
+                          "gemm_frac_fp8_peak": flops / (g_ms * 1e-3) / 1e12 / fp8_peak,
+                          "quant_ms": q_ms, "quant_gbs": qbytes / (q_ms * 1e-3) / 1e9,
+                          "quant_frac_hbm": qbytes / (q_ms * 1e-3) / 1e9 / hbm,
+                          "l2": "flushed before every timed launch", "clocks": clocks}), flush=True)
+        del layout, Wp, sw, wsum, X, A, sx, z, Y, ws
+        torch.cuda.empty_cache()
+    if not args.sweep_only or args.sweep_only == "qoq_w4a8_llama70b_down":
+        # QoQ: per-token INT8 activations (two code planes per block), progressive UINT4 weights
+        w = wl.llama70b_down()
+        layout = fmpq.Layout(w.K, w.perm, np.ones(w.K // 128, dtype=np.uint8))
+        X = torch.from_numpy(w.X).cuda()
+        Wd = torch.from_numpy(w.W).cuda()
+        Wp, s1, s2, z2 = fmpq.qoq_pack_weights(layout, Wd)
+        del Wd
+        A = torch.empty(layout.packed_a_bytes(w.M), dtype=torch.uint8, device="cuda")
+        sx = torch.empty(w.M, dtype=torch.float16, device="cuda")
+        sums = torch.empty((layout.nb, w.M), dtype=torch.int32, device="cuda")
+        Y = torch.empty((w.M, w.N), dtype=torch.float16, device="cuda")
+        ws = layout.workspace(w.M, w.N, variant=True)
+        sampler.start()
+        q_ms = timed(lambda: fmpq.qoq_quantize(layout, X, A, sx, sums))
+        g_ms = timed(lambda: fmpq.qoq_gemm(layout, A, sx, sums, Wp, s1, s2, z2, w.M, w.N, Y, workspace=ws))
+        clocks = sampler.stop()
+        flops = 2.0 * w.M * w.N * w.K
+        qbytes = 2 * w.M * w.K + layout.packed_a_bytes(w.M) + 2 * w.M + 4 * layout.nb * w.M
+        print(json.dumps({"sweep": "qoq_w4a8_llama70b_down", "M": w.M, "K": w.K, "N": w.N,
+                          "gemm_ms": g_ms, "gemm_tflops_effective": flops / (g_ms * 1e-3) / 1e12,
+                          "gemm_frac_fp8_peak_of_mma_work": 2 * flops / (g_ms * 1e-3) / 1e12 / fp8_peak,
+                          "quant_ms": q_ms, "quant_gbs": qbytes / (q_ms * 1e-3) / 1e9,
+                          "quant_frac_hbm": qbytes / (q_ms * 1e-3) / 1e9 / hbm,
+                          "l2": "flushed before every timed launch", "clocks": clocks}), flush=True)
+        del layout, Wp, s1, s2, z2, X, A, sx, sums, Y, ws
         torch.cuda.empty_cache()
     if not args.sweep_only or args.sweep_only == "calibrate_llama70b_down":
         # offline calibration: per-channel absmax over the 4096 x 28672 activations (HBM-bound)

@@ -227,6 +227,165 @@ fmpq_status w4ax_gemm_partials(const fmpq_layout* L, const void* A_packed, const
     return launched(fmpq::launch_gemm(*L, a, static_cast<cudaStream_t>(stream)));
 }
 
+// ---- quantization variants: QUIK asymmetric activations, QoQ progressive group quantization
+
+size_t fmpq_variant_gemm_workspace_bytes(const fmpq_layout* L, int64_t M, int64_t N) {
+    if (L == nullptr || M < 1 || N < 1) return 0;
+    return fmpq::gemm_workspace_bytes(*L, M, N, true);
+}
+
+fmpq_status fmpq_quantize_asym(const fmpq_layout* L, const void* X, int64_t ldx, int64_t M, void* A_packed,
+                               void* a_scales, void* a_zeros, void* stream) {
+    if (L == nullptr || X == nullptr || A_packed == nullptr || a_scales == nullptr || a_zeros == nullptr)
+        return FMPQ_ERR_INVALID_ARG;
+    if (L->n8 != 0) return FMPQ_ERR_INVALID_ARG;   // every block 4-bit
+    if (M < 1 || M > INT32_MAX || ldx < L->K_in) return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (ldx % 8 != 0 || !aligned16(X) || !aligned16(A_packed) || !aligned16(a_scales) || !aligned16(a_zeros))
+        return FMPQ_ERR_MISALIGNED;
+    if (fmpq_status st = check_device(L)) return st;
+    return launched(fmpq::launch_quantize(*L, X, ldx, M, A_packed, a_scales, static_cast<cudaStream_t>(stream),
+                                          nullptr, 0.0f, fmpq::kQuantAsym, a_zeros));
+}
+
+fmpq_status w4_weight_sums(const fmpq_layout* L, const void* W_packed, const void* w_scales, int64_t N, float* w_sums,
+                           void* stream) {
+    if (L == nullptr || W_packed == nullptr || w_scales == nullptr || w_sums == nullptr) return FMPQ_ERR_INVALID_ARG;
+    if (N < 16 || N % 16 != 0 || N > INT32_MAX) return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(W_packed) || !aligned16(w_scales) || !aligned16(w_sums)) return FMPQ_ERR_MISALIGNED;
+    if (fmpq_status st = check_device(L)) return st;
+    return launched(fmpq::launch_weight_sums(*L, W_packed, w_scales, N, w_sums, static_cast<cudaStream_t>(stream)));
+}
+
+fmpq_status w4ax_gemm_asym(const fmpq_layout* L, const void* A_packed, const void* a_scales, const void* a_zeros,
+                           const void* W_packed, const void* w_scales, const float* w_sums, int64_t M, int64_t N,
+                           void* Y, int64_t ldy, void* workspace, size_t workspace_bytes, void* stream) {
+    if (L == nullptr || A_packed == nullptr || a_scales == nullptr || a_zeros == nullptr || W_packed == nullptr ||
+        w_scales == nullptr || w_sums == nullptr || Y == nullptr)
+        return FMPQ_ERR_INVALID_ARG;
+    if (L->n8 != 0) return FMPQ_ERR_INVALID_ARG;
+    if (M < 1 || M > INT32_MAX || N < 16 || N % 16 != 0 || N > INT32_MAX || ldy < N)
+        return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (ldy % 8 != 0 || !aligned16(A_packed) || !aligned16(a_scales) || !aligned16(a_zeros) || !aligned16(W_packed) ||
+        !aligned16(w_scales) || !aligned16(w_sums) || !aligned16(Y))
+        return FMPQ_ERR_MISALIGNED;
+    const size_t need = fmpq::gemm_workspace_bytes(*L, M, N, true);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return FMPQ_ERR_WORKSPACE;
+    if (need > 0 && !aligned16(workspace)) return FMPQ_ERR_MISALIGNED;
+    if (fmpq_status st = check_device(L)) return st;
+    fmpq::GemmArgs a{};
+    a.A = A_packed;
+    a.a_scales = a_scales;
+    a.W = W_packed;
+    a.w_scales = w_scales;
+    a.M = M;
+    a.N = N;
+    a.Y = Y;
+    a.ldy = ldy;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    a.zero_kind = fmpq::kZeroQuik;
+    a.a_zeros = a_zeros;
+    a.w_sums = w_sums;
+    return launched(fmpq::launch_gemm(*L, a, static_cast<cudaStream_t>(stream)));
+}
+
+fmpq_status qoq_pack_weights(const fmpq_layout* L, const void* W, int64_t ldw, int64_t N, void* W_packed,
+                             void* ch_scales, uint8_t* grp_scales, uint8_t* grp_zeros, void* stream) {
+    if (L == nullptr || W == nullptr || W_packed == nullptr || ch_scales == nullptr || grp_scales == nullptr ||
+        grp_zeros == nullptr)
+        return FMPQ_ERR_INVALID_ARG;
+    if (N < 16 || N % 16 != 0 || N > INT32_MAX || ldw < L->K || L->K_in != L->K) return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (ldw % 8 != 0 || !aligned16(W) || !aligned16(W_packed) || !aligned16(ch_scales) || !aligned16(grp_scales) ||
+        !aligned16(grp_zeros))
+        return FMPQ_ERR_MISALIGNED;
+    if (fmpq_status st = check_device(L)) return st;
+    return launched(fmpq::launch_qoq_pack_weights(*L, W, ldw, N, W_packed, ch_scales, grp_scales, grp_zeros,
+                                                  static_cast<cudaStream_t>(stream)));
+}
+
+fmpq_status qoq_unpack_weights(const fmpq_layout* L, const void* W_packed, int64_t N, uint8_t* q4, void* stream) {
+    if (L == nullptr || W_packed == nullptr || q4 == nullptr) return FMPQ_ERR_INVALID_ARG;
+    if (N < 16 || N % 16 != 0 || N > INT32_MAX) return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(W_packed) || !aligned16(q4)) return FMPQ_ERR_MISALIGNED;
+    if (fmpq_status st = check_device(L)) return st;
+    return launched(fmpq::launch_unpack_weights(*L, W_packed, N, reinterpret_cast<int8_t*>(q4),
+                                                static_cast<cudaStream_t>(stream), true));
+}
+
+fmpq_status qoq_quantize(const fmpq_layout* L, const void* X, int64_t ldx, int64_t M, void* A_packed, void* a_scales,
+                         int32_t* a_sums, void* stream) {
+    if (L == nullptr || X == nullptr || A_packed == nullptr || a_scales == nullptr || a_sums == nullptr)
+        return FMPQ_ERR_INVALID_ARG;
+    if (L->n8 != L->nb) return FMPQ_ERR_INVALID_ARG;   // every block INT8
+    if (M < 1 || M > INT32_MAX || ldx < L->K || L->K_in != L->K) return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (ldx % 8 != 0 || !aligned16(X) || !aligned16(A_packed) || !aligned16(a_scales) || !aligned16(a_sums))
+        return FMPQ_ERR_MISALIGNED;
+    if (fmpq_status st = check_device(L)) return st;
+    return launched(fmpq::launch_quantize(*L, X, ldx, M, A_packed, a_scales, static_cast<cudaStream_t>(stream),
+                                          nullptr, 0.0f, fmpq::kQuantTok, a_sums));
+}
+
+fmpq_status qoq_gemm(const fmpq_layout* L, const void* A_packed, const void* a_scales, const int32_t* a_sums,
+                     const void* W_packed, const void* ch_scales, const uint8_t* grp_scales, const uint8_t* grp_zeros,
+                     int64_t M, int64_t N, void* Y, int64_t ldy, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+    if (L == nullptr || A_packed == nullptr || a_scales == nullptr || a_sums == nullptr || W_packed == nullptr ||
+        ch_scales == nullptr || grp_scales == nullptr || grp_zeros == nullptr || Y == nullptr)
+        return FMPQ_ERR_INVALID_ARG;
+    if (L->n8 != L->nb) return FMPQ_ERR_INVALID_ARG;
+    if (M < 1 || M > INT32_MAX || N < 16 || N % 16 != 0 || N > INT32_MAX || ldy < N)
+        return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (ldy % 8 != 0 || !aligned16(A_packed) || !aligned16(a_scales) || !aligned16(a_sums) || !aligned16(W_packed) ||
+        !aligned16(ch_scales) || !aligned16(grp_scales) || !aligned16(grp_zeros) || !aligned16(Y))
+        return FMPQ_ERR_MISALIGNED;
+    const size_t need = fmpq::gemm_workspace_bytes(*L, M, N, true);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return FMPQ_ERR_WORKSPACE;
+    if (need > 0 && !aligned16(workspace)) return FMPQ_ERR_MISALIGNED;
+    if (fmpq_status st = check_device(L)) return st;
+    fmpq::GemmArgs a{};
+    a.A = A_packed;
+    a.a_scales = a_scales;
+    a.W = W_packed;
+    a.w_scales = ch_scales;   // not read by the QoQ path; a valid pointer
+    a.M = M;
+    a.N = N;
+    a.Y = Y;
+    a.ldy = ldy;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    a.zero_kind = fmpq::kZeroQoq;
+    a.unsigned_w = true;
+    a.a_sums = a_sums;
+    a.ch_scales = ch_scales;
+    a.grp_scales = grp_scales;
+    a.grp_zeros = grp_zeros;
+    return launched(fmpq::launch_gemm(*L, a, static_cast<cudaStream_t>(stream)));
+}
+
+fmpq_status qoq_gemm_partials(const fmpq_layout* L, const void* A_packed, const void* W_packed, int64_t M, int64_t N,
+                              int64_t m0, int64_t mcount, int64_t n0, int64_t ncount, int32_t* P, void* stream) {
+    if (L == nullptr || A_packed == nullptr || W_packed == nullptr || P == nullptr) return FMPQ_ERR_INVALID_ARG;
+    if (M < 1 || M > INT32_MAX || N < 16 || N % 16 != 0 || N > INT32_MAX) return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (m0 < 0 || mcount < 1 || m0 + mcount > M || n0 < 0 || ncount < 1 || n0 + ncount > N)
+        return FMPQ_ERR_INVALID_ARG;
+    if (!aligned16(A_packed) || !aligned16(W_packed)) return FMPQ_ERR_MISALIGNED;
+    if (fmpq_status st = check_device(L)) return st;
+    fmpq::GemmArgs a{};
+    a.A = A_packed;
+    a.W = W_packed;
+    a.M = M;
+    a.N = N;
+    a.P = P;
+    a.pm0 = m0;
+    a.pmcount = mcount;
+    a.pn0 = n0;
+    a.pncount = ncount;
+    a.unsigned_w = true;
+    a.a_scales = A_packed;   // scales are not read by the partial-sum export
+    a.w_scales = W_packed;
+    return launched(fmpq::launch_gemm(*L, a, static_cast<cudaStream_t>(stream)));
+}
+
 fmpq_status fmpq_channel_absmax(const void* X, int64_t ldx, int64_t T, int32_t K, uint32_t* absmax, void* stream) {
     if (X == nullptr || absmax == nullptr) return FMPQ_ERR_INVALID_ARG;
     if (K < FMPQ_BLOCK || K > FMPQ_MAX_K || K % FMPQ_BLOCK != 0 || T < 1 || ldx < K) return FMPQ_ERR_UNSUPPORTED_SHAPE;

@@ -59,6 +59,8 @@ constexpr int kSwStride = 68;
 struct ScaleSlot {
     float sw[4 * kSwStride];  // weight scales of the tile's 256 columns (permuted, see above)
     float sx[128];            // activation scales of this CTA's 128 rows, times 2^18
+    float wz[4 * kSwStride];  // zero-point variants: the weight factor of the zero term (same order)
+    float xz[128];            //   and the activation factor, per row
 };
 
 struct __align__(1024) Smem {
@@ -107,10 +109,23 @@ struct Params {
     // partial-sum export
     int32_t* P;
     int pm0, pmcount, pn0, pncount;
+    // quantization variants (see GemmArgs)
+    uint32_t wmask;        // code bits the converter keeps: 0x87878787 sign-magnitude, 0x0F0F0F0F unsigned
+    int zero_kind;
+    const uint16_t* a_zeros;
+    const int32_t* a_sums;
+    const float* w_sums;
+    const uint16_t* ch_scales;
+    const uint8_t* grp_scales;
+    const uint8_t* grp_zeros;
 };
 
-__device__ __forceinline__ uint32_t lo4(uint32_t w) { return w & 0x87878787u; }
-__device__ __forceinline__ uint32_t hi4(uint32_t w) { return __funnelshift_r(w, w, 4) & 0x87878787u; }
+// Codes 0-3 and 4-7 of a packed word as operand bytes. Sign-magnitude words keep |q| in bits
+// 0-2 / 4-6 and the signs in bits 7 / 3 of the next byte (mask 0x87878787); unsigned words
+// (QoQ) hold the codes in the low / high nibbles (mask 0x0F0F0F0F). Either way the byte is
+// the E4M3 value (-1)^s * m * 2^-9 for m <= 15.
+__device__ __forceinline__ uint32_t lo4(uint32_t w, uint32_t mask) { return w & mask; }
+__device__ __forceinline__ uint32_t hi4(uint32_t w, uint32_t mask) { return __funnelshift_r(w, w, 4) & mask; }
 
 // Work unit u -> (pair tile, split). Tiles run in bands of kGroupM m-tiles; inside a band
 // the m-tile varies fastest, so the pairs running together share activation and weight
@@ -300,17 +315,38 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, uint32_
     auto sw_pos = [](int i) { return ((i & 7) >> 1) * kSwStride + (i >> 3) * 2 + (i & 1); };
     const int swd0 = sw_pos(ct), swd1 = sw_pos(ct + 128);
 
+    const uint32_t wm = p.wmask;
     int u = blockIdx.x >> 1;
     if (u >= num_units) return;
     Unit t = unit_of(p, u);
     int b = t.b0;
-    uint16_t sc0 = 0, sc1 = 0, sc2 = 0;
+    // this thread's entries of the block's scales: weight columns ct and ct + 128, activation
+    // row ct (and the zero-term factors of the variants), fetched one block ahead as raw values
+    // and converted when they are staged, so that the loads' latency hides behind a block
+    uint32_t sc0 = 0, sc1 = 0, sc2 = 0;   // fp16 bits: weight scales (QoQ: s1) and activation scale
+    uint32_t zc0 = 0, zc1 = 0, zc2 = 0;   // QUIK: w_sums (fp32 bits) and the zero point (fp16 bits);
+                                          // QoQ: s2 | z2 << 8 per column and the code sum
     auto load_scales = [&](const Unit& tt, int bb) {
         const int n0 = tt.nt * kTileN, m0 = tt.mt * kPairM + static_cast<int>(rank) * 128;
-        const uint16_t* ws = p.w_scales + static_cast<int64_t>(bb) * p.N + n0;
-        sc0 = (n0 + ct < p.N) ? __ldg(ws + ct) : uint16_t(0);
-        sc1 = (n0 + ct + 128 < p.N) ? __ldg(ws + ct + 128) : uint16_t(0);
-        sc2 = (m0 + ct < p.M) ? __ldg(p.a_scales + static_cast<int64_t>(bb) * p.M + m0 + ct) : uint16_t(0);
+        const int n_a = n0 + ct, n_b = n0 + ct + 128, m = m0 + ct;
+        const int64_t wb = static_cast<int64_t>(bb) * p.N, xb = static_cast<int64_t>(bb) * p.M;
+        if (p.zero_kind != kZeroQoq) {
+            sc0 = n_a < p.N ? __ldg(p.w_scales + wb + n_a) : 0u;
+            sc1 = n_b < p.N ? __ldg(p.w_scales + wb + n_b) : 0u;
+            sc2 = m < p.M ? __ldg(p.a_scales + xb + m) : 0u;
+            if (p.zero_kind == kZeroQuik) {
+                zc0 = n_a < p.N ? __float_as_uint(__ldg(p.w_sums + wb + n_a)) : 0u;
+                zc1 = n_b < p.N ? __float_as_uint(__ldg(p.w_sums + wb + n_b)) : 0u;
+                zc2 = m < p.M ? __ldg(p.a_zeros + xb + m) : 0u;
+            }
+        } else {
+            sc0 = n_a < p.N ? __ldg(p.ch_scales + n_a) : 0u;
+            sc1 = n_b < p.N ? __ldg(p.ch_scales + n_b) : 0u;
+            sc2 = m < p.M ? __ldg(p.a_scales + m) : 0u;
+            zc0 = n_a < p.N ? (__ldg(p.grp_scales + wb + n_a) | (static_cast<uint32_t>(__ldg(p.grp_zeros + wb + n_a)) << 8)) : 0u;
+            zc1 = n_b < p.N ? (__ldg(p.grp_scales + wb + n_b) | (static_cast<uint32_t>(__ldg(p.grp_zeros + wb + n_b)) << 8)) : 0u;
+            zc2 = m < p.M ? static_cast<uint32_t>(__ldg(p.a_sums + xb + m)) : 0u;
+        }
     };
     load_scales(t, b);
     bool ok = true;
@@ -336,13 +372,33 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, uint32_
 #pragma unroll
         for (int k = 0; k < kPieces; ++k) {
             const uint4 v = w[k];
-            *reinterpret_cast<uint4*>(dst + dstA + k * kRowStep * 128) = make_uint4(lo4(v.x), hi4(v.x), lo4(v.y), hi4(v.y));
-            *reinterpret_cast<uint4*>(dst + dstB + k * kRowStep * 128) = make_uint4(lo4(v.z), hi4(v.z), lo4(v.w), hi4(v.w));
+            *reinterpret_cast<uint4*>(dst + dstA + k * kRowStep * 128) =
+                make_uint4(lo4(v.x, wm), hi4(v.x, wm), lo4(v.y, wm), hi4(v.y, wm));
+            *reinterpret_cast<uint4*>(dst + dstB + k * kRowStep * 128) =
+                make_uint4(lo4(v.z, wm), hi4(v.z, wm), lo4(v.w, wm), hi4(v.w, wm));
         }
         ScaleSlot& sl = s.sc[ss];
-        sl.sw[swd0] = __half2float(__ushort_as_half(sc0));
-        sl.sw[swd1] = __half2float(__ushort_as_half(sc1));
-        sl.sx[ct] = __half2float(__ushort_as_half(sc2)) * 262144.0f;   // 2^18 undoes the operand encoding
+        auto h2f = [](uint32_t h) { return __half2float(__ushort_as_half(static_cast<unsigned short>(h))); };
+        const float fx = h2f(sc2);
+        sl.sx[ct] = fx * 262144.0f;   // 2^18 undoes the operand encoding
+        if (p.zero_kind != kZeroQoq) {
+            sl.sw[swd0] = h2f(sc0);
+            sl.sw[swd1] = h2f(sc1);
+            if (p.zero_kind == kZeroQuik) {
+                sl.wz[swd0] = __uint_as_float(zc0);
+                sl.wz[swd1] = __uint_as_float(zc1);
+                sl.xz[ct] = h2f(zc2);
+            }
+        } else {
+            // QoQ: weight scale s1 * s2 (exact in fp32); zero term -(s1 s2 z2)[n] * (sx * code sum)[m]
+            const float w0 = h2f(sc0) * static_cast<float>(zc0 & 0xFFu);
+            const float w1 = h2f(sc1) * static_cast<float>(zc1 & 0xFFu);
+            sl.sw[swd0] = w0;
+            sl.sw[swd1] = w1;
+            sl.wz[swd0] = -w0 * static_cast<float>(zc0 >> 8);
+            sl.wz[swd1] = -w1 * static_cast<float>(zc1 >> 8);
+            sl.xz[ct] = fx * static_cast<float>(static_cast<int32_t>(zc2));
+        }
         dev::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -367,7 +423,7 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, uint32_
 // and all 256 columns, read with tcgen05.ld 16x256b: thread t holds rows t/4 and t/4 + 8 of
 // that slab and columns 8g + 2(t%4) + {0, 1}, g = 0..31 (four registers per 8 columns:
 // row0 col0, row0 col1, row1 col0, row1 col1).
-template <bool kPartials>
+template <bool kPartials, bool kZero>
 __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, uint32_t rank, int warp, int lane,
                                               uint32_t tmem, volatile int* abort_flag) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
@@ -413,25 +469,55 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, uint32_t
                     const float2 sxa = make_float2(xa, xa);
                     const float2 sxb = make_float2(xb, xb);
                     const float4* swv = reinterpret_cast<const float4*>(sl.sw + tq * kSwStride);
-                    // 8 chunks of 32 columns; the TMEM load of chunk c+1 overlaps the math of c
-                    uint32_t d0[16], d1[16];
-                    dev::tmem_ld16x256b_x4(taddr, d0);
+                    if constexpr (!kZero) {
+                        // 8 chunks of 32 columns; the TMEM load of chunk c+1 overlaps the math of c
+                        uint32_t d0[16], d1[16];
+                        dev::tmem_ld16x256b_x4(taddr, d0);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const float4 f0 = swv[2 * c], f1 = swv[2 * c + 1];   // column pairs g = 4c..4c+3
-                        uint32_t (&dc)[16] = (c & 1) ? d1 : d0;
-                        uint32_t (&dn)[16] = (c & 1) ? d0 : d1;
-                        dev::tmem_ld_wait16(dc);
-                        if (c < 7) dev::tmem_ld16x256b_x4(taddr + (c + 1) * 32, dn);
-                        const float2 swp[4] = {make_float2(f0.x, f0.y), make_float2(f0.z, f0.w),
-                                               make_float2(f1.x, f1.y), make_float2(f1.z, f1.w)};
+                        for (int c = 0; c < 8; ++c) {
+                            const float4 f0 = swv[2 * c], f1 = swv[2 * c + 1];   // column pairs g = 4c..4c+3
+                            uint32_t (&dc)[16] = (c & 1) ? d1 : d0;
+                            uint32_t (&dn)[16] = (c & 1) ? d0 : d1;
+                            dev::tmem_ld_wait16(dc);
+                            if (c < 7) dev::tmem_ld16x256b_x4(taddr + (c + 1) * 32, dn);
+                            const float2 swp[4] = {make_float2(f0.x, f0.y), make_float2(f0.z, f0.w),
+                                                   make_float2(f1.x, f1.y), make_float2(f1.z, f1.w)};
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int g = 4 * c + i;
-                            const float2 ca = dev::fmul2(swp[i], sxa);
-                            const float2 cb = dev::fmul2(swp[i], sxb);
-                            accA[g] = dev::ffma2(make_float2(__uint_as_float(dc[4 * i]), __uint_as_float(dc[4 * i + 1])), ca, accA[g]);
-                            accB[g] = dev::ffma2(make_float2(__uint_as_float(dc[4 * i + 2]), __uint_as_float(dc[4 * i + 3])), cb, accB[g]);
+                            for (int i = 0; i < 4; ++i) {
+                                const int g = 4 * c + i;
+                                const float2 ca = dev::fmul2(swp[i], sxa);
+                                const float2 cb = dev::fmul2(swp[i], sxb);
+                                accA[g] = dev::ffma2(make_float2(__uint_as_float(dc[4 * i]), __uint_as_float(dc[4 * i + 1])), ca, accA[g]);
+                                accB[g] = dev::ffma2(make_float2(__uint_as_float(dc[4 * i + 2]), __uint_as_float(dc[4 * i + 3])), cb, accB[g]);
+                            }
+                        }
+                    } else {
+                        // zero-point variants: the block's term x_zero[m] * w_zero[n] is added too;
+                        // single-buffered loads leave the second buffer's registers to its factors
+                        const float4* wzv = reinterpret_cast<const float4*>(sl.wz + tq * kSwStride);
+                        const float2 xza = make_float2(sl.xz[lr0], sl.xz[lr0]);
+                        const float2 xzb = make_float2(sl.xz[lr1], sl.xz[lr1]);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            uint32_t dc[16];
+                            dev::tmem_ld16x256b_x4(taddr + c * 32, dc);
+                            dev::tmem_ld_wait16(dc);
+                            const float4 f0 = swv[2 * c], f1 = swv[2 * c + 1];
+                            const float4 z0 = wzv[2 * c], z1 = wzv[2 * c + 1];
+                            const float2 swp[4] = {make_float2(f0.x, f0.y), make_float2(f0.z, f0.w),
+                                                   make_float2(f1.x, f1.y), make_float2(f1.z, f1.w)};
+                            const float2 wzp[4] = {make_float2(z0.x, z0.y), make_float2(z0.z, z0.w),
+                                                   make_float2(z1.x, z1.y), make_float2(z1.z, z1.w)};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int g = 4 * c + i;
+                                const float2 ca = dev::fmul2(swp[i], sxa);
+                                const float2 cb = dev::fmul2(swp[i], sxb);
+                                accA[g] = dev::ffma2(make_float2(__uint_as_float(dc[4 * i]), __uint_as_float(dc[4 * i + 1])), ca, accA[g]);
+                                accB[g] = dev::ffma2(make_float2(__uint_as_float(dc[4 * i + 2]), __uint_as_float(dc[4 * i + 3])), cb, accB[g]);
+                                accA[g] = dev::ffma2(xza, wzp[i], accA[g]);
+                                accB[g] = dev::ffma2(xzb, wzp[i], accB[g]);
+                            }
                         }
                     }
                 } else {
@@ -524,7 +610,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, uint32_t
     if (!ok && lane == 0) fail(p, abort_flag);
 }
 
-template <bool kPartials>
+template <bool kPartials, bool kZero>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) w4ax_gemm_kernel(const Params p) {
     extern __shared__ uint8_t smem_raw[];
     Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -586,7 +672,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) w4ax_ge
         }
     } else {
         dev::setmaxnreg_inc<192>();
-        epilogue_role<kPartials>(p, s, rank, warp, lane, tmem, abort_flag);
+        epilogue_role<kPartials, kZero>(p, s, rank, warp, lane, tmem, abort_flag);
     }
 
     dev::tc_fence_before();
@@ -600,6 +686,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) w4ax_ge
 
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory of the GEMM exceeds the 227 KB a CTA may use");
 
 // Pairs (2-CTA clusters) that can be resident at once: the persistent grid never launches
 // more, so no cluster waits for another to finish. Asked once per device.
@@ -613,9 +700,9 @@ int max_pairs(const fmpq_layout& L) {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = sizeof(Smem) + 1024;
     int clusters = 0;
-    if (cudaFuncSetAttribute(w4ax_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(w4ax_gemm_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(sizeof(Smem) + 1024)) == cudaSuccess &&
-        cudaOccupancyMaxActiveClusters(&clusters, w4ax_gemm_kernel<false>, &cfg) == cudaSuccess && clusters > 0 &&
+        cudaOccupancyMaxActiveClusters(&clusters, w4ax_gemm_kernel<false, false>, &cfg) == cudaSuccess && clusters > 0 &&
         clusters < pairs)
         pairs = clusters;
     cudaGetLastError();   // a failed query leaves no sticky error behind
@@ -636,31 +723,31 @@ int64_t pair_tiles(int64_t M, int64_t N) { return ((M + kPairM - 1) / kPairM) * 
 
 }  // namespace
 
-size_t gemm_counter_bytes(const fmpq_layout& L, int64_t M, int64_t N) {
-    if (gemm_small_path(M)) return gemm_small_counter_bytes(L, M, N);
+size_t gemm_counter_bytes(const fmpq_layout& L, int64_t M, int64_t N, bool variant) {
+    if (!variant && gemm_small_path(M)) return gemm_small_counter_bytes(L, M, N);
     const int64_t tiles = pair_tiles(M, N);
     if (choose_splits(L, tiles) == 1) return 0;
     return static_cast<size_t>(tiles) * 2 * sizeof(int32_t) + 16;
 }
 
-size_t gemm_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N) {
-    if (gemm_small_path(M)) return gemm_small_workspace_bytes(L, M, N);
+size_t gemm_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N, bool variant) {
+    if (!variant && gemm_small_path(M)) return gemm_small_workspace_bytes(L, M, N);
     const int64_t tiles = pair_tiles(M, N);
     const int splits = choose_splits(L, tiles);
     if (splits == 1) return 0;
-    return static_cast<size_t>(tiles) * splits * kPairM * kTileN * sizeof(float) + gemm_counter_bytes(L, M, N);
+    return static_cast<size_t>(tiles) * splits * kPairM * kTileN * sizeof(float) + gemm_counter_bytes(L, M, N, variant);
 }
 
 cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& a, cudaStream_t stream) {
-    if (a.P == nullptr && gemm_small_path(a.M)) return launch_gemm_small(L, a, stream);
+    const bool variant = a.zero_kind != kZeroNone || a.unsigned_w;
+    if (a.P == nullptr && !variant && gemm_small_path(a.M)) return launch_gemm_small(L, a, stream);
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(w4ax_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kSmemBytes));
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(w4ax_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSmemBytes));
-        if (e != cudaSuccess) return e;
+        for (auto fn : {w4ax_gemm_kernel<false, false>, w4ax_gemm_kernel<true, false>, w4ax_gemm_kernel<false, true>}) {
+            const cudaError_t e =
+                cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
+            if (e != cudaSuccess) return e;
+        }
         attr_set = true;
     }
     Params p{};
@@ -676,6 +763,14 @@ cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& a, cudaStream_t st
     p.mask = L.d_mask;
     p.poff = L.d_poff;
     p.status = L.d_status;
+    p.wmask = a.unsigned_w ? 0x0F0F0F0Fu : 0x87878787u;
+    p.zero_kind = a.zero_kind;
+    p.a_zeros = static_cast<const uint16_t*>(a.a_zeros);
+    p.a_sums = a.a_sums;
+    p.w_sums = a.w_sums;
+    p.ch_scales = static_cast<const uint16_t*>(a.ch_scales);
+    p.grp_scales = a.grp_scales;
+    p.grp_zeros = a.grp_zeros;
     const bool partials = a.P != nullptr;
     if (partials) {
         p.mt0 = static_cast<int>(a.pm0 / kPairM);
@@ -693,7 +788,7 @@ cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& a, cudaStream_t st
         p.mtiles = static_cast<int>((a.M + kPairM - 1) / kPairM);
         p.nt0 = 0;
         p.ntiles = static_cast<int>((a.N + kTileN - 1) / kTileN);
-        p.splits = choose_splits(L, static_cast<int64_t>(p.mtiles) * p.ntiles);
+        p.splits = choose_splits(L, static_cast<int64_t>(p.mtiles) * p.ntiles);   // as gemm_workspace_bytes
         if (p.splits > 1) {
             const int64_t tiles = static_cast<int64_t>(p.mtiles) * p.ntiles;
             p.ws_partial = static_cast<float*>(a.workspace);
@@ -705,9 +800,11 @@ cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& a, cudaStream_t st
     const int pairs = static_cast<int>(units < max_pairs(L) ? units : max_pairs(L));
     const int grid = 2 * pairs;   // clusters of two CTAs (one pair per two SMs)
     if (partials)
-        w4ax_gemm_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(p);
+        w4ax_gemm_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(p);
+    else if (a.zero_kind != kZeroNone)
+        w4ax_gemm_kernel<false, true><<<grid, kThreads, kSmemBytes, stream>>>(p);
     else
-        w4ax_gemm_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(p);
+        w4ax_gemm_kernel<false, false><<<grid, kThreads, kSmemBytes, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -28,12 +28,24 @@ constexpr int kTileN = 256;          // packed-weight row grouping and GEMM tile
 
 // Launchers (return cudaGetLastError() after the launch).
 // gamma_perm != nullptr: the quantized values are the row's RMSNorm with that gamma (permuted
-// channel order) and eps.
+// channel order) and eps. mode: kQuantSym (FMPQ), kQuantAsym (QUIK asymmetric, aux = zero points
+// fp16 [nb][M]), kQuantTok (QoQ per-token INT8, aux = block code sums int32 [nb][M]; scales [M]).
+enum { kQuantSym = 0, kQuantAsym = 2, kQuantTok = 3 };
 cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, int64_t M, void* A, void* scales,
-                            cudaStream_t stream, const void* gamma_perm = nullptr, float eps = 0.0f);
+                            cudaStream_t stream, const void* gamma_perm = nullptr, float eps = 0.0f,
+                            int mode = kQuantSym, void* aux = nullptr);
+// QoQ progressive weights: unsigned 4-bit codes in the packed layout, s1 fp16 [N], s2 / z2 [nb][N].
+cudaError_t launch_qoq_pack_weights(const fmpq_layout& L, const void* W, int64_t ldw, int64_t N, void* Wp,
+                                    void* s1, uint8_t* s2, uint8_t* z2, cudaStream_t stream);
+// QUIK zero-point term: wsum [nb][N] = w_scale * sum of the block's codes (packed sign-magnitude).
+cudaError_t launch_weight_sums(const fmpq_layout& L, const void* Wp, const void* w_scales, int64_t N, float* wsum,
+                               cudaStream_t stream);
 cudaError_t launch_pack_weights(const fmpq_layout& L, const void* W, int64_t ldw, int64_t N, void* Wp,
                                 void* scales, cudaStream_t stream);
-cudaError_t launch_unpack_weights(const fmpq_layout& L, const void* Wp, int64_t N, int8_t* Wq, cudaStream_t stream);
+cudaError_t launch_unpack_weights(const fmpq_layout& L, const void* Wp, int64_t N, int8_t* Wq, cudaStream_t stream,
+                                  bool unsigned_codes = false);
+
+enum { kZeroNone = 0, kZeroQuik = 1, kZeroQoq = 2 };
 
 struct GemmArgs {
     const void* A;
@@ -48,12 +60,27 @@ struct GemmArgs {
     // partial-sum export (debug): when P != nullptr the kernel writes P instead of Y
     int32_t* P;
     int64_t pm0, pmcount, pn0, pncount;
+    // Quantization variants (the defaults are FMPQ: signed weight codes, per-block activation
+    // scales, no zero-point term). Each block then adds x_zero[m] * w_zero[n] to the output:
+    //   kZeroQuik: x_zero = a_zeros[b][m] (fp16), w_zero = w_sums[b][n] (fp32)
+    //   kZeroQoq:  activation scale a_scales[m] for every block; weight scale
+    //              ch_scales[n] * grp_scales[b][n]; x_zero = a_scales[m] * a_sums[b][m],
+    //              w_zero = -ch_scales[n] * grp_scales[b][n] * grp_zeros[b][n]
+    int zero_kind = kZeroNone;
+    bool unsigned_w = false;          // weight codes are unsigned 4-bit (QoQ), not sign-magnitude
+    const void* a_zeros = nullptr;
+    const int32_t* a_sums = nullptr;
+    const float* w_sums = nullptr;
+    const void* ch_scales = nullptr;
+    const uint8_t* grp_scales = nullptr;
+    const uint8_t* grp_zeros = nullptr;
 };
 
 // Workspace of a split-K launch: FP32 partial tiles followed by the arrival counters
 // (gemm_counter_bytes of it, at the end). Both are 0 when the shape needs no split.
-size_t gemm_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N);
-size_t gemm_counter_bytes(const fmpq_layout& L, int64_t M, int64_t N);
+// `variant`: a quantization variant (they always run the 2-SM kernel, whatever M).
+size_t gemm_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N, bool variant = false);
+size_t gemm_counter_bytes(const fmpq_layout& L, int64_t M, int64_t N, bool variant = false);
 cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& args, cudaStream_t stream);
 
 // Outlier split, FP16 path: gather X[:, cols] into X_out, Y += X_out * W_out^T (cuBLAS, loaded on

@@ -111,6 +111,7 @@ constexpr int kQWarpsMin = 16, kQWarpsMax = 28;
 constexpr int kQNormWarps = 8;                     // fused RMSNorm: warps computing the rows' norms
 constexpr int kQMaxThreads = (kQWarpsMax + 1) * 32;   // >= (16 + 1 + 8) * 32
 constexpr int kQSmemBudget = 200 * 1024;
+enum : int { kQSym = 0, kQNorm = 1, kQAsym = 2, kQTok = 3 };   // quantizer modes
 
 struct QuantParams {
     const uint16_t* X;
@@ -128,6 +129,8 @@ struct QuantParams {
     int32_t* status;
     const uint16_t* gamma_perm;   // fused RMSNorm: gamma in the permuted channel order
     float eps;
+    uint16_t* zeros;              // QUIK asymmetric: zero points [nb][M]
+    int32_t* sums;                // QoQ per-token INT8: sums of each block's codes [nb][M]
 };
 
 __device__ __forceinline__ float rcp_approx(float x) {
@@ -154,6 +157,70 @@ __device__ __forceinline__ uint32_t high_plane(uint32_t w) {
     return __byte_perm(0x1C181000u, 0x26242220u, sel) | (w & 0x80808080u);
 }
 
+// Order key of two fp16 values (one per half of the word): a 16-bit key per half that orders
+// like the values, -0 below +0 (negative: all bits flipped; positive: the sign bit set).
+__device__ __forceinline__ uint32_t f16x2_order_keys(uint32_t x) {
+    return x ^ (0x80008000u | (((x >> 15) & 0x00010001u) * 0x7FFFu));
+}
+__device__ __forceinline__ uint32_t f16_from_order_key(uint32_t k) { return (k ^ ((k & 0x8000u) ? 0x8000u : 0xFFFFu)) & 0xFFFFu; }
+
+// One QUIK-asymmetric block step of a half-warp (8 values per lane in h2): zero point, scale,
+// codes in [0, 15], stores. The quotient (x - z) / s is approximated by a product with the
+// reciprocal (error below 2^-17 for quotients up to 16); where that lands within 2^-16 of a
+// half-integer the warp recomputes its quotients with IEEE division, so the rounding is that
+// of the IEEE fp32 quotient.
+template <typename Params>
+__device__ __forceinline__ void quantize_asym_step(const Params& p, const uint32_t (&h2)[4], bool valid, int b, int64_t m,
+                                                   uint32_t chunk_off, int sub, uint32_t hmask, const int32_t* s_poff) {
+    uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t key = f16x2_order_keys(h2[k]);
+        kmin = __vminu2(kmin, key);
+        kmax = __vmaxu2(kmax, key);
+    }
+    kmin = __reduce_min_sync(hmask, min(kmin & 0xFFFFu, kmin >> 16));
+    kmax = __reduce_max_sync(hmask, max(kmax & 0xFFFFu, kmax >> 16));
+    const uint32_t zbits = f16_from_order_key(kmin);
+    const float z = __half2float(__ushort_as_half(static_cast<unsigned short>(zbits)));
+    const float mx = __half2float(__ushort_as_half(static_cast<unsigned short>(f16_from_order_key(kmax))));
+    const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, z), 15.0f));
+    const float sc = __half2float(s16);
+    const float inv = sc > 0.0f ? rcp_approx(sc) : 0.0f;
+    constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23: adding it rounds to an integer (RNE)
+    float d[8], tm[8];
+    bool near_half = false;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2[k]));
+        d[2 * k] = __fsub_rn(f.x, z);
+        d[2 * k + 1] = __fsub_rn(f.y, z);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        tm[k] = __fmaf_rn(d[k], inv, kMagic);
+        near_half |= fabsf(__fmaf_rn(d[k], inv, kMagic - tm[k])) >= 0.5f - 1.52587890625e-05f;   // 2^-16
+    }
+    if (__any_sync(0xFFFFFFFFu, near_half && sc > 0.0f)) {
+        if (sc > 0.0f) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) tm[k] = __fadd_rn(__fdiv_rn(d[k], sc), kMagic);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) tm[k] = sc > 0.0f ? fminf(tm[k], kMagic + 15.0f) : kMagic;
+    const uint32_t w0 = low_bytes4(tm[0], tm[1], tm[2], tm[3]);
+    const uint32_t w1 = low_bytes4(tm[4], tm[5], tm[6], tm[7]);
+    if (valid) {
+        uint8_t* dst = p.A + (static_cast<int64_t>(s_poff[b]) * p.M + m) * kBlock + chunk_off;
+        *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
+        if (sub == 0) {
+            p.scales[static_cast<int64_t>(b) * p.M + m] = __half_as_ushort(s16);
+            p.zeros[static_cast<int64_t>(b) * p.M + m] = static_cast<uint16_t>(zbits);
+        }
+    }
+}
+
 // Shared memory: [S] rows of X | gather offsets [iters][16 warps][32 lanes] (8 byte offsets of
 // 16 bits per lane and block pair) | plane offset per block | full / empty barriers per stage.
 __host__ __device__ inline size_t quant_gtab_offset(int K, int S) { return (2ull * K * S + 15) & ~15ull; }
@@ -173,9 +240,18 @@ __host__ __device__ inline size_t quant_bars_offset(int K, int S, int iters, int
 // by 16 lanes of 8 consecutive channels each (sequential fp32 adds of the exact squares), the
 // 16 lane sums are combined by an xor tree (8, 4, 2, 1), and the chunk sums by 32 lanes taking
 // chunks l, l+32, ... sequentially and an xor tree (16, ..., 1).
+// kQAsym (QUIK explainer, "反量化背后的数学": asymmetric activations): every block 4-bit with a
+// zero point z = the block's smallest input (value order, -0 below +0) and
+// s = fp16_rn((fp32(max) - fp32(z)) / 15); q = clamp(rne(fp32(fp32(x) - fp32(z)) / fp32(s)), 0, 15)
+// with IEEE fp32 operations; codes in one plane with the sign bit clear.
+// kQTok (QServe explainer, "运行时设计": W4A8 GEMMs take per-token INT8 activations): the row's
+// absmax (computed by the norm warps ahead of the quantizing warps) gives one scale per token,
+// s = fp16_rn(fp32(absmax) / 127); every block INT8; the sum of each block's codes is written too.
 // kTwo: the 16-warp instantiation that two CTAs share an SM with (registers bounded for it).
-template <bool kNorm, bool kTwo = false>
+template <int kMode, bool kTwo = false>
 __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, kTwo ? 2 : 1) quantize_kernel(QuantParams p) {
+    constexpr bool kNorm = kMode == kQNorm;
+    constexpr bool kRowWarps = kMode == kQNorm || kMode == kQTok;   // a per-row statistic comes first
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int K = p.K, Kr = p.Kin, nb = p.nb, S = p.stages;
     uint16_t* rows_s = reinterpret_cast<uint16_t*>(smem_raw);                                // [S][Kin]
@@ -194,7 +270,7 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             dev::mbar_init(&full[s], 1);
-            dev::mbar_init(&empty[s], p.cwarps + (kNorm ? kQNormWarps : 0));
+            dev::mbar_init(&empty[s], p.cwarps + (kRowWarps ? kQNormWarps : 0));
             dev::mbar_init(&nsync[s], kQNormWarps);
             dev::mbar_init(&rready[s], 1);
         }
@@ -233,7 +309,7 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
         // ---------------- norm warps (fused RMSNorm): per row, the chunk sums of squares (norm
         // warp w takes the chunk pairs w, w + 2, ...; each half-warp one chunk) and then, in
         // norm warp 0, the row total and r; they run ahead of the quantizing warps
-        if constexpr (kNorm) {
+        if constexpr (kRowWarps) {
             const int nw = warp - W - 1;
             const int half = lane >> 4, sub16 = lane & 15;
             const uint32_t hm = half ? 0xFFFF0000u : 0x0000FFFFu;
@@ -252,15 +328,26 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
                     if (b < nb) {
                         const uint4 v = *reinterpret_cast<const uint4*>(row + (b * kBlock + sub16 * 8) * 2);
                         const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                        if constexpr (kNorm) {
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[k]));
-                            acc = __fadd_rn(acc, __fmul_rn(f.x, f.x));   // squares of fp16 values are exact
-                            acc = __fadd_rn(acc, __fmul_rn(f.y, f.y));
+                            for (int k = 0; k < 4; ++k) {
+                                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[k]));
+                                acc = __fadd_rn(acc, __fmul_rn(f.x, f.x));   // squares of fp16 values are exact
+                                acc = __fadd_rn(acc, __fmul_rn(f.y, f.y));
+                            }
+                        } else {
+                            // the chunk's absmax (fp16 magnitudes order like their bit patterns)
+                            uint32_t m2 = 0;
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) m2 = __vmaxu2(m2, w4[k] & 0x7FFF7FFFu);
+                            acc = __half2float(__ushort_as_half(static_cast<unsigned short>(max(m2 & 0xFFFFu, m2 >> 16))));
                         }
                     }
 #pragma unroll
-                    for (int st = 8; st >= 1; st >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(hm, acc, st));
+                    for (int st = 8; st >= 1; st >>= 1) {
+                        const float o = __shfl_xor_sync(hm, acc, st);
+                        acc = kNorm ? __fadd_rn(acc, o) : fmaxf(acc, o);
+                    }
                     if (b < nb && sub16 == 0) cs[b] = acc;
                 }
                 __syncwarp();
@@ -269,12 +356,15 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
                     ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&nsync[s], ph, &abort_flag));
                     if (!ok) break;
                     float t = 0.0f;
-                    for (int b = lane; b < nb; b += 32) t = __fadd_rn(t, cs[b]);
+                    for (int b = lane; b < nb; b += 32) t = kNorm ? __fadd_rn(t, cs[b]) : fmaxf(t, cs[b]);
 #pragma unroll
-                    for (int st = 16; st >= 1; st >>= 1) t = __fadd_rn(t, __shfl_xor_sync(0xFFFFFFFFu, t, st));
-                    const float ms = __fdiv_rn(t, static_cast<float>(K));
+                    for (int st = 16; st >= 1; st >>= 1) {
+                        const float o = __shfl_xor_sync(0xFFFFFFFFu, t, st);
+                        t = kNorm ? __fadd_rn(t, o) : fmaxf(t, o);
+                    }
                     if (lane == 0) {
-                        r_s[s] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, p.eps)));
+                        // RMSNorm: r = 1 / sqrt(T / K + eps); per-token INT8: the row's absmax
+                        r_s[s] = kNorm ? __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, static_cast<float>(K)), p.eps))) : t;
                         dev::mbar_arrive(&rready[s]);
                     }
                 }
@@ -320,10 +410,14 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
             const uint32_t chunk_off = ((static_cast<uint32_t>(sub >> 1) ^ static_cast<uint32_t>(m & 7)) << 4) +
                                        static_cast<uint32_t>(sub & 1) * 8u;
             float r_norm = 1.0f;
-            if constexpr (kNorm) {
-                ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&rready[s], ph, &abort_flag));   // the row's factor
+            if constexpr (kRowWarps) {
+                ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&rready[s], ph, &abort_flag));   // the row's statistic
                 if (!ok) break;
                 r_norm = r_s[s];
+            }
+            if constexpr (kMode == kQTok) {
+                if (warp == 0 && lane == 0)
+                    p.scales[m] = __half_as_ushort(__float2half_rn(__fmul_rn(r_norm, 1.0f / 127.0f)));
             }
 #pragma unroll 1
             for (int j = 0; j < iters; ++j) {                // warp-uniform bound
@@ -340,6 +434,11 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
                         const uint32_t hi = *reinterpret_cast<const uint16_t*>(row + (gw[k] >> 16));
                         h2[k] = __byte_perm(lo, hi, 0x5410);
                     }
+                }
+                if constexpr (kMode == kQAsym) {
+                    quantize_asym_step(p, h2, valid, warp + 2 * W * j + (upper ? W : 0), m, chunk_off, sub, hmask,
+                                       s_poff);
+                    continue;
                 }
                 if constexpr (kNorm) {
                     // normalize: y = fp16_rn((x * r) * gamma), gamma of the lane's 8 permuted channels
@@ -368,8 +467,9 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
                 const __half lm = __hmax(__low2half(mx), __high2half(mx));
                 const uint32_t amax_bits = __reduce_max_sync(hmask, static_cast<uint32_t>(__half_as_ushort(lm)));
                 // scale: fp16(fp32(absmax) * fp32(1/qmax)) equals fp16(fp32(absmax) / qmax)
-                // for every finite fp16 absmax and qmax in {7, 127}
-                const float amax = __half2float(__ushort_as_half(static_cast<unsigned short>(amax_bits)));
+                // for every finite fp16 absmax and qmax in {7, 127}; per-token INT8 takes the
+                // row's absmax instead of the block's
+                const float amax = kMode == kQTok ? r_norm : __half2float(__ushort_as_half(static_cast<unsigned short>(amax_bits)));
                 const float qm = is8 ? 127.0f : 7.0f;
                 const __half s16 = __float2half_rn(__fmul_rn(amax, is8 ? (1.0f / 127.0f) : (1.0f / 7.0f)));
                 const float sc = __half2float(s16);
@@ -427,7 +527,18 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
                         *reinterpret_cast<uint2*>(dst) = make_uint2(w0 & 0x8F8F8F8Fu, w1 & 0x8F8F8F8Fu);
                         *reinterpret_cast<uint2*>(dst + plane_stride) = make_uint2(high_plane(w0), high_plane(w1));
                     }
-                    if (sub == 0) p.scales[static_cast<int64_t>(b) * p.M + m] = __half_as_ushort(s16);
+                    if constexpr (kMode == kQTok) {
+                        // the sum of the block's signed codes: magnitudes (bits 0-6) times +-1
+                        // from the sign bits, four bytes per dp4a
+                        auto sum4 = [](uint32_t w) {
+                            const uint32_t pm = 0x01010101u | (((w >> 7) & 0x01010101u) * 0xFEu);
+                            return __dp4a(static_cast<int>(w & 0x7F7F7F7Fu), static_cast<int>(pm), 0);
+                        };
+                        const int t = __reduce_add_sync(hmask, sum4(w0) + sum4(w1));
+                        if (sub == 0) p.sums[static_cast<int64_t>(b) * p.M + m] = t;
+                    } else {
+                        if (sub == 0) p.scales[static_cast<int64_t>(b) * p.M + m] = __half_as_ushort(s16);
+                    }
                 }
             }
             __syncwarp();
@@ -477,8 +588,111 @@ __global__ void __launch_bounds__(256) pack_weights_kernel(PackParams p) {
     if (lane == 0 && n < p.N) p.scales[static_cast<int64_t>(b) * p.N + n] = sbits;
 }
 
-// Debug decode of the packed weights to int8 codes [N][K] (permuted channel order).
-__global__ void unpack_weights_kernel(const uint8_t* Wp, int64_t N, int K, int nb, int8_t* Wq) {
+// ---------------------------------------------------------------------------------
+// QoQ progressive group quantization (QServe explainer, "渐进式分组量化"), offline: one warp per
+// output channel n.
+//   s1 = fp16_rn(fp32(absmax of the row) / 119); q8 = clamp(rne(fp32(w) / fp32(s1)), -119, 119)
+//   (IEEE division; the protective range keeps the dequantized group codes inside INT8);
+//   per block b (the group): the range of its q8 extended to include 0, [mn, mx];
+//   s2 = max(1, ceil((mx - mn) / 15)), z2 = clamp(rne(-mn / s2), 0, 15),
+//   q4 = clamp(rne(q8 / s2) + z2, 0, 15) (exact rationals, ties to even).
+// Codes are packed as unsigned nibbles in the packed-weight tile layout: byte j of a word holds
+// code j in bits 0-3 and code 4 + j in bits 4-7. The row's absmax is over its K channels (the
+// layout selects all of them).
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ int rne_div_int(int a, int b) {   // b > 0
+    int q = a / b, r = a % b;
+    if (r < 0) {
+        q -= 1;
+        r += b;
+    }
+    if (2 * r > b || (2 * r == b && (q & 1))) ++q;
+    return q;
+}
+
+struct QoqPackParams {
+    const uint16_t* W;
+    int64_t ldw;
+    int64_t N, Npad;
+    int K, nb;
+    const uint16_t* perm;
+    uint8_t* Wp;
+    uint16_t* s1;
+    uint8_t* s2;
+    uint8_t* z2;
+};
+
+__global__ void __launch_bounds__(256) qoq_pack_weights_kernel(QoqPackParams p) {
+    const int lane = threadIdx.x & 31;
+    const int64_t n = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (n >= p.Npad) return;   // warp-uniform
+    float s1f = 0.0f;
+    if (n < p.N) {
+        uint32_t m = 0;
+        const uint16_t* row = p.W + n * p.ldw;
+        for (int c = lane; c < p.K; c += 32) m = max(m, static_cast<uint32_t>(row[c] & 0x7FFFu));
+        m = __reduce_max_sync(0xFFFFFFFFu, m);
+        const __half sb = __float2half_rn(__fdiv_rn(__half2float(__ushort_as_half(static_cast<unsigned short>(m))), 119.0f));
+        s1f = __half2float(sb);
+        if (lane == 0) p.s1[n] = __half_as_ushort(sb);
+    }
+    for (int b = 0; b < p.nb; ++b) {
+        uint32_t v = 0;   // this lane's 4 codes, one per byte
+        if (n < p.N) {
+            int q8[4];
+            int lo = 0, hi = 0;   // the range includes 0
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float w = __half2float(__ushort_as_half(p.W[n * p.ldw + p.perm[b * kBlock + lane * 4 + i]]));
+                int q = s1f > 0.0f ? __float2int_rn(__fdiv_rn(w, s1f)) : 0;   // round half to even
+                q = min(119, max(-119, q));
+                q8[i] = q;
+                lo = min(lo, q);
+                hi = max(hi, q);
+            }
+            lo = __reduce_min_sync(0xFFFFFFFFu, lo);
+            hi = __reduce_max_sync(0xFFFFFFFFu, hi);
+            const int s2 = max(1, (hi - lo + 14) / 15);
+            const int z2 = min(15, max(0, rne_div_int(-lo, s2)));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v |= static_cast<uint32_t>(min(15, max(0, rne_div_int(q8[i], s2) + z2))) << (8 * i);
+            if (lane == 0) {
+                p.s2[static_cast<int64_t>(b) * p.N + n] = static_cast<uint8_t>(s2);
+                p.z2[static_cast<int64_t>(b) * p.N + n] = static_cast<uint8_t>(z2);
+            }
+        }
+        // lanes 2g, 2g+1 hold channels 8g..8g+3 and 8g+4..8g+7
+        const uint32_t mine = (lane & 1) ? (v << 4) : v;
+        const uint32_t word = mine | __shfl_xor_sync(0xFFFFFFFFu, mine, 1);
+        uint8_t* dst = p.Wp + ((n / kTileN) * p.nb + b) * 16384 + (n % kTileN) * 64;
+        if ((lane & 1) == 0) reinterpret_cast<uint32_t*>(dst)[lane >> 1] = word;
+    }
+}
+
+// Offline weight sums for the QUIK zero-point term: wsum[b][n] = w_scale[b][n] * (sum of the
+// block's codes), one thread per (n, b), from the packed sign-magnitude words.
+__global__ void weight_sums_kernel(const uint8_t* Wp, const uint16_t* w_scales, int64_t N, int nb, float* wsum) {
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (t >= N * nb) return;
+    const int b = static_cast<int>(t / N);
+    const int64_t n = t % N;
+    const uint32_t* row = reinterpret_cast<const uint32_t*>(Wp + ((n / kTileN) * nb + b) * 16384 + (n % kTileN) * 64);
+    auto sum4 = [](uint32_t x) {   // four sign-magnitude bytes: magnitude bits 0-2, sign bit 7
+        const uint32_t pm = 0x01010101u | (((x >> 7) & 0x01010101u) * 0xFEu);
+        return __dp4a(static_cast<int>(x & 0x07070707u), static_cast<int>(pm), 0);
+    };
+    int sum = 0;
+#pragma unroll
+    for (int g = 0; g < 16; ++g) {
+        const uint32_t w = row[g];
+        sum += sum4(w & 0x87878787u) + sum4(__funnelshift_r(w, w, 4) & 0x87878787u);
+    }
+    wsum[t] = __half2float(__ushort_as_half(w_scales[t])) * static_cast<float>(sum);   // exact
+}
+
+// Debug decode of the packed weights to int8 codes [N][K] (permuted channel order);
+// unsigned_codes: the QoQ nibble format.
+__global__ void unpack_weights_kernel(const uint8_t* Wp, int64_t N, int K, int nb, int8_t* Wq, bool unsigned_codes) {
     const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;  // one word
     const int64_t words_per_row = K / 8;
     if (t >= N * words_per_row) return;
@@ -491,6 +705,11 @@ __global__ void unpack_weights_kernel(const uint8_t* Wp, int64_t N, int K, int n
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const uint32_t byte = (w >> (8 * j)) & 0xFFu;
+        if (unsigned_codes) {
+            out[j] = static_cast<int8_t>(byte & 15u);
+            out[4 + j] = static_cast<int8_t>(byte >> 4);
+            continue;
+        }
         const uint32_t next = (w >> (8 * ((j + 1) & 3))) & 0xFFu;
         const int lo = byte & 7, hi = (byte >> 4) & 7;
         out[j] = static_cast<int8_t>((byte & 0x80u) ? -lo : lo);
@@ -501,10 +720,12 @@ __global__ void unpack_weights_kernel(const uint8_t* Wp, int64_t N, int K, int n
 }  // namespace
 
 cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, int64_t M, void* A, void* scales,
-                            cudaStream_t stream, const void* gamma_perm, float eps) {
+                            cudaStream_t stream, const void* gamma_perm, float eps, int mode, void* aux) {
     const int K = L.K, Kin = L.K_in;
+    if (gamma_perm != nullptr) mode = kQNorm;
+    const bool row_warps = mode == kQNorm || mode == kQTok;
     int cw = kQWarpsMin;
-    if (gamma_perm == nullptr)
+    if (!row_warps)
         for (int w = kQWarpsMax; w > kQWarpsMin; --w)
             if (L.nb % (2 * w) == 0) {
                 cw = w;
@@ -521,13 +742,13 @@ cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, in
     // half the budget and both fit; the warps of the second CTA hide the first one's latencies.
     int per_sm = 1;
     int stages = stages_for(kQSmemBudget);
-    if (gamma_perm == nullptr && cw == kQWarpsMin && stages_for(kQSmemBudget / 2) >= 3) {
+    if (mode == kQSym && cw == kQWarpsMin && stages_for(kQSmemBudget / 2) >= 3) {
         const int st2 = stages_for(kQSmemBudget / 2);
         const size_t smem2 = quant_bars_offset(Kin, st2, iters * cw, L.nb) + 8ull * (4 * st2);
         int blocks = 0;
-        if (cudaFuncSetAttribute(quantize_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(quantize_kernel<kQSym, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kQSmemBudget + 16 * 1024) == cudaSuccess &&
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, quantize_kernel<false, true>, (cw + 1) * 32, smem2) ==
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, quantize_kernel<kQSym, true>, (cw + 1) * 32, smem2) ==
                 cudaSuccess &&
             blocks >= 2) {
             per_sm = 2;
@@ -539,12 +760,11 @@ cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, in
     const size_t smem = quant_bars_offset(Kin, stages, iters * cw, L.nb) + 8ull * (4 * stages);
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(quantize_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kQSmemBudget + 16 * 1024);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(quantize_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kQSmemBudget + 16 * 1024);
-        if (e != cudaSuccess) return e;
+        for (auto fn : {quantize_kernel<kQSym>, quantize_kernel<kQNorm>, quantize_kernel<kQAsym>, quantize_kernel<kQTok>}) {
+            const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       kQSmemBudget + 16 * 1024);
+            if (e != cudaSuccess) return e;
+        }
         attr_set = true;
     }
     QuantParams p;
@@ -565,14 +785,21 @@ cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, in
     p.status = L.d_status;
     p.gamma_perm = static_cast<const uint16_t*>(gamma_perm);
     p.eps = eps;
+    p.zeros = mode == kQAsym ? static_cast<uint16_t*>(aux) : nullptr;
+    p.sums = mode == kQTok ? static_cast<int32_t*>(aux) : nullptr;
     const int64_t ctas = static_cast<int64_t>(L.num_sms) * per_sm;
-    const int64_t grid = M < ctas ? M : ctas;
-    if (gamma_perm != nullptr)
-        quantize_kernel<true><<<static_cast<unsigned>(grid), (cw + 1 + kQNormWarps) * 32, smem, stream>>>(p);
-    else if (per_sm == 2)
-        quantize_kernel<false, true><<<static_cast<unsigned>(grid), (cw + 1) * 32, smem, stream>>>(p);
-    else
-        quantize_kernel<false><<<static_cast<unsigned>(grid), (cw + 1) * 32, smem, stream>>>(p);
+    const unsigned grid = static_cast<unsigned>(M < ctas ? M : ctas);
+    const unsigned threads = static_cast<unsigned>((cw + 1 + (row_warps ? kQNormWarps : 0)) * 32);
+    switch (mode) {
+        case kQNorm: quantize_kernel<kQNorm><<<grid, threads, smem, stream>>>(p); break;
+        case kQAsym: quantize_kernel<kQAsym><<<grid, threads, smem, stream>>>(p); break;
+        case kQTok: quantize_kernel<kQTok><<<grid, threads, smem, stream>>>(p); break;
+        default:
+            if (per_sm == 2)
+                quantize_kernel<kQSym, true><<<grid, threads, smem, stream>>>(p);
+            else
+                quantize_kernel<kQSym><<<grid, threads, smem, stream>>>(p);
+    }
     return cudaGetLastError();
 }
 
@@ -594,11 +821,39 @@ cudaError_t launch_pack_weights(const fmpq_layout& L, const void* W, int64_t ldw
     return cudaGetLastError();
 }
 
-cudaError_t launch_unpack_weights(const fmpq_layout& L, const void* Wp, int64_t N, int8_t* Wq, cudaStream_t stream) {
+cudaError_t launch_unpack_weights(const fmpq_layout& L, const void* Wp, int64_t N, int8_t* Wq, cudaStream_t stream,
+                                  bool unsigned_codes) {
     const int64_t words = N * (L.K / 8);
     const int64_t blocks = (words + 255) / 256;
     unpack_weights_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(static_cast<const uint8_t*>(Wp), N,
-                                                                             L.K, L.nb, Wq);
+                                                                             L.K, L.nb, Wq, unsigned_codes);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_qoq_pack_weights(const fmpq_layout& L, const void* W, int64_t ldw, int64_t N, void* Wp,
+                                    void* s1, uint8_t* s2, uint8_t* z2, cudaStream_t stream) {
+    QoqPackParams p;
+    p.W = static_cast<const uint16_t*>(W);
+    p.ldw = ldw;
+    p.N = N;
+    p.Npad = (N + kTileN - 1) / kTileN * kTileN;
+    p.K = L.K;
+    p.nb = L.nb;
+    p.perm = L.d_perm16;
+    p.Wp = static_cast<uint8_t*>(Wp);
+    p.s1 = static_cast<uint16_t*>(s1);
+    p.s2 = s2;
+    p.z2 = z2;
+    const int64_t blocks = (p.Npad * 32 + 255) / 256;
+    qoq_pack_weights_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_weight_sums(const fmpq_layout& L, const void* Wp, const void* w_scales, int64_t N, float* wsum,
+                               cudaStream_t stream) {
+    const int64_t threads = N * L.nb;
+    weight_sums_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(
+        static_cast<const uint8_t*>(Wp), static_cast<const uint16_t*>(w_scales), N, L.nb, wsum);
     return cudaGetLastError();
 }
 

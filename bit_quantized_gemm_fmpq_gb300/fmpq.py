@@ -46,6 +46,15 @@ SIGNATURES = {
     "w4ax_gemm_partials": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P]),
     "fmpq_device_status": (_I32, [_P, ctypes.POINTER(_I32), _I32]),
     "fmpq_rmsnorm_quantize": (_I32, [_P, _P, _I64, _I64, _P, ctypes.c_float, _P, _P, _P]),
+    "fmpq_variant_gemm_workspace_bytes": (_SZ, [_P, _I64, _I64]),
+    "fmpq_quantize_asym": (_I32, [_P, _P, _I64, _I64, _P, _P, _P, _P]),
+    "w4_weight_sums": (_I32, [_P, _P, _P, _I64, _P, _P]),
+    "w4ax_gemm_asym": (_I32, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, _I64, _P, _SZ, _P]),
+    "qoq_pack_weights": (_I32, [_P, _P, _I64, _I64, _P, _P, _P, _P, _P]),
+    "qoq_unpack_weights": (_I32, [_P, _P, _I64, _P, _P]),
+    "qoq_quantize": (_I32, [_P, _P, _I64, _I64, _P, _P, _P, _P]),
+    "qoq_gemm": (_I32, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, _I64, _P, _SZ, _P]),
+    "qoq_gemm_partials": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P]),
     "fmpq_layout_create_select": (_I32, [_I32, _I32, _P, _P, ctypes.POINTER(_P)]),
     "fmpq_outlier_gemm_fp16": (_I32, [_P, _I64, _I64, _P, _I32, _P, _I64, _I64, _P, _P, _I64, _P]),
     "fmpq_channel_absmax": (_I32, [_P, _I64, _I64, _I32, _P, _P]),
@@ -149,10 +158,12 @@ class Layout:
     def workspace_bytes(self, M: int, N: int) -> int:
         return int(self._lib.w4ax_gemm_workspace_bytes(self._h, M, N))
 
-    def workspace(self, M: int, N: int):
-        """A zero-initialised, reusable workspace tensor for (M, N) (cached per size)."""
+    def workspace(self, M: int, N: int, variant: bool = False):
+        """A zero-initialised, reusable workspace tensor for (M, N) (cached per size); variant:
+        for the quantization variants' GEMMs."""
         import torch
-        nbytes = self.workspace_bytes(M, N)
+        nbytes = (int(self._lib.fmpq_variant_gemm_workspace_bytes(self._h, M, N)) if variant
+                  else self.workspace_bytes(M, N))
         if nbytes == 0:
             return None
         ws = self._workspaces.get(nbytes)
@@ -331,3 +342,106 @@ def fmpq_outlier_gemm_fp16(X, cols, W_out, Y, X_out=None, stream=None):
         _ptr(X), X.stride(0), M, _ptr(cols), n_out, _ptr(W_out), W_out.stride(0), N, _ptr(X_out), _ptr(Y),
         Y.stride(0), _stream(stream)))
     return Y
+
+
+# ---- quantization variants: QUIK asymmetric activations, QoQ progressive group quantization
+
+def _gemm_ws(layout: Layout, M: int, N: int, workspace):
+    if workspace is None:
+        workspace = layout.workspace(M, N, variant=True)
+    return workspace, (workspace.numel() if workspace is not None else 0)
+
+
+def fmpq_quantize_asym(layout: Layout, X, A_packed=None, a_scales=None, a_zeros=None, stream=None):
+    """Asymmetric 4-bit activations. Returns (A_packed u8, a_scales fp16 [nb, M], a_zeros fp16 [nb, M])."""
+    import torch
+    M = X.shape[0]
+    if A_packed is None:
+        A_packed = torch.empty(layout.packed_a_bytes(M), dtype=torch.uint8, device=X.device)
+    if a_scales is None:
+        a_scales = torch.empty((layout.nb, M), dtype=torch.float16, device=X.device)
+    if a_zeros is None:
+        a_zeros = torch.empty((layout.nb, M), dtype=torch.float16, device=X.device)
+    _check("fmpq_quantize_asym", layout._lib.fmpq_quantize_asym(layout.handle, _ptr(X), X.stride(0), M, _ptr(A_packed),
+                                                                  _ptr(a_scales), _ptr(a_zeros), _stream(stream)))
+    return A_packed, a_scales, a_zeros
+
+
+def w4_weight_sums(layout: Layout, W_packed, w_scales, N: int, out=None, stream=None):
+    """w_sums fp32 [nb, N] = w_scales * (sum of each block's weight codes)."""
+    import torch
+    if out is None:
+        out = torch.empty((layout.nb, N), dtype=torch.float32, device=W_packed.device)
+    _check("w4_weight_sums", layout._lib.w4_weight_sums(layout.handle, _ptr(W_packed), _ptr(w_scales), N, _ptr(out),
+                                                          _stream(stream)))
+    return out
+
+
+def w4ax_gemm_asym(layout: Layout, A_packed, a_scales, a_zeros, W_packed, w_scales, w_sums, M: int, N: int,
+                   Y=None, workspace=None, stream=None):
+    import torch
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float16, device=A_packed.device)
+    workspace, ws_bytes = _gemm_ws(layout, M, N, workspace)
+    _check("w4ax_gemm_asym", layout._lib.w4ax_gemm_asym(
+        layout.handle, _ptr(A_packed), _ptr(a_scales), _ptr(a_zeros), _ptr(W_packed), _ptr(w_scales), _ptr(w_sums),
+        M, N, _ptr(Y), Y.stride(0), _ptr(workspace), ws_bytes, _stream(stream)))
+    return Y
+
+
+def qoq_pack_weights(layout: Layout, W, W_packed=None, stream=None):
+    """Returns (W_packed u8, ch_scales fp16 [N], grp_scales u8 [nb, N], grp_zeros u8 [nb, N])."""
+    import torch
+    N = W.shape[0]
+    if W_packed is None:
+        W_packed = torch.empty(layout.packed_w_bytes(N), dtype=torch.uint8, device=W.device)
+    s1 = torch.empty(N, dtype=torch.float16, device=W.device)
+    s2 = torch.empty((layout.nb, N), dtype=torch.uint8, device=W.device)
+    z2 = torch.empty((layout.nb, N), dtype=torch.uint8, device=W.device)
+    _check("qoq_pack_weights", layout._lib.qoq_pack_weights(layout.handle, _ptr(W), W.stride(0), N, _ptr(W_packed),
+                                                              _ptr(s1), _ptr(s2), _ptr(z2), _stream(stream)))
+    return W_packed, s1, s2, z2
+
+
+def qoq_unpack_weights(layout: Layout, W_packed, N: int, stream=None):
+    import torch
+    q4 = torch.empty((N, layout.K), dtype=torch.uint8, device=W_packed.device)
+    _check("qoq_unpack_weights", layout._lib.qoq_unpack_weights(layout.handle, _ptr(W_packed), N, _ptr(q4),
+                                                                  _stream(stream)))
+    return q4
+
+
+def qoq_quantize(layout: Layout, X, A_packed=None, a_scales=None, a_sums=None, stream=None):
+    """Per-token INT8 activations. Returns (A_packed u8, a_scales fp16 [M], a_sums int32 [nb, M])."""
+    import torch
+    M = X.shape[0]
+    if A_packed is None:
+        A_packed = torch.empty(layout.packed_a_bytes(M), dtype=torch.uint8, device=X.device)
+    if a_scales is None:
+        a_scales = torch.empty(M, dtype=torch.float16, device=X.device)
+    if a_sums is None:
+        a_sums = torch.empty((layout.nb, M), dtype=torch.int32, device=X.device)
+    _check("qoq_quantize", layout._lib.qoq_quantize(layout.handle, _ptr(X), X.stride(0), M, _ptr(A_packed),
+                                                      _ptr(a_scales), _ptr(a_sums), _stream(stream)))
+    return A_packed, a_scales, a_sums
+
+
+def qoq_gemm(layout: Layout, A_packed, a_scales, a_sums, W_packed, ch_scales, grp_scales, grp_zeros, M: int,
+             N: int, Y=None, workspace=None, stream=None):
+    import torch
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float16, device=A_packed.device)
+    workspace, ws_bytes = _gemm_ws(layout, M, N, workspace)
+    _check("qoq_gemm", layout._lib.qoq_gemm(
+        layout.handle, _ptr(A_packed), _ptr(a_scales), _ptr(a_sums), _ptr(W_packed), _ptr(ch_scales),
+        _ptr(grp_scales), _ptr(grp_zeros), M, N, _ptr(Y), Y.stride(0), _ptr(workspace), ws_bytes, _stream(stream)))
+    return Y
+
+
+def qoq_gemm_partials(layout: Layout, A_packed, W_packed, M: int, N: int, m0: int, mcount: int, n0: int,
+                      ncount: int, stream=None):
+    import torch
+    P = torch.zeros((mcount, ncount, layout.nb), dtype=torch.int32, device=A_packed.device)
+    _check("qoq_gemm_partials", layout._lib.qoq_gemm_partials(layout.handle, _ptr(A_packed), _ptr(W_packed), M, N,
+                                                                m0, mcount, n0, ncount, _ptr(P), _stream(stream)))
+    return P

@@ -239,6 +239,84 @@ FMPQ_API fmpq_status fmpq_plan_layout(int32_t K, const uint32_t* absmax_host, in
  * outside [0, 1]. */
 FMPQ_API int32_t fmpq_outlier_blocks(int32_t K, double fraction);
 
+/* ---- Quantization variants the pages describe beside FMPQ ----
+ * Both run on the same layouts, packed formats and 2-SM GEMM kernel (for every M), with one
+ * more term per block in the epilogue. Their workspace (same rules as w4ax_gemm's): */
+FMPQ_API size_t fmpq_variant_gemm_workspace_bytes(const fmpq_layout* layout, int64_t M, int64_t N);
+
+/* QUIK asymmetric activations (QUIK explainer, "反量化背后的数学": activations take a scale and a
+ * zero point, weights a scale only; the zero point's term z * sum(w) needs only the weights'
+ * sum, computed offline). The layout must have no INT8 block (FMPQ_ERR_INVALID_ARG): QUIK keeps
+ * its outliers in FP16 (fmpq_outlier_gemm_fp16). Per token m and block b:
+ *   z = the block's smallest input (value order, -0 below +0)   -> a_zeros[b][m] (fp16 bits)
+ *   s = fp16_rn( fp32( fp32(max) - fp32(z) ) / 15 )              -> a_scales[b][m]
+ *   q = clamp( rne( fp32( fp32(x) - fp32(z) ) / fp32(s) ), 0, 15 ), q = 0 when s == 0
+ * (IEEE fp32 subtraction and division, round half to even), so x ~ s * q + z. A_packed has the
+ * fmpq_quantize format with the sign bits clear (byte = E4M3 of q * 2^-9).
+ *   a_scales, a_zeros  fp16 [K/128][M], 16-byte aligned. Other arguments as fmpq_quantize. */
+FMPQ_API fmpq_status fmpq_quantize_asym(const fmpq_layout* layout, const void* X, int64_t ldx, int64_t M,
+                                        void* A_packed, void* a_scales, void* a_zeros, void* stream);
+
+/* Offline weight sums of the zero-point term: w_sums[b][n] = w_scales[b][n] * (sum of the
+ * block's codes of output channel n) in fp32 (exact), from w4_pack_weights' outputs.
+ *   w_sums  fp32 [K/128][N] (device, caller-owned), 16-byte aligned. */
+FMPQ_API fmpq_status w4_weight_sums(const fmpq_layout* layout, const void* W_packed, const void* w_scales,
+                                    int64_t N, float* w_sums, void* stream);
+
+/* The GEMM on asymmetric activations:
+ *   Y[m][n] = fp16_rn( sum_b ( a_scales[b][m] * w_scales[b][n] * P[m][n][b]
+ *                              + a_zeros[b][m] * w_sums[b][n] ) ),   FP32 accumulation,
+ * P the exact integer sums of the unsigned activation codes times the weight codes. Shapes,
+ * alignment, workspace (fmpq_variant_gemm_workspace_bytes) as w4ax_gemm. */
+FMPQ_API fmpq_status w4ax_gemm_asym(const fmpq_layout* layout, const void* A_packed, const void* a_scales,
+                                    const void* a_zeros, const void* W_packed, const void* w_scales,
+                                    const float* w_sums, int64_t M, int64_t N, void* Y, int64_t ldy,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* QoQ progressive group quantization with W4A8 GEMMs (QServe explainer, "渐进式分组量化" and
+ * "运行时设计"). The layout must have every block INT8 (FMPQ_ERR_INVALID_ARG) and K_in == K.
+ *
+ * Offline weights: per output channel n, then per group g (the layout's 128-channel blocks):
+ *   s1[n] = fp16_rn( fp32(absmax of W[n][0..K)) / 119 )           (protective range [-119, 119])
+ *   q8    = clamp( rne( fp32(w) / fp32(s1) ), -119, 119 )          (IEEE division; 0 if s1 == 0)
+ *   [mn, mx] = the range of the group's q8 extended to include 0
+ *   s2 = max(1, ceil((mx - mn) / 15)), z2 = clamp(rne(-mn / s2), 0, 15)   (integers)
+ *   q4 = clamp( rne(q8 / s2) + z2, 0, 15 )                          (exact rationals, ties to even)
+ * The dequantized (q4 - z2) * s2 stays in [-127, 127].
+ *   W_packed    fmpq_packed_w_bytes(layout, N): unsigned 4-bit codes (permuted order).
+ *   ch_scales   fp16 [N] (s1); grp_scales, grp_zeros uint8 [K/128][N] (s2, z2). 16-byte aligned. */
+FMPQ_API fmpq_status qoq_pack_weights(const fmpq_layout* layout, const void* W, int64_t ldw, int64_t N,
+                                      void* W_packed, void* ch_scales, uint8_t* grp_scales, uint8_t* grp_zeros,
+                                      void* stream);
+
+/* Debug/test: decode qoq_pack_weights' codes to q4 uint8 [N][K] (permuted order). */
+FMPQ_API fmpq_status qoq_unpack_weights(const fmpq_layout* layout, const void* W_packed, int64_t N, uint8_t* q4,
+                                        void* stream);
+
+/* Per-token INT8 activations: s[m] = fp16_rn( fp32(absmax of row m) / 127 ),
+ * q = clamp( rne(fp32(x) / fp32(s)), -127, 127 ), every block packed as an INT8 block of
+ * fmpq_quantize's format (A_packed: fmpq_packed_a_bytes); a_sums[b][m] = the sum of the
+ * block's codes (the term the group zero point multiplies).
+ *   a_scales  fp16 [M]; a_sums int32 [K/128][M]. 16-byte aligned. */
+FMPQ_API fmpq_status qoq_quantize(const fmpq_layout* layout, const void* X, int64_t ldx, int64_t M,
+                                  void* A_packed, void* a_scales, int32_t* a_sums, void* stream);
+
+/* The W4A8 GEMM, the group zero point subtracted after the multiplication (QServe explainer,
+ * "W4A8逐组快速反量化"):
+ *   Y[m][n] = fp16_rn( a_scales[m] * ch_scales[n] *
+ *                      sum_b grp_scales[b][n] * ( P[m][n][b] - grp_zeros[b][n] * a_sums[b][m] ) ),
+ * P the exact integer sums of the INT8 activation codes times the unsigned codes q4, FP32
+ * accumulation. Shapes, alignment, workspace (fmpq_variant_gemm_workspace_bytes) as w4ax_gemm. */
+FMPQ_API fmpq_status qoq_gemm(const fmpq_layout* layout, const void* A_packed, const void* a_scales,
+                              const int32_t* a_sums, const void* W_packed, const void* ch_scales,
+                              const uint8_t* grp_scales, const uint8_t* grp_zeros, int64_t M, int64_t N, void* Y,
+                              int64_t ldy, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Debug/test: P of qoq_gemm (INT8 codes times q4), as w4ax_gemm_partials. */
+FMPQ_API fmpq_status qoq_gemm_partials(const fmpq_layout* layout, const void* A_packed, const void* W_packed,
+                                       int64_t M, int64_t N, int64_t m0, int64_t mcount, int64_t n0,
+                                       int64_t ncount, int32_t* P, void* stream);
+
 /* Read (and, if clear != 0, reset) the layout's device status word. Synchronizes the
  * device. *code = FMPQ_OK or the first error a kernel recorded (e.g. FMPQ_ERR_TIMEOUT). */
 FMPQ_API fmpq_status fmpq_device_status(const fmpq_layout* layout, int32_t* code, int32_t clear);

@@ -203,3 +203,127 @@ def test_qoq_epilogue_closed_form(oracle_mod):
     # the INT8 intermediate is reproduced by the group codes within s2 / 2 except where clipped
     deq8 = (r["q4"].astype(np.int64) - r["z2"][blk, :].T) * r["s2"][blk, :].T
     assert np.all(np.abs(deq8 - r["q8"]) <= r["s2"][blk, :].T)
+
+
+# ---------------------------------------------------------------------- GPU parity
+
+@pytest.fixture(scope="module")
+def fmpq_gpu():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_quantized_gemm_fmpq_gb300 import build, fmpq
+    build.build()
+    fmpq.load_library()
+    return fmpq
+
+
+def _inputs(M, N, K, seed, offset=0.0, pad=0):
+    """Seeded activations (normal, 10% outlier channels x U(20, 100), optional offset) with a
+    row stride of K + pad, and weights; row 0 holds the asymmetric worked example's block."""
+    from bit_quantized_gemm_fmpq_gb300 import workloads as wl
+    w = wl.synthetic(M, N, K, n8=0, seed=seed, outlier_frac=0.0)
+    rng = np.random.default_rng(seed + 7)
+    X = w.X.astype(np.float32) + offset
+    X[:, rng.choice(K, size=max(1, K // 10), replace=False)] *= rng.uniform(20, 100)
+    X = X.astype(np.float16)
+    ex = np.zeros(BLOCK, dtype=np.float16)
+    ex[:7] = [-1.0, 14.0, 0.5, 1.5, 2.5, -0.5, 3.25]      # exact ties of (x - z) / s
+    X[0, w.perm[:BLOCK]] = ex
+    big = np.zeros((M, K + pad), dtype=np.float16)
+    big[:, :K] = X
+    return X, big, w.W, w.perm
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("M,N,K,offset,pad", [(1, 256, 128, 0.0, 0), (37, 512, 1024, 0.0, 8),
+                                              (300, 768, 4096, 2.0, 0), (1024, 1024, 8192, 0.0, 16)])
+def test_asym_matches_oracle(fmpq_gpu, oracle_mod, M, N, K, offset, pad):
+    from tests.gpu_helpers import Y_TOL, to_dev, y_error
+    X, big, W, perm = _inputs(M, N, K, seed=M + K, offset=offset, pad=pad)
+    layout = fmpq_gpu.Layout(K, perm, np.zeros(K // BLOCK, np.uint8))
+    Xd = to_dev(big)[:, :K]
+    A, sx, z = fmpq_gpu.fmpq_quantize_asym(layout, Xd)
+    Wp, sw = fmpq_gpu.w4_pack_weights(layout, to_dev(W))
+    wsum = fmpq_gpu.w4_weight_sums(layout, Wp, sw, N)
+    Y = fmpq_gpu.w4ax_gemm_asym(layout, A, sx, z, Wp, sw, wsum, M, N)
+    mc, nc = min(M, 48), min(N, 64)
+    m0, n0 = M - mc, N - nc
+    P = fmpq_gpu.w4ax_gemm_partials(layout, A, Wp, M, N, m0, mc, n0, nc)
+    ref = oracle_mod.asym_reference(X, W, perm)
+    assert np.array_equal(sx.cpu().numpy().view(np.uint16), ref["a_scales"]), "scales differ"
+    assert np.array_equal(z.cpu().numpy().view(np.uint16), ref["a_zeros"]), "zero points differ"
+    assert np.array_equal(A.cpu().numpy(), ref["A_packed"]), "codes differ"
+    assert np.array_equal(wsum.cpu().numpy(), ref["wsum"]), "weight sums differ"
+    assert np.array_equal(P.cpu().numpy(), ref["P"][m0:, n0:]), "partial sums differ"
+    err = y_error(Y.cpu().numpy(), ref["Y"])
+    assert err <= Y_TOL, err
+    assert fmpq_gpu.fmpq_device_status(layout) == 0
+    layout.close()
+
+
+@pytest.mark.gpu
+def test_asym_select_layout(fmpq_gpu, oracle_mod):
+    """QUIK's base part: 896 channels selected from rows of 1024 (the outliers left to FP16)."""
+    from tests.gpu_helpers import Y_TOL, to_dev, y_error
+    M, N, K_in, K = 64, 256, 1024, 896
+    X, _, W, _ = _inputs(M, N, K_in, seed=3)
+    rng = np.random.default_rng(4)
+    base = np.sort(rng.choice(K_in, size=K, replace=False)).astype(np.int32)
+    layout = fmpq_gpu.select_layout(K, K_in, base, np.zeros(K // BLOCK, np.uint8))
+    A, sx, z = fmpq_gpu.fmpq_quantize_asym(layout, to_dev(X))
+    Wp, sw = fmpq_gpu.w4_pack_weights(layout, to_dev(W))
+    wsum = fmpq_gpu.w4_weight_sums(layout, Wp, sw, N)
+    Y = fmpq_gpu.w4ax_gemm_asym(layout, A, sx, z, Wp, sw, wsum, M, N)
+    ref = oracle_mod.asym_reference(X[:, base], W[:, base], np.arange(K, dtype=np.int32))
+    assert np.array_equal(A.cpu().numpy(), ref["A_packed"])
+    assert np.array_equal(z.cpu().numpy().view(np.uint16), ref["a_zeros"])
+    assert y_error(Y.cpu().numpy(), ref["Y"]) <= Y_TOL
+    layout.close()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("M,N,K,pad", [(1, 256, 128, 0), (45, 512, 1024, 8), (300, 768, 4096, 0),
+                                       (1024, 1024, 8192, 16)])
+def test_qoq_matches_oracle(fmpq_gpu, oracle_mod, M, N, K, pad):
+    from tests.gpu_helpers import Y_TOL, to_dev, y_error
+    X, big, W, perm = _inputs(M, N, K, seed=2 * M + K, pad=pad)
+    Wb = (W.astype(np.float32) + np.float32(0.01)).astype(np.float16)   # groups off-centre: non-trivial zero points
+    layout = fmpq_gpu.Layout(K, perm, np.ones(K // BLOCK, np.uint8))
+    A, sx, sums = fmpq_gpu.qoq_quantize(layout, to_dev(big)[:, :K])
+    Wp, s1, s2, z2 = fmpq_gpu.qoq_pack_weights(layout, to_dev(Wb))
+    q4 = fmpq_gpu.qoq_unpack_weights(layout, Wp, N)
+    Y = fmpq_gpu.qoq_gemm(layout, A, sx, sums, Wp, s1, s2, z2, M, N)
+    mc, nc = min(M, 40), min(N, 72)
+    P = fmpq_gpu.qoq_gemm_partials(layout, A, Wp, M, N, 0, mc, 0, nc)
+    ref = oracle_mod.qoq_reference(X, Wb, perm)
+    assert np.array_equal(s1.cpu().numpy().view(np.uint16), ref["s1"]), "channel scales differ"
+    assert np.array_equal(s2.cpu().numpy(), ref["s2"]), "group scales differ"
+    assert np.array_equal(z2.cpu().numpy(), ref["z2"]), "group zero points differ"
+    assert np.array_equal(q4.cpu().numpy(), ref["q4"]), "weight codes differ"
+    assert np.array_equal(sx.cpu().numpy().view(np.uint16), ref["a_scales"]), "token scales differ"
+    assert np.array_equal(sums.cpu().numpy(), ref["a_sums"]), "code sums differ"
+    assert np.array_equal(A.cpu().numpy(), ref["A_packed"]), "activation codes differ"
+    assert np.array_equal(P.cpu().numpy(), ref["P"][:mc, :nc]), "partial sums differ"
+    err = y_error(Y.cpu().numpy(), ref["Y"])
+    assert err <= Y_TOL, err
+    assert fmpq_gpu.fmpq_device_status(layout) == 0
+    layout.close()
+
+
+@pytest.mark.gpu
+def test_variant_argument_errors(fmpq_gpu):
+    """Layouts that do not fit the variant are refused before any launch."""
+    from tests.gpu_helpers import to_dev
+    K, M, N = 256, 8, 256
+    X = to_dev(np.zeros((M, K), np.float16))
+    mixed = fmpq_gpu.Layout(K, np.arange(K, dtype=np.int32), np.array([0, 1], np.uint8))
+    with pytest.raises(fmpq_gpu.FmpqError):
+        fmpq_gpu.fmpq_quantize_asym(mixed, X)             # an INT8 block in an asymmetric layout
+    with pytest.raises(fmpq_gpu.FmpqError):
+        fmpq_gpu.qoq_quantize(mixed, X)                   # QoQ needs every block INT8
+    sel = fmpq_gpu.select_layout(128, 256, np.arange(128, dtype=np.int32), np.ones(1, np.uint8))
+    with pytest.raises(fmpq_gpu.FmpqError):
+        fmpq_gpu.qoq_quantize(sel, X)                     # per-token scale over the whole row only
+    mixed.close()
+    sel.close()
