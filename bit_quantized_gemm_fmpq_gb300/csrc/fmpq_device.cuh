@@ -251,6 +251,21 @@ __device__ __forceinline__ void tmem_ld16x256b_x4(uint32_t taddr, uint32_t (&r)[
         : "r"(taddr));
 }
 
+// tcgen05.ld 16x256b, 2 repetitions: 16 TMEM lanes x 16 columns, registers as in the x4 form
+// (repetition i in registers 4i..4i+3). Written asynchronously: read only after tmem_ld_wait8.
+__device__ __forceinline__ void tmem_ld16x256b_x2(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait8(uint32_t (&r)[8]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
+                 :
+                 : "memory");
+}
+
 // Wait for every tcgen05.ld of this thread; the array is passed through so that no read of
 // it can be scheduled before the wait.
 __device__ __forceinline__ void tmem_ld_wait16(uint32_t (&r)[16]) {

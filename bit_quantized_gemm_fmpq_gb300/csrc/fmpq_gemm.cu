@@ -469,55 +469,25 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, uint32_t
                     const float2 sxa = make_float2(xa, xa);
                     const float2 sxb = make_float2(xb, xb);
                     const float4* swv = reinterpret_cast<const float4*>(sl.sw + tq * kSwStride);
-                    if constexpr (!kZero) {
-                        // 8 chunks of 32 columns; the TMEM load of chunk c+1 overlaps the math of c
-                        uint32_t d0[16], d1[16];
-                        dev::tmem_ld16x256b_x4(taddr, d0);
+                    // 8 chunks of 32 columns; the TMEM load of chunk c+1 overlaps the math of c
+                    uint32_t d0[16], d1[16];
+                    dev::tmem_ld16x256b_x4(taddr, d0);
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const float4 f0 = swv[2 * c], f1 = swv[2 * c + 1];   // column pairs g = 4c..4c+3
-                            uint32_t (&dc)[16] = (c & 1) ? d1 : d0;
-                            uint32_t (&dn)[16] = (c & 1) ? d0 : d1;
-                            dev::tmem_ld_wait16(dc);
-                            if (c < 7) dev::tmem_ld16x256b_x4(taddr + (c + 1) * 32, dn);
-                            const float2 swp[4] = {make_float2(f0.x, f0.y), make_float2(f0.z, f0.w),
-                                                   make_float2(f1.x, f1.y), make_float2(f1.z, f1.w)};
+                    for (int c = 0; c < 8; ++c) {
+                        const float4 f0 = swv[2 * c], f1 = swv[2 * c + 1];   // column pairs g = 4c..4c+3
+                        uint32_t (&dc)[16] = (c & 1) ? d1 : d0;
+                        uint32_t (&dn)[16] = (c & 1) ? d0 : d1;
+                        dev::tmem_ld_wait16(dc);
+                        if (c < 7) dev::tmem_ld16x256b_x4(taddr + (c + 1) * 32, dn);
+                        const float2 swp[4] = {make_float2(f0.x, f0.y), make_float2(f0.z, f0.w),
+                                               make_float2(f1.x, f1.y), make_float2(f1.z, f1.w)};
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const int g = 4 * c + i;
-                                const float2 ca = dev::fmul2(swp[i], sxa);
-                                const float2 cb = dev::fmul2(swp[i], sxb);
-                                accA[g] = dev::ffma2(make_float2(__uint_as_float(dc[4 * i]), __uint_as_float(dc[4 * i + 1])), ca, accA[g]);
-                                accB[g] = dev::ffma2(make_float2(__uint_as_float(dc[4 * i + 2]), __uint_as_float(dc[4 * i + 3])), cb, accB[g]);
-                            }
-                        }
-                    } else {
-                        // zero-point variants: the block's term x_zero[m] * w_zero[n] is added too;
-                        // single-buffered loads leave the second buffer's registers to its factors
-                        const float4* wzv = reinterpret_cast<const float4*>(sl.wz + tq * kSwStride);
-                        const float2 xza = make_float2(sl.xz[lr0], sl.xz[lr0]);
-                        const float2 xzb = make_float2(sl.xz[lr1], sl.xz[lr1]);
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            uint32_t dc[16];
-                            dev::tmem_ld16x256b_x4(taddr + c * 32, dc);
-                            dev::tmem_ld_wait16(dc);
-                            const float4 f0 = swv[2 * c], f1 = swv[2 * c + 1];
-                            const float4 z0 = wzv[2 * c], z1 = wzv[2 * c + 1];
-                            const float2 swp[4] = {make_float2(f0.x, f0.y), make_float2(f0.z, f0.w),
-                                                   make_float2(f1.x, f1.y), make_float2(f1.z, f1.w)};
-                            const float2 wzp[4] = {make_float2(z0.x, z0.y), make_float2(z0.z, z0.w),
-                                                   make_float2(z1.x, z1.y), make_float2(z1.z, z1.w)};
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const int g = 4 * c + i;
-                                const float2 ca = dev::fmul2(swp[i], sxa);
-                                const float2 cb = dev::fmul2(swp[i], sxb);
-                                accA[g] = dev::ffma2(make_float2(__uint_as_float(dc[4 * i]), __uint_as_float(dc[4 * i + 1])), ca, accA[g]);
-                                accB[g] = dev::ffma2(make_float2(__uint_as_float(dc[4 * i + 2]), __uint_as_float(dc[4 * i + 3])), cb, accB[g]);
-                                accA[g] = dev::ffma2(xza, wzp[i], accA[g]);
-                                accB[g] = dev::ffma2(xzb, wzp[i], accB[g]);
-                            }
+                        for (int i = 0; i < 4; ++i) {
+                            const int g = 4 * c + i;
+                            const float2 ca = dev::fmul2(swp[i], sxa);
+                            const float2 cb = dev::fmul2(swp[i], sxb);
+                            accA[g] = dev::ffma2(make_float2(__uint_as_float(dc[4 * i]), __uint_as_float(dc[4 * i + 1])), ca, accA[g]);
+                            accB[g] = dev::ffma2(make_float2(__uint_as_float(dc[4 * i + 2]), __uint_as_float(dc[4 * i + 3])), cb, accB[g]);
                         }
                     }
                 } else {
@@ -542,9 +512,31 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, uint32_t
                 dev::tc_fence_before();
             }
             __syncwarp();
-            if (lane == 0 && ok) {
-                dev::mbar_arrive_remote(release);
-                dev::mbar_arrive(&s.sc_empty[ss]);
+            if constexpr (kZero && !kPartials) {
+                // the accumulator is read: release it first; then the block's zero-point term
+                // x_zero[m] * w_zero[n], a second pass over the registers, from the scale slot
+                if (lane == 0 && ok) dev::mbar_arrive_remote(release);
+                if (ok) {
+                    const ScaleSlot& slz = s.sc[ss];
+                    const float4* wzv = reinterpret_cast<const float4*>(slz.wz + tq * kSwStride);
+                    const float2 xza = make_float2(slz.xz[lr0], slz.xz[lr0]);
+                    const float2 xzb = make_float2(slz.xz[lr1], slz.xz[lr1]);
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const float4 z = wzv[c];   // column pairs g = 2c, 2c + 1
+                        accA[2 * c] = dev::ffma2(xza, make_float2(z.x, z.y), accA[2 * c]);
+                        accB[2 * c] = dev::ffma2(xzb, make_float2(z.x, z.y), accB[2 * c]);
+                        accA[2 * c + 1] = dev::ffma2(xza, make_float2(z.z, z.w), accA[2 * c + 1]);
+                        accB[2 * c + 1] = dev::ffma2(xzb, make_float2(z.z, z.w), accB[2 * c + 1]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0 && ok) dev::mbar_arrive(&s.sc_empty[ss]);
+            } else {
+                if (lane == 0 && ok) {
+                    dev::mbar_arrive_remote(release);
+                    dev::mbar_arrive(&s.sc_empty[ss]);
+                }
             }
         }
         if constexpr (!kPartials) {
