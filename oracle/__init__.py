@@ -86,6 +86,8 @@ def _load():
             lib.oracle_qoq_quantize_activations.argtypes = [P, i64, i32, i32, P, P, P, P, P]
             lib.oracle_qoq_quantize_activations.restype = i32
             lib.oracle_epilogue_qoq_f64.argtypes = [P, P, P, P, P, P, i32, i32, i32, P]
+            lib.oracle_gemm_sample_asym.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, P, P, P, P]
+            lib.oracle_gemm_sample_qoq.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, P, P, P, P]
             _lib = lib
     return _lib
 
@@ -405,3 +407,31 @@ def qoq_reference(X, W, perm):
     P = partials_u4(Aq, w["q4"])
     Y = epilogue_qoq(P, sx, sums, w["s1"], w["s2"], w["z2"])
     return dict(A_packed=A, a_scales=sx, a_sums=sums, Aq=Aq, P=P, Y=Y, **w)
+
+
+def gemm_sample_asym(Aq, Wq, a_scales, a_zeros, w_scales, wsum, ms, ns):
+    """QUIK asymmetric GEMM at sampled positions: (P [S, nb], Y [S])."""
+    Aq, Wq = _c(Aq, np.int8), _c(Wq, np.int8)
+    M, K = Aq.shape
+    N = Wq.shape[0]
+    ms, ns = _c(ms, np.int32), _c(ns, np.int32)
+    P = np.zeros((ms.size, K // BLOCK), dtype=np.int32)
+    Y = np.zeros(ms.size, dtype=np.float64)
+    _load().oracle_gemm_sample_asym(_ptr(Aq), _ptr(Wq), _ptr(_c(a_scales, np.uint16)), _ptr(_c(a_zeros, np.uint16)),
+                                    _ptr(_c(w_scales, np.uint16)), _ptr(_c(wsum, np.float32)), M, N, K, ms.size,
+                                    _ptr(ms), _ptr(ns), _ptr(P), _ptr(Y))
+    return P, Y
+
+
+def gemm_sample_qoq(Aq, q4, a_scales, a_sums, s1, s2, z2, ms, ns):
+    """QoQ W4A8 GEMM at sampled positions: (P [S, nb], Y [S])."""
+    Aq, q4 = _c(Aq, np.int8), _c(q4, np.uint8)
+    M, K = Aq.shape
+    N = q4.shape[0]
+    ms, ns = _c(ms, np.int32), _c(ns, np.int32)
+    P = np.zeros((ms.size, K // BLOCK), dtype=np.int32)
+    Y = np.zeros(ms.size, dtype=np.float64)
+    _load().oracle_gemm_sample_qoq(_ptr(Aq), _ptr(q4), _ptr(_c(a_scales, np.uint16)), _ptr(_c(a_sums, np.int32)),
+                                   _ptr(_c(s1, np.uint16)), _ptr(_c(s2, np.uint8)), _ptr(_c(z2, np.uint8)), M, N, K,
+                                   ms.size, _ptr(ms), _ptr(ns), _ptr(P), _ptr(Y))
+    return P, Y

@@ -778,3 +778,47 @@ void oracle_epilogue_qoq_f64(const int32_t* P, const uint16_t* a_scales, const i
             Y[(int64_t)m * N + n] = (double)oracle_f16_to_f32(a_scales[m]) * (double)oracle_f16_to_f32(s1[n]) * acc;
         }
 }
+
+/* Sampled outputs of the two variants for large shapes, (ms[s], ns[s]) positions: exact partial
+ * sums P[s][b] and Y[s] by the variant's formula above (fp64, block order). */
+void oracle_gemm_sample_asym(const int8_t* Aq, const int8_t* Wq, const uint16_t* a_scales, const uint16_t* a_zeros,
+                             const uint16_t* w_scales, const float* wsum, int M, int N, int K, int S,
+                             const int32_t* ms, const int32_t* ns, int32_t* P, double* Y) {
+    const int nb = K / ORACLE_BLOCK;
+#pragma omp parallel for schedule(static)
+    for (int s = 0; s < S; ++s) {
+        const int m = ms[s], n = ns[s];
+        double acc = 0.0;
+        for (int b = 0; b < nb; ++b) {
+            int64_t p = 0;
+            for (int j = b * ORACLE_BLOCK; j < (b + 1) * ORACLE_BLOCK; ++j)
+                p += (int64_t)Aq[(int64_t)m * K + j] * (int64_t)Wq[(int64_t)n * K + j];
+            if (P) P[(int64_t)s * nb + b] = (int32_t)p;
+            const double sx = oracle_f16_to_f32(a_scales[(int64_t)b * M + m]);
+            const double z = oracle_f16_to_f32(a_zeros[(int64_t)b * M + m]);
+            const double sw = oracle_f16_to_f32(w_scales[(int64_t)b * N + n]);
+            acc += sx * sw * (double)p + z * (double)wsum[(int64_t)b * N + n];
+        }
+        Y[s] = acc;
+    }
+}
+
+void oracle_gemm_sample_qoq(const int8_t* Aq, const uint8_t* q4, const uint16_t* a_scales, const int32_t* a_sums,
+                            const uint16_t* s1, const uint8_t* s2, const uint8_t* z2, int M, int N, int K, int S,
+                            const int32_t* ms, const int32_t* ns, int32_t* P, double* Y) {
+    const int nb = K / ORACLE_BLOCK;
+#pragma omp parallel for schedule(static)
+    for (int s = 0; s < S; ++s) {
+        const int m = ms[s], n = ns[s];
+        double acc = 0.0;
+        for (int b = 0; b < nb; ++b) {
+            int64_t p = 0;
+            for (int j = b * ORACLE_BLOCK; j < (b + 1) * ORACLE_BLOCK; ++j)
+                p += (int64_t)Aq[(int64_t)m * K + j] * (int64_t)q4[(int64_t)n * K + j];
+            if (P) P[(int64_t)s * nb + b] = (int32_t)p;
+            const int64_t g = (int64_t)b * N + n;
+            acc += (double)s2[g] * (double)(p - (int64_t)z2[g] * a_sums[(int64_t)b * M + m]);
+        }
+        Y[s] = (double)oracle_f16_to_f32(a_scales[m]) * (double)oracle_f16_to_f32(s1[n]) * acc;
+    }
+}

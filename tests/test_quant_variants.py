@@ -327,3 +327,101 @@ def test_variant_argument_errors(fmpq_gpu):
         fmpq_gpu.qoq_quantize(sel, X)                     # per-token scale over the whole row only
     mixed.close()
     sel.close()
+
+
+def test_variant_samples_agree_with_whole_reference(oracle_mod):
+    """The sampled forms used at full size give the whole-matrix references' values."""
+    rng = np.random.default_rng(21)
+    M, N, K = 7, 11, 384
+    X = (rng.standard_normal((M, K)) + 0.5).astype(np.float16)
+    W = (rng.standard_normal((N, K)) * 0.03 + 0.005).astype(np.float16)
+    perm = rng.permutation(K).astype(np.int32)
+    ms, ns = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    r = oracle_mod.asym_reference(X, W, perm)
+    P, Y = oracle_mod.gemm_sample_asym(r["Aq"], r["Wq"], r["a_scales"], r["a_zeros"], r["w_scales"], r["wsum"],
+                                       ms.ravel(), ns.ravel())
+    assert np.array_equal(P.reshape(M, N, -1), r["P"]) and np.array_equal(Y.reshape(M, N), r["Y"])
+    q = oracle_mod.qoq_reference(X, W, perm)
+    P, Y = oracle_mod.gemm_sample_qoq(q["Aq"], q["q4"], q["a_scales"], q["a_sums"], q["s1"], q["s2"], q["z2"],
+                                      ms.ravel(), ns.ravel())
+    assert np.array_equal(P.reshape(M, N, -1), q["P"]) and np.array_equal(Y.reshape(M, N), q["Y"])
+
+
+def _sampled_y_error(Yg, Ys):
+    floor = 1e-2 * np.sqrt(np.mean(Ys ** 2))
+    return float(np.max(np.abs(Yg - Ys) / np.maximum(np.abs(Ys), floor)))
+
+
+@pytest.mark.gpu
+def test_asym_full_size(fmpq_gpu, oracle_mod):
+    """The benchmark's LLaMA-70B down-projection shape (4096 x 28672 -> 8192), every block 4-bit:
+    codes, scales, zero points and weight sums bit-exact, a window of partial sums, Y sampled."""
+    import torch
+    from bit_quantized_gemm_fmpq_gb300 import workloads as wl
+    from tests.gpu_helpers import Y_TOL, to_dev
+    w = wl.llama70b_down()
+    layout = fmpq_gpu.Layout(w.K, w.perm, np.zeros(w.K // BLOCK, np.uint8))
+    A, sx, z = fmpq_gpu.fmpq_quantize_asym(layout, to_dev(w.X))
+    Wp, sw = fmpq_gpu.w4_pack_weights(layout, to_dev(w.W))
+    wsum = fmpq_gpu.w4_weight_sums(layout, Wp, sw, w.N)
+    Y = fmpq_gpu.w4ax_gemm_asym(layout, A, sx, z, Wp, sw, wsum, w.M, w.N)
+    m0, mc, n0, nc = 4000, 96, 8000, 192
+    P = fmpq_gpu.w4ax_gemm_partials(layout, A, Wp, w.M, w.N, m0, mc, n0, nc).cpu().numpy()
+    A_ref, sx_ref, z_ref, Aq = oracle_mod.quantize_activations_asym(w.X, w.perm)
+    assert np.array_equal(A.cpu().numpy(), A_ref)
+    assert np.array_equal(sx.cpu().numpy().view(np.uint16), sx_ref)
+    assert np.array_equal(z.cpu().numpy().view(np.uint16), z_ref)
+    del A_ref
+    Wq, sw_ref = oracle_mod.quantize_weights(w.W, w.perm)
+    wsum_ref = oracle_mod.weight_sums(Wq, sw_ref)
+    assert np.array_equal(wsum.cpu().numpy(), wsum_ref)
+    ms, ns = np.meshgrid(np.arange(m0, m0 + mc), np.arange(n0, n0 + nc), indexing="ij")
+    Pw, _ = oracle_mod.gemm_sample_asym(Aq, Wq, sx_ref, z_ref, sw_ref, wsum_ref, ms.ravel(), ns.ravel())
+    assert np.array_equal(P.reshape(-1, w.K // BLOCK), Pw)
+    rng = np.random.default_rng(0)
+    sm = np.concatenate([rng.integers(0, w.M, 4096), [0, w.M - 1]]).astype(np.int32)
+    sn = np.concatenate([rng.integers(0, w.N, 4096), [0, w.N - 1]]).astype(np.int32)
+    _, Ys = oracle_mod.gemm_sample_asym(Aq, Wq, sx_ref, z_ref, sw_ref, wsum_ref, sm, sn)
+    err = _sampled_y_error(Y.cpu().numpy()[sm, sn].astype(np.float64), Ys)
+    assert err <= Y_TOL, err
+    assert fmpq_gpu.fmpq_device_status(layout) == 0
+    layout.close()
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.gpu
+def test_qoq_full_size(fmpq_gpu, oracle_mod):
+    """The same shape through QoQ: per-token INT8 codes and sums, progressive weights (s1, s2,
+    z2, codes) bit-exact, a window of partial sums, Y sampled."""
+    import torch
+    from bit_quantized_gemm_fmpq_gb300 import workloads as wl
+    from tests.gpu_helpers import Y_TOL, to_dev
+    w = wl.llama70b_down()
+    layout = fmpq_gpu.Layout(w.K, w.perm, np.ones(w.K // BLOCK, np.uint8))
+    A, sx, sums = fmpq_gpu.qoq_quantize(layout, to_dev(w.X))
+    Wp, s1, s2, z2 = fmpq_gpu.qoq_pack_weights(layout, to_dev(w.W))
+    Y = fmpq_gpu.qoq_gemm(layout, A, sx, sums, Wp, s1, s2, z2, w.M, w.N)
+    m0, mc, n0, nc = 0, 64, 8192 - 128, 128
+    P = fmpq_gpu.qoq_gemm_partials(layout, A, Wp, w.M, w.N, m0, mc, n0, nc).cpu().numpy()
+    q4 = fmpq_gpu.qoq_unpack_weights(layout, Wp, w.N).cpu().numpy()
+    A_ref, sx_ref, sums_ref, Aq = oracle_mod.qoq_quantize_activations(w.X, w.perm)
+    assert np.array_equal(A.cpu().numpy(), A_ref)
+    assert np.array_equal(sx.cpu().numpy().view(np.uint16), sx_ref)
+    assert np.array_equal(sums.cpu().numpy(), sums_ref)
+    del A_ref
+    r = oracle_mod.qoq_quantize_weights(w.W, w.perm)
+    assert np.array_equal(q4, r["q4"])
+    assert np.array_equal(s1.cpu().numpy().view(np.uint16), r["s1"])
+    assert np.array_equal(s2.cpu().numpy(), r["s2"]) and np.array_equal(z2.cpu().numpy(), r["z2"])
+    ms, ns = np.meshgrid(np.arange(m0, m0 + mc), np.arange(n0, n0 + nc), indexing="ij")
+    Pw, _ = oracle_mod.gemm_sample_qoq(Aq, r["q4"], sx_ref, sums_ref, r["s1"], r["s2"], r["z2"], ms.ravel(), ns.ravel())
+    assert np.array_equal(P.reshape(-1, w.K // BLOCK), Pw)
+    rng = np.random.default_rng(1)
+    sm = np.concatenate([rng.integers(0, w.M, 4096), [0, w.M - 1]]).astype(np.int32)
+    sn = np.concatenate([rng.integers(0, w.N, 4096), [0, w.N - 1]]).astype(np.int32)
+    _, Ys = oracle_mod.gemm_sample_qoq(Aq, r["q4"], sx_ref, sums_ref, r["s1"], r["s2"], r["z2"], sm, sn)
+    err = _sampled_y_error(Y.cpu().numpy()[sm, sn].astype(np.float64), Ys)
+    assert err <= Y_TOL, err
+    assert fmpq_gpu.fmpq_device_status(layout) == 0
+    layout.close()
+    torch.cuda.empty_cache()
