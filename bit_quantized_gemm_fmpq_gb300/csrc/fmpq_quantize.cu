@@ -483,16 +483,20 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
                 constexpr float kMagic = 12582912.0f;
                 float ax[8], tm[8];
                 bool near_half = false;
+                // two channels per instruction: fma.rn.f32x2 is the IEEE fma in each half; the
+                // fractional part of |x| * inv is |x| * inv - (tm - kMagic), with tm - kMagic exact
+                const float2 inv2 = make_float2(inv, inv), mg2 = make_float2(kMagic, kMagic);
+                const float2 neg1 = make_float2(-1.0f, -1.0f);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ab[k]));
-                    ax[2 * k] = f.x;
-                    ax[2 * k + 1] = f.y;
-                }
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    tm[k] = __fmaf_rn(ax[k], inv, kMagic);
-                    near_half |= fabsf(__fmaf_rn(ax[k], inv, kMagic - tm[k])) > 0.4999f;
+                    const float2 a2 = __half22float2(*reinterpret_cast<const __half2*>(&ab[k]));
+                    const float2 t2 = dev::ffma2(a2, inv2, mg2);
+                    const float2 f2 = dev::ffma2(a2, inv2, dev::ffma2(t2, neg1, mg2));
+                    ax[2 * k] = a2.x;
+                    ax[2 * k + 1] = a2.y;
+                    tm[2 * k] = t2.x;
+                    tm[2 * k + 1] = t2.y;
+                    near_half |= fmaxf(fabsf(f2.x), fabsf(f2.y)) > 0.4999f;
                 }
                 if (__any_sync(0xFFFFFFFFu, near_half) && sc > 0.0f) {
                     // (a zero scale keeps every code 0: its lanes skip the correction)
