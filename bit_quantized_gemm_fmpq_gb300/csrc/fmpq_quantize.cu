@@ -109,6 +109,7 @@ __device__ __forceinline__ uint32_t pack_int4_pair(uint32_t v, int lane) {
 // rounds), else 16; the fused-norm kernel uses 16 compute warps and 8 norm warps.
 constexpr int kQWarpsMin = 16, kQWarpsMax = 28;
 constexpr int kQNormWarps = 8;                     // fused RMSNorm: warps computing the rows' norms
+constexpr int kQTokWarps = 4;                      // per-token INT8: warps taking the rows' absmax
 constexpr int kQMaxThreads = (kQWarpsMax + 1) * 32;   // >= (16 + 1 + 8) * 32
 constexpr int kQSmemBudget = 200 * 1024;
 enum : int { kQSym = 0, kQNorm = 1, kQAsym = 2, kQTok = 3 };   // quantizer modes
@@ -120,7 +121,8 @@ struct QuantParams {
     int K, nb, stages;
     int Kin;                // staged row width: the channels a layout may select from (>= K)
     int iters;              // rounds per compute warp: ceil(nb / (2 * cwarps))
-    int cwarps;             // compute warps (the producer is warp cwarps, norm warps follow)
+    int cwarps;             // compute warps (the producer is warp cwarps, statistic warps follow)
+    int rwarps;             // row-statistic warps (fused RMSNorm: 8; per-token INT8 absmax: 4)
     const uint16_t* perm;
     const uint8_t* mask;
     const int32_t* poff;
@@ -270,8 +272,8 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             dev::mbar_init(&full[s], 1);
-            dev::mbar_init(&empty[s], p.cwarps + (kRowWarps ? kQNormWarps : 0));
-            dev::mbar_init(&nsync[s], kQNormWarps);
+            dev::mbar_init(&empty[s], p.cwarps + (kRowWarps ? p.rwarps : 0));
+            dev::mbar_init(&nsync[s], p.rwarps);
             dev::mbar_init(&rready[s], 1);
         }
         abort_flag = 0;
@@ -322,7 +324,7 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
                 if (!ok) break;
                 const uint8_t* row = reinterpret_cast<const uint8_t*>(rows_s + static_cast<size_t>(s) * Kr);
                 float* cs = chunk_s + static_cast<size_t>(s) * nb;
-                for (int q = nw; 2 * q < nb; q += kQNormWarps) {
+                for (int q = nw; 2 * q < nb; q += p.rwarps) {
                     const int b = 2 * q + half;
                     float acc = 0.0f;
                     if (b < nb) {
@@ -728,8 +730,12 @@ cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, in
     const int K = L.K, Kin = L.K_in;
     if (gamma_perm != nullptr) mode = kQNorm;
     const bool row_warps = mode == kQNorm || mode == kQTok;
+    // the per-token absmax is cheap: 4 statistic warps keep ahead, leaving room for 24 quantizing warps
+    const int rwarps = mode == kQNorm ? kQNormWarps : mode == kQTok ? kQTokWarps : 0;
     int cw = kQWarpsMin;
-    if (!row_warps)
+    if (mode == kQTok)
+        cw = kQMaxThreads / 32 - 1 - kQTokWarps;
+    else if (!row_warps)
         for (int w = kQWarpsMax; w > kQWarpsMin; --w)
             if (L.nb % (2 * w) == 0) {
                 cw = w;
@@ -781,6 +787,7 @@ cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, in
     p.stages = stages;
     p.iters = iters;
     p.cwarps = cw;
+    p.rwarps = rwarps;
     p.perm = L.d_perm16;
     p.mask = L.d_mask;
     p.poff = L.d_poff;
@@ -793,7 +800,7 @@ cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, in
     p.sums = mode == kQTok ? static_cast<int32_t*>(aux) : nullptr;
     const int64_t ctas = static_cast<int64_t>(L.num_sms) * per_sm;
     const unsigned grid = static_cast<unsigned>(M < ctas ? M : ctas);
-    const unsigned threads = static_cast<unsigned>((cw + 1 + (row_warps ? kQNormWarps : 0)) * 32);
+    const unsigned threads = static_cast<unsigned>((cw + 1 + rwarps) * 32);
     switch (mode) {
         case kQNorm: quantize_kernel<kQNorm><<<grid, threads, smem, stream>>>(p); break;
         case kQAsym: quantize_kernel<kQAsym><<<grid, threads, smem, stream>>>(p); break;
