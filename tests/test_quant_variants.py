@@ -425,3 +425,38 @@ def test_qoq_full_size(fmpq_gpu, oracle_mod):
     assert fmpq_gpu.fmpq_device_status(layout) == 0
     layout.close()
     torch.cuda.empty_cache()
+
+
+@pytest.mark.gpu
+def test_quik_whole_path(fmpq_gpu, oracle_mod):
+    """QUIK end to end (QUIK explainer, "第二步: 前向传播" and "反量化背后的数学"): base columns
+    through asymmetric INT4 (a layout selecting them from the full rows), outlier columns in
+    FP16, the two results added in Y. Each part against its exact value: the INT4 output within
+    the output tolerance, the merge within one fp16 rounding of each part."""
+    import torch
+    from tests.gpu_helpers import Y_TOL, to_dev, y_error
+    M, N, K_in, n_out = 200, 512, 2048, 128
+    rng = np.random.default_rng(31)
+    X = (rng.standard_normal((M, K_in)) + 0.3).astype(np.float32)
+    out_cols = np.sort(rng.choice(K_in, size=n_out, replace=False)).astype(np.int32)
+    X[:, out_cols] *= rng.uniform(20, 100, size=n_out).astype(np.float32)
+    X = X.astype(np.float16)
+    W = (rng.standard_normal((N, K_in)) * 0.02).astype(np.float16)
+    base = np.setdiff1d(np.arange(K_in), out_cols).astype(np.int32)
+    K = base.size
+    layout = fmpq_gpu.select_layout(K, K_in, base, np.zeros(K // BLOCK, np.uint8))
+    Xd, Wd = to_dev(X), to_dev(W)
+    A, sx, z = fmpq_gpu.fmpq_quantize_asym(layout, Xd)
+    Wp, sw = fmpq_gpu.w4_pack_weights(layout, Wd)
+    wsum = fmpq_gpu.w4_weight_sums(layout, Wp, sw, N)
+    Y = fmpq_gpu.w4ax_gemm_asym(layout, A, sx, z, Wp, sw, wsum, M, N)
+    Y_base = Y.cpu().numpy().astype(np.float64)
+    W_out = Wd[:, torch.from_numpy(out_cols).long().cuda()].contiguous()
+    fmpq_gpu.fmpq_outlier_gemm_fp16(Xd, to_dev(out_cols), W_out, Y)
+    Ym = Y.cpu().numpy().astype(np.float64)
+    ref = oracle_mod.asym_reference(X[:, base], W[:, base], np.arange(K, dtype=np.int32))
+    assert y_error(Y_base, ref["Y"]) <= Y_TOL
+    yo = X[:, out_cols].astype(np.float64) @ W[:, out_cols].astype(np.float64).T
+    ulp = lambda v: np.spacing(np.abs(v).astype(np.float16)).astype(np.float64)
+    assert np.all(np.abs(Ym - (Y_base + yo)) <= ulp(yo) + ulp(Ym))
+    layout.close()
