@@ -38,6 +38,17 @@ def test_reference_base_part_is_the_int4_gemm_of_the_base_columns(oracle_mod):
     assert np.array_equal(yb, ref["Y"])
 
 
+def test_reference_outlier_part_selects_the_weight_columns(oracle_mod):
+    """Unit outlier activations (token m holds 1 in outlier column m, 0 elsewhere) give back
+    the outlier weights: yo[m][n] = W[n][out[m]], exactly, and the base part is 0."""
+    X, W, base, out = _problem(16, 256, 16, 48, 5)
+    X[:] = 0
+    X[np.arange(16), out] = 1.0
+    yb, yo = oracle_mod.quik_reference(X, W, base, out)
+    assert np.all(yb == 0)
+    assert np.array_equal(yo, W[:, out].T.astype(np.float64))
+
+
 @pytest.fixture(scope="module")
 def fmpq_gpu():
     import torch
