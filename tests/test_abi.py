@@ -57,3 +57,26 @@ def test_invalid_layout_arguments_fail_before_touching_a_device(lib):
     badmask = (ctypes.c_uint8 * 2)(0, 3)
     assert lib.fmpq_layout_create(256, perm, badmask, ctypes.byref(out)) == 1    # mask value
     assert lib.fmpq_layout_create(256, None, mask, ctypes.byref(out)) == 1
+
+
+def test_entry_points_refuse_null_arguments_without_a_device(lib):
+    """Every compute entry point checks its pointers before any device call (status 1 =
+    FMPQ_ERR_INVALID_ARG), so a caller's mistake is reported synchronously."""
+    P = ctypes.c_void_p
+    i64 = ctypes.c_int64
+    z = P(None)
+    calls = {
+        "fmpq_quantize": (z, z, i64(8), i64(1), z, z, z),
+        "fmpq_quantize_asym": (z, z, i64(8), i64(1), z, z, z, z),
+        "qoq_quantize": (z, z, i64(8), i64(1), z, z, z, z),
+        "w4_pack_weights": (z, z, i64(8), i64(16), z, z, z),
+        "qoq_pack_weights": (z, z, i64(8), i64(16), z, z, z, z, z),
+        "w4_weight_sums": (z, z, z, i64(16), z, z),
+        "w4ax_gemm": (z, z, z, z, z, i64(1), i64(16), z, i64(16), z, ctypes.c_size_t(0), z),
+        "w4ax_gemm_asym": (z, z, z, z, z, z, z, i64(1), i64(16), z, i64(16), z, ctypes.c_size_t(0), z),
+        "qoq_gemm": (z, z, z, z, z, z, z, z, i64(1), i64(16), z, i64(16), z, ctypes.c_size_t(0), z),
+    }
+    for name, args in calls.items():
+        fn = getattr(lib, name)
+        fn.restype = ctypes.c_int
+        assert fn(*args) == 1, name

@@ -460,3 +460,52 @@ def test_quik_whole_path(fmpq_gpu, oracle_mod):
     ulp = lambda v: np.spacing(np.abs(v).astype(np.float16)).astype(np.float64)
     assert np.all(np.abs(Ym - (Y_base + yo)) <= ulp(yo) + ulp(Ym))
     layout.close()
+
+
+def test_qoq_group_codes_are_the_nearest_level(oracle_mod):
+    """Brute force over the 16 levels (q4 - z2) * s2 of each group: the oracle's code is the
+    level nearest to the INT8 value, ties to the even multiple of s2 (round half to even of
+    q8 / s2), for every range inside [-119, 119] and the values of the range."""
+    rng = np.random.default_rng(13)
+    lo = rng.integers(-119, 120, 3000)
+    hi = rng.integers(-119, 120, 3000)
+    lo, hi = np.minimum(lo, hi), np.maximum(lo, hi)
+    q8 = np.stack([rng.integers(l, h + 1, BLOCK) for l, h in zip(lo, hi)]).astype(np.int64)
+    q8[:, 0], q8[:, 1] = lo, hi
+    s2, z2, q4 = oracle_mod.qoq_group(q8.astype(np.int8))
+    levels = (np.arange(16)[None, :] - z2[:, None]) * s2[:, None]          # [G, 16]
+    dist = np.abs(q8[:, :, None] - levels[:, None, :])                     # [G, 128, 16]
+    best = dist.min(axis=2, keepdims=True)
+    cand = dist == best
+    k = np.arange(16)[None, None, :] - z2[:, None, None]                   # multiple of s2
+    # among equally near levels prefer the even multiple
+    pref = np.where(cand & (k % 2 == 0), 0, np.where(cand, 1, 2))
+    want = np.argmin(pref * 1000 + np.arange(16)[None, None, :], axis=2)
+    assert np.array_equal(q4.astype(np.int64), want)
+
+
+def test_asym_codes_are_the_nearest_level_on_dyadic_inputs(oracle_mod):
+    """Inputs on a grid of 1/16 in [-4, 4) with max - min = 15 * 2^-k: the scale is exact, every
+    difference and quotient is exact in fp32, so the code is the nearest of the 16 levels
+    z + q s (ties to even q), found by brute force."""
+    rng = np.random.default_rng(17)
+    M = 64
+    X = np.zeros((M, BLOCK), dtype=np.float32)
+    for m in range(M):
+        s = 2.0 ** -int(rng.integers(1, 5))                 # 1/2 .. 1/16
+        z = float(rng.integers(-64, 0)) / 16.0
+        v = z + rng.integers(0, 15 * 16, BLOCK) / 16.0 * s   # multiples of s/16 inside [z, z + 15 s)
+        v[0], v[1] = z, z + 15 * s
+        X[m] = v
+    X16 = X.astype(np.float16)
+    assert np.array_equal(X16.astype(np.float32), X)          # exactly representable
+    _, sv, zv, Aq = oracle_mod.quantize_activations_asym(X16, np.arange(BLOCK, dtype=np.int32))
+    s = oracle_mod.f16_bits_to_f32(sv).astype(np.float64)
+    z = oracle_mod.f16_bits_to_f32(zv).astype(np.float64)
+    levels = z[:, None] + np.arange(16)[None, :] * s[:, None]
+    dist = np.abs(X.astype(np.float64)[:, :, None] - levels[:, None, :])
+    best = dist.min(axis=2, keepdims=True)
+    cand = dist == best
+    pref = np.where(cand & (np.arange(16) % 2 == 0)[None, None, :], 0, np.where(cand, 1, 2))
+    want = np.argmin(pref * 1000 + np.arange(16)[None, None, :], axis=2)
+    assert np.array_equal(Aq.astype(np.int64), want)
