@@ -144,10 +144,18 @@ class ClockSampler:
                 "samples": len(sms)}
 
 
-def kernel_source_hash() -> str:
+# Sources each recorded kernel is compiled from: a recorded figure stays valid while these are
+# unchanged (an edit to another kernel's file does not touch this kernel's code).
+KERNEL_SOURCES = {
+    "w4ax_gemm": ("fmpq_gemm.cu", "fmpq_device.cuh", "fmpq_internal.h"),
+    "fmpq_quantize": ("fmpq_quantize.cu", "fmpq_device.cuh", "fmpq_internal.h"),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_quantized_gemm_fmpq_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -161,7 +169,7 @@ def recorded_traffic(kernel: str):
     with open(PROFILE_TRAFFIC) as f:
         d = json.load(f)
     e = d.get(kernel)
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or e.get("source_hash") != kernel_source_hash(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 
