@@ -6,10 +6,13 @@
 // round-half-even quantization to INT8 (outlier blocks) or INT4 (the rest; COMET news
 // article, section 1), and encoding into the operand-ready code planes documented in fmpq.h.
 //
-// HBM-bound design: persistent CTAs (one per SM) stream whole rows into shared memory with
-// TMA bulk copies (a dedicated producer warp, several stages), keep each lane's gather
-// offsets in registers, gather from shared memory, and write the code planes with
-// coalesced stores (each half-warp writes one 128-byte plane row).
+// Design: persistent CTAs (one per SM, two for short rows) stream whole rows into shared
+// memory with bulk copies (a dedicated producer warp, several stages), take each lane's
+// gather offsets from a table staged once in shared memory, gather from the staged rows, and
+// write the code planes with coalesced stores (each half-warp writes one 128-byte plane row).
+// Other modes of the same kernel: RMSNorm fused in front (norm warps compute each row's
+// factor ahead of the quantizing warps), QUIK asymmetric codes with zero points, and QoQ
+// per-token INT8 codes with block code sums.
 #include <cuda_fp16.h>
 
 #include "fmpq_device.cuh"
@@ -94,9 +97,9 @@ __device__ __forceinline__ uint32_t pack_int4_pair(uint32_t v, int lane) {
 // Activation quantizer.
 //
 // A warp quantizes two blocks of one token at a time: lanes 0-15 one block, lanes 16-31
-// another, 8 channels per lane. Warp w of the 16 compute warps owns blocks w, w+16,
-// w+32, ... for every token, so each lane keeps the gather offsets of its channels in
-// registers for the whole kernel. Rows of X are streamed into a shared-memory ring by a
+// another, 8 channels per lane. Warp w of the W compute warps owns blocks w, w + W, w + 2W,
+// ... for every token, so its gather offsets are the same for every row: they are staged
+// once in a shared-memory table. Rows of X are streamed into a shared-memory ring by a
 // producer warp (bulk copies); the gather reads them from there.
 //
 // Output: operand-ready code planes (layout in fmpq.h). A code's byte is sign<<7 | the
@@ -106,11 +109,12 @@ __device__ __forceinline__ uint32_t pack_int4_pair(uint32_t v, int lane) {
 // ---------------------------------------------------------------------------------
 // Compute warps W: per round the half-warps of warp w take blocks w + 2Wj and w + W + 2Wj. The
 // launch picks the largest W in [16, 28] with nb a multiple of 2W (every warp the same number of
-// rounds), else 16; the fused-norm kernel uses 16 compute warps and 8 norm warps.
+// rounds), else 16; the fused-norm kernel uses 16 compute warps and 8 norm warps, the per-token
+// INT8 kernel 24 compute warps and 4 absmax warps.
 constexpr int kQWarpsMin = 16, kQWarpsMax = 28;
 constexpr int kQNormWarps = 8;                     // fused RMSNorm: warps computing the rows' norms
 constexpr int kQTokWarps = 4;                      // per-token INT8: warps taking the rows' absmax
-constexpr int kQMaxThreads = (kQWarpsMax + 1) * 32;   // >= (16 + 1 + 8) * 32
+constexpr int kQMaxThreads = (kQWarpsMax + 1) * 32;   // >= (16 + 1 + 8) * 32 and (24 + 1 + 4) * 32
 constexpr int kQSmemBudget = 200 * 1024;
 enum : int { kQSym = 0, kQNorm = 1, kQAsym = 2, kQTok = 3 };   // quantizer modes
 
