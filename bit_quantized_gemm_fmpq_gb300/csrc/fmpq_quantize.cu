@@ -196,16 +196,20 @@ __device__ __forceinline__ void quantize_asym_step(const Params& p, const uint32
     constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23: adding it rounds to an integer (RNE)
     float d[8], tm[8];
     bool near_half = false;
+    // two channels per instruction (fma.rn.f32x2: the IEEE fma in each half)
+    const float2 inv2 = make_float2(inv, inv), mg2 = make_float2(kMagic, kMagic);
+    const float2 neg1 = make_float2(-1.0f, -1.0f);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2[k]));
-        d[2 * k] = __fsub_rn(f.x, z);
-        d[2 * k + 1] = __fsub_rn(f.y, z);
-    }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        tm[k] = __fmaf_rn(d[k], inv, kMagic);
-        near_half |= fabsf(__fmaf_rn(d[k], inv, kMagic - tm[k])) >= 0.5f - 1.52587890625e-05f;   // 2^-16
+        const float2 d2 = make_float2(__fsub_rn(f.x, z), __fsub_rn(f.y, z));
+        const float2 t2 = dev::ffma2(d2, inv2, mg2);
+        const float2 f2 = dev::ffma2(d2, inv2, dev::ffma2(t2, neg1, mg2));   // (x - z) * inv - rounded
+        d[2 * k] = d2.x;
+        d[2 * k + 1] = d2.y;
+        tm[2 * k] = t2.x;
+        tm[2 * k + 1] = t2.y;
+        near_half |= fmaxf(fabsf(f2.x), fabsf(f2.y)) >= 0.5f - 1.52587890625e-05f;   // 2^-16
     }
     if (__any_sync(0xFFFFFFFFu, near_half && sc > 0.0f)) {
         if (sc > 0.0f) {
