@@ -15,6 +15,11 @@
  *     dequantization scales in an FP32 epilogue (COMET abstract: mixed W4A4/W4A8 matrix
  *     multiplication with a mixed-precision data layout; QUIK explainer, section "kernel
  *     fusion": dequantization fused into the GEMM epilogue).
+ * Beside it: the layout derived from calibration data (fmpq_channel_absmax, fmpq_plan_layout),
+ * the quantizer fused with RMSNorm (fmpq_rmsnorm_quantize), QUIK's FP16 outlier split
+ * (fmpq_layout_create_select, fmpq_outlier_gemm_fp16), QUIK asymmetric activations
+ * (fmpq_quantize_asym, w4ax_gemm_asym) and QoQ progressive group quantization with W4A8
+ * GEMMs (qoq_pack_weights, qoq_quantize, qoq_gemm).
  *
  * Conventions for every call:
  *   - Pointers are DEVICE pointers unless the parameter name ends in "_host".
@@ -23,7 +28,8 @@
  *     fmpq_layout_create on the device current at that time).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream),
  *     never synchronize (except fmpq_layout_create/destroy and fmpq_device_status), and
- *     allocate no memory.
+ *     allocate no memory (except the first fmpq_outlier_gemm_fp16 call on a device, which
+ *     creates that device's cuBLAS handle).
  *   - Argument errors are reported synchronously by the return value and launch nothing.
  *     A CUDA launch failure returns FMPQ_ERR_CUDA. A device-side wait that gives up (a
  *     bounded wait, never a hang) records FMPQ_ERR_TIMEOUT in the layout's device status
