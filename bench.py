@@ -174,6 +174,15 @@ def recorded_traffic(kernel: str):
     return e.get("dram_bytes_per_launch")
 
 
+def quant_algorithmic_bytes(M: int, K: int, n8: int) -> int:
+    """Algorithmic HBM bytes of one quantizer pass: the fp16 input (2MK), the codes at their
+    nominal widths (INT4 blocks half a byte per code, INT8 blocks one byte) and one fp16 scale
+    per token and block."""
+    nb = K // 128
+    k8 = 128 * n8
+    return 2 * M * K + M * ((K - k8) // 2 + k8) + 2 * M * nb
+
+
 # ------------------------------------------------------------------------------- CPU oracle
 
 def oracle_sample_rate(w, target_s: float, rows: int = 8, cols: int = 4096, max_rounds: int = 2000):
@@ -318,8 +327,10 @@ def run_sweep(args):
         if fmpq.fmpq_device_status(layout) != 0:
             raise RuntimeError(f"device status after {name}")
         flops = 2.0 * M * N * K
-        gbytes = layout.packed_a_bytes(M) + 2 * layout.nb * M + layout.packed_w_bytes(N) + 2 * layout.nb * N + 2 * M * N
-        qbytes = 2 * M * K + 2 * K + layout.packed_a_bytes(M) + 2 * layout.nb * M
+        k8 = 128 * int(w.mask.sum())
+        a_alg = M * ((K - k8) // 2 + k8)   # codes at their nominal widths
+        gbytes = a_alg + 2 * layout.nb * M + layout.packed_w_bytes(N) + 2 * layout.nb * N + 2 * M * N
+        qbytes = quant_algorithmic_bytes(M, K, int(w.mask.sum()))
         t_tensor = flops / (fp8_peak * 1e12) * 1e3
         t_hbm = gbytes / (hbm * 1e9) * 1e3
         bound = "tensor" if t_tensor >= t_hbm else "hbm"
@@ -352,7 +363,7 @@ def run_sweep(args):
         ms_plain = timed(lambda: fmpq.fmpq_quantize(layout, X, A, sx))
         ms = timed(lambda: fmpq.fmpq_rmsnorm_quantize(layout, X, gperm, 1e-5, A, sx))
         clocks = sampler.stop()
-        nbytes = 2 * w.M * w.K + 2 * w.K + layout.packed_a_bytes(w.M) + 2 * layout.nb * w.M
+        nbytes = quant_algorithmic_bytes(w.M, w.K, int(w.mask.sum())) + 2 * w.K
         print(json.dumps({"sweep": "rmsnorm_quantize_llama70b_down", "M": w.M, "K": w.K, "bound": "hbm",
                           "kernel": "quantize_kernel<true>", "ms": ms, "quantize_only_ms": ms_plain,
                           "gbs": nbytes / (ms * 1e-3) / 1e9, "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm,
@@ -554,8 +565,10 @@ def main():
     peaks = measured_peaks()
     fp8_peak = peaks["bf16_tflops"] * 2.0   # nominal dense fp8/bf16 ratio (4.5 / 2.25)
     gemm_tflops = flops / (gemm_ms * 1e-3) / 1e12
-    a_bytes = layout.packed_a_bytes(M)
-    quant_bytes = 2 * M * K + 2 * K + a_bytes + 2 * layout.nb * M
+    # algorithmic bytes of the quantizer: read X (2MK), write the codes at their nominal widths
+    # (half a byte per INT4 code, one per INT8 code) and the fp16 scales
+    quant_bytes = quant_algorithmic_bytes(M, K, int(w.mask.sum()))
+    quant_moved = 2 * M * K + layout.packed_a_bytes(M) + 2 * layout.nb * M   # what the kernel writes
     quant_gbs = quant_bytes / (quant_ms * 1e-3) / 1e9
 
     # ---- end to end through the public API with host buffers
@@ -604,7 +617,8 @@ def main():
                    "parallelism": f"replicated weights, one {M}-token batch per GPU"},
         "gemm": {"ms": gemm_ms, "tflops_effective": gemm_tflops, "frac_fp8_peak": gemm_tflops / fp8_peak},
         "quantizer": {"ms": quant_ms, "gbs": quant_gbs, "frac_hbm": quant_gbs / peaks["hbm_gbs"],
-                      "bytes": quant_bytes},
+                      "bytes": quant_bytes, "bytes_basis": "2MK + M(K4/2 + K8) + 2M*nb (algorithmic)",
+                      "bytes_moved": quant_moved},
         "offline_pack_ms": pack_ms,
         "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak, "unit": "TFLOP/s",
                      "frac": gemm_tflops / fp8_peak, "traffic": recorded_traffic("w4ax_gemm"),

@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -12,6 +13,35 @@
 #include "fmpq_internal.h"
 
 static_assert(FMPQ_MAX_K / FMPQ_BLOCK <= fmpq::kMaxBlocks, "kernel block tables hold every block");
+
+namespace fmpq {
+
+cudaError_t ensure_smem_limit(const void* kernel, int bytes) {
+    struct Entry {
+        const void* kernel;
+        int device;
+        int bytes;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> done;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry& d : done)
+        if (d.kernel == kernel && d.device == dev && d.bytes >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    for (Entry& d : done)
+        if (d.kernel == kernel && d.device == dev) {
+            d.bytes = bytes;
+            return cudaSuccess;
+        }
+    done.push_back(Entry{kernel, dev, bytes});
+    return cudaSuccess;
+}
+
+}  // namespace fmpq
 
 namespace {
 

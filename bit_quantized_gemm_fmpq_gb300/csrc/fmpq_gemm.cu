@@ -692,8 +692,8 @@ int max_pairs(const fmpq_layout& L) {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = sizeof(Smem) + 1024;
     int clusters = 0;
-    if (cudaFuncSetAttribute(w4ax_gemm_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sizeof(Smem) + 1024)) == cudaSuccess &&
+    if (ensure_smem_limit(reinterpret_cast<const void*>(w4ax_gemm_kernel<false, false>),
+                          static_cast<int>(sizeof(Smem) + 1024)) == cudaSuccess &&
         cudaOccupancyMaxActiveClusters(&clusters, w4ax_gemm_kernel<false, false>, &cfg) == cudaSuccess && clusters > 0 &&
         clusters < pairs)
         pairs = clusters;
@@ -732,15 +732,10 @@ size_t gemm_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N, bool var
 
 cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& a, cudaStream_t stream) {
     const bool variant = a.zero_kind != kZeroNone || a.unsigned_w;
-    if (a.P == nullptr && !variant && gemm_small_path(a.M)) return launch_gemm_small(L, a, stream);
-    static bool attr_set = false;
-    if (!attr_set) {
-        for (auto fn : {w4ax_gemm_kernel<false, false>, w4ax_gemm_kernel<true, false>, w4ax_gemm_kernel<false, true>}) {
-            const cudaError_t e =
-                cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
-            if (e != cudaSuccess) return e;
-        }
-        attr_set = true;
+    if (!variant && gemm_small_path(a.M)) return launch_gemm_small(L, a, stream);
+    for (auto fn : {w4ax_gemm_kernel<false, false>, w4ax_gemm_kernel<true, false>, w4ax_gemm_kernel<false, true>}) {
+        const cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(fn), static_cast<int>(kSmemBytes));
+        if (e != cudaSuccess) return e;
     }
     Params p{};
     p.A = static_cast<const uint8_t*>(a.A);

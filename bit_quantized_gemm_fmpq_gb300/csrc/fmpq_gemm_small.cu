@@ -92,6 +92,9 @@ struct SParams {
     int splits;            // K splits per tile (1 = none)
     float* ws_partial;     // [ntiles][splits][256][T] FP32 partial sums (splits > 1)
     int32_t* ws_count;     // [ntiles][2] arrival counters per CTA half (zero between calls)
+    // partial-sum export (debug): P[m - pm0][n - pn0][b] for the window, instead of Y
+    int32_t* P;
+    int pm0, pmcount, pn0, pncount;
 };
 
 __device__ __forceinline__ uint32_t lo4s(uint32_t w) { return w & 0x87878787u; }
@@ -317,7 +320,7 @@ __device__ __forceinline__ void s_converter_role(const SParams& p, SSmem<kT>& s,
 // Warp q holds TMEM lanes 32q..32q+31: thread `lane` owns output channel
 // n0 + rank*128 + 32q + lane and accumulates its T token columns (32x32b loads, 16 columns
 // at a time, the next load in flight during the math of the current one).
-template <int kT>
+template <int kT, bool kPartials>
 __device__ __forceinline__ void s_epilogue_role(const SParams& p, SSmem<kT>& s, uint32_t rank, int q, int lane,
                                                 uint32_t tmem, volatile int* abort_flag) {
     constexpr int kAcc = acc_slots<kT>();
@@ -343,7 +346,28 @@ __device__ __forceinline__ void s_epilogue_role(const SParams& p, SSmem<kT>& s, 
                      dev::mbar_wait(&s.acc_full[ab], (v / kAcc) & 1, abort_flag);
                 ok = __all_sync(0xFFFFFFFFu, ok);
             }
-            if (ok) {
+            if (ok && kPartials) {
+                // export the exact partial sums of block t.block(i) for the window: column j of
+                // the accumulator is token j, P = D * 2^18 (operand encoding)
+                dev::tc_fence_after();
+                const int b = t.block(i);
+                const uint32_t taddr = tmem + lane_addr + static_cast<uint32_t>(ab * kT);
+                const bool n_in = n < p.N && n >= p.pn0 && n < p.pn0 + p.pncount;
+#pragma unroll 1
+                for (int c = 0; c < kChunks; ++c) {
+                    uint32_t d[16];
+                    dev::tmem_ld16(taddr + c * 16, d);
+                    dev::tmem_ld_wait16(d);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int m = 16 * c + j;
+                        if (n_in && m < p.M && m >= p.pm0 && m < p.pm0 + p.pmcount)
+                            p.P[(static_cast<int64_t>(m - p.pm0) * p.pncount + (n - p.pn0)) * p.nb + b] =
+                                __float2int_rn(__uint_as_float(d[j]) * 262144.0f);
+                    }
+                }
+                dev::tc_fence_before();
+            } else if (ok) {
                 dev::tc_fence_after();
                 const SScaleSlot& sl = s.sc[ss];
                 const float swr = sl.sw[lrow];
@@ -385,6 +409,9 @@ __device__ __forceinline__ void s_epilogue_role(const SParams& p, SSmem<kT>& s, 
                 if (2 * j + 1 < mvalid) p.Y[static_cast<int64_t>(2 * j + 1) * p.ldy + n] = __half_as_ushort(__float2half_rn(acc[j].y));
             }
         };
+        if constexpr (kPartials) {
+            continue;   // the window's partial sums are written; no output
+        }
         if (p.splits == 1) {
             store();
         } else {
@@ -428,7 +455,7 @@ __device__ __forceinline__ void s_epilogue_role(const SParams& p, SSmem<kT>& s, 
     if (!ok && lane == 0) sfail(p, abort_flag);
 }
 
-template <int kT>
+template <int kT, bool kPartials>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSThreads, 1) w4ax_gemm_small_kernel(const SParams p) {
     extern __shared__ uint8_t smem_raw[];
     SSmem<kT>& s = *reinterpret_cast<SSmem<kT>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -496,7 +523,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSThreads, 1) w4ax_g
     } else {
         dev::setmaxnreg_inc<192>();
         if (warp < 8 + kSEpiWarps) {
-            s_epilogue_role<kT>(p, s, rank, warp & 3, lane, tmem, abort_flag);
+            s_epilogue_role<kT, kPartials>(p, s, rank, warp & 3, lane, tmem, abort_flag);
         } else {
             s_converter_role<kT>(p, s, rank, 1, (warp - 12) * 32 + lane, lane, abort_flag);
         }
@@ -527,9 +554,9 @@ int small_max_pairs_t(const fmpq_layout& L) {
     cfg.blockDim = dim3(kSThreads);
     cfg.dynamicSmemBytes = small_smem_bytes<kT>();
     int clusters = 0;
-    if (cudaFuncSetAttribute(w4ax_gemm_small_kernel<kT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(small_smem_bytes<kT>())) == cudaSuccess &&
-        cudaOccupancyMaxActiveClusters(&clusters, w4ax_gemm_small_kernel<kT>, &cfg) == cudaSuccess && clusters > 0 &&
+    if (ensure_smem_limit(reinterpret_cast<const void*>(w4ax_gemm_small_kernel<kT, false>),
+                          static_cast<int>(small_smem_bytes<kT>())) == cudaSuccess &&
+        cudaOccupancyMaxActiveClusters(&clusters, w4ax_gemm_small_kernel<kT, false>, &cfg) == cudaSuccess && clusters > 0 &&
         clusters < pairs)
         pairs = clusters;
     cudaGetLastError();   // a failed query leaves no sticky error behind
@@ -558,14 +585,14 @@ int small_splits(const fmpq_layout& L, int64_t ntiles, int T) {
 
 template <int kT>
 cudaError_t launch_small_t(const fmpq_layout& L, const SParams& p, int pairs, cudaStream_t stream) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        const cudaError_t e = cudaFuncSetAttribute(w4ax_gemm_small_kernel<kT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(small_smem_bytes<kT>()));
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    w4ax_gemm_small_kernel<kT><<<2 * pairs, kSThreads, small_smem_bytes<kT>(), stream>>>(p);
+    const void* fn = p.P != nullptr ? reinterpret_cast<const void*>(w4ax_gemm_small_kernel<kT, true>)
+                                    : reinterpret_cast<const void*>(w4ax_gemm_small_kernel<kT, false>);
+    const cudaError_t e = ensure_smem_limit(fn, static_cast<int>(small_smem_bytes<kT>()));
+    if (e != cudaSuccess) return e;
+    if (p.P != nullptr)
+        w4ax_gemm_small_kernel<kT, true><<<2 * pairs, kSThreads, small_smem_bytes<kT>(), stream>>>(p);
+    else
+        w4ax_gemm_small_kernel<kT, false><<<2 * pairs, kSThreads, small_smem_bytes<kT>(), stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -604,7 +631,14 @@ cudaError_t launch_gemm_small(const fmpq_layout& L, const GemmArgs& a, cudaStrea
     const int T = tokens_tile(a.M);
     p.ntiles = static_cast<int>((a.N + kTileN - 1) / kTileN);
     p.splits = small_splits(L, p.ntiles, T);
-    if (p.splits > 1) {
+    if (a.P != nullptr) {
+        // partial-sum export: every unit writes its blocks' sums directly (no workspace)
+        p.P = a.P;
+        p.pm0 = static_cast<int>(a.pm0);
+        p.pmcount = static_cast<int>(a.pmcount);
+        p.pn0 = static_cast<int>(a.pn0);
+        p.pncount = static_cast<int>(a.pncount);
+    } else if (p.splits > 1) {
         p.ws_partial = static_cast<float*>(a.workspace);
         p.ws_count = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(a.workspace) +
                                                 static_cast<size_t>(p.ntiles) * p.splits * 256 * T * sizeof(float));

@@ -26,6 +26,11 @@ constexpr int kBlock = 128;
 constexpr int kMaxBlocks = 256;     // K <= 32768
 constexpr int kTileN = 256;          // packed-weight row grouping and GEMM tile width
 
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current device. Function
+// attributes are per device: the first call for each (kernel, device) sets it, later calls
+// return at once. Thread-safe.
+cudaError_t ensure_smem_limit(const void* kernel, int bytes);
+
 // Launchers (return cudaGetLastError() after the launch).
 // gamma_perm != nullptr: the quantized values are the row's RMSNorm with that gamma (permuted
 // channel order) and eps. mode: kQuantSym (FMPQ), kQuantAsym (QUIK asymmetric, aux = zero points

@@ -11,6 +11,11 @@
 // GPU that loads the library keeps it until the process exits. Host code only holds a
 // stand-in for it, not a device address, so the address is looked up once per device
 // with cudaGetSymbolAddress (with that device current) and cached.
+//
+// The split-K kernel needs its per-tile arrival counters at zero when it starts. A call that
+// completes leaves them at zero, but one that gave up on a device-side wait (FMPQ_ERR_TIMEOUT)
+// may not, so every call clears the counters it will use with a cudaMemsetAsync on the
+// caller's stream (no allocation) before the launch.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -33,16 +38,17 @@ std::mutex g_mutex;
 unsigned char* g_base[kMaxDevices] = {};
 
 // Device address of the scratch array on `dev` (which must be current). The first call on
-// a device looks it up and zeroes the counters.
+// a device looks it up (host-side work only: no device work, no allocation).
 fmpq_status scratch_base(int dev, unsigned char** out) {
     if (dev < 0 || dev >= kMaxDevices) return FMPQ_ERR_DEVICE;
     std::lock_guard<std::mutex> lock(g_mutex);
     if (g_base[dev] == nullptr) {
         void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_scratch) != cudaSuccess || ptr == nullptr) return FMPQ_ERR_CUDA;
-        unsigned char* base = static_cast<unsigned char*>(ptr);
-        if (cudaMemset(base + kScratchBytes, 0, kCounterBytes) != cudaSuccess) return FMPQ_ERR_CUDA;
-        g_base[dev] = base;
+        if (cudaGetSymbolAddress(&ptr, g_scratch) != cudaSuccess || ptr == nullptr) {
+            cudaGetLastError();
+            return FMPQ_ERR_CUDA;
+        }
+        g_base[dev] = static_cast<unsigned char*>(ptr);
     }
     *out = g_base[dev];
     return FMPQ_OK;
@@ -90,6 +96,9 @@ fmpq_status w4ax_gemm_noalloc(const fmpq_layout* L, const void* A_packed, const 
         // kScratchBytes so the counters land at the fixed counter region
         a.workspace = base + (kScratchBytes - partials);
         a.workspace_bytes = need;
+        // counters start at zero even after an earlier call that gave up on a device wait
+        if (cudaMemsetAsync(base + kScratchBytes, 0, counters, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return FMPQ_ERR_CUDA;
     }
     return fmpq::launch_gemm(*L, a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FMPQ_OK : FMPQ_ERR_CUDA;
 }

@@ -240,16 +240,47 @@ __host__ __device__ inline size_t quant_poff_offset(int K, int S, int tab_entrie
 __host__ __device__ inline size_t quant_chunk_offset(int K, int S, int iters, int nb) {
     return quant_poff_offset(K, S, iters) + ((4ull * nb + 15) & ~15ull);
 }
+// Row-statistic scratch per stage: the per-token INT8 kernel keeps one fp32 absmax per chunk,
+// the fused RMSNorm kernel one exact (lo, hi) pair of 64-bit sums per norm warp.
+__host__ __device__ inline size_t quant_stat_bytes(int S, int nb) {
+    const size_t chunks = 4ull * S * nb, pairs = 16ull * S * kQNormWarps;
+    return chunks > pairs ? chunks : pairs;
+}
 __host__ __device__ inline size_t quant_bars_offset(int K, int S, int iters, int nb) {
-    return quant_chunk_offset(K, S, iters, nb) + ((4ull * S * nb + 4ull * S + 15) & ~15ull);
+    return quant_chunk_offset(K, S, iters, nb) + ((quant_stat_bytes(S, nb) + 4ull * S + 15) & ~15ull);
+}
+
+// Exact sum of squares of fp16 values. A finite fp16 x is mant * 2^(max(e,1) - 25) (e the
+// exponent field, mant < 2^11), so x^2 = mant^2 * 2^(sh - 48) with sh = 2 max(e,1) - 2 in
+// [0, 58]: an integer number of 2^-48 units. Squares with sh < 32 go to `lo` (units 2^-48),
+// the others to `hi` (units 2^-16); a lane adds at most 128 squares, so neither overflows.
+__device__ __forceinline__ void add_square_exact(uint32_t h, uint64_t& lo, uint64_t& hi) {
+    const uint32_t e = (h >> 10) & 31u;
+    const uint32_t mant = (h & 1023u) | (e ? 1024u : 0u);
+    const uint32_t sh = e ? 2u * e - 2u : 0u;
+    const uint32_t sq = mant * mant;
+    const bool big = sh >= 32u;
+    const uint64_t t = static_cast<uint64_t>(sq) << (big ? sh - 32u : sh);
+    lo += big ? 0ull : t;
+    hi += big ? t : 0ull;
+}
+
+// Carry lo's bits above 2^32 into hi: afterwards the sum is hi * 2^32 + lo, lo < 2^32.
+__device__ __forceinline__ void carry_exact(uint64_t& lo, uint64_t& hi) {
+    hi += lo >> 32;
+    lo &= 0xFFFFFFFFull;
+}
+
+// (hi * 2^32 + lo) * 2^-48 rounded once to fp32 (nearest, ties to even); lo < 2^32. When the
+// sum needs more than 64 bits, lo only matters as a sticky bit far below the rounding position.
+__device__ __forceinline__ float exact_to_f32(uint64_t lo, uint64_t hi) {
+    if ((hi >> 32) == 0) return __fmul_rn(__ull2float_rn((hi << 32) | lo), 3.5527136788005009e-15f);   // 2^-48
+    return __fmul_rn(__ull2float_rn(hi | (lo != 0 ? 1ull : 0ull)), 1.52587890625e-05f);                // 2^-16
 }
 
 // kNorm: the quantized values are RMSNorm(x) = fp16_rn((fp32(x) * r) * fp32(gamma)) with
-// r = 1 / sqrt(T / K + eps) (IEEE divisions and square root), where T is the row's sum of
-// squares in a fixed order: every 128-channel chunk of the row (input channel order) is summed
-// by 16 lanes of 8 consecutive channels each (sequential fp32 adds of the exact squares), the
-// 16 lane sums are combined by an xor tree (8, 4, 2, 1), and the chunk sums by 32 lanes taking
-// chunks l, l+32, ... sequentially and an xor tree (16, ..., 1).
+// r = 1 / sqrt(T / K + eps) (IEEE divisions and square root), where T is the row's exact sum of
+// squares rounded once to fp32 (integer accumulation, so it does not depend on the order).
 // kQAsym (QUIK explainer, "反量化背后的数学": asymmetric activations): every block 4-bit with a
 // zero point z = the block's smallest input (value order, -0 below +0) and
 // s = fp16_rn((fp32(max) - fp32(z)) / 15); q = clamp(rne(fp32(fp32(x) - fp32(z)) / fp32(s)), 0, 15)
@@ -268,7 +299,8 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
     uint4* gtab = reinterpret_cast<uint4*>(smem_raw + quant_gtab_offset(Kr, S));              // [iters][W][32]
     int32_t* s_poff = reinterpret_cast<int32_t*>(smem_raw + quant_poff_offset(Kr, S, p.iters * p.cwarps)); // [nb]
     float* chunk_s = reinterpret_cast<float*>(smem_raw + quant_chunk_offset(Kr, S, p.iters * p.cwarps, nb));  // [S][nb]
-    float* r_s = chunk_s + static_cast<size_t>(S) * nb;                                            // [S]
+    uint64_t* wsum_s = reinterpret_cast<uint64_t*>(chunk_s);                                     // [S][8][2] (norm)
+    float* r_s = chunk_s + quant_stat_bytes(S, nb) / 4;                                            // [S]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + quant_bars_offset(Kr, S, p.iters * p.cwarps, nb));
     uint64_t* full = bars;            // [S] the row has landed
     uint64_t* empty = bars + S;       // [S] every reader is done with the row
@@ -316,10 +348,70 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
         }
         __syncwarp();
     } else if (warp > W) {
-        // ---------------- norm warps (fused RMSNorm): per row, the chunk sums of squares (norm
-        // warp w takes the chunk pairs w, w + 2, ...; each half-warp one chunk) and then, in
-        // norm warp 0, the row total and r; they run ahead of the quantizing warps
-        if constexpr (kRowWarps) {
+        // ---------------- row-statistic warps, ahead of the quantizing warps. Warp w takes the
+        // chunk pairs w, w + rwarps, ... (each half-warp one 128-channel chunk). Fused RMSNorm:
+        // the exact sum of squares of the row (integer accumulation, order-free), rounded once to
+        // fp32 by warp 0, then r. Per-token INT8: the chunk maxima, then the row's absmax.
+        if constexpr (kNorm) {
+            const int nw = warp - W - 1;
+            const int half = lane >> 4, sub16 = lane & 15;
+            int64_t i = 0;
+            bool ok = true;
+            for (int64_t m = blockIdx.x; m < p.M; m += gridDim.x, ++i) {
+                const int s = static_cast<int>(i % S);
+                const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
+                ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&full[s], ph, &abort_flag));
+                if (!ok) break;
+                const uint8_t* row = reinterpret_cast<const uint8_t*>(rows_s + static_cast<size_t>(s) * Kr);
+                uint64_t lo = 0, hi = 0;
+                for (int q = nw; 2 * q < nb; q += p.rwarps) {
+                    const int b = 2 * q + half;
+                    if (b < nb) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(row + (b * kBlock + sub16 * 8) * 2);
+                        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            add_square_exact(w4[k] & 0xFFFFu, lo, hi);
+                            add_square_exact(w4[k] >> 16, lo, hi);
+                        }
+                    }
+                }
+                carry_exact(lo, hi);
+#pragma unroll
+                for (int st = 16; st >= 1; st >>= 1) {
+                    lo += __shfl_xor_sync(0xFFFFFFFFu, lo, st);
+                    hi += __shfl_xor_sync(0xFFFFFFFFu, hi, st);
+                }
+                uint64_t* ws = wsum_s + static_cast<size_t>(s) * (2 * kQNormWarps);
+                if (lane == 0) {
+                    ws[2 * nw] = lo;
+                    ws[2 * nw + 1] = hi;
+                }
+                __syncwarp();
+                if (lane == 0) dev::mbar_arrive(&nsync[s]);
+                if (nw == 0) {
+                    ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&nsync[s], ph, &abort_flag));
+                    if (!ok) break;
+                    uint64_t tl = lane < p.rwarps ? ws[2 * lane] : 0ull;
+                    uint64_t th = lane < p.rwarps ? ws[2 * lane + 1] : 0ull;
+#pragma unroll
+                    for (int st = 4; st >= 1; st >>= 1) {   // rwarps <= 8
+                        tl += __shfl_xor_sync(0xFFFFFFFFu, tl, st);
+                        th += __shfl_xor_sync(0xFFFFFFFFu, th, st);
+                    }
+                    if (lane == 0) {
+                        carry_exact(tl, th);
+                        const float t = exact_to_f32(tl, th);
+                        // r = 1 / sqrt(T / K + eps), IEEE fp32 division, addition and square root
+                        r_s[s] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, static_cast<float>(K)), p.eps)));
+                        dev::mbar_arrive(&rready[s]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) dev::mbar_arrive(&empty[s]);
+            }
+            if (!ok && lane == 0) abort_flag = 1;
+        } else if constexpr (kRowWarps) {
             const int nw = warp - W - 1;
             const int half = lane >> 4, sub16 = lane & 15;
             const uint32_t hm = half ? 0xFFFF0000u : 0x0000FFFFu;
@@ -338,26 +430,14 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
                     if (b < nb) {
                         const uint4 v = *reinterpret_cast<const uint4*>(row + (b * kBlock + sub16 * 8) * 2);
                         const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-                        if constexpr (kNorm) {
+                        // the chunk's absmax (fp16 magnitudes order like their bit patterns)
+                        uint32_t m2 = 0;
 #pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[k]));
-                                acc = __fadd_rn(acc, __fmul_rn(f.x, f.x));   // squares of fp16 values are exact
-                                acc = __fadd_rn(acc, __fmul_rn(f.y, f.y));
-                            }
-                        } else {
-                            // the chunk's absmax (fp16 magnitudes order like their bit patterns)
-                            uint32_t m2 = 0;
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) m2 = __vmaxu2(m2, w4[k] & 0x7FFF7FFFu);
-                            acc = __half2float(__ushort_as_half(static_cast<unsigned short>(max(m2 & 0xFFFFu, m2 >> 16))));
-                        }
+                        for (int k = 0; k < 4; ++k) m2 = __vmaxu2(m2, w4[k] & 0x7FFF7FFFu);
+                        acc = __half2float(__ushort_as_half(static_cast<unsigned short>(max(m2 & 0xFFFFu, m2 >> 16))));
                     }
 #pragma unroll
-                    for (int st = 8; st >= 1; st >>= 1) {
-                        const float o = __shfl_xor_sync(hm, acc, st);
-                        acc = kNorm ? __fadd_rn(acc, o) : fmaxf(acc, o);
-                    }
+                    for (int st = 8; st >= 1; st >>= 1) acc = fmaxf(acc, __shfl_xor_sync(hm, acc, st));
                     if (b < nb && sub16 == 0) cs[b] = acc;
                 }
                 __syncwarp();
@@ -366,15 +446,11 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
                     ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&nsync[s], ph, &abort_flag));
                     if (!ok) break;
                     float t = 0.0f;
-                    for (int b = lane; b < nb; b += 32) t = kNorm ? __fadd_rn(t, cs[b]) : fmaxf(t, cs[b]);
+                    for (int b = lane; b < nb; b += 32) t = fmaxf(t, cs[b]);
 #pragma unroll
-                    for (int st = 16; st >= 1; st >>= 1) {
-                        const float o = __shfl_xor_sync(0xFFFFFFFFu, t, st);
-                        t = kNorm ? __fadd_rn(t, o) : fmaxf(t, o);
-                    }
+                    for (int st = 16; st >= 1; st >>= 1) t = fmaxf(t, __shfl_xor_sync(0xFFFFFFFFu, t, st));
                     if (lane == 0) {
-                        // RMSNorm: r = 1 / sqrt(T / K + eps); per-token INT8: the row's absmax
-                        r_s[s] = kNorm ? __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, static_cast<float>(K)), p.eps))) : t;
+                        r_s[s] = t;   // the row's absmax
                         dev::mbar_arrive(&rready[s]);
                     }
                 }
@@ -751,7 +827,7 @@ cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, in
             }
     const int iters = (L.nb + 2 * cw - 1) / (2 * cw);
     const size_t fixed = static_cast<size_t>(iters) * cw * 32 * 16 + ((4ull * L.nb + 15) & ~15ull) +
-                         ((4ull * 8 * L.nb + 4ull * 8 + 15) & ~15ull) + 32 * 16 + 1024;
+                         ((quant_stat_bytes(8, L.nb) + 4ull * 8 + 15) & ~15ull) + 32 * 16 + 1024;
     auto stages_for = [&](size_t budget) {
         const int st = budget > fixed ? static_cast<int>((budget - fixed) / (2ull * Kin)) : 0;
         return st > 8 ? 8 : st;
@@ -764,8 +840,8 @@ cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, in
         const int st2 = stages_for(kQSmemBudget / 2);
         const size_t smem2 = quant_bars_offset(Kin, st2, iters * cw, L.nb) + 8ull * (4 * st2);
         int blocks = 0;
-        if (cudaFuncSetAttribute(quantize_kernel<kQSym, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kQSmemBudget + 16 * 1024) == cudaSuccess &&
+        if (ensure_smem_limit(reinterpret_cast<const void*>(quantize_kernel<kQSym, true>), kQSmemBudget + 16 * 1024) ==
+                cudaSuccess &&
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, quantize_kernel<kQSym, true>, (cw + 1) * 32, smem2) ==
                 cudaSuccess &&
             blocks >= 2) {
@@ -776,14 +852,9 @@ cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, in
     }
     stages = stages < 1 ? 1 : stages;
     const size_t smem = quant_bars_offset(Kin, stages, iters * cw, L.nb) + 8ull * (4 * stages);
-    static bool attr_set = false;
-    if (!attr_set) {
-        for (auto fn : {quantize_kernel<kQSym>, quantize_kernel<kQNorm>, quantize_kernel<kQAsym>, quantize_kernel<kQTok>}) {
-            const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                       kQSmemBudget + 16 * 1024);
-            if (e != cudaSuccess) return e;
-        }
-        attr_set = true;
+    for (auto fn : {quantize_kernel<kQSym>, quantize_kernel<kQNorm>, quantize_kernel<kQAsym>, quantize_kernel<kQTok>}) {
+        const cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(fn), kQSmemBudget + 16 * 1024);
+        if (e != cudaSuccess) return e;
     }
     QuantParams p;
     p.X = static_cast<const uint16_t*>(X);

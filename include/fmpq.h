@@ -128,11 +128,8 @@ FMPQ_API fmpq_status fmpq_quantize(const fmpq_layout* layout, const void* X, int
  * "运行时设计"). Codes, scales and layout are those of fmpq_quantize applied to
  *   y[m][c] = fp16_rn( (fp32(x[m][c]) * r_m) * fp32(gamma[c]) ),
  *   r_m = 1 / sqrt(T_m / K + eps)   (IEEE fp32 division, square root and addition),
- * where T_m, the sum of x[m][c]^2, is formed in a fixed order so that results are reproducible:
- * each 128-channel chunk of the row (input channel order) is summed by 16 partial sums of 8
- * consecutive channels (sequential fp32 additions of the exact squares) combined by an xor
- * tree of strides 8, 4, 2, 1; the chunk sums are summed by 32 partial sums taking chunks
- * l, l + 32, l + 64, ... combined by an xor tree of strides 16, 8, 4, 2, 1.
+ * where T_m is the exact sum of x[m][c]^2 over the row, rounded once to fp32 (nearest, ties to
+ * even). It does not depend on any summation order.
  *   gamma_perm  fp16 [K]: gamma in the permuted order, gamma_perm[j] = gamma[perm[j]]
  *               (prepared once, like the weights). 16-byte aligned.
  *   eps         positive and finite (FMPQ_ERR_INVALID_ARG otherwise).
@@ -165,7 +162,9 @@ FMPQ_API size_t w4ax_gemm_workspace_bytes(const fmpq_layout* layout, int64_t M, 
  *   workspace  w4ax_gemm_workspace_bytes(layout, M, N) bytes (may be NULL when that is 0);
  *              zero-filled once before its first use; each call returns the arrival
  *              counters it uses to zero, so the buffer is reused without re-initialization.
- *              Calls that share a workspace must not run concurrently.
+ *              A call that records FMPQ_ERR_TIMEOUT may leave counters nonzero: zero-fill
+ *              the workspace again before reusing it. Calls that share a workspace must not
+ *              run concurrently.
  * The split-K reduction sums the K-splits in a fixed order, so results are deterministic. */
 FMPQ_API fmpq_status w4ax_gemm(const fmpq_layout* layout, const void* A_packed, const void* a_scales,
                       const void* W_packed, const void* w_scales, int64_t M, int64_t N,
@@ -178,11 +177,14 @@ FMPQ_API fmpq_status w4ax_gemm(const fmpq_layout* layout, const void* A_packed, 
  * counters, which every GPU that loads the library holds until exit. The paper has no
  * counterpart; this is an interface convenience.
  *   - Arguments and results are those of w4ax_gemm (no workspace arguments).
- *   - The first call on a device looks up the array's device address and zeroes its counters
- *     (synchronously); make that first call before any stream capture.
+ *   - The first call on a device looks up the array's device address (host-side work only);
+ *     make that first call before any stream capture.
+ *   - When the shape needs the array, each call first clears the arrival counters it uses
+ *     with a memset on `stream` (so a call after one that gave up with FMPQ_ERR_TIMEOUT still
+ *     starts from zero), then launches the GEMM on `stream`.
  *   - Shapes whose workspace would exceed the array return FMPQ_ERR_WORKSPACE.
- *   - All calls share the array: calls that overlap on the GPU (e.g. on two streams) race
- *     and must be serialized by the caller.
+ *   - All calls share the array, which keeps the last call's contents: calls that overlap on
+ *     the GPU (e.g. on two streams) race and must be serialized by the caller.
  *   - Allocates nothing. */
 FMPQ_API fmpq_status w4ax_gemm_noalloc(const fmpq_layout* layout, const void* A_packed,
                                        const void* a_scales, const void* W_packed,

@@ -55,6 +55,7 @@ def _load():
             lib.oracle_f32_to_f16_array.argtypes = [P, i64, P]
             lib.oracle_f16_to_f32_array.argtypes = [P, i64, P]
             lib.oracle_rmsnorm.argtypes = [P, i64, i32, i32, P, ctypes.c_float, P]
+            lib.oracle_rmsnorm_sumsq.argtypes = [P, i64, i32, i32, P]
             lib.oracle_channel_absmax.argtypes = [P, i64, i32, P]
             lib.oracle_plan_layout.argtypes = [i32, P, i32, P, P]
             lib.oracle_plan_layout.restype = i32
@@ -204,8 +205,9 @@ def epilogue(P, a_scales, w_scales, exact: bool = False) -> np.ndarray:
     return Y
 
 
-def gemm_sample(Aq, Wq, a_scales, w_scales, ms, ns):
-    """Per-block partials P [S, nb] and Y [S] at output positions (ms[s], ns[s])."""
+def gemm_sample(Aq, Wq, a_scales, w_scales, ms, ns, want_partials=True):
+    """Per-block partials P [S, nb] (None unless want_partials) and Y [S] at output positions
+    (ms[s], ns[s])."""
     Aq = _c(Aq, np.int8)
     Wq = _c(Wq, np.int8)
     M, K = Aq.shape
@@ -213,10 +215,10 @@ def gemm_sample(Aq, Wq, a_scales, w_scales, ms, ns):
     ms = _c(ms, np.int32)
     ns = _c(ns, np.int32)
     S = ms.size
-    P = np.zeros((S, K // BLOCK), dtype=np.int32)
+    P = np.zeros((S, K // BLOCK), dtype=np.int32) if want_partials else None
     Y = np.zeros(S, dtype=np.float64)
     _load().oracle_gemm_sample(_ptr(Aq), _ptr(Wq), _ptr(_c(a_scales, np.uint16)), _ptr(_c(w_scales, np.uint16)),
-                               M, N, K, S, _ptr(ms), _ptr(ns), _ptr(P), _ptr(Y))
+                               M, N, K, S, _ptr(ms), _ptr(ns), _ptr(P) if P is not None else None, _ptr(Y))
     return P, Y
 
 
@@ -257,9 +259,19 @@ def outlier_blocks(K: int, fraction: float) -> int:
     return min((n_out + BLOCK - 1) // BLOCK, K // BLOCK)
 
 
+def rmsnorm_sumsq(X) -> np.ndarray:
+    """T[m] = the exact sum of the squares of fp16 row X[m], rounded once to fp32 (nearest,
+    ties to even); float32 [M]."""
+    X = np.ascontiguousarray(np.asarray(X, dtype=np.float16)).view(np.uint16)
+    M, K = X.shape
+    T = np.empty(M, dtype=np.float32)
+    _load().oracle_rmsnorm_sumsq(_ptr(X), K, M, K, _ptr(T))
+    return T
+
+
 def rmsnorm(X, gamma, eps: float) -> np.ndarray:
-    """RMSNorm of fp16 X [M][K] with fp16 gamma [K] (input channel order), in the reduction
-    order the library specifies; returns float16 [M][K]."""
+    """RMSNorm of fp16 X [M][K] with fp16 gamma [K] (input channel order): r = 1/sqrt(T/K + eps)
+    with T the exact sum of squares rounded once to fp32; returns float16 [M][K]."""
     X = np.ascontiguousarray(np.asarray(X, dtype=np.float16)).view(np.uint16)
     g = np.ascontiguousarray(np.asarray(gamma, dtype=np.float16)).view(np.uint16)
     M, K = X.shape

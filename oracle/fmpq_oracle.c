@@ -485,54 +485,56 @@ int oracle_plan_layout(int K, const uint32_t* stat, int n8, int32_t* perm, uint8
  * RMSNorm fused into the quantizer (QServe explainer, "运行时设计": the activation
  * quantization of the QKV projection and the first FFN layer is fused into the layer norm
  * before them; the LLaMA family's layer norm is RMSNorm, y = x / sqrt(mean(x^2) + eps) * gamma).
- * The sum of squares is formed in the order the library specifies (16 partial sums of 8
- * channels per 128-channel chunk with an xor tree, then 32 partial sums over the chunks with
- * an xor tree), every step an IEEE fp32 operation, so the normalized fp16 values are exact
- * functions of the input. The quantizer above then takes y as its input.
+ * The sum of squares T is the exact real sum of the squared fp16 inputs, rounded once to
+ * fp32 (round to nearest, ties to even): it does not depend on any summation order. Every
+ * later step is one IEEE fp32 operation, so the normalized fp16 values are exact functions of
+ * the input. The quantizer above then takes y as its input.
  * ------------------------------------------------------------------------------------ */
 
-/* v[j] <- v[j] + v[j ^ s] for s = n/2, ..., 1 (all j at once); every entry ends equal. */
-static void xor_tree_f32(float* v, int n) {
-    float tmp[32];
-    for (int s = n / 2; s >= 1; s /= 2) {
-        for (int j = 0; j < n; ++j) tmp[j] = v[j] + v[j ^ s];
-        for (int j = 0; j < n; ++j) v[j] = tmp[j];
+/* A finite fp16 value is n * 2^-24 for an integer n (|n| < 2^40), so its square is n^2 * 2^-48:
+ * an integer count of 2^-48 below 2^80, and a row of at most 32768 of them stays below 2^95. */
+static unsigned __int128 f16_square_fixed48(uint16_t h) {
+    const unsigned e = (h >> 10) & 31u, f = h & 1023u;
+    const uint64_t mant = e ? (1024u + f) : f;           /* |x| = mant * 2^(max(e,1) - 25) */
+    const unsigned shift = 2u * (e ? e : 1u) - 2u;       /* x^2 = mant^2 * 2^(shift - 48) */
+    return (unsigned __int128)(mant * mant) << shift;
+}
+
+/* Round v * 2^-48 (v an exact non-negative integer) to the nearest fp32, ties to even. */
+static float fixed48_to_f32(unsigned __int128 v) {
+    if (v == 0) return 0.0f;
+    int bits = 0;
+    for (unsigned __int128 t = v; t != 0; t >>= 1) ++bits;
+    if (bits <= 24) return ldexpf((float)(uint64_t)v, -48);  /* exact */
+    const int drop = bits - 24;
+    uint64_t q = (uint64_t)(v >> drop);                       /* the top 24 bits */
+    const unsigned __int128 rem = v - ((unsigned __int128)q << drop);
+    const unsigned __int128 half = (unsigned __int128)1 << (drop - 1);
+    if (rem > half || (rem == half && (q & 1u))) ++q;         /* q may become 2^24: still exact */
+    return ldexpf((float)q, drop - 48);
+}
+
+/* T[m] = the exact sum of X[m][c]^2 over the K channels, rounded once to fp32. */
+void oracle_rmsnorm_sumsq(const uint16_t* X, int64_t ldx, int M, int K, float* T) {
+    for (int m = 0; m < M; ++m) {
+        unsigned __int128 acc = 0;
+        for (int c = 0; c < K; ++c) acc += f16_square_fixed48(X[(int64_t)m * ldx + c]);
+        T[m] = fixed48_to_f32(acc);
     }
 }
 
-/* Y [M][K] (input channel order) = RMSNorm of X [M][ldx] with gamma [K] (input order). */
+/* Y [M][K] (input channel order) = RMSNorm of X [M][ldx] with gamma [K] (input order):
+ * r = 1 / sqrt(T / K + eps), y = fp16_rn((fp32(x) * r) * fp32(gamma)), each an IEEE fp32 step. */
 void oracle_rmsnorm(const uint16_t* X, int64_t ldx, int M, int K, const uint16_t* gamma, float eps, uint16_t* Y) {
-    const int nb = K / 128;
-    float* chunk = (float*)malloc(sizeof(float) * (size_t)nb);
-    if (chunk == NULL) return;
     for (int m = 0; m < M; ++m) {
-        const uint16_t* x = X + (int64_t)m * ldx;
-        for (int b = 0; b < nb; ++b) {
-            float lanes[16];
-            for (int j = 0; j < 16; ++j) {
-                float a = 0.0f;
-                for (int i = 0; i < 8; ++i) {
-                    const float v = oracle_f16_to_f32(x[128 * b + 8 * j + i]);
-                    a = a + v * v;                        /* v*v is exact: one rounding per add */
-                }
-                lanes[j] = a;
-            }
-            xor_tree_f32(lanes, 16);
-            chunk[b] = lanes[0];
-        }
-        float t[32];
-        for (int l = 0; l < 32; ++l) {
-            float a = 0.0f;
-            for (int b = l; b < nb; b += 32) a = a + chunk[b];
-            t[l] = a;
-        }
-        xor_tree_f32(t, 32);
-        const float ms = t[0] / (float)K;
+        float t;
+        oracle_rmsnorm_sumsq(X + (int64_t)m * ldx, ldx, 1, K, &t);
+        const float ms = t / (float)K;
         const float r = 1.0f / sqrtf(ms + eps);
+        const uint16_t* x = X + (int64_t)m * ldx;
         for (int c = 0; c < K; ++c)
             Y[(int64_t)m * K + c] = oracle_f32_to_f16((oracle_f16_to_f32(x[c]) * r) * oracle_f16_to_f32(gamma[c]));
     }
-    free(chunk);
 }
 
 /* ====================================================================================

@@ -146,9 +146,10 @@ def test_argument_errors(fmpq_mod):
 
 # --------------------------------------------------------------------- full-size configs
 
-def _sampled_check(fmpq_mod, oracle_mod, w, n_samples=4096, window=(0, 16, 0, 32), seed=0):
+def _sampled_check(fmpq_mod, oracle_mod, w, n_samples=4096, window=(0, 16, 0, 32), seed=0, full_y=False):
     """Full-size run in the benchmark's launch configuration; bit-exact quantizer, weights and
-    a window of partial sums; Y at sampled positions against the oracle's fp64 epilogue."""
+    a window of partial sums; Y at sampled positions against the oracle's fp64 epilogue (every
+    position when full_y)."""
     import torch
     layout = fmpq_mod.Layout(w.K, w.perm, w.mask)
     got, dev = run_gpu(layout, w.X, w.W, want_partials=window)
@@ -165,9 +166,13 @@ def _sampled_check(fmpq_mod, oracle_mod, w, n_samples=4096, window=(0, 16, 0, 32
     Pw, _ = oracle_mod.gemm_sample(Aq, Wq_ref, sx_ref, sw_ref, ms.ravel(), ns.ravel())
     assert np.array_equal(got["P"].reshape(-1, w.K // 128), Pw), "partial sums differ"
     rng = np.random.default_rng(seed)
-    sm = np.concatenate([rng.integers(0, w.M, n_samples), [0, w.M - 1, w.M - 1]]).astype(np.int32)
-    sn = np.concatenate([rng.integers(0, w.N, n_samples), [0, 0, w.N - 1]]).astype(np.int32)
-    _, Ys = oracle_mod.gemm_sample(Aq, Wq_ref, sx_ref, sw_ref, sm, sn)
+    if full_y:
+        gm, gn = np.meshgrid(np.arange(w.M), np.arange(w.N), indexing="ij")
+        sm, sn = gm.ravel().astype(np.int32), gn.ravel().astype(np.int32)
+    else:
+        sm = np.concatenate([rng.integers(0, w.M, n_samples), [0, w.M - 1, w.M - 1]]).astype(np.int32)
+        sn = np.concatenate([rng.integers(0, w.N, n_samples), [0, 0, w.N - 1]]).astype(np.int32)
+    _, Ys = oracle_mod.gemm_sample(Aq, Wq_ref, sx_ref, sw_ref, sm, sn, want_partials=False)
     Yg = got["Y"][sm, sn].astype(np.float64)
     # the floor uses the rms of the sampled reference values
     floor = 1e-2 * np.sqrt(np.mean(Ys ** 2))
@@ -189,7 +194,9 @@ def test_config_llama70b_down(fmpq_mod, oracle_mod):
 
 @pytest.mark.parametrize("M", wl.DECODE_MS)
 def test_config_decode(fmpq_mod, oracle_mod, M):
-    _sampled_check(fmpq_mod, oracle_mod, wl.decode(M), window=(0, M, 100, 300))
+    """Decode shapes (the few-token kernel): every output element against the oracle, and the
+    per-block partial sums of a 300-channel window bit-exact through the same kernel."""
+    _sampled_check(fmpq_mod, oracle_mod, wl.decode(M), window=(0, M, 100, 300), full_y=True)
 
 
 @pytest.mark.parametrize("frac", wl.LOAD_BALANCE_FRACS)

@@ -44,6 +44,67 @@ def test_oracle_rmsnorm_scale_invariance(oracle_mod):
     assert np.array_equal(y1.view(np.uint16), y4.view(np.uint16))
 
 
+def _exact_sumsq_f32(row):
+    """The exact sum of squares of an fp16 row, rounded to fp32 by mpmath at 24-bit precision
+    (round to nearest, ties to even). fp16 values times 2^24 are integers, so the sum is the
+    exact integer sum of their squares times 2^-48 (Python integers, no rounding)."""
+    mpmath = pytest.importorskip("mpmath")
+    n = (np.asarray(row, dtype=np.float16).astype(np.float64) * 2.0 ** 24).astype(np.int64)
+    total = sum(int(v) * int(v) for v in n)
+    with mpmath.workprec(24):
+        t = mpmath.ldexp(mpmath.mpf(total), -48)   # mpf() of an int rounds once to 24 bits
+    return np.float32(float(t))
+
+
+def _rows_that_round(K, count, seed):
+    """Rows whose squares span a wide range (Laplace bulk, a few large outliers, tiny values)
+    so that partial sums round in fp32."""
+    rng = np.random.default_rng(seed)
+    X = rng.laplace(0.0, 1.0, (count, K)).astype(np.float32)
+    X[:, rng.choice(K, K // 10, replace=False)] *= rng.uniform(20, 100, K // 10).astype(np.float32)
+    X[:, rng.choice(K, K // 8, replace=False)] *= np.float32(1e-3)
+    return X.astype(np.float16)
+
+
+def test_oracle_rmsnorm_sumsq_is_exact_then_rounded(oracle_mod):
+    """T equals the exact sum rounded once (mpmath), on rows where fp32 summation in any fixed
+    order visibly rounds: the pin fails for a sequential or a pairwise fp32 sum (both checked
+    to differ from the exact result on some of these rows)."""
+    for K, count, seed in ((4096, 24, 1), (28672, 6, 2)):
+        X = _rows_that_round(K, count, seed)
+        T = oracle_mod.rmsnorm_sumsq(X)
+        exact = np.array([_exact_sumsq_f32(r) for r in X], dtype=np.float32)
+        assert np.array_equal(T.view(np.uint32), exact.view(np.uint32))
+        sq = X.astype(np.float32) ** 2                       # exact squares
+        sequential = np.cumsum(sq, axis=1, dtype=np.float32)[:, -1]
+        pairwise = np.sum(sq, axis=1, dtype=np.float32)
+        assert np.any(sequential != exact), "rows too benign: a sequential fp32 sum would pass"
+        assert np.any(pairwise != exact), "rows too benign: a pairwise fp32 sum would pass"
+
+
+def test_oracle_rmsnorm_from_exact_sumsq(oracle_mod):
+    """y = fp16(fp32(x) * r * gamma), r = 1/sqrt(T/K + eps), each an IEEE fp32 step (numpy
+    float32), from the exactly rounded T."""
+    X = _rows_that_round(2048, 8, 3)
+    g = np.random.default_rng(4).uniform(0.5, 1.5, 2048).astype(np.float16)
+    eps = np.float32(1e-5)
+    Y = oracle_mod.rmsnorm(X, g, float(eps))
+    for m in range(X.shape[0]):
+        t = _exact_sumsq_f32(X[m])
+        r = np.float32(1.0) / np.sqrt(t / np.float32(2048) + eps)
+        y = ((X[m].astype(np.float32) * r) * g.astype(np.float32)).astype(np.float16)
+        assert np.array_equal(Y[m].view(np.uint16), y.view(np.uint16))
+
+
+def test_oracle_rmsnorm_order_free(oracle_mod):
+    """The exact sum does not depend on the channel order: permuting a row's channels leaves T
+    unchanged bit for bit."""
+    X = _rows_that_round(8192, 4, 5)
+    perm = np.random.default_rng(6).permutation(8192)
+    assert np.array_equal(oracle_mod.rmsnorm_sumsq(X).view(np.uint32),
+                          oracle_mod.rmsnorm_sumsq(X[:, perm]).view(np.uint32))
+
+
 def test_oracle_rmsnorm_zero_row(oracle_mod):
     x = np.zeros((1, 256), dtype=np.float16)
     y = oracle_mod.rmsnorm(x, np.ones(256, dtype=np.float16), 1e-5)

@@ -1,8 +1,11 @@
 """GPU test of w4ax_gemm_noalloc, the GEMM entry point for callers that cannot allocate
 device memory (the library supplies the split-K workspace from its own fixed device array).
-Its output must match w4ax_gemm's within the tolerance the parity tests use, on two calls in
-a row (the second call reuses the array the first one left behind). This file is collected
-last so a run that stops at the first failure has already run every other test."""
+
+Both entry points run the same deterministic kernel, so w4ax_gemm_noalloc must reproduce
+w4ax_gemm's output bit for bit, on two calls in a row (the second call reuses the array the
+first one left behind), and both must agree with the oracle within the parity tolerance. This
+file is collected last so a run that stops at the first failure has already run every other
+test."""
 import numpy as np
 import pytest
 
@@ -23,19 +26,24 @@ def fmpq_mod():
     return fmpq
 
 
-@pytest.mark.parametrize("M,N,K,n8", [
-    (16, 512, 2048, 2),    # few output tiles: split-K, the workspace comes from the fixed array
-    (1, 1024, 4096, 3),    # one token, split-K
-    (300, 784, 1024, 2),   # enough tiles: no workspace needed
+@pytest.mark.parametrize("M,N,K,n8,split", [
+    (16, 512, 2048, 2, True),     # few output tiles: split-K, the workspace comes from the fixed array
+    (1, 1024, 4096, 3, True),     # one token, split-K
+    (300, 784, 1024, 2, False),   # enough tiles: no workspace needed
 ])
-def test_noalloc_matches_gemm(fmpq_mod, M, N, K, n8):
+def test_noalloc_matches_gemm(fmpq_mod, oracle_mod, M, N, K, n8, split):
     w = wl.synthetic(M, N, K, n8=n8, seed=M * 7 + N + K)
     layout = fmpq_mod.Layout(w.K, w.perm, w.mask)
+    # the split-K cases must really go through the library's fixed array
+    assert (layout.workspace_bytes(M, N) > 0) == split
     A, sx = fmpq_mod.fmpq_quantize(layout, to_dev(w.X))
     Wp, sw = fmpq_mod.w4_pack_weights(layout, to_dev(w.W))
-    ref = fmpq_mod.w4ax_gemm(layout, A, sx, Wp, sw, M, N).cpu().numpy().astype(np.float64)
+    ref = fmpq_mod.w4ax_gemm(layout, A, sx, Wp, sw, M, N).cpu().numpy()
+    oracle_y = oracle_mod.reference(w.X, w.W, w.perm, w.mask)["Y"]
+    assert y_error(ref, oracle_y) <= Y_TOL
     for _ in range(2):
         Y = fmpq_mod.w4ax_gemm_noalloc(layout, A, sx, Wp, sw, M, N).cpu().numpy()
-        assert y_error(Y, ref) <= Y_TOL
+        assert np.array_equal(Y.view(np.uint16), ref.view(np.uint16))
+        assert y_error(Y, oracle_y) <= Y_TOL
     assert fmpq_mod.fmpq_device_status(layout) == 0
     layout.close()
