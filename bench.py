@@ -370,7 +370,7 @@ def run_sweep(args):
                           "l2": "flushed before every timed launch", "clocks": clocks}), flush=True)
         del layout
     if not args.sweep_only or args.sweep_only == "outlier_split_llama70b_down":
-        # outlier split: 256 outlier channels in FP16 (cuBLAS), the other 28416 through the INT4 path
+        # outlier split: 256 outlier channels in FP16 (tensor-core kernel), the other 28416 through the INT4 path
         w = wl.llama70b_down()
         n_out = 256
         rng = np.random.default_rng(6)
@@ -392,7 +392,7 @@ def run_sweep(args):
         fmpq.fmpq_quantize(layout, X, A, sx)
         sampler.start()
         ms_base = timed(lambda: fmpq.w4ax_gemm(layout, A, sx, Wp, sw, w.M, w.N, Y, workspace=ws))
-        ms_out = timed(lambda: fmpq.fmpq_outlier_gemm_fp16(X, cols, W_out, Y, X_out))
+        ms_out = timed(lambda: fmpq.fmpq_outlier_gemm_fp16(layout, X, cols, W_out, Y, X_out))
         clocks = sampler.stop()
         print(json.dumps({"sweep": "outlier_split_llama70b_down", "M": w.M, "K_base": Kb, "n_out": n_out, "N": w.N,
                           "int4_path_ms": ms_base, "fp16_outlier_path_ms": ms_out,

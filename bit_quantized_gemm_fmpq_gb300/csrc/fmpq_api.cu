@@ -430,21 +430,22 @@ fmpq_status fmpq_channel_absmax(const void* X, int64_t ldx, int64_t T, int32_t K
     return launched(fmpq::launch_channel_absmax(X, ldx, T, K, absmax, sms, static_cast<cudaStream_t>(stream)));
 }
 
-fmpq_status fmpq_outlier_gemm_fp16(const void* X, int64_t ldx, int64_t M, const int32_t* cols, int32_t n_out,
-                                   const void* W_out, int64_t ldw_out, int64_t N, void* X_out, void* Y, int64_t ldy,
-                                   void* stream) {
-    if (X == nullptr || cols == nullptr || W_out == nullptr || X_out == nullptr || Y == nullptr)
+fmpq_status fmpq_outlier_gemm_fp16(const fmpq_layout* L, const void* X, int64_t ldx, int64_t M, const int32_t* cols,
+                                   int32_t n_out, const void* W_out, int64_t ldw_out, int64_t N, void* X_out, void* Y,
+                                   int64_t ldy, void* stream) {
+    if (L == nullptr || X == nullptr || cols == nullptr || W_out == nullptr || X_out == nullptr || Y == nullptr)
         return FMPQ_ERR_INVALID_ARG;
-    if (M < 1 || M > INT32_MAX || n_out < 8 || n_out % 8 != 0 || n_out > FMPQ_MAX_K || N < 1 || N > INT32_MAX ||
-        ldx < 1 || ldw_out < n_out || ldy < N || ldw_out > INT32_MAX || ldy > INT32_MAX)
+    if (M < 1 || M > INT32_MAX || n_out < 8 || n_out % 8 != 0 || n_out > FMPQ_MAX_K || N < 1 ||
+        N > 65535ll * 128 || ldx < 1 || ldw_out < n_out || ldy < N || ldw_out > INT32_MAX || ldy > INT32_MAX)
         return FMPQ_ERR_UNSUPPORTED_SHAPE;
     if (ldx % 8 != 0 || ldw_out % 8 != 0 || ldy % 8 != 0 || !aligned16(X) || !aligned16(cols) || !aligned16(W_out) ||
         !aligned16(X_out) || !aligned16(Y))
         return FMPQ_ERR_MISALIGNED;
-    bool cublas_ok = true;
+    if (fmpq_status st = check_device(L)) return st;
+    bool maps_ok = true;
     const cudaError_t e = fmpq::launch_outlier_gemm(X, ldx, M, cols, n_out, W_out, ldw_out, N, X_out, Y, ldy,
-                                                    static_cast<cudaStream_t>(stream), &cublas_ok);
-    return (e == cudaSuccess && cublas_ok) ? FMPQ_OK : FMPQ_ERR_CUDA;
+                                                    L->d_status, static_cast<cudaStream_t>(stream), &maps_ok);
+    return (e == cudaSuccess && maps_ok) ? FMPQ_OK : FMPQ_ERR_CUDA;
 }
 
 fmpq_status fmpq_plan_layout(int32_t K, const uint32_t* absmax_host, int32_t n8, int32_t* perm_host,

@@ -88,11 +88,12 @@ size_t gemm_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N, bool var
 size_t gemm_counter_bytes(const fmpq_layout& L, int64_t M, int64_t N, bool variant = false);
 cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& args, cudaStream_t stream);
 
-// Outlier split, FP16 path: gather X[:, cols] into X_out, Y += X_out * W_out^T (cuBLAS, loaded on
-// first use). *cublas_ok is false when cuBLAS cannot be loaded or a cuBLAS call fails.
+// Outlier split, FP16 path: gather X[:, cols] into X_out, Y += X_out * W_out^T (tcgen05 kind::f16
+// tiles; device-side timeouts go to `status`). *maps_ok is false when a TMA tensor map cannot be
+// encoded (nothing is launched then).
 cudaError_t launch_outlier_gemm(const void* X, int64_t ldx, int64_t M, const int32_t* cols, int n_out,
                                 const void* W_out, int64_t ldw_out, int64_t N, void* X_out, void* Y, int64_t ldy,
-                                cudaStream_t stream, bool* cublas_ok);
+                                int32_t* status, cudaStream_t stream, bool* maps_ok);
 
 // Calibration: per-channel absmax (zeroes `out`, then reduces) and the host layout planner.
 cudaError_t launch_channel_absmax(const void* X, int64_t ldx, int64_t T, int K, uint32_t* out, int num_sms,

@@ -56,7 +56,7 @@ SIGNATURES = {
     "qoq_gemm": (_I32, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, _I64, _P, _SZ, _P]),
     "qoq_gemm_partials": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P]),
     "fmpq_layout_create_select": (_I32, [_I32, _I32, _P, _P, ctypes.POINTER(_P)]),
-    "fmpq_outlier_gemm_fp16": (_I32, [_P, _I64, _I64, _P, _I32, _P, _I64, _I64, _P, _P, _I64, _P]),
+    "fmpq_outlier_gemm_fp16": (_I32, [_P, _P, _I64, _I64, _P, _I32, _P, _I64, _I64, _P, _P, _I64, _P]),
     "fmpq_channel_absmax": (_I32, [_P, _I64, _I64, _I32, _P, _P]),
     "fmpq_plan_layout": (_I32, [_I32, _P, _I32, _P, _P]),
     "fmpq_outlier_blocks": (_I32, [_I32, ctypes.c_double]),
@@ -330,8 +330,9 @@ def select_layout(K: int, K_in: int, select, mask) -> "Layout":
     return lay
 
 
-def fmpq_outlier_gemm_fp16(X, cols, W_out, Y, X_out=None, stream=None):
-    """Y += X[:, cols] @ W_out^T in FP16 (the outlier path of an outlier split)."""
+def fmpq_outlier_gemm_fp16(layout: "Layout", X, cols, W_out, Y, X_out=None, stream=None):
+    """Y += X[:, cols] @ W_out^T in FP16 (the outlier path of an outlier split); `layout` is the
+    base part's layout (its device status word records device-side timeouts)."""
     import torch
     M = X.shape[0]
     n_out = cols.numel()
@@ -339,7 +340,7 @@ def fmpq_outlier_gemm_fp16(X, cols, W_out, Y, X_out=None, stream=None):
     if X_out is None:
         X_out = torch.empty((M, n_out), dtype=torch.float16, device=X.device)
     _check("fmpq_outlier_gemm_fp16", load_library().fmpq_outlier_gemm_fp16(
-        _ptr(X), X.stride(0), M, _ptr(cols), n_out, _ptr(W_out), W_out.stride(0), N, _ptr(X_out), _ptr(Y),
+        layout.handle, _ptr(X), X.stride(0), M, _ptr(cols), n_out, _ptr(W_out), W_out.stride(0), N, _ptr(X_out), _ptr(Y),
         Y.stride(0), _stream(stream)))
     return Y
 

@@ -28,8 +28,7 @@
  *     fmpq_layout_create on the device current at that time).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream),
  *     never synchronize (except fmpq_layout_create/destroy and fmpq_device_status), and
- *     allocate no memory (except the first fmpq_outlier_gemm_fp16 call on a device, which
- *     creates that device's cuBLAS handle).
+ *     allocate no memory.
  *   - Argument errors are reported synchronously by the return value and launch nothing.
  *     A CUDA launch failure returns FMPQ_ERR_CUDA. A device-side wait that gives up (a
  *     bounded wait, never a hang) records FMPQ_ERR_TIMEOUT in the layout's device status
@@ -202,18 +201,20 @@ FMPQ_API fmpq_status w4ax_gemm_partials(const fmpq_layout* layout, const void* A
 /* The FP16 path of an outlier split (QUIK explainer, "第二步: 前向传播": the outlier columns are
  * multiplied in FP16 by the unquantized outlier weights and added to the INT4 path's result):
  *   X_out[m][j] = X[m][cols[j]]   (0 for an index outside [0, ldx))
- *   Y[m][n]    += sum_j X_out[m][j] * W_out[n][j]   (FP32 accumulation, fp16 result)
+ *   Y[m][n]    += sum_j X_out[m][j] * W_out[n][j]   (FP32 accumulation, one fp16 rounding of
+ *                                                     the sum Y + product)
+ *   layout     the base part's layout (fmpq_layout_create_select); only its device and its
+ *              device status word are used (a device-side timeout is recorded there).
  *   X          fp16 [M][ldx] (device); cols int32 [n_out] (device); n_out % 8 == 0.
  *   W_out      fp16 [N][ldw_out], ldw_out >= n_out, the outlier columns of the weights (offline).
  *   X_out      fp16 [M][n_out] device workspace (caller-owned), overwritten.
- *   Y          fp16 [M][ldy], ldy >= N: read and updated in place (run the INT4 path first).
- * The product is a plain FP16 GEMM from cuBLAS, loaded at run time on the first call (which
- * also creates the device's cuBLAS handle: make it before any stream capture). Calls on one
- * device share that handle and are serialized by a host lock. FMPQ_ERR_CUDA if cuBLAS cannot
- * be loaded or fails. */
-FMPQ_API fmpq_status fmpq_outlier_gemm_fp16(const void* X, int64_t ldx, int64_t M, const int32_t* cols,
-                                            int32_t n_out, const void* W_out, int64_t ldw_out, int64_t N,
-                                            void* X_out, void* Y, int64_t ldy, void* stream);
+ *   Y          fp16 [M][ldy], ldy >= N, N <= 8388480: read and updated in place (run the INT4
+ *              path first).
+ * The product runs on the tensor cores (tcgen05 kind::f16, FP32 accumulator in TMEM) in the
+ * library's own kernel; nothing is allocated. FMPQ_ERR_CUDA if a launch fails. */
+FMPQ_API fmpq_status fmpq_outlier_gemm_fp16(const fmpq_layout* layout, const void* X, int64_t ldx, int64_t M,
+                                            const int32_t* cols, int32_t n_out, const void* W_out, int64_t ldw_out,
+                                            int64_t N, void* X_out, void* Y, int64_t ldy, void* stream);
 
 /* ---- Offline layout derivation from calibration activations ----
  * The activation outliers sit in a small set of channels (about 10%: COMET news article,

@@ -1,12 +1,13 @@
 """Outlier split (QUIK explainer, "第二步: 前向传播"): the base columns through the INT4 path
-(a layout selecting them from the full rows), the outlier columns in FP16 (gathered, then a
-plain FP16 GEMM added to the output).
+(a layout selecting them from the full rows), the outlier columns in FP16 (gathered, then the
+library's FP16 tensor-core GEMM added to the output).
 
 CPU: the reference pinned against the full-layout reference. GPU: the selected-layout quantizer
 bit-exact against the oracle on the gathered base columns; the INT4 path's output against its
-exact value within the output tolerance, and the merged output (the INT4 output in fp16 plus the
-FP16 outlier product, as the pages merge them) against that fp16 output plus the exact outlier
-product within the fp16 roundings of the merge."""
+exact value within the output tolerance; the FP16 outlier product alone, and the merged output
+(the INT4 output in fp16 plus the FP16 outlier product, as the pages merge them), against the
+oracle's exact product element by element, within one fp16 rounding and the FP32 summation
+bound."""
 import numpy as np
 import pytest
 
@@ -60,6 +61,35 @@ def fmpq_gpu():
     return fmpq
 
 
+def _fp32_sum_bound(X, W, out):
+    """A bound on the FP32 accumulation error of the outlier product: each of the n_out
+    additions errs by at most 2^-24 of the running magnitude, at most sum_j |x_j w_j|."""
+    Xo = np.abs(X[:, out].astype(np.float64))
+    Wo = np.abs(W[:, out].astype(np.float64))
+    return out.size * 2.0 ** -24 * (Xo @ Wo.T)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("M,N,n_out", [(256, 512, 128), (37, 272, 256), (1, 1024, 64), (130, 200, 72)])
+def test_outlier_product_matches_oracle(fmpq_gpu, oracle_mod, M, N, n_out):
+    """The FP16 outlier product alone (Y starts at 0) against the oracle's exact product, element
+    by element: one fp16 rounding of the FP32 sum. Ragged M, N and outlier counts that leave
+    partial 128-row, 128-column and 64-channel boxes."""
+    import torch
+    X, W, base, out = _problem(M, 256, n_out, N, M + 3 * N)
+    layout = fmpq_gpu.select_layout(256, 256 + n_out, base, np.zeros(2, np.uint8))
+    _, yo = oracle_mod.quik_reference(X, W, base, out)
+    Y = torch.zeros((M, N), dtype=torch.float16, device="cuda")
+    fmpq_gpu.fmpq_outlier_gemm_fp16(layout, torch.from_numpy(X).cuda(), torch.from_numpy(out).cuda(),
+                                    torch.from_numpy(np.ascontiguousarray(W[:, out])).cuda(), Y)
+    Yg = Y.cpu().numpy().astype(np.float64)
+    half_ulp = 0.5 * np.spacing(np.abs(Yg).astype(np.float16)).astype(np.float64)
+    err = np.abs(Yg - yo)
+    assert np.all(err <= half_ulp + _fp32_sum_bound(X, W, out)), f"product error {err.max():.3e}"
+    assert fmpq_gpu.fmpq_device_status(layout) == 0
+    layout.close()
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("M,K_base,n_out,N", [(256, 1024, 128, 512), (37, 512, 256, 272), (1, 384, 64, 1024)])
 def test_outlier_split_end_to_end(fmpq_gpu, oracle_mod, M, K_base, n_out, N):
@@ -83,13 +113,14 @@ def test_outlier_split_end_to_end(fmpq_gpu, oracle_mod, M, K_base, n_out, N):
     assert err <= Y_TOL, f"INT4 path relative error {err:.3e}"
     cols = torch.from_numpy(out).cuda()
     W_out = torch.from_numpy(np.ascontiguousarray(W[:, out])).cuda()
-    fmpq_gpu.fmpq_outlier_gemm_fp16(Xd, cols, W_out, Y)
-    # merge: the FP16 outlier product and the sum are each rounded to fp16, so the merged output
-    # is within one fp16 ulp of the product plus one of the result of base output + exact product
-    Ym = Y.cpu().numpy()
-    ulp = lambda v: np.spacing(np.abs(v).astype(np.float16)).astype(np.float64)
-    err = np.abs(Ym.astype(np.float64) - (Y_base.astype(np.float64) + yo))
-    assert np.all(err <= ulp(yo) + ulp(Ym)), f"merge error {err.max():.3e}"
+    fmpq_gpu.fmpq_outlier_gemm_fp16(layout, Xd, cols, W_out, Y)
+    # merge, element by element against the oracle's exact outlier product: the FP32 sum of the
+    # product and the fp16 base output, rounded once to fp16
+    Ym = Y.cpu().numpy().astype(np.float64)
+    half_ulp = 0.5 * np.spacing(np.abs(Ym).astype(np.float16)).astype(np.float64)
+    bound = half_ulp + _fp32_sum_bound(X, W, out) + 2.0 ** -24 * (np.abs(Y_base.astype(np.float64)) + np.abs(yo))
+    err = np.abs(Ym - (Y_base.astype(np.float64) + yo))
+    assert np.all(err <= bound), f"merge error {err.max():.3e}"
     assert fmpq_gpu.fmpq_device_status(layout) == 0
     layout.close()
 
@@ -100,7 +131,9 @@ def test_outlier_split_argument_errors(fmpq_gpu):
     X = torch.zeros((4, 256), dtype=torch.float16, device="cuda")
     Y = torch.zeros((4, 64), dtype=torch.float16, device="cuda")
     W_out = torch.zeros((64, 16), dtype=torch.float16, device="cuda")
+    layout = fmpq_gpu.select_layout(128, 256, np.arange(128, dtype=np.int32), np.zeros(1, np.uint8))
     with pytest.raises(fmpq_gpu.FmpqError):       # 12 outlier columns: not a multiple of 8
-        fmpq_gpu.fmpq_outlier_gemm_fp16(X, torch.zeros(12, dtype=torch.int32, device="cuda"), W_out, Y)
+        fmpq_gpu.fmpq_outlier_gemm_fp16(layout, X, torch.zeros(12, dtype=torch.int32, device="cuda"), W_out, Y)
+    layout.close()
     with pytest.raises(fmpq_gpu.FmpqError):       # a selection with a repeated channel
         fmpq_gpu.select_layout(128, 256, np.zeros(128, np.int32), np.zeros(1, np.uint8))

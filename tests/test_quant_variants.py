@@ -432,7 +432,7 @@ def test_quik_whole_path(fmpq_gpu, oracle_mod):
     """QUIK end to end (QUIK explainer, "第二步: 前向传播" and "反量化背后的数学"): base columns
     through asymmetric INT4 (a layout selecting them from the full rows), outlier columns in
     FP16, the two results added in Y. Each part against its exact value: the INT4 output within
-    the output tolerance, the merge within one fp16 rounding of each part."""
+    the output tolerance, the merge within one fp16 rounding and the FP32 summation bound."""
     import torch
     from tests.gpu_helpers import Y_TOL, to_dev, y_error
     M, N, K_in, n_out = 200, 512, 2048, 128
@@ -452,13 +452,16 @@ def test_quik_whole_path(fmpq_gpu, oracle_mod):
     Y = fmpq_gpu.w4ax_gemm_asym(layout, A, sx, z, Wp, sw, wsum, M, N)
     Y_base = Y.cpu().numpy().astype(np.float64)
     W_out = Wd[:, torch.from_numpy(out_cols).long().cuda()].contiguous()
-    fmpq_gpu.fmpq_outlier_gemm_fp16(Xd, to_dev(out_cols), W_out, Y)
+    fmpq_gpu.fmpq_outlier_gemm_fp16(layout, Xd, to_dev(out_cols), W_out, Y)
     Ym = Y.cpu().numpy().astype(np.float64)
     ref = oracle_mod.asym_reference(X[:, base], W[:, base], np.arange(K, dtype=np.int32))
     assert y_error(Y_base, ref["Y"]) <= Y_TOL
-    yo = X[:, out_cols].astype(np.float64) @ W[:, out_cols].astype(np.float64).T
-    ulp = lambda v: np.spacing(np.abs(v).astype(np.float16)).astype(np.float64)
-    assert np.all(np.abs(Ym - (Y_base + yo)) <= ulp(yo) + ulp(Ym))
+    _, yo = oracle_mod.quik_reference(X, W, base, out_cols)
+    # one fp16 rounding of (fp16 base output + FP32 sum of the outlier products)
+    Xo, Wo = np.abs(X[:, out_cols].astype(np.float64)), np.abs(W[:, out_cols].astype(np.float64))
+    bound = (0.5 * np.spacing(np.abs(Ym).astype(np.float16)).astype(np.float64) + n_out * 2.0 ** -24 * (Xo @ Wo.T)
+             + 2.0 ** -24 * (np.abs(Y_base) + np.abs(yo)))
+    assert np.all(np.abs(Ym - (Y_base + yo)) <= bound)
     layout.close()
 
 

@@ -29,7 +29,8 @@ def fmpq_mod():
 @pytest.mark.parametrize("M,N,K,n8,split", [
     (16, 512, 2048, 2, True),     # few output tiles: split-K, the workspace comes from the fixed array
     (1, 1024, 4096, 3, True),     # one token, split-K
-    (300, 784, 1024, 2, False),   # enough tiles: no workspace needed
+    (300, 784, 1024, 2, True),    # 8 output tiles: split-K
+    (1024, 2560, 512, 1, False),  # 40 output tiles: no workspace needed
 ])
 def test_noalloc_matches_gemm(fmpq_mod, oracle_mod, M, N, K, n8, split):
     w = wl.synthetic(M, N, K, n8=n8, seed=M * 7 + N + K)
