@@ -461,6 +461,23 @@ fmpq_status fmpq_plan_layout(int32_t K, const uint32_t* absmax_host, int32_t n8,
     return FMPQ_OK;
 }
 
+fmpq_status fmpq_plan_layout_budget(int32_t K, const uint32_t* absmax_host, const void* X_calib_host, int64_t T,
+                                    int64_t ldx, double eps, int32_t* n8_out, double* err_out, int32_t* perm_host,
+                                    uint8_t* mask_host) {
+    if (absmax_host == nullptr || X_calib_host == nullptr || n8_out == nullptr || err_out == nullptr ||
+        perm_host == nullptr || mask_host == nullptr)
+        return FMPQ_ERR_INVALID_ARG;
+    if (K < FMPQ_BLOCK || K > FMPQ_MAX_K || K % FMPQ_BLOCK != 0 || T < 1 || ldx < K) return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (!(eps >= 0.0) || !std::isfinite(eps)) return FMPQ_ERR_INVALID_ARG;
+    try {
+        *n8_out = fmpq::plan_layout_budget(K, absmax_host, static_cast<const uint16_t*>(X_calib_host), T, ldx, eps,
+                                           err_out, perm_host, mask_host);
+    } catch (const std::bad_alloc&) {
+        return FMPQ_ERR_INVALID_ARG;
+    }
+    return FMPQ_OK;
+}
+
 int32_t fmpq_outlier_blocks(int32_t K, double fraction) {
     if (K < FMPQ_BLOCK || K > FMPQ_MAX_K || K % FMPQ_BLOCK != 0 || !(fraction >= 0.0 && fraction <= 1.0)) return -1;
     const long long n_out = std::llround(fraction * K);

@@ -10,8 +10,12 @@
 //                          a slice of the tokens with 16-byte loads (8 channels per thread) and
 //                          folds its maxima into the output with one atomicMax per channel.
 //   plan_layout            host: rank the channels, fill the last n8 blocks with the top ones.
+//   plan_layout_budget     host: the fewest INT8 blocks whose layout keeps the calibration
+//                          tokens' relative quantization error within a budget.
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <numeric>
 #include <vector>
@@ -95,6 +99,69 @@ void plan_layout(int K, const uint32_t* absmax, int n8, int32_t* perm, uint8_t* 
         if (!top[c]) perm[j++] = c;              // INT4 blocks: the other channels, in order
     for (int i = 0; i < n_top; ++i) perm[j++] = rank[i];   // the last n8 blocks, by rank
     for (int b = 0; b < nb; ++b) mask[b] = b >= nb - n8 ? 1 : 0;
+}
+
+namespace {
+
+// x * 2^24 for a finite fp16 bit pattern: |x| = mant * 2^(max(e,1) - 25), so x * 2^24 is the
+// integer mant * 2^(max(e,1) - 1), below 2^40.
+int64_t fp16_fixed24(uint16_t h) {
+    const int e = (h >> 10) & 31;
+    const int64_t mant = (h & 1023) + (e != 0 ? 1024 : 0);
+    const int64_t v = mant << (e > 0 ? e - 1 : 0);
+    return (h & 0x8000u) != 0 ? -v : v;
+}
+
+float fp16_value(uint16_t h) {
+    __half_raw r;
+    r.x = h;
+    return __half2float(__half(r));
+}
+
+}  // namespace
+
+double layout_error(int K, const uint16_t* Xc, int64_t T, int64_t ldx, const int32_t* perm, const uint8_t* mask) {
+    const int nb = K / kBlock;
+    double worst = 0.0;
+    for (int64_t t = 0; t < T; ++t) {
+        const uint16_t* row = Xc + t * ldx;
+        unsigned __int128 err2 = 0, norm2 = 0;   // exact, in units of 2^-48
+        for (int b = 0; b < nb; ++b) {
+            const int32_t* ch = perm + static_cast<int64_t>(b) * kBlock;
+            // the activation quantizer's rule: s = fp16_rn(fp32(absmax) / qmax),
+            // q = clamp(rne(fp32(x) / fp32(s)), -qmax, qmax), q = 0 for a zero scale
+            uint16_t amax = 0;
+            for (int j = 0; j < kBlock; ++j) amax = std::max<uint16_t>(amax, row[ch[j]] & 0x7FFFu);
+            const int qmax = mask[b] ? 127 : 7;
+            const __half_raw s16 = __half(__float2half_rn(fp16_value(amax) / static_cast<float>(qmax)));
+            const float s = fp16_value(s16.x);
+            const int64_t s24 = fp16_fixed24(s16.x);
+            for (int j = 0; j < kBlock; ++j) {
+                const uint16_t h = row[ch[j]];
+                int64_t q = 0;
+                if (s != 0.0f) {
+                    q = static_cast<int64_t>(std::nearbyint(fp16_value(h) / s));
+                    q = std::min<int64_t>(qmax, std::max<int64_t>(-qmax, q));
+                }
+                const int64_t x24 = fp16_fixed24(h);
+                const int64_t d24 = x24 - q * s24;   // x - q*s, exact
+                err2 += static_cast<unsigned __int128>(static_cast<__int128>(d24) * d24);
+                norm2 += static_cast<unsigned __int128>(static_cast<__int128>(x24) * x24);
+            }
+        }
+        if (norm2 != 0) worst = std::max(worst, std::sqrt(static_cast<double>(err2) / static_cast<double>(norm2)));
+    }
+    return worst;
+}
+
+int plan_layout_budget(int K, const uint32_t* absmax, const uint16_t* Xc, int64_t T, int64_t ldx, double eps,
+                       double* err, int32_t* perm, uint8_t* mask) {
+    const int nb = K / kBlock;
+    for (int n8 = 0;; ++n8) {
+        plan_layout(K, absmax, n8, perm, mask);
+        *err = layout_error(K, Xc, T, ldx, perm, mask);
+        if (*err <= eps || n8 == nb) return n8;
+    }
 }
 
 }  // namespace fmpq

@@ -99,6 +99,12 @@ cudaError_t launch_outlier_gemm(const void* X, int64_t ldx, int64_t M, const int
 cudaError_t launch_channel_absmax(const void* X, int64_t ldx, int64_t T, int K, uint32_t* out, int num_sms,
                                   cudaStream_t stream);
 void plan_layout(int K, const uint32_t* absmax, int n8, int32_t* perm, uint8_t* mask);
+// Largest relative quantization error ||x - xhat|| / ||x|| over T calibration tokens (fp16,
+// host, [T][ldx]) under a layout; and the smallest n8 whose planned layout keeps it within eps
+// (K/128 when none does), writing that layout and its error.
+double layout_error(int K, const uint16_t* Xc, int64_t T, int64_t ldx, const int32_t* perm, const uint8_t* mask);
+int plan_layout_budget(int K, const uint32_t* absmax, const uint16_t* Xc, int64_t T, int64_t ldx, double eps,
+                       double* err, int32_t* perm, uint8_t* mask);
 
 // Few tokens (M <= 128): the operand-swapped GEMM (output channels on the tensor core's M side,
 // tokens on its N side). launch_gemm and the workspace queries dispatch to it.

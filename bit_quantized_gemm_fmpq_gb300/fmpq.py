@@ -59,6 +59,7 @@ SIGNATURES = {
     "fmpq_outlier_gemm_fp16": (_I32, [_P, _P, _I64, _I64, _P, _I32, _P, _I64, _I64, _P, _P, _I64, _P]),
     "fmpq_channel_absmax": (_I32, [_P, _I64, _I64, _I32, _P, _P]),
     "fmpq_plan_layout": (_I32, [_I32, _P, _I32, _P, _P]),
+    "fmpq_plan_layout_budget": (_I32, [_I32, _P, _P, _I64, _I64, ctypes.c_double, _P, _P, _P, _P]),
     "fmpq_outlier_blocks": (_I32, [_I32, ctypes.c_double]),
     "fmpq_status_string": (ctypes.c_char_p, [_I32]),
     "fmpq_version": (_I32, []),
@@ -298,6 +299,23 @@ def fmpq_plan_layout(absmax, n8: int):
     _check("fmpq_plan_layout", load_library().fmpq_plan_layout(K, a.ctypes.data, n8, perm.ctypes.data,
                                                                    mask.ctypes.data))
     return perm, mask
+
+
+def fmpq_plan_layout_budget(absmax, X_calib, eps: float):
+    """Host planner with an error budget: the fewest INT8 blocks whose layout keeps the largest
+    relative quantization error of the calibration tokens X_calib (fp16 [T, K], host) within
+    eps. Returns (n8, err, perm int32 [K], mask uint8 [K/128])."""
+    a = np.ascontiguousarray(np.asarray(absmax).astype(np.uint32))
+    Xc = np.ascontiguousarray(np.asarray(X_calib, dtype=np.float16))
+    T, K = Xc.shape
+    perm = np.empty(K, dtype=np.int32)
+    mask = np.empty(K // BLOCK, dtype=np.uint8)
+    n8 = np.zeros(1, dtype=np.int32)
+    err = np.zeros(1, dtype=np.float64)
+    _check("fmpq_plan_layout_budget", load_library().fmpq_plan_layout_budget(
+        K, a.ctypes.data, Xc.ctypes.data, T, K, float(eps), n8.ctypes.data, err.ctypes.data, perm.ctypes.data,
+        mask.ctypes.data))
+    return int(n8[0]), float(err[0]), perm, mask
 
 
 def fmpq_outlier_blocks(K: int, fraction: float) -> int:

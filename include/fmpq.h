@@ -243,6 +243,25 @@ FMPQ_API fmpq_status fmpq_channel_absmax(const void* X, int64_t ldx, int64_t T, 
 FMPQ_API fmpq_status fmpq_plan_layout(int32_t K, const uint32_t* absmax_host, int32_t n8, int32_t* perm_host,
                                       uint8_t* mask_host);
 
+/* Layout with the fewest INT8 blocks that keeps the quantization error of calibration tokens
+ * within a budget (host only: no device work, callable without a GPU). The INT8 blocks are there
+ * to keep the outliers' quantization error small (COMET news article, section 1); the error of a
+ * layout on the calibration tokens is
+ *   err = max over tokens t of ||x_t - xhat_t||_2 / ||x_t||_2   (0 for an all-zero token),
+ * xhat_t the token's dequantized codes q * s under the layout (the rule of fmpq_quantize); both
+ * squared norms are summed exactly and converted once to fp64, then one fp64 division and one
+ * square root. For n8 = 0, 1, ..., K/128 the layout is fmpq_plan_layout(K, absmax_host, n8); the
+ * first whose err <= eps is written, else the one for n8 = K/128 (every block INT8).
+ *   absmax_host[K]       per-channel statistic (e.g. fmpq_channel_absmax of the same tokens).
+ *   X_calib_host         fp16 [T][ldx] calibration tokens, input channel order, T >= 1, ldx >= K.
+ *   eps                  the budget, finite and >= 0 (e.g. 0.05).
+ *   n8_out, err_out      out: the INT8 blocks chosen and that layout's err (err > eps only when
+ *                        even n8 = K/128 misses the budget).
+ *   perm_host, mask_host out: as fmpq_plan_layout. */
+FMPQ_API fmpq_status fmpq_plan_layout_budget(int32_t K, const uint32_t* absmax_host, const void* X_calib_host, int64_t T,
+                                             int64_t ldx, double eps, int32_t* n8_out, double* err_out,
+                                             int32_t* perm_host, uint8_t* mask_host);
+
 /* INT8 blocks for an outlier fraction of the channels: ceil(round(fraction * K) / 128), with
  * round taking halves away from zero, at most K/128; -1 for an invalid K or a fraction
  * outside [0, 1]. */

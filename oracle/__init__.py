@@ -59,6 +59,10 @@ def _load():
             lib.oracle_channel_absmax.argtypes = [P, i64, i32, P]
             lib.oracle_plan_layout.argtypes = [i32, P, i32, P, P]
             lib.oracle_plan_layout.restype = i32
+            lib.oracle_layout_error.argtypes = [P, i64, i32, P, P, P]
+            lib.oracle_layout_error.restype = i32
+            lib.oracle_plan_layout_budget.argtypes = [i32, P, P, i64, ctypes.c_double, P, P, P, P]
+            lib.oracle_plan_layout_budget.restype = i32
             lib.oracle_quantize_activations.argtypes = [P, i64, i32, i32, P, P, P, P, P]
             lib.oracle_quantize_activations.restype = i32
             lib.oracle_unpack_activations.argtypes = [P, P, i32, i32, P]
@@ -252,6 +256,32 @@ def plan_layout(stat, n8: int):
         raise ValueError("bad calibration arguments")
     return perm, mask
 
+
+def layout_error(Xc, perm, mask) -> float:
+    """Largest relative quantization error ||x - xhat|| / ||x|| over calibration tokens Xc
+    (fp16 [T, K], input channel order) under the layout (perm, mask)."""
+    Xc = _c(np.asarray(Xc, dtype=np.float16).view(np.uint16), np.uint16)
+    T, K = Xc.shape
+    err = np.zeros(1, dtype=np.float64)
+    if _load().oracle_layout_error(_ptr(Xc), T, K, _ptr(_c(perm, np.int32)), _ptr(_c(mask, np.uint8)), _ptr(err)) != 0:
+        raise ValueError("bad layout")
+    return float(err[0])
+
+
+def plan_layout_budget(stat, Xc, eps: float):
+    """The smallest n8 whose planned layout keeps layout_error within eps on Xc (n8 = K/128
+    when none does): returns (n8, err, perm, mask)."""
+    stat = _c(stat, np.uint32)
+    Xc = _c(np.asarray(Xc, dtype=np.float16).view(np.uint16), np.uint16)
+    T, K = Xc.shape
+    perm = np.empty(K, dtype=np.int32)
+    mask = np.empty(K // BLOCK, dtype=np.uint8)
+    n8 = np.zeros(1, dtype=np.int32)
+    err = np.zeros(1, dtype=np.float64)
+    if _load().oracle_plan_layout_budget(K, _ptr(stat), _ptr(Xc), T, ctypes.c_double(eps), _ptr(n8), _ptr(err),
+                                         _ptr(perm), _ptr(mask)) != 0:
+        raise ValueError("bad arguments")
+    return int(n8[0]), float(err[0]), perm, mask
 
 def outlier_blocks(K: int, fraction: float) -> int:
     """ceil(round(fraction*K) / 128), halves rounded away from zero, at most K/128."""

@@ -482,6 +482,74 @@ int oracle_plan_layout(int K, const uint32_t* stat, int n8, int32_t* perm, uint8
 }
 
 /* ------------------------------------------------------------------------------------
+ * Choosing the number of INT8 blocks by an error budget (COMET news article, section 1: the
+ * outlier channels, about 10% of them, are gathered into blocks that keep INT8 precision so
+ * that quantization error stays small; QUIK explainer, "第一步: 识别与重排": the outlier columns
+ * are identified offline on calibration data). The pages fix no error measure or budget; the
+ * reading taken: the error of a layout on calibration tokens is the largest, over the tokens,
+ * relative Euclidean error ||x - xhat|| / ||x|| of the token's dequantized codes xhat = q * s
+ * (0 for an all-zero token), and the planner takes the smallest n8 whose error is within eps.
+ * ------------------------------------------------------------------------------------ */
+
+/* x * 2^24 for a finite fp16 x: an integer (|x| = mant * 2^(max(e,1) - 25)). */
+static int64_t f16_times_2p24(uint16_t h) {
+    const unsigned e = (h >> 10) & 31u, f = h & 1023u;
+    const int64_t mant = e ? 1024 + (int64_t)f : (int64_t)f;
+    const int64_t v = mant << (e ? e - 1 : 0);
+    return (h & 0x8000u) ? -v : v;
+}
+
+/* err = max over the T calibration tokens (fp16 [T][K], input channel order) of
+ * sqrt(||x - xhat||^2 / ||x||^2) under the layout (perm, mask). Both squared norms are exact
+ * integers in units of 2^-48 (x and q*s are integer multiples of 2^-24), converted once to
+ * fp64; the ratio is one fp64 division and one square root. */
+int oracle_layout_error(const uint16_t* Xc, int64_t T, int K, const int32_t* perm, const uint8_t* mask, double* err) {
+    if (K <= 0 || K % ORACLE_BLOCK != 0) return -1;
+    const int nb = K / ORACLE_BLOCK;
+    double worst = 0.0;
+    for (int64_t t = 0; t < T; ++t) {
+        const uint16_t* x = Xc + t * K;
+        unsigned __int128 num = 0, den = 0;
+        for (int b = 0; b < nb; ++b) {
+            uint16_t xs[ORACLE_BLOCK];
+            int8_t q[ORACLE_BLOCK];
+            for (int j = 0; j < ORACLE_BLOCK; ++j) xs[j] = x[perm[b * ORACLE_BLOCK + j]];
+            const uint16_t s16 = quantize_block(xs, mask[b] ? 127 : 7, q);
+            const int64_t ns = f16_times_2p24(s16);
+            for (int j = 0; j < ORACLE_BLOCK; ++j) {
+                const int64_t nx = f16_times_2p24(xs[j]);
+                const int64_t nd = nx - (int64_t)q[j] * ns;
+                num += (unsigned __int128)((__int128)nd * nd);
+                den += (unsigned __int128)((__int128)nx * nx);
+            }
+        }
+        const double e = den != 0 ? sqrt((double)num / (double)den) : 0.0;
+        if (e > worst) worst = e;
+    }
+    *err = worst;
+    return 0;
+}
+
+/* The smallest n8 in [0, K/128] whose planned layout (oracle_plan_layout with that n8) has an
+ * error within eps on the calibration tokens; when none has, n8 = K/128 (every block INT8).
+ * Writes that layout, n8 and its error. */
+int oracle_plan_layout_budget(int K, const uint32_t* stat, const uint16_t* Xc, int64_t T, double eps, int32_t* n8_out,
+                              double* err_out, int32_t* perm, uint8_t* mask) {
+    if (K <= 0 || K % ORACLE_BLOCK != 0) return -1;
+    const int nb = K / ORACLE_BLOCK;
+    for (int n8 = 0;; ++n8) {
+        double e = 0.0;
+        if (oracle_plan_layout(K, stat, n8, perm, mask) != 0 || oracle_layout_error(Xc, T, K, perm, mask, &e) != 0)
+            return -1;
+        if (e <= eps || n8 == nb) {
+            *n8_out = n8;
+            *err_out = e;
+            return 0;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------------------
  * RMSNorm fused into the quantizer (QServe explainer, "运行时设计": the activation
  * quantization of the QKV projection and the first FFN layer is fused into the layer norm
  * before them; the LLaMA family's layer norm is RMSNorm, y = x / sqrt(mean(x^2) + eps) * gamma).

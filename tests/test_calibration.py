@@ -14,6 +14,108 @@ from bit_quantized_gemm_fmpq_gb300 import workloads as wl
 BLOCK = 128
 
 
+# ---------------------------------------------------------------------- error budget (CPU)
+
+def _calib_batch(T, K, seed):
+    """Laplace tokens with 10% outlier channels (x U(20, 100)), the workloads' statistics."""
+    rng = np.random.default_rng(seed)
+    X = rng.laplace(0.0, 1.0, (T, K)).astype(np.float32)
+    cols = rng.choice(K, K // 10, replace=False)
+    X[:, cols] *= rng.uniform(20.0, 100.0, cols.size).astype(np.float32)
+    return X.astype(np.float16)
+
+
+def test_oracle_layout_error_closed_form(oracle_mod):
+    """A block of ones: s = fp16(1/7) = 585 * 2^-12, so every code is 1 and x - q*s = 2^-12
+    (INT4); s = fp16(1/127) = 1032 * 2^-17 gives 2^-14 (INT8). The relative error of the token
+    is that difference, exactly."""
+    s4 = np.float16(np.float32(1) / np.float32(7))
+    s8 = np.float16(np.float32(1) / np.float32(127))
+    assert 1.0 - 7 * float(s4) == 2.0 ** -12 and 1.0 - 127 * float(s8) == 2.0 ** -14
+    X = np.ones((3, 128), dtype=np.float16)
+    ident = np.arange(128, dtype=np.int32)
+    assert oracle_mod.layout_error(X, ident, np.array([0], np.uint8)) == 2.0 ** -12
+    assert oracle_mod.layout_error(X, ident, np.array([1], np.uint8)) == 2.0 ** -14
+    X[1] = 0                                             # an all-zero token counts as 0
+    assert oracle_mod.layout_error(X, ident, np.array([0], np.uint8)) == 2.0 ** -12
+
+
+def test_oracle_layout_error_exact_codes(oracle_mod):
+    """Tokens whose blocks hold integers in [-7, 7] with a 7 in each block are represented
+    exactly by INT4 codes (s = 1): the error is 0 and the planner takes no INT8 block even for
+    eps = 0."""
+    rng = np.random.default_rng(3)
+    X = rng.integers(-7, 8, size=(5, 512)).astype(np.float16)
+    X[:, ::BLOCK] = 7
+    ident = np.arange(512, dtype=np.int32)
+    assert oracle_mod.layout_error(X, ident, np.zeros(4, np.uint8)) == 0.0
+    stat = oracle_mod.channel_absmax(X)
+    n8, err, perm, mask = oracle_mod.plan_layout_budget(stat, X, 0.0)
+    assert (n8, err) == (0, 0.0) and perm.tolist() == list(range(512))
+
+
+def test_oracle_layout_error_against_numpy(oracle_mod):
+    """The error equals the ratio of norms computed in numpy from the oracle quantizer's codes
+    and scales (dequantized q * s, fp64 norms), within fp64 summation error."""
+    X = _calib_batch(12, 2048, 4)
+    stat = oracle_mod.channel_absmax(X)
+    perm, mask = oracle_mod.plan_layout(stat, 2)
+    _, sx, Aq = oracle_mod.quantize_activations(X, perm, mask)
+    s = sx.view(np.float16).astype(np.float64)                 # [nb][T]
+    xhat = Aq.astype(np.float64) * np.repeat(s.T, BLOCK, axis=1)
+    xp = X[:, perm].astype(np.float64)
+    want = np.max(np.linalg.norm(xp - xhat, axis=1) / np.linalg.norm(xp, axis=1))
+    assert abs(oracle_mod.layout_error(X, perm, mask) - want) <= 1e-12 * want
+
+
+def test_oracle_budget_decisions(oracle_mod):
+    """One block of ones: errors 2^-12 (INT4) and 2^-14 (INT8). A budget of 2^-13 needs the INT8
+    block; 2^-12 does not; 2^-15 cannot be met, so every block is INT8 and err > eps."""
+    X = np.ones((2, 128), dtype=np.float16)
+    stat = oracle_mod.channel_absmax(X)
+    assert oracle_mod.plan_layout_budget(stat, X, 2.0 ** -13)[:2] == (1, 2.0 ** -14)
+    assert oracle_mod.plan_layout_budget(stat, X, 2.0 ** -12)[:2] == (0, 2.0 ** -12)
+    assert oracle_mod.plan_layout_budget(stat, X, 2.0 ** -15)[:2] == (1, 2.0 ** -14)
+
+
+@pytest.mark.parametrize("eps", [0.02, 0.05, 0.1])
+def test_oracle_budget_is_the_smallest(oracle_mod, eps):
+    """Brute force: the chosen n8 meets the budget and n8 - 1 does not."""
+    X = _calib_batch(16, 2048, 5)
+    stat = oracle_mod.channel_absmax(X)
+    n8, err, perm, mask = oracle_mod.plan_layout_budget(stat, X, eps)
+    assert err <= eps and err == oracle_mod.layout_error(X, perm, mask)
+    assert np.array_equal(oracle_mod.plan_layout(stat, n8)[0], perm)
+    if n8 > 0:
+        p0, m0 = oracle_mod.plan_layout(stat, n8 - 1)
+        assert oracle_mod.layout_error(X, p0, m0) > eps
+
+
+@pytest.mark.parametrize("T,K,eps", [(32, 8192, 0.03), (32, 8192, 0.06), (8, 4096, 0.0), (64, 1024, 0.08)])
+def test_library_budget_planner_matches_oracle(T, K, eps, oracle_mod):
+    """The library's host planner (C ABI, no GPU needed) bit-exact against the oracle: n8, the
+    error (the same fp64 value), the permutation and the mask."""
+    from bit_quantized_gemm_fmpq_gb300 import fmpq
+    fmpq.load_library()
+    X = _calib_batch(T, K, T + K)
+    stat = oracle_mod.channel_absmax(X)
+    want = oracle_mod.plan_layout_budget(stat, X, eps)
+    got = fmpq.fmpq_plan_layout_budget(stat, X, eps)
+    assert got[:2] == want[:2]
+    assert np.array_equal(got[2], want[2]) and np.array_equal(got[3], want[3])
+
+
+def test_library_budget_planner_closed_form():
+    from bit_quantized_gemm_fmpq_gb300 import fmpq
+    fmpq.load_library()
+    X = np.ones((2, 128), dtype=np.float16)
+    stat = np.full(128, 0x3C00, dtype=np.uint32)
+    assert fmpq.fmpq_plan_layout_budget(stat, X, 2.0 ** -13)[:2] == (1, 2.0 ** -14)
+    assert fmpq.fmpq_plan_layout_budget(stat, X, 2.0 ** -12)[:2] == (0, 2.0 ** -12)
+    with pytest.raises(fmpq.FmpqError):
+        fmpq.fmpq_plan_layout_budget(stat, X, -1.0)
+
+
 # ---------------------------------------------------------------------- oracle pins (CPU)
 
 def test_oracle_absmax_planted_maxima(oracle_mod):
