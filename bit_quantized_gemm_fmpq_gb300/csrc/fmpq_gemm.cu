@@ -73,14 +73,15 @@ struct __align__(1024) Smem {
     int32_t poff[kMaxBlocks];            // first code plane of each block
     uint8_t mask[kMaxBlocks];            // 1 = INT8 block (two planes)
     uint32_t maskw[kMaxBlocks / 32];     // the same, one bit per block
-    // blk_full[b % kBlk]: block b's operands are in place in this CTA -- the activation
-    //   planes (bulk-copy bytes), the converted weight tile (converter warps). In the even
-    //   CTA it also gathers everything else the MMAs of block b wait for: the odd CTA's
-    //   operands (one forwarded arrival) and the accumulator they overwrite (the epilogue
-    //   warps of both CTAs, done with block b - 2). One wait per block for the issuer.
+    // a_full[b % kBlk]: block b's activation planes have landed here (bulk-copy bytes only,
+    //   so a drain after an abort can always wait for the copies in flight).
+    // blk_full[b % kBlk]: block b's converted weight tile and scales are staged here
+    //   (converter warps). In the even CTA it also gathers everything else the MMAs of block b
+    //   wait for: the odd CTA's operands (one forwarded arrival) and the accumulator they
+    //   overwrite (the epilogue warps of both CTAs, done with block b - 2).
     // blk_empty[b % kBlk]: block b's MMAs have finished (its activation slots and converted
     //   weight slot may be reused); committed by the even CTA to both CTAs.
-    uint64_t blk_full[kBlk], blk_empty[kBlk];
+    uint64_t a_full[kBlk], blk_full[kBlk], blk_empty[kBlk];
     uint64_t w_full[kWStages], w_empty[kWStages];
     uint64_t sc_full[kScStages], sc_empty[kScStages];
     uint64_t acc_full[2];
@@ -215,7 +216,7 @@ __device__ __forceinline__ void activation_producer(const Params& p, Smem& s, ui
                                                                 (static_cast<uint32_t>(last) / kBlk) & 1, abort_flag));
             }
             if (!ok) break;
-            uint64_t* bar = &s.blk_full[it % kBlk];
+            uint64_t* bar = &s.a_full[it % kBlk];
             if (lane == 0) dev::mbar_arrive_expect_tx(bar, abytes * planes);   // rows past M: nothing to copy
             const uint8_t* a0 = p.A + static_cast<int64_t>(s.poff[b]) * plane_bytes + static_cast<int64_t>(r0) * kBlock;
             for (int pl = 0; pl < planes; ++pl, ++pc) {
@@ -229,22 +230,22 @@ __device__ __forceinline__ void activation_producer(const Params& p, Smem& s, ui
         }
     }
     if (!ok && lane == 0) fail(p, abort_flag);
-    // drain copies in flight: the last blocks' blk_full phases (they complete with the copies)
+    // drain copies in flight: a_full completes on the copies' bytes alone
     if (lane == 0) {
         for (uint32_t k = 0; k < kBlk && k < it; ++k) {
             const uint32_t b = it - 1 - k;
-            dev::mbar_wait(&s.blk_full[b % kBlk], (b / kBlk) & 1, nullptr);
+            dev::mbar_wait(&s.a_full[b % kBlk], (b / kBlk) & 1, nullptr);
         }
     }
     __syncwarp();
 }
 
 // ---------------------------------------------------------------- MMA issuer / forwarder (warp 1)
-// Even CTA: per block, waits for blk_full (both CTAs' operands and the free accumulator),
-// issues the pair MMAs and commits blk_empty and acc_full to both CTAs. Odd CTA: forwards
-// blk_full. This warp's time per block lies on the loop through the two accumulators
-// (MMAs -> epilogue -> release -> next MMAs), so it does one mbarrier wait per block and
-// reads the INT8 mask one 32-bit word per 32 blocks.
+// Even CTA: per block, waits for its planes (a_full) and blk_full (its converted weights, the
+// odd CTA's forward and the free accumulator), issues the pair MMAs and commits blk_empty and
+// acc_full to both CTAs. Odd CTA: forwards a_full + blk_full. This warp's time per block lies
+// on the loop through the two accumulators (MMAs -> epilogue -> release -> next MMAs); the
+// INT8 mask is read one 32-bit word per 32 blocks.
 __device__ __forceinline__ void mma_role(const Params& p, Smem& s, uint32_t rank, int lane, uint32_t tmem,
                                          volatile int* abort_flag) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
@@ -257,7 +258,8 @@ __device__ __forceinline__ void mma_role(const Params& p, Smem& s, uint32_t rank
             if (b == t.b0 || (b & 31) == 0) mw = s.maskw[b >> 5];
             const int planes = 1 + static_cast<int>((mw >> (b & 31)) & 1u);
             // the whole warp waits (converged); lane 0 issues
-            ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&s.blk_full[it % kBlk], (it / kBlk) & 1, abort_flag));
+            ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&s.a_full[it % kBlk], (it / kBlk) & 1, abort_flag) &&
+                                             dev::mbar_wait(&s.blk_full[it % kBlk], (it / kBlk) & 1, abort_flag));
             if (!ok) break;
             if (rank != 0) {
                 // odd CTA: this block's operands are in place here; tell the even CTA
@@ -611,9 +613,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) w4ax_ge
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kBlk; ++i) {
-            // producer (expect-tx arrival) + converter warps; in the even CTA also the odd
-            // CTA's forward and both CTAs' epilogue warps (accumulator released)
-            dev::mbar_init(&s.blk_full[i], 1 + kConvWarps + (rank == 0 ? 1 + 2 * kEpiWarps : 0));
+            dev::mbar_init(&s.a_full[i], 1);   // the producer's expect-tx arrival
+            // converter warps; in the even CTA also the odd CTA's forward and both CTAs'
+            // epilogue warps (accumulator released)
+            dev::mbar_init(&s.blk_full[i], kConvWarps + (rank == 0 ? 1 + 2 * kEpiWarps : 0));
             dev::mbar_init(&s.blk_empty[i], 1);
         }
         for (int i = 0; i < kWStages; ++i) {
