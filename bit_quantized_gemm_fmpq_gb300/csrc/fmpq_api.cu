@@ -257,6 +257,37 @@ fmpq_status w4ax_gemm_partials(const fmpq_layout* L, const void* A_packed, const
     return launched(fmpq::launch_gemm(*L, a, static_cast<cudaStream_t>(stream)));
 }
 
+fmpq_status w4ax_gemm_fault_test(const fmpq_layout* L, const void* A_packed, const void* a_scales, const void* W_packed,
+                                 const void* w_scales, int64_t M, int64_t N, void* Y, int64_t ldy, void* workspace,
+                                 size_t workspace_bytes, int32_t withhold_copy, uint32_t poll_limit, void* stream) {
+    if (L == nullptr || A_packed == nullptr || a_scales == nullptr || W_packed == nullptr || w_scales == nullptr ||
+        Y == nullptr)
+        return FMPQ_ERR_INVALID_ARG;
+    if (M <= 128 || M > INT32_MAX || N < 16 || N % 16 != 0 || N > INT32_MAX || ldy < N)
+        return FMPQ_ERR_UNSUPPORTED_SHAPE;   // the few-token kernel has no such test hook
+    if (withhold_copy < 0 || withhold_copy >= L->nb || poll_limit < 1024) return FMPQ_ERR_INVALID_ARG;
+    if (ldy % 8 != 0 || !aligned16(A_packed) || !aligned16(a_scales) || !aligned16(W_packed) ||
+        !aligned16(w_scales) || !aligned16(Y))
+        return FMPQ_ERR_MISALIGNED;
+    const size_t need = fmpq::gemm_workspace_bytes(*L, M, N);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return FMPQ_ERR_WORKSPACE;
+    if (fmpq_status st = check_device(L)) return st;
+    fmpq::GemmArgs a{};
+    a.A = A_packed;
+    a.a_scales = a_scales;
+    a.W = W_packed;
+    a.w_scales = w_scales;
+    a.M = M;
+    a.N = N;
+    a.Y = Y;
+    a.ldy = ldy;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    a.withhold = withhold_copy;
+    a.poll_limit = poll_limit;
+    return launched(fmpq::launch_gemm(*L, a, static_cast<cudaStream_t>(stream)));
+}
+
 // ---- quantization variants: QUIK asymmetric activations, QoQ progressive group quantization
 
 size_t fmpq_variant_gemm_workspace_bytes(const fmpq_layout* L, int64_t M, int64_t N) {

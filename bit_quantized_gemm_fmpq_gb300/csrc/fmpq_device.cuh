@@ -45,10 +45,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete. Returns false if it did not
-// complete within kMaxPolls polls, or if *abort (when given) became nonzero meanwhile.
+// complete within max_polls polls, or if *abort (when given) became nonzero meanwhile.
 // Drains of copies in flight pass abort = nullptr so they always wait for completion.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort) {
-    for (uint32_t i = 0; i < kMaxPolls; ++i) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort,
+                                          uint32_t max_polls = kMaxPolls) {
+    for (uint32_t i = 0; i < max_polls; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if (abort != nullptr && (i & 255u) == 255u && *abort) return false;
     }

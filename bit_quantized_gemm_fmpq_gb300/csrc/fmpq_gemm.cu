@@ -119,6 +119,10 @@ struct Params {
     const uint16_t* ch_scales;
     const uint8_t* grp_scales;
     const uint8_t* grp_zeros;
+    // failure-detection test: polls before a device wait gives up, and the index of the packed
+    // weight copy the first CTA withholds (-1: none)
+    uint32_t poll_limit;
+    int withhold;
 };
 
 // Codes 0-3 and 4-7 of a packed word as operand bytes. Sign-magnitude words keep |q| in bits
@@ -158,7 +162,7 @@ __device__ __forceinline__ void fail(const Params& p, volatile int* abort_flag) 
 // streams this CTA's 128 activation rows of each block's plane(s). Separate threads, so the
 // activation prefetch depth is set by its own ring, not by the weight conversion.
 __device__ __forceinline__ void weight_producer(const Params& p, Smem& s, uint32_t rank, int lane,
-                                                volatile int* abort_flag) {
+                                                volatile int* abort_flag, uint32_t polls, int withhold) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
     uint32_t wc = 0;
     bool ok = true;
@@ -167,9 +171,11 @@ __device__ __forceinline__ void weight_producer(const Params& p, Smem& s, uint32
         for (int b = t.b0; b < t.b1; ++b, ++wc) {
             const int ws = wc % kWStages;
             // the whole warp waits (converged); lane 0 issues
-            ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&s.w_empty[ws], ((wc / kWStages) & 1) ^ 1, abort_flag));
+            ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&s.w_empty[ws], ((wc / kWStages) & 1) ^ 1, abort_flag, polls));
             if (!ok) break;
-            if (lane == 0) {
+            // (a failure-detection test withholds one copy of the first CTA: nothing is issued,
+            // so the converters' wait on it runs out)
+            if (lane == 0 && !(blockIdx.x == 0 && static_cast<int>(wc) == withhold)) {
                 dev::mbar_arrive_expect_tx(&s.w_full[ws], 128 * 64);
                 dev::bulk_g2s(s.pkW[ws], p.W + (static_cast<int64_t>(t.nt) * p.nb + b) * (256 * 64) + rank * (128 * 64),
                               128 * 64, &s.w_full[ws]);
@@ -182,14 +188,14 @@ __device__ __forceinline__ void weight_producer(const Params& p, Smem& s, uint32
         for (int ws = 0; ws < kWStages; ++ws) {   // drain copies in flight
             if (wc <= static_cast<uint32_t>(ws)) break;
             const uint32_t last = ws + ((wc - 1 - ws) / kWStages) * kWStages;
-            dev::mbar_wait(&s.w_full[ws], (last / kWStages) & 1, nullptr);
+            dev::mbar_wait(&s.w_full[ws], (last / kWStages) & 1, nullptr, polls);
         }
     }
     __syncwarp();
 }
 
 __device__ __forceinline__ void activation_producer(const Params& p, Smem& s, uint32_t rank, int lane,
-                                                    volatile int* abort_flag) {
+                                                    volatile int* abort_flag, uint32_t polls) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
     uint32_t pc = 0, it = 0;        // planes and blocks issued
     int32_t slot_block[kASlots];    // block that last used each plane slot (-1: none)
@@ -213,7 +219,7 @@ __device__ __forceinline__ void activation_producer(const Params& p, Smem& s, ui
                     if (i == sl) last = slot_block[i];
                 if (last >= 0)
                     ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&s.blk_empty[last % kBlk],
-                                                                (static_cast<uint32_t>(last) / kBlk) & 1, abort_flag));
+                                                                (static_cast<uint32_t>(last) / kBlk) & 1, abort_flag, polls));
             }
             if (!ok) break;
             uint64_t* bar = &s.a_full[it % kBlk];
@@ -234,7 +240,7 @@ __device__ __forceinline__ void activation_producer(const Params& p, Smem& s, ui
     if (lane == 0) {
         for (uint32_t k = 0; k < kBlk && k < it; ++k) {
             const uint32_t b = it - 1 - k;
-            dev::mbar_wait(&s.a_full[b % kBlk], (b / kBlk) & 1, nullptr);
+            dev::mbar_wait(&s.a_full[b % kBlk], (b / kBlk) & 1, nullptr, polls);
         }
     }
     __syncwarp();
@@ -247,7 +253,7 @@ __device__ __forceinline__ void activation_producer(const Params& p, Smem& s, ui
 // on the loop through the two accumulators (MMAs -> epilogue -> release -> next MMAs); the
 // INT8 mask is read one 32-bit word per 32 blocks.
 __device__ __forceinline__ void mma_role(const Params& p, Smem& s, uint32_t rank, int lane, uint32_t tmem,
-                                         volatile int* abort_flag) {
+                                         volatile int* abort_flag, uint32_t polls) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
     uint32_t it = 0, pc = 0, mw = 0;
     bool ok = true;
@@ -258,8 +264,8 @@ __device__ __forceinline__ void mma_role(const Params& p, Smem& s, uint32_t rank
             if (b == t.b0 || (b & 31) == 0) mw = s.maskw[b >> 5];
             const int planes = 1 + static_cast<int>((mw >> (b & 31)) & 1u);
             // the whole warp waits (converged); lane 0 issues
-            ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&s.a_full[it % kBlk], (it / kBlk) & 1, abort_flag) &&
-                                             dev::mbar_wait(&s.blk_full[it % kBlk], (it / kBlk) & 1, abort_flag));
+            ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&s.a_full[it % kBlk], (it / kBlk) & 1, abort_flag, polls) &&
+                                             dev::mbar_wait(&s.blk_full[it % kBlk], (it / kBlk) & 1, abort_flag, polls));
             if (!ok) break;
             if (rank != 0) {
                 // odd CTA: this block's operands are in place here; tell the even CTA
@@ -290,7 +296,7 @@ __device__ __forceinline__ void mma_role(const Params& p, Smem& s, uint32_t rank
     if (rank == 0 && lane == 0) {
         // every MMA issued must finish before TMEM is released
         dev::mma_commit_pair(&s.mma_done);
-        dev::mbar_wait(&s.mma_done, 0, nullptr);
+        dev::mbar_wait(&s.mma_done, 0, nullptr, polls);
     }
     __syncwarp();
 }
@@ -304,7 +310,7 @@ __device__ __forceinline__ void mma_role(const Params& p, Smem& s, uint32_t rank
 // block's scales -- entries ct, ct + 128, ct + 256 of [256 weight scales | this CTA's 128
 // activation scales] -- for the epilogue, fetched one block ahead.
 __device__ __forceinline__ void converter_role(const Params& p, Smem& s, uint32_t rank, int warp, int lane,
-                                               volatile int* abort_flag) {
+                                               volatile int* abort_flag, uint32_t polls) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
     const int ct = (warp - kConvWarp0) * 32 + lane;
     const int r0 = ct >> 2, c4 = ct & 3;
@@ -358,11 +364,11 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, uint32_
         const int ss = it % kScStages;
         // every lane waits (a converged warp polls faster than one lane with 31 parked);
         // the vote keeps the decision uniform
-        ok = dev::mbar_wait(&s.w_full[ws], (it / kWStages) & 1, abort_flag) &&
-             dev::mbar_wait(&s.sc_empty[ss], ((it / kScStages) & 1) ^ 1, abort_flag);
+        ok = dev::mbar_wait(&s.w_full[ws], (it / kWStages) & 1, abort_flag, polls) &&
+             dev::mbar_wait(&s.sc_empty[ss], ((it / kScStages) & 1) ^ 1, abort_flag, polls);
         if (ok && it >= static_cast<uint32_t>(kCvStages)) {   // converted slot: MMAs of block it - kCvStages done
             const uint32_t prev = it - kCvStages;
-            ok = dev::mbar_wait(&s.blk_empty[prev % kBlk], (prev / kBlk) & 1, abort_flag);
+            ok = dev::mbar_wait(&s.blk_empty[prev % kBlk], (prev / kBlk) & 1, abort_flag, polls);
         }
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok) break;
@@ -427,7 +433,7 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, uint32_
 // row0 col0, row0 col1, row1 col0, row1 col1).
 template <bool kPartials, bool kZero>
 __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, uint32_t rank, int warp, int lane,
-                                              uint32_t tmem, volatile int* abort_flag) {
+                                              uint32_t tmem, volatile int* abort_flag, uint32_t polls) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
     const int ew = warp - 8;                         // 0..7
     const int q = warp & 3;                          // TMEM lane quarter of this warp
@@ -456,8 +462,8 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, uint32_t
             if (ok) {
                 // every lane waits (each acquires the scales it reads); the vote keeps the
                 // decision uniform
-                ok = dev::mbar_wait(&s.sc_full[ss], (v / kScStages) & 1, abort_flag) &&
-                     dev::mbar_wait(&s.acc_full[ab], (v >> 1) & 1, abort_flag);
+                ok = dev::mbar_wait(&s.sc_full[ss], (v / kScStages) & 1, abort_flag, polls) &&
+                     dev::mbar_wait(&s.acc_full[ab], (v >> 1) & 1, abort_flag, polls);
                 ok = __all_sync(0xFFFFFFFFu, ok);
             }
             const ScaleSlot& sl = s.sc[ss];
@@ -604,7 +610,9 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, uint32_t
     if (!ok && lane == 0) fail(p, abort_flag);
 }
 
-template <bool kPartials, bool kZero>
+// kTest: the failure-detection test instantiation (runtime poll bound, a withheld weight copy);
+// the others bound every wait by the compile-time dev::kMaxPolls.
+template <bool kPartials, bool kZero, bool kTest = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) w4ax_gemm_kernel(const Params p) {
     extern __shared__ uint8_t smem_raw[];
     Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -653,21 +661,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) w4ax_ge
     dev::tc_fence_after();
     const uint32_t tmem = s.tmem_base;
     volatile int* abort_flag = &s.abort_flag;
+    const uint32_t polls = kTest ? p.poll_limit : dev::kMaxPolls;
+    const int withhold = kTest ? p.withhold : -1;
 
     if (warp < 8) {
         dev::setmaxnreg_dec<64>();
         if (warp == 0) {
-            weight_producer(p, s, rank, lane, abort_flag);
+            weight_producer(p, s, rank, lane, abort_flag, polls, withhold);
         } else if (warp == 1) {
-            mma_role(p, s, rank, lane, tmem, abort_flag);
+            mma_role(p, s, rank, lane, tmem, abort_flag, polls);
         } else if (warp < kConvWarp0 + kConvWarps) {
-            converter_role(p, s, rank, warp, lane, abort_flag);
+            converter_role(p, s, rank, warp, lane, abort_flag, polls);
         } else if (warp == 6) {
-            activation_producer(p, s, rank, lane, abort_flag);
+            activation_producer(p, s, rank, lane, abort_flag, polls);
         }
     } else {
         dev::setmaxnreg_inc<192>();
-        epilogue_role<kPartials, kZero>(p, s, rank, warp, lane, tmem, abort_flag);
+        epilogue_role<kPartials, kZero>(p, s, rank, warp, lane, tmem, abort_flag, polls);
     }
 
     dev::tc_fence_before();
@@ -735,8 +745,9 @@ size_t gemm_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N, bool var
 
 cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& a, cudaStream_t stream) {
     const bool variant = a.zero_kind != kZeroNone || a.unsigned_w;
-    if (!variant && gemm_small_path(a.M)) return launch_gemm_small(L, a, stream);
-    for (auto fn : {w4ax_gemm_kernel<false, false>, w4ax_gemm_kernel<true, false>, w4ax_gemm_kernel<false, true>}) {
+    if (!variant && gemm_small_path(a.M) && a.withhold < 0) return launch_gemm_small(L, a, stream);
+    for (auto fn : {w4ax_gemm_kernel<false, false>, w4ax_gemm_kernel<true, false>, w4ax_gemm_kernel<false, true>,
+                    w4ax_gemm_kernel<false, false, true>}) {
         const cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(fn), static_cast<int>(kSmemBytes));
         if (e != cudaSuccess) return e;
     }
@@ -761,6 +772,8 @@ cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& a, cudaStream_t st
     p.ch_scales = static_cast<const uint16_t*>(a.ch_scales);
     p.grp_scales = a.grp_scales;
     p.grp_zeros = a.grp_zeros;
+    p.poll_limit = a.poll_limit != 0 ? a.poll_limit : dev::kMaxPolls;
+    p.withhold = a.withhold;
     const bool partials = a.P != nullptr;
     if (partials) {
         p.mt0 = static_cast<int>(a.pm0 / kPairM);
@@ -789,7 +802,9 @@ cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& a, cudaStream_t st
     const int64_t units = static_cast<int64_t>(p.mtiles) * p.ntiles * p.splits;
     const int pairs = static_cast<int>(units < max_pairs(L) ? units : max_pairs(L));
     const int grid = 2 * pairs;   // clusters of two CTAs (one pair per two SMs)
-    if (partials)
+    if (a.withhold >= 0)
+        w4ax_gemm_kernel<false, false, true><<<grid, kThreads, kSmemBytes, stream>>>(p);
+    else if (partials)
         w4ax_gemm_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(p);
     else if (a.zero_kind != kZeroNone)
         w4ax_gemm_kernel<false, true><<<grid, kThreads, kSmemBytes, stream>>>(p);

@@ -79,6 +79,10 @@ struct GemmArgs {
     const void* ch_scales = nullptr;
     const uint8_t* grp_scales = nullptr;
     const uint8_t* grp_zeros = nullptr;
+    // failure-detection test (2-SM kernel only): polls before a device wait gives up (0: the
+    // default bound) and the packed weight copy the first CTA withholds (-1: none)
+    uint32_t poll_limit = 0;
+    int withhold = -1;
 };
 
 // Workspace of a split-K launch: FP32 partial tiles followed by the arrival counters

@@ -43,6 +43,7 @@ SIGNATURES = {
     "w4ax_gemm_workspace_bytes": (_SZ, [_P, _I64, _I64]),
     "w4ax_gemm": (_I32, [_P, _P, _P, _P, _P, _I64, _I64, _P, _I64, _P, _SZ, _P]),
     "w4ax_gemm_noalloc": (_I32, [_P, _P, _P, _P, _P, _I64, _I64, _P, _I64, _P]),
+    "w4ax_gemm_fault_test": (_I32, [_P, _P, _P, _P, _P, _I64, _I64, _P, _I64, _P, _SZ, _I32, ctypes.c_uint32, _P]),
     "w4ax_gemm_partials": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P]),
     "fmpq_device_status": (_I32, [_P, ctypes.POINTER(_I32), _I32]),
     "fmpq_rmsnorm_quantize": (_I32, [_P, _P, _I64, _I64, _P, ctypes.c_float, _P, _P, _P]),
@@ -240,6 +241,22 @@ def w4ax_gemm(layout: Layout, A_packed, a_scales, W_packed, w_scales, M: int, N:
     _check("w4ax_gemm", layout._lib.w4ax_gemm(layout.handle, _ptr(A_packed), _ptr(a_scales), _ptr(W_packed),
                                                 _ptr(w_scales), M, N, _ptr(Y), Y.stride(0), _ptr(workspace),
                                                 ws_bytes, _stream(stream)))
+    return Y
+
+
+def w4ax_gemm_fault_test(layout: Layout, A_packed, a_scales, W_packed, w_scales, M: int, N: int, withhold_copy: int,
+                         poll_limit: int, Y=None, workspace=None, stream=None):
+    """Debug/test of failure detection: w4ax_gemm with one packed weight copy of the first CTA
+    withheld and every device wait bounded by poll_limit polls; records FMPQ_ERR_TIMEOUT."""
+    import torch
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float16, device=A_packed.device)
+    if workspace is None:
+        workspace = layout.workspace(M, N)
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    _check("w4ax_gemm_fault_test", layout._lib.w4ax_gemm_fault_test(
+        layout.handle, _ptr(A_packed), _ptr(a_scales), _ptr(W_packed), _ptr(w_scales), M, N, _ptr(Y), Y.stride(0),
+        _ptr(workspace), ws_bytes, int(withhold_copy), int(poll_limit), _stream(stream)))
     return Y
 
 

@@ -198,6 +198,18 @@ FMPQ_API fmpq_status w4ax_gemm_partials(const fmpq_layout* layout, const void* A
                                int64_t mcount, int64_t n0, int64_t ncount, int32_t* P,
                                void* stream);
 
+/* Debug/test of failure detection: w4ax_gemm (M > 128, the 2-SM kernel) in which the first
+ * CTA's weight producer never issues its withhold_copy-th packed weight copy (counted from 0,
+ * < K/128), and every device-side wait gives up after poll_limit polls (>= 1024). The wait on
+ * the missing copy runs out, the kernel's roles leave their loops, wait for the copies they did
+ * issue and release TMEM; the call records FMPQ_ERR_TIMEOUT in the layout's device status word
+ * and Y is unspecified. Nothing faults or hangs; the next normal call is unaffected (a split-K
+ * workspace's counters still return to zero). Other arguments as w4ax_gemm. */
+FMPQ_API fmpq_status w4ax_gemm_fault_test(const fmpq_layout* layout, const void* A_packed, const void* a_scales,
+                                          const void* W_packed, const void* w_scales, int64_t M, int64_t N, void* Y,
+                                          int64_t ldy, void* workspace, size_t workspace_bytes,
+                                          int32_t withhold_copy, uint32_t poll_limit, void* stream);
+
 /* The FP16 path of an outlier split (QUIK explainer, "第二步: 前向传播": the outlier columns are
  * multiplied in FP16 by the unquantized outlier weights and added to the INT4 path's result):
  *   X_out[m][j] = X[m][cols[j]]   (0 for an index outside [0, ldx))
