@@ -618,7 +618,7 @@ def main():
         "gemm": {"ms": gemm_ms, "tflops_effective": gemm_tflops, "frac_fp8_peak": gemm_tflops / fp8_peak},
         "quantizer": {"ms": quant_ms, "gbs": quant_gbs, "frac_hbm": quant_gbs / peaks["hbm_gbs"],
                       "bytes": quant_bytes, "bytes_basis": "2MK + M(K4/2 + K8) + 2M*nb (algorithmic)",
-                      "bytes_moved": quant_moved},
+                      "bytes_moved": quant_moved, "traffic": recorded_traffic("fmpq_quantize")},
         "offline_pack_ms": pack_ms,
         "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak, "unit": "TFLOP/s",
                      "frac": gemm_tflops / fp8_peak, "traffic": recorded_traffic("w4ax_gemm"),
