@@ -282,7 +282,8 @@ def run_sweep(args):
     configs += [(f"decode_m{m}", (lambda m=m: wl.decode(m))) for m in (1, 8, 16, 32, 64, 128)]
     configs += [(f"load_balance_{int(f * 100)}pct", (lambda f=f: wl.load_balance(f))) for f in (0.0, 0.10, 0.25, 0.50)]
     if args.sweep_only:
-        names = [c[0] for c in configs] + ["rmsnorm_quantize_llama70b_down", "outlier_split_llama70b_down",
+        names = [c[0] for c in configs] + ["rmsnorm_quantize_llama70b_down", "swiglu_quantize_llama70b_down",
+                                           "outlier_split_llama70b_down",
                                            "quik_asym_llama70b_down", "qoq_w4a8_llama70b_down",
                                            "calibrate_llama70b_down"]
         if args.sweep_only not in names:
@@ -369,6 +370,25 @@ def run_sweep(args):
                           "gbs": nbytes / (ms * 1e-3) / 1e9, "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm,
                           "l2": "flushed before every timed launch", "clocks": clocks}), flush=True)
         del layout
+    if not args.sweep_only or args.sweep_only == "swiglu_quantize_llama70b_down":
+        # the quantizer fused with SwiGLU on the LLaMA-70B down projection's 4096 x 28672 activations
+        w = wl.llama70b_down()
+        layout = fmpq.Layout(w.K, w.perm, w.mask)
+        rng = np.random.default_rng(8)
+        G = torch.from_numpy((rng.standard_normal((w.M, w.K)) * 2.0).astype(np.float16)).cuda()
+        U = torch.from_numpy(w.X).cuda()
+        A = torch.empty(layout.packed_a_bytes(w.M), dtype=torch.uint8, device="cuda")
+        sx = torch.empty((layout.nb, w.M), dtype=torch.float16, device="cuda")
+        sampler.start()
+        ms = timed(lambda: fmpq.fmpq_swiglu_quantize(layout, G, U, A, sx))
+        clocks = sampler.stop()
+        nbytes = quant_algorithmic_bytes(w.M, w.K, int(w.mask.sum())) + 2 * w.M * w.K   # G and U read
+        print(json.dumps({"sweep": "swiglu_quantize_llama70b_down", "M": w.M, "K": w.K, "bound": "hbm",
+                          "kernel": "swiglu_quantize_kernel", "ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9,
+                          "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm,
+                          "l2": "flushed before every timed launch", "clocks": clocks}), flush=True)
+        del layout, G, U, A, sx
+        torch.cuda.empty_cache()
     if not args.sweep_only or args.sweep_only == "outlier_split_llama70b_down":
         # outlier split: 256 outlier channels in FP16 (tensor-core kernel), the other 28416 through the INT4 path
         w = wl.llama70b_down()

@@ -181,6 +181,19 @@ fmpq_status fmpq_rmsnorm_quantize(const fmpq_layout* L, const void* X, int64_t l
                                           gamma_perm, eps));
 }
 
+fmpq_status fmpq_swiglu_quantize(const fmpq_layout* L, const void* G_perm, int64_t ldg, const void* U_perm,
+                                 int64_t ldu, int64_t M, void* A_packed, void* a_scales, void* stream) {
+    if (L == nullptr || G_perm == nullptr || U_perm == nullptr || A_packed == nullptr || a_scales == nullptr)
+        return FMPQ_ERR_INVALID_ARG;
+    if (M < 1 || M > INT32_MAX || ldg < L->K || ldu < L->K) return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (ldg % 8 != 0 || ldu % 8 != 0 || !aligned16(G_perm) || !aligned16(U_perm) || !aligned16(A_packed) ||
+        !aligned16(a_scales))
+        return FMPQ_ERR_MISALIGNED;
+    if (fmpq_status st = check_device(L)) return st;
+    return launched(fmpq::launch_swiglu_quantize(*L, G_perm, ldg, U_perm, ldu, M, A_packed, a_scales,
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
 fmpq_status w4_pack_weights(const fmpq_layout* L, const void* W, int64_t ldw, int64_t N, void* W_packed,
                             void* w_scales, void* stream) {
     if (L == nullptr || W == nullptr || W_packed == nullptr || w_scales == nullptr) return FMPQ_ERR_INVALID_ARG;

@@ -39,6 +39,9 @@ enum { kQuantSym = 0, kQuantAsym = 2, kQuantTok = 3 };
 cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, int64_t M, void* A, void* scales,
                             cudaStream_t stream, const void* gamma_perm = nullptr, float eps = 0.0f,
                             int mode = kQuantSym, void* aux = nullptr);
+// The quantizer fused with SwiGLU: G, U fp16 [M][ld] in the layout's permuted channel order.
+cudaError_t launch_swiglu_quantize(const fmpq_layout& L, const void* G, int64_t ldg, const void* U, int64_t ldu,
+                                   int64_t M, void* A, void* scales, cudaStream_t stream);
 // QoQ progressive weights: unsigned 4-bit codes in the packed layout, s1 fp16 [N], s2 / z2 [nb][N].
 cudaError_t launch_qoq_pack_weights(const fmpq_layout& L, const void* W, int64_t ldw, int64_t N, void* Wp,
                                     void* s1, uint8_t* s2, uint8_t* z2, cudaStream_t stream);

@@ -231,6 +231,107 @@ __device__ __forceinline__ void quantize_asym_step(const Params& p, const uint32
     }
 }
 
+// One block step of the symmetric quantizer for a warp: each half-warp holds 8 fp16 values
+// per lane (h2: half2 words) of one 128-channel block b of token m. It takes the block's absmax
+// (kTok: the row's absmax tok_amax instead), the fp16 scale, the codes rne(|x| / s) and their
+// operand-ready bytes, and writes them to the block's plane(s) (first plane poff_b of planes of M
+// rows) and the scale (kTok: the sum of the block's codes) when `valid`. Both half-warps call it
+// together: it votes across the warp.
+template <bool kTok>
+__device__ __forceinline__ void quantize_codes_step(const uint32_t (&h2)[4], bool valid, bool is8, int b, int64_t m,
+                                                    uint32_t chunk_off, int sub, uint32_t hmask, int32_t poff_b,
+                                                    uint8_t* A, int64_t M, uint16_t* scales, int32_t* sums,
+                                                    float tok_amax) {
+    // absmax of the half-warp's 128 values
+    uint32_t ab[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) ab[k] = h2[k] & 0x7FFF7FFFu;
+    const __half2 m01 = __hmax2(*reinterpret_cast<const __half2*>(&ab[0]),
+                                *reinterpret_cast<const __half2*>(&ab[1]));
+    const __half2 m23 = __hmax2(*reinterpret_cast<const __half2*>(&ab[2]),
+                                *reinterpret_cast<const __half2*>(&ab[3]));
+    const __half2 mx = __hmax2(m01, m23);
+    const __half lm = __hmax(__low2half(mx), __high2half(mx));
+    const uint32_t amax_bits = __reduce_max_sync(hmask, static_cast<uint32_t>(__half_as_ushort(lm)));
+    // scale: fp16(fp32(absmax) * fp32(1/qmax)) equals fp16(fp32(absmax) / qmax)
+    // for every finite fp16 absmax and qmax in {7, 127}; per-token INT8 takes the
+    // row's absmax instead of the block's
+    const float amax = kTok ? tok_amax : __half2float(__ushort_as_half(static_cast<unsigned short>(amax_bits)));
+    const float qm = is8 ? 127.0f : 7.0f;
+    const __half s16 = __float2half_rn(__fmul_rn(amax, is8 ? (1.0f / 127.0f) : (1.0f / 7.0f)));
+    const float sc = __half2float(s16);
+    const float inv = sc > 0.0f ? rcp_approx(sc) : 0.0f;
+
+    // codes: rne(|x| / s). tm = fma(|x|, inv, 1.5 * 2^23) rounds |x| * inv
+    // (relative error < 2^-22) to an integer held in tm's low mantissa bits;
+    // quotients within 1e-4 of a half-integer are settled with the exact
+    // remainder |x| - r*s (the exact quotient of two fp16 values is never
+    // within 3e-5 of a half-integer unless it is one)
+    constexpr float kMagic = 12582912.0f;
+    float ax[8], tm[8];
+    bool near_half = false;
+    // two channels per instruction: fma.rn.f32x2 is the IEEE fma in each half; the
+    // fractional part of |x| * inv is |x| * inv - (tm - kMagic), with tm - kMagic exact
+    const float2 inv2 = make_float2(inv, inv), mg2 = make_float2(kMagic, kMagic);
+    const float2 neg1 = make_float2(-1.0f, -1.0f);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 a2 = __half22float2(*reinterpret_cast<const __half2*>(&ab[k]));
+        const float2 t2 = dev::ffma2(a2, inv2, mg2);
+        const float2 f2 = dev::ffma2(a2, inv2, dev::ffma2(t2, neg1, mg2));
+        ax[2 * k] = a2.x;
+        ax[2 * k + 1] = a2.y;
+        tm[2 * k] = t2.x;
+        tm[2 * k + 1] = t2.y;
+        near_half |= fmaxf(fabsf(f2.x), fabsf(f2.y)) > 0.4999f;
+    }
+    if (__any_sync(0xFFFFFFFFu, near_half) && sc > 0.0f) {
+        // (a zero scale keeps every code 0: its lanes skip the correction)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            float r = tm[k] - kMagic;
+            const float e = fmaf(-r, sc, ax[k]);   // exact remainder |x| - r*s
+            const float e2 = e + e;
+            if (e2 > sc) r += 1.0f;
+            else if (e2 < -sc) r -= 1.0f;
+            else if ((e2 == sc || e2 == -sc) && (static_cast<int>(r) & 1)) r += (e2 > 0.0f) ? 1.0f : -1.0f;  // tie: to even
+            tm[k] = r + kMagic;
+        }
+    }
+    if (__any_sync(0xFFFFFFFFu, sc > 0.0f && sc < 6.103515625e-05f)) {
+        // subnormal scale: the quotient can round past qmax
+#pragma unroll
+        for (int k = 0; k < 8; ++k) tm[k] = fminf(tm[k], qm + kMagic);
+    }
+    uint32_t w0 = low_bytes4(tm[0], tm[1], tm[2], tm[3]);
+    uint32_t w1 = low_bytes4(tm[4], tm[5], tm[6], tm[7]);
+    // sign bits of the inputs (bit 15 of each half) into bit 7 of each byte
+    w0 |= __byte_perm(h2[0], h2[1], 0x7531) & 0x80808080u;
+    w1 |= __byte_perm(h2[2], h2[3], 0x7531) & 0x80808080u;
+
+    if (valid) {
+        uint8_t* dst = A + (static_cast<int64_t>(poff_b) * M + m) * kBlock + chunk_off;
+        if (!is8) {
+            *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
+        } else {
+            *reinterpret_cast<uint2*>(dst) = make_uint2(w0 & 0x8F8F8F8Fu, w1 & 0x8F8F8F8Fu);
+            *reinterpret_cast<uint2*>(dst + M * kBlock) = make_uint2(high_plane(w0), high_plane(w1));
+        }
+        if constexpr (kTok) {
+            // the sum of the block's signed codes: magnitudes (bits 0-6) times +-1
+            // from the sign bits, four bytes per dp4a
+            auto sum4 = [](uint32_t w) {
+                const uint32_t pm = 0x01010101u | (((w >> 7) & 0x01010101u) * 0xFEu);
+                return __dp4a(static_cast<int>(w & 0x7F7F7F7Fu), static_cast<int>(pm), 0);
+            };
+            const int t = __reduce_add_sync(hmask, sum4(w0) + sum4(w1));
+            if (sub == 0) sums[static_cast<int64_t>(b) * M + m] = t;
+        } else {
+            if (sub == 0) scales[static_cast<int64_t>(b) * M + m] = __half_as_ushort(s16);
+        }
+    }
+}
+
 // Shared memory: [S] rows of X | gather offsets [iters][16 warps][32 lanes] (8 byte offsets of
 // 16 bits per lane and block pair) | plane offset per block | full / empty barriers per stage.
 __host__ __device__ inline size_t quant_gtab_offset(int K, int S) { return (2ull * K * S + 15) & ~15ull; }
@@ -483,7 +584,6 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
         }
         __syncwarp();
         const int iters = (nb - warp + 2 * W - 1) / (2 * W);   // rounds with a valid lower block
-        const int64_t plane_stride = p.M * kBlock;
 
         int64_t i = 0;
         bool ok = true;
@@ -541,94 +641,10 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
                         h2[k] = *reinterpret_cast<const uint32_t*>(&y);
                     }
                 }
-                // absmax of the half-warp's 128 values
-                uint32_t ab[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) ab[k] = h2[k] & 0x7FFF7FFFu;
-                const __half2 m01 = __hmax2(*reinterpret_cast<const __half2*>(&ab[0]),
-                                            *reinterpret_cast<const __half2*>(&ab[1]));
-                const __half2 m23 = __hmax2(*reinterpret_cast<const __half2*>(&ab[2]),
-                                            *reinterpret_cast<const __half2*>(&ab[3]));
-                const __half2 mx = __hmax2(m01, m23);
-                const __half lm = __hmax(__low2half(mx), __high2half(mx));
-                const uint32_t amax_bits = __reduce_max_sync(hmask, static_cast<uint32_t>(__half_as_ushort(lm)));
-                // scale: fp16(fp32(absmax) * fp32(1/qmax)) equals fp16(fp32(absmax) / qmax)
-                // for every finite fp16 absmax and qmax in {7, 127}; per-token INT8 takes the
-                // row's absmax instead of the block's
-                const float amax = kMode == kQTok ? r_norm : __half2float(__ushort_as_half(static_cast<unsigned short>(amax_bits)));
-                const float qm = is8 ? 127.0f : 7.0f;
-                const __half s16 = __float2half_rn(__fmul_rn(amax, is8 ? (1.0f / 127.0f) : (1.0f / 7.0f)));
-                const float sc = __half2float(s16);
-                const float inv = sc > 0.0f ? rcp_approx(sc) : 0.0f;
-
-                // codes: rne(|x| / s). tm = fma(|x|, inv, 1.5 * 2^23) rounds |x| * inv
-                // (relative error < 2^-22) to an integer held in tm's low mantissa bits;
-                // quotients within 1e-4 of a half-integer are settled with the exact
-                // remainder |x| - r*s (the exact quotient of two fp16 values is never
-                // within 3e-5 of a half-integer unless it is one)
-                constexpr float kMagic = 12582912.0f;
-                float ax[8], tm[8];
-                bool near_half = false;
-                // two channels per instruction: fma.rn.f32x2 is the IEEE fma in each half; the
-                // fractional part of |x| * inv is |x| * inv - (tm - kMagic), with tm - kMagic exact
-                const float2 inv2 = make_float2(inv, inv), mg2 = make_float2(kMagic, kMagic);
-                const float2 neg1 = make_float2(-1.0f, -1.0f);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float2 a2 = __half22float2(*reinterpret_cast<const __half2*>(&ab[k]));
-                    const float2 t2 = dev::ffma2(a2, inv2, mg2);
-                    const float2 f2 = dev::ffma2(a2, inv2, dev::ffma2(t2, neg1, mg2));
-                    ax[2 * k] = a2.x;
-                    ax[2 * k + 1] = a2.y;
-                    tm[2 * k] = t2.x;
-                    tm[2 * k + 1] = t2.y;
-                    near_half |= fmaxf(fabsf(f2.x), fabsf(f2.y)) > 0.4999f;
-                }
-                if (__any_sync(0xFFFFFFFFu, near_half) && sc > 0.0f) {
-                    // (a zero scale keeps every code 0: its lanes skip the correction)
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        float r = tm[k] - kMagic;
-                        const float e = fmaf(-r, sc, ax[k]);   // exact remainder |x| - r*s
-                        const float e2 = e + e;
-                        if (e2 > sc) r += 1.0f;
-                        else if (e2 < -sc) r -= 1.0f;
-                        else if ((e2 == sc || e2 == -sc) && (static_cast<int>(r) & 1)) r += (e2 > 0.0f) ? 1.0f : -1.0f;  // tie: to even
-                        tm[k] = r + kMagic;
-                    }
-                }
-                if (__any_sync(0xFFFFFFFFu, sc > 0.0f && sc < 6.103515625e-05f)) {
-                    // subnormal scale: the quotient can round past qmax
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) tm[k] = fminf(tm[k], qm + kMagic);
-                }
-                uint32_t w0 = low_bytes4(tm[0], tm[1], tm[2], tm[3]);
-                uint32_t w1 = low_bytes4(tm[4], tm[5], tm[6], tm[7]);
-                // sign bits of the inputs (bit 15 of each half) into bit 7 of each byte
-                w0 |= __byte_perm(h2[0], h2[1], 0x7531) & 0x80808080u;
-                w1 |= __byte_perm(h2[2], h2[3], 0x7531) & 0x80808080u;
-
-                if (valid) {
-                    const int b = warp + 2 * W * j + (upper ? W : 0);
-                    uint8_t* dst = p.A + (static_cast<int64_t>(s_poff[b]) * p.M + m) * kBlock + chunk_off;
-                    if (!is8) {
-                        *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
-                    } else {
-                        *reinterpret_cast<uint2*>(dst) = make_uint2(w0 & 0x8F8F8F8Fu, w1 & 0x8F8F8F8Fu);
-                        *reinterpret_cast<uint2*>(dst + plane_stride) = make_uint2(high_plane(w0), high_plane(w1));
-                    }
-                    if constexpr (kMode == kQTok) {
-                        // the sum of the block's signed codes: magnitudes (bits 0-6) times +-1
-                        // from the sign bits, four bytes per dp4a
-                        auto sum4 = [](uint32_t w) {
-                            const uint32_t pm = 0x01010101u | (((w >> 7) & 0x01010101u) * 0xFEu);
-                            return __dp4a(static_cast<int>(w & 0x7F7F7F7Fu), static_cast<int>(pm), 0);
-                        };
-                        const int t = __reduce_add_sync(hmask, sum4(w0) + sum4(w1));
-                        if (sub == 0) p.sums[static_cast<int64_t>(b) * p.M + m] = t;
-                    } else {
-                        if (sub == 0) p.scales[static_cast<int64_t>(b) * p.M + m] = __half_as_ushort(s16);
-                    }
+                {
+                    const int bb = warp + 2 * W * j + (upper ? W : 0);
+                    quantize_codes_step<kMode == kQTok>(h2, valid, is8, bb, m, chunk_off, sub, hmask,
+                                                        valid ? s_poff[bb] : 0, p.A, p.M, p.scales, p.sums, r_norm);
                 }
             }
             __syncwarp();
@@ -638,6 +654,156 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
     }
     __syncthreads();
     if (threadIdx.x == 0 && abort_flag) dev::report(p.status, dev::kStatusTimeout);
+}
+
+// ---------------------------------------------------------------------------------
+// SwiGLU fused with the quantizer (QServe explainer, "运行时设计": the activation quantization of
+// the second FFN layer is fused into the activation kernel): h = fp16_rn(g * u / (1 + e^-g)),
+// then the symmetric quantizer on h. The gate and up outputs arrive in the layout's permuted
+// channel order (the projections' output channels are permuted offline, like the weights), so
+// a warp reads its two blocks of a token with coalesced 16-byte loads: no staging, no gather.
+// One warp per (token, block pair), 8 channels per lane, grid-stride over the pairs.
+// ---------------------------------------------------------------------------------
+struct SwigluParams {
+    const uint16_t* G;
+    const uint16_t* U;
+    int64_t ldg, ldu, M;
+    int nb;
+    const uint8_t* mask;
+    const int32_t* poff;
+    uint8_t* A;
+    uint16_t* scales;
+};
+
+// Float-float arithmetic (a value is hi + lo, |lo| <= ulp(hi) / 2): error-free sums and
+// products (Knuth's two-sum, Dekker's fast two-sum, the fma product), used to settle the
+// rounding of SwiGLU values that lie near an fp16 rounding boundary.
+struct FF {
+    float hi, lo;
+};
+__device__ __forceinline__ FF ff_two_sum(float a, float b) {
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    return FF{s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
+}
+__device__ __forceinline__ FF ff_fast_two_sum(float a, float b) {   // |a| >= |b|
+    const float s = __fadd_rn(a, b);
+    return FF{s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+__device__ __forceinline__ FF ff_mul(FF x, FF y) {
+    const float p = __fmul_rn(x.hi, y.hi);
+    const float e = fmaf(x.hi, y.hi, -p);
+    return ff_fast_two_sum(p, e + (x.hi * y.lo + x.lo * y.hi));
+}
+__device__ __forceinline__ FF ff_add(FF x, FF y) {
+    const FF s = ff_two_sum(x.hi, y.hi);
+    return ff_fast_two_sum(s.hi, s.lo + (x.lo + y.lo));
+}
+
+// e^x for -25 <= x <= 88 in float-float, relative error below 2^-34: x = k ln2 + r with
+// |r| <= ln2 / 2 (Cody-Waite: ln2 split into a 15-bit head, so k * head is exact for |k| < 512,
+// and a tail), e^r by its Taylor series to r^11 / 11! (truncation below 2^-40) in Horner form,
+// then the exact scaling by 2^k.
+__device__ __forceinline__ FF ff_exp(float x) {
+    constexpr double kLn2 = 0.69314718055994530942;
+    constexpr float kLn2Hi = 0.693145751953125f;                              // 15 significant bits
+    constexpr float kLn2Lo = static_cast<float>(kLn2 - 0.693145751953125);
+    const float k = rintf(x * 1.44269504088896341f);
+    const float rh = fmaf(-k, kLn2Hi, x);                                      // exact
+    const FF t{__fmul_rn(k, kLn2Lo), fmaf(k, kLn2Lo, -__fmul_rn(k, kLn2Lo))};
+    FF r = ff_two_sum(rh, -t.hi);
+    r = ff_fast_two_sum(r.hi, __fsub_rn(r.lo, t.lo));
+    // 1 / n! for n = 11 .. 0 as float-float (head rounded from the double, tail the rest)
+    constexpr double kInvFact[12] = {1.0, 1.0, 0.5, 1.0 / 6, 1.0 / 24, 1.0 / 120, 1.0 / 720, 1.0 / 5040,
+                                     1.0 / 40320, 1.0 / 362880, 1.0 / 3628800, 1.0 / 39916800};
+    FF p{static_cast<float>(kInvFact[11]), static_cast<float>(kInvFact[11] - static_cast<float>(kInvFact[11]))};
+#pragma unroll
+    for (int n = 10; n >= 0; --n) {
+        const FF c{static_cast<float>(kInvFact[n]), static_cast<float>(kInvFact[n] - static_cast<float>(kInvFact[n]))};
+        p = ff_add(ff_mul(p, r), c);
+    }
+    const int ki = static_cast<int>(k);
+    return FF{ldexpf(p.hi, ki), ldexpf(p.lo, ki)};
+}
+
+// h for two channels (half2 words g2, u2), h = fp16_rn(g u / (1 + e^-g)) (a zero result keeps
+// the IEEE sign of g u). The fp32 value v = g u / (1 + e^-g) errs by at most 5 * 2^-24 (relative;
+// expf and the division within 2 ulp each, two roundings), so h = fp16_rn(v) unless the roundings
+// of |v| (1 - 2^-21) and |v| (1 + 2^-21) differ (for normal fp16 results tested on v's dropped
+// mantissa bits first). Then the exact value lies on one side of the
+// rounding boundary m between those two candidates, and the side is the sign of
+// |g u| - m (1 + e^-g): an exact sum plus m e^-g in float-float. The rare case that even this
+// leaves undecided (|T| below 2^-30 m e^-g) is computed in fp64.
+// The rare path (about 0.15% of the values), kept out of line so that the hot loop stays compact:
+// h1 < h2 are the candidate magnitudes, a = |g u|, e = expf(-g).
+__device__ __noinline__ uint16_t swiglu_settle(float g, float u, float a, float e, uint16_t h1, uint16_t h2) {
+    // the boundary between the candidates (exact in fp32; 65520 when h2 is the overflow)
+    const float f1 = __half2float(__ushort_as_half(h1));
+    const float f2 = h2 == 0x7C00u ? 65536.0f : __half2float(__ushort_as_half(h2));
+    const float m = 0.5f * (f1 + f2);
+    const float x = -g;
+    const FF E = x < -25.0f ? FF{e, 0.0f} : ff_exp(fminf(x, 88.0f));
+    const FF mE = ff_mul(FF{m, 0.0f}, E);
+    const FF t = ff_add(ff_two_sum(a, -m), FF{-mE.hi, -mE.lo});   // |g u| - m (1 + e^-g)
+    const float tv = t.hi != 0.0f ? t.hi : t.lo;
+    if (fabsf(tv) > 9.3132257461547852e-10f * m * E.hi) return tv > 0.0f ? h2 : h1;   // 2^-30
+    const double gd = static_cast<double>(g);
+    return __half_as_ushort(__double2half(fabs(gd * static_cast<double>(u)) / (1.0 + exp(-gd))));
+}
+
+__device__ __forceinline__ uint16_t swiglu_f16(float g, float u) {
+    const float gu = __fmul_rn(g, u);                     // exact: fp16 x fp16
+    const float a = fabsf(gu);
+    const float e = expf(-g);
+    const float v = __fdividef(a, __fadd_rn(1.0f, e));
+    const uint16_t sign = (__float_as_uint(gu) >> 16) & 0x8000u;
+    // For v in fp16's normal range the rounding drops v's 13 low mantissa bits: v is far from a
+    // rounding boundary when they are more than 8 units (> 5 * 2^-24 relative) away from 0x1000.
+    const int low = static_cast<int>(__float_as_uint(v) & 0x1FFFu) - 0x1000;
+    if (v >= 6.103515625e-05f && (low > 8 || low < -8)) return __half_as_ushort(__float2half_rn(v)) | sign;
+    const uint16_t h1 = __half_as_ushort(__float2half_rn(__fmul_rn(v, 1.0f - 4.76837158203125e-07f)));
+    const uint16_t h2 = __half_as_ushort(__float2half_rn(__fmul_rn(v, 1.0f + 4.76837158203125e-07f)));
+    return (h1 == h2 ? h1 : swiglu_settle(g, u, a, e, h1, h2)) | sign;
+}
+
+__device__ __forceinline__ uint32_t swiglu_f16x2(uint32_t g2, uint32_t u2) {
+    const float2 g = __half22float2(*reinterpret_cast<const __half2*>(&g2));
+    const float2 u = __half22float2(*reinterpret_cast<const __half2*>(&u2));
+    return static_cast<uint32_t>(swiglu_f16(g.x, u.x)) | (static_cast<uint32_t>(swiglu_f16(g.y, u.y)) << 16);
+}
+
+__global__ void __launch_bounds__(256) swiglu_quantize_kernel(SwigluParams p) {
+    const int lane = threadIdx.x & 31;
+    const bool upper = lane >= 16;
+    const int sub = lane & 15;
+    const uint32_t hmask = upper ? 0xFFFF0000u : 0x0000FFFFu;
+    const int pairs = (p.nb + 1) / 2;
+    const int64_t items = p.M * pairs;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t item = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); item < items;
+         item += warps) {   // warp-uniform
+        const int64_t m = item / pairs;
+        const int b = 2 * static_cast<int>(item % pairs) + (upper ? 1 : 0);
+        const bool valid = b < p.nb;
+        uint32_t h2[4] = {0u, 0u, 0u, 0u};
+        bool is8 = false;
+        int32_t poff_b = 0;
+        if (valid) {
+            const int64_t c = static_cast<int64_t>(b) * kBlock + sub * 8;
+            const uint4 g = __ldg(reinterpret_cast<const uint4*>(p.G + m * p.ldg + c));
+            const uint4 u = __ldg(reinterpret_cast<const uint4*>(p.U + m * p.ldu + c));
+            h2[0] = swiglu_f16x2(g.x, u.x);
+            h2[1] = swiglu_f16x2(g.y, u.y);
+            h2[2] = swiglu_f16x2(g.z, u.z);
+            h2[3] = swiglu_f16x2(g.w, u.w);
+            is8 = __ldg(p.mask + b) != 0;
+            poff_b = __ldg(p.poff + b);
+        }
+        const uint32_t chunk_off = ((static_cast<uint32_t>(sub >> 1) ^ static_cast<uint32_t>(m & 7)) << 4) +
+                                   static_cast<uint32_t>(sub & 1) * 8u;
+        quantize_codes_step<false>(h2, valid, is8, b, m, chunk_off, sub, hmask, poff_b, p.A, p.M, p.scales, nullptr,
+                                   0.0f);
+    }
 }
 
 // ---------------------------------------------------------------------------------
@@ -890,6 +1056,27 @@ cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, in
             else
                 quantize_kernel<kQSym><<<grid, threads, smem, stream>>>(p);
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_quantize(const fmpq_layout& L, const void* G, int64_t ldg, const void* U, int64_t ldu,
+                                   int64_t M, void* A, void* scales, cudaStream_t stream) {
+    SwigluParams p;
+    p.G = static_cast<const uint16_t*>(G);
+    p.U = static_cast<const uint16_t*>(U);
+    p.ldg = ldg;
+    p.ldu = ldu;
+    p.M = M;
+    p.nb = L.nb;
+    p.mask = L.d_mask;
+    p.poff = L.d_poff;
+    p.A = static_cast<uint8_t*>(A);
+    p.scales = static_cast<uint16_t*>(scales);
+    const int64_t items = M * ((L.nb + 1) / 2);
+    const int64_t ctas_needed = (items + 7) / 8;                       // 8 warps per CTA
+    const int64_t ctas_max = static_cast<int64_t>(L.num_sms) * 8;      // up to 64 warps per SM
+    const unsigned grid = static_cast<unsigned>(ctas_needed < ctas_max ? ctas_needed : ctas_max);
+    swiglu_quantize_kernel<<<grid, 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

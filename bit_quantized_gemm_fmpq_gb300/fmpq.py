@@ -47,6 +47,7 @@ SIGNATURES = {
     "w4ax_gemm_partials": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P]),
     "fmpq_device_status": (_I32, [_P, ctypes.POINTER(_I32), _I32]),
     "fmpq_rmsnorm_quantize": (_I32, [_P, _P, _I64, _I64, _P, ctypes.c_float, _P, _P, _P]),
+    "fmpq_swiglu_quantize": (_I32, [_P, _P, _I64, _P, _I64, _I64, _P, _P, _P]),
     "fmpq_variant_gemm_workspace_bytes": (_SZ, [_P, _I64, _I64]),
     "fmpq_quantize_asym": (_I32, [_P, _P, _I64, _I64, _P, _P, _P, _P]),
     "w4_weight_sums": (_I32, [_P, _P, _P, _I64, _P, _P]),
@@ -191,6 +192,21 @@ def fmpq_quantize(layout: Layout, X, A_packed=None, a_scales=None, stream=None):
         a_scales = torch.empty((layout.nb, M), dtype=torch.float16, device=X.device)
     _check("fmpq_quantize", layout._lib.fmpq_quantize(layout.handle, _ptr(X), X.stride(0), M, _ptr(A_packed),
                                                         _ptr(a_scales), _stream(stream)))
+    return A_packed, a_scales
+
+
+def fmpq_swiglu_quantize(layout: Layout, G_perm, U_perm, A_packed=None, a_scales=None, stream=None):
+    """SwiGLU (silu(g) * u, rounded once to fp16) fused with the activation quantizer; G_perm and
+    U_perm fp16 [M, >=K] in the layout's permuted channel order."""
+    import torch
+    M = G_perm.shape[0]
+    if A_packed is None:
+        A_packed = torch.empty(layout.packed_a_bytes(M), dtype=torch.uint8, device=G_perm.device)
+    if a_scales is None:
+        a_scales = torch.empty((layout.nb, M), dtype=torch.float16, device=G_perm.device)
+    _check("fmpq_swiglu_quantize", load_library().fmpq_swiglu_quantize(
+        layout.handle, _ptr(G_perm), G_perm.stride(0), _ptr(U_perm), U_perm.stride(0), M, _ptr(A_packed),
+        _ptr(a_scales), _stream(stream)))
     return A_packed, a_scales
 
 

@@ -16,7 +16,7 @@
  *     multiplication with a mixed-precision data layout; QUIK explainer, section "kernel
  *     fusion": dequantization fused into the GEMM epilogue).
  * Beside it: the layout derived from calibration data (fmpq_channel_absmax, fmpq_plan_layout),
- * the quantizer fused with RMSNorm (fmpq_rmsnorm_quantize), QUIK's FP16 outlier split
+ * the quantizer fused with RMSNorm (fmpq_rmsnorm_quantize) or SwiGLU (fmpq_swiglu_quantize), QUIK's FP16 outlier split
  * (fmpq_layout_create_select, fmpq_outlier_gemm_fp16), QUIK asymmetric activations
  * (fmpq_quantize_asym, w4ax_gemm_asym) and QoQ progressive group quantization with W4A8
  * GEMMs (qoq_pack_weights, qoq_quantize, qoq_gemm).
@@ -136,6 +136,21 @@ FMPQ_API fmpq_status fmpq_quantize(const fmpq_layout* layout, const void* X, int
 FMPQ_API fmpq_status fmpq_rmsnorm_quantize(const fmpq_layout* layout, const void* X, int64_t ldx, int64_t M,
                                            const void* gamma_perm, float eps, void* A_packed, void* a_scales,
                                            void* stream);
+
+/* The quantizer fused with the SwiGLU activation before the second FFN layer (QServe explainer,
+ * "运行时设计": activation quantization fused into the kernel that produces the activation). Codes,
+ * scales and layout are those of fmpq_quantize applied to
+ *   h[m][j] = fp16_rn( g[m][j] * u[m][j] / (1 + e^(-g[m][j])) )
+ * rounded once from the real value (ties to even; exact unless that value lies within ~2^-50 of an
+ * fp16 rounding boundary); a zero h keeps the IEEE sign of g * u.
+ *   G_perm, U_perm  fp16 [M][ldg], [M][ldu]: the gate and up projections' outputs in the layout's
+ *                   PERMUTED channel order (column j is channel perm[j]: the projections' output
+ *                   channels are reordered offline by the layout's permutation, as the weights are);
+ *                   ldg, ldu >= K, multiples of 8, 16-byte aligned.
+ * Other arguments as fmpq_quantize. Results are unspecified where h overflows fp16. */
+FMPQ_API fmpq_status fmpq_swiglu_quantize(const fmpq_layout* layout, const void* G_perm, int64_t ldg,
+                                          const void* U_perm, int64_t ldu, int64_t M, void* A_packed, void* a_scales,
+                                          void* stream);
 
 /* Offline weight preparation: W fp16 [N][ldw] (ldw >= K, ldw % 8 == 0, N % 16 == 0)
  * -> W_packed (fmpq_packed_w_bytes) and w_scales fp16 [K/128][N], INT4 range [-7, 7]

@@ -56,6 +56,7 @@ def _load():
             lib.oracle_f16_to_f32_array.argtypes = [P, i64, P]
             lib.oracle_rmsnorm.argtypes = [P, i64, i32, i32, P, ctypes.c_float, P]
             lib.oracle_rmsnorm_sumsq.argtypes = [P, i64, i32, i32, P]
+            lib.oracle_swiglu.argtypes = [P, P, i64, P]
             lib.oracle_channel_absmax.argtypes = [P, i64, i32, P]
             lib.oracle_plan_layout.argtypes = [i32, P, i32, P, P]
             lib.oracle_plan_layout.restype = i32
@@ -308,6 +309,16 @@ def rmsnorm(X, gamma, eps: float) -> np.ndarray:
     Y = np.empty((M, K), dtype=np.uint16)
     _load().oracle_rmsnorm(_ptr(X), K, M, K, _ptr(g), ctypes.c_float(eps), _ptr(Y))
     return Y.view(np.float16)
+
+
+def swiglu(G, U) -> np.ndarray:
+    """h = fp16_rn(g * u / (1 + e^-g)) elementwise for fp16 arrays G, U of one shape."""
+    G = np.ascontiguousarray(np.asarray(G, dtype=np.float16)).view(np.uint16)
+    U = np.ascontiguousarray(np.asarray(U, dtype=np.float16)).view(np.uint16)
+    assert G.shape == U.shape
+    H = np.empty(G.shape, dtype=np.uint16)
+    _load().oracle_swiglu(_ptr(G), _ptr(U), G.size, _ptr(H))
+    return H.view(np.float16)
 
 
 # ---------------------------------------------------------------------- outlier split (QUIK)

@@ -68,11 +68,11 @@ static double round_half_even_d(double r) {
     return (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
 }
 
-/* value -> binary16 bits, round to nearest, ties to even (finite inputs; NaN -> 0x7e00). */
-uint16_t oracle_f32_to_f16(float x) {
+/* value -> binary16 bits, round to nearest, ties to even (NaN -> 0x7e00). */
+static uint16_t f64_to_f16(double x) {
     if (isnan(x)) return 0x7e00;
     uint16_t sign = signbit(x) ? 0x8000 : 0;
-    double a = fabs((double)x);
+    double a = fabs(x);
     if (a >= 65520.0) return sign | 0x7c00;           /* 65504 + half an ulp (16): overflow */
     if (a == 0.0) return sign;
     /* quantum of the binade that contains a (subnormal binades share 2^-24) */
@@ -93,6 +93,8 @@ uint16_t oracle_f32_to_f16(float x) {
     if (expf >= 31) return sign | 0x7c00;
     return sign | (uint16_t)((expf << 10) | frac);
 }
+
+uint16_t oracle_f32_to_f16(float x) { return f64_to_f16((double)x); }
 
 void oracle_f32_to_f16_array(const float* x, int64_t n, uint16_t* out) {
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_f32_to_f16(x[i]);
@@ -602,6 +604,24 @@ void oracle_rmsnorm(const uint16_t* X, int64_t ldx, int M, int K, const uint16_t
         const uint16_t* x = X + (int64_t)m * ldx;
         for (int c = 0; c < K; ++c)
             Y[(int64_t)m * K + c] = oracle_f32_to_f16((oracle_f16_to_f32(x[c]) * r) * oracle_f16_to_f32(gamma[c]));
+    }
+}
+
+/* ------------------------------------------------------------------------------------
+ * SwiGLU fused into the quantizer (QServe explainer, "运行时设计": the activation quantization
+ * of the second FFN layer is fused into the activation kernel before it; the LLaMA FFN's
+ * activation is SwiGLU, h = silu(g) * u with silu(g) = g / (1 + e^-g), g and u the gate and up
+ * projections' outputs). The page gives no precision; the reading taken: h is the real value
+ * g * u / (1 + e^-g) rounded once to fp16 (ties to even). Here it is evaluated in fp64: g * u
+ * is exact, exp and the division err by a few 2^-53, far below fp16's rounding step, so the
+ * result is the correctly rounded value unless the exact one lies within ~2^-50 (relative) of
+ * an fp16 rounding boundary. A zero result keeps the IEEE sign of g * u.
+ * ------------------------------------------------------------------------------------ */
+void oracle_swiglu(const uint16_t* G, const uint16_t* U, int64_t n, uint16_t* H) {
+    for (int64_t i = 0; i < n; ++i) {
+        const double g = (double)oracle_f16_to_f32(G[i]);
+        const double u = (double)oracle_f16_to_f32(U[i]);
+        H[i] = f64_to_f16((g * u) / (1.0 + exp(-g)));
     }
 }
 
