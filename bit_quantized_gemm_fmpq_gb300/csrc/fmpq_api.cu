@@ -100,6 +100,8 @@ fmpq_status create_layout(int32_t K, int32_t K_in, const int32_t* perm_host, con
     L->num_sms = sms;
     L->planes = planes;
     L->row_bytes = static_cast<int64_t>(planes) * FMPQ_BLOCK;
+    for (int b = 0; b < nb; ++b)
+        if (outlier_block_mask_host[b]) L->mask_bits[b >> 5] |= 1u << (b & 31);
     bool ok = cudaMalloc(&L->d_perm16, sizeof(uint16_t) * K) == cudaSuccess &&
               cudaMalloc(&L->d_mask, static_cast<size_t>(nb)) == cudaSuccess &&
               cudaMalloc(&L->d_poff, sizeof(int32_t) * nb) == cudaSuccess &&

@@ -1,26 +1,38 @@
-// FMPQ W4Ax GEMM for few tokens (M <= 128, the decode shapes) on sm_103a.
+// FMPQ W4Ax GEMM for few tokens (M <= 64, the decode shapes) on sm_103a.
 //
 // Same result as the main GEMM: Y[m][n] = sum_b a_scale[b][m] * w_scale[b][n] * P[m][n][b],
 // P = exact per-block integer dot products (COMET abstract: mixed W4A4/W4A8 GEMM; QUIK
 // explainer, "kernel fusion": dequantization in the GEMM epilogue). With few tokens the
 // weights are the only large operand and the GEMM is bound by reading them from HBM, so
 // the roles of the operands are swapped:
-//   * the tensor core's M side is the output channels: a pair of CTAs covers 256 weight
-//     rows (128 per CTA), converted from the 4-bit packed tile exactly as in the main GEMM;
-//   * its N side is the tokens, T = 16, 32, 64 or 128 (M rounded up), each CTA holding T/2
+//   * the tensor core's M side is the output channels: a CTA covers 128 weight rows,
+//     converted from the 4-bit packed tile exactly as in the main GEMM;
+//   * its N side is the tokens, T = 16, 32 or 64 (M rounded up), the CTA holding all T
 //     rows of every activation code plane in shared memory;
-//   * an accumulator is 128 lanes x T columns of TMEM, so 4-8 of them are in flight and
+//   * an accumulator is 128 lanes x T columns of TMEM, so 8 of them are in flight and
 //     the per-block FP32 epilogue is 128 x T scale-and-adds per CTA;
+//   * every CTA works alone (tcgen05.mma cta_group::1): with the token operand this small a
+//     CTA pair would share almost nothing, and its cross-CTA handoffs would lie on the
+//     per-block chain;
 //   * two groups of converter warps take alternate blocks, so that converting the weights
 //     keeps up with streaming them;
-//   * few output tiles: K is split across pairs (deterministic split-K).
+//   * few output tiles: K is split across CTAs (deterministic split-K).
+// Streaming (measured on GB300): the TMA engine of an SM completes a copy no faster than
+// about one per 400-450 cycles whatever its size up to 8 KB, so every copy here is large:
+// the weights two blocks of the CTA's 128 rows at a time (16 KB, one 4-D tensor-map box),
+// the activation rows several code planes at a time (a 3-D box of T rows per plane whose rows
+// past M read as zero) and the scales a chunk of blocks at a time (2-D boxes). All of it goes
+// through TMA: plain loads and cp.async issued while the SM's weight copies are in flight
+// wait behind them for several microseconds, and a thread's mbarrier arrival (a release)
+// waits for every plain load it has in flight.
 //
-// Warp roles (512 threads, one CTA per SM, clusters of two, persistent over units):
-//   warp 0       weight producer: this CTA's 128 rows (8 KB) of each packed weight tile
-//   warp 1       even CTA: tcgen05 pair-MMA issuer; odd CTA: forwards operand readiness
-//   warps 2-5    converter group 0 (even blocks);  warps 12-15  converter group 1 (odd blocks)
-//   warp 6       activation producer: this CTA's T/2 token rows of each block's plane(s)
+// Warp roles (512 threads, one CTA per SM, persistent over units):
+//   warp 0       weight producer (four blocks of the CTA's 128 rows per copy)
+//   warp 6       operand producer: activation planes and scales
+//   warps 1, 7   tcgen05 MMA issuers (blocks in turn)
+//   warps 2-5    converter group 0 (even blocks of a unit);  warps 12-15  group 1 (odd blocks)
 //   warps 8-11   epilogue: TMEM lane quarter warp % 4, one output channel per thread
+#include <cuda.h>
 #include <cuda_fp16.h>
 
 #include "fmpq_device.cuh"
@@ -30,51 +42,66 @@ namespace fmpq {
 namespace {
 
 constexpr int kSThreads = 512;
+constexpr int kSTile = 128;    // output channels per CTA tile
 constexpr int kSCvStages = 4;  // converted weight tiles (two per converter group)
-constexpr int kSScStages = 4;  // per-block scales staged for the epilogue
-constexpr int kSBSlots = 8;    // activation plane slots (an INT4 block takes one, INT8 two)
-constexpr int kSBlk = 16;      // per-block readiness / release barriers (ring over blocks)
+constexpr int kSBlk = 16;      // per-block barriers (ring over blocks)
 constexpr int kSConvWarps = 4; // warps per converter group
 constexpr int kSEpiWarps = 4;
 constexpr uint32_t kSTmemCols = 512;
+constexpr int kSQuad = 4;         // blocks per weight copy
+constexpr int kSSc = 3;           // scale chunks staged
 
 // Accumulators of T columns in flight (TMEM holds 512 columns; at most 8 are used).
 template <int kT>
 __host__ __device__ constexpr int acc_slots() { return (512 / kT) < 8 ? (512 / kT) : 8; }
 
-// Packed weight stages (8 KB bulk copies). Every weight byte comes from HBM once, so the
-// stream runs at (bytes in flight) / (HBM latency): the ring takes the shared memory the
-// activation slots leave (T/2 rows each), about 80-128 KB in flight per SM.
+// Activation plane slots (T rows of 128 bytes each; an INT4 block takes one, INT8 two),
+// filled a_planes() consecutive planes per copy (8-16 KB).
 template <int kT>
-__host__ __device__ constexpr int w_stages() { return kT <= 32 ? 16 : kT == 64 ? 14 : 10; }
+__host__ __device__ constexpr int b_slots() { return kT <= 16 ? 16 : kT <= 32 ? 8 : 4; }
+template <int kT>
+__host__ __device__ constexpr int a_planes() { return kT <= 32 ? 4 : 2; }
+template <int kT>
+__host__ __device__ constexpr int a_copies() { return b_slots<kT>() / a_planes<kT>(); }   // ring of copies
 
-struct SScaleSlot {
-    float sw[128];  // weight scales of this CTA's 128 output channels
-    float sx[128];  // activation scales of the T tokens, times 2^18 (operand encoding)
-};
+// Packed weight stages (32 KB copies, four blocks each). Every weight byte comes from HBM once,
+// so the stream runs at (bytes in flight) / (HBM latency): the ring takes the shared memory
+// the activation slots leave, 96 KB in flight per SM.
+template <int kT>
+__host__ __device__ constexpr int w_stages() { return 3; }
+
+// Scale chunks: at most scale_chunk() blocks of a unit per chunk (the host may choose fewer,
+// SParams::sc_chunk); kSSc chunks are staged. Activation scales of a chunk: C rows of T (M a
+// multiple of 8: a 2-D box) or a run of the [nb][M] array from an 8-element boundary (a 1-D
+// box of at most 256 elements).
+template <int kT>
+__host__ __device__ constexpr int scale_chunk() { return kT <= 32 ? 16 : 8; }
+template <int kT>
+__host__ __device__ constexpr int sx_elems() { return scale_chunk<kT>() * kT > 256 ? scale_chunk<kT>() * kT : 256; }
 
 template <int kT>
 struct __align__(1024) SSmem {
-    uint8_t cvA[kSCvStages][128 * 128];     // E4M3 weight operand: this CTA's 128 rows x 128 K
-    uint8_t opB[kSBSlots][(kT / 2) * 128];  // activation code planes: T/2 token rows x 128 K
-    uint8_t pkW[w_stages<kT>()][128 * 64];  // packed weight codes of this CTA's 128 rows
-    SScaleSlot sc[kSScStages];
-    int32_t poff[kMaxBlocks];               // first code plane of each block
-    uint8_t mask[kMaxBlocks];               // 1 = INT8 block (two planes)
-    uint32_t maskw[kMaxBlocks / 32];        // the same, one bit per block
-    // blk_full[b % kSBlk]: block b's operands are in place in this CTA (activation rows by
-    //   bulk copy, converted weights by one converter group). In the even CTA it also
-    //   collects the odd CTA's forwarded readiness and the release of the accumulator the
-    //   block writes (the epilogue warps of both CTAs).
-    // blk_empty[b % kSBlk]: block b's MMAs are done; committed by the even CTA to both.
-    uint64_t blk_full[kSBlk], blk_empty[kSBlk];
+    uint8_t cvA[kSCvStages][128 * 128];          // E4M3 weight operand: 128 rows x 128 K
+    uint8_t opB[b_slots<kT>()][kT * 128];        // activation code planes: T token rows x 128 K
+    uint8_t pkW[w_stages<kT>()][kSQuad * 128 * 64];   // packed codes of the CTA's 128 rows, four blocks
+    uint16_t swr[kSSc][scale_chunk<kT>()][128];       // weight scales of the CTA's 128 channels (fp16)
+    uint16_t sxr[kSSc][sx_elems<kT>()];               // activation scales (fp16), see scale_chunk
+    // a_full[c % a_copies]: activation copy c has landed.
+    // blk_full[b % kSBlk]: block b's converted weights are in place (one converter group)
+    //   and the accumulator it writes has been read (the epilogue warps).
+    // blk_empty[b % kSBlk]: block b's MMAs are done: its accumulator is full and its operand
+    //   slots may be reused.
+    uint64_t a_full[a_copies<kT>()], blk_full[kSBlk], blk_empty[kSBlk];
     uint64_t w_full[w_stages<kT>()], w_empty[w_stages<kT>()];
-    uint64_t sc_full[kSScStages], sc_empty[kSScStages];
-    uint64_t acc_full[8];
-    uint64_t mma_done;
+    uint64_t scl_full[kSSc], scl_empty[kSSc];         // scale chunk staged / read by the epilogue
+    float sxf[kSEpiWarps][scale_chunk<kT>() * kT];    // each epilogue warp's copy of the chunk's
+                                                      // activation scales as FP32, 0 past M
+    uint32_t maskw[kMaxBlocks / 32];                  // INT8 blocks (bit b % 32 of word b / 32)
+    uint64_t mma_done[2];   // one per MMA issuer
+    uint64_t red_ready;   // split-K (ranks > 0): rank 0's shared memory is free for the partials
+    uint64_t red_full;    // split-K (rank 0): every other split's partials have landed
     uint32_t tmem_base;
     int abort_flag;
-    int fixup_last;
 };
 
 struct SParams {
@@ -85,16 +112,16 @@ struct SParams {
     uint16_t* Y;
     int64_t ldy;
     int M, N, nb;
-    const uint8_t* mask;
-    const int32_t* poff;
+    uint32_t mask_bits[kMaxBlocks / 32];   // INT8 blocks (bit b % 32 of word b / 32)
     int32_t* status;
-    int ntiles;            // 256-channel output tiles
+    int ntiles;            // 128-channel output tiles
     int splits;            // K splits per tile (1 = none)
-    float* ws_partial;     // [ntiles][splits][256][T] FP32 partial sums (splits > 1)
-    int32_t* ws_count;     // [ntiles][2] arrival counters per CTA half (zero between calls)
     // partial-sum export (debug): P[m - pm0][n - pn0][b] for the window, instead of Y
     int32_t* P;
     int pm0, pmcount, pn0, pncount;
+    int sc_chunk;          // blocks per scale chunk (<= scale_chunk<T>)
+    int sx_rows;           // 1: activation scales staged as rows of T (M % 8 == 0); 0: as a run
+    int sx_box;            // elements of a run (sx_rows == 0)
 };
 
 __device__ __forceinline__ uint32_t lo4s(uint32_t w) { return w & 0x87878787u; }
@@ -119,150 +146,253 @@ __device__ __forceinline__ void sfail(const SParams& p, volatile int* abort_flag
     dev::report(p.status, dev::kStatusTimeout);
 }
 
-// ---------------------------------------------------------------- weight producer (warp 0)
+// ---------------------------------------------------------------- producers (warps 0, 6)
+// An SM's TMA engine takes copies first in, first out, and issuing one costs its thread a few
+// hundred cycles: the weights (warp 0) and the activation planes and scales (warp 6) have a
+// producer thread each, and both rings run about as many blocks ahead, so that the copies
+// reach the engine roughly in the order the blocks are consumed. For block i of a unit:
+//   * i % C == 0: scale chunk k (blocks i .. i + C - 1; the last chunk of a unit may be shorter,
+//     its extra rows unused) to slot k % kSSc: the weight scales of the unit's 128 output
+//     channels (a 2-D box of C rows; channels past N read as zero) and the activation scales,
+//     C rows of T tokens (M % 8 == 0; tokens past M zero) or the run of the [nb][M] array from
+//     the 8-element boundary at or below (b0 + i) * M;
+//   * the activation copies up to the one holding i's last plane. A unit's code planes are
+//     consecutive in the packed activations (blocks b0 .. b0 + n - 1 hold planes poff[b0]
+//     onwards), so copy c of a unit holds planes q0 + cP .. q0 + cP + P - 1 (P = a_planes) as P
+//     slots of T rows: rows at or past M read as zero, and planes past the unit's (or past the
+//     end) are read unused. Copy g (counted over the CTA's units) goes to slots
+//     (g % a_copies) * P onwards once the blocks that read the copy before it there have had
+//     their MMAs done;
+//   * i % 4 == 0 (weight producer): copy i / 4, blocks i .. i + 3 of the CTA's 128 rows (one 4-D
+//     box; past a unit's last block it reads the following blocks, or zeros past the tensor's
+//     end, unused).
+// The roles that walk every block (producer, issuer) are chains of dependent instructions,
+// each a few cycles; the per-block work is kept to shifts and adds: planes come from a
+// bitmap word shifted one block at a time, plane offsets are running sums, and the scale chunk
+// boundary is a countdown.
+struct SPlaneWalk {
+    uint32_t word;   // bitmap bits of the next blocks
+    int left;        // bits left in `word`
+    int widx;        // index of `word` in the bitmap
+    __device__ __forceinline__ void start(const uint32_t* mw, int b) {
+        widx = b >> 5;
+        word = mw[widx] >> (b & 31);
+        left = 32 - (b & 31);
+    }
+    // planes of the next block (1 or 2)
+    __device__ __forceinline__ int next(const uint32_t* mw) {
+        const int planes = 1 + static_cast<int>(word & 1u);
+        word >>= 1;
+        if (--left == 0) {
+            ++widx;
+            word = widx < kMaxBlocks / 32 ? mw[widx] : 0u;
+            left = 32;
+        }
+        return planes;
+    }
+};
+
+// The first code plane of block b (an INT8 block has two), from the bitmap of INT8 blocks
+// (copied from the kernel parameters to shared memory at the start).
+__device__ __forceinline__ int spoff(const uint32_t* mw, int b) {
+    int q = b;
+    for (int w = 0; w < (b >> 5); ++w) q += __popc(mw[w]);
+    return q + __popc(mw[b >> 5] & ((1u << (b & 31)) - 1u));
+}
+
 template <int kT>
-__device__ __forceinline__ void s_weight_producer(const SParams& p, SSmem<kT>& s, uint32_t rank, int lane,
+__device__ __forceinline__ void s_weight_producer(const SParams& p, const CUtensorMap* tmw, SSmem<kT>& s, int lane,
                                                   volatile int* abort_flag) {
     constexpr int kSWStages = w_stages<kT>();
+    if (lane != 0) return;   // one thread: no warp-wide steps on the per-copy path
     const int num_units = p.ntiles * p.splits;
     uint32_t wc = 0;
+    int ws = 0, wpar = 1;    // ring position and the parity its empty barrier waits for
     bool ok = true;
-    for (int u = blockIdx.x >> 1; ok && u < num_units; u += gridDim.x >> 1) {
+    for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
         const SUnit t = sunit_of(p, u);
-        for (int i = 0; i < t.n; ++i, ++wc) {
-            const int b = t.block(i);
-            const int ws = wc % kSWStages;
-            ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&s.w_empty[ws], ((wc / kSWStages) & 1) ^ 1, abort_flag));
+        for (int i = 0; i < t.n; i += kSQuad) {
+            ok = dev::mbar_wait(&s.w_empty[ws], wpar, abort_flag);
             if (!ok) break;
-            if (lane == 0) {
-                dev::mbar_arrive_expect_tx(&s.w_full[ws], 128 * 64);
-                dev::bulk_g2s(s.pkW[ws], p.W + (static_cast<int64_t>(t.nt) * p.nb + b) * (256 * 64) + rank * (128 * 64),
-                              128 * 64, &s.w_full[ws]);
+            dev::mbar_arrive_expect_tx(&s.w_full[ws], kSQuad * 128 * 64);
+            // {byte, 256-byte line, half of the 256-row group, group * nb + block}
+            dev::tma_load_4d(s.pkW[ws], tmw, 0, 0, t.nt & 1, (t.nt >> 1) * p.nb + t.block(i), &s.w_full[ws]);
+            ++wc;
+            if (++ws == kSWStages) {
+                ws = 0;
+                wpar ^= 1;
             }
-            __syncwarp();
         }
     }
-    if (!ok && lane == 0) sfail(p, abort_flag);
-    if (lane == 0) {
-        for (int ws = 0; ws < kSWStages; ++ws) {   // drain copies in flight
-            if (wc <= static_cast<uint32_t>(ws)) break;
-            const uint32_t last = ws + ((wc - 1 - ws) / kSWStages) * kSWStages;
-            dev::mbar_wait(&s.w_full[ws], (last / kSWStages) & 1, nullptr);
-        }
+    if (!ok) sfail(p, abort_flag);
+    for (uint32_t j = 0; j < static_cast<uint32_t>(kSWStages) && j < wc; ++j) {   // drain (copy bytes only)
+        const uint32_t c = wc - 1 - j;
+        dev::mbar_wait(&s.w_full[c % kSWStages], (c / kSWStages) & 1, nullptr);
     }
-    __syncwarp();
 }
 
-// ---------------------------------------------------------------- activation producer (warp 6)
-// This CTA's T/2 token rows [rank*T/2, rank*T/2 + T/2) of each block's plane(s): one bulk copy
-// of the rows below M (the quantizer's row swizzle, row mod 8, matches the tile's since T/2 is
-// a multiple of 8). Rows at or past M are never written and stay zero.
 template <int kT>
-__device__ __forceinline__ void s_activation_producer(const SParams& p, SSmem<kT>& s, uint32_t rank, int lane,
-                                                      volatile int* abort_flag) {
+__device__ __forceinline__ void s_operand_producer(const SParams& p, const CUtensorMap* tma, const CUtensorMap* tmsw,
+                                                   const CUtensorMap* tmsx, SSmem<kT>& s, int lane,
+                                                   volatile int* abort_flag) {
+    constexpr int kP = a_planes<kT>(), kC = a_copies<kT>();
+    constexpr int kPShift = kP == 4 ? 2 : kP == 2 ? 1 : 0;
+    if (lane != 0) return;   // one thread: no warp-wide steps on the per-block path
     const int num_units = p.ntiles * p.splits;
-    uint32_t pc = 0, it = 0;
-    int32_t slot_block[kSBSlots];
+    const int C = p.sc_chunk;
+    const uint32_t sbytes = static_cast<uint32_t>(C) * 128 * 2 +
+                            static_cast<uint32_t>(p.sx_rows ? C * kT * 2 : p.sx_box * 2);
+    uint32_t g = 0, it = 0, k = 0;       // activation copies, blocks, scale chunks
+    int ks = 0, kpar = 1;                // scale ring position and the parity its empty barrier waits for
+    int32_t last_use[kC];                // per activation ring position: its copy's last reader
 #pragma unroll
-    for (int i = 0; i < kSBSlots; ++i) slot_block[i] = -1;
+    for (int j = 0; j < kC; ++j) last_use[j] = -1;
     bool ok = true;
-    const int64_t plane_bytes = static_cast<int64_t>(p.M) * kBlock;
-    const int r0 = static_cast<int>(rank) * (kT / 2);
-    const uint32_t abytes = static_cast<uint32_t>(max(0, min(kT / 2, p.M - r0))) * kBlock;
-    for (int u = blockIdx.x >> 1; ok && u < num_units; u += gridDim.x >> 1) {
+    for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
         const SUnit t = sunit_of(p, u);
+        const int q0 = spoff(s.maskw, t.b0);
+        const uint32_t g0 = g;
+        SPlaneWalk pw;
+        pw.start(s.maskw, t.b0);
+        int q = 0, sc_left = 0;   // the block's first plane (unit-relative); blocks left in the scale chunk
         for (int i = 0; ok && i < t.n; ++i, ++it) {
             const int b = t.block(i);
-            const int planes = s.mask[b] ? 2 : 1;
-            for (int pl = 0; ok && pl < planes; ++pl) {
-                const int sl = (pc + pl) % kSBSlots;
+            if (sc_left == 0) {
+                sc_left = C;
+                ok = dev::mbar_wait(&s.scl_empty[ks], kpar, abort_flag);
+                if (!ok) break;
+                dev::mbar_arrive_expect_tx(&s.scl_full[ks], sbytes);
+                dev::tma_load_2d(&s.swr[ks][0][0], tmsw, t.nt * kSTile, b, &s.scl_full[ks]);
+                if (p.sx_rows)
+                    dev::tma_load_2d(&s.sxr[ks][0], tmsx, 0, b, &s.scl_full[ks]);
+                else
+                    dev::tma_load_1d(&s.sxr[ks][0], tmsx, (b * p.M) & ~7, &s.scl_full[ks]);
+                ++k;
+                if (++ks == kSSc) {
+                    ks = 0;
+                    kpar ^= 1;
+                }
+            }
+            --sc_left;
+            const int planes = pw.next(s.maskw);
+            const uint32_t first = g0 + static_cast<uint32_t>(q >> kPShift);
+            const uint32_t need = g0 + static_cast<uint32_t>((q + planes - 1) >> kPShift);
+            q += planes;
+            while (g <= need) {
+                const int pos = static_cast<int>(g % kC);
                 int32_t last = -1;
 #pragma unroll
-                for (int i = 0; i < kSBSlots; ++i)
-                    if (i == sl) last = slot_block[i];
+                for (int j = 0; j < kC; ++j)
+                    if (j == pos) last = last_use[j];
                 if (last >= 0)
-                    ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&s.blk_empty[last % kSBlk],
-                                                                (static_cast<uint32_t>(last) / kSBlk) & 1, abort_flag));
+                    ok = dev::mbar_wait(&s.blk_empty[last % kSBlk], (static_cast<uint32_t>(last) / kSBlk) & 1, abort_flag);
+                if (!ok) break;
+                dev::mbar_arrive_expect_tx(&s.a_full[pos], kP * kT * 128);
+                // {byte, token row, plane}
+                dev::tma_load_3d(s.opB[pos * kP], tma, 0, 0, q0 + static_cast<int>(g - g0) * kP, &s.a_full[pos]);
+                ++g;
             }
             if (!ok) break;
-            uint64_t* bar = &s.blk_full[it % kSBlk];
-            if (lane == 0) dev::mbar_arrive_expect_tx(bar, abytes * planes);
-            const uint8_t* a0 = p.A + static_cast<int64_t>(s.poff[b]) * plane_bytes + static_cast<int64_t>(r0) * kBlock;
-            for (int pl = 0; pl < planes; ++pl, ++pc) {
-                const int sl = pc % kSBSlots;
+            {   // block it is now the last reader of its copies (first, and need if another)
+                const int pf = static_cast<int>(first % kC), pn = static_cast<int>(need % kC);
 #pragma unroll
-                for (int i = 0; i < kSBSlots; ++i)
-                    if (i == sl) slot_block[i] = static_cast<int32_t>(it);
-                if (lane == 0 && abytes > 0) dev::bulk_g2s(s.opB[sl], a0 + pl * plane_bytes, abytes, bar);
+                for (int j = 0; j < kC; ++j)
+                    if (j == pf || j == pn) last_use[j] = static_cast<int32_t>(it);
             }
-            __syncwarp();
         }
     }
-    if (!ok && lane == 0) sfail(p, abort_flag);
-    if (lane == 0) {
-        for (uint32_t k = 0; k < kSBlk && k < it; ++k) {   // drain: the last blocks' copies
-            const uint32_t b = it - 1 - k;
-            dev::mbar_wait(&s.blk_full[b % kSBlk], (b / kSBlk) & 1, nullptr);
-        }
+    if (!ok) sfail(p, abort_flag);
+    // drain copies in flight (their barriers complete on copy bytes only)
+    for (uint32_t j = 0; j < static_cast<uint32_t>(kC) && j < g; ++j) {
+        const uint32_t c = g - 1 - j;
+        dev::mbar_wait(&s.a_full[c % kC], (c / kC) & 1, nullptr);
     }
-    __syncwarp();
+    for (uint32_t j = 0; j < static_cast<uint32_t>(kSSc) && j < k; ++j) {
+        const uint32_t c = k - 1 - j;
+        dev::mbar_wait(&s.scl_full[c % kSSc], (c / kSSc) & 1, nullptr);
+    }
 }
 
-// ---------------------------------------------------------------- MMA issuer / forwarder (warp 1)
+// ---------------------------------------------------------------- MMA issuers (warps 1, 7)
+// Block it: its converted weight tile and the activation copies holding its plane(s) (the
+// same copy arithmetic as the producer), then 4 MMAs (K = 32 each) per plane into accumulator
+// it % kAcc. Checking a block's barriers and issuing its MMAs is a chain of several hundred
+// cycles of instruction latency, so kSIssuers issuers take the blocks in turn (`par`): each
+// commits only the MMAs it issued, and every block has its own accumulator.
+constexpr int kSIssuers = 2;
+
 template <int kT>
-__device__ __forceinline__ void s_mma_role(const SParams& p, SSmem<kT>& s, uint32_t rank, int lane, uint32_t tmem,
+__device__ __forceinline__ void s_mma_role(const SParams& p, SSmem<kT>& s, int lane, uint32_t tmem, int par,
                                            volatile int* abort_flag) {
     constexpr int kAcc = acc_slots<kT>();
-    constexpr uint32_t kIdesc = dev::idesc_e4m3_f32(256, kT);
+    constexpr int kP = a_planes<kT>(), kC = a_copies<kT>();
+    constexpr uint32_t kIdesc = dev::idesc_e4m3_f32(128, kT);
+    constexpr int kPShift = kP == 4 ? 2 : kP == 2 ? 1 : 0;
     const int num_units = p.ntiles * p.splits;
-    uint32_t it = 0, pc = 0;
+    // descriptors of the first converted stage and the first activation slot; the others are
+    // whole multiples of 16 bytes further (the descriptor's address field counts 16-byte units)
+    const uint64_t ad0 = dev::sdesc_k_sw128(dev::smem_u32(s.cvA[0]));
+    const uint64_t bd0 = dev::sdesc_k_sw128(dev::smem_u32(s.opB[0]));
+    uint32_t it = 0, g0 = 0;   // blocks, and activation copies of the units before this one
+    int64_t waited = -1;       // the last activation copy this issuer has waited for
+    int turn = 0;              // it % kSIssuers
     bool ok = true;
-    const uint32_t leader_blk_full = dev::mapa(&s.blk_full[0], 0);
-    for (int u = blockIdx.x >> 1; ok && u < num_units; u += gridDim.x >> 1) {
+    for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
         const SUnit t = sunit_of(p, u);
+        SPlaneWalk pw;
+        pw.start(s.maskw, t.b0);
+        int q = 0;   // the block's first plane (unit-relative)
         for (int i = 0; ok && i < t.n; ++i, ++it) {
-            const int planes = 1 + static_cast<int>((s.maskw[t.block(i) >> 5] >> (t.block(i) & 31)) & 1u);
-            ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&s.blk_full[it % kSBlk], (it / kSBlk) & 1, abort_flag));
-            if (!ok) break;
-            if (rank != 0) {
-                if (lane == 0) dev::mbar_arrive_remote(leader_blk_full + static_cast<uint32_t>(it % kSBlk) * 8u);
-                __syncwarp();
-                pc += planes;
+            const int planes = pw.next(s.maskw);
+            const bool mine = turn == par;
+            if (++turn == kSIssuers) turn = 0;
+            if (!mine) {
+                q += planes;
                 continue;
             }
+            const uint32_t c0 = g0 + static_cast<uint32_t>(q >> kPShift);
+            const uint32_t c1 = g0 + static_cast<uint32_t>((q + planes - 1) >> kPShift);
+            ok = dev::mbar_wait(&s.blk_full[it % kSBlk], (it / kSBlk) & 1, abort_flag);
+            if (ok && static_cast<int64_t>(c0) > waited) ok = dev::mbar_wait(&s.a_full[c0 % kC], (c0 / kC) & 1, abort_flag);
+            if (ok && c1 != c0) ok = dev::mbar_wait(&s.a_full[c1 % kC], (c1 / kC) & 1, abort_flag);
+            waited = c1;
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (!ok) break;
             const int ab = static_cast<int>(it % kAcc);
             if (lane == 0) {
                 dev::tc_fence_after();
-                const uint64_t ad = dev::sdesc_k_sw128(dev::smem_u32(s.cvA[it % kSCvStages]));
+                const uint64_t ad = ad0 + static_cast<uint64_t>((it % kSCvStages) * (128 * 128 / 16));
                 const uint32_t d = tmem + static_cast<uint32_t>(ab * kT);
                 for (int pl = 0; pl < planes; ++pl) {
-                    const uint64_t bd = dev::sdesc_k_sw128(dev::smem_u32(s.opB[(pc + pl) % kSBSlots]));
+                    const uint32_t c = g0 + static_cast<uint32_t>((q + pl) >> kPShift);
+                    const int slot = static_cast<int>(c % kC) * kP + ((q + pl) & (kP - 1));
+                    const uint64_t bd = bd0 + static_cast<uint64_t>(slot * (kT * 128 / 16));
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        dev::mma_e4m3_pair(d, ad + 2 * k, bd + 2 * k, kIdesc, (pl > 0 || k > 0) ? 1u : 0u);
+                        dev::mma_e4m3(d, ad + 2 * k, bd + 2 * k, kIdesc, (pl > 0 || k > 0) ? 1u : 0u);
                 }
-                dev::mma_commit_pair(&s.blk_empty[it % kSBlk]);
-                dev::mma_commit_pair(&s.acc_full[ab]);
+                dev::mma_commit(&s.blk_empty[it % kSBlk]);   // also tells the epilogue accumulator ab is full
             }
             __syncwarp();
-            pc += planes;
+            q += planes;
         }
+        g0 += static_cast<uint32_t>(((q - 1) >> kPShift) + 1);   // the unit's copies
     }
     if (!ok && lane == 0) sfail(p, abort_flag);
-    if (rank == 0 && lane == 0) {
-        dev::mma_commit_pair(&s.mma_done);   // every MMA issued finishes before TMEM is released
-        dev::mbar_wait(&s.mma_done, 0, nullptr);
+    if (lane == 0) {
+        dev::mma_commit(&s.mma_done[par]);   // every MMA issued finishes before TMEM is released
+        dev::mbar_wait(&s.mma_done[par], 0, nullptr);
     }
     __syncwarp();
 }
 
 // ---------------------------------------------------------------- converters (warps 2-5, 12-15)
-// Group g converts the blocks it with it % 2 == g (packed codes -> 128B-swizzled E4M3 tile, the
-// same mapping as the main GEMM's converters) and stages their scales: weight scale of this
-// CTA's output channel ct and, for ct < T, the activation scale of token ct (times 2^18).
+// Group g converts the blocks i of each unit with i % 2 == g (packed codes -> 128B-swizzled
+// E4M3 tile, the same mapping as the main GEMM's converters; block i sits in quarter i % 4 of
+// the unit's weight copy i / 4).
 template <int kT>
-__device__ __forceinline__ void s_converter_role(const SParams& p, SSmem<kT>& s, uint32_t rank, int group, int ct,
-                                                 int lane, volatile int* abort_flag) {
+__device__ __forceinline__ void s_converter_role(const SParams& p, SSmem<kT>& s, int group, int ct, int lane,
+                                                 volatile int* abort_flag) {
     const int num_units = p.ntiles * p.splits;
     const int r0 = ct >> 2, c4 = ct & 3;
     const uint32_t phase = static_cast<uint32_t>(r0 & 7);
@@ -273,25 +403,21 @@ __device__ __forceinline__ void s_converter_role(const SParams& p, SSmem<kT>& s,
     constexpr int kPieces = 4;     // 512 pieces of 16 bytes over 128 threads
     constexpr int kRowStep = 32;   // rows between a thread's pieces
     bool ok = true;
-    uint32_t it = 0;
-    for (int u = blockIdx.x >> 1; ok && u < num_units; u += gridDim.x >> 1) {
+    uint32_t it = 0, wbase = 0;   // blocks and weight copies of the units before this one
+    for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
         const SUnit t = sunit_of(p, u);
-        const int n = t.nt * kTileN + static_cast<int>(rank) * 128 + ct;
-        for (int i = 0; i < t.n; ++i, ++it) {
-            if (static_cast<int>(it & 1u) != group) continue;
-            const int b = t.block(i);
-            const uint16_t swv = (n < p.N) ? __ldg(p.w_scales + static_cast<int64_t>(b) * p.N + n) : uint16_t(0);
-            const uint16_t sxv = (ct < kT && ct < p.M) ? __ldg(p.a_scales + static_cast<int64_t>(b) * p.M + ct) : uint16_t(0);
-            const int ws = it % kSWStages, cs = it % kSCvStages, ss = it % kSScStages;
-            ok = dev::mbar_wait(&s.w_full[ws], (it / kSWStages) & 1, abort_flag) &&
-                 dev::mbar_wait(&s.sc_empty[ss], ((it / kSScStages) & 1) ^ 1, abort_flag);
-            if (ok && it >= static_cast<uint32_t>(kSCvStages)) {   // converted slot: MMAs of block it - 4 done
-                const uint32_t prev = it - kSCvStages;
+        for (int i = group; i < t.n; i += 2) {
+            const uint32_t bi = it + i;                 // the block's position in the CTA's sequence
+            const uint32_t wc = wbase + (i >> 2);       // its weight copy
+            const int ws = wc % kSWStages, cs = bi % kSCvStages;
+            ok = dev::mbar_wait(&s.w_full[ws], (wc / kSWStages) & 1, abort_flag);
+            if (ok && bi >= static_cast<uint32_t>(kSCvStages)) {   // converted slot: MMAs of block bi - 4 done
+                const uint32_t prev = bi - kSCvStages;
                 ok = dev::mbar_wait(&s.blk_empty[prev % kSBlk], (prev / kSBlk) & 1, abort_flag);
             }
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
-            const uint8_t* src = s.pkW[ws] + src0;
+            const uint8_t* src = s.pkW[ws] + (i & 3) * (128 * 64) + src0;
             uint8_t* dst = s.cvA[cs];
             uint4 w[kPieces];
 #pragma unroll
@@ -302,50 +428,68 @@ __device__ __forceinline__ void s_converter_role(const SParams& p, SSmem<kT>& s,
                 *reinterpret_cast<uint4*>(dst + dstA + k * kRowStep * 128) = make_uint4(lo4s(v.x), hi4s(v.x), lo4s(v.y), hi4s(v.y));
                 *reinterpret_cast<uint4*>(dst + dstB + k * kRowStep * 128) = make_uint4(lo4s(v.z), hi4s(v.z), lo4s(v.w), hi4s(v.w));
             }
-            s.sc[ss].sw[ct] = __half2float(__ushort_as_half(swv));
-            if (ct < kT) s.sc[ss].sx[ct] = __half2float(__ushort_as_half(sxv)) * 262144.0f;
             dev::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
                 dev::mbar_arrive(&s.w_empty[ws]);
-                dev::mbar_arrive(&s.blk_full[it % kSBlk]);
-                dev::mbar_arrive(&s.sc_full[ss]);
+                // a unit's last copy may hold fewer than four of its blocks: arrive for the rest
+                if (i + 1 == t.n)
+                    for (int r = i & 3; r < 3; ++r) dev::mbar_arrive(&s.w_empty[ws]);
+                dev::mbar_arrive(&s.blk_full[bi % kSBlk]);
             }
         }
+        it += t.n;
+        wbase += (t.n + 3) / 4;
     }
     if (!ok && lane == 0) sfail(p, abort_flag);
 }
 
 // ---------------------------------------------------------------- epilogue (warps 8-11)
 // Warp q holds TMEM lanes 32q..32q+31: thread `lane` owns output channel
-// n0 + rank*128 + 32q + lane and accumulates its T token columns (32x32b loads, 16 columns
-// at a time, the next load in flight during the math of the current one).
+// nt * 128 + 32q + lane and accumulates its T token columns (32x32b loads, 16 columns at a
+// time, the next load in flight during the math of the current one).
 template <int kT, bool kPartials>
-__device__ __forceinline__ void s_epilogue_role(const SParams& p, SSmem<kT>& s, uint32_t rank, int q, int lane,
-                                                uint32_t tmem, volatile int* abort_flag) {
+__device__ __forceinline__ void s_epilogue_role(const SParams& p, SSmem<kT>& s, int q, int lane, uint32_t tmem,
+                                                volatile int* abort_flag) {
     constexpr int kAcc = acc_slots<kT>();
     constexpr int kChunks = kT / 16;
+    const int C = p.sc_chunk;
     const int num_units = p.ntiles * p.splits;
-    const int lrow = 32 * q + lane;                       // this CTA's row (output channel)
+    const int lrow = 32 * q + lane;                       // the CTA's row (output channel)
     const int et = q * 32 + lane;                         // 0..127
     const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
-    const uint32_t leader_blk_full = dev::mapa(&s.blk_full[0], 0);
     const int mvalid = min(p.M, kT);
-    uint32_t v = 0;
+    uint32_t v = 0, ck = 0;   // blocks and scale chunks before this one
     bool ok = true;
-    for (int u = blockIdx.x >> 1; u < num_units; u += gridDim.x >> 1) {
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
         const SUnit t = sunit_of(p, u);
-        const int n = t.nt * kTileN + static_cast<int>(rank) * 128 + lrow;
+        const int n = t.nt * kSTile + lrow;
         float2 acc[kT / 2];
 #pragma unroll
         for (int j = 0; j < kT / 2; ++j) acc[j] = make_float2(0.f, 0.f);
+        int jr = -1;   // row in the scale chunk
         for (int i = 0; i < t.n; ++i, ++v) {
-            const int ab = static_cast<int>(v % kAcc), ss = v % kSScStages;
-            if (ok) {
-                ok = dev::mbar_wait(&s.sc_full[ss], (v / kSScStages) & 1, abort_flag) &&
-                     dev::mbar_wait(&s.acc_full[ab], (v / kAcc) & 1, abort_flag);
-                ok = __all_sync(0xFFFFFFFFu, ok);
+            const int ab = static_cast<int>(v % kAcc);
+            if (++jr == C) jr = 0;
+            const int slot = static_cast<int>(ck % kSSc);
+            if (ok && jr == 0) {
+                // a new scale chunk: this warp's FP32 copy of its activation scales (rows of T)
+                ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&s.scl_full[slot], (ck / kSSc) & 1, abort_flag));
+                if (ok && !kPartials) {
+                    const int x0 = ((t.b0 + i) * p.M) & ~7;
+                    for (int e = lane; e < C * kT; e += 32) {
+                        const int j = e / kT, m = e % kT;
+                        float v = 0.0f;
+                        if (p.sx_rows)
+                            v = __half2float(__ushort_as_half(s.sxr[slot][e]));
+                        else if (m < p.M && i + j < t.n)
+                            v = __half2float(__ushort_as_half(s.sxr[slot][(t.b0 + i + j) * p.M + m - x0]));
+                        s.sxf[q][e] = v;
+                    }
+                    __syncwarp();
+                }
             }
+            if (ok) ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&s.blk_empty[v % kSBlk], (v / kSBlk) & 1, abort_flag));
             if (ok && kPartials) {
                 // export the exact partial sums of block t.block(i) for the window: column j of
                 // the accumulator is token j, P = D * 2^18 (operand encoding)
@@ -369,9 +513,11 @@ __device__ __forceinline__ void s_epilogue_role(const SParams& p, SSmem<kT>& s, 
                 dev::tc_fence_before();
             } else if (ok) {
                 dev::tc_fence_after();
-                const SScaleSlot& sl = s.sc[ss];
-                const float swr = sl.sw[lrow];
-                const float2 sw2 = make_float2(swr, swr);
+                // sw * 2^18 * sx: the accumulator holds P * 2^-18 (operand encoding); scaling by a
+                // power of two is exact, so this is the product sw * sx * P rounded once per term
+                const float swv = __half2float(__ushort_as_half(s.swr[slot][jr][lrow])) * 262144.0f;
+                const float2 sw2 = make_float2(swv, swv);
+                const float4* sxv = reinterpret_cast<const float4*>(&s.sxf[q][jr * kT]);
                 const uint32_t taddr = tmem + lane_addr + static_cast<uint32_t>(ab * kT);
                 uint32_t d0[16], d1[16];
                 dev::tmem_ld16(taddr, d0);
@@ -381,25 +527,28 @@ __device__ __forceinline__ void s_epilogue_role(const SParams& p, SSmem<kT>& s, 
                     uint32_t (&dn)[16] = (c & 1) ? d0 : d1;
                     dev::tmem_ld_wait16(dc);
                     if (c + 1 < kChunks) dev::tmem_ld16(taddr + (c + 1) * 16, dn);
-                    const float4* sxv = reinterpret_cast<const float4*>(sl.sx + 16 * c);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float4 x = sxv[i];   // same address in every lane: one broadcast
+                    for (int k = 0; k < 4; ++k) {
+                        const float4 x = sxv[4 * c + k];   // same address in every lane: one broadcast
                         const float2 c0 = dev::fmul2(sw2, make_float2(x.x, x.y));
                         const float2 c1 = dev::fmul2(sw2, make_float2(x.z, x.w));
-                        const int j = 8 * c + 2 * i;
-                        acc[j] = dev::ffma2(make_float2(__uint_as_float(dc[4 * i]), __uint_as_float(dc[4 * i + 1])), c0, acc[j]);
-                        acc[j + 1] = dev::ffma2(make_float2(__uint_as_float(dc[4 * i + 2]), __uint_as_float(dc[4 * i + 3])), c1, acc[j + 1]);
+                        const int j = 8 * c + 2 * k;
+                        acc[j] = dev::ffma2(make_float2(__uint_as_float(dc[4 * k]), __uint_as_float(dc[4 * k + 1])), c0, acc[j]);
+                        acc[j + 1] = dev::ffma2(make_float2(__uint_as_float(dc[4 * k + 2]), __uint_as_float(dc[4 * k + 3])), c1, acc[j + 1]);
                     }
                 }
                 dev::tc_fence_before();
             }
             __syncwarp();
             if (lane == 0 && ok) {
-                // accumulator ab is free for block v + kAcc, whose MMAs the even CTA issues
-                dev::mbar_arrive_remote(leader_blk_full + static_cast<uint32_t>((v + kAcc) % kSBlk) * 8u);
-                dev::mbar_arrive(&s.sc_empty[ss]);
+                // accumulator ab is free for block v + kAcc
+                dev::mbar_arrive(&s.blk_full[(v + kAcc) % kSBlk]);
+                if (jr == C - 1 || i == t.n - 1) dev::mbar_arrive(&s.scl_empty[slot]);   // the chunk is read
             }
+            if (jr == C - 1 || i == t.n - 1) ++ck;
+        }
+        if constexpr (kPartials) {
+            continue;   // the window's partial sums are written; no output
         }
         auto store = [&]() {
             if (n >= p.N) return;
@@ -409,210 +558,255 @@ __device__ __forceinline__ void s_epilogue_role(const SParams& p, SSmem<kT>& s, 
                 if (2 * j + 1 < mvalid) p.Y[static_cast<int64_t>(2 * j + 1) * p.ldy + n] = __half_as_ushort(__float2half_rn(acc[j].y));
             }
         };
-        if constexpr (kPartials) {
-            continue;   // the window's partial sums are written; no output
-        }
         if (p.splits == 1) {
             store();
-        } else {
-            // split-K: publish this split's partial (this CTA's 128 channels x T); the last
-            // split to arrive sums all of them in split order (deterministic)
-            const int hrow = static_cast<int>(rank) * 128 + lrow;
-            float* mine = p.ws_partial + ((static_cast<int64_t>(t.nt) * p.splits + t.split) * 256 + hrow) * kT;
+        } else if (ok) {
+            // split-K inside the cluster (one CTA per split of the tile, rank = split): the
+            // other splits' partials meet in rank 0's shared memory, which its pipeline no
+            // longer uses once its last block's MMAs are done, and rank 0 adds them to its own
+            // in split order (deterministic) and stores Y.
+            float* recv = reinterpret_cast<float*>(&s.cvA[0][0]);   // [splits - 1][128][T] in rank 0
+            dev::cluster_wait_acquire();   // every CTA of the cluster has initialised its barriers
+            if (t.split == 0) {
+                if (et == 0)
+                    for (int r = 1; r < p.splits; ++r) dev::mbar_arrive_remote_release(dev::mapa(&s.red_ready, r));
+                ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait_cluster(&s.red_full, 0));
+                if (ok) {
+                    for (int r = 1; r < p.splits; ++r) {
+                        const float4* o = reinterpret_cast<const float4*>(recv + (static_cast<int64_t>(r - 1) * kSTile + lrow) * kT);
 #pragma unroll
-            for (int j = 0; j < kT / 2; j += 2)
-                __stcg(reinterpret_cast<float4*>(mine + 2 * j), make_float4(acc[j].x, acc[j].y, acc[j + 1].x, acc[j + 1].y));
-            __threadfence();
-            dev::named_bar_sync(1, kSEpiWarps * 32);
-            if (et == 0) {
-                int32_t* cnt = p.ws_count + t.nt * 2 + rank;
-                const int prev = atomicAdd(cnt, 1);
-                const int last = (prev == p.splits - 1);
-                if (last) *cnt = 0;   // reusable for the next call
-                s.fixup_last = last;
-            }
-            dev::named_bar_sync(1, kSEpiWarps * 32);
-            if (s.fixup_last) {
-                __threadfence();
-#pragma unroll
-                for (int j = 0; j < kT / 2; ++j) acc[j] = make_float2(0.f, 0.f);
-                for (int sp = 0; sp < p.splits; ++sp) {
-                    const float* o = p.ws_partial + ((static_cast<int64_t>(t.nt) * p.splits + sp) * 256 + hrow) * kT;
-#pragma unroll
-                    for (int j = 0; j < kT / 2; j += 2) {
-                        const float4 f = __ldcg(reinterpret_cast<const float4*>(o + 2 * j));
-                        acc[j].x += f.x;
-                        acc[j].y += f.y;
-                        acc[j + 1].x += f.z;
-                        acc[j + 1].y += f.w;
+                        for (int j = 0; j < kT / 2; j += 2) {
+                            const float4 f = o[j / 2];
+                            acc[j].x += f.x;
+                            acc[j].y += f.y;
+                            acc[j + 1].x += f.z;
+                            acc[j + 1].y += f.w;
+                        }
                     }
+                    store();
                 }
-                store();
+            } else {
+                ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait_cluster(&s.red_ready, 0));
+                if (ok) {
+                    const uint32_t dst = dev::mapa(recv + (static_cast<int64_t>(t.split - 1) * kSTile + lrow) * kT, 0);
+#pragma unroll
+                    for (int j = 0; j < kT / 2; j += 2)
+                        dev::st_cluster_v4(dst + static_cast<uint32_t>(j) * 8u, acc[j].x, acc[j].y, acc[j + 1].x, acc[j + 1].y);
+                    __syncwarp();
+                    if (lane == 0) dev::mbar_arrive_remote_release(dev::mapa(&s.red_full, 0));
+                }
             }
-            dev::named_bar_sync(1, kSEpiWarps * 32);   // fixup_last is read before the next unit rewrites it
         }
     }
     if (!ok && lane == 0) sfail(p, abort_flag);
 }
 
 template <int kT, bool kPartials>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSThreads, 1) w4ax_gemm_small_kernel(const SParams p) {
+__global__ void __launch_bounds__(kSThreads, 1)
+    w4ax_gemm_small_kernel(const SParams p, const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tma,
+                           const __grid_constant__ CUtensorMap tmsw, const __grid_constant__ CUtensorMap tmsx) {
     extern __shared__ uint8_t smem_raw[];
     SSmem<kT>& s = *reinterpret_cast<SSmem<kT>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     constexpr int kAcc = acc_slots<kT>();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t rank = dev::cluster_ctarank();
 
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kSBlk; ++i) {
-            // activation producer (expect-tx) + one converter group; in the even CTA also the
-            // odd CTA's forward and the epilogue warps of both CTAs (accumulator released)
-            dev::mbar_init(&s.blk_full[i], 1 + kSConvWarps + (rank == 0 ? 1 + 2 * kSEpiWarps : 0));
+    // barriers: a few per thread of the first two warps, each thread fencing its own inits
+    {
+        constexpr int kW = w_stages<kT>();
+        const int i = threadIdx.x;
+        if (i < kSBlk) {
+            if (i < a_copies<kT>()) dev::mbar_init(&s.a_full[i], 1);    // the activation producer's expect-tx
+            dev::mbar_init(&s.blk_full[i], kSConvWarps + kSEpiWarps);  // a converter group, the epilogue
             dev::mbar_init(&s.blk_empty[i], 1);
+        } else if (i < kSBlk + kW) {
+            dev::mbar_init(&s.w_full[i - kSBlk], 1);
+            dev::mbar_init(&s.w_empty[i - kSBlk], kSQuad * kSConvWarps);  // a converter group per block
+        } else if (i < kSBlk + kW + kSSc) {
+            dev::mbar_init(&s.scl_full[i - kSBlk - kW], 1);
+            dev::mbar_init(&s.scl_empty[i - kSBlk - kW], kSEpiWarps);
+        } else if (i == kSBlk + kW + kSSc) {
+#pragma unroll
+            for (int w = 0; w < kMaxBlocks / 32; ++w) s.maskw[w] = p.mask_bits[w];
+            for (int j = 0; j < 2; ++j) dev::mbar_init(&s.mma_done[j], 1);
+            dev::mbar_init(&s.red_ready, 1);
+            dev::mbar_init(&s.red_full, p.splits > 1 ? (p.splits - 1) * kSEpiWarps : 1);
+            s.abort_flag = 0;
         }
-        for (int i = 0; i < w_stages<kT>(); ++i) {
-            dev::mbar_init(&s.w_full[i], 1);
-            dev::mbar_init(&s.w_empty[i], kSConvWarps);
-        }
-        for (int i = 0; i < kSScStages; ++i) {
-            dev::mbar_init(&s.sc_full[i], kSConvWarps);
-            dev::mbar_init(&s.sc_empty[i], kSEpiWarps);
-        }
-        for (int i = 0; i < kAcc; ++i) dev::mbar_init(&s.acc_full[i], 1);
-        dev::mbar_init(&s.mma_done, 1);
-        s.abort_flag = 0;
-        if (rank == 0) {
-            // the first kAcc blocks find their accumulators free
-            for (int i = 0; i < kAcc; ++i)
-                for (int k = 0; k < 2 * kSEpiWarps; ++k) dev::mbar_arrive(&s.blk_full[i]);
-        }
-        dev::fence_barrier_init();
+        static_assert(kSBlk + w_stages<kT>() + kSSc + 1 <= 64, "barrier init spans two warps");
+        if (i < 64) dev::fence_barrier_init();   // each initializing thread publishes its own
     }
-    for (int b = threadIdx.x; b < p.nb; b += kSThreads) {
-        s.mask[b] = p.mask[b];
-        s.poff[b] = p.poff[b];
+    __syncthreads();
+    dev::cluster_arrive_release();   // split-K: the barriers are ready for the other CTAs' arrivals
+    if (threadIdx.x < kAcc * kSEpiWarps) {
+        // the first kAcc blocks find their accumulators free
+        dev::mbar_arrive(&s.blk_full[threadIdx.x / kSEpiWarps]);
     }
-    if (warp < kMaxBlocks / 32) {
-        const int b = warp * 32 + lane;
-        const uint32_t bits = __ballot_sync(0xFFFFFFFFu, b < p.nb && p.mask[b] != 0);
-        if (lane == 0) s.maskw[warp] = bits;
-    }
-    // token rows at or past M are never copied: they must read as zero codes
-    for (int i = threadIdx.x; i < kSBSlots * (kT / 2) * 128 / 16; i += kSThreads)
-        reinterpret_cast<uint4*>(&s.opB[0][0])[i] = make_uint4(0u, 0u, 0u, 0u);
-    dev::fence_proxy_async_smem();
-    if (warp == 1) dev::tmem_alloc_pair(&s.tmem_base, kSTmemCols);
+    if (warp == 1) dev::tmem_alloc(&s.tmem_base, kSTmemCols);
     dev::tc_fence_before();
     __syncthreads();
-    dev::cluster_sync();
     dev::tc_fence_after();
     const uint32_t tmem = s.tmem_base;
     volatile int* abort_flag = &s.abort_flag;
 
-    if (warp < 8) {
-        dev::setmaxnreg_dec<64>();
-        if (warp == 0) {
-            s_weight_producer<kT>(p, s, rank, lane, abort_flag);
-        } else if (warp == 1) {
-            s_mma_role<kT>(p, s, rank, lane, tmem, abort_flag);
-        } else if (warp >= 2 && warp < 2 + kSConvWarps) {
-            s_converter_role<kT>(p, s, rank, 0, (warp - 2) * 32 + lane, lane, abort_flag);
-        } else if (warp == 6) {
-            s_activation_producer<kT>(p, s, rank, lane, abort_flag);
-        }
+    // (no per-role register split: at 128 registers a thread every role fits)
+    if (warp == 0) {
+        if (lane == 0) dev::tma_prefetch_map(&tmw);
+        s_weight_producer<kT>(p, &tmw, s, lane, abort_flag);
     } else {
-        dev::setmaxnreg_inc<192>();
-        if (warp < 8 + kSEpiWarps) {
-            s_epilogue_role<kT, kPartials>(p, s, rank, warp & 3, lane, tmem, abort_flag);
+        if (warp < 8) {
+            if (warp == 1 || warp == 7) {
+                static_assert(kSIssuers == 2, "issuer warps 1, 7");
+                s_mma_role<kT>(p, s, lane, tmem, warp == 1 ? 0 : 1, abort_flag);
+            } else if (warp == 6) {
+                if (lane == 0) {
+                    dev::tma_prefetch_map(&tma);
+                    dev::tma_prefetch_map(&tmsw);
+                    dev::tma_prefetch_map(&tmsx);
+                }
+                s_operand_producer<kT>(p, &tma, &tmsw, &tmsx, s, lane, abort_flag);
+            } else if (warp >= 2 && warp < 2 + kSConvWarps) {
+                s_converter_role<kT>(p, s, 0, (warp - 2) * 32 + lane, lane, abort_flag);
+            }
         } else {
-            s_converter_role<kT>(p, s, rank, 1, (warp - 12) * 32 + lane, lane, abort_flag);
+            if (warp < 8 + kSEpiWarps) {
+                s_epilogue_role<kT, kPartials>(p, s, warp & 3, lane, tmem, abort_flag);
+            } else {
+                s_converter_role<kT>(p, s, 1, (warp - 12) * 32 + lane, lane, abort_flag);
+            }
         }
     }
 
     dev::tc_fence_before();
     __syncthreads();
-    dev::cluster_sync();   // the peer's MMAs, commits and arrivals on this CTA are done
     if (warp == 1) {
         dev::tc_fence_after();
-        dev::tmem_dealloc_pair(tmem, kSTmemCols);
+        dev::tmem_dealloc(tmem, kSTmemCols);
     }
 }
 
 template <int kT>
 constexpr size_t small_smem_bytes() { return sizeof(SSmem<kT>) + 1024; }
 
-int tokens_tile(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128; }
-
+// Shared memory from the converted-weight stages through the packed-weight ring: free once a
+// CTA's last MMAs are done, it receives the other splits' partial sums in a cluster's rank 0.
 template <int kT>
-int small_max_pairs_t(const fmpq_layout& L) {
-    static int cached[64] = {};
-    const int dev = L.device;
-    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
-    int pairs = L.num_sms / 2 > 0 ? L.num_sms / 2 : 1;
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
-    cfg.blockDim = dim3(kSThreads);
-    cfg.dynamicSmemBytes = small_smem_bytes<kT>();
-    int clusters = 0;
-    if (ensure_smem_limit(reinterpret_cast<const void*>(w4ax_gemm_small_kernel<kT, false>),
-                          static_cast<int>(small_smem_bytes<kT>())) == cudaSuccess &&
-        cudaOccupancyMaxActiveClusters(&clusters, w4ax_gemm_small_kernel<kT, false>, &cfg) == cudaSuccess && clusters > 0 &&
-        clusters < pairs)
-        pairs = clusters;
-    cudaGetLastError();   // a failed query leaves no sticky error behind
-    if (dev >= 0 && dev < 64) cached[dev] = pairs;
-    return pairs;
+constexpr size_t recv_bytes_t() { return offsetof(SSmem<kT>, swr); }
+size_t recv_bytes(int T) {
+    return T <= 16 ? recv_bytes_t<16>() : T <= 32 ? recv_bytes_t<32>() : recv_bytes_t<64>();
 }
+static_assert(small_smem_bytes<16>() <= 232448 && small_smem_bytes<32>() <= 232448 &&
+                  small_smem_bytes<64>() <= 232448,
+              "shared memory of the few-token GEMM exceeds the 227 KB a CTA may use");
 
-int small_max_pairs(const fmpq_layout& L, int T) {
-    switch (T) {
-        case 16: return small_max_pairs_t<16>(L);
-        case 32: return small_max_pairs_t<32>(L);
-        case 64: return small_max_pairs_t<64>(L);
-        default: return small_max_pairs_t<128>(L);
-    }
-}
+int tokens_tile(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : 64; }
 
-// Splits so that the units (tiles x splits) come close to one per resident pair.
+// CTAs that can be resident at once (one per SM): the persistent grid never launches more.
+int small_max_ctas(const fmpq_layout& L) { return L.num_sms > 0 ? L.num_sms : 1; }
+
+// Splits so that the units (tiles x splits) come close to one per SM. A tile's splits run as
+// one cluster (at most 8 CTAs) whose rank 0 receives the others' partials in the shared memory
+// its pipeline has finished with.
 int small_splits(const fmpq_layout& L, int64_t ntiles, int T) {
-    const int pairs = small_max_pairs(L, T);
-    if (ntiles * 2 > pairs) return 1;
-    int s = static_cast<int>(pairs / ntiles);
+    const int ctas = small_max_ctas(L);
+    if (ntiles * 2 > ctas) return 1;
+    int s = static_cast<int>(ctas / ntiles);
     if (s > L.nb) s = L.nb;
-    if (s > 16) s = 16;
+    if (s > 8) s = 8;
+    const int room = 1 + static_cast<int>(recv_bytes(T) / (static_cast<size_t>(kSTile) * T * sizeof(float)));
+    if (s > room) s = room;
     return s < 1 ? 1 : s;
 }
 
+struct SMaps {
+    CUtensorMap w, a, sw, sx;
+};
+
 template <int kT>
-cudaError_t launch_small_t(const fmpq_layout& L, const SParams& p, int pairs, cudaStream_t stream) {
+cudaError_t launch_small_t(const SParams& p, const SMaps& m, int ctas, cudaStream_t stream) {
     const void* fn = p.P != nullptr ? reinterpret_cast<const void*>(w4ax_gemm_small_kernel<kT, true>)
                                     : reinterpret_cast<const void*>(w4ax_gemm_small_kernel<kT, false>);
     const cudaError_t e = ensure_smem_limit(fn, static_cast<int>(small_smem_bytes<kT>()));
     if (e != cudaSuccess) return e;
-    if (p.P != nullptr)
-        w4ax_gemm_small_kernel<kT, true><<<2 * pairs, kSThreads, small_smem_bytes<kT>(), stream>>>(p);
-    else
-        w4ax_gemm_small_kernel<kT, false><<<2 * pairs, kSThreads, small_smem_bytes<kT>(), stream>>>(p);
-    return cudaGetLastError();
+    if (p.P != nullptr) {
+        w4ax_gemm_small_kernel<kT, true><<<ctas, kSThreads, small_smem_bytes<kT>(), stream>>>(p, m.w, m.a, m.sw, m.sx);
+        return cudaGetLastError();
+    }
+    // the splits of a tile are consecutive CTAs: one cluster per tile (ctas = tiles x splits)
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+    cfg.blockDim = dim3(kSThreads);
+    cfg.dynamicSmemBytes = small_smem_bytes<kT>();
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.splits);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, w4ax_gemm_small_kernel<kT, false>, p, m.w, m.a, m.sw, m.sx);
+}
+
+bool encode(CUtensorMap* map, CUtensorMapDataType type, int rank, const void* base, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box) {
+    const EncodeTiledFn enc = encode_tiled();
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return enc != nullptr &&
+           enc(map, type, static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The packed weights as a 4-D byte tensor {256 bytes, 32 lines, 2 halves, groups * nb blocks}:
+// a half (128 rows x 64 bytes) is 8 KB contiguous, read as 32 lines of 256 bytes, and a box of
+// {256, 32, 1, 2} is the CTA's 128 rows of two consecutive blocks, 16 KB. (Boxes with a
+// narrow inner extent, such as the 64-byte rows themselves, move far fewer bytes per cycle.)
+// The packed activations as {128 bytes, M token rows, planes}: a box of {128, T, P} is P planes
+// of T rows, the rows past M zero. The weight scales as {N, nb} fp16, boxes of {128, C}; the
+// activation scales as {M, nb} fp16 with boxes of {T, C} when rows are 16-byte multiples
+// (M % 8 == 0), else as a run of nb * M with boxes of sx_box elements.
+template <int kT>
+bool make_small_maps(SMaps* m, SParams* p, const fmpq_layout& L, const GemmArgs& a) {
+    const int64_t groups = (a.N + kTileN - 1) / kTileN;
+    const cuuint64_t wd[4] = {256, 32, 2, static_cast<cuuint64_t>(groups * L.nb)};
+    const cuuint64_t ws[3] = {256, 128 * 64, 256 * 64};
+    const cuuint32_t wb[4] = {256, 32, 1, kSQuad};
+    const cuuint64_t ad[3] = {128, static_cast<cuuint64_t>(a.M), static_cast<cuuint64_t>(L.planes)};
+    const cuuint64_t as[2] = {128, static_cast<cuuint64_t>(a.M) * 128};
+    const cuuint32_t ab[3] = {128, static_cast<cuuint32_t>(kT), static_cast<cuuint32_t>(a_planes<kT>())};
+    int C = scale_chunk<kT>();
+    p->sx_rows = a.M % 8 == 0 ? 1 : 0;
+    if (!p->sx_rows && C > static_cast<int>((256 - 7) / a.M)) C = static_cast<int>((256 - 7) / a.M);
+    p->sc_chunk = C;
+    p->sx_box = static_cast<int>((C * a.M + 7 + 7) / 8 * 8);
+    const cuuint64_t swd[2] = {static_cast<cuuint64_t>(a.N), static_cast<cuuint64_t>(L.nb)};
+    const cuuint64_t sws[1] = {static_cast<cuuint64_t>(a.N) * 2};
+    const cuuint32_t swb[2] = {128, static_cast<cuuint32_t>(C)};
+    if (!encode(&m->w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, a.W, wd, ws, wb) ||
+        !encode(&m->a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.A, ad, as, ab) ||
+        !encode(&m->sw, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, a.w_scales, swd, sws, swb))
+        return false;
+    if (p->sx_rows) {
+        const cuuint64_t d[2] = {static_cast<cuuint64_t>(a.M), static_cast<cuuint64_t>(L.nb)};
+        const cuuint64_t st[1] = {static_cast<cuuint64_t>(a.M) * 2};
+        const cuuint32_t b[2] = {static_cast<cuuint32_t>(kT), static_cast<cuuint32_t>(C)};
+        return encode(&m->sx, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, a.a_scales, d, st, b);
+    }
+    const cuuint64_t d[1] = {static_cast<cuuint64_t>(L.nb) * static_cast<cuuint64_t>(a.M)};
+    const cuuint64_t st[1] = {d[0] * 2};   // (a rank-1 map has no strides; not read)
+    const cuuint32_t b[1] = {static_cast<cuuint32_t>(p->sx_box)};
+    return encode(&m->sx, CU_TENSOR_MAP_DATA_TYPE_UINT16, 1, a.a_scales, d, st, b);
 }
 
 }  // namespace
 
-bool gemm_small_path(int64_t M) { return M >= 1 && M <= 128; }
+// Up to 64 tokens; from 65 on, the main GEMM's 256-token tiles are faster than one CTA
+// holding 128 tokens' running sums per output channel (measured at M = 96 and 128).
+bool gemm_small_path(int64_t M) { return M >= 1 && M <= 64; }
 
-size_t gemm_small_counter_bytes(const fmpq_layout& L, int64_t M, int64_t N) {
-    const int64_t ntiles = (N + kTileN - 1) / kTileN;
-    if (small_splits(L, ntiles, tokens_tile(M)) == 1) return 0;
-    return static_cast<size_t>(ntiles) * 2 * sizeof(int32_t) + 16;
-}
-
-size_t gemm_small_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N) {
-    const int64_t ntiles = (N + kTileN - 1) / kTileN;
-    const int T = tokens_tile(M);
-    const int splits = small_splits(L, ntiles, T);
-    if (splits == 1) return 0;
-    return static_cast<size_t>(ntiles) * splits * 256 * T * sizeof(float) + gemm_small_counter_bytes(L, M, N);
-}
+// Split-K partials meet in a cluster's shared memory: no workspace.
+size_t gemm_small_counter_bytes(const fmpq_layout&, int64_t, int64_t) { return 0; }
+size_t gemm_small_workspace_bytes(const fmpq_layout&, int64_t, int64_t) { return 0; }
 
 cudaError_t launch_gemm_small(const fmpq_layout& L, const GemmArgs& a, cudaStream_t stream) {
     SParams p{};
@@ -625,11 +819,11 @@ cudaError_t launch_gemm_small(const fmpq_layout& L, const GemmArgs& a, cudaStrea
     p.M = static_cast<int>(a.M);
     p.N = static_cast<int>(a.N);
     p.nb = L.nb;
-    p.mask = L.d_mask;
-    p.poff = L.d_poff;
+    static_assert(sizeof(L.mask_bits) * 8 >= kMaxBlocks, "block bitmap too small");
+    for (int w = 0; w < kMaxBlocks / 32; ++w) p.mask_bits[w] = L.mask_bits[w];
     p.status = L.d_status;
     const int T = tokens_tile(a.M);
-    p.ntiles = static_cast<int>((a.N + kTileN - 1) / kTileN);
+    p.ntiles = static_cast<int>((a.N + kSTile - 1) / kSTile);
     p.splits = small_splits(L, p.ntiles, T);
     if (a.P != nullptr) {
         // partial-sum export: every unit writes its blocks' sums directly (no workspace)
@@ -638,19 +832,24 @@ cudaError_t launch_gemm_small(const fmpq_layout& L, const GemmArgs& a, cudaStrea
         p.pmcount = static_cast<int>(a.pmcount);
         p.pn0 = static_cast<int>(a.pn0);
         p.pncount = static_cast<int>(a.pncount);
-    } else if (p.splits > 1) {
-        p.ws_partial = static_cast<float*>(a.workspace);
-        p.ws_count = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(a.workspace) +
-                                                static_cast<size_t>(p.ntiles) * p.splits * 256 * T * sizeof(float));
     }
-    const int64_t units = static_cast<int64_t>(p.ntiles) * p.splits;
-    const int maxp = small_max_pairs(L, T);
-    const int pairs = static_cast<int>(units < maxp ? units : maxp);
+    SMaps maps;
+    bool mapped = false;
     switch (T) {
-        case 16: return launch_small_t<16>(L, p, pairs, stream);
-        case 32: return launch_small_t<32>(L, p, pairs, stream);
-        case 64: return launch_small_t<64>(L, p, pairs, stream);
-        default: return launch_small_t<128>(L, p, pairs, stream);
+        case 16: mapped = make_small_maps<16>(&maps, &p, L, a); break;
+        case 32: mapped = make_small_maps<32>(&maps, &p, L, a); break;
+        case 64: mapped = make_small_maps<64>(&maps, &p, L, a); break;
+        default: mapped = make_small_maps<64>(&maps, &p, L, a); break;
+    }
+    if (!mapped) return cudaErrorNotSupported;
+    const int64_t units = static_cast<int64_t>(p.ntiles) * p.splits;
+    const int maxc = small_max_ctas(L);
+    const int ctas = static_cast<int>(units < maxc ? units : maxc);
+    switch (T) {
+        case 16: return launch_small_t<16>(p, maps, ctas, stream);
+        case 32: return launch_small_t<32>(p, maps, ctas, stream);
+        case 64: return launch_small_t<64>(p, maps, ctas, stream);
+        default: return launch_small_t<64>(p, maps, ctas, stream);
     }
 }
 

@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 struct fmpq_layout {
@@ -17,6 +18,7 @@ struct fmpq_layout {
     int32_t* d_poff = nullptr;     // [nb] first code plane of each block (planes before it)
     int32_t* d_status = nullptr;   // device status word
     int32_t planes = 0;            // code planes: n4 + 2*n8
+    uint32_t mask_bits[8] = {};    // the INT8 blocks as a bitmap (bit b % 32 of word b / 32)
     int64_t row_bytes = 0;         // packed-A bytes per token: 128 * planes
 };
 
@@ -30,6 +32,13 @@ constexpr int kTileN = 256;          // packed-weight row grouping and GEMM tile
 // attributes are per device: the first call for each (kernel, device) sets it, later calls
 // return at once. Thread-safe.
 cudaError_t ensure_smem_limit(const void* kernel, int bytes);
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime (no link to
+// libcuda); nullptr when the driver does not provide it.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled();
 
 // Launchers (return cudaGetLastError() after the launch).
 // gamma_perm != nullptr: the quantized values are the row's RMSNorm with that gamma (permuted

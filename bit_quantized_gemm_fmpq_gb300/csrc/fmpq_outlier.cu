@@ -178,25 +178,6 @@ __global__ void __launch_bounds__(kOThreads, 2)
     }
 }
 
-// cuTensorMapEncodeTiled from the driver, looked up through the runtime (no link to libcuda).
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_tiled() {
-    static EncodeTiledFn fn = []() -> EncodeTiledFn {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess) {
-            cudaGetLastError();
-            return nullptr;
-        }
-        return reinterpret_cast<EncodeTiledFn>(p);
-    }();
-    return fn;
-}
-
 // A 2-D fp16 tensor [rows][cols] with row stride ld (elements), read in boxes of 64 x box_rows
 // with the 128-byte swizzle.
 bool make_map(EncodeTiledFn enc, CUtensorMap* map, const void* base, int64_t cols, int64_t rows, int64_t ld,
@@ -211,6 +192,20 @@ bool make_map(EncodeTiledFn enc, CUtensorMap* map, const void* base, int64_t col
 }
 
 }  // namespace
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
 
 cudaError_t launch_outlier_gemm(const void* X, int64_t ldx, int64_t M, const int32_t* cols, int n_out,
                                 const void* W_out, int64_t ldw_out, int64_t N, void* X_out, void* Y, int64_t ldy,

@@ -55,12 +55,14 @@ def test_tiny_config(fmpq_mod, oracle_mod):
     (200, 512, 1024, 8),     # all INT8
     (200, 512, 1024, 0),     # all INT4
     (40, 256, 128, 0),       # single block
-    # few tokens (the operand-swapped GEMM): token tiles of 16/32/64/128, ragged N
+    # few tokens (the operand-swapped GEMM, M <= 64): token tiles of 16/32/64, ragged N
     (5, 272, 384, 1),        # 16-token tile, last channel tile 16 wide
     (17, 528, 1024, 2),      # 32-token tile with 17 tokens
-    (100, 784, 2048, 3),     # 128-token tile with 100 tokens, ragged N
-    (128, 400, 640, 5),      # all INT8, full 128-token tile
     (33, 256, 256, 0),       # all INT4, 64-token tile
+    (64, 400, 640, 5),       # all INT8, full 64-token tile
+    # 65-128 tokens: the main GEMM with one partly filled 256-token tile
+    (100, 784, 2048, 3),     # 100 tokens, ragged N
+    (128, 400, 640, 5),      # all INT8, 128 tokens
 ])
 def test_shapes(fmpq_mod, oracle_mod, M, N, K, n8):
     w = wl.synthetic(M, N, K, n8=n8, seed=M + N + K)
@@ -105,11 +107,15 @@ def test_strided_inputs_and_outputs(fmpq_mod, oracle_mod):
     layout.close()
 
 
-def test_repeated_calls_and_workspace_reuse(fmpq_mod, oracle_mod):
-    """Split-K workspace counters return to zero: repeated calls give identical output."""
-    w = wl.synthetic(16, 512, 2048, n8=2, seed=21)
+@pytest.mark.parametrize("M,uses_workspace", [
+    (16, False),    # few tokens: the splits of a tile meet in a cluster's shared memory
+    (256, True),    # the main GEMM's split-K: workspace counters return to zero
+])
+def test_repeated_calls_and_workspace_reuse(fmpq_mod, oracle_mod, M, uses_workspace):
+    """Split-K in both GEMMs: repeated calls give identical output."""
+    w = wl.synthetic(M, 512, 2048, n8=2, seed=21)
     layout = fmpq_mod.Layout(w.K, w.perm, w.mask)
-    assert layout.workspace_bytes(w.M, w.N) > 0
+    assert (layout.workspace_bytes(w.M, w.N) > 0) == uses_workspace
     Xd, Wd = to_dev(w.X), to_dev(w.W)
     A, sx = fmpq_mod.fmpq_quantize(layout, Xd)
     Wp, sw = fmpq_mod.w4_pack_weights(layout, Wd)
