@@ -305,25 +305,35 @@ def run_sweep(args):
         sampler.start()
         q_ms = timed(lambda: fmpq.fmpq_quantize(layout, X, A, sx))
         g_ms = timed(lambda: fmpq.w4ax_gemm(layout, A, sx, Wp, sw, M, N, Y, workspace=ws))
-        graph_ms = None
+        graph_ms = quant_graph_ms = step_graph_ms = None
         if M <= 128:
             copies = [Wp] + [Wp.clone() for _ in range(4)]   # 5 x packed W > L2
             reps = 20
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                for r in range(reps):
-                    fmpq.w4ax_gemm(layout, A, sx, copies[r % len(copies)], sw, M, N, Y, workspace=ws)
-            for _ in range(3):
-                g.replay()
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            for _ in range(5):
-                g.replay()
-            e1.record()
-            torch.cuda.synchronize()
-            graph_ms = e0.elapsed_time(e1) / (5 * reps)
-            del copies, g
+
+            def graph_time(body):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for r in range(reps):
+                        body(r)
+                for _ in range(3):
+                    g.replay()
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(5):
+                    g.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                return e0.elapsed_time(e1) / (5 * reps)
+
+            def gemm(r):
+                fmpq.w4ax_gemm(layout, A, sx, copies[r % len(copies)], sw, M, N, Y, workspace=ws)
+
+            graph_ms = graph_time(gemm)
+            quant_graph_ms = graph_time(lambda r: fmpq.fmpq_quantize(layout, X, A, sx))
+            # the decode step: quantize the token(s), then the GEMM
+            step_graph_ms = graph_time(lambda r: (fmpq.fmpq_quantize(layout, X, A, sx), gemm(r)))
+            del copies
         clocks = sampler.stop()
         if fmpq.fmpq_device_status(layout) != 0:
             raise RuntimeError(f"device status after {name}")
@@ -345,7 +355,9 @@ def run_sweep(args):
             "gemm_graph_frac": (max(t_tensor, t_hbm) / graph_ms) if graph_ms else None,
             "quant_ms": q_ms, "quant_gbs": qbytes / (q_ms * 1e-3) / 1e9,
             "quant_frac_hbm": qbytes / (q_ms * 1e-3) / 1e9 / hbm,
-            "l2": "flushed before every timed launch (graph: 5 rotating weight copies, no flush)",
+            "quant_graph_ms": quant_graph_ms, "step_graph_ms": step_graph_ms,
+            "l2": "flushed before every timed launch (graphs: back-to-back launches, 5 rotating weight "
+                  "copies, no flush)",
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

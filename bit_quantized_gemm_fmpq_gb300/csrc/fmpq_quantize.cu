@@ -657,6 +657,48 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
 }
 
 // ---------------------------------------------------------------------------------
+// Few tokens: one warp per (token, block pair) straight from X, the channels gathered through
+// the permutation with plain loads (the row stays in L1/L2 across the row's warps). The
+// row-pipelined kernel gives each CTA whole rows, so with fewer tokens than SMs most SMs idle
+// and each row's copy latency is exposed; this form spreads a token's blocks over the GPU.
+// Same code step as the row kernel, so the codes and scales are identical.
+// ---------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) quantize_direct_kernel(QuantParams p) {
+    const int lane = threadIdx.x & 31;
+    const bool upper = lane >= 16;
+    const int sub = lane & 15;
+    const uint32_t hmask = upper ? 0xFFFF0000u : 0x0000FFFFu;
+    const int pairs = (p.nb + 1) / 2;
+    const int64_t items = p.M * pairs;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t item = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); item < items;
+         item += warps) {   // warp-uniform
+        const int64_t m = item / pairs;
+        const int b = 2 * static_cast<int>(item % pairs) + (upper ? 1 : 0);
+        const bool valid = b < p.nb;
+        uint32_t h2[4] = {0u, 0u, 0u, 0u};
+        bool is8 = false;
+        int32_t poff_b = 0;
+        if (valid) {
+            // channels b*128 + 8*sub .. + 7 of the permuted order
+            const uint4 pv = __ldg(reinterpret_cast<const uint4*>(p.perm + static_cast<int64_t>(b) * kBlock + sub * 8));
+            const uint16_t* row = p.X + m * p.ldx;
+            const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                h2[k] = static_cast<uint32_t>(__ldg(row + (pw[k] & 0xFFFFu))) |
+                        (static_cast<uint32_t>(__ldg(row + (pw[k] >> 16))) << 16);
+            is8 = __ldg(p.mask + b) != 0;
+            poff_b = __ldg(p.poff + b);
+        }
+        const uint32_t chunk_off = ((static_cast<uint32_t>(sub >> 1) ^ static_cast<uint32_t>(m & 7)) << 4) +
+                                   static_cast<uint32_t>(sub & 1) * 8u;
+        quantize_codes_step<false>(h2, valid, is8, b, m, chunk_off, sub, hmask, poff_b, p.A, p.M, p.scales, nullptr,
+                                   0.0f);
+    }
+}
+
+// ---------------------------------------------------------------------------------
 // SwiGLU fused with the quantizer (QServe explainer, "运行时设计": the activation quantization of
 // the second FFN layer is fused into the activation kernel): h = fp16_rn(g * u / (1 + e^-g)),
 // then the symmetric quantizer on h. The gate and up outputs arrive in the layout's permuted
@@ -1043,6 +1085,15 @@ cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, in
     p.eps = eps;
     p.zeros = mode == kQAsym ? static_cast<uint16_t*>(aux) : nullptr;
     p.sums = mode == kQTok ? static_cast<int32_t*>(aux) : nullptr;
+    if (mode == kQSym && M < L.num_sms) {
+        // fewer tokens than SMs: a warp per (token, block pair) instead of a CTA per row
+        const int64_t items = M * ((L.nb + 1) / 2);
+        const int64_t ctas_needed = (items + 7) / 8;                       // 8 warps per CTA
+        const int64_t ctas_max = static_cast<int64_t>(L.num_sms) * 8;
+        quantize_direct_kernel<<<static_cast<unsigned>(ctas_needed < ctas_max ? ctas_needed : ctas_max), 256, 0,
+                                 stream>>>(p);
+        return cudaGetLastError();
+    }
     const int64_t ctas = static_cast<int64_t>(L.num_sms) * per_sm;
     const unsigned grid = static_cast<unsigned>(M < ctas ? M : ctas);
     const unsigned threads = static_cast<unsigned>((cw + 1 + rwarps) * 32);
