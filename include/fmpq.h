@@ -163,9 +163,11 @@ FMPQ_API fmpq_status w4_pack_weights(const fmpq_layout* layout, const void* W, i
 FMPQ_API fmpq_status w4_unpack_weights(const fmpq_layout* layout, const void* W_packed, int64_t N,
                               int8_t* Wq, void* stream);
 
-/* Workspace bytes w4ax_gemm needs for this shape (0 when it needs none). Shapes with few
- * output tiles split K across CTAs; the workspace then holds the FP32 partial tiles and one
- * arrival counter per output tile. */
+/* Workspace bytes w4ax_gemm needs for this shape (0 when it needs none). With M > 64 and few
+ * output tiles the GEMM splits K across CTA pairs; the workspace then holds the FP32 partial
+ * tiles and one arrival counter per output tile. With M <= 64 (the few-token kernel) the
+ * K-splits of a tile run as one thread-block cluster and meet in its shared memory: no
+ * workspace. */
 FMPQ_API size_t w4ax_gemm_workspace_bytes(const fmpq_layout* layout, int64_t M, int64_t N);
 
 /* The W4Ax GEMM:
