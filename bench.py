@@ -603,30 +603,61 @@ def main():
     quant_moved = 2 * M * K + layout.packed_a_bytes(M) + 2 * layout.nb * M   # what the kernel writes
     quant_gbs = quant_bytes / (quant_ms * 1e-3) / 1e9
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers: every step copies its input from
+    # pinned host memory and its result back. The steps run as a serving pipeline would: the
+    # input of step k + 1 is copied (on its own stream) while step k computes, and the result
+    # of step k is read back while step k + 1 computes (two device buffers for each). One timed
+    # region over all steps; no L2 flush inside it (X and the packed weights exceed L2).
     e2e = None
     if not args.no_e2e:
         Xh = torch.from_numpy(w.X).pin_memory()
-        Yh = torch.empty((M, N), dtype=torch.float16).pin_memory()
+        Yhs = [torch.empty((M, N), dtype=torch.float16).pin_memory() for _ in range(2)]
+        Xs = [X, torch.empty_like(X)]
+        Ys = [Y, torch.empty_like(Y)]
+        h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
         n_e2e = max(3, min(args.steps, 50))
-        for _ in range(2):
-            X.copy_(Xh, non_blocking=True)
-            step()
-            Yh.copy_(Y, non_blocking=True)
-        torch.cuda.synchronize()
-        t_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_e2e)]
-        for i in range(n_e2e):
-            t_ev[i][0].record(stream)
-            X.copy_(Xh, non_blocking=True)
-            step()
-            Yh.copy_(Y, non_blocking=True)
-            t_ev[i][1].record(stream)
-            flush.zero_()
-        torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in t_ev), world, "cuda")
+
+        def step_on(Xk, Yk):
+            fmpq.fmpq_quantize(layout, Xk, A, sx, stream=stream)
+            fmpq.w4ax_gemm(layout, A, sx, Wp, sw, M, N, Yk, workspace=ws, stream=stream)
+
+        def pipeline(n):
+            ev = lambda: torch.cuda.Event(enable_timing=False)
+            h2d_ev, comp_ev, d2h_ev = [ev() for _ in range(n)], [ev() for _ in range(n)], [ev() for _ in range(n)]
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            h2d.wait_event(t0)
+            with torch.cuda.stream(h2d):
+                Xs[0].copy_(Xh, non_blocking=True)
+            h2d_ev[0].record(h2d)
+            for k in range(n):
+                stream.wait_event(h2d_ev[k])
+                if k >= 2:
+                    stream.wait_event(d2h_ev[k - 2])        # result buffer k % 2 has been read back
+                step_on(Xs[k % 2], Ys[k % 2])
+                comp_ev[k].record(stream)
+                if k + 1 < n:
+                    if k >= 1:
+                        h2d.wait_event(comp_ev[k - 1])      # input buffer (k + 1) % 2 is free
+                    with torch.cuda.stream(h2d):
+                        Xs[(k + 1) % 2].copy_(Xh, non_blocking=True)
+                    h2d_ev[k + 1].record(h2d)
+                d2h.wait_event(comp_ev[k])
+                with torch.cuda.stream(d2h):
+                    Yhs[k % 2].copy_(Ys[k % 2], non_blocking=True)
+                d2h_ev[k].record(d2h)
+            stream.wait_event(d2h_ev[n - 1])
+            t1.record(stream)
+            torch.cuda.synchronize()
+            return t0.elapsed_time(t1) / n
+
+        pipeline(3)   # warm-up
+        e2e_ms = max_over_ranks(pipeline(n_e2e), world, "cuda")
         e2e = {"value": aggregate_tops(world, flops, e2e_ms), "unit": "TOPS",
-               "h2d_bytes_per_step": int(Xh.numel() * 2), "d2h_bytes_per_step": int(Yh.numel() * 2),
-               "ms_per_step": e2e_ms}
+               "h2d_bytes_per_step": int(Xh.numel() * 2), "d2h_bytes_per_step": int(Yhs[0].numel() * 2),
+               "ms_per_step": e2e_ms,
+               "pipeline": "each step's input copy and result read-back overlap the neighbouring steps' "
+                           "compute (two device buffers each, copy streams); one timed region over the steps"}
 
     if rank != 0:
         if world > 1:
