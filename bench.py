@@ -423,11 +423,24 @@ def run_sweep(args):
         ws = layout.workspace(w.M, w.N)
         fmpq.fmpq_quantize(layout, X, A, sx)
         sampler.start()
+        ms_q = timed(lambda: fmpq.fmpq_quantize(layout, X, A, sx))
+        ms_qs = timed(lambda: fmpq.fmpq_quantize_split(layout, X, cols, A_packed=A, a_scales=sx, X_out=X_out))
         ms_base = timed(lambda: fmpq.w4ax_gemm(layout, A, sx, Wp, sw, w.M, w.N, Y, workspace=ws))
         ms_out = timed(lambda: fmpq.fmpq_outlier_gemm_fp16(layout, X, cols, W_out, Y, X_out))
+        ms_prod = timed(lambda: fmpq.fmpq_outlier_product_fp16(layout, X_out, W_out, Y))
+
+        def fused_step():
+            # the QUIK forward pass with the split in the quantizer's pass over X
+            fmpq.fmpq_quantize_split(layout, X, cols, A_packed=A, a_scales=sx, X_out=X_out)
+            fmpq.w4ax_gemm(layout, A, sx, Wp, sw, w.M, w.N, Y, workspace=ws)
+            fmpq.fmpq_outlier_product_fp16(layout, X_out, W_out, Y)
+        ms_step = timed(fused_step)
         clocks = sampler.stop()
         print(json.dumps({"sweep": "outlier_split_llama70b_down", "M": w.M, "K_base": Kb, "n_out": n_out, "N": w.N,
-                          "int4_path_ms": ms_base, "fp16_outlier_path_ms": ms_out,
+                          "quantize_ms": ms_q, "quantize_split_ms": ms_qs,
+                          "int4_path_ms": ms_base, "fp16_outlier_path_ms": ms_out, "fp16_product_ms": ms_prod,
+                          "fused_step_ms": ms_step,
+                          "fused_step_tops": 2.0 * w.M * w.N * w.K / (ms_step * 1e-3) / 1e12,
                           "int4_path_tflops_effective": 2.0 * w.M * w.N * Kb / (ms_base * 1e-3) / 1e12,
                           "fp16_outlier_path_tflops": 2.0 * w.M * w.N * n_out / (ms_out * 1e-3) / 1e12,
                           "l2": "flushed before every timed launch", "clocks": clocks}), flush=True)

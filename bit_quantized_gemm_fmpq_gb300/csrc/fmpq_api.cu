@@ -490,7 +490,44 @@ fmpq_status fmpq_outlier_gemm_fp16(const fmpq_layout* L, const void* X, int64_t 
     if (fmpq_status st = check_device(L)) return st;
     bool maps_ok = true;
     const cudaError_t e = fmpq::launch_outlier_gemm(X, ldx, M, cols, n_out, W_out, ldw_out, N, X_out, Y, ldy,
-                                                    L->d_status, static_cast<cudaStream_t>(stream), &maps_ok);
+                                                    L->num_sms, L->d_status, static_cast<cudaStream_t>(stream),
+                                                    &maps_ok);
+    return (e == cudaSuccess && maps_ok) ? FMPQ_OK : FMPQ_ERR_CUDA;
+}
+
+fmpq_status fmpq_quantize_split(const fmpq_layout* L, const void* X, int64_t ldx, int64_t M, const int32_t* cols,
+                                int32_t n_out, int32_t asym, void* A_packed, void* a_scales, void* a_zeros,
+                                void* X_out, void* stream) {
+    if (L == nullptr || X == nullptr || cols == nullptr || A_packed == nullptr || a_scales == nullptr ||
+        X_out == nullptr || (asym != 0 && a_zeros == nullptr) || (asym != 0 && asym != 1))
+        return FMPQ_ERR_INVALID_ARG;
+    if (asym != 0 && L->n8 != 0) return FMPQ_ERR_INVALID_ARG;   // asymmetric: every block 4-bit
+    if (M < 1 || M > INT32_MAX || ldx < L->K_in || n_out < 8 || n_out % 8 != 0 || n_out > FMPQ_MAX_K)
+        return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (ldx % 8 != 0 || !aligned16(X) || !aligned16(A_packed) || !aligned16(a_scales) || !aligned16(cols) ||
+        !aligned16(X_out) || (asym != 0 && !aligned16(a_zeros)))
+        return FMPQ_ERR_MISALIGNED;
+    if (fmpq_status st = check_device(L)) return st;
+    const fmpq::QuantSplit split{cols, n_out, X_out};
+    return launched(fmpq::launch_quantize(*L, X, ldx, M, A_packed, a_scales, static_cast<cudaStream_t>(stream),
+                                          nullptr, 0.0f, asym ? fmpq::kQuantAsym : fmpq::kQuantSym,
+                                          asym ? a_zeros : nullptr, &split));
+}
+
+fmpq_status fmpq_outlier_product_fp16(const fmpq_layout* L, const void* X_out, int64_t M, int32_t n_out,
+                                      const void* W_out, int64_t ldw_out, int64_t N, void* Y, int64_t ldy,
+                                      void* stream) {
+    if (L == nullptr || X_out == nullptr || W_out == nullptr || Y == nullptr) return FMPQ_ERR_INVALID_ARG;
+    if (M < 1 || M > INT32_MAX || n_out < 8 || n_out % 8 != 0 || n_out > FMPQ_MAX_K || N < 1 ||
+        N > 65535ll * 128 || ldw_out < n_out || ldy < N || ldw_out > INT32_MAX || ldy > INT32_MAX)
+        return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (ldw_out % 8 != 0 || ldy % 8 != 0 || !aligned16(W_out) || !aligned16(X_out) || !aligned16(Y))
+        return FMPQ_ERR_MISALIGNED;
+    if (fmpq_status st = check_device(L)) return st;
+    bool maps_ok = true;
+    const cudaError_t e = fmpq::launch_outlier_gemm(nullptr, 0, M, nullptr, n_out, W_out, ldw_out, N,
+                                                    const_cast<void*>(X_out), Y, ldy, L->num_sms, L->d_status,
+                                                    static_cast<cudaStream_t>(stream), &maps_ok);
     return (e == cudaSuccess && maps_ok) ? FMPQ_OK : FMPQ_ERR_CUDA;
 }
 

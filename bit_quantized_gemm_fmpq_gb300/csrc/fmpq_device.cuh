@@ -183,9 +183,20 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, int x, int y, con
                  "r"(y), "r"(smem_u32(src))
                  : "memory");
 }
+// Element-wise add of a shared-memory box into the tensor (the element type is the tensor map's;
+// the addition is performed at the L2, rounded to nearest; elements outside the tensor are skipped).
+__device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, int x, int y, const void* src) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];"
+                 ::"l"(tmap), "r"(x), "r"(y), "r"(smem_u32(src))
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until every committed bulk store of this thread has finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// At most one committed store group still reading shared memory.
+__device__ __forceinline__ void bulk_wait_group_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// Every committed store group complete (its writes performed).
+__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Make generic-proxy shared-memory writes visible to the async proxy (tensor core reads).
 // ---------------------------------------------------------------------------- cp.async
@@ -398,6 +409,22 @@ __device__ __forceinline__ void tmem_ld_wait16(uint32_t (&r)[16]) {
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Named barrier that also ORs a predicate over the participating threads: every thread gets the
+// same answer (a uniform decision, e.g. to leave a loop that later barriers sit in).
+__device__ __forceinline__ bool named_bar_sync_or(uint32_t id, uint32_t nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n"
+        ".reg .pred p, q;\n"
+        "setp.ne.u32 p, %1, 0;\n"
+        "barrier.red.or.pred q, %2, %3, p;\n"
+        "selp.u32 %0, 1, 0, q;\n"
+        "}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
 }
 // Arrive on a named barrier without waiting (a producer releasing threads that bar.sync on it).
 __device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {

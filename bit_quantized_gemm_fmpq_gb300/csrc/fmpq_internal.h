@@ -45,9 +45,16 @@ EncodeTiledFn encode_tiled();
 // channel order) and eps. mode: kQuantSym (FMPQ), kQuantAsym (QUIK asymmetric, aux = zero points
 // fp16 [nb][M]), kQuantTok (QoQ per-token INT8, aux = block code sums int32 [nb][M]; scales [M]).
 enum { kQuantSym = 0, kQuantAsym = 2, kQuantTok = 3 };
+// QUIK input split fused into the quantizer: X_out[m][j] = X[m][cols[j]] (0 outside [0, K_in)),
+// n a multiple of 8, cols and X_out 16-byte aligned.
+struct QuantSplit {
+    const int32_t* cols;
+    int n;
+    void* X_out;
+};
 cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, int64_t M, void* A, void* scales,
                             cudaStream_t stream, const void* gamma_perm = nullptr, float eps = 0.0f,
-                            int mode = kQuantSym, void* aux = nullptr);
+                            int mode = kQuantSym, void* aux = nullptr, const QuantSplit* split = nullptr);
 // The quantizer fused with SwiGLU: G, U fp16 [M][ld] in the layout's permuted channel order.
 cudaError_t launch_swiglu_quantize(const fmpq_layout& L, const void* G, int64_t ldg, const void* U, int64_t ldu,
                                    int64_t M, void* A, void* scales, cudaStream_t stream);
@@ -109,7 +116,7 @@ cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& args, cudaStream_t
 // encoded (nothing is launched then).
 cudaError_t launch_outlier_gemm(const void* X, int64_t ldx, int64_t M, const int32_t* cols, int n_out,
                                 const void* W_out, int64_t ldw_out, int64_t N, void* X_out, void* Y, int64_t ldy,
-                                int32_t* status, cudaStream_t stream, bool* maps_ok);
+                                int num_sms, int32_t* status, cudaStream_t stream, bool* maps_ok);
 
 // Calibration: per-channel absmax (zeroes `out`, then reduces) and the host layout planner.
 cudaError_t launch_channel_absmax(const void* X, int64_t ldx, int64_t T, int K, uint32_t* out, int num_sms,

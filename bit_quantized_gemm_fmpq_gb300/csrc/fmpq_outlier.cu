@@ -3,16 +3,21 @@
 // added to the output of the INT4 path (the base columns, fmpq_layout_create_select +
 // w4ax_gemm).
 //
-//   outlier_gather_kernel  X[:, cols] -> a dense fp16 [M][n_out] operand (one element per thread)
+//   outlier_gather_kernel  X[:, cols] -> a dense fp16 [M][n_out] operand (one element per thread);
+//                          skipped when the quantizer already split the columns off
 //   outlier_gemm_kernel    Y[m][n] += sum_j X_out[m][j] * W_out[n][j] on the tensor cores
-//                          (tcgen05.mma kind::f16, FP32 accumulator in TMEM), one 128 x 128
-//                          output tile per CTA:
-//     warp 0       TMA producer: the tile's Y (read-modify-write) and, per 64-channel chunk of
-//                  the outlier columns, the X_out and W_out boxes (128-byte swizzle), 2 stages
-//     warp 1       TMEM allocation and the single-thread MMA issuer (M = 128, N = 128, K = 16)
+//                          (tcgen05.mma kind::f16, FP32 accumulators in TMEM); one persistent CTA
+//                          per SM walks a contiguous range of 128 x 128 output tiles:
+//     warp 0       TMA producer: per tile its Y (read-modify-write, two tiles in flight), the
+//                  W_out panel (128 rows x n_out, kept while consecutive tiles share it, for
+//                  n_out <= 256) and the X_out boxes per 64-channel chunk (128-byte swizzle,
+//                  a 6-stage ring; W_out boxes join the ring when the panel does not fit)
+//     warp 1       TMEM allocation and the single-thread MMA issuer (M = 128, N = 128, K = 16),
+//                  two accumulators so the next tile's MMAs overlap this tile's epilogue
 //     warps 2-5    epilogue: TMEM lane quarter warp % 4, one output row per thread; adds the
 //                  FP32 accumulator to Y in shared memory and stores the tile with TMA
-// The product is HBM-bound on Y's read and write (n_out is small); two CTAs share an SM.
+// The product is bound by Y's HBM read and write (n_out is small) and by the copy engine's
+// rate for X_out, which every tile re-reads from L2; the resident panel removes W_out's share.
 // Nothing is allocated: the tensor maps live in kernel parameter space.
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -37,38 +42,65 @@ __global__ void outlier_gather_kernel(const uint16_t* X, int64_t ldx, int64_t M,
 
 constexpr int kOThreads = 192;
 constexpr int kOTileM = 128, kOTileN = 128, kOChunk = 64;   // kOChunk fp16 = one 128-byte swizzle row
-constexpr int kOStages = 2;
-constexpr uint32_t kOTmemCols = 128;
+constexpr int kOPanel = 4;            // W_out chunks kept resident across tiles: n_out <= 256
+constexpr int kOBoxes = 10;           // operand boxes: panel (4) + X_out ring (6), or a ring of 5 (X_out, W_out) pairs
+constexpr int kOMaxStages = 6;
+constexpr int kOBox = kOTileM * kOChunk * 2;   // one 128-row x 64-channel fp16 box (16 KB)
+constexpr uint32_t kOTmemCols = 256;  // two 128-column FP32 accumulators
 constexpr uint32_t kOIdesc = dev::idesc_f16_f32(kOTileM, kOTileN);
 
 struct __align__(1024) OSmem {
-    uint8_t a[kOStages][kOTileM * kOChunk * 2];   // X_out box: 128 rows x 64 channels (swizzled)
-    uint8_t b[kOStages][kOTileN * kOChunk * 2];   // W_out box: 128 rows x 64 channels (swizzled)
-    uint8_t y[2][kOTileM * 64 * 2];               // Y tile as two boxes of 64 columns (swizzled)
-    uint64_t full[kOStages], empty[kOStages];
-    uint64_t y_full, mma_done;
+    uint8_t box[kOBoxes][kOBox];  // X_out / W_out boxes: 128 rows x 64 channels (swizzled)
+    uint8_t y[2][2][kOBox];       // two fp16 product tiles in flight, each as two boxes of 64 columns (swizzled)
+    uint64_t full[kOMaxStages], empty[kOMaxStages];
+    uint64_t w_full, w_free;      // panel landed / every MMA reading the panel finished
+    uint64_t acc_full[2], acc_empty[2];
+    uint64_t mma_done;
     uint32_t tmem_base;
     int abort_flag;
 };
 constexpr size_t kOSmemBytes = sizeof(OSmem) + 1024;
+static_assert(kOSmemBytes <= 227 * 1024, "outlier GEMM shared memory above the per-CTA limit");
 
-__global__ void __launch_bounds__(kOThreads, 2)
+// Tiles run n-major (consecutive tiles share W_out's 128 rows) and each CTA takes a contiguous
+// range of them, so with a resident panel a CTA loads W_out once or twice in all.
+struct OTiles {
+    int mtiles;
+    int64_t t0, t1;
+    __device__ int mt(int64_t t) const { return static_cast<int>(t % mtiles); }
+    __device__ int nt(int64_t t) const { return static_cast<int>(t / mtiles); }
+};
+
+__global__ void __launch_bounds__(kOThreads, 1)
     outlier_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                        const __grid_constant__ CUtensorMap tm_y, int n_out, int n_cols, int32_t* status) {
+                        const __grid_constant__ CUtensorMap tm_y, int n_out, int n_cols, int mtiles, int64_t tiles,
+                        int32_t* status) {
     extern __shared__ uint8_t smem_raw[];
     OSmem& s = *reinterpret_cast<OSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * kOTileM, n0 = blockIdx.y * kOTileN;
-    const int yboxes = n_cols - n0 > 64 ? 2 : 1;   // a Y box wholly past N is neither loaded nor stored
+    const OTiles tl{mtiles, static_cast<int64_t>(blockIdx.x) * tiles / gridDim.x,
+                    static_cast<int64_t>(blockIdx.x + 1) * tiles / gridDim.x};
     const int chunks = (n_out + kOChunk - 1) / kOChunk;
+    const bool panel = chunks <= kOPanel;
+    // panel: W_out chunk c in box c, ring stage st's X_out in box kOPanel + st (6 stages);
+    // otherwise stage st holds X_out in box 2 st and W_out in box 2 st + 1 (5 stages)
+    const int S = panel ? kOBoxes - kOPanel : kOBoxes / 2;
+    auto xbox = [&](int st) { return s.box[panel ? kOPanel + st : 2 * st]; };
+    auto wbox = [&](int st, int c) { return s.box[panel ? c : 2 * st + 1]; };
+    auto yboxes = [&](int nt) { return n_cols - nt * kOTileN > 64 ? 2 : 1; };   // a box wholly past N is skipped
     volatile int* abort_flag = &s.abort_flag;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kOStages; ++i) {
+        for (int i = 0; i < kOMaxStages; ++i) {
             dev::mbar_init(&s.full[i], 1);
             dev::mbar_init(&s.empty[i], 1);
         }
-        dev::mbar_init(&s.y_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            dev::mbar_init(&s.acc_full[i], 1);
+            dev::mbar_init(&s.acc_empty[i], 4);   // one arrival per epilogue warp
+        }
+        dev::mbar_init(&s.w_full, 1);
+        dev::mbar_init(&s.w_free, 1);
         dev::mbar_init(&s.mma_done, 1);
         s.abort_flag = 0;
         dev::fence_barrier_init();
@@ -78,96 +110,153 @@ __global__ void __launch_bounds__(kOThreads, 2)
     __syncthreads();
     dev::tc_fence_after();
     const uint32_t tmem = s.tmem_base;
+    auto fail = [&]() {
+        *abort_flag = 1;
+        dev::report(status, dev::kStatusTimeout);
+    };
 
     if (warp == 0) {
+        // ---------------- TMA producer: the W_out panel when a tile starts a new one, and the
+        // X_out (+ W_out) boxes per 64-channel chunk
         if (lane == 0) {
-            // the tile's Y first: the epilogue adds to it
-            dev::mbar_arrive_expect_tx(&s.y_full, yboxes * kOTileM * 64 * 2);
-            dev::tma_load_2d(s.y[0], &tm_y, n0, m0, &s.y_full);
-            if (yboxes == 2) dev::tma_load_2d(s.y[1], &tm_y, n0 + 64, m0, &s.y_full);
-            int kc = 0;
-            for (; kc < chunks; ++kc) {
-                const int st = kc % kOStages;
-                if (!dev::mbar_wait(&s.empty[st], ((kc / kOStages) & 1) ^ 1, abort_flag)) {
-                    *abort_flag = 1;
-                    dev::report(status, dev::kStatusTimeout);
-                    break;
+            int64_t gx = 0;   // chunks issued (ring position)
+            int loads = 0;    // panels issued
+            int cur_nt = -1;
+            bool ok = true;
+            for (int64_t t = tl.t0; t < tl.t1 && ok; ++t) {
+                const int m0 = tl.mt(t) * kOTileM, nt = tl.nt(t), n0 = nt * kOTileN;
+                if (panel && nt != cur_nt) {
+                    // the previous panel's last MMAs must have finished reading it
+                    if (loads > 0 && !dev::mbar_wait(&s.w_free, static_cast<uint32_t>((loads - 1) & 1), abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    dev::mbar_arrive_expect_tx(&s.w_full, chunks * kOBox);
+                    for (int c = 0; c < chunks; ++c) dev::tma_load_2d(wbox(0, c), &tm_w, c * kOChunk, n0, &s.w_full);
+                    ++loads;
+                    cur_nt = nt;
                 }
-                dev::mbar_arrive_expect_tx(&s.full[st], (kOTileM + kOTileN) * kOChunk * 2);
-                dev::tma_load_2d(s.a[st], &tm_x, kc * kOChunk, m0, &s.full[st]);
-                dev::tma_load_2d(s.b[st], &tm_w, kc * kOChunk, n0, &s.full[st]);
+                for (int c = 0; c < chunks; ++c, ++gx) {
+                    const int st = static_cast<int>(gx % S);
+                    if (!dev::mbar_wait(&s.empty[st], static_cast<uint32_t>((gx / S) & 1) ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    dev::mbar_arrive_expect_tx(&s.full[st], panel ? kOBox : 2 * kOBox);
+                    dev::tma_load_2d(xbox(st), &tm_x, c * kOChunk, m0, &s.full[st]);
+                    if (!panel) dev::tma_load_2d(wbox(st, c), &tm_w, c * kOChunk, n0, &s.full[st]);
+                }
             }
+            if (!ok) fail();
             // drain: every load issued lands before the CTA exits
-            for (int k = kc - 1; k >= 0 && k >= kc - kOStages; --k)
-                dev::mbar_wait(&s.full[k % kOStages], (k / kOStages) & 1, nullptr);
-            dev::mbar_wait(&s.y_full, 0, nullptr);
+            for (int64_t k = gx - 1; k >= 0 && k >= gx - S; --k)
+                dev::mbar_wait(&s.full[k % S], static_cast<uint32_t>((k / S) & 1), nullptr);
+            if (loads > 0) dev::mbar_wait(&s.w_full, static_cast<uint32_t>((loads - 1) & 1), nullptr);
         }
         __syncwarp();
     } else if (warp == 1) {
+        // ---------------- MMA issuer: accumulator i % 2 for this CTA's tile i
         if (lane == 0) {
-            for (int kc = 0; kc < chunks; ++kc) {
-                const int st = kc % kOStages;
-                if (!dev::mbar_wait(&s.full[st], (kc / kOStages) & 1, abort_flag)) {
-                    *abort_flag = 1;
-                    dev::report(status, dev::kStatusTimeout);
+            int64_t gx = 0;
+            int loads = 0;
+            int cur_nt = -1;
+            int64_t i = 0;
+            bool ok = true;
+            for (int64_t t = tl.t0; t < tl.t1 && ok; ++t, ++i) {
+                const int nt = tl.nt(t), ab = static_cast<int>(i & 1);
+                if (!dev::mbar_wait(&s.acc_empty[ab], static_cast<uint32_t>((i >> 1) & 1) ^ 1u, abort_flag)) {
+                    ok = false;
                     break;
                 }
+                if (panel && nt != cur_nt) {
+                    if (!dev::mbar_wait(&s.w_full, static_cast<uint32_t>(loads & 1), abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    ++loads;
+                    cur_nt = nt;
+                }
                 dev::tc_fence_after();
-                const uint64_t ad = dev::sdesc_k_sw128(dev::smem_u32(s.a[st]));
-                const uint64_t bd = dev::sdesc_k_sw128(dev::smem_u32(s.b[st]));
+                const uint32_t d = tmem + static_cast<uint32_t>(ab) * kOTileN;
+                for (int c = 0; c < chunks; ++c, ++gx) {
+                    const int st = static_cast<int>(gx % S);
+                    if (!dev::mbar_wait(&s.full[st], static_cast<uint32_t>((gx / S) & 1), abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    dev::tc_fence_after();
+                    const uint64_t ad = dev::sdesc_k_sw128(dev::smem_u32(xbox(st)));
+                    const uint64_t bd = dev::sdesc_k_sw128(dev::smem_u32(wbox(st, c)));
 #pragma unroll
-                for (int k = 0; k < kOChunk / 16; ++k)   // 32 bytes of K per MMA: +2 in the address field
-                    dev::mma_f16(tmem, ad + 2 * k, bd + 2 * k, kOIdesc, (kc > 0 || k > 0) ? 1u : 0u);
-                dev::mma_commit(&s.empty[st]);
+                    for (int k = 0; k < kOChunk / 16; ++k)   // 32 bytes of K per MMA: +2 in the address field
+                        dev::mma_f16(d, ad + 2 * k, bd + 2 * k, kOIdesc, (c > 0 || k > 0) ? 1u : 0u);
+                    dev::mma_commit(&s.empty[st]);
+                }
+                if (!ok) break;
+                dev::mma_commit(&s.acc_full[ab]);
+                // the panel retires after the last tile that reads it
+                if (panel && (t + 1 == tl.t1 || tl.nt(t + 1) != nt)) dev::mma_commit(&s.w_free);
             }
+            if (!ok) fail();
             dev::mma_commit(&s.mma_done);   // every MMA issued completes before mma_done
             dev::mbar_wait(&s.mma_done, 0, nullptr);   // and before TMEM is released
         }
         __syncwarp();
     } else {
-        // epilogue: thread owns tile row r (TMEM lane r); columns in chunks of 32
+        // ---------------- epilogue: thread owns tile row r (TMEM lane r). The FP32 product is
+        // rounded to fp16 (the FP16 outlier result) into a staging tile, which one thread adds to Y
+        // with a TMA reduce-add (the merge, done at the L2: Y = fp16(Y + product)).
         const int q = warp & 3;
         const int r = 32 * q + lane;
-        bool ok = dev::mbar_wait(&s.mma_done, 0, abort_flag) && dev::mbar_wait(&s.y_full, 0, abort_flag);
-        ok = __all_sync(0xFFFFFFFFu, ok) && !*abort_flag;
-        if (ok) {
+        const bool storer = warp == 2 && lane == 0;
+        int64_t i = 0;
+        for (int64_t t = tl.t0; t < tl.t1; ++t, ++i) {
+            const int mt = tl.mt(t), nt = tl.nt(t), ab = static_cast<int>(i & 1);
+            const int nyb = yboxes(nt);
+            bool ok = dev::mbar_wait(&s.acc_full[ab], static_cast<uint32_t>((i >> 1) & 1), abort_flag);
+            ok = __all_sync(0xFFFFFFFFu, ok) && !*abort_flag;
+            if (!ok && lane == 0) fail();
+            // staging tile ab is free: the storer saw the reduce of tile i - 2 finish reading it.
+            // The barrier also makes the decision to stop the same in all four warps.
+            if (dev::named_bar_sync_or(1, 128, !ok)) break;
             dev::tc_fence_after();
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16);
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(ab) * kOTileN;
 #pragma unroll 1
-            for (int c = 0; c < 4 * yboxes; ++c) {   // 16 columns at a time
-                uint32_t d[16];
-                dev::tmem_ld16(taddr + 16 * c, d);
-                dev::tmem_ld_wait16(d);
-                uint8_t* box = s.y[c >> 2];
+            for (int c = 0; c < 2 * nyb; ++c) {   // 32 columns at a time
+                uint32_t d0[16], d1[16];
+                dev::tmem_ld16(taddr + 32 * c, d0);
+                dev::tmem_ld16(taddr + 32 * c + 16, d1);
+                dev::tmem_ld_wait16(d0);
+                dev::tmem_ld_wait16(d1);
+                uint8_t* box = s.y[ab][c >> 1];
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    // 16-byte chunk (c % 4) * 2 + j of row r sits at chunk position (that ^ r % 8)
-                    const uint32_t pos = ((static_cast<uint32_t>((c & 3) * 2 + j) ^ static_cast<uint32_t>(r & 7)) << 4);
-                    uint4* yp = reinterpret_cast<uint4*>(box + r * 128 + pos);
-                    uint4 v = *yp;
-                    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                for (int j = 0; j < 4; ++j) {
+                    // 16-byte chunk (c % 2) * 4 + j of row r sits at chunk position (that ^ r % 8)
+                    const uint32_t pos = (static_cast<uint32_t>((c & 1) * 4 + j) ^ static_cast<uint32_t>(r & 7)) << 4;
+                    const uint32_t* dj = j < 2 ? d0 + 8 * j : d1 + 8 * (j - 2);
+                    uint32_t w[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float2 old = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-                        const __half2 nv = __floats2half2_rn(old.x + __uint_as_float(d[8 * j + 2 * e]),
-                                                             old.y + __uint_as_float(d[8 * j + 2 * e + 1]));
-                        w[e] = *reinterpret_cast<const uint32_t*>(&nv);
+                        const __half2 h = __floats2half2_rn(__uint_as_float(dj[2 * e]), __uint_as_float(dj[2 * e + 1]));
+                        w[e] = *reinterpret_cast<const uint32_t*>(&h);
                     }
-                    *yp = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4*>(box + r * 128 + pos) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
-            dev::fence_proxy_async_smem();   // the TMA store reads what these threads wrote
-        } else if (lane == 0) {
-            *abort_flag = 1;
-            dev::report(status, dev::kStatusTimeout);
+            dev::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(&s.acc_empty[ab]);   // the accumulator is free again
+            dev::fence_proxy_async_smem();   // the reduce reads what these threads wrote
+            dev::named_bar_sync(2, 128);
+            if (storer) {
+                dev::tma_reduce_add_2d(&tm_y, nt * kOTileN, mt * kOTileM, s.y[ab][0]);
+                if (nyb == 2) dev::tma_reduce_add_2d(&tm_y, nt * kOTileN + 64, mt * kOTileM, s.y[ab][1]);
+                dev::bulk_commit_group();
+                dev::bulk_wait_group_read1();   // tile i - 1's reduce has read its staging tile
+            }
+            __syncwarp();
         }
-        dev::named_bar_sync(1, 128);
-        if (warp == 2 && lane == 0 && !*abort_flag) {
-            dev::tma_store_2d(&tm_y, n0, m0, s.y[0]);
-            if (yboxes == 2) dev::tma_store_2d(&tm_y, n0 + 64, m0, s.y[1]);
-            dev::bulk_commit_group();
-            dev::bulk_wait_group_read0();   // shared memory stays valid until the store has read it
-        }
+        if (storer) dev::bulk_wait_group0();   // every reduce performed before the CTA exits
         __syncwarp();
     }
     dev::tc_fence_before();
@@ -209,7 +298,7 @@ EncodeTiledFn encode_tiled() {
 
 cudaError_t launch_outlier_gemm(const void* X, int64_t ldx, int64_t M, const int32_t* cols, int n_out,
                                 const void* W_out, int64_t ldw_out, int64_t N, void* X_out, void* Y, int64_t ldy,
-                                int32_t* status, cudaStream_t stream, bool* maps_ok) {
+                                int num_sms, int32_t* status, cudaStream_t stream, bool* maps_ok) {
     *maps_ok = true;
     const EncodeTiledFn enc = encode_tiled();
     CUtensorMap tm_x, tm_w, tm_y;
@@ -218,15 +307,20 @@ cudaError_t launch_outlier_gemm(const void* X, int64_t ldx, int64_t M, const int
         *maps_ok = false;
         return cudaSuccess;
     }
-    const unsigned gy = static_cast<unsigned>(M < 65535 ? M : 65535);
-    outlier_gather_kernel<<<dim3(static_cast<unsigned>((n_out + 255) / 256), gy), 256, 0, stream>>>(
-        static_cast<const uint16_t*>(X), ldx, M, cols, n_out, static_cast<uint16_t*>(X_out));
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    cudaError_t e;
+    if (X != nullptr) {   // otherwise X_out already holds the outlier columns (split by the quantizer)
+        const unsigned gy = static_cast<unsigned>(M < 65535 ? M : 65535);
+        outlier_gather_kernel<<<dim3(static_cast<unsigned>((n_out + 255) / 256), gy), 256, 0, stream>>>(
+            static_cast<const uint16_t*>(X), ldx, M, cols, n_out, static_cast<uint16_t*>(X_out));
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     e = ensure_smem_limit(reinterpret_cast<const void*>(outlier_gemm_kernel), static_cast<int>(kOSmemBytes));
     if (e != cudaSuccess) return e;
-    const dim3 grid(static_cast<unsigned>((M + kOTileM - 1) / kOTileM), static_cast<unsigned>((N + kOTileN - 1) / kOTileN));
-    outlier_gemm_kernel<<<grid, kOThreads, kOSmemBytes, stream>>>(tm_x, tm_w, tm_y, n_out, static_cast<int>(N), status);
+    const int64_t mtiles = (M + kOTileM - 1) / kOTileM, tiles = mtiles * ((N + kOTileN - 1) / kOTileN);
+    const int64_t grid = tiles < num_sms ? tiles : (num_sms > 0 ? num_sms : 1);
+    outlier_gemm_kernel<<<static_cast<unsigned>(grid), kOThreads, kOSmemBytes, stream>>>(
+        tm_x, tm_w, tm_y, n_out, static_cast<int>(N), static_cast<int>(mtiles), tiles, status);
     return cudaGetLastError();
 }
 

@@ -137,7 +137,27 @@ struct QuantParams {
     float eps;
     uint16_t* zeros;              // QUIK asymmetric: zero points [nb][M]
     int32_t* sums;                // QoQ per-token INT8: sums of each block's codes [nb][M]
+    // QUIK input split: X_out[m][j] = X[m][split_cols[j]] (fp16, 0 outside the row's width)
+    const int32_t* split_cols;
+    int n_split;                  // a multiple of 8; 0 = no split
+    uint16_t* X_out;
 };
+
+// Outlier columns cols[0..n) of one row into out[0..n): lane l takes columns 8l..8l+7 of every
+// 256, read through load(c) for 0 <= c < width (0 otherwise), one 16-byte store per 8 columns.
+template <typename Load>
+__device__ __forceinline__ void split_row(const int32_t* cols, int n, uint16_t* out, int lane, int width, Load load) {
+    for (int j0 = 8 * lane; j0 < n; j0 += 256) {
+        const int4 c0 = __ldg(reinterpret_cast<const int4*>(cols + j0));
+        const int4 c1 = __ldg(reinterpret_cast<const int4*>(cols + j0 + 4));
+        const int c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        uint32_t h[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) h[k] = (c[k] >= 0 && c[k] < width) ? static_cast<uint32_t>(load(c[k])) : 0u;
+        *reinterpret_cast<uint4*>(out + j0) =
+            make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+    }
+}
 
 __device__ __forceinline__ float rcp_approx(float x) {
     float r;
@@ -413,7 +433,7 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             dev::mbar_init(&full[s], 1);
-            dev::mbar_init(&empty[s], p.cwarps + (kRowWarps ? p.rwarps : 0));
+            dev::mbar_init(&empty[s], p.cwarps + (kRowWarps ? p.rwarps : 0) + (p.n_split > 0 ? 1 : 0));
             dev::mbar_init(&nsync[s], p.rwarps);
             dev::mbar_init(&rready[s], 1);
         }
@@ -448,6 +468,21 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
             }
         }
         __syncwarp();
+    } else if (warp > W + p.rwarps) {
+        // ---------------- split warp (QUIK explainer, "核融合": the one pass over the input also
+        // extracts the outlier part): each staged row's outlier columns, copied out in fp16
+        int64_t i = 0;
+        bool ok = true;
+        for (int64_t m = blockIdx.x; m < p.M; m += gridDim.x, ++i) {
+            const int s = static_cast<int>(i % S);
+            ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&full[s], static_cast<uint32_t>((i / S) & 1), &abort_flag));
+            if (!ok) break;
+            const uint16_t* row = rows_s + static_cast<size_t>(s) * Kr;
+            split_row(p.split_cols, p.n_split, p.X_out + m * p.n_split, lane, Kr, [&](int c) { return row[c]; });
+            __syncwarp();
+            if (lane == 0) dev::mbar_arrive(&empty[s]);
+        }
+        if (!ok && lane == 0) abort_flag = 1;
     } else if (warp > W) {
         // ---------------- row-statistic warps, ahead of the quantizing warps. Warp w takes the
         // chunk pairs w, w + rwarps, ... (each half-warp one 128-channel chunk). Fused RMSNorm:
@@ -669,12 +704,22 @@ __global__ void __launch_bounds__(256) quantize_direct_kernel(QuantParams p) {
     const int sub = lane & 15;
     const uint32_t hmask = upper ? 0xFFFF0000u : 0x0000FFFFu;
     const int pairs = (p.nb + 1) / 2;
-    const int64_t items = p.M * pairs;
+    const int per_token = pairs + (p.n_split + 255) / 256;   // block pairs, then split chunks of 256 columns
+    const int64_t items = p.M * per_token;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
     for (int64_t item = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); item < items;
          item += warps) {   // warp-uniform
-        const int64_t m = item / pairs;
-        const int b = 2 * static_cast<int>(item % pairs) + (upper ? 1 : 0);
+        const int64_t m = item / per_token;
+        const int r = static_cast<int>(item % per_token);
+        if (r >= pairs) {
+            // QUIK input split: this token's outlier columns j .. j + 255
+            const int j = 256 * (r - pairs);
+            const uint16_t* row = p.X + m * p.ldx;
+            split_row(p.split_cols + j, min(256, p.n_split - j), p.X_out + m * p.n_split + j, lane, p.Kin,
+                      [&](int c) { return __ldg(row + c); });
+            continue;
+        }
+        const int b = 2 * r + (upper ? 1 : 0);
         const bool valid = b < p.nb;
         uint32_t h2[4] = {0u, 0u, 0u, 0u};
         bool is8 = false;
@@ -1018,17 +1063,19 @@ __global__ void unpack_weights_kernel(const uint8_t* Wp, int64_t N, int K, int n
 }  // namespace
 
 cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, int64_t M, void* A, void* scales,
-                            cudaStream_t stream, const void* gamma_perm, float eps, int mode, void* aux) {
+                            cudaStream_t stream, const void* gamma_perm, float eps, int mode, void* aux,
+                            const QuantSplit* split) {
     const int K = L.K, Kin = L.K_in;
     if (gamma_perm != nullptr) mode = kQNorm;
     const bool row_warps = mode == kQNorm || mode == kQTok;
     // the per-token absmax is cheap: 4 statistic warps keep ahead, leaving room for 24 quantizing warps
     const int rwarps = mode == kQNorm ? kQNormWarps : mode == kQTok ? kQTokWarps : 0;
+    const int swarps = split != nullptr && split->n > 0 ? 1 : 0;   // the split warp
     int cw = kQWarpsMin;
     if (mode == kQTok)
-        cw = kQMaxThreads / 32 - 1 - kQTokWarps;
+        cw = kQMaxThreads / 32 - 1 - kQTokWarps - swarps;
     else if (!row_warps)
-        for (int w = kQWarpsMax; w > kQWarpsMin; --w)
+        for (int w = kQWarpsMax - swarps; w > kQWarpsMin; --w)
             if (L.nb % (2 * w) == 0) {
                 cw = w;
                 break;
@@ -1044,7 +1091,7 @@ cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, in
     // half the budget and both fit; the warps of the second CTA hide the first one's latencies.
     int per_sm = 1;
     int stages = stages_for(kQSmemBudget);
-    if (mode == kQSym && cw == kQWarpsMin && stages_for(kQSmemBudget / 2) >= 3) {
+    if (mode == kQSym && cw == kQWarpsMin && !swarps && stages_for(kQSmemBudget / 2) >= 3) {
         const int st2 = stages_for(kQSmemBudget / 2);
         const size_t smem2 = quant_bars_offset(Kin, st2, iters * cw, L.nb) + 8ull * (4 * st2);
         int blocks = 0;
@@ -1085,9 +1132,12 @@ cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, in
     p.eps = eps;
     p.zeros = mode == kQAsym ? static_cast<uint16_t*>(aux) : nullptr;
     p.sums = mode == kQTok ? static_cast<int32_t*>(aux) : nullptr;
+    p.split_cols = swarps ? split->cols : nullptr;
+    p.n_split = swarps ? split->n : 0;
+    p.X_out = swarps ? static_cast<uint16_t*>(split->X_out) : nullptr;
     if (mode == kQSym && M < L.num_sms) {
         // fewer tokens than SMs: a warp per (token, block pair) instead of a CTA per row
-        const int64_t items = M * ((L.nb + 1) / 2);
+        const int64_t items = M * ((L.nb + 1) / 2 + (p.n_split + 255) / 256);
         const int64_t ctas_needed = (items + 7) / 8;                       // 8 warps per CTA
         const int64_t ctas_max = static_cast<int64_t>(L.num_sms) * 8;
         quantize_direct_kernel<<<static_cast<unsigned>(ctas_needed < ctas_max ? ctas_needed : ctas_max), 256, 0,
@@ -1096,7 +1146,7 @@ cudaError_t launch_quantize(const fmpq_layout& L, const void* X, int64_t ldx, in
     }
     const int64_t ctas = static_cast<int64_t>(L.num_sms) * per_sm;
     const unsigned grid = static_cast<unsigned>(M < ctas ? M : ctas);
-    const unsigned threads = static_cast<unsigned>((cw + 1 + rwarps) * 32);
+    const unsigned threads = static_cast<unsigned>((cw + 1 + rwarps + swarps) * 32);
     switch (mode) {
         case kQNorm: quantize_kernel<kQNorm><<<grid, threads, smem, stream>>>(p); break;
         case kQAsym: quantize_kernel<kQAsym><<<grid, threads, smem, stream>>>(p); break;

@@ -59,6 +59,8 @@ SIGNATURES = {
     "qoq_gemm_partials": (_I32, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _P, _P]),
     "fmpq_layout_create_select": (_I32, [_I32, _I32, _P, _P, ctypes.POINTER(_P)]),
     "fmpq_outlier_gemm_fp16": (_I32, [_P, _P, _I64, _I64, _P, _I32, _P, _I64, _I64, _P, _P, _I64, _P]),
+    "fmpq_quantize_split": (_I32, [_P, _P, _I64, _I64, _P, _I32, _I32, _P, _P, _P, _P, _P]),
+    "fmpq_outlier_product_fp16": (_I32, [_P, _P, _I64, _I32, _P, _I64, _I64, _P, _I64, _P]),
     "fmpq_channel_absmax": (_I32, [_P, _I64, _I64, _I32, _P, _P]),
     "fmpq_plan_layout": (_I32, [_I32, _P, _I32, _P, _P]),
     "fmpq_plan_layout_budget": (_I32, [_I32, _P, _P, _I64, _I64, ctypes.c_double, _P, _P, _P, _P]),
@@ -393,6 +395,36 @@ def fmpq_outlier_gemm_fp16(layout: "Layout", X, cols, W_out, Y, X_out=None, stre
     _check("fmpq_outlier_gemm_fp16", load_library().fmpq_outlier_gemm_fp16(
         layout.handle, _ptr(X), X.stride(0), M, _ptr(cols), n_out, _ptr(W_out), W_out.stride(0), N, _ptr(X_out), _ptr(Y),
         Y.stride(0), _stream(stream)))
+    return Y
+
+
+def fmpq_quantize_split(layout: "Layout", X, cols, asym: bool = False, A_packed=None, a_scales=None, a_zeros=None,
+                        X_out=None, stream=None):
+    """The quantizer (symmetric, or asymmetric with asym=True) that also splits off X[:, cols]
+    into X_out in the same pass. Returns (A_packed, a_scales, a_zeros or None, X_out)."""
+    import torch
+    M = X.shape[0]
+    n_out = cols.numel()
+    if A_packed is None:
+        A_packed = torch.empty(layout.packed_a_bytes(M), dtype=torch.uint8, device=X.device)
+    if a_scales is None:
+        a_scales = torch.empty((layout.nb, M), dtype=torch.float16, device=X.device)
+    if asym and a_zeros is None:
+        a_zeros = torch.empty((layout.nb, M), dtype=torch.float16, device=X.device)
+    if X_out is None:
+        X_out = torch.empty((M, n_out), dtype=torch.float16, device=X.device)
+    _check("fmpq_quantize_split", layout._lib.fmpq_quantize_split(
+        layout.handle, _ptr(X), X.stride(0), M, _ptr(cols), n_out, 1 if asym else 0, _ptr(A_packed), _ptr(a_scales),
+        _ptr(a_zeros if asym else None), _ptr(X_out), _stream(stream)))
+    return A_packed, a_scales, (a_zeros if asym else None), X_out
+
+
+def fmpq_outlier_product_fp16(layout: "Layout", X_out, W_out, Y, stream=None):
+    """Y = fp16(Y + fp16(X_out @ W_out^T)) with X_out already split off (fmpq_quantize_split)."""
+    M, n_out = X_out.shape
+    N = W_out.shape[0]
+    _check("fmpq_outlier_product_fp16", load_library().fmpq_outlier_product_fp16(
+        layout.handle, _ptr(X_out), M, n_out, _ptr(W_out), W_out.stride(0), N, _ptr(Y), Y.stride(0), _stream(stream)))
     return Y
 
 

@@ -228,10 +228,12 @@ FMPQ_API fmpq_status w4ax_gemm_fault_test(const fmpq_layout* layout, const void*
                                           int32_t withhold_copy, uint32_t poll_limit, void* stream);
 
 /* The FP16 path of an outlier split (QUIK explainer, "第二步: 前向传播": the outlier columns are
- * multiplied in FP16 by the unquantized outlier weights and added to the INT4 path's result):
+ * multiplied in FP16 by the unquantized outlier weights; the INT4 result, dequantized to FP16,
+ * is added to this FP16 outlier result):
  *   X_out[m][j] = X[m][cols[j]]   (0 for an index outside [0, ldx))
- *   Y[m][n]    += sum_j X_out[m][j] * W_out[n][j]   (FP32 accumulation, one fp16 rounding of
- *                                                     the sum Y + product)
+ *   P[m][n]     = fp16_rn( sum_j X_out[m][j] * W_out[n][j] )   (FP32 accumulation: the FP16
+ *                                                              outlier result)
+ *   Y[m][n]     = fp16_rn( Y[m][n] + P[m][n] )   (the merge, an fp16 addition)
  *   layout     the base part's layout (fmpq_layout_create_select); only its device and its
  *              device status word are used (a device-side timeout is recorded there).
  *   X          fp16 [M][ldx] (device); cols int32 [n_out] (device); n_out % 8 == 0.
@@ -244,6 +246,28 @@ FMPQ_API fmpq_status w4ax_gemm_fault_test(const fmpq_layout* layout, const void*
 FMPQ_API fmpq_status fmpq_outlier_gemm_fp16(const fmpq_layout* layout, const void* X, int64_t ldx, int64_t M,
                                             const int32_t* cols, int32_t n_out, const void* W_out, int64_t ldw_out,
                                             int64_t N, void* X_out, void* Y, int64_t ldy, void* stream);
+
+/* The input split fused into the quantizer (QUIK explainer, "核融合": one kernel reads the input,
+ * takes the statistics, quantizes the base part and extracts the outlier part in one pass).
+ * Writes what fmpq_quantize (asym = 0) or fmpq_quantize_asym (asym = 1) writes for the layout's
+ * selected channels, and in the same pass over X
+ *   X_out[m][j] = X[m][cols[j]]   (0 for an index outside [0, K_in)),
+ * the operand of fmpq_outlier_product_fp16.
+ *   cols    int32 [n_out] (device), 8 <= n_out <= FMPQ_MAX_K, n_out % 8 == 0, 16-byte aligned.
+ *   X_out   fp16 [M][n_out] (device, caller-owned), 16-byte aligned.
+ *   a_zeros asym = 1: fp16 [K/128][M] zero points (the layout must have no INT8 block); ignored
+ *           for asym = 0.
+ * Other arguments and errors as fmpq_quantize / fmpq_quantize_asym. */
+FMPQ_API fmpq_status fmpq_quantize_split(const fmpq_layout* layout, const void* X, int64_t ldx, int64_t M,
+                                         const int32_t* cols, int32_t n_out, int32_t asym, void* A_packed,
+                                         void* a_scales, void* a_zeros, void* X_out, void* stream);
+
+/* fmpq_outlier_gemm_fp16 without its gather: X_out fp16 [M][n_out] already holds the outlier
+ * columns (fmpq_quantize_split). Y[m][n] = fp16_rn(Y[m][n] + fp16_rn(sum_j X_out[m][j] *
+ * W_out[n][j])); arguments, limits and errors as fmpq_outlier_gemm_fp16. */
+FMPQ_API fmpq_status fmpq_outlier_product_fp16(const fmpq_layout* layout, const void* X_out, int64_t M,
+                                               int32_t n_out, const void* W_out, int64_t ldw_out, int64_t N,
+                                               void* Y, int64_t ldy, void* stream);
 
 /* ---- Offline layout derivation from calibration activations ----
  * The activation outliers sit in a small set of channels (about 10%: COMET news article,

@@ -1,13 +1,14 @@
 """Outlier split (QUIK explainer, "第二步: 前向传播"): the base columns through the INT4 path
-(a layout selecting them from the full rows), the outlier columns in FP16 (gathered, then the
+(a layout selecting them from the full rows), the outlier columns in FP16 (gathered, or split off
+by the quantizer in its one pass over the input as in the QUIK explainer's "核融合", then the
 library's FP16 tensor-core GEMM added to the output).
 
 CPU: the reference pinned against the full-layout reference. GPU: the selected-layout quantizer
-bit-exact against the oracle on the gathered base columns; the INT4 path's output against its
-exact value within the output tolerance; the FP16 outlier product alone, and the merged output
-(the INT4 output in fp16 plus the FP16 outlier product, as the pages merge them), against the
-oracle's exact product element by element, within one fp16 rounding and the FP32 summation
-bound."""
+bit-exact against the oracle on the gathered base columns, and its split-off outlier columns
+bit-exact against X[:, cols]; the INT4 path's output against its exact value within the output
+tolerance; the FP16 outlier product alone, and the merged output (the INT4 output in fp16 plus
+the FP16 outlier result, added in fp16 as the pages merge them), against the oracle's exact
+product element by element, within the fp16 roundings and the FP32 summation bound."""
 import numpy as np
 import pytest
 
@@ -70,18 +71,26 @@ def _fp32_sum_bound(X, W, out):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("M,N,n_out", [(256, 512, 128), (37, 272, 256), (1, 1024, 64), (130, 200, 72)])
-def test_outlier_product_matches_oracle(fmpq_gpu, oracle_mod, M, N, n_out):
+@pytest.mark.parametrize("M,N,n_out,presplit", [(256, 512, 128, False), (37, 272, 256, False), (1, 1024, 64, False),
+                                                (130, 200, 72, False), (130, 200, 264, True),
+                                                (2048, 2560, 192, False), (2048, 2560, 320, True)])
+def test_outlier_product_matches_oracle(fmpq_gpu, oracle_mod, M, N, n_out, presplit):
     """The FP16 outlier product alone (Y starts at 0) against the oracle's exact product, element
     by element: one fp16 rounding of the FP32 sum. Ragged M, N and outlier counts that leave
-    partial 128-row, 128-column and 64-channel boxes."""
+    partial 128-row, 128-column and 64-channel boxes. n_out <= 256 keeps each CTA's W_out rows
+    resident across its tiles, more streams them with X_out; the 2048 x 2560 cases give the
+    persistent CTAs several tiles each, with ranges that cross into a new W_out panel. presplit:
+    the product-only entry point on X[:, cols] given as X_out."""
     import torch
     X, W, base, out = _problem(M, 256, n_out, N, M + 3 * N)
     layout = fmpq_gpu.select_layout(256, 256 + n_out, base, np.zeros(2, np.uint8))
     _, yo = oracle_mod.quik_reference(X, W, base, out)
     Y = torch.zeros((M, N), dtype=torch.float16, device="cuda")
-    fmpq_gpu.fmpq_outlier_gemm_fp16(layout, torch.from_numpy(X).cuda(), torch.from_numpy(out).cuda(),
-                                    torch.from_numpy(np.ascontiguousarray(W[:, out])).cuda(), Y)
+    W_out = torch.from_numpy(np.ascontiguousarray(W[:, out])).cuda()
+    if presplit:
+        fmpq_gpu.fmpq_outlier_product_fp16(layout, torch.from_numpy(np.ascontiguousarray(X[:, out])).cuda(), W_out, Y)
+    else:
+        fmpq_gpu.fmpq_outlier_gemm_fp16(layout, torch.from_numpy(X).cuda(), torch.from_numpy(out).cuda(), W_out, Y)
     Yg = Y.cpu().numpy().astype(np.float64)
     half_ulp = 0.5 * np.spacing(np.abs(Yg).astype(np.float16)).astype(np.float64)
     err = np.abs(Yg - yo)
@@ -114,13 +123,82 @@ def test_outlier_split_end_to_end(fmpq_gpu, oracle_mod, M, K_base, n_out, N):
     cols = torch.from_numpy(out).cuda()
     W_out = torch.from_numpy(np.ascontiguousarray(W[:, out])).cuda()
     fmpq_gpu.fmpq_outlier_gemm_fp16(layout, Xd, cols, W_out, Y)
-    # merge, element by element against the oracle's exact outlier product: the FP32 sum of the
-    # product and the fp16 base output, rounded once to fp16
+    # merge, element by element against the oracle's exact outlier product. The pages' order: the
+    # FP16 outlier result (the FP32 sum rounded to fp16) is added to the fp16 base output in fp16
+    # (one more rounding), so the error is half an fp16 ulp of the result plus half an fp16 ulp of
+    # the product (taken one binade up, so that an FP32 sum just above a power of two is covered)
+    # plus the FP32 summation bound
     Ym = Y.cpu().numpy().astype(np.float64)
     half_ulp = 0.5 * np.spacing(np.abs(Ym).astype(np.float16)).astype(np.float64)
-    bound = half_ulp + _fp32_sum_bound(X, W, out) + 2.0 ** -24 * (np.abs(Y_base.astype(np.float64)) + np.abs(yo))
+    prod_half_ulp = 0.5 * np.spacing((np.abs(yo) * (1 + 2.0 ** -9)).astype(np.float16)).astype(np.float64)
+    bound = half_ulp + prod_half_ulp + _fp32_sum_bound(X, W, out)
     err = np.abs(Ym - (Y_base.astype(np.float64) + yo))
     assert np.all(err <= bound), f"merge error {err.max():.3e}"
+    assert fmpq_gpu.fmpq_device_status(layout) == 0
+    layout.close()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("M,K_base,n_out,asym,n8", [(300, 1024, 128, False, 2), (37, 512, 256, False, 1),
+                                                    (5, 384, 264, False, 0), (200, 2048, 136, True, 0),
+                                                    (160, 1280, 520, True, 0)])
+def test_quantize_split_codes_and_outlier_columns(fmpq_gpu, oracle_mod, M, K_base, n_out, asym, n8):
+    """The quantizer with the input split (QUIK explainer, "核融合"): the codes and scales (and
+    zero points) are the oracle's for the base columns, bit for bit, and X_out is X[:, cols] bit
+    for bit, 0 for an index outside [0, K_in). Fewer tokens than SMs take the per-warp kernel,
+    more the row-pipelined one; n_out spans one to three 256-column chunks."""
+    import torch
+    X, _, base, out = _problem(M, K_base, n_out, 8, 7 * M + n_out)
+    K_in = K_base + n_out
+    cols = out.copy()
+    cols[3], cols[-2] = -1, K_in + 8   # outside the row: read as 0
+    mask = np.zeros(K_base // BLOCK, np.uint8)
+    mask[K_base // BLOCK - n8:] = 1
+    layout = fmpq_gpu.select_layout(K_base, K_in, base, mask)
+    A, sx, z, X_out = fmpq_gpu.fmpq_quantize_split(layout, torch.from_numpy(X).cuda(), torch.from_numpy(cols).cuda(),
+                                                   asym=asym)
+    Xb = np.ascontiguousarray(X[:, base])
+    if asym:
+        A_ref, sx_ref, z_ref, _ = oracle_mod.quantize_activations_asym(Xb, np.arange(K_base, dtype=np.int32))
+        assert np.array_equal(z.cpu().numpy().view(np.uint16), z_ref)
+    else:
+        A_ref, sx_ref, _ = oracle_mod.quantize_activations(Xb, np.arange(K_base, dtype=np.int32), mask)
+    assert np.array_equal(A.cpu().numpy(), A_ref) and np.array_equal(sx.cpu().numpy().view(np.uint16), sx_ref)
+    expect = np.where((cols >= 0) & (cols < K_in), X[:, np.clip(cols, 0, K_in - 1)], np.float16(0))
+    assert np.array_equal(X_out.cpu().numpy().view(np.uint16), expect.view(np.uint16))
+    assert fmpq_gpu.fmpq_device_status(layout) == 0
+    layout.close()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("M,K_base,n_out,N", [(256, 1024, 128, 512), (9, 512, 264, 272)])
+def test_outlier_split_fused_path(fmpq_gpu, oracle_mod, M, K_base, n_out, N):
+    """The QUIK forward pass with the split fused into the quantizer: quantize + split, INT4 GEMM,
+    FP16 product on the split columns added in fp16. The merged output against the oracle's
+    exact parts within the fp16 roundings and the FP32 summation bound; the merged output equals
+    the unfused path's (gather kernel) bit for bit."""
+    import torch
+    from tests.gpu_helpers import Y_TOL, y_error
+    X, W, base, out = _problem(M, K_base, n_out, N, 11 * M + N)
+    layout = fmpq_gpu.select_layout(K_base, K_base + n_out, base, np.zeros(K_base // BLOCK, np.uint8))
+    Xd, cols = torch.from_numpy(X).cuda(), torch.from_numpy(out).cuda()
+    A, sx, _, X_out = fmpq_gpu.fmpq_quantize_split(layout, Xd, cols)
+    Wp, sw = fmpq_gpu.w4_pack_weights(layout, torch.from_numpy(W).cuda())
+    Y = fmpq_gpu.w4ax_gemm(layout, A, sx, Wp, sw, M, N)
+    Y_base = Y.cpu().numpy().astype(np.float64)
+    Y2 = Y.clone()
+    W_out = torch.from_numpy(np.ascontiguousarray(W[:, out])).cuda()
+    fmpq_gpu.fmpq_outlier_product_fp16(layout, X_out, W_out, Y)
+    fmpq_gpu.fmpq_outlier_gemm_fp16(layout, Xd, cols, W_out, Y2)
+    yb, yo = oracle_mod.quik_reference(X, W, base, out)
+    assert y_error(Y_base, yb) <= Y_TOL
+    Ym = Y.cpu().numpy().astype(np.float64)
+    bound = (0.5 * np.spacing(np.abs(Ym).astype(np.float16)).astype(np.float64)
+             + 0.5 * np.spacing((np.abs(yo) * (1 + 2.0 ** -9)).astype(np.float16)).astype(np.float64)
+             + _fp32_sum_bound(X, W, out))
+    err = np.abs(Ym - (Y_base + yo))
+    assert np.all(err <= bound), f"merge error {err.max():.3e}"
+    assert torch.equal(Y.view(torch.int16), Y2.view(torch.int16))
     assert fmpq_gpu.fmpq_device_status(layout) == 0
     layout.close()
 
@@ -134,6 +212,11 @@ def test_outlier_split_argument_errors(fmpq_gpu):
     layout = fmpq_gpu.select_layout(128, 256, np.arange(128, dtype=np.int32), np.zeros(1, np.uint8))
     with pytest.raises(fmpq_gpu.FmpqError):       # 12 outlier columns: not a multiple of 8
         fmpq_gpu.fmpq_outlier_gemm_fp16(layout, X, torch.zeros(12, dtype=torch.int32, device="cuda"), W_out, Y)
+    with pytest.raises(fmpq_gpu.FmpqError):       # the same for the split quantizer
+        fmpq_gpu.fmpq_quantize_split(layout, X, torch.zeros(12, dtype=torch.int32, device="cuda"))
+    with pytest.raises(fmpq_gpu.FmpqError):       # the product alone: 12 columns, not a multiple of 8
+        fmpq_gpu.fmpq_outlier_product_fp16(layout, torch.zeros((4, 12), dtype=torch.float16, device="cuda"),
+                                           torch.zeros((64, 12), dtype=torch.float16, device="cuda"), Y)
     layout.close()
     with pytest.raises(fmpq_gpu.FmpqError):       # a selection with a repeated channel
         fmpq_gpu.select_layout(128, 256, np.zeros(128, np.int32), np.zeros(1, np.uint8))
