@@ -119,6 +119,9 @@ struct Params {
     const uint16_t* ch_scales;
     const uint8_t* grp_scales;
     const uint8_t* grp_zeros;
+    // QUIK with the zero-point term precomputed on the tensor cores: yz[m][n] (FP32, row
+    // stride N), added once per output before the fp16 rounding; nullptr: one pass per block
+    const float* yz;
     // failure-detection test: polls before a device wait gives up, and the index of the packed
     // weight copy the first CTA withholds (-1: none)
     uint32_t poll_limit;
@@ -208,6 +211,15 @@ __device__ __forceinline__ void activation_producer(const Params& p, Smem& s, ui
         const int r0 = t.mt * kPairM + static_cast<int>(rank) * 128;
         const uint32_t abytes = static_cast<uint32_t>(max(0, min(128, p.M - r0))) * kBlock;
         for (int b = t.b0; ok && b < t.b1; ++b, ++it) {
+            if (p.yz != nullptr && b == t.b0 && t.split == 0) {
+                // QUIK: the tile's rows of the precomputed zero-point term go to the L2 while the
+                // epilogue is still on earlier blocks (one 1 KB row per prefetch)
+                const int cols = min(kTileN, p.N - t.nt * kTileN);   // N % 16 == 0: a multiple of 64 bytes
+                for (int r = lane; r < 128; r += 32)
+                    if (r0 + r < p.M)
+                        dev::bulk_prefetch_l2(p.yz + static_cast<int64_t>(r0 + r) * p.N + t.nt * kTileN,
+                                              static_cast<uint32_t>(cols) * 4u);
+            }
             const int planes = s.mask[b] ? 2 : 1;
             // the slots of this block's planes must have been released by the MMAs of the
             // blocks that used them last (the whole warp waits, converged; lane 0 issues)
@@ -342,7 +354,7 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, uint32_
             sc0 = n_a < p.N ? __ldg(p.w_scales + wb + n_a) : 0u;
             sc1 = n_b < p.N ? __ldg(p.w_scales + wb + n_b) : 0u;
             sc2 = m < p.M ? __ldg(p.a_scales + xb + m) : 0u;
-            if (p.zero_kind == kZeroQuik) {
+            if (p.zero_kind == kZeroQuik && p.yz == nullptr) {
                 zc0 = n_a < p.N ? __float_as_uint(__ldg(p.w_sums + wb + n_a)) : 0u;
                 zc1 = n_b < p.N ? __float_as_uint(__ldg(p.w_sums + wb + n_b)) : 0u;
                 zc2 = m < p.M ? __ldg(p.a_zeros + xb + m) : 0u;
@@ -392,7 +404,7 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, uint32_
         if (p.zero_kind != kZeroQoq) {
             sl.sw[swd0] = h2f(sc0);
             sl.sw[swd1] = h2f(sc1);
-            if (p.zero_kind == kZeroQuik) {
+            if (p.zero_kind == kZeroQuik && p.yz == nullptr) {
                 sl.wz[swd0] = __uint_as_float(zc0);
                 sl.wz[swd1] = __uint_as_float(zc1);
                 sl.xz[ct] = h2f(zc2);
@@ -431,7 +443,9 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, uint32_
 // and all 256 columns, read with tcgen05.ld 16x256b: thread t holds rows t/4 and t/4 + 8 of
 // that slab and columns 8g + 2(t%4) + {0, 1}, g = 0..31 (four registers per 8 columns:
 // row0 col0, row0 col1, row1 col0, row1 col1).
-template <bool kPartials, bool kZero>
+// kZ: the zero-point term. 0 none; 1 one FP32 pass per block (x_zero[m] * w_zero[n] from the
+// scale slot, QoQ); 2 precomputed over all blocks (yz), the starting value of the accumulators.
+template <bool kPartials, int kZ>
 __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, uint32_t rank, int warp, int lane,
                                               uint32_t tmem, volatile int* abort_flag, uint32_t polls) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
@@ -455,6 +469,20 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, uint32_t
         for (int g = 0; g < 32; ++g) {
             accA[g] = make_float2(0.f, 0.f);
             accB[g] = make_float2(0.f, 0.f);
+        }
+        if constexpr (kZ == 2 && !kPartials) {
+            // QUIK: the accumulators start from the zero-point term summed over all blocks (one
+            // split of a split-K tile carries it); the producer brought these rows to the L2
+            if (t.split == 0) {
+#pragma unroll
+                for (int g = 0; g < 32; ++g) {
+                    const int col = n0 + 8 * g + 2 * tq;
+                    if (col < p.N) {
+                        if (ok0) accA[g] = __ldg(reinterpret_cast<const float2*>(p.yz + static_cast<int64_t>(row0) * p.N + col));
+                        if (ok1) accB[g] = __ldg(reinterpret_cast<const float2*>(p.yz + static_cast<int64_t>(row1) * p.N + col));
+                    }
+                }
+            }
         }
         for (int b = t.b0; b < t.b1; ++b, ++v) {
             const int ab = v & 1;
@@ -520,7 +548,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, uint32_t
                 dev::tc_fence_before();
             }
             __syncwarp();
-            if constexpr (kZero && !kPartials) {
+            if constexpr (kZ == 1 && !kPartials) {
                 // the accumulator is read: release it first; then the block's zero-point term
                 // x_zero[m] * w_zero[n], a second pass over the registers, from the scale slot
                 if (lane == 0 && ok) dev::mbar_arrive_remote(release);
@@ -612,7 +640,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, uint32_t
 
 // kTest: the failure-detection test instantiation (runtime poll bound, a withheld weight copy);
 // the others bound every wait by the compile-time dev::kMaxPolls.
-template <bool kPartials, bool kZero, bool kTest = false>
+template <bool kPartials, int kZ, bool kTest = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) w4ax_gemm_kernel(const Params p) {
     extern __shared__ uint8_t smem_raw[];
     Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -677,7 +705,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) w4ax_ge
         }
     } else {
         dev::setmaxnreg_inc<192>();
-        epilogue_role<kPartials, kZero>(p, s, rank, warp, lane, tmem, abort_flag, polls);
+        epilogue_role<kPartials, kZ>(p, s, rank, warp, lane, tmem, abort_flag, polls);
     }
 
     dev::tc_fence_before();
@@ -705,9 +733,9 @@ int max_pairs(const fmpq_layout& L) {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = sizeof(Smem) + 1024;
     int clusters = 0;
-    if (ensure_smem_limit(reinterpret_cast<const void*>(w4ax_gemm_kernel<false, false>),
+    if (ensure_smem_limit(reinterpret_cast<const void*>(w4ax_gemm_kernel<false, 0>),
                           static_cast<int>(sizeof(Smem) + 1024)) == cudaSuccess &&
-        cudaOccupancyMaxActiveClusters(&clusters, w4ax_gemm_kernel<false, false>, &cfg) == cudaSuccess && clusters > 0 &&
+        cudaOccupancyMaxActiveClusters(&clusters, w4ax_gemm_kernel<false, 0>, &cfg) == cudaSuccess && clusters > 0 &&
         clusters < pairs)
         pairs = clusters;
     cudaGetLastError();   // a failed query leaves no sticky error behind
@@ -743,11 +771,15 @@ size_t gemm_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N, bool var
     return static_cast<size_t>(tiles) * splits * kPairM * kTileN * sizeof(float) + gemm_counter_bytes(L, M, N, variant);
 }
 
+size_t quik_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N) {
+    return ((gemm_workspace_bytes(L, M, N, true) + 1023) & ~size_t(1023)) + zero_term_bytes(L, M, N);
+}
+
 cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& a, cudaStream_t stream) {
     const bool variant = a.zero_kind != kZeroNone || a.unsigned_w;
     if (!variant && gemm_small_path(a.M) && a.withhold < 0) return launch_gemm_small(L, a, stream);
-    for (auto fn : {w4ax_gemm_kernel<false, false>, w4ax_gemm_kernel<true, false>, w4ax_gemm_kernel<false, true>,
-                    w4ax_gemm_kernel<false, false, true>}) {
+    for (auto fn : {w4ax_gemm_kernel<false, 0>, w4ax_gemm_kernel<true, 0>, w4ax_gemm_kernel<false, 1>,
+                    w4ax_gemm_kernel<false, 2>, w4ax_gemm_kernel<false, 0, true>}) {
         const cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(fn), static_cast<int>(kSmemBytes));
         if (e != cudaSuccess) return e;
     }
@@ -799,17 +831,29 @@ cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& a, cudaStream_t st
                                                     static_cast<size_t>(tiles) * p.splits * kPairM * kTileN * sizeof(float));
         }
     }
+    if (a.zero_kind == kZeroQuik && !partials) {
+        // the zero-point term for every output first, after the split-K part of the workspace
+        uint8_t* zero_ws = static_cast<uint8_t*>(a.workspace) +
+                           ((gemm_workspace_bytes(L, a.M, a.N, true) + 1023) & ~size_t(1023));
+        bool maps_ok = true;
+        const cudaError_t e = launch_zero_term(L, a.a_zeros, a.w_sums, a.M, a.N, zero_ws, stream, &maps_ok);
+        if (e != cudaSuccess) return e;
+        if (!maps_ok) return cudaErrorInvalidValue;
+        p.yz = reinterpret_cast<const float*>(zero_ws);
+    }
     const int64_t units = static_cast<int64_t>(p.mtiles) * p.ntiles * p.splits;
     const int pairs = static_cast<int>(units < max_pairs(L) ? units : max_pairs(L));
     const int grid = 2 * pairs;   // clusters of two CTAs (one pair per two SMs)
     if (a.withhold >= 0)
-        w4ax_gemm_kernel<false, false, true><<<grid, kThreads, kSmemBytes, stream>>>(p);
+        w4ax_gemm_kernel<false, 0, true><<<grid, kThreads, kSmemBytes, stream>>>(p);
     else if (partials)
-        w4ax_gemm_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(p);
+        w4ax_gemm_kernel<true, 0><<<grid, kThreads, kSmemBytes, stream>>>(p);
+    else if (p.yz != nullptr)
+        w4ax_gemm_kernel<false, 2><<<grid, kThreads, kSmemBytes, stream>>>(p);
     else if (a.zero_kind != kZeroNone)
-        w4ax_gemm_kernel<false, true><<<grid, kThreads, kSmemBytes, stream>>>(p);
+        w4ax_gemm_kernel<false, 1><<<grid, kThreads, kSmemBytes, stream>>>(p);
     else
-        w4ax_gemm_kernel<false, false><<<grid, kThreads, kSmemBytes, stream>>>(p);
+        w4ax_gemm_kernel<false, 0><<<grid, kThreads, kSmemBytes, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -1,23 +1,34 @@
+// Tensor-core side products of the quantization variants.
+//
 // The FP16 outlier path of an outlier split (QUIK explainer, "第二步: 前向传播"): the input's
-// outlier columns are multiplied in FP16 by the unquantized outlier weights and the result is
-// added to the output of the INT4 path (the base columns, fmpq_layout_create_select +
+// outlier columns are multiplied in FP16 by the unquantized outlier weights, and the FP16 result
+// is added to the output of the INT4 path (the base columns, fmpq_layout_create_select +
 // w4ax_gemm).
 //
 //   outlier_gather_kernel  X[:, cols] -> a dense fp16 [M][n_out] operand (one element per thread);
 //                          skipped when the quantizer already split the columns off
-//   outlier_gemm_kernel    Y[m][n] += sum_j X_out[m][j] * W_out[n][j] on the tensor cores
-//                          (tcgen05.mma kind::f16, FP32 accumulators in TMEM); one persistent CTA
-//                          per SM walks a contiguous range of 128 x 128 output tiles:
-//     warp 0       TMA producer: per tile its Y (read-modify-write, two tiles in flight), the
-//                  W_out panel (128 rows x n_out, kept while consecutive tiles share it, for
-//                  n_out <= 256) and the X_out boxes per 64-channel chunk (128-byte swizzle,
-//                  a 6-stage ring; W_out boxes join the ring when the panel does not fit)
+//   outlier_gemm_kernel    Y[m][n] = fp16(Y[m][n] + fp16(sum_j X_out[m][j] * W_out[n][j])) on the
+//                          tensor cores (tcgen05.mma kind::f16, FP32 accumulators in TMEM); one
+//                          persistent CTA per SM walks a contiguous n-major range of 128 x 128
+//                          output tiles:
+//     warp 0       TMA producer: the W_out panel (128 rows x n_out, kept while consecutive tiles
+//                  share it, for n_out <= 256) and the X_out boxes per 64-channel chunk
+//                  (128-byte swizzle, a 6-stage ring; W_out boxes join the ring when the panel
+//                  does not fit)
 //     warp 1       TMEM allocation and the single-thread MMA issuer (M = 128, N = 128, K = 16),
 //                  two accumulators so the next tile's MMAs overlap this tile's epilogue
-//     warps 2-5    epilogue: TMEM lane quarter warp % 4, one output row per thread; adds the
-//                  FP32 accumulator to Y in shared memory and stores the tile with TMA
-// The product is bound by Y's HBM read and write (n_out is small) and by the copy engine's
-// rate for X_out, which every tile re-reads from L2; the resident panel removes W_out's share.
+//     warps 2-5    epilogue: TMEM lane quarter warp % 4, one output row per thread; rounds the
+//                  FP32 product to fp16 into a staging tile that one thread adds to Y with a TMA
+//                  reduce-add (the merge, done at the L2)
+//   The product is bound by the copy engine's rate for X_out, which every tile re-reads from the
+//   L2; the resident panel removes W_out's share.
+//
+// The QUIK zero-point term (QUIK explainer, "反量化背后的数学": the zero point's contribution is
+// z times the sum of the dequantized weights): yz[m][n] = sum_b z[b][m] * ws[b][n] in FP32, the
+// same kernel in its tf32 form (kind::tf32, fp32 operands, FP32 rows stored straight from the
+// epilogue) on operands that zero_operands_kernel lays out so that every product is exact. The
+// variant GEMM adds yz once per output instead of one FP32 pass per block.
+//
 // Nothing is allocated: the tensor maps live in kernel parameter space.
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -47,7 +58,6 @@ constexpr int kOBoxes = 10;           // operand boxes: panel (4) + X_out ring (
 constexpr int kOMaxStages = 6;
 constexpr int kOBox = kOTileM * kOChunk * 2;   // one 128-row x 64-channel fp16 box (16 KB)
 constexpr uint32_t kOTmemCols = 256;  // two 128-column FP32 accumulators
-constexpr uint32_t kOIdesc = dev::idesc_f16_f32(kOTileM, kOTileN);
 
 struct __align__(1024) OSmem {
     uint8_t box[kOBoxes][kOBox];  // X_out / W_out boxes: 128 rows x 64 channels (swizzled)
@@ -71,16 +81,22 @@ struct OTiles {
     __device__ int nt(int64_t t) const { return static_cast<int>(t / mtiles); }
 };
 
+// kTf32 = false: the FP16 outlier product, merged into the fp16 Y with a TMA reduce-add.
+// kTf32 = true: the same pipeline on fp32 operands read as tf32 (a 128-byte box row is 32 of
+// them), the FP32 product stored to yz [m_rows][ldz] (the QUIK zero-point term).
+template <bool kTf32>
 __global__ void __launch_bounds__(kOThreads, 1)
     outlier_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                         const __grid_constant__ CUtensorMap tm_y, int n_out, int n_cols, int mtiles, int64_t tiles,
-                        int32_t* status) {
+                        float* yz, int64_t ldz, int m_rows, int32_t* status) {
+    constexpr int kElems = kTf32 ? 32 : kOChunk;   // K elements per 128-byte box row
+    constexpr uint32_t kIdesc = kTf32 ? dev::idesc_tf32_f32(kOTileM, kOTileN) : dev::idesc_f16_f32(kOTileM, kOTileN);
     extern __shared__ uint8_t smem_raw[];
     OSmem& s = *reinterpret_cast<OSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const OTiles tl{mtiles, static_cast<int64_t>(blockIdx.x) * tiles / gridDim.x,
                     static_cast<int64_t>(blockIdx.x + 1) * tiles / gridDim.x};
-    const int chunks = (n_out + kOChunk - 1) / kOChunk;
+    const int chunks = (n_out + kElems - 1) / kElems;
     const bool panel = chunks <= kOPanel;
     // panel: W_out chunk c in box c, ring stage st's X_out in box kOPanel + st (6 stages);
     // otherwise stage st holds X_out in box 2 st and W_out in box 2 st + 1 (5 stages)
@@ -132,7 +148,7 @@ __global__ void __launch_bounds__(kOThreads, 1)
                         break;
                     }
                     dev::mbar_arrive_expect_tx(&s.w_full, chunks * kOBox);
-                    for (int c = 0; c < chunks; ++c) dev::tma_load_2d(wbox(0, c), &tm_w, c * kOChunk, n0, &s.w_full);
+                    for (int c = 0; c < chunks; ++c) dev::tma_load_2d(wbox(0, c), &tm_w, c * kElems, n0, &s.w_full);
                     ++loads;
                     cur_nt = nt;
                 }
@@ -143,8 +159,8 @@ __global__ void __launch_bounds__(kOThreads, 1)
                         break;
                     }
                     dev::mbar_arrive_expect_tx(&s.full[st], panel ? kOBox : 2 * kOBox);
-                    dev::tma_load_2d(xbox(st), &tm_x, c * kOChunk, m0, &s.full[st]);
-                    if (!panel) dev::tma_load_2d(wbox(st, c), &tm_w, c * kOChunk, n0, &s.full[st]);
+                    dev::tma_load_2d(xbox(st), &tm_x, c * kElems, m0, &s.full[st]);
+                    if (!panel) dev::tma_load_2d(wbox(st, c), &tm_w, c * kElems, n0, &s.full[st]);
                 }
             }
             if (!ok) fail();
@@ -188,8 +204,12 @@ __global__ void __launch_bounds__(kOThreads, 1)
                     const uint64_t ad = dev::sdesc_k_sw128(dev::smem_u32(xbox(st)));
                     const uint64_t bd = dev::sdesc_k_sw128(dev::smem_u32(wbox(st, c)));
 #pragma unroll
-                    for (int k = 0; k < kOChunk / 16; ++k)   // 32 bytes of K per MMA: +2 in the address field
-                        dev::mma_f16(d, ad + 2 * k, bd + 2 * k, kOIdesc, (c > 0 || k > 0) ? 1u : 0u);
+                    for (int k = 0; k < 4; ++k) {   // 32 bytes of K per MMA: +2 in the address field
+                        if constexpr (kTf32)
+                            dev::mma_tf32(d, ad + 2 * k, bd + 2 * k, kIdesc, (c > 0 || k > 0) ? 1u : 0u);
+                        else
+                            dev::mma_f16(d, ad + 2 * k, bd + 2 * k, kIdesc, (c > 0 || k > 0) ? 1u : 0u);
+                    }
                     dev::mma_commit(&s.empty[st]);
                 }
                 if (!ok) break;
@@ -221,42 +241,68 @@ __global__ void __launch_bounds__(kOThreads, 1)
             if (dev::named_bar_sync_or(1, 128, !ok)) break;
             dev::tc_fence_after();
             const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(ab) * kOTileN;
+            if constexpr (kTf32) {
+                // FP32 rows straight to yz: thread r writes 512 contiguous bytes of its row
+                const int row = mt * kOTileM + r;
 #pragma unroll 1
-            for (int c = 0; c < 2 * nyb; ++c) {   // 32 columns at a time
-                uint32_t d0[16], d1[16];
-                dev::tmem_ld16(taddr + 32 * c, d0);
-                dev::tmem_ld16(taddr + 32 * c + 16, d1);
-                dev::tmem_ld_wait16(d0);
-                dev::tmem_ld_wait16(d1);
-                uint8_t* box = s.y[ab][c >> 1];
+                for (int c = 0; c < 2 * nyb; ++c) {
+                    uint32_t d0[16], d1[16];
+                    dev::tmem_ld16(taddr + 32 * c, d0);
+                    dev::tmem_ld16(taddr + 32 * c + 16, d1);
+                    dev::tmem_ld_wait16(d0);
+                    dev::tmem_ld_wait16(d1);
+                    if (row < m_rows) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    // 16-byte chunk (c % 2) * 4 + j of row r sits at chunk position (that ^ r % 8)
-                    const uint32_t pos = (static_cast<uint32_t>((c & 1) * 4 + j) ^ static_cast<uint32_t>(r & 7)) << 4;
-                    const uint32_t* dj = j < 2 ? d0 + 8 * j : d1 + 8 * (j - 2);
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const __half2 h = __floats2half2_rn(__uint_as_float(dj[2 * e]), __uint_as_float(dj[2 * e + 1]));
-                        w[e] = *reinterpret_cast<const uint32_t*>(&h);
+                        for (int g = 0; g < 8; ++g) {
+                            const int col = nt * kOTileN + 32 * c + 4 * g;
+                            const uint32_t* dg = g < 4 ? d0 + 4 * g : d1 + 4 * (g - 4);
+                            if (col + 4 <= n_cols)
+                                *reinterpret_cast<uint4*>(yz + static_cast<int64_t>(row) * ldz + col) =
+                                    make_uint4(dg[0], dg[1], dg[2], dg[3]);
+                        }
                     }
-                    *reinterpret_cast<uint4*>(box + r * 128 + pos) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
+                dev::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) dev::mbar_arrive(&s.acc_empty[ab]);
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < 2 * nyb; ++c) {   // 32 columns at a time
+                    uint32_t d0[16], d1[16];
+                    dev::tmem_ld16(taddr + 32 * c, d0);
+                    dev::tmem_ld16(taddr + 32 * c + 16, d1);
+                    dev::tmem_ld_wait16(d0);
+                    dev::tmem_ld_wait16(d1);
+                    uint8_t* box = s.y[ab][c >> 1];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        // 16-byte chunk (c % 2) * 4 + j of row r sits at chunk position (that ^ r % 8)
+                        const uint32_t pos = (static_cast<uint32_t>((c & 1) * 4 + j) ^ static_cast<uint32_t>(r & 7)) << 4;
+                        const uint32_t* dj = j < 2 ? d0 + 8 * j : d1 + 8 * (j - 2);
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const __half2 h = __floats2half2_rn(__uint_as_float(dj[2 * e]), __uint_as_float(dj[2 * e + 1]));
+                            w[e] = *reinterpret_cast<const uint32_t*>(&h);
+                        }
+                        *reinterpret_cast<uint4*>(box + r * 128 + pos) = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+                dev::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) dev::mbar_arrive(&s.acc_empty[ab]);   // the accumulator is free again
+                dev::fence_proxy_async_smem();   // the reduce reads what these threads wrote
+                dev::named_bar_sync(2, 128);
+                if (storer) {
+                    dev::tma_reduce_add_2d(&tm_y, nt * kOTileN, mt * kOTileM, s.y[ab][0]);
+                    if (nyb == 2) dev::tma_reduce_add_2d(&tm_y, nt * kOTileN + 64, mt * kOTileM, s.y[ab][1]);
+                    dev::bulk_commit_group();
+                    dev::bulk_wait_group_read1();   // tile i - 1's reduce has read its staging tile
+                }
+                __syncwarp();
             }
-            dev::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) dev::mbar_arrive(&s.acc_empty[ab]);   // the accumulator is free again
-            dev::fence_proxy_async_smem();   // the reduce reads what these threads wrote
-            dev::named_bar_sync(2, 128);
-            if (storer) {
-                dev::tma_reduce_add_2d(&tm_y, nt * kOTileN, mt * kOTileM, s.y[ab][0]);
-                if (nyb == 2) dev::tma_reduce_add_2d(&tm_y, nt * kOTileN + 64, mt * kOTileM, s.y[ab][1]);
-                dev::bulk_commit_group();
-                dev::bulk_wait_group_read1();   // tile i - 1's reduce has read its staging tile
-            }
-            __syncwarp();
         }
-        if (storer) dev::bulk_wait_group0();   // every reduce performed before the CTA exits
+        if (!kTf32 && storer) dev::bulk_wait_group0();   // every reduce performed before the CTA exits
         __syncwarp();
     }
     dev::tc_fence_before();
@@ -267,18 +313,66 @@ __global__ void __launch_bounds__(kOThreads, 1)
     }
 }
 
-// A 2-D fp16 tensor [rows][cols] with row stride ld (elements), read in boxes of 64 x box_rows
-// with the 128-byte swizzle.
+// A 2-D fp16 (or fp32) tensor [rows][cols] with row stride ld (elements), read in boxes of one
+// 128-byte row (64 fp16 or 32 fp32) x box_rows with the 128-byte swizzle.
 bool make_map(EncodeTiledFn enc, CUtensorMap* map, const void* base, int64_t cols, int64_t rows, int64_t ld,
-              uint32_t box_rows) {
+              uint32_t box_rows, bool fp32 = false) {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * (fp32 ? 4 : 2)};
+    const cuuint32_t box[2] = {fp32 ? 32u : 64u, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return enc(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+               const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+// QUIK zero-point term operands (K' = 2 nbp, nbp = nb rounded up to 32):
+//   Zp[m][j] = z[j mod nbp][m]                (fp16 zero points, exact in fp32 and in tf32)
+//   Wp[n][j] = hi(ws[j][n]) for j < nbp, ws[j - nbp][n] - hi(ws[j - nbp][n]) after
+// (0 for block indices >= nb), hi = ws with the 13 low mantissa bits cleared. Both parts are
+// exact in tf32 when ws has at most 22 significant bits (w_sums = fp16 scale x code sum has
+// at most 21), so sum_j Zp Wp is sum_b z ws with exact products.
+__global__ void zero_operands_kernel(const uint16_t* a_zeros, const float* w_sums, int64_t M, int64_t N, int nb,
+                                     int nbp, float* Zp, float* Wp) {
+    // one 32 x 32 tile of (block b, row r) per CTA, transposed through shared memory so that both
+    // the reads (along r) and the writes (along b) are coalesced; z = 0: Zp, z = 1: Wp
+    __shared__ float t[32][33];
+    const bool w = blockIdx.z != 0;
+    const int64_t R = w ? N : M;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 32;
+    if (r0 >= R) return;   // uniform per CTA
+    const int b0 = blockIdx.y * 32, kp = 2 * nbp;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8 threads
+    for (int k = ty; k < 32; k += 8) {
+        const int b = b0 + k;
+        const int64_t r = r0 + tx;
+        float v = 0.0f;
+        if (b < nb && r < R)
+            v = w ? w_sums[static_cast<int64_t>(b) * N + r]
+                  : __half2float(__ushort_as_half(a_zeros[static_cast<int64_t>(b) * M + r]));
+        t[k][tx] = v;
+    }
+    __syncthreads();
+    float* out = w ? Wp : Zp;
+    for (int k = ty; k < 32; k += 8) {
+        const int64_t r = r0 + k;
+        if (r >= R) continue;
+        const float v = t[tx][k];
+        const int j = b0 + tx;   // < nbp
+        if (w) {
+            const float hi = __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
+            out[r * kp + j] = hi;
+            out[r * kp + nbp + j] = __fsub_rn(v, hi);
+        } else {
+            out[r * kp + j] = v;
+            out[r * kp + nbp + j] = v;
+        }
+    }
+}
+
+int zero_nbp(int nb) { return (nb + 31) / 32 * 32; }
+size_t align1k(size_t x) { return (x + 1023) & ~size_t(1023); }
 
 }  // namespace
 
@@ -315,12 +409,49 @@ cudaError_t launch_outlier_gemm(const void* X, int64_t ldx, int64_t M, const int
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    e = ensure_smem_limit(reinterpret_cast<const void*>(outlier_gemm_kernel), static_cast<int>(kOSmemBytes));
+    e = ensure_smem_limit(reinterpret_cast<const void*>(outlier_gemm_kernel<false>), static_cast<int>(kOSmemBytes));
     if (e != cudaSuccess) return e;
     const int64_t mtiles = (M + kOTileM - 1) / kOTileM, tiles = mtiles * ((N + kOTileN - 1) / kOTileN);
     const int64_t grid = tiles < num_sms ? tiles : (num_sms > 0 ? num_sms : 1);
-    outlier_gemm_kernel<<<static_cast<unsigned>(grid), kOThreads, kOSmemBytes, stream>>>(
-        tm_x, tm_w, tm_y, n_out, static_cast<int>(N), static_cast<int>(mtiles), tiles, status);
+    outlier_gemm_kernel<false><<<static_cast<unsigned>(grid), kOThreads, kOSmemBytes, stream>>>(
+        tm_x, tm_w, tm_y, n_out, static_cast<int>(N), static_cast<int>(mtiles), tiles, nullptr, 0,
+        static_cast<int>(M), status);
+    return cudaGetLastError();
+}
+
+size_t zero_term_bytes(const fmpq_layout& L, int64_t M, int64_t N) {
+    const size_t kp = 2 * static_cast<size_t>(zero_nbp(L.nb));
+    return align1k(static_cast<size_t>(M) * N * 4) + align1k(static_cast<size_t>(M) * kp * 4) +
+           align1k(static_cast<size_t>(N) * kp * 4);
+}
+
+cudaError_t launch_zero_term(const fmpq_layout& L, const void* a_zeros, const float* w_sums, int64_t M, int64_t N,
+                             void* ws, cudaStream_t stream, bool* maps_ok) {
+    *maps_ok = true;
+    const int nbp = zero_nbp(L.nb), kp = 2 * nbp;
+    float* yz = static_cast<float*>(ws);
+    float* zp = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + align1k(static_cast<size_t>(M) * N * 4));
+    float* wp = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(zp) + align1k(static_cast<size_t>(M) * kp * 4));
+    const EncodeTiledFn enc = encode_tiled();
+    CUtensorMap tm_x, tm_w;
+    if (enc == nullptr || !make_map(enc, &tm_x, zp, kp, M, kp, kOTileM, true) ||
+        !make_map(enc, &tm_w, wp, kp, N, kp, kOTileN, true)) {
+        *maps_ok = false;
+        return cudaSuccess;
+    }
+    const int64_t rmax = M > N ? M : N;
+    const dim3 tgrid(static_cast<unsigned>((rmax + 31) / 32), static_cast<unsigned>(nbp / 32), 2);
+    zero_operands_kernel<<<tgrid, 256, 0, stream>>>(static_cast<const uint16_t*>(a_zeros), w_sums, M, N, L.nb, nbp,
+                                                   zp, wp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = ensure_smem_limit(reinterpret_cast<const void*>(outlier_gemm_kernel<true>), static_cast<int>(kOSmemBytes));
+    if (e != cudaSuccess) return e;
+    const int64_t mtiles = (M + kOTileM - 1) / kOTileM, tiles = mtiles * ((N + kOTileN - 1) / kOTileN);
+    const int64_t grid = tiles < L.num_sms ? tiles : (L.num_sms > 0 ? L.num_sms : 1);
+    outlier_gemm_kernel<true><<<static_cast<unsigned>(grid), kOThreads, kOSmemBytes, stream>>>(
+        tm_x, tm_w, tm_x, kp, static_cast<int>(N), static_cast<int>(mtiles), tiles, yz, N, static_cast<int>(M),
+        L.d_status);
     return cudaGetLastError();
 }
 

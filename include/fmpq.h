@@ -321,8 +321,11 @@ FMPQ_API fmpq_status fmpq_plan_layout_budget(int32_t K, const uint32_t* absmax_h
 FMPQ_API int32_t fmpq_outlier_blocks(int32_t K, double fraction);
 
 /* ---- Quantization variants the pages describe beside FMPQ ----
- * Both run on the same layouts, packed formats and 2-SM GEMM kernel (for every M), with one
- * more term per block in the epilogue. Their workspace (same rules as w4ax_gemm's): */
+ * Both run on the same layouts, packed formats and 2-SM GEMM kernel (for every M), with a
+ * zero-point term. Their workspace: the larger of the two variants' needs. QoQ needs the
+ * split-K part only (as w4ax_gemm: 0 for shapes with enough tiles); QUIK needs it too, plus its
+ * zero-point term (M*N*4 bytes and the term's operands) for every shape, so its workspace is
+ * never empty. */
 FMPQ_API size_t fmpq_variant_gemm_workspace_bytes(const fmpq_layout* layout, int64_t M, int64_t N);
 
 /* QUIK asymmetric activations (QUIK explainer, "反量化背后的数学": activations take a scale and a
@@ -347,8 +350,10 @@ FMPQ_API fmpq_status w4_weight_sums(const fmpq_layout* layout, const void* W_pac
 /* The GEMM on asymmetric activations:
  *   Y[m][n] = fp16_rn( sum_b ( a_scales[b][m] * w_scales[b][n] * P[m][n][b]
  *                              + a_zeros[b][m] * w_sums[b][n] ) ),   FP32 accumulation,
- * P the exact integer sums of the unsigned activation codes times the weight codes. Shapes,
- * alignment, workspace (fmpq_variant_gemm_workspace_bytes) as w4ax_gemm. */
+ * P the exact integer sums of the unsigned activation codes times the weight codes. The zero-point
+ * sum over b is formed first on the tensor cores (tf32 with a two-term split of w_sums, so every
+ * product is exact) into the workspace, and added once per output. Shapes and alignment as
+ * w4ax_gemm; workspace: fmpq_variant_gemm_workspace_bytes (never 0), else FMPQ_ERR_WORKSPACE. */
 FMPQ_API fmpq_status w4ax_gemm_asym(const fmpq_layout* layout, const void* A_packed, const void* a_scales,
                                     const void* a_zeros, const void* W_packed, const void* w_scales,
                                     const float* w_sums, int64_t M, int64_t N, void* Y, int64_t ldy,
