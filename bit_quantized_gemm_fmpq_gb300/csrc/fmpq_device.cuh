@@ -288,29 +288,6 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N) {
            | ((M >> 4) << 24);  // M / 16
 }
 
-// Instruction descriptor: kind::tf32, A = B = TF32 (fp32 words, the low 13 mantissa bits
-// ignored), D = F32, both K-major, shape MxN.
-__host__ __device__ constexpr uint32_t idesc_tf32_f32(uint32_t M, uint32_t N) {
-    return (1u << 4)            // D format: F32
-           | (2u << 7)          // A format: TF32
-           | (2u << 10)         // B format: TF32
-           | ((N >> 3) << 17)   // N / 8
-           | ((M >> 4) << 24);  // M / 16
-}
-
-// D[tmem] (+)= A[smem] * B[smem]^T with tf32 operands, one instruction (K = 8).
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n"
-        ".reg .pred p;\n"
-        "setp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n"
-        "}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // D[tmem] (+)= A[smem] * B[smem]^T with fp16 operands, one instruction (K = 16).
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                         uint32_t accumulate) {

@@ -119,7 +119,8 @@ cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& args, cudaStream_t
 
 // QUIK zero-point term on the tensor cores, for the variant GEMM to add once per output:
 // yz[m][n] = sum_b a_zeros[b][m] * w_sums[b][n] (FP32) at the start of ws, operands after it
-// (zero_term_bytes in all). tcgen05 kind::tf32 on the zero points and a two-term split of w_sums.
+// (zero_term_bytes in all). tcgen05 kind::f16 on the zero points and a scaled two-term fp16 split
+// of w_sums (exact products).
 size_t zero_term_bytes(const fmpq_layout& L, int64_t M, int64_t N);
 cudaError_t launch_zero_term(const fmpq_layout& L, const void* a_zeros, const float* w_sums, int64_t M, int64_t N,
                              void* ws, cudaStream_t stream, bool* maps_ok);

@@ -24,10 +24,11 @@
 //   L2; the resident panel removes W_out's share.
 //
 // The QUIK zero-point term (QUIK explainer, "反量化背后的数学": the zero point's contribution is
-// z times the sum of the dequantized weights): yz[m][n] = sum_b z[b][m] * ws[b][n] in FP32, the
-// same kernel in its tf32 form (kind::tf32, fp32 operands, FP32 rows stored straight from the
-// epilogue) on operands that zero_operands_kernel lays out so that every product is exact. The
-// variant GEMM adds yz once per output instead of one FP32 pass per block.
+// z times the sum of the weights, which is computed offline): yz[m][n] = sum_b z[b][m] *
+// ws[b][n] in FP32, the same kernel with its FP32 rows stored straight from the epilogue
+// (outlier_gemm_kernel<true>), on fp16 operands that zero_operands_kernel lays out so that the
+// products are exact (the zero points, and a scaled two-term split of ws). The variant GEMM
+// starts its accumulators from yz instead of one FP32 pass per block.
 //
 // Nothing is allocated: the tensor maps live in kernel parameter space.
 #include <cuda.h>
@@ -53,15 +54,15 @@ __global__ void outlier_gather_kernel(const uint16_t* X, int64_t ldx, int64_t M,
 
 constexpr int kOThreads = 192;
 constexpr int kOTileM = 128, kOTileN = 128, kOChunk = 64;   // kOChunk fp16 = one 128-byte swizzle row
-constexpr int kOPanel = 4;            // W_out chunks kept resident across tiles: n_out <= 256
-constexpr int kOBoxes = 10;           // operand boxes: panel (4) + X_out ring (6), or a ring of 5 (X_out, W_out) pairs
-constexpr int kOMaxStages = 6;
+constexpr int kOMaxStages = 7;
 constexpr int kOBox = kOTileM * kOChunk * 2;   // one 128-row x 64-channel fp16 box (16 KB)
 constexpr uint32_t kOTmemCols = 256;  // two 128-column FP32 accumulators
 
 struct __align__(1024) OSmem {
-    uint8_t box[kOBoxes][kOBox];  // X_out / W_out boxes: 128 rows x 64 channels (swizzled)
-    uint8_t y[2][2][kOBox];       // two fp16 product tiles in flight, each as two boxes of 64 columns (swizzled)
+    // 14 boxes of 128 rows x 64 channels (swizzled). The merged product uses the first 10 for its
+    // operands and the last 4 as two fp16 staging tiles (two boxes of 64 columns each); the
+    // stored product (no staging) uses all 14 for operands.
+    uint8_t box[14][kOBox];
     uint64_t full[kOMaxStages], empty[kOMaxStages];
     uint64_t w_full, w_free;      // panel landed / every MMA reading the panel finished
     uint64_t acc_full[2], acc_empty[2];
@@ -81,28 +82,33 @@ struct OTiles {
     __device__ int nt(int64_t t) const { return static_cast<int>(t / mtiles); }
 };
 
-// kTf32 = false: the FP16 outlier product, merged into the fp16 Y with a TMA reduce-add.
-// kTf32 = true: the same pipeline on fp32 operands read as tf32 (a 128-byte box row is 32 of
-// them), the FP32 product stored to yz [m_rows][ldz] (the QUIK zero-point term).
-template <bool kTf32>
+// kStore = false: the FP16 outlier product, merged into the fp16 Y with a TMA reduce-add.
+// kStore = true: the FP32 product, each column times colscale[n], stored to yz [m_rows][ldz]
+// (the QUIK zero-point term).
+template <bool kStore>
 __global__ void __launch_bounds__(kOThreads, 1)
     outlier_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                         const __grid_constant__ CUtensorMap tm_y, int n_out, int n_cols, int mtiles, int64_t tiles,
-                        float* yz, int64_t ldz, int m_rows, int32_t* status) {
-    constexpr int kElems = kTf32 ? 32 : kOChunk;   // K elements per 128-byte box row
-    constexpr uint32_t kIdesc = kTf32 ? dev::idesc_tf32_f32(kOTileM, kOTileN) : dev::idesc_f16_f32(kOTileM, kOTileN);
+                        float* yz, int64_t ldz, int m_rows, const float* colscale, int32_t* status) {
+    constexpr int kElems = kOChunk;   // K elements per 128-byte box row
+    constexpr uint32_t kIdesc = dev::idesc_f16_f32(kOTileM, kOTileN);
+    // W_out chunks kept resident across tiles (n_out <= 256, or 448 for the stored product) and
+    // the operand boxes there are
+    constexpr int kPanel = kStore ? 7 : 4;
+    constexpr int kBoxes = kStore ? 14 : 10;
     extern __shared__ uint8_t smem_raw[];
     OSmem& s = *reinterpret_cast<OSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const OTiles tl{mtiles, static_cast<int64_t>(blockIdx.x) * tiles / gridDim.x,
                     static_cast<int64_t>(blockIdx.x + 1) * tiles / gridDim.x};
     const int chunks = (n_out + kElems - 1) / kElems;
-    const bool panel = chunks <= kOPanel;
-    // panel: W_out chunk c in box c, ring stage st's X_out in box kOPanel + st (6 stages);
-    // otherwise stage st holds X_out in box 2 st and W_out in box 2 st + 1 (5 stages)
-    const int S = panel ? kOBoxes - kOPanel : kOBoxes / 2;
-    auto xbox = [&](int st) { return s.box[panel ? kOPanel + st : 2 * st]; };
+    const bool panel = chunks <= kPanel;
+    // panel: W_out chunk c in box c, ring stage st's X_out in box kPanel + st (6 or 7 stages);
+    // otherwise stage st holds X_out in box 2 st and W_out in box 2 st + 1 (5 or 7 stages)
+    const int S = panel ? kBoxes - kPanel : kBoxes / 2;
+    auto xbox = [&](int st) { return s.box[panel ? kPanel + st : 2 * st]; };
     auto wbox = [&](int st, int c) { return s.box[panel ? c : 2 * st + 1]; };
+    auto ybox = [&](int buf, int half) { return s.box[10 + 2 * buf + half]; };
     auto yboxes = [&](int nt) { return n_cols - nt * kOTileN > 64 ? 2 : 1; };   // a box wholly past N is skipped
     volatile int* abort_flag = &s.abort_flag;
 
@@ -205,10 +211,7 @@ __global__ void __launch_bounds__(kOThreads, 1)
                     const uint64_t bd = dev::sdesc_k_sw128(dev::smem_u32(wbox(st, c)));
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {   // 32 bytes of K per MMA: +2 in the address field
-                        if constexpr (kTf32)
-                            dev::mma_tf32(d, ad + 2 * k, bd + 2 * k, kIdesc, (c > 0 || k > 0) ? 1u : 0u);
-                        else
-                            dev::mma_f16(d, ad + 2 * k, bd + 2 * k, kIdesc, (c > 0 || k > 0) ? 1u : 0u);
+                        dev::mma_f16(d, ad + 2 * k, bd + 2 * k, kIdesc, (c > 0 || k > 0) ? 1u : 0u);
                     }
                     dev::mma_commit(&s.empty[st]);
                 }
@@ -241,7 +244,7 @@ __global__ void __launch_bounds__(kOThreads, 1)
             if (dev::named_bar_sync_or(1, 128, !ok)) break;
             dev::tc_fence_after();
             const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(ab) * kOTileN;
-            if constexpr (kTf32) {
+            if constexpr (kStore) {
                 // FP32 rows straight to yz: thread r writes 512 contiguous bytes of its row
                 const int row = mt * kOTileM + r;
 #pragma unroll 1
@@ -256,9 +259,12 @@ __global__ void __launch_bounds__(kOThreads, 1)
                         for (int g = 0; g < 8; ++g) {
                             const int col = nt * kOTileN + 32 * c + 4 * g;
                             const uint32_t* dg = g < 4 ? d0 + 4 * g : d1 + 4 * (g - 4);
-                            if (col + 4 <= n_cols)
-                                *reinterpret_cast<uint4*>(yz + static_cast<int64_t>(row) * ldz + col) =
-                                    make_uint4(dg[0], dg[1], dg[2], dg[3]);
+                            if (col + 4 <= n_cols) {
+                                const float4 cs = __ldg(reinterpret_cast<const float4*>(colscale + col));
+                                *reinterpret_cast<float4*>(yz + static_cast<int64_t>(row) * ldz + col) =
+                                    make_float4(__uint_as_float(dg[0]) * cs.x, __uint_as_float(dg[1]) * cs.y,
+                                                __uint_as_float(dg[2]) * cs.z, __uint_as_float(dg[3]) * cs.w);
+                            }
                         }
                     }
                 }
@@ -273,7 +279,7 @@ __global__ void __launch_bounds__(kOThreads, 1)
                     dev::tmem_ld16(taddr + 32 * c + 16, d1);
                     dev::tmem_ld_wait16(d0);
                     dev::tmem_ld_wait16(d1);
-                    uint8_t* box = s.y[ab][c >> 1];
+                    uint8_t* box = ybox(ab, c >> 1);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         // 16-byte chunk (c % 2) * 4 + j of row r sits at chunk position (that ^ r % 8)
@@ -294,15 +300,15 @@ __global__ void __launch_bounds__(kOThreads, 1)
                 dev::fence_proxy_async_smem();   // the reduce reads what these threads wrote
                 dev::named_bar_sync(2, 128);
                 if (storer) {
-                    dev::tma_reduce_add_2d(&tm_y, nt * kOTileN, mt * kOTileM, s.y[ab][0]);
-                    if (nyb == 2) dev::tma_reduce_add_2d(&tm_y, nt * kOTileN + 64, mt * kOTileM, s.y[ab][1]);
+                    dev::tma_reduce_add_2d(&tm_y, nt * kOTileN, mt * kOTileM, ybox(ab, 0));
+                    if (nyb == 2) dev::tma_reduce_add_2d(&tm_y, nt * kOTileN + 64, mt * kOTileM, ybox(ab, 1));
                     dev::bulk_commit_group();
                     dev::bulk_wait_group_read1();   // tile i - 1's reduce has read its staging tile
                 }
                 __syncwarp();
             }
         }
-        if (!kTf32 && storer) dev::bulk_wait_group0();   // every reduce performed before the CTA exits
+        if (!kStore && storer) dev::bulk_wait_group0();   // every reduce performed before the CTA exits
         __syncwarp();
     }
     dev::tc_fence_before();
@@ -313,60 +319,56 @@ __global__ void __launch_bounds__(kOThreads, 1)
     }
 }
 
-// A 2-D fp16 (or fp32) tensor [rows][cols] with row stride ld (elements), read in boxes of one
-// 128-byte row (64 fp16 or 32 fp32) x box_rows with the 128-byte swizzle.
+// A 2-D fp16 tensor [rows][cols] with row stride ld (elements), read in boxes of 64 x box_rows
+// with the 128-byte swizzle.
 bool make_map(EncodeTiledFn enc, CUtensorMap* map, const void* base, int64_t cols, int64_t rows, int64_t ld,
-              uint32_t box_rows, bool fp32 = false) {
+              uint32_t box_rows) {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * (fp32 ? 4 : 2)};
-    const cuuint32_t box[2] = {fp32 ? 32u : 64u, box_rows};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    const cuuint32_t box[2] = {64, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    return enc(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-               const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// QUIK zero-point term operands (K' = 2 nbp, nbp = nb rounded up to 32):
-//   Zp[m][j] = z[j mod nbp][m]                (fp16 zero points, exact in fp32 and in tf32)
-//   Wp[n][j] = hi(ws[j][n]) for j < nbp, ws[j - nbp][n] - hi(ws[j - nbp][n]) after
-// (0 for block indices >= nb), hi = ws with the 13 low mantissa bits cleared. Both parts are
-// exact in tf32 when ws has at most 22 significant bits (w_sums = fp16 scale x code sum has
-// at most 21), so sum_j Zp Wp is sum_b z ws with exact products.
+// QUIK zero-point term operands, fp16, K' = 2 nbp (nbp = nb rounded up to 32), one warp per row:
+//   Zp[m][j] = z[j mod nbp][m]                              (the fp16 zero points)
+//   Wp[n][j] = hi_b for j = b < nbp, lo_b for j = nbp + b     (0 for block indices >= nb)
+// with hi_b = fp16_rn(2^e_n ws[b][n]), lo_b = fp16_rn(2^e_n ws[b][n] - hi_b), e_n putting the
+// column's largest |ws| in [2^14, 2^15), colscale[n] = 2^-e_n. hi + lo hold 22 significant bits
+// (w_sums = fp16 scale x code sum has at most 21), so z * hi + z * lo is z * ws exactly in FP32,
+// except for terms below 2^-18 of their column's largest, whose lo part is an fp16 subnormal
+// (error below 2^-40 of the column's largest term).
 __global__ void zero_operands_kernel(const uint16_t* a_zeros, const float* w_sums, int64_t M, int64_t N, int nb,
-                                     int nbp, float* Zp, float* Wp) {
-    // one 32 x 32 tile of (block b, row r) per CTA, transposed through shared memory so that both
-    // the reads (along r) and the writes (along b) are coalesced; z = 0: Zp, z = 1: Wp
-    __shared__ float t[32][33];
-    const bool w = blockIdx.z != 0;
-    const int64_t R = w ? N : M;
-    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 32;
-    if (r0 >= R) return;   // uniform per CTA
-    const int b0 = blockIdx.y * 32, kp = 2 * nbp;
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8 threads
-    for (int k = ty; k < 32; k += 8) {
-        const int b = b0 + k;
-        const int64_t r = r0 + tx;
-        float v = 0.0f;
-        if (b < nb && r < R)
-            v = w ? w_sums[static_cast<int64_t>(b) * N + r]
-                  : __half2float(__ushort_as_half(a_zeros[static_cast<int64_t>(b) * M + r]));
-        t[k][tx] = v;
-    }
-    __syncthreads();
-    float* out = w ? Wp : Zp;
-    for (int k = ty; k < 32; k += 8) {
-        const int64_t r = r0 + k;
-        if (r >= R) continue;
-        const float v = t[tx][k];
-        const int j = b0 + tx;   // < nbp
-        if (w) {
-            const float hi = __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
-            out[r * kp + j] = hi;
-            out[r * kp + nbp + j] = __fsub_rn(v, hi);
-        } else {
-            out[r * kp + j] = v;
-            out[r * kp + nbp + j] = v;
+                                     int nbp, uint16_t* Zp, uint16_t* Wp, float* colscale) {
+    const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;   // warp-uniform
+    const int lane = threadIdx.x & 31;
+    const int kp = 2 * nbp;
+    if (r < M) {
+        uint16_t* row = Zp + r * kp;
+        for (int b = lane; b < nbp; b += 32) {
+            const uint16_t z = b < nb ? a_zeros[static_cast<int64_t>(b) * M + r] : uint16_t(0);
+            row[b] = z;
+            row[nbp + b] = z;
+        }
+    } else if (r < M + N) {
+        const int64_t n = r - M;
+        float mx = 0.0f;
+        for (int b = lane; b < nb; b += 32) mx = fmaxf(mx, fabsf(w_sums[static_cast<int64_t>(b) * N + n]));
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        int x = 0;
+        if (mx > 0.0f) frexpf(mx, &x);          // mx = f 2^x, f in [0.5, 1)
+        const int e = mx > 0.0f ? min(15 - x, 100) : 0;
+        if (lane == 0) colscale[n] = ldexpf(1.0f, -e);
+        uint16_t* row = Wp + n * kp;
+        for (int b = lane; b < nbp; b += 32) {
+            const float v = b < nb ? ldexpf(w_sums[static_cast<int64_t>(b) * N + n], e) : 0.0f;
+            const __half h = __float2half_rn(v);
+            const __half l = __float2half_rn(__fsub_rn(v, __half2float(h)));
+            row[b] = __half_as_ushort(h);
+            row[nbp + b] = __half_as_ushort(l);
         }
     }
 }
@@ -415,34 +417,37 @@ cudaError_t launch_outlier_gemm(const void* X, int64_t ldx, int64_t M, const int
     const int64_t grid = tiles < num_sms ? tiles : (num_sms > 0 ? num_sms : 1);
     outlier_gemm_kernel<false><<<static_cast<unsigned>(grid), kOThreads, kOSmemBytes, stream>>>(
         tm_x, tm_w, tm_y, n_out, static_cast<int>(N), static_cast<int>(mtiles), tiles, nullptr, 0,
-        static_cast<int>(M), status);
+        static_cast<int>(M), nullptr, status);
     return cudaGetLastError();
 }
 
 size_t zero_term_bytes(const fmpq_layout& L, int64_t M, int64_t N) {
     const size_t kp = 2 * static_cast<size_t>(zero_nbp(L.nb));
-    return align1k(static_cast<size_t>(M) * N * 4) + align1k(static_cast<size_t>(M) * kp * 4) +
-           align1k(static_cast<size_t>(N) * kp * 4);
+    return align1k(static_cast<size_t>(M) * N * 4) + align1k(static_cast<size_t>(M) * kp * 2) +
+           align1k(static_cast<size_t>(N) * kp * 2) + align1k(static_cast<size_t>(N) * 4);
 }
 
 cudaError_t launch_zero_term(const fmpq_layout& L, const void* a_zeros, const float* w_sums, int64_t M, int64_t N,
                              void* ws, cudaStream_t stream, bool* maps_ok) {
     *maps_ok = true;
     const int nbp = zero_nbp(L.nb), kp = 2 * nbp;
-    float* yz = static_cast<float*>(ws);
-    float* zp = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + align1k(static_cast<size_t>(M) * N * 4));
-    float* wp = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(zp) + align1k(static_cast<size_t>(M) * kp * 4));
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    float* yz = reinterpret_cast<float*>(base);
+    base += align1k(static_cast<size_t>(M) * N * 4);
+    uint16_t* zp = reinterpret_cast<uint16_t*>(base);
+    base += align1k(static_cast<size_t>(M) * kp * 2);
+    uint16_t* wp = reinterpret_cast<uint16_t*>(base);
+    base += align1k(static_cast<size_t>(N) * kp * 2);
+    float* colscale = reinterpret_cast<float*>(base);
     const EncodeTiledFn enc = encode_tiled();
     CUtensorMap tm_x, tm_w;
-    if (enc == nullptr || !make_map(enc, &tm_x, zp, kp, M, kp, kOTileM, true) ||
-        !make_map(enc, &tm_w, wp, kp, N, kp, kOTileN, true)) {
+    if (enc == nullptr || !make_map(enc, &tm_x, zp, kp, M, kp, kOTileM) || !make_map(enc, &tm_w, wp, kp, N, kp, kOTileN)) {
         *maps_ok = false;
         return cudaSuccess;
     }
-    const int64_t rmax = M > N ? M : N;
-    const dim3 tgrid(static_cast<unsigned>((rmax + 31) / 32), static_cast<unsigned>(nbp / 32), 2);
-    zero_operands_kernel<<<tgrid, 256, 0, stream>>>(static_cast<const uint16_t*>(a_zeros), w_sums, M, N, L.nb, nbp,
-                                                   zp, wp);
+    const int64_t warps = M + N;
+    zero_operands_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, stream>>>(
+        static_cast<const uint16_t*>(a_zeros), w_sums, M, N, L.nb, nbp, zp, wp, colscale);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     e = ensure_smem_limit(reinterpret_cast<const void*>(outlier_gemm_kernel<true>), static_cast<int>(kOSmemBytes));
@@ -451,7 +456,7 @@ cudaError_t launch_zero_term(const fmpq_layout& L, const void* a_zeros, const fl
     const int64_t grid = tiles < L.num_sms ? tiles : (L.num_sms > 0 ? L.num_sms : 1);
     outlier_gemm_kernel<true><<<static_cast<unsigned>(grid), kOThreads, kOSmemBytes, stream>>>(
         tm_x, tm_w, tm_x, kp, static_cast<int>(N), static_cast<int>(mtiles), tiles, yz, N, static_cast<int>(M),
-        L.d_status);
+        colscale, L.d_status);
     return cudaGetLastError();
 }
 

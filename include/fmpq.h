@@ -351,8 +351,8 @@ FMPQ_API fmpq_status w4_weight_sums(const fmpq_layout* layout, const void* W_pac
  *   Y[m][n] = fp16_rn( sum_b ( a_scales[b][m] * w_scales[b][n] * P[m][n][b]
  *                              + a_zeros[b][m] * w_sums[b][n] ) ),   FP32 accumulation,
  * P the exact integer sums of the unsigned activation codes times the weight codes. The zero-point
- * sum over b is formed first on the tensor cores (tf32 with a two-term split of w_sums, so every
- * product is exact) into the workspace, and added once per output. Shapes and alignment as
+ * sum over b is formed first on the tensor cores (fp16 zero points times a scaled two-term fp16
+ * split of w_sums, products exact) into the workspace, and added once per output. Shapes and alignment as
  * w4ax_gemm; workspace: fmpq_variant_gemm_workspace_bytes (never 0), else FMPQ_ERR_WORKSPACE. */
 FMPQ_API fmpq_status w4ax_gemm_asym(const fmpq_layout* layout, const void* A_packed, const void* a_scales,
                                     const void* a_zeros, const void* W_packed, const void* w_scales,
