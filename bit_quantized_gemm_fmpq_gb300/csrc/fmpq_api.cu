@@ -307,7 +307,7 @@ fmpq_status w4ax_gemm_fault_test(const fmpq_layout* L, const void* A_packed, con
 
 size_t fmpq_variant_gemm_workspace_bytes(const fmpq_layout* L, int64_t M, int64_t N) {
     if (L == nullptr || M < 1 || N < 1) return 0;
-    return fmpq::quik_workspace_bytes(*L, M, N);   // the larger of the two variants' needs
+    return fmpq::variant_workspace_bytes(*L, M, N);
 }
 
 fmpq_status fmpq_quantize_asym(const fmpq_layout* L, const void* X, int64_t ldx, int64_t M, void* A_packed,
@@ -344,7 +344,7 @@ fmpq_status w4ax_gemm_asym(const fmpq_layout* L, const void* A_packed, const voi
     if (ldy % 8 != 0 || !aligned16(A_packed) || !aligned16(a_scales) || !aligned16(a_zeros) || !aligned16(W_packed) ||
         !aligned16(w_scales) || !aligned16(w_sums) || !aligned16(Y))
         return FMPQ_ERR_MISALIGNED;
-    const size_t need = fmpq::quik_workspace_bytes(*L, M, N);
+    const size_t need = fmpq::variant_workspace_bytes(*L, M, N);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return FMPQ_ERR_WORKSPACE;
     if (need > 0 && !aligned16(workspace)) return FMPQ_ERR_MISALIGNED;
     if (fmpq_status st = check_device(L)) return st;
@@ -414,7 +414,7 @@ fmpq_status qoq_gemm(const fmpq_layout* L, const void* A_packed, const void* a_s
     if (ldy % 8 != 0 || !aligned16(A_packed) || !aligned16(a_scales) || !aligned16(a_sums) || !aligned16(W_packed) ||
         !aligned16(ch_scales) || !aligned16(grp_scales) || !aligned16(grp_zeros) || !aligned16(Y))
         return FMPQ_ERR_MISALIGNED;
-    const size_t need = fmpq::gemm_workspace_bytes(*L, M, N, true);
+    const size_t need = fmpq::variant_workspace_bytes(*L, M, N);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return FMPQ_ERR_WORKSPACE;
     if (need > 0 && !aligned16(workspace)) return FMPQ_ERR_MISALIGNED;
     if (fmpq_status st = check_device(L)) return st;

@@ -59,8 +59,6 @@ constexpr int kSwStride = 68;
 struct ScaleSlot {
     float sw[4 * kSwStride];  // weight scales of the tile's 256 columns (permuted, see above)
     float sx[128];            // activation scales of this CTA's 128 rows, times 2^18
-    float wz[4 * kSwStride];  // zero-point variants: the weight factor of the zero term (same order)
-    float xz[128];            //   and the activation factor, per row
 };
 
 struct __align__(1024) Smem {
@@ -113,14 +111,10 @@ struct Params {
     // quantization variants (see GemmArgs)
     uint32_t wmask;        // code bits the converter keeps: 0x87878787 sign-magnitude, 0x0F0F0F0F unsigned
     int zero_kind;
-    const uint16_t* a_zeros;
-    const int32_t* a_sums;
-    const float* w_sums;
     const uint16_t* ch_scales;
     const uint8_t* grp_scales;
-    const uint8_t* grp_zeros;
-    // QUIK with the zero-point term precomputed on the tensor cores: yz[m][n] (FP32, row
-    // stride N), added once per output before the fp16 rounding; nullptr: one pass per block
+    // the variants' zero-point term summed over all blocks on the tensor cores beforehand:
+    // yz[m][n] (FP32, row stride N), the accumulators' starting value; nullptr for FMPQ
     const float* yz;
     // failure-detection test: polls before a device wait gives up, and the index of the packed
     // weight copy the first CTA withholds (-1: none)
@@ -211,15 +205,6 @@ __device__ __forceinline__ void activation_producer(const Params& p, Smem& s, ui
         const int r0 = t.mt * kPairM + static_cast<int>(rank) * 128;
         const uint32_t abytes = static_cast<uint32_t>(max(0, min(128, p.M - r0))) * kBlock;
         for (int b = t.b0; ok && b < t.b1; ++b, ++it) {
-            if (p.yz != nullptr && b == t.b0 && t.split == 0) {
-                // QUIK: the tile's rows of the precomputed zero-point term go to the L2 while the
-                // epilogue is still on earlier blocks (one 1 KB row per prefetch)
-                const int cols = min(kTileN, p.N - t.nt * kTileN);   // N % 16 == 0: a multiple of 64 bytes
-                for (int r = lane; r < 128; r += 32)
-                    if (r0 + r < p.M)
-                        dev::bulk_prefetch_l2(p.yz + static_cast<int64_t>(r0 + r) * p.N + t.nt * kTileN,
-                                              static_cast<uint32_t>(cols) * 4u);
-            }
             const int planes = s.mask[b] ? 2 : 1;
             // the slots of this block's planes must have been released by the MMAs of the
             // blocks that used them last (the whole warp waits, converged; lane 0 issues)
@@ -340,12 +325,21 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, uint32_
     if (u >= num_units) return;
     Unit t = unit_of(p, u);
     int b = t.b0;
+    // variants: as the converters reach a tile, its rows of the precomputed zero-point term go to
+    // the L2 (one 1 KB row per thread), a few blocks before the epilogue starts from them
+    auto prefetch_zero_term = [&](const Unit& tt) {
+        const int row = tt.mt * kPairM + static_cast<int>(rank) * 128 + ct;
+        if (p.yz != nullptr && tt.split == 0 && row < p.M) {
+            const int cols = min(kTileN, p.N - tt.nt * kTileN);   // N % 16 == 0: a multiple of 64 bytes
+            dev::bulk_prefetch_l2(p.yz + static_cast<int64_t>(row) * p.N + tt.nt * kTileN, static_cast<uint32_t>(cols) * 4u);
+        }
+    };
+    prefetch_zero_term(t);
     // this thread's entries of the block's scales: weight columns ct and ct + 128, activation
-    // row ct (and the zero-term factors of the variants), fetched one block ahead as raw values
-    // and converted when they are staged, so that the loads' latency hides behind a block
+    // row ct, fetched one block ahead as raw values and converted when they are staged, so that
+    // the loads' latency hides behind a block
     uint32_t sc0 = 0, sc1 = 0, sc2 = 0;   // fp16 bits: weight scales (QoQ: s1) and activation scale
-    uint32_t zc0 = 0, zc1 = 0, zc2 = 0;   // QUIK: w_sums (fp32 bits) and the zero point (fp16 bits);
-                                          // QoQ: s2 | z2 << 8 per column and the code sum
+    uint32_t gc0 = 0, gc1 = 0;            // QoQ: the group scale s2 per column
     auto load_scales = [&](const Unit& tt, int bb) {
         const int n0 = tt.nt * kTileN, m0 = tt.mt * kPairM + static_cast<int>(rank) * 128;
         const int n_a = n0 + ct, n_b = n0 + ct + 128, m = m0 + ct;
@@ -354,18 +348,12 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, uint32_
             sc0 = n_a < p.N ? __ldg(p.w_scales + wb + n_a) : 0u;
             sc1 = n_b < p.N ? __ldg(p.w_scales + wb + n_b) : 0u;
             sc2 = m < p.M ? __ldg(p.a_scales + xb + m) : 0u;
-            if (p.zero_kind == kZeroQuik && p.yz == nullptr) {
-                zc0 = n_a < p.N ? __float_as_uint(__ldg(p.w_sums + wb + n_a)) : 0u;
-                zc1 = n_b < p.N ? __float_as_uint(__ldg(p.w_sums + wb + n_b)) : 0u;
-                zc2 = m < p.M ? __ldg(p.a_zeros + xb + m) : 0u;
-            }
         } else {
             sc0 = n_a < p.N ? __ldg(p.ch_scales + n_a) : 0u;
             sc1 = n_b < p.N ? __ldg(p.ch_scales + n_b) : 0u;
             sc2 = m < p.M ? __ldg(p.a_scales + m) : 0u;
-            zc0 = n_a < p.N ? (__ldg(p.grp_scales + wb + n_a) | (static_cast<uint32_t>(__ldg(p.grp_zeros + wb + n_a)) << 8)) : 0u;
-            zc1 = n_b < p.N ? (__ldg(p.grp_scales + wb + n_b) | (static_cast<uint32_t>(__ldg(p.grp_zeros + wb + n_b)) << 8)) : 0u;
-            zc2 = m < p.M ? static_cast<uint32_t>(__ldg(p.a_sums + xb + m)) : 0u;
+            gc0 = n_a < p.N ? __ldg(p.grp_scales + wb + n_a) : 0u;
+            gc1 = n_b < p.N ? __ldg(p.grp_scales + wb + n_b) : 0u;
         }
     };
     load_scales(t, b);
@@ -404,20 +392,10 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, uint32_
         if (p.zero_kind != kZeroQoq) {
             sl.sw[swd0] = h2f(sc0);
             sl.sw[swd1] = h2f(sc1);
-            if (p.zero_kind == kZeroQuik && p.yz == nullptr) {
-                sl.wz[swd0] = __uint_as_float(zc0);
-                sl.wz[swd1] = __uint_as_float(zc1);
-                sl.xz[ct] = h2f(zc2);
-            }
         } else {
-            // QoQ: weight scale s1 * s2 (exact in fp32); zero term -(s1 s2 z2)[n] * (sx * code sum)[m]
-            const float w0 = h2f(sc0) * static_cast<float>(zc0 & 0xFFu);
-            const float w1 = h2f(sc1) * static_cast<float>(zc1 & 0xFFu);
-            sl.sw[swd0] = w0;
-            sl.sw[swd1] = w1;
-            sl.wz[swd0] = -w0 * static_cast<float>(zc0 >> 8);
-            sl.wz[swd1] = -w1 * static_cast<float>(zc1 >> 8);
-            sl.xz[ct] = fx * static_cast<float>(static_cast<int32_t>(zc2));
+            // QoQ: weight scale s1 * s2 (exact in fp32)
+            sl.sw[swd0] = h2f(sc0) * static_cast<float>(gc0);
+            sl.sw[swd1] = h2f(sc1) * static_cast<float>(gc1);
         }
         dev::fence_proxy_async_smem();
         __syncwarp();
@@ -432,6 +410,7 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, uint32_
             if (u >= num_units) break;
             t = unit_of(p, u);
             b = t.b0;
+            prefetch_zero_term(t);
         }
         load_scales(t, b);
     }
@@ -443,8 +422,8 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, uint32_
 // and all 256 columns, read with tcgen05.ld 16x256b: thread t holds rows t/4 and t/4 + 8 of
 // that slab and columns 8g + 2(t%4) + {0, 1}, g = 0..31 (four registers per 8 columns:
 // row0 col0, row0 col1, row1 col0, row1 col1).
-// kZ: the zero-point term. 0 none; 1 one FP32 pass per block (x_zero[m] * w_zero[n] from the
-// scale slot, QoQ); 2 precomputed over all blocks (yz), the starting value of the accumulators.
+// kZ: the zero-point term of the quantization variants. 0 none; 2 summed over all blocks
+// beforehand (yz, launch_zero_term), the starting value of the accumulators.
 template <bool kPartials, int kZ>
 __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, uint32_t rank, int warp, int lane,
                                               uint32_t tmem, volatile int* abort_flag, uint32_t polls) {
@@ -548,31 +527,9 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, uint32_t
                 dev::tc_fence_before();
             }
             __syncwarp();
-            if constexpr (kZ == 1 && !kPartials) {
-                // the accumulator is read: release it first; then the block's zero-point term
-                // x_zero[m] * w_zero[n], a second pass over the registers, from the scale slot
-                if (lane == 0 && ok) dev::mbar_arrive_remote(release);
-                if (ok) {
-                    const ScaleSlot& slz = s.sc[ss];
-                    const float4* wzv = reinterpret_cast<const float4*>(slz.wz + tq * kSwStride);
-                    const float2 xza = make_float2(slz.xz[lr0], slz.xz[lr0]);
-                    const float2 xzb = make_float2(slz.xz[lr1], slz.xz[lr1]);
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const float4 z = wzv[c];   // column pairs g = 2c, 2c + 1
-                        accA[2 * c] = dev::ffma2(xza, make_float2(z.x, z.y), accA[2 * c]);
-                        accB[2 * c] = dev::ffma2(xzb, make_float2(z.x, z.y), accB[2 * c]);
-                        accA[2 * c + 1] = dev::ffma2(xza, make_float2(z.z, z.w), accA[2 * c + 1]);
-                        accB[2 * c + 1] = dev::ffma2(xzb, make_float2(z.z, z.w), accB[2 * c + 1]);
-                    }
-                }
-                __syncwarp();
-                if (lane == 0 && ok) dev::mbar_arrive(&s.sc_empty[ss]);
-            } else {
-                if (lane == 0 && ok) {
-                    dev::mbar_arrive_remote(release);
-                    dev::mbar_arrive(&s.sc_empty[ss]);
-                }
+            if (lane == 0 && ok) {
+                dev::mbar_arrive_remote(release);
+                dev::mbar_arrive(&s.sc_empty[ss]);
             }
         }
         if constexpr (!kPartials) {
@@ -771,15 +728,15 @@ size_t gemm_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N, bool var
     return static_cast<size_t>(tiles) * splits * kPairM * kTileN * sizeof(float) + gemm_counter_bytes(L, M, N, variant);
 }
 
-size_t quik_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N) {
+size_t variant_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N) {
     return ((gemm_workspace_bytes(L, M, N, true) + 1023) & ~size_t(1023)) + zero_term_bytes(L, M, N);
 }
 
 cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& a, cudaStream_t stream) {
     const bool variant = a.zero_kind != kZeroNone || a.unsigned_w;
     if (!variant && gemm_small_path(a.M) && a.withhold < 0) return launch_gemm_small(L, a, stream);
-    for (auto fn : {w4ax_gemm_kernel<false, 0>, w4ax_gemm_kernel<true, 0>, w4ax_gemm_kernel<false, 1>,
-                    w4ax_gemm_kernel<false, 2>, w4ax_gemm_kernel<false, 0, true>}) {
+    for (auto fn : {w4ax_gemm_kernel<false, 0>, w4ax_gemm_kernel<true, 0>, w4ax_gemm_kernel<false, 2>,
+                    w4ax_gemm_kernel<false, 0, true>}) {
         const cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(fn), static_cast<int>(kSmemBytes));
         if (e != cudaSuccess) return e;
     }
@@ -798,12 +755,8 @@ cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& a, cudaStream_t st
     p.status = L.d_status;
     p.wmask = a.unsigned_w ? 0x0F0F0F0Fu : 0x87878787u;
     p.zero_kind = a.zero_kind;
-    p.a_zeros = static_cast<const uint16_t*>(a.a_zeros);
-    p.a_sums = a.a_sums;
-    p.w_sums = a.w_sums;
     p.ch_scales = static_cast<const uint16_t*>(a.ch_scales);
     p.grp_scales = a.grp_scales;
-    p.grp_zeros = a.grp_zeros;
     p.poll_limit = a.poll_limit != 0 ? a.poll_limit : dev::kMaxPolls;
     p.withhold = a.withhold;
     const bool partials = a.P != nullptr;
@@ -831,12 +784,12 @@ cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& a, cudaStream_t st
                                                     static_cast<size_t>(tiles) * p.splits * kPairM * kTileN * sizeof(float));
         }
     }
-    if (a.zero_kind == kZeroQuik && !partials) {
+    if (a.zero_kind != kZeroNone && !partials) {
         // the zero-point term for every output first, after the split-K part of the workspace
         uint8_t* zero_ws = static_cast<uint8_t*>(a.workspace) +
                            ((gemm_workspace_bytes(L, a.M, a.N, true) + 1023) & ~size_t(1023));
         bool maps_ok = true;
-        const cudaError_t e = launch_zero_term(L, a.a_zeros, a.w_sums, a.M, a.N, zero_ws, stream, &maps_ok);
+        const cudaError_t e = launch_zero_term(L, a, zero_ws, stream, &maps_ok);
         if (e != cudaSuccess) return e;
         if (!maps_ok) return cudaErrorInvalidValue;
         p.yz = reinterpret_cast<const float*>(zero_ws);
@@ -850,8 +803,6 @@ cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& a, cudaStream_t st
         w4ax_gemm_kernel<true, 0><<<grid, kThreads, kSmemBytes, stream>>>(p);
     else if (p.yz != nullptr)
         w4ax_gemm_kernel<false, 2><<<grid, kThreads, kSmemBytes, stream>>>(p);
-    else if (a.zero_kind != kZeroNone)
-        w4ax_gemm_kernel<false, 1><<<grid, kThreads, kSmemBytes, stream>>>(p);
     else
         w4ax_gemm_kernel<false, 0><<<grid, kThreads, kSmemBytes, stream>>>(p);
     return cudaGetLastError();

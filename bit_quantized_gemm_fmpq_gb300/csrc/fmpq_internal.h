@@ -86,13 +86,13 @@ struct GemmArgs {
     int64_t pm0, pmcount, pn0, pncount;
     // Quantization variants (the defaults are FMPQ: signed weight codes, per-block activation
     // scales, no zero-point term). Each block then adds x_zero[m] * w_zero[n] to the output:
-    //   kZeroQuik: x_zero = a_zeros[b][m] (fp16), w_zero = w_sums[b][n] (fp32); summed over the
-    //              blocks on the tensor cores first (launch_zero_term, in the workspace after the
-    //              split-K part) and added once per output
+    //   kZeroQuik: x_zero = a_zeros[b][m] (fp16), w_zero = w_sums[b][n] (fp32)
 
     //   kZeroQoq:  activation scale a_scales[m] for every block; weight scale
     //              ch_scales[n] * grp_scales[b][n]; x_zero = a_scales[m] * a_sums[b][m],
     //              w_zero = -ch_scales[n] * grp_scales[b][n] * grp_zeros[b][n]
+    // Outside the partial-sum export the term is summed over the blocks on the tensor cores first
+    // (launch_zero_term, in the workspace after the split-K part) and starts the accumulators.
     int zero_kind = kZeroNone;
     bool unsigned_w = false;          // weight codes are unsigned 4-bit (QoQ), not sign-magnitude
     const void* a_zeros = nullptr;
@@ -112,18 +112,19 @@ struct GemmArgs {
 // `variant`: a quantization variant (they always run the 2-SM kernel, whatever M).
 size_t gemm_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N, bool variant = false);
 size_t gemm_counter_bytes(const fmpq_layout& L, int64_t M, int64_t N, bool variant = false);
-// The QUIK variant's workspace: the split-K part (rounded up to 1 KB), then the zero-point term
-// (zero_term_bytes). Needed whatever the shape.
-size_t quik_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N);
+// A quantization variant's workspace: the split-K part (rounded up to 1 KB), then the zero-point
+// term (zero_term_bytes). Needed whatever the shape.
+size_t variant_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N);
 cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& args, cudaStream_t stream);
 
-// QUIK zero-point term on the tensor cores, for the variant GEMM to add once per output:
-// yz[m][n] = sum_b a_zeros[b][m] * w_sums[b][n] (FP32) at the start of ws, operands after it
-// (zero_term_bytes in all). tcgen05 kind::f16 on the zero points and a scaled two-term fp16 split
-// of w_sums (exact products).
+// The variants' zero-point term on the tensor cores, for the GEMM to start its accumulators
+// from: yz[m][n] = sum_b x_zero[b][m] * w_zero[b][n] (FP32) at the start of ws, its operands
+// after it (zero_term_bytes in all). tcgen05 kind::f16 on operands split so that every product
+// is exact (QUIK: the zero points and a scaled two-term split of w_sums; QoQ: the code sums in
+// two parts and s2 * z2, with s1 and the token scale applied to each output).
 size_t zero_term_bytes(const fmpq_layout& L, int64_t M, int64_t N);
-cudaError_t launch_zero_term(const fmpq_layout& L, const void* a_zeros, const float* w_sums, int64_t M, int64_t N,
-                             void* ws, cudaStream_t stream, bool* maps_ok);
+cudaError_t launch_zero_term(const fmpq_layout& L, const GemmArgs& args, void* ws, cudaStream_t stream,
+                             bool* maps_ok);
 
 // Outlier split, FP16 path: gather X[:, cols] into X_out, Y += X_out * W_out^T (tcgen05 kind::f16
 // tiles; device-side timeouts go to `status`). *maps_ok is false when a TMA tensor map cannot be

@@ -83,13 +83,14 @@ struct OTiles {
 };
 
 // kStore = false: the FP16 outlier product, merged into the fp16 Y with a TMA reduce-add.
-// kStore = true: the FP32 product, each column times colscale[n], stored to yz [m_rows][ldz]
-// (the QUIK zero-point term).
+// kStore = true: the FP32 product, times colscale[n] and (when given) rowscale[m], stored to
+// yz [m_rows][ldz] (the zero-point terms of the quantization variants).
 template <bool kStore>
 __global__ void __launch_bounds__(kOThreads, 1)
     outlier_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                         const __grid_constant__ CUtensorMap tm_y, int n_out, int n_cols, int mtiles, int64_t tiles,
-                        float* yz, int64_t ldz, int m_rows, const float* colscale, int32_t* status) {
+                        float* yz, int64_t ldz, int m_rows, const float* colscale, const float* rowscale,
+                        int32_t* status) {
     constexpr int kElems = kOChunk;   // K elements per 128-byte box row
     constexpr uint32_t kIdesc = dev::idesc_f16_f32(kOTileM, kOTileN);
     // W_out chunks kept resident across tiles (n_out <= 256, or 448 for the stored product) and
@@ -247,6 +248,7 @@ __global__ void __launch_bounds__(kOThreads, 1)
             if constexpr (kStore) {
                 // FP32 rows straight to yz: thread r writes 512 contiguous bytes of its row
                 const int row = mt * kOTileM + r;
+                const float rs = (rowscale != nullptr && row < m_rows) ? __ldg(rowscale + row) : 1.0f;
 #pragma unroll 1
                 for (int c = 0; c < 2 * nyb; ++c) {
                     uint32_t d0[16], d1[16];
@@ -262,8 +264,8 @@ __global__ void __launch_bounds__(kOThreads, 1)
                             if (col + 4 <= n_cols) {
                                 const float4 cs = __ldg(reinterpret_cast<const float4*>(colscale + col));
                                 *reinterpret_cast<float4*>(yz + static_cast<int64_t>(row) * ldz + col) =
-                                    make_float4(__uint_as_float(dg[0]) * cs.x, __uint_as_float(dg[1]) * cs.y,
-                                                __uint_as_float(dg[2]) * cs.z, __uint_as_float(dg[3]) * cs.w);
+                                    make_float4(__uint_as_float(dg[0]) * cs.x * rs, __uint_as_float(dg[1]) * cs.y * rs,
+                                                __uint_as_float(dg[2]) * cs.z * rs, __uint_as_float(dg[3]) * cs.w * rs);
                             }
                         }
                     }
@@ -373,6 +375,44 @@ __global__ void zero_operands_kernel(const uint16_t* a_zeros, const float* w_sum
     }
 }
 
+// QoQ zero-point term (QServe explainer, "W4A8逐组快速反量化": the group zero point is subtracted
+// after the multiplication). Per block b the term is -s1[n] s2[b][n] z2[b][n] * sx[m] sums[b][m];
+// s1[n] and sx[m] leave the sum over b, which is an integer sum T[m][n] = sum_b sums[b][m] c[b][n]
+// with c = s2 z2 <= 240. The operands split each code sum into 128 hi + lo (both exact in fp16,
+// as is c), so every product is exact in FP32:
+//   Zp[m][j] = 128 hi(sums[b][m]) for j = b < nbp, lo(sums[b][m]) for j = nbp + b
+//   Wp[n][j] = c[b][n] for both halves,  colscale[n] = -s1[n],  rowscale[m] = sx[m].
+__global__ void qoq_zero_operands_kernel(const int32_t* a_sums, const uint16_t* a_scales, const uint16_t* ch_scales,
+                                         const uint8_t* grp_scales, const uint8_t* grp_zeros, int64_t M, int64_t N,
+                                         int nb, int nbp, uint16_t* Zp, uint16_t* Wp, float* colscale,
+                                         float* rowscale) {
+    const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;   // warp-uniform
+    const int lane = threadIdx.x & 31;
+    const int kp = 2 * nbp;
+    if (r < M) {
+        uint16_t* row = Zp + r * kp;
+        for (int b = lane; b < nbp; b += 32) {
+            const int32_t v = b < nb ? a_sums[static_cast<int64_t>(b) * M + r] : 0;
+            const int32_t hi = v >> 7;   // floor(v / 128); lo = v - 128 hi in [0, 128)
+            row[b] = __half_as_ushort(__float2half_rn(static_cast<float>(hi * 128)));
+            row[nbp + b] = __half_as_ushort(__float2half_rn(static_cast<float>(v - hi * 128)));
+        }
+        if (lane == 0) rowscale[r] = __half2float(__ushort_as_half(a_scales[r]));
+    } else if (r < M + N) {
+        const int64_t n = r - M;
+        uint16_t* row = Wp + n * kp;
+        for (int b = lane; b < nbp; b += 32) {
+            const int64_t i = static_cast<int64_t>(b) * N + n;
+            const uint16_t c = b < nb ? __half_as_ushort(__float2half_rn(static_cast<float>(
+                                            static_cast<int>(grp_scales[i]) * static_cast<int>(grp_zeros[i]))))
+                                      : uint16_t(0);
+            row[b] = c;
+            row[nbp + b] = c;
+        }
+        if (lane == 0) colscale[n] = -__half2float(__ushort_as_half(ch_scales[n]));
+    }
+}
+
 int zero_nbp(int nb) { return (nb + 31) / 32 * 32; }
 size_t align1k(size_t x) { return (x + 1023) & ~size_t(1023); }
 
@@ -417,18 +457,20 @@ cudaError_t launch_outlier_gemm(const void* X, int64_t ldx, int64_t M, const int
     const int64_t grid = tiles < num_sms ? tiles : (num_sms > 0 ? num_sms : 1);
     outlier_gemm_kernel<false><<<static_cast<unsigned>(grid), kOThreads, kOSmemBytes, stream>>>(
         tm_x, tm_w, tm_y, n_out, static_cast<int>(N), static_cast<int>(mtiles), tiles, nullptr, 0,
-        static_cast<int>(M), nullptr, status);
+        static_cast<int>(M), nullptr, nullptr, status);
     return cudaGetLastError();
 }
 
 size_t zero_term_bytes(const fmpq_layout& L, int64_t M, int64_t N) {
     const size_t kp = 2 * static_cast<size_t>(zero_nbp(L.nb));
     return align1k(static_cast<size_t>(M) * N * 4) + align1k(static_cast<size_t>(M) * kp * 2) +
-           align1k(static_cast<size_t>(N) * kp * 2) + align1k(static_cast<size_t>(N) * 4);
+           align1k(static_cast<size_t>(N) * kp * 2) + align1k(static_cast<size_t>(N) * 4) +
+           align1k(static_cast<size_t>(M) * 4);
 }
 
-cudaError_t launch_zero_term(const fmpq_layout& L, const void* a_zeros, const float* w_sums, int64_t M, int64_t N,
-                             void* ws, cudaStream_t stream, bool* maps_ok) {
+cudaError_t launch_zero_term(const fmpq_layout& L, const GemmArgs& a, void* ws, cudaStream_t stream, bool* maps_ok) {
+    const int64_t M = a.M, N = a.N;
+    const bool qoq = a.zero_kind == kZeroQoq;
     *maps_ok = true;
     const int nbp = zero_nbp(L.nb), kp = 2 * nbp;
     uint8_t* base = static_cast<uint8_t*>(ws);
@@ -439,6 +481,8 @@ cudaError_t launch_zero_term(const fmpq_layout& L, const void* a_zeros, const fl
     uint16_t* wp = reinterpret_cast<uint16_t*>(base);
     base += align1k(static_cast<size_t>(N) * kp * 2);
     float* colscale = reinterpret_cast<float*>(base);
+    base += align1k(static_cast<size_t>(N) * 4);
+    float* rowscale = reinterpret_cast<float*>(base);
     const EncodeTiledFn enc = encode_tiled();
     CUtensorMap tm_x, tm_w;
     if (enc == nullptr || !make_map(enc, &tm_x, zp, kp, M, kp, kOTileM) || !make_map(enc, &tm_w, wp, kp, N, kp, kOTileN)) {
@@ -446,8 +490,13 @@ cudaError_t launch_zero_term(const fmpq_layout& L, const void* a_zeros, const fl
         return cudaSuccess;
     }
     const int64_t warps = M + N;
-    zero_operands_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, stream>>>(
-        static_cast<const uint16_t*>(a_zeros), w_sums, M, N, L.nb, nbp, zp, wp, colscale);
+    if (qoq)
+        qoq_zero_operands_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, stream>>>(
+            a.a_sums, static_cast<const uint16_t*>(a.a_scales), static_cast<const uint16_t*>(a.ch_scales),
+            a.grp_scales, a.grp_zeros, M, N, L.nb, nbp, zp, wp, colscale, rowscale);
+    else
+        zero_operands_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, stream>>>(
+            static_cast<const uint16_t*>(a.a_zeros), a.w_sums, M, N, L.nb, nbp, zp, wp, colscale);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     e = ensure_smem_limit(reinterpret_cast<const void*>(outlier_gemm_kernel<true>), static_cast<int>(kOSmemBytes));
@@ -456,7 +505,7 @@ cudaError_t launch_zero_term(const fmpq_layout& L, const void* a_zeros, const fl
     const int64_t grid = tiles < L.num_sms ? tiles : (L.num_sms > 0 ? L.num_sms : 1);
     outlier_gemm_kernel<true><<<static_cast<unsigned>(grid), kOThreads, kOSmemBytes, stream>>>(
         tm_x, tm_w, tm_x, kp, static_cast<int>(N), static_cast<int>(mtiles), tiles, yz, N, static_cast<int>(M),
-        colscale, L.d_status);
+        colscale, qoq ? rowscale : nullptr, L.d_status);
     return cudaGetLastError();
 }
 

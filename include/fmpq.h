@@ -322,10 +322,9 @@ FMPQ_API int32_t fmpq_outlier_blocks(int32_t K, double fraction);
 
 /* ---- Quantization variants the pages describe beside FMPQ ----
  * Both run on the same layouts, packed formats and 2-SM GEMM kernel (for every M), with a
- * zero-point term. Their workspace: the larger of the two variants' needs. QoQ needs the
- * split-K part only (as w4ax_gemm: 0 for shapes with enough tiles); QUIK needs it too, plus its
- * zero-point term (M*N*4 bytes and the term's operands) for every shape, so its workspace is
- * never empty. */
+ * zero-point term. The term is summed over the blocks on the tensor cores first, into the
+ * workspace, and starts the GEMM's accumulators. Their workspace (never 0; the same for both):
+ * w4ax_gemm's split-K part plus the term (M*N*4 bytes and the term's operands). */
 FMPQ_API size_t fmpq_variant_gemm_workspace_bytes(const fmpq_layout* layout, int64_t M, int64_t N);
 
 /* QUIK asymmetric activations (QUIK explainer, "反量化背后的数学": activations take a scale and a
@@ -392,7 +391,10 @@ FMPQ_API fmpq_status qoq_quantize(const fmpq_layout* layout, const void* X, int6
  *   Y[m][n] = fp16_rn( a_scales[m] * ch_scales[n] *
  *                      sum_b grp_scales[b][n] * ( P[m][n][b] - grp_zeros[b][n] * a_sums[b][m] ) ),
  * P the exact integer sums of the INT8 activation codes times the unsigned codes q4, FP32
- * accumulation. Shapes, alignment, workspace (fmpq_variant_gemm_workspace_bytes) as w4ax_gemm. */
+ * accumulation. The zero-point part, -a_scales[m] * ch_scales[n] * sum_b grp_scales[b][n] *
+ * grp_zeros[b][n] * a_sums[b][m], is summed first on the tensor cores (exact integer products)
+ * into the workspace and starts the accumulators. Shapes and alignment as w4ax_gemm; workspace:
+ * fmpq_variant_gemm_workspace_bytes (never 0), else FMPQ_ERR_WORKSPACE. */
 FMPQ_API fmpq_status qoq_gemm(const fmpq_layout* layout, const void* A_packed, const void* a_scales,
                               const int32_t* a_sums, const void* W_packed, const void* ch_scales,
                               const uint8_t* grp_scales, const uint8_t* grp_zeros, int64_t M, int64_t N, void* Y,
