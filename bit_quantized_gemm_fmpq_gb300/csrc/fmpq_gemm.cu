@@ -40,7 +40,7 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kPairM = 256;   // rows of a pair tile (128 per CTA)
 constexpr int kASlots = 8;    // activation plane slots (an INT4 block takes one, INT8 two)
-constexpr int kWStages = 6;   // packed weight half-tiles (bulk copies)
+constexpr int kWStages = 7;   // packed weight half-tiles (bulk copies)
 constexpr int kCvStages = 2;  // converted weight half-tiles
 constexpr int kScStages = 4;  // per-block scales staged for the epilogue
 constexpr int kBlk = 16;      // per-block readiness / release barriers (ring over blocks)
