@@ -27,7 +27,7 @@
 // waits for every plain load it has in flight.
 //
 // Warp roles (512 threads, one CTA per SM, persistent over units):
-//   warp 0       weight producer (four blocks of the CTA's 128 rows per copy)
+//   warp 0       weight producer (two blocks of the CTA's 128 rows per copy)
 //   warp 6       operand producer: activation planes and scales
 //   warps 1, 7   tcgen05 MMA issuers (blocks in turn)
 //   warps 2-5    converter group 0 (even blocks of a unit);  warps 12-15  group 1 (odd blocks)
@@ -48,7 +48,7 @@ constexpr int kSBlk = 16;      // per-block barriers (ring over blocks)
 constexpr int kSConvWarps = 4; // warps per converter group
 constexpr int kSEpiWarps = 4;
 constexpr uint32_t kSTmemCols = 512;
-constexpr int kSQuad = 4;         // blocks per weight copy
+constexpr int kSQuad = 2;         // blocks per weight copy
 constexpr int kSSc = 3;           // scale chunks staged
 
 // Accumulators of T columns in flight (TMEM holds 512 columns; at most 8 are used).
@@ -64,11 +64,11 @@ __host__ __device__ constexpr int a_planes() { return kT <= 32 ? 4 : 2; }
 template <int kT>
 __host__ __device__ constexpr int a_copies() { return b_slots<kT>() / a_planes<kT>(); }   // ring of copies
 
-// Packed weight stages (32 KB copies, four blocks each). Every weight byte comes from HBM once,
+// Packed weight stages (16 KB copies, two blocks each). Every weight byte comes from HBM once,
 // so the stream runs at (bytes in flight) / (HBM latency): the ring takes the shared memory
 // the activation slots leave, 96 KB in flight per SM.
 template <int kT>
-__host__ __device__ constexpr int w_stages() { return 3; }
+__host__ __device__ constexpr int w_stages() { return 6; }
 
 // Scale chunks: at most scale_chunk() blocks of a unit per chunk (the host may choose fewer,
 // SParams::sc_chunk); kSSc chunks are staged. Activation scales of a chunk: C rows of T (M a
@@ -83,7 +83,7 @@ template <int kT>
 struct __align__(1024) SSmem {
     uint8_t cvA[kSCvStages][128 * 128];          // E4M3 weight operand: 128 rows x 128 K
     uint8_t opB[b_slots<kT>()][kT * 128];        // activation code planes: T token rows x 128 K
-    uint8_t pkW[w_stages<kT>()][kSQuad * 128 * 64];   // packed codes of the CTA's 128 rows, four blocks
+    uint8_t pkW[w_stages<kT>()][kSQuad * 128 * 64];   // packed codes of the CTA's 128 rows, kSQuad blocks
     uint16_t swr[kSSc][scale_chunk<kT>()][128];       // weight scales of the CTA's 128 channels (fp16)
     uint16_t sxr[kSSc][sx_elems<kT>()];               // activation scales (fp16), see scale_chunk
     // a_full[c % a_copies]: activation copy c has landed.
@@ -388,8 +388,8 @@ __device__ __forceinline__ void s_mma_role(const SParams& p, SSmem<kT>& s, int l
 
 // ---------------------------------------------------------------- converters (warps 2-5, 12-15)
 // Group g converts the blocks i of each unit with i % 2 == g (packed codes -> 128B-swizzled
-// E4M3 tile, the same mapping as the main GEMM's converters; block i sits in quarter i % 4 of
-// the unit's weight copy i / 4).
+// E4M3 tile, the same mapping as the main GEMM's converters; block i sits in part i % kSQuad of
+// the unit's weight copy i / kSQuad).
 template <int kT>
 __device__ __forceinline__ void s_converter_role(const SParams& p, SSmem<kT>& s, int group, int ct, int lane,
                                                  volatile int* abort_flag) {
@@ -408,7 +408,7 @@ __device__ __forceinline__ void s_converter_role(const SParams& p, SSmem<kT>& s,
         const SUnit t = sunit_of(p, u);
         for (int i = group; i < t.n; i += 2) {
             const uint32_t bi = it + i;                 // the block's position in the CTA's sequence
-            const uint32_t wc = wbase + (i >> 2);       // its weight copy
+            const uint32_t wc = wbase + (i / kSQuad);   // its weight copy
             const int ws = wc % kSWStages, cs = bi % kSCvStages;
             ok = dev::mbar_wait(&s.w_full[ws], (wc / kSWStages) & 1, abort_flag);
             if (ok && bi >= static_cast<uint32_t>(kSCvStages)) {   // converted slot: MMAs of block bi - 4 done
@@ -417,7 +417,7 @@ __device__ __forceinline__ void s_converter_role(const SParams& p, SSmem<kT>& s,
             }
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
-            const uint8_t* src = s.pkW[ws] + (i & 3) * (128 * 64) + src0;
+            const uint8_t* src = s.pkW[ws] + (i % kSQuad) * (128 * 64) + src0;
             uint8_t* dst = s.cvA[cs];
             uint4 w[kPieces];
 #pragma unroll
@@ -432,14 +432,14 @@ __device__ __forceinline__ void s_converter_role(const SParams& p, SSmem<kT>& s,
             __syncwarp();
             if (lane == 0) {
                 dev::mbar_arrive(&s.w_empty[ws]);
-                // a unit's last copy may hold fewer than four of its blocks: arrive for the rest
+                // a unit's last copy may hold fewer than kSQuad of its blocks: arrive for the rest
                 if (i + 1 == t.n)
-                    for (int r = i & 3; r < 3; ++r) dev::mbar_arrive(&s.w_empty[ws]);
+                    for (int r = i % kSQuad; r < kSQuad - 1; ++r) dev::mbar_arrive(&s.w_empty[ws]);
                 dev::mbar_arrive(&s.blk_full[bi % kSBlk]);
             }
         }
         it += t.n;
-        wbase += (t.n + 3) / 4;
+        wbase += (t.n + kSQuad - 1) / kSQuad;
     }
     if (!ok && lane == 0) sfail(p, abort_flag);
 }
