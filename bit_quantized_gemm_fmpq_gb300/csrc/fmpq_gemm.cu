@@ -422,9 +422,9 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, uint32_
 // and all 256 columns, read with tcgen05.ld 16x256b: thread t holds rows t/4 and t/4 + 8 of
 // that slab and columns 8g + 2(t%4) + {0, 1}, g = 0..31 (four registers per 8 columns:
 // row0 col0, row0 col1, row1 col0, row1 col1).
-// kZ: the zero-point term of the quantization variants. 0 none; 2 summed over all blocks
-// beforehand (yz, launch_zero_term), the starting value of the accumulators.
-template <bool kPartials, int kZ>
+// kYz: the quantization variants' zero-point term, summed over all blocks beforehand (yz,
+// launch_zero_term), is the accumulators' starting value.
+template <bool kPartials, bool kYz>
 __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, uint32_t rank, int warp, int lane,
                                               uint32_t tmem, volatile int* abort_flag, uint32_t polls) {
     const int num_units = p.mtiles * p.ntiles * p.splits;
@@ -449,9 +449,9 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, uint32_t
             accA[g] = make_float2(0.f, 0.f);
             accB[g] = make_float2(0.f, 0.f);
         }
-        if constexpr (kZ == 2 && !kPartials) {
-            // QUIK: the accumulators start from the zero-point term summed over all blocks (one
-            // split of a split-K tile carries it); the producer brought these rows to the L2
+        if constexpr (kYz && !kPartials) {
+            // the accumulators start from the zero-point term summed over all blocks (one split of
+            // a split-K tile carries it); the converters brought these rows to the L2
             if (t.split == 0) {
 #pragma unroll
                 for (int g = 0; g < 32; ++g) {
@@ -597,7 +597,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, uint32_t
 
 // kTest: the failure-detection test instantiation (runtime poll bound, a withheld weight copy);
 // the others bound every wait by the compile-time dev::kMaxPolls.
-template <bool kPartials, int kZ, bool kTest = false>
+template <bool kPartials, bool kYz, bool kTest = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) w4ax_gemm_kernel(const Params p) {
     extern __shared__ uint8_t smem_raw[];
     Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -662,7 +662,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) w4ax_ge
         }
     } else {
         dev::setmaxnreg_inc<192>();
-        epilogue_role<kPartials, kZ>(p, s, rank, warp, lane, tmem, abort_flag, polls);
+        epilogue_role<kPartials, kYz>(p, s, rank, warp, lane, tmem, abort_flag, polls);
     }
 
     dev::tc_fence_before();
@@ -690,9 +690,9 @@ int max_pairs(const fmpq_layout& L) {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = sizeof(Smem) + 1024;
     int clusters = 0;
-    if (ensure_smem_limit(reinterpret_cast<const void*>(w4ax_gemm_kernel<false, 0>),
+    if (ensure_smem_limit(reinterpret_cast<const void*>(w4ax_gemm_kernel<false, false>),
                           static_cast<int>(sizeof(Smem) + 1024)) == cudaSuccess &&
-        cudaOccupancyMaxActiveClusters(&clusters, w4ax_gemm_kernel<false, 0>, &cfg) == cudaSuccess && clusters > 0 &&
+        cudaOccupancyMaxActiveClusters(&clusters, w4ax_gemm_kernel<false, false>, &cfg) == cudaSuccess && clusters > 0 &&
         clusters < pairs)
         pairs = clusters;
     cudaGetLastError();   // a failed query leaves no sticky error behind
@@ -735,8 +735,8 @@ size_t variant_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N) {
 cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& a, cudaStream_t stream) {
     const bool variant = a.zero_kind != kZeroNone || a.unsigned_w;
     if (!variant && gemm_small_path(a.M) && a.withhold < 0) return launch_gemm_small(L, a, stream);
-    for (auto fn : {w4ax_gemm_kernel<false, 0>, w4ax_gemm_kernel<true, 0>, w4ax_gemm_kernel<false, 2>,
-                    w4ax_gemm_kernel<false, 0, true>}) {
+    for (auto fn : {w4ax_gemm_kernel<false, false>, w4ax_gemm_kernel<true, false>, w4ax_gemm_kernel<false, true>,
+                    w4ax_gemm_kernel<false, false, true>}) {
         const cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(fn), static_cast<int>(kSmemBytes));
         if (e != cudaSuccess) return e;
     }
@@ -798,13 +798,13 @@ cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& a, cudaStream_t st
     const int pairs = static_cast<int>(units < max_pairs(L) ? units : max_pairs(L));
     const int grid = 2 * pairs;   // clusters of two CTAs (one pair per two SMs)
     if (a.withhold >= 0)
-        w4ax_gemm_kernel<false, 0, true><<<grid, kThreads, kSmemBytes, stream>>>(p);
+        w4ax_gemm_kernel<false, false, true><<<grid, kThreads, kSmemBytes, stream>>>(p);
     else if (partials)
-        w4ax_gemm_kernel<true, 0><<<grid, kThreads, kSmemBytes, stream>>>(p);
+        w4ax_gemm_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(p);
     else if (p.yz != nullptr)
-        w4ax_gemm_kernel<false, 2><<<grid, kThreads, kSmemBytes, stream>>>(p);
+        w4ax_gemm_kernel<false, true><<<grid, kThreads, kSmemBytes, stream>>>(p);
     else
-        w4ax_gemm_kernel<false, 0><<<grid, kThreads, kSmemBytes, stream>>>(p);
+        w4ax_gemm_kernel<false, false><<<grid, kThreads, kSmemBytes, stream>>>(p);
     return cudaGetLastError();
 }
 
