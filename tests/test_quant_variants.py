@@ -327,6 +327,19 @@ def test_variant_argument_errors(fmpq_gpu):
         fmpq_gpu.qoq_quantize(sel, X)                     # per-token scale over the whole row only
     mixed.close()
     sel.close()
+    # the variants' workspace holds their zero-point term: never empty, and required
+    import torch
+    asym = fmpq_gpu.Layout(K, np.arange(K, dtype=np.int32), np.zeros(2, np.uint8))
+    assert int(asym._lib.fmpq_variant_gemm_workspace_bytes(asym.handle, M, N)) > 0
+    A, sx, z = fmpq_gpu.fmpq_quantize_asym(asym, X)
+    Wp, sw = fmpq_gpu.w4_pack_weights(asym, to_dev(np.zeros((N, K), np.float16)))
+    wsum = fmpq_gpu.w4_weight_sums(asym, Wp, sw, N)
+    Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fmpq_gpu.FmpqError) as e:
+        fmpq_gpu.w4ax_gemm_asym(asym, A, sx, z, Wp, sw, wsum, M, N, Y, workspace=small)
+    assert e.value.code == 7                              # FMPQ_ERR_WORKSPACE
+    asym.close()
 
 
 def test_variant_samples_agree_with_whole_reference(oracle_mod):
