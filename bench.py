@@ -305,7 +305,7 @@ def run_sweep(args):
         sampler.start()
         q_ms = timed(lambda: fmpq.fmpq_quantize(layout, X, A, sx))
         g_ms = timed(lambda: fmpq.w4ax_gemm(layout, A, sx, Wp, sw, M, N, Y, workspace=ws))
-        graph_ms = quant_graph_ms = step_graph_ms = None
+        graph_ms = quant_graph_ms = step_graph_ms = step_graph_one_call_ms = None
         if M <= 128:
             copies = [Wp] + [Wp.clone() for _ in range(4)]   # 5 x packed W > L2
             reps = 20
@@ -333,6 +333,9 @@ def run_sweep(args):
             quant_graph_ms = graph_time(lambda r: fmpq.fmpq_quantize(layout, X, A, sx))
             # the decode step: quantize the token(s), then the GEMM
             step_graph_ms = graph_time(lambda r: (fmpq.fmpq_quantize(layout, X, A, sx), gemm(r)))
+            # the same step as one call: the GEMM's prologue and weight stream overlap the quantizer
+            step_graph_one_call_ms = graph_time(lambda r: fmpq.fmpq_quantize_gemm(
+                layout, X, copies[r % len(copies)], sw, N, A_packed=A, a_scales=sx, Y=Y, workspace=ws))
             del copies
         clocks = sampler.stop()
         if fmpq.fmpq_device_status(layout) != 0:
@@ -356,6 +359,7 @@ def run_sweep(args):
             "quant_ms": q_ms, "quant_gbs": qbytes / (q_ms * 1e-3) / 1e9,
             "quant_frac_hbm": qbytes / (q_ms * 1e-3) / 1e9 / hbm,
             "quant_graph_ms": quant_graph_ms, "step_graph_ms": step_graph_ms,
+            "step_graph_one_call_ms": step_graph_one_call_ms,
             "l2": "flushed before every timed launch (graphs: back-to-back launches, 5 rotating weight "
                   "copies, no flush)",
             "clocks": clocks,
@@ -631,8 +635,8 @@ def main():
         n_e2e = max(3, min(args.steps, 50))
 
         def step_on(Xk, Yk):
-            fmpq.fmpq_quantize(layout, Xk, A, sx, stream=stream)
-            fmpq.w4ax_gemm(layout, A, sx, Wp, sw, M, N, Yk, workspace=ws, stream=stream)
+            fmpq.fmpq_quantize_gemm(layout, Xk, Wp, sw, N, A_packed=A, a_scales=sx, Y=Yk, workspace=ws,
+                                    stream=stream)
 
         def pipeline(n):
             ev = lambda: torch.cuda.Event(enable_timing=False)

@@ -247,6 +247,39 @@ fmpq_status w4ax_gemm(const fmpq_layout* L, const void* A_packed, const void* a_
     return launched(fmpq::launch_gemm(*L, a, static_cast<cudaStream_t>(stream)));
 }
 
+fmpq_status fmpq_quantize_gemm(const fmpq_layout* L, const void* X, int64_t ldx, int64_t M, void* A_packed,
+                               void* a_scales, const void* W_packed, const void* w_scales, int64_t N, void* Y,
+                               int64_t ldy, void* workspace, size_t workspace_bytes, void* stream) {
+    // every argument of both steps is checked before anything is launched
+    if (L == nullptr || X == nullptr || A_packed == nullptr || a_scales == nullptr || W_packed == nullptr ||
+        w_scales == nullptr || Y == nullptr)
+        return FMPQ_ERR_INVALID_ARG;
+    if (M < 1 || M > INT32_MAX || ldx < L->K_in || N < 16 || N % 16 != 0 || N > INT32_MAX || ldy < N)
+        return FMPQ_ERR_UNSUPPORTED_SHAPE;
+    if (ldx % 8 != 0 || ldy % 8 != 0 || !aligned16(X) || !aligned16(A_packed) || !aligned16(a_scales) ||
+        !aligned16(W_packed) || !aligned16(w_scales) || !aligned16(Y))
+        return FMPQ_ERR_MISALIGNED;
+    const size_t need = fmpq::gemm_workspace_bytes(*L, M, N);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return FMPQ_ERR_WORKSPACE;
+    if (need > 0 && !aligned16(workspace)) return FMPQ_ERR_MISALIGNED;
+    if (fmpq_status st = check_device(L)) return st;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (fmpq_status st = launched(fmpq::launch_quantize(*L, X, ldx, M, A_packed, a_scales, s))) return st;
+    fmpq::GemmArgs a{};
+    a.A = A_packed;
+    a.a_scales = a_scales;
+    a.W = W_packed;
+    a.w_scales = w_scales;
+    a.M = M;
+    a.N = N;
+    a.Y = Y;
+    a.ldy = ldy;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    a.pdl = true;   // the quantizer just launched on this stream is the GEMM's only prerequisite
+    return launched(fmpq::launch_gemm(*L, a, s));
+}
+
 fmpq_status w4ax_gemm_partials(const fmpq_layout* L, const void* A_packed, const void* W_packed, int64_t M,
                                int64_t N, int64_t m0, int64_t mcount, int64_t n0, int64_t ncount, int32_t* P,
                                void* stream) {

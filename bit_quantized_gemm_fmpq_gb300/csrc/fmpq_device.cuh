@@ -183,6 +183,13 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, int x, int y, con
                  "r"(y), "r"(smem_u32(src))
                  : "memory");
 }
+// Programmatic dependent launch. launch_dependents: the grid launched after this one with the
+// programmatic-serialization attribute may start once every CTA of this grid has executed it
+// (or exited). wait: block until the grids this one depends on have completed and their memory
+// operations are visible (returns at once for a grid launched without that attribute).
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Bring bytes (a multiple of 16, 16-byte aligned address) of global memory into the L2 ahead of
 // use; nothing waits for it.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {

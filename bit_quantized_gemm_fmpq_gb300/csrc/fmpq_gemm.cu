@@ -200,6 +200,7 @@ __device__ __forceinline__ void activation_producer(const Params& p, Smem& s, ui
     for (int i = 0; i < kASlots; ++i) slot_block[i] = -1;
     bool ok = true;
     const int64_t plane_bytes = static_cast<int64_t>(p.M) * kBlock;
+    dev::pdl_wait();   // as the quantizer's programmatic dependent: its codes are complete after this
     for (int u = blockIdx.x >> 1; ok && u < num_units; u += gridDim.x >> 1) {
         const Unit t = unit_of(p, u);
         const int r0 = t.mt * kPairM + static_cast<int>(rank) * 128;
@@ -335,6 +336,7 @@ __device__ __forceinline__ void converter_role(const Params& p, Smem& s, uint32_
         }
     };
     prefetch_zero_term(t);
+    dev::pdl_wait();   // the activation scales come from the quantizer (see activation_producer)
     // this thread's entries of the block's scales: weight columns ct and ct + 128, activation
     // row ct, fetched one block ahead as raw values and converted when they are staged, so that
     // the loads' latency hides behind a block
@@ -803,7 +805,19 @@ cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& a, cudaStream_t st
         w4ax_gemm_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(p);
     else if (p.yz != nullptr)
         w4ax_gemm_kernel<false, true><<<grid, kThreads, kSmemBytes, stream>>>(p);
-    else
+    else if (a.pdl) {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, w4ax_gemm_kernel<false, false>, p);
+    } else
         w4ax_gemm_kernel<false, false><<<grid, kThreads, kSmemBytes, stream>>>(p);
     return cudaGetLastError();
 }

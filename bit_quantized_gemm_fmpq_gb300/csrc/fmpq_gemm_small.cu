@@ -238,6 +238,9 @@ __device__ __forceinline__ void s_operand_producer(const SParams& p, const CUten
     constexpr int kP = a_planes<kT>(), kC = a_copies<kT>();
     constexpr int kPShift = kP == 4 ? 2 : kP == 2 ? 1 : 0;
     if (lane != 0) return;   // one thread: no warp-wide steps on the per-block path
+    // launched as the quantizer's programmatic dependent: the codes and scales are complete
+    // only after this (the other roles need nothing the quantizer writes)
+    dev::pdl_wait();
     const int num_units = p.ntiles * p.splits;
     const int C = p.sc_chunk;
     const uint32_t sbytes = static_cast<uint32_t>(C) * 128 * 2 +
@@ -722,7 +725,7 @@ struct SMaps {
 };
 
 template <int kT>
-cudaError_t launch_small_t(const SParams& p, const SMaps& m, int ctas, cudaStream_t stream) {
+cudaError_t launch_small_t(const SParams& p, const SMaps& m, int ctas, cudaStream_t stream, bool pdl) {
     const void* fn = p.P != nullptr ? reinterpret_cast<const void*>(w4ax_gemm_small_kernel<kT, true>)
                                     : reinterpret_cast<const void*>(w4ax_gemm_small_kernel<kT, false>);
     const cudaError_t e = ensure_smem_limit(fn, static_cast<int>(small_smem_bytes<kT>()));
@@ -737,13 +740,15 @@ cudaError_t launch_small_t(const SParams& p, const SMaps& m, int ctas, cudaStrea
     cfg.blockDim = dim3(kSThreads);
     cfg.dynamicSmemBytes = small_smem_bytes<kT>();
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(p.splits);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, w4ax_gemm_small_kernel<kT, false>, p, m.w, m.a, m.sw, m.sx);
 }
 
@@ -846,10 +851,10 @@ cudaError_t launch_gemm_small(const fmpq_layout& L, const GemmArgs& a, cudaStrea
     const int maxc = small_max_ctas(L);
     const int ctas = static_cast<int>(units < maxc ? units : maxc);
     switch (T) {
-        case 16: return launch_small_t<16>(p, maps, ctas, stream);
-        case 32: return launch_small_t<32>(p, maps, ctas, stream);
-        case 64: return launch_small_t<64>(p, maps, ctas, stream);
-        default: return launch_small_t<64>(p, maps, ctas, stream);
+        case 16: return launch_small_t<16>(p, maps, ctas, stream, a.pdl);
+        case 32: return launch_small_t<32>(p, maps, ctas, stream, a.pdl);
+        case 64: return launch_small_t<64>(p, maps, ctas, stream, a.pdl);
+        default: return launch_small_t<64>(p, maps, ctas, stream, a.pdl);
     }
 }
 

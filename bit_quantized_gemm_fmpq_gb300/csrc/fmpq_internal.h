@@ -105,6 +105,10 @@ struct GemmArgs {
     // default bound) and the packed weight copy the first CTA withholds (-1: none)
     uint32_t poll_limit = 0;
     int withhold = -1;
+    // launched right after this library's quantizer as its programmatic dependent: the GEMM's
+    // prologue and weight stream start while the quantizer runs; the roles that read its codes
+    // and scales wait for its completion (griddepcontrol.wait)
+    bool pdl = false;
 };
 
 // Workspace of a split-K launch: FP32 partial tiles followed by the arrival counters

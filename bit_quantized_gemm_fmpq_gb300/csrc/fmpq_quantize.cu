@@ -430,6 +430,9 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // a GEMM launched as this grid's programmatic dependent may start its prologue and weight
+    // stream now; it waits for this grid's completion before reading the codes
+    dev::pdl_launch_dependents();
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             dev::mbar_init(&full[s], 1);
@@ -699,6 +702,7 @@ __global__ void __launch_bounds__(kTwo ? (kQWarpsMin + 1) * 32 : kQMaxThreads, k
 // Same code step as the row kernel, so the codes and scales are identical.
 // ---------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) quantize_direct_kernel(QuantParams p) {
+    dev::pdl_launch_dependents();   // as in quantize_kernel
     const int lane = threadIdx.x & 31;
     const bool upper = lane >= 16;
     const int sub = lane & 15;

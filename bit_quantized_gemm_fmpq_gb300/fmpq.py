@@ -60,6 +60,7 @@ SIGNATURES = {
     "fmpq_layout_create_select": (_I32, [_I32, _I32, _P, _P, ctypes.POINTER(_P)]),
     "fmpq_outlier_gemm_fp16": (_I32, [_P, _P, _I64, _I64, _P, _I32, _P, _I64, _I64, _P, _P, _I64, _P]),
     "fmpq_quantize_split": (_I32, [_P, _P, _I64, _I64, _P, _I32, _I32, _P, _P, _P, _P, _P]),
+    "fmpq_quantize_gemm": (_I32, [_P, _P, _I64, _I64, _P, _P, _P, _P, _I64, _P, _I64, _P, _I64, _P]),
     "fmpq_outlier_product_fp16": (_I32, [_P, _P, _I64, _I32, _P, _I64, _I64, _P, _I64, _P]),
     "fmpq_channel_absmax": (_I32, [_P, _I64, _I64, _I32, _P, _P]),
     "fmpq_plan_layout": (_I32, [_I32, _P, _I32, _P, _P]),
@@ -259,6 +260,27 @@ def w4ax_gemm(layout: Layout, A_packed, a_scales, W_packed, w_scales, M: int, N:
     _check("w4ax_gemm", layout._lib.w4ax_gemm(layout.handle, _ptr(A_packed), _ptr(a_scales), _ptr(W_packed),
                                                 _ptr(w_scales), M, N, _ptr(Y), Y.stride(0), _ptr(workspace),
                                                 ws_bytes, _stream(stream)))
+    return Y
+
+
+def fmpq_quantize_gemm(layout: Layout, X, W_packed, w_scales, N: int, A_packed=None, a_scales=None, Y=None,
+                       workspace=None, stream=None):
+    """fmpq_quantize then w4ax_gemm in one call (the GEMM's prologue and weight stream overlap the
+    quantizer). Returns Y (fp16 [M, N])."""
+    import torch
+    M = X.shape[0]
+    if A_packed is None:
+        A_packed = torch.empty(layout.packed_a_bytes(M), dtype=torch.uint8, device=X.device)
+    if a_scales is None:
+        a_scales = torch.empty((layout.nb, M), dtype=torch.float16, device=X.device)
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float16, device=X.device)
+    if workspace is None:
+        workspace = layout.workspace(M, N)
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    _check("fmpq_quantize_gemm", layout._lib.fmpq_quantize_gemm(
+        layout.handle, _ptr(X), X.stride(0), M, _ptr(A_packed), _ptr(a_scales), _ptr(W_packed), _ptr(w_scales), N,
+        _ptr(Y), Y.stride(0), _ptr(workspace), ws_bytes, _stream(stream)))
     return Y
 
 

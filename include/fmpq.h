@@ -207,6 +207,19 @@ FMPQ_API fmpq_status w4ax_gemm_noalloc(const fmpq_layout* layout, const void* A_
                                        const void* w_scales, int64_t M, int64_t N, void* Y,
                                        int64_t ldy, void* stream);
 
+/* fmpq_quantize followed by w4ax_gemm on the same stream, as one call: the stand-alone
+ * quantization node ahead of a GEMM whose input no fusable kernel produces, such as the
+ * attention output projection (QServe explainer, "运行时设计"). The GEMM is launched as the
+ * quantizer's programmatic dependent, so its prologue and weight stream run while the
+ * quantizer does, and it reads the codes and activation scales only once the quantizer has
+ * completed. Results, arguments (those of both calls; A_packed and a_scales are written,
+ * then read) and errors as the two calls; every argument is checked before either kernel is
+ * launched. */
+FMPQ_API fmpq_status fmpq_quantize_gemm(const fmpq_layout* layout, const void* X, int64_t ldx, int64_t M,
+                                        void* A_packed, void* a_scales, const void* W_packed,
+                                        const void* w_scales, int64_t N, void* Y, int64_t ldy,
+                                        void* workspace, size_t workspace_bytes, void* stream);
+
 /* Debug/test: the exact per-block integer partial sums P computed by the GEMM's own
  * tensor-core path, for the window [m0, m0+mcount) x [n0, n0+ncount):
  *   P int32 [mcount][ncount][K/128]. */
