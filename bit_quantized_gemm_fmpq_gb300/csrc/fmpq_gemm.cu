@@ -486,27 +486,37 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& s, uint32_t
                     const float2 sxa = make_float2(xa, xa);
                     const float2 sxb = make_float2(xb, xb);
                     const float4* swv = reinterpret_cast<const float4*>(sl.sw + tq * kSwStride);
-                    // 8 chunks of 32 columns; the TMEM load of chunk c+1 overlaps the math of c
-                    uint32_t d0[16], d1[16];
-                    dev::tmem_ld16x256b_x4(taddr, d0);
+                    auto math = [&](const uint32_t* d, int g0, int n) {
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const float4 f0 = swv[2 * c], f1 = swv[2 * c + 1];   // column pairs g = 4c..4c+3
-                        uint32_t (&dc)[16] = (c & 1) ? d1 : d0;
-                        uint32_t (&dn)[16] = (c & 1) ? d0 : d1;
-                        dev::tmem_ld_wait16(dc);
-                        if (c < 7) dev::tmem_ld16x256b_x4(taddr + (c + 1) * 32, dn);
-                        const float2 swp[4] = {make_float2(f0.x, f0.y), make_float2(f0.z, f0.w),
-                                               make_float2(f1.x, f1.y), make_float2(f1.z, f1.w)};
+                        for (int i = 0; i < n; i += 2) {
+                            const float4 f = swv[(g0 + i) >> 1];
+                            const float2 sp[2] = {make_float2(f.x, f.y), make_float2(f.z, f.w)};
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int g = 4 * c + i;
-                            const float2 ca = dev::fmul2(swp[i], sxa);
-                            const float2 cb = dev::fmul2(swp[i], sxb);
-                            accA[g] = dev::ffma2(make_float2(__uint_as_float(dc[4 * i]), __uint_as_float(dc[4 * i + 1])), ca, accA[g]);
-                            accB[g] = dev::ffma2(make_float2(__uint_as_float(dc[4 * i + 2]), __uint_as_float(dc[4 * i + 3])), cb, accB[g]);
+                            for (int j = 0; j < 2; ++j) {
+                                const int g = g0 + i + j, k = 4 * (i + j);
+                                const float2 ca = dev::fmul2(sp[j], sxa);
+                                const float2 cb = dev::fmul2(sp[j], sxb);
+                                accA[g] = dev::ffma2(make_float2(__uint_as_float(d[k]), __uint_as_float(d[k + 1])), ca, accA[g]);
+                                accB[g] = dev::ffma2(make_float2(__uint_as_float(d[k + 2]), __uint_as_float(d[k + 3])), cb, accB[g]);
+                            }
                         }
-                    }
+                    };
+                    // 4 chunks of 64 columns; the TMEM load of the next chunk is in flight during the
+                    // math of the current one (a wait covers every load issued before it, so
+                    // larger chunks, not more loads, are what cut the round trips)
+                    uint32_t dA[32], dB[32];
+                    dev::tmem_ld16x256b_x8(taddr, dA);
+                    dev::tmem_ld_wait32(dA);
+                    dev::tmem_ld16x256b_x8(taddr + 64, dB);
+                    math(dA, 0, 8);
+                    dev::tmem_ld_wait32(dB);
+                    dev::tmem_ld16x256b_x8(taddr + 128, dA);
+                    math(dB, 8, 8);
+                    dev::tmem_ld_wait32(dA);
+                    dev::tmem_ld16x256b_x8(taddr + 192, dB);
+                    math(dA, 16, 8);
+                    dev::tmem_ld_wait32(dB);
+                    math(dB, 24, 8);
                 } else {
                     // export exact partial sums of the requested window
 #pragma unroll 1
@@ -652,7 +662,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) w4ax_ge
     const int withhold = kTest ? p.withhold : -1;
 
     if (warp < 8) {
-        dev::setmaxnreg_dec<64>();
+        dev::setmaxnreg_dec<56>();
         if (warp == 0) {
             weight_producer(p, s, rank, lane, abort_flag, polls, withhold);
         } else if (warp == 1) {
@@ -663,7 +673,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) w4ax_ge
             activation_producer(p, s, rank, lane, abort_flag, polls);
         }
     } else {
-        dev::setmaxnreg_inc<192>();
+        dev::setmaxnreg_inc<200>();
         epilogue_role<kPartials, kYz>(p, s, rank, warp, lane, tmem, abort_flag, polls);
     }
 
