@@ -88,3 +88,38 @@ def test_argument_errors(fmpq_mod):
     torch.cuda.synchronize()
     assert int(A.count_nonzero()) == 0 and int(sx.count_nonzero()) == 0
     layout.close()
+
+
+@pytest.mark.parametrize("M", [16, 256])
+def test_inside_cuda_graph(fmpq_mod, M):
+    """Captured in a CUDA graph (the programmatic dependency becomes a graph edge) and replayed
+    with a new input: the same Y as the two separate calls on that input."""
+    import torch
+    w = wl.synthetic(M, 1024, 2048, n8=2, seed=40 + M)
+    layout = fmpq_mod.Layout(w.K, w.perm, w.mask)
+    Wp, sw = fmpq_mod.w4_pack_weights(layout, to_dev(w.W))
+    X = to_dev(w.X)
+    A = torch.empty(layout.packed_a_bytes(M), dtype=torch.uint8, device="cuda")
+    sx = torch.empty((layout.nb, M), dtype=torch.float16, device="cuda")
+    Y = torch.empty((M, w.N), dtype=torch.float16, device="cuda")
+    ws = layout.workspace(M, w.N)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        fmpq_mod.fmpq_quantize_gemm(layout, X, Wp, sw, w.N, A_packed=A, a_scales=sx, Y=Y, workspace=ws, stream=s)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(3):
+                fmpq_mod.fmpq_quantize_gemm(layout, X, Wp, sw, w.N, A_packed=A, a_scales=sx, Y=Y, workspace=ws,
+                                            stream=s)
+    torch.cuda.synchronize()
+    X.copy_(to_dev(wl.synthetic(M, 1024, 2048, n8=2, seed=41 + M).X))
+    g.replay()
+    torch.cuda.synchronize()
+    A2, sx2 = fmpq_mod.fmpq_quantize(layout, X)
+    Yref = fmpq_mod.w4ax_gemm(layout, A2, sx2, Wp, sw, M, w.N)
+    torch.cuda.synchronize()
+    assert torch.equal(Y.view(torch.int16), Yref.view(torch.int16))
+    assert fmpq_mod.fmpq_device_status(layout) == 0
+    del g
+    layout.close()
