@@ -50,6 +50,7 @@ constexpr int kSEpiWarps = 4;
 constexpr uint32_t kSTmemCols = 512;
 constexpr int kSQuad = 2;         // blocks per weight copy
 constexpr int kSSc = 3;           // scale chunks staged
+constexpr int kSIssuers = 2;      // MMA issuer warps, taking the blocks in turn
 
 // Accumulators of T columns in flight (TMEM holds 512 columns; at most 8 are used).
 template <int kT>
@@ -247,9 +248,14 @@ __device__ __forceinline__ void s_operand_producer(const SParams& p, const CUten
                             static_cast<uint32_t>(p.sx_rows ? C * kT * 2 : p.sx_box * 2);
     uint32_t g = 0, it = 0, k = 0;       // activation copies, blocks, scale chunks
     int ks = 0, kpar = 1;                // scale ring position and the parity its empty barrier waits for
-    int32_t last_use[kC];                // per activation ring position: its copy's last reader
+    // Per issuer and activation ring position: the last block of that issuer reading the copy
+    // the position holds. The two issuers take alternate blocks and each commit covers only its
+    // own MMAs, so a later block of one issuer can finish before an earlier block of the other:
+    // a position is free once the last reader of each issuer is done (an issuer's blocks finish
+    // in the order it issued them).
+    int32_t last_even[kC], last_odd[kC];
 #pragma unroll
-    for (int j = 0; j < kC; ++j) last_use[j] = -1;
+    for (int j = 0; j < kC; ++j) last_even[j] = last_odd[j] = -1;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
         const SUnit t = sunit_of(p, u);
@@ -283,12 +289,18 @@ __device__ __forceinline__ void s_operand_producer(const SParams& p, const CUten
             q += planes;
             while (g <= need) {
                 const int pos = static_cast<int>(g % kC);
-                int32_t last = -1;
+                int32_t le = -1, lo = -1;
 #pragma unroll
                 for (int j = 0; j < kC; ++j)
-                    if (j == pos) last = last_use[j];
-                if (last >= 0)
-                    ok = dev::mbar_wait(&s.blk_empty[last % kSBlk], (static_cast<uint32_t>(last) / kSBlk) & 1, abort_flag);
+                    if (j == pos) {
+                        le = last_even[j];
+                        lo = last_odd[j];
+                        last_even[j] = last_odd[j] = -1;   // the new copy's readers register below
+                    }
+                if (le >= 0)
+                    ok = dev::mbar_wait(&s.blk_empty[le % kSBlk], (static_cast<uint32_t>(le) / kSBlk) & 1, abort_flag);
+                if (ok && lo >= 0)
+                    ok = dev::mbar_wait(&s.blk_empty[lo % kSBlk], (static_cast<uint32_t>(lo) / kSBlk) & 1, abort_flag);
                 if (!ok) break;
                 dev::mbar_arrive_expect_tx(&s.a_full[pos], kP * kT * 128);
                 // {byte, token row, plane}
@@ -296,11 +308,15 @@ __device__ __forceinline__ void s_operand_producer(const SParams& p, const CUten
                 ++g;
             }
             if (!ok) break;
-            {   // block it is now the last reader of its copies (first, and need if another)
+            {   // block it is now its issuer's last reader of its copies (first, and need if another)
                 const int pf = static_cast<int>(first % kC), pn = static_cast<int>(need % kC);
+                const bool odd = (it % kSIssuers) != 0;
 #pragma unroll
                 for (int j = 0; j < kC; ++j)
-                    if (j == pf || j == pn) last_use[j] = static_cast<int32_t>(it);
+                    if (j == pf || j == pn) {
+                        if (odd) last_odd[j] = static_cast<int32_t>(it);
+                        else last_even[j] = static_cast<int32_t>(it);
+                    }
             }
         }
     }
@@ -321,8 +337,7 @@ __device__ __forceinline__ void s_operand_producer(const SParams& p, const CUten
 // same copy arithmetic as the producer), then 4 MMAs (K = 32 each) per plane into accumulator
 // it % kAcc. Checking a block's barriers and issuing its MMAs is a chain of several hundred
 // cycles of instruction latency, so kSIssuers issuers take the blocks in turn (`par`): each
-// commits only the MMAs it issued, and every block has its own accumulator.
-constexpr int kSIssuers = 2;
+// commits only the MMAs it issued, and every block has its own accumulator (kSIssuers).
 
 template <int kT>
 __device__ __forceinline__ void s_mma_role(const SParams& p, SSmem<kT>& s, int lane, uint32_t tmem, int par,

@@ -230,3 +230,43 @@ def test_scale_every_fp16_absmax(fmpq_mod, oracle_mod):
     assert np.array_equal(A.cpu().numpy(), A_ref)
     assert fmpq_mod.fmpq_device_status(layout) == 0
     layout.close()
+
+
+@pytest.mark.parametrize("M", [16, 32, 64])
+@pytest.mark.parametrize("one_call", [False, True])
+def test_back_to_back_steps(fmpq_mod, M, one_call):
+    """Few-token GEMM (K = N = 8192) in 20 back-to-back steps, each with its own Y, captured in a
+    CUDA graph and replayed 100 times: every step's Y is bit-identical to a single eager call.
+    The activation copies' slots are refilled only after every block reading them is done,
+    including blocks of the other MMA issuer that finish after a later block; a refill that
+    waited for the last reader alone corrupted ~1% of the steps at 64 tokens."""
+    import torch
+    w = wl.decode(M)
+    layout = fmpq_mod.Layout(w.K, w.perm, w.mask)
+    X = to_dev(w.X)
+    Wp, sw = fmpq_mod.w4_pack_weights(layout, to_dev(w.W))
+    A0, sx0 = fmpq_mod.fmpq_quantize(layout, X)
+    Yref = fmpq_mod.w4ax_gemm(layout, A0, sx0, Wp, sw, M, w.N)
+    Wc = [Wp] + [Wp.clone() for _ in range(4)]
+    A, sx = torch.empty_like(A0), torch.empty_like(sx0)
+    Ys = [torch.empty_like(Yref) for _ in range(20)]
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for r in range(20):
+            if one_call:
+                fmpq_mod.fmpq_quantize_gemm(layout, X, Wc[r % 5], sw, w.N, A_packed=A, a_scales=sx, Y=Ys[r])
+            else:
+                fmpq_mod.fmpq_quantize(layout, X, A, sx)
+                fmpq_mod.w4ax_gemm(layout, A, sx, Wc[r % 5], sw, M, w.N, Ys[r])
+    bad = 0
+    for _ in range(100):
+        for Y in Ys:
+            Y.fill_(1.0)
+        g.replay()
+        torch.cuda.synchronize()
+        bad += sum(0 if torch.equal(Y.view(torch.int16), Yref.view(torch.int16)) else 1 for Y in Ys)
+    assert bad == 0, f"{bad} of 2000 steps differ"
+    assert fmpq_mod.fmpq_device_status(layout) == 0
+    del g
+    layout.close()
