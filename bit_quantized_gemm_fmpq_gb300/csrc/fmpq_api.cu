@@ -311,8 +311,8 @@ fmpq_status w4ax_gemm_fault_test(const fmpq_layout* L, const void* A_packed, con
     if (L == nullptr || A_packed == nullptr || a_scales == nullptr || W_packed == nullptr || w_scales == nullptr ||
         Y == nullptr)
         return FMPQ_ERR_INVALID_ARG;
-    if (M <= 128 || M > INT32_MAX || N < 16 || N % 16 != 0 || N > INT32_MAX || ldy < N)
-        return FMPQ_ERR_UNSUPPORTED_SHAPE;   // the few-token kernel has no such test hook
+    if (M < 1 || M > INT32_MAX || N < 16 || N % 16 != 0 || N > INT32_MAX || ldy < N)
+        return FMPQ_ERR_UNSUPPORTED_SHAPE;
     if (withhold_copy < 0 || withhold_copy >= L->nb || poll_limit < 1024) return FMPQ_ERR_INVALID_ARG;
     if (ldy % 8 != 0 || !aligned16(A_packed) || !aligned16(a_scales) || !aligned16(W_packed) ||
         !aligned16(w_scales) || !aligned16(Y))

@@ -746,7 +746,7 @@ size_t variant_workspace_bytes(const fmpq_layout& L, int64_t M, int64_t N) {
 
 cudaError_t launch_gemm(const fmpq_layout& L, const GemmArgs& a, cudaStream_t stream) {
     const bool variant = a.zero_kind != kZeroNone || a.unsigned_w;
-    if (!variant && gemm_small_path(a.M) && a.withhold < 0) return launch_gemm_small(L, a, stream);
+    if (!variant && gemm_small_path(a.M)) return launch_gemm_small(L, a, stream);
     for (auto fn : {w4ax_gemm_kernel<false, false>, w4ax_gemm_kernel<true, false>, w4ax_gemm_kernel<false, true>,
                     w4ax_gemm_kernel<false, false, true>}) {
         const cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(fn), static_cast<int>(kSmemBytes));

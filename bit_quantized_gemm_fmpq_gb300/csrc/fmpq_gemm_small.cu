@@ -115,6 +115,8 @@ struct SParams {
     int M, N, nb;
     uint32_t mask_bits[kMaxBlocks / 32];   // INT8 blocks (bit b % 32 of word b / 32)
     int32_t* status;
+    uint32_t polls;        // bound of every barrier wait (a failure-detection test lowers it)
+    int withhold;          // packed weight copy the first CTA withholds (-1: none; the test hook)
     int ntiles;            // 128-channel output tiles
     int splits;            // K splits per tile (1 = none)
     // partial-sum export (debug): P[m - pm0][n - pn0][b] for the window, instead of Y
@@ -203,7 +205,7 @@ __device__ __forceinline__ int spoff(const uint32_t* mw, int b) {
 
 template <int kT>
 __device__ __forceinline__ void s_weight_producer(const SParams& p, const CUtensorMap* tmw, SSmem<kT>& s, int lane,
-                                                  volatile int* abort_flag) {
+                                                  volatile int* abort_flag, uint32_t polls, int withhold) {
     constexpr int kSWStages = w_stages<kT>();
     if (lane != 0) return;   // one thread: no warp-wide steps on the per-copy path
     const int num_units = p.ntiles * p.splits;
@@ -213,11 +215,15 @@ __device__ __forceinline__ void s_weight_producer(const SParams& p, const CUtens
     for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
         const SUnit t = sunit_of(p, u);
         for (int i = 0; i < t.n; i += kSQuad) {
-            ok = dev::mbar_wait(&s.w_empty[ws], wpar, abort_flag);
+            ok = dev::mbar_wait(&s.w_empty[ws], wpar, abort_flag, polls);
             if (!ok) break;
-            dev::mbar_arrive_expect_tx(&s.w_full[ws], kSQuad * 128 * 64);
-            // {byte, 256-byte line, half of the 256-row group, group * nb + block}
-            dev::tma_load_4d(s.pkW[ws], tmw, 0, 0, t.nt & 1, (t.nt >> 1) * p.nb + t.block(i), &s.w_full[ws]);
+            // (a failure-detection test withholds one copy of the first CTA: nothing is issued,
+            // so the converters' wait on it runs out; the drain below skips it)
+            if (!(blockIdx.x == 0 && static_cast<int>(wc) == withhold)) {
+                dev::mbar_arrive_expect_tx(&s.w_full[ws], kSQuad * 128 * 64);
+                // {byte, 256-byte line, half of the 256-row group, group * nb + block}
+                dev::tma_load_4d(s.pkW[ws], tmw, 0, 0, t.nt & 1, (t.nt >> 1) * p.nb + t.block(i), &s.w_full[ws]);
+            }
             ++wc;
             if (++ws == kSWStages) {
                 ws = 0;
@@ -228,14 +234,15 @@ __device__ __forceinline__ void s_weight_producer(const SParams& p, const CUtens
     if (!ok) sfail(p, abort_flag);
     for (uint32_t j = 0; j < static_cast<uint32_t>(kSWStages) && j < wc; ++j) {   // drain (copy bytes only)
         const uint32_t c = wc - 1 - j;
-        dev::mbar_wait(&s.w_full[c % kSWStages], (c / kSWStages) & 1, nullptr);
+        if (blockIdx.x == 0 && static_cast<int>(c) == withhold) continue;
+        dev::mbar_wait(&s.w_full[c % kSWStages], (c / kSWStages) & 1, nullptr, polls);
     }
 }
 
 template <int kT>
 __device__ __forceinline__ void s_operand_producer(const SParams& p, const CUtensorMap* tma, const CUtensorMap* tmsw,
                                                    const CUtensorMap* tmsx, SSmem<kT>& s, int lane,
-                                                   volatile int* abort_flag) {
+                                                   volatile int* abort_flag, uint32_t polls) {
     constexpr int kP = a_planes<kT>(), kC = a_copies<kT>();
     constexpr int kPShift = kP == 4 ? 2 : kP == 2 ? 1 : 0;
     if (lane != 0) return;   // one thread: no warp-wide steps on the per-block path
@@ -268,7 +275,7 @@ __device__ __forceinline__ void s_operand_producer(const SParams& p, const CUten
             const int b = t.block(i);
             if (sc_left == 0) {
                 sc_left = C;
-                ok = dev::mbar_wait(&s.scl_empty[ks], kpar, abort_flag);
+                ok = dev::mbar_wait(&s.scl_empty[ks], kpar, abort_flag, polls);
                 if (!ok) break;
                 dev::mbar_arrive_expect_tx(&s.scl_full[ks], sbytes);
                 dev::tma_load_2d(&s.swr[ks][0][0], tmsw, t.nt * kSTile, b, &s.scl_full[ks]);
@@ -298,9 +305,9 @@ __device__ __forceinline__ void s_operand_producer(const SParams& p, const CUten
                         last_even[j] = last_odd[j] = -1;   // the new copy's readers register below
                     }
                 if (le >= 0)
-                    ok = dev::mbar_wait(&s.blk_empty[le % kSBlk], (static_cast<uint32_t>(le) / kSBlk) & 1, abort_flag);
+                    ok = dev::mbar_wait(&s.blk_empty[le % kSBlk], (static_cast<uint32_t>(le) / kSBlk) & 1, abort_flag, polls);
                 if (ok && lo >= 0)
-                    ok = dev::mbar_wait(&s.blk_empty[lo % kSBlk], (static_cast<uint32_t>(lo) / kSBlk) & 1, abort_flag);
+                    ok = dev::mbar_wait(&s.blk_empty[lo % kSBlk], (static_cast<uint32_t>(lo) / kSBlk) & 1, abort_flag, polls);
                 if (!ok) break;
                 dev::mbar_arrive_expect_tx(&s.a_full[pos], kP * kT * 128);
                 // {byte, token row, plane}
@@ -324,11 +331,11 @@ __device__ __forceinline__ void s_operand_producer(const SParams& p, const CUten
     // drain copies in flight (their barriers complete on copy bytes only)
     for (uint32_t j = 0; j < static_cast<uint32_t>(kC) && j < g; ++j) {
         const uint32_t c = g - 1 - j;
-        dev::mbar_wait(&s.a_full[c % kC], (c / kC) & 1, nullptr);
+        dev::mbar_wait(&s.a_full[c % kC], (c / kC) & 1, nullptr, polls);
     }
     for (uint32_t j = 0; j < static_cast<uint32_t>(kSSc) && j < k; ++j) {
         const uint32_t c = k - 1 - j;
-        dev::mbar_wait(&s.scl_full[c % kSSc], (c / kSSc) & 1, nullptr);
+        dev::mbar_wait(&s.scl_full[c % kSSc], (c / kSSc) & 1, nullptr, polls);
     }
 }
 
@@ -341,7 +348,7 @@ __device__ __forceinline__ void s_operand_producer(const SParams& p, const CUten
 
 template <int kT>
 __device__ __forceinline__ void s_mma_role(const SParams& p, SSmem<kT>& s, int lane, uint32_t tmem, int par,
-                                           volatile int* abort_flag) {
+                                           volatile int* abort_flag, uint32_t polls) {
     constexpr int kAcc = acc_slots<kT>();
     constexpr int kP = a_planes<kT>(), kC = a_copies<kT>();
     constexpr uint32_t kIdesc = dev::idesc_e4m3_f32(128, kT);
@@ -370,9 +377,9 @@ __device__ __forceinline__ void s_mma_role(const SParams& p, SSmem<kT>& s, int l
             }
             const uint32_t c0 = g0 + static_cast<uint32_t>(q >> kPShift);
             const uint32_t c1 = g0 + static_cast<uint32_t>((q + planes - 1) >> kPShift);
-            ok = dev::mbar_wait(&s.blk_full[it % kSBlk], (it / kSBlk) & 1, abort_flag);
-            if (ok && static_cast<int64_t>(c0) > waited) ok = dev::mbar_wait(&s.a_full[c0 % kC], (c0 / kC) & 1, abort_flag);
-            if (ok && c1 != c0) ok = dev::mbar_wait(&s.a_full[c1 % kC], (c1 / kC) & 1, abort_flag);
+            ok = dev::mbar_wait(&s.blk_full[it % kSBlk], (it / kSBlk) & 1, abort_flag, polls);
+            if (ok && static_cast<int64_t>(c0) > waited) ok = dev::mbar_wait(&s.a_full[c0 % kC], (c0 / kC) & 1, abort_flag, polls);
+            if (ok && c1 != c0) ok = dev::mbar_wait(&s.a_full[c1 % kC], (c1 / kC) & 1, abort_flag, polls);
             waited = c1;
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
@@ -399,7 +406,7 @@ __device__ __forceinline__ void s_mma_role(const SParams& p, SSmem<kT>& s, int l
     if (!ok && lane == 0) sfail(p, abort_flag);
     if (lane == 0) {
         dev::mma_commit(&s.mma_done[par]);   // every MMA issued finishes before TMEM is released
-        dev::mbar_wait(&s.mma_done[par], 0, nullptr);
+        dev::mbar_wait(&s.mma_done[par], 0, nullptr, polls);
     }
     __syncwarp();
 }
@@ -410,7 +417,7 @@ __device__ __forceinline__ void s_mma_role(const SParams& p, SSmem<kT>& s, int l
 // the unit's weight copy i / kSQuad).
 template <int kT>
 __device__ __forceinline__ void s_converter_role(const SParams& p, SSmem<kT>& s, int group, int ct, int lane,
-                                                 volatile int* abort_flag) {
+                                                 volatile int* abort_flag, uint32_t polls) {
     const int num_units = p.ntiles * p.splits;
     const int r0 = ct >> 2, c4 = ct & 3;
     const uint32_t phase = static_cast<uint32_t>(r0 & 7);
@@ -428,10 +435,10 @@ __device__ __forceinline__ void s_converter_role(const SParams& p, SSmem<kT>& s,
             const uint32_t bi = it + i;                 // the block's position in the CTA's sequence
             const uint32_t wc = wbase + (i / kSQuad);   // its weight copy
             const int ws = wc % kSWStages, cs = bi % kSCvStages;
-            ok = dev::mbar_wait(&s.w_full[ws], (wc / kSWStages) & 1, abort_flag);
+            ok = dev::mbar_wait(&s.w_full[ws], (wc / kSWStages) & 1, abort_flag, polls);
             if (ok && bi >= static_cast<uint32_t>(kSCvStages)) {   // converted slot: MMAs of block bi - 4 done
                 const uint32_t prev = bi - kSCvStages;
-                ok = dev::mbar_wait(&s.blk_empty[prev % kSBlk], (prev / kSBlk) & 1, abort_flag);
+                ok = dev::mbar_wait(&s.blk_empty[prev % kSBlk], (prev / kSBlk) & 1, abort_flag, polls);
             }
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
@@ -468,7 +475,7 @@ __device__ __forceinline__ void s_converter_role(const SParams& p, SSmem<kT>& s,
 // time, the next load in flight during the math of the current one).
 template <int kT, bool kPartials>
 __device__ __forceinline__ void s_epilogue_role(const SParams& p, SSmem<kT>& s, int q, int lane, uint32_t tmem,
-                                                volatile int* abort_flag) {
+                                                volatile int* abort_flag, uint32_t polls) {
     constexpr int kAcc = acc_slots<kT>();
     constexpr int kChunks = kT / 16;
     const int C = p.sc_chunk;
@@ -492,7 +499,7 @@ __device__ __forceinline__ void s_epilogue_role(const SParams& p, SSmem<kT>& s, 
             const int slot = static_cast<int>(ck % kSSc);
             if (ok && jr == 0) {
                 // a new scale chunk: this warp's FP32 copy of its activation scales (rows of T)
-                ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&s.scl_full[slot], (ck / kSSc) & 1, abort_flag));
+                ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&s.scl_full[slot], (ck / kSSc) & 1, abort_flag, polls));
                 if (ok && !kPartials) {
                     const int x0 = ((t.b0 + i) * p.M) & ~7;
                     for (int e = lane; e < C * kT; e += 32) {
@@ -507,7 +514,7 @@ __device__ __forceinline__ void s_epilogue_role(const SParams& p, SSmem<kT>& s, 
                     __syncwarp();
                 }
             }
-            if (ok) ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&s.blk_empty[v % kSBlk], (v / kSBlk) & 1, abort_flag));
+            if (ok) ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait(&s.blk_empty[v % kSBlk], (v / kSBlk) & 1, abort_flag, polls));
             if (ok && kPartials) {
                 // export the exact partial sums of block t.block(i) for the window: column j of
                 // the accumulator is token j, P = D * 2^18 (operand encoding)
@@ -588,7 +595,7 @@ __device__ __forceinline__ void s_epilogue_role(const SParams& p, SSmem<kT>& s, 
             if (t.split == 0) {
                 if (et == 0)
                     for (int r = 1; r < p.splits; ++r) dev::mbar_arrive_remote_release(dev::mapa(&s.red_ready, r));
-                ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait_cluster(&s.red_full, 0));
+                ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait_cluster(&s.red_full, 0, polls));
                 if (ok) {
                     for (int r = 1; r < p.splits; ++r) {
                         const float4* o = reinterpret_cast<const float4*>(recv + (static_cast<int64_t>(r - 1) * kSTile + lrow) * kT);
@@ -604,7 +611,7 @@ __device__ __forceinline__ void s_epilogue_role(const SParams& p, SSmem<kT>& s, 
                     store();
                 }
             } else {
-                ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait_cluster(&s.red_ready, 0));
+                ok = __all_sync(0xFFFFFFFFu, dev::mbar_wait_cluster(&s.red_ready, 0, polls));
                 if (ok) {
                     const uint32_t dst = dev::mapa(recv + (static_cast<int64_t>(t.split - 1) * kSTile + lrow) * kT, 0);
 #pragma unroll
@@ -619,7 +626,9 @@ __device__ __forceinline__ void s_epilogue_role(const SParams& p, SSmem<kT>& s, 
     if (!ok && lane == 0) sfail(p, abort_flag);
 }
 
-template <int kT, bool kPartials>
+// kTest: the failure-detection test instantiation (runtime poll bound, a withheld weight copy);
+// otherwise both are compile-time constants.
+template <int kT, bool kPartials, bool kTest = false>
 __global__ void __launch_bounds__(kSThreads, 1)
     w4ax_gemm_small_kernel(const SParams p, const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tma,
                            const __grid_constant__ CUtensorMap tmsw, const __grid_constant__ CUtensorMap tmsx) {
@@ -665,31 +674,33 @@ __global__ void __launch_bounds__(kSThreads, 1)
     dev::tc_fence_after();
     const uint32_t tmem = s.tmem_base;
     volatile int* abort_flag = &s.abort_flag;
+    const uint32_t polls = kTest ? p.polls : dev::kMaxPolls;
+    const int withhold = kTest ? p.withhold : -1;
 
     // (no per-role register split: at 128 registers a thread every role fits)
     if (warp == 0) {
         if (lane == 0) dev::tma_prefetch_map(&tmw);
-        s_weight_producer<kT>(p, &tmw, s, lane, abort_flag);
+        s_weight_producer<kT>(p, &tmw, s, lane, abort_flag, polls, withhold);
     } else {
         if (warp < 8) {
             if (warp == 1 || warp == 7) {
                 static_assert(kSIssuers == 2, "issuer warps 1, 7");
-                s_mma_role<kT>(p, s, lane, tmem, warp == 1 ? 0 : 1, abort_flag);
+                s_mma_role<kT>(p, s, lane, tmem, warp == 1 ? 0 : 1, abort_flag, polls);
             } else if (warp == 6) {
                 if (lane == 0) {
                     dev::tma_prefetch_map(&tma);
                     dev::tma_prefetch_map(&tmsw);
                     dev::tma_prefetch_map(&tmsx);
                 }
-                s_operand_producer<kT>(p, &tma, &tmsw, &tmsx, s, lane, abort_flag);
+                s_operand_producer<kT>(p, &tma, &tmsw, &tmsx, s, lane, abort_flag, polls);
             } else if (warp >= 2 && warp < 2 + kSConvWarps) {
-                s_converter_role<kT>(p, s, 0, (warp - 2) * 32 + lane, lane, abort_flag);
+                s_converter_role<kT>(p, s, 0, (warp - 2) * 32 + lane, lane, abort_flag, polls);
             }
         } else {
             if (warp < 8 + kSEpiWarps) {
-                s_epilogue_role<kT, kPartials>(p, s, warp & 3, lane, tmem, abort_flag);
+                s_epilogue_role<kT, kPartials>(p, s, warp & 3, lane, tmem, abort_flag, polls);
             } else {
-                s_converter_role<kT>(p, s, 1, (warp - 12) * 32 + lane, lane, abort_flag);
+                s_converter_role<kT>(p, s, 1, (warp - 12) * 32 + lane, lane, abort_flag, polls);
             }
         }
     }
@@ -741,8 +752,10 @@ struct SMaps {
 
 template <int kT>
 cudaError_t launch_small_t(const SParams& p, const SMaps& m, int ctas, cudaStream_t stream, bool pdl) {
+    const bool test = p.withhold >= 0;
     const void* fn = p.P != nullptr ? reinterpret_cast<const void*>(w4ax_gemm_small_kernel<kT, true>)
-                                    : reinterpret_cast<const void*>(w4ax_gemm_small_kernel<kT, false>);
+                     : test        ? reinterpret_cast<const void*>(w4ax_gemm_small_kernel<kT, false, true>)
+                                   : reinterpret_cast<const void*>(w4ax_gemm_small_kernel<kT, false>);
     const cudaError_t e = ensure_smem_limit(fn, static_cast<int>(small_smem_bytes<kT>()));
     if (e != cudaSuccess) return e;
     if (p.P != nullptr) {
@@ -764,6 +777,7 @@ cudaError_t launch_small_t(const SParams& p, const SMaps& m, int ctas, cudaStrea
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 2 : 1;
+    if (test) return cudaLaunchKernelEx(&cfg, w4ax_gemm_small_kernel<kT, false, true>, p, m.w, m.a, m.sw, m.sx);
     return cudaLaunchKernelEx(&cfg, w4ax_gemm_small_kernel<kT, false>, p, m.w, m.a, m.sw, m.sx);
 }
 
@@ -842,6 +856,8 @@ cudaError_t launch_gemm_small(const fmpq_layout& L, const GemmArgs& a, cudaStrea
     static_assert(sizeof(L.mask_bits) * 8 >= kMaxBlocks, "block bitmap too small");
     for (int w = 0; w < kMaxBlocks / 32; ++w) p.mask_bits[w] = L.mask_bits[w];
     p.status = L.d_status;
+    p.polls = a.poll_limit != 0 ? a.poll_limit : dev::kMaxPolls;
+    p.withhold = a.withhold;
     const int T = tokens_tile(a.M);
     p.ntiles = static_cast<int>((a.N + kSTile - 1) / kSTile);
     p.splits = small_splits(L, p.ntiles, T);

@@ -228,13 +228,16 @@ FMPQ_API fmpq_status w4ax_gemm_partials(const fmpq_layout* layout, const void* A
                                int64_t mcount, int64_t n0, int64_t ncount, int32_t* P,
                                void* stream);
 
-/* Debug/test of failure detection: w4ax_gemm (M > 128, the 2-SM kernel) in which the first
- * CTA's weight producer never issues its withhold_copy-th packed weight copy (counted from 0,
- * < K/128), and every device-side wait gives up after poll_limit polls (>= 1024). The wait on
- * the missing copy runs out, the kernel's roles leave their loops, wait for the copies they did
- * issue and release TMEM; the call records FMPQ_ERR_TIMEOUT in the layout's device status word
- * and Y is unspecified. Nothing faults or hangs; the next normal call is unaffected (a split-K
- * workspace's counters still return to zero). Other arguments as w4ax_gemm. */
+/* Debug/test of failure detection: w4ax_gemm (the 2-SM kernel for M > 64, the few-token kernel
+ * for M <= 64) in which the first CTA's weight producer never issues its withhold_copy-th packed
+ * weight copy (counted from 0, < K/128; a few-token copy holds two blocks, and a copy the CTA
+ * never reaches withholds nothing), and every device-side wait gives up after poll_limit polls
+ * (>= 1024). The wait on the missing copy runs out, the kernel's roles leave their loops, wait
+ * for the copies they did issue and release TMEM; the call records FMPQ_ERR_TIMEOUT in the
+ * layout's device status word and Y is unspecified. Nothing faults or hangs: in the few-token
+ * kernel's clusters the aborted CTA stops before any exchange with the other splits, whose
+ * waits for it run out in turn. The next normal call is unaffected (a split-K workspace's
+ * counters still return to zero). Other arguments as w4ax_gemm. */
 FMPQ_API fmpq_status w4ax_gemm_fault_test(const fmpq_layout* layout, const void* A_packed, const void* a_scales,
                                           const void* W_packed, const void* w_scales, int64_t M, int64_t N, void* Y,
                                           int64_t ldy, void* workspace, size_t workspace_bytes,
